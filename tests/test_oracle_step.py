@@ -1,0 +1,152 @@
+"""Whole-step checks of the oracle: an independent scalar-loop restatement on
+tiny shapes, plus cache, causality and batch-independence invariants."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from oracle import numerics
+
+
+def _bf(bits):
+    return float(numerics.bf16_bits_to_f64(np.array([bits], dtype=np.uint16))[0])
+
+
+def _scalar_step(wl, model, kv, tokens, positions):
+    """A second statement of the decode step with Python scalars and loops only
+    (no numpy linear algebra, no shared helper besides bf16 bit reading)."""
+    L, H, nq, nkv, d, I, V = (wl.n_layers, wl.hidden, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
+                              wl.intermediate, wl.vocab)
+    eps, theta = wl.rms_eps, wl.rope_theta
+    group = nq // nkv
+
+    def weight(lin, r, c):
+        if isinstance(lin, dict):
+            word = int(lin["w"][r, c // 8]) & 0xFFFFFFFF
+            q = (word >> (4 * (c % 8))) & 15
+            return _bf(lin["scales"][r, c // 64]) * q + _bf(lin["biases"][r, c // 64])
+        return _bf(lin[r, c])
+
+    def matvec(lin, x, n_out):
+        return [sum(weight(lin, r, c) * x[c] for c in range(len(x))) for r in range(n_out)]
+
+    def norm(x, w):
+        ms = sum(v * v for v in x) / len(x)
+        inv = 1.0 / math.sqrt(ms + eps)
+        return [x[i] * inv * _bf(w[i]) for i in range(len(x))]
+
+    def rope(x, pos):
+        half = d // 2
+        y = [0.0] * d
+        for i in range(half):
+            a = pos * theta ** (-2.0 * i / d)
+            y[i] = x[i] * math.cos(a) - x[i + half] * math.sin(a)
+            y[i + half] = x[i + half] * math.cos(a) + x[i] * math.sin(a)
+        return y
+
+    out_logits = []
+    for b in range(len(tokens)):
+        P = int(positions[b])
+        h = [_bf(v) for v in model["embed"][int(tokens[b])]]
+        for l in range(L):
+            lay = model["layers"][l]
+            xn = norm(h, lay["in_norm"])
+            q = matvec(lay["q"], xn, nq * d)
+            k = matvec(lay["k"], xn, nkv * d)
+            v = matvec(lay["v"], xn, nkv * d)
+            qh = [rope(norm(q[j * d:(j + 1) * d], lay["q_norm"]), P) for j in range(nq)]
+            kh = [rope(norm(k[j * d:(j + 1) * d], lay["k_norm"]), P) for j in range(nkv)]
+            vh = [v[j * d:(j + 1) * d] for j in range(nkv)]
+            # keys/values the new token sees: cached slots 0..P-1, then its own (bf16-rounded)
+            att = []
+            for j in range(nq):
+                hk = j // group
+                keys = [[_bf(x) for x in kv[l, 0, b, hk, t]] for t in range(P)]
+                vals = [[_bf(x) for x in kv[l, 1, b, hk, t]] for t in range(P)]
+                keys.append([float(numerics.round_to_bf16(np.array(x))) for x in kh[hk]])
+                vals.append([float(numerics.round_to_bf16(np.array(x))) for x in vh[hk]])
+                sc = [sum(qh[j][i] * key[i] for i in range(d)) / math.sqrt(d) for key in keys]
+                mx = max(sc)
+                ex = [math.exp(s - mx) for s in sc]
+                tot = sum(ex)
+                att.extend(sum(ex[t] / tot * vals[t][i] for t in range(P + 1)) for i in range(d))
+            o = matvec(lay["o"], att, H)
+            h = [h[i] + o[i] for i in range(H)]
+            xn = norm(h, lay["post_norm"])
+            gt = matvec(lay["gate"], xn, I)
+            up = matvec(lay["up"], xn, I)
+            g = [gt[i] / (1.0 + math.exp(-gt[i])) * up[i] for i in range(I)]
+            dn = matvec(lay["down"], g, H)
+            h = [h[i] + dn[i] for i in range(H)]
+        out_logits.append(matvec(model["lm_head"], norm(h, model["final_norm"]), V))
+    return np.array(out_logits)
+
+
+def _np_model(model):
+    def conv(x):
+        if isinstance(x, dict):
+            return {k: conv(v) for k, v in x.items()}
+        if isinstance(x, list):
+            return [conv(v) for v in x]
+        return oracle.decoder._to_numpy(x)
+    return {k: conv(v) for k, v in model.items()}
+
+
+@pytest.mark.parametrize("fmt", [synthetic.BF16, synthetic.AFFINE4_G64])
+def test_step_matches_scalar_restatement(fmt):
+    wl = synthetic.custom(n_layers=2, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16,
+                          intermediate=128, vocab=40, weight_format=fmt, batch=2, prefill=5, steps=1,
+                          seed=7)
+    model = synthetic.generate(wl)
+    model["positions"][1] = 2  # ragged lengths
+    npm = _np_model(model)
+    kv = npm["kv"].copy()
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    logits, am = oracle.decode_step(m, kv, npm["tokens"], npm["positions"])
+    ref = _scalar_step(wl, npm, npm["kv"], npm["tokens"], npm["positions"])
+    assert np.allclose(logits, ref, rtol=1e-11, atol=1e-12)
+    assert am.tolist() == [int(np.argmax(r)) for r in ref]
+
+
+def test_step_writes_only_slot_p_and_ignores_later_slots():
+    wl = synthetic.custom(n_layers=2, hidden=64, n_q_heads=2, n_kv_heads=1, head_dim=32, intermediate=96,
+                          vocab=50, batch=2, prefill=6, steps=3, seed=3)
+    model = synthetic.generate(wl)
+    npm = _np_model(model)
+    P = npm["positions"]
+    kv0 = npm["kv"].copy()
+    kv = kv0.copy()
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    logits, _ = oracle.decode_step(m, kv, npm["tokens"], P)
+    changed = np.argwhere(kv != kv0)
+    assert len(changed) > 0
+    for l, p, b, h, t, i in changed:
+        assert t == P[b]
+    # junk in the slots after P must not change anything
+    kv_junk = kv0.copy()
+    for b in range(2):
+        kv_junk[:, :, b, :, P[b] + 1:, :] = numerics.f64_to_bf16_bits(np.full_like(
+            kv_junk[:, :, b, :, P[b] + 1:, :], 1000.0, dtype=np.float64))
+    logits2, _ = oracle.decode_step(m, kv_junk, npm["tokens"], P)
+    assert np.array_equal(logits, logits2)
+
+
+def test_step_sequences_are_independent():
+    wl = synthetic.custom(n_layers=1, hidden=64, n_q_heads=2, n_kv_heads=1, head_dim=32, intermediate=96,
+                          vocab=50, batch=3, prefill=4, steps=1, seed=11)
+    model = synthetic.generate(wl)
+    npm = _np_model(model)
+    npm["positions"][:] = [4, 1, 3]
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    kv = npm["kv"].copy()
+    logits, am = oracle.decode_step(m, kv, npm["tokens"], npm["positions"])
+    for b in range(3):
+        wl1 = wl.replace(batch=1)
+        m1 = oracle.OracleModel(wl1, m.raw)
+        kv1 = npm["kv"][:, :, b:b + 1].copy()
+        l1, a1 = oracle.decode_step(m1, kv1, npm["tokens"][b:b + 1], npm["positions"][b:b + 1])
+        assert np.allclose(l1[0], logits[b], rtol=1e-13, atol=1e-13)
+        assert np.array_equal(kv1[:, :, 0], kv[:, :, b])
