@@ -1,0 +1,339 @@
+"""Decode-step benchmark: tokens/s and achieved HBM GB/s of the GB300 step.
+
+One "step" = one dec_step call (the whole decode path: embedding, every layer,
+lm_head and argmax) for one batch, followed by the greedy feedback kernel
+(token <- argmax, position += 1).  Inputs are seeded synthetic tensors already
+resident in HBM; the per-step weights (> 1 GB for every model-sized workload)
+are larger than L2, so no flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                       [--impl ours|reference] [--no-cpu-baseline]
+With --gpus N > 1 (launched by torchrun) every rank runs an independent replica
+of the workload on its own GPU (the step has no cross-sequence exchange); the
+value is the sum of all ranks' tokens over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+DEFAULT_CONFIG = "qwen3-0.6b"
+METRIC = "decode tokens/s and achieved HBM GB/s (fraction of GB300 peak) per step"
+
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel class, keyed by workload and class, valid only for the kernel
+# sources whose digest is recorded with it (see profiles/).
+NCU_TRAFFIC: dict = {}
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "token_decode_step_gb300" / "csrc").glob("*.cu*")):
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[dict, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        return json.loads(p.read_text()), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args, rank: int, world: int) -> dict | None:
+    import torch
+    import synthetic
+    from token_decode_step_gb300 import build as build_mod
+    if rank == 0 or not (ROOT / "token_decode_step_gb300" / "libdec.so").exists():
+        build_mod.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from token_decode_step_gb300 import dec as D
+    from token_decode_step_gb300.torch_glue import Decoder
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl0 = synthetic.WORKLOADS[args.config]
+    total = args.warmup + args.steps + args.profile_steps + args.e2e_steps + 2
+    wl = wl0.replace(steps=total)  # cache capacity for every step this run takes
+    model = synthetic.generate(wl, device=dev)
+    dec = Decoder(wl, model)
+    B, V = wl.batch, wl.vocab
+    tokens = model["tokens"].clone()
+    positions = model["positions"].clone()
+    kv = model["kv"]
+    logits = torch.empty((B, V), dtype=torch.float32, device=dev)
+    argmax = torch.empty((B,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    p0 = float(model["positions"].float().mean())
+
+    def one_step():
+        dec.step(tokens, positions, kv, logits, argmax, stream)
+        dec.advance(argmax, tokens, positions, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize(dev)
+    pos_start = float(positions.float().mean())
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    mean_p = pos_start + (args.steps - 1) / 2.0  # mean cached length over the timed steps
+
+    # per-kernel-class durations: the same step with per-launch CUDA events (no graph)
+    cls_ms = [0.0] * D.DEC_K_COUNT
+    cls_n = [0] * D.DEC_K_COUNT
+    prof_p = float(positions.float().mean())
+    for _ in range(args.profile_steps):
+        dec.profile_step(tokens, positions, kv, logits, argmax, cls_ms, cls_n, stream)
+        dec.advance(argmax, tokens, positions, stream)
+    torch.cuda.synchronize(dev)
+    prof_mean_p = prof_p + (args.profile_steps - 1) / 2.0
+
+    # end to end through the C ABI with host buffers: H2D tokens+positions, step, D2H argmax
+    h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_pos = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_am = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    h_tok.copy_(tokens.cpu())
+    h_pos.copy_(positions.cpu())
+    d_tok = torch.empty_like(tokens)
+    d_pos = torch.empty_like(positions)
+    def e2e_step():
+        d_tok.copy_(h_tok, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        dec.step(d_tok, d_pos, kv, None, argmax, stream)
+        h_am.copy_(argmax, non_blocking=True)
+        stream.synchronize()
+        h_tok.copy_(h_am)
+        h_pos.add_(1)
+
+    e2e_step()  # captures the graph for this pointer set (untimed)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+
+    per_step = [1, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, 1]  # launches per class
+    bytes_step = sum(n * dec.kernel_bytes(c, mean_p) for c, n in enumerate(per_step))
+    cls_bytes = [dec.kernel_bytes(c, prof_mean_p) for c in range(D.DEC_K_COUNT)]
+    launches = dec.launches_per_step
+    dec.close()
+    return {"ms": ms, "mean_p": mean_p, "bytes_step": bytes_step, "cls_ms": cls_ms, "cls_n": cls_n,
+            "cls_bytes": cls_bytes, "e2e_s": e2e_s, "launches": launches, "wl": wl0, "B": B,
+            "clocks": clk.summary()}
+
+
+def cpu_oracle_sample(config: str, budget_s: float) -> dict:
+    """Time the CPU oracle (as it stands) on whole decode steps of the workload,
+    stopping after the first step that ends past budget_s."""
+    import numpy as np
+    import oracle
+    import synthetic
+    wl = synthetic.WORKLOADS[config].replace(steps=8)
+    model = synthetic.generate(wl, device="cpu")
+    m = oracle.OracleModel.from_synthetic(wl, model, cache_weights=True)
+    kv = model["kv"].view(__import__("torch").int16).numpy().view(np.uint16).copy()
+    tokens = model["tokens"].numpy().copy()
+    pos = model["positions"].numpy().copy()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        _, am = oracle.decode_step(m, kv, tokens, pos)
+        tokens = am.astype(np.int32)
+        pos = pos + 1
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= wl.steps:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": wl.batch * done / el, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} greedy step(s) of {config} (batch {wl.batch}) from the initial cache, "
+                      f"first-use float64 weight conversion included, {el:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--profile-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle, timed as it stands on the host cores (rank 0 only)
+        if rank != 0:
+            return
+        s = cpu_oracle_sample(args.config, args.cpu_budget)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": s["value"], "unit": "tok/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": args.config}, "cpu_baseline": s,
+            "e2e": {"value": s["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    r = run_ours(args, rank, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    from token_decode_step_gb300 import dec as D
+    wl, B = r["wl"], r["B"]
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    steps = args.steps
+    tok_s = world * B * steps / (r["ms"] / 1e3)
+    step_ms = r["ms"] / steps
+    step_gbs = r["bytes_step"] / (step_ms / 1e3) / 1e9
+
+    # dominant kernel class by measured time
+    cls_ms, cls_n = r["cls_ms"], r["cls_n"]
+    dom = max(range(D.DEC_K_COUNT), key=lambda c: cls_ms[c])
+    dom_name = D.KERNEL_CLASS_NAMES[dom]
+    dom_avg_ms = cls_ms[dom] / max(1, cls_n[dom])
+    line = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.weight_format == "bf16" else "int4-affine-g64",
+        "data": "synthetic (seeded, random-init weights; see synthetic/workloads.py)",
+        "config": {
+            "workload": args.config, "batch": B, "layers": wl.n_layers, "hidden": wl.hidden,
+            "cached_positions": wl.prefill if not isinstance(wl.prefill, tuple) else list(wl.prefill),
+            "weight_format": wl.weight_format, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (per-step weights exceed 129 MB); no flush",
+            "timing": "CUDA events on the launching stream, CUDA-graph replay per step",
+        },
+        "step_hbm_gbs": round(step_gbs, 1),
+        "step_hbm_frac": round(step_gbs / hbm_peak, 4),
+        "step_bytes": int(r["bytes_step"]),
+        "peak_hbm_gbs": hbm_peak,
+        "peak_kind": peak_kind,
+        "gpu_launches": (r["launches"] + 1) * steps,
+        "clocks": r["clocks"],
+        "kernel_ms_per_launch": {D.KERNEL_CLASS_NAMES[c]: round(cls_ms[c] / max(1, cls_n[c]), 5)
+                                 for c in range(D.DEC_K_COUNT)},
+        "kernel_share": {D.KERNEL_CLASS_NAMES[c]: round(cls_ms[c] / max(1e-12, sum(cls_ms)), 4)
+                         for c in range(D.DEC_K_COUNT)},
+    }
+    e2e_tok_s = B * args.e2e_steps / r["e2e_s"]
+    line["e2e"] = {"value": round(e2e_tok_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 8 * B,
+                   "d2h_bytes_per_step": 4 * B}
+    db = r["cls_bytes"][dom]
+    line["roofline"] = {"bound": "hbm", "kernel": dom_name, "achieved": None, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": None, "traffic": None}
+    if db:
+        ach = db / (dom_avg_ms / 1e3) / 1e9
+        line["roofline"].update({"achieved": round(ach, 1), "frac": round(ach / hbm_peak, 4),
+                                 "bytes_per_launch": int(db), "avg_launch_ms": round(dom_avg_ms, 5)})
+        tr = NCU_TRAFFIC.get(args.config, {}).get(dom_name)
+        if tr and tr.get("csrc") == csrc_digest():
+            line["roofline"]["traffic"] = tr["bytes"]
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(args.config, args.cpu_budget)
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

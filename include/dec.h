@@ -1,0 +1,200 @@
+/*
+ * dec.h - C ABI of the GB300 one-token decode step for a Qwen3-style dense decoder.
+ *
+ * One call of dec_step() runs one greedy decode step for B independent
+ * sequences, entirely on the GPU (sm_103a):
+ *
+ *   h = embed[token]                                   (gather)
+ *   for each layer:
+ *     xn = RMSNorm(h) * in_norm                        (fused into the QKV GEMV)
+ *     q, k, v = Wq xn, Wk xn, Wv xn                    (one fused GEMV)
+ *     q, k = per-head RMSNorm (q_norm / k_norm), then rotate-half RoPE at P
+ *     cache[P] = bf16(k), bf16(v); o = softmax(q K^T / sqrt(d)) V over 0..P
+ *                                                      (one fused attention kernel,
+ *                                                       split over the positions,
+ *                                                       log-sum-exp merge)
+ *     h += Wo o                                        (GEMV + residual)
+ *     h += Wdown(silu(Wgate xn) * (Wup xn)), xn = RMSNorm(h) * post_norm
+ *   logits = Wlm RMSNorm(h) * final_norm; argmax      (vocab-tiled GEMV, two-stage argmax)
+ *
+ * Sources (page title and section):
+ *   - ANEForge, "LLMs on the ANE", "What's inside": pre-norm block order,
+ *     rotate-half RoPE, GQA (KV heads shared by groups of query heads);
+ *     "Correctness": separate head_dim, per-head q/k RMSNorm before RoPE;
+ *     "lm_head on the ANE": lm_head tiled along the vocab, greedy argmax.
+ *   - Butter, architecture.md, figure "SINGLE-TOKEN DECODE": the kernel
+ *     sequence, KV append into a preallocated buffer at offset = cache length,
+ *     one command buffer per token (here: one CUDA graph per step); GPU
+ *     sampling (greedy argmax on the device, 4-byte result).
+ *   - oxinfer crate page, "MLX checkpoints": affine 4-bit weights, eight per
+ *     uint32, one bf16 scale and bias per group of 64, w = scale*q + bias.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device memory of the current device.  Host
+ *     pointers (config, weight tables, outputs of size queries) are plain
+ *     host memory, read only during the call.
+ *   - Functions returning dec_status report host-detectable errors
+ *     immediately; the message is available from dec_last_error() (thread
+ *     local, valid until the next failing call on the same thread).
+ *   - Work is enqueued on the caller's stream and is asynchronous.  CUDA
+ *     faults surface at the caller's next synchronisation, or as
+ *     DEC_ERR_CUDA from a later call.
+ */
+#ifndef TOKEN_DECODE_STEP_DEC_H
+#define TOKEN_DECODE_STEP_DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DEC_API __attribute__((visibility("default")))
+#else
+#define DEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (an opaque CUDA stream handle); NULL = legacy default stream. */
+typedef struct CUstream_st *dec_stream_t;
+
+typedef enum {
+    DEC_OK = 0,
+    DEC_ERR_INVALID_ARG = 1,   /* NULL/inconsistent argument */
+    DEC_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle (see dec_config) */
+    DEC_ERR_OOM = 3,           /* cudaMalloc failed */
+    DEC_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    DEC_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (status word bit) */
+    DEC_ERR_DEVICE_INPUT = 6   /* a token id or position was out of range (status word bit) */
+} dec_status;
+
+typedef enum {
+    DEC_W_BF16 = 0,            /* bf16 [out][in] row-major */
+    DEC_W_AFFINE4_G64 = 1      /* w = uint32 [out][in/8] (nibble k of word j is input 8j+k,
+                                  bits 4k..4k+3), scales, biases = bf16 [out][in/64] */
+} dec_wfmt;
+
+/* Model and run shape.  Supported (else DEC_ERR_UNSUPPORTED): head_dim in {64, 128};
+   n_q_heads / n_kv_heads in {1, 2, 4}; hidden and intermediate multiples of 64;
+   vocab >= 1; batch 1; max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG): every
+   size positive, rms_eps > 0, rope_theta > 1, n_q_heads a multiple of n_kv_heads. */
+typedef struct {
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
+    float rms_eps, rope_theta;
+    int linear_fmt;            /* dec_wfmt, applies to every linear including lm_head */
+    int batch, max_ctx;        /* sequences per step; cache slots per sequence */
+} dec_config;
+
+/* One linear layer, row-major [out][in] in device memory.  bf16: w only (scales,
+   biases ignored).  affine 4-bit: all three, layouts as in dec_wfmt. */
+typedef struct {
+    const void *w;
+    const void *scales;
+    const void *biases;
+} dec_linear;
+
+typedef struct {
+    const void *in_norm;       /* bf16 [hidden] */
+    const void *post_norm;     /* bf16 [hidden] */
+    const void *q_norm;        /* bf16 [head_dim], shared by the layer's query heads */
+    const void *k_norm;        /* bf16 [head_dim], shared by the layer's KV heads */
+    dec_linear q, k, v;        /* [n_q*d][hidden], [n_kv*d][hidden], [n_kv*d][hidden] */
+    dec_linear o;              /* [hidden][n_q*d] */
+    dec_linear gate, up;       /* [intermediate][hidden] */
+    dec_linear down;           /* [hidden][intermediate] */
+} dec_layer_weights;
+
+typedef struct {
+    const void *embed;         /* bf16 [vocab][hidden] (bf16 in every format) */
+    const void *final_norm;    /* bf16 [hidden] */
+    dec_linear lm_head;        /* [vocab][hidden], untied from embed */
+    const dec_layer_weights *layers;   /* host array of n_layers entries */
+} dec_weights;
+
+typedef struct dec_handle dec_handle;
+
+/* Validate cfg, allocate the handle's device memory, repack every weight into
+   the handle's own layout (device-to-device, on an internal stream that is
+   synchronised before returning), and upload the RoPE frequency table.  The
+   caller may free its weight buffers once this returns.  Returns NULL on
+   failure (see dec_last_error()).  Uses the current CUDA device. */
+DEC_API dec_handle *dec_create(const dec_config *cfg, const dec_weights *weights);
+
+/* One decode step (Butter "SINGLE-TOKEN DECODE" sequence), enqueued on `stream`.
+     token_ids  device int32 [batch]: input token per sequence.
+     positions  device int32 [batch]: P_b = cached positions of sequence b; the
+                step writes K/V slot P_b, attends over slots 0..P_b and applies
+                RoPE at angle P_b.  The caller advances positions.
+     kv_cache   device, dec_kv_cache_bytes(cfg) bytes, bf16
+                [n_layers][2][batch][n_kv_heads][max_ctx][head_dim] (plane 0 = K,
+                plane 1 = V, post-norm post-RoPE keys), caller-owned.
+     logits_out device float [batch][vocab], or NULL to skip writing logits.
+     argmax_out device int32 [batch]: greedy token (lowest index on equal
+                logits).  May alias token_ids (read happens first).
+   Out-of-range token ids or positions are clamped on the device and flagged in
+   the status word (dec_get_device_status); nothing outside the buffers is
+   touched.  By default the step runs as one CUDA graph, re-captured whenever
+   the set of pointers changes.  One handle must not be used by two streams at once. */
+DEC_API dec_status dec_step(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
+                    void *kv_cache, float *logits_out, int32_t *argmax_out,
+                    dec_stream_t stream);
+
+/* Free every device resource of the handle (caller buffers are untouched).
+   The caller must make sure no step of this handle is still running. */
+DEC_API void dec_destroy(dec_handle *h);
+
+/* Bytes of the KV cache for cfg (0 if cfg is NULL or invalid). */
+DEC_API size_t dec_kv_cache_bytes(const dec_config *cfg);
+
+/* Message of the last failing call on this thread ("" if none). */
+DEC_API const char *dec_last_error(void);
+
+/* Read and clear the device status word (call after synchronising the stream of
+   the steps in question).  *out receives the raw bits (1: token id out of range,
+   2: position out of range, 4: bounded wait timed out).  Returns DEC_OK when the
+   word was 0, DEC_ERR_DEVICE_INPUT / DEC_ERR_TIMEOUT otherwise. */
+DEC_API dec_status dec_get_device_status(dec_handle *h, int *out);
+
+/* Test hook: write the dequantised weights of one linear as float32 [out][in]
+   (row-major, canonical row order) to device memory `out`, computed from the
+   handle's packed copy with the same nibble unpacking the GEMV kernels use and a
+   single rounding (fmaf(scale, q, bias)); for bf16 the exact value.
+   which: 0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down, 7 lm_head (layer ignored). */
+DEC_API dec_status dec_debug_dequant(dec_handle *h, int layer, int which, float *out, dec_stream_t stream);
+
+/* Greedy feedback helper: token_ids[b] = argmax[b]; positions[b] += 1, for b < batch,
+   as one small kernel on `stream` (device pointers). */
+DEC_API dec_status dec_advance(const int32_t *argmax, int32_t *token_ids, int32_t *positions, int batch,
+                       dec_stream_t stream);
+
+/* 1 (default): dec_step replays a captured CUDA graph; 0: launch kernels one by one. */
+DEC_API dec_status dec_set_graph_mode(dec_handle *h, int enabled);
+
+/* Kernel classes reported by dec_profile_step. */
+enum {
+    DEC_K_EMBED = 0, DEC_K_QKV = 1, DEC_K_ATTN = 2, DEC_K_OPROJ = 3, DEC_K_GATEUP = 4,
+    DEC_K_DOWN = 5, DEC_K_LMHEAD = 6, DEC_K_COUNT = 7
+};
+
+/* Run one step with individual launches, each bracketed by CUDA events recorded
+   on `stream`, then synchronise `stream` and add each launch's elapsed time (ms)
+   to ms[class] and 1 to launches[class] (host arrays of n_classes >= DEC_K_COUNT
+   entries).  Same arguments and results as dec_step. */
+DEC_API dec_status dec_profile_step(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
+                            void *kv_cache, float *logits_out, int32_t *argmax_out,
+                            dec_stream_t stream, double *ms, int *launches, int n_classes);
+
+/* Algorithmic bytes one launch of a kernel class moves at cached length P (same P
+   for all sequences): weights (+ norms) read once, KV rows 0..P read, activations
+   excluded.  Host-side arithmetic on the handle's config. */
+DEC_API double dec_kernel_bytes(const dec_handle *h, int kernel_class, double mean_cached_len);
+
+/* Number of kernels one dec_step launches. */
+DEC_API int dec_launches_per_step(const dec_handle *h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOKEN_DECODE_STEP_DEC_H */

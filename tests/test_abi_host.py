@@ -1,0 +1,93 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every symbol that
+include/dec.h declares, and rejects bad configurations on the host before any
+CUDA call (so these run without a GPU)."""
+
+import ctypes
+import pathlib
+import re
+import subprocess
+
+import pytest
+
+ROOT = pathlib.Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "dec.h"
+
+
+@pytest.fixture(scope="module")
+def dec():
+    from token_decode_step_gb300 import build
+    build.build()
+    from token_decode_step_gb300 import dec as d
+    return d
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"DEC_API\s+[\w\s\*]+?\b(dec_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_core_calls():
+    names = declared_functions()
+    for core in ("dec_create", "dec_step", "dec_destroy", "dec_kv_cache_bytes", "dec_last_error"):
+        assert core in names
+
+
+def test_library_exports_every_declared_symbol(dec):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(dec._LIB_PATH)], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (dec_\w+)", out))
+    missing = set(declared_functions()) - exported
+    assert not missing, f"declared but not exported: {missing}"
+    for name in declared_functions():
+        assert hasattr(dec.lib, name)
+
+
+def _cfg(dec, **kw):
+    base = dict(n_layers=2, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, intermediate=768, vocab=4096,
+                rms_eps=1e-6, rope_theta=1e6, linear_fmt=0, batch=1, max_ctx=144)
+    base.update(kw)
+    return dec.DecConfig(**base)
+
+
+def test_kv_cache_bytes(dec):
+    assert dec.dec_kv_cache_bytes(_cfg(dec)) == 2 * 2 * 1 * 2 * 144 * 64 * 2
+    assert dec.lib.dec_kv_cache_bytes(None) == 0
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(head_dim=96), 2, "head_dim"),
+    (dict(n_q_heads=6, n_kv_heads=2), 2, "1, 2 or 4"),
+    (dict(n_q_heads=5, n_kv_heads=2), 1, "multiple"),
+    (dict(hidden=200), 2, "multiples of 64"),
+    (dict(rms_eps=0.0), 1, "rms_eps"),
+    (dict(linear_fmt=7), 1, "linear_fmt"),
+    (dict(vocab=0), 1, "positive"),
+])
+def test_create_rejects_bad_config(dec, kw, status, msg):
+    with pytest.raises(dec.DecError) as ei:
+        dec.dec_create(_cfg(dec, **kw), dec.DecWeights())
+    assert msg in str(ei.value)
+
+
+def test_create_rejects_null_weights(dec):
+    with pytest.raises(dec.DecError) as ei:
+        dec.dec_create(_cfg(dec), dec.DecWeights())
+    assert "non-NULL" in str(ei.value)
+
+
+def test_create_rejects_misaligned_weight_pointer(dec):
+    layers = (dec.DecLayerWeights * 2)()
+    for i in range(2):
+        lw = dec.DecLayerWeights(16, 16, 16, 16, *(dec.DecLinear(32, None, None) for _ in range(7)))
+        layers[i] = lw
+    layers[1].o = dec.DecLinear(40, None, None)  # not 16-byte aligned
+    w = dec.DecWeights(16, 16, dec.DecLinear(16, None, None), ctypes.cast(layers, ctypes.POINTER(dec.DecLayerWeights)))
+    with pytest.raises(dec.DecError) as ei:
+        dec.dec_create(_cfg(dec), w)
+    assert "layer 1 o" in str(ei.value)
+
+
+def test_step_rejects_null_handle(dec):
+    st = dec.lib.dec_step(None, 16, 16, 16, None, 16, None)
+    assert st == dec.DEC_ERR_INVALID_ARG
+    assert "handle" in dec.dec_last_error()

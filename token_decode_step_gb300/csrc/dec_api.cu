@@ -1,0 +1,729 @@
+// C ABI of the decode step: handle lifetime, argument checks, weight packing,
+// the per-step launch sequence, CUDA-graph capture/replay and profiling.
+//
+// The launch sequence follows Butter architecture.md, figure "SINGLE-TOKEN
+// DECODE" (gather -> per layer: rms_norm+qkv, rope+append+sdpa, o+add,
+// rms_norm+gate/up+silu_mul, down+add -> rms_norm+lm_head -> argmax), with the
+// norms and elementwise steps fused into the neighbouring kernels.  The page's
+// "one command buffer per token" becomes one CUDA graph per step, and the
+// argument-buffer idea (weights bound once, per-token state small) becomes a
+// graph whose kernel parameters are fixed per pointer set.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "dec_internal.cuh"
+
+using namespace dec;
+
+// ---------------------------------------------------------------- errors
+
+static thread_local char g_err[512] = "";
+
+static void set_err(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+#define DEC_CUDA(call)                                                                     \
+  do {                                                                                     \
+    cudaError_t e_ = (call);                                                               \
+    if (e_ != cudaSuccess) {                                                               \
+      set_err("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return DEC_ERR_CUDA;                                                                 \
+    }                                                                                      \
+  } while (0)
+
+// ---------------------------------------------------------------- handle
+
+namespace {
+
+struct PackedLinear {
+  void* w = nullptr;       // bf16 [N][K] or uint32 [N][K/8]
+  uint32_t* sb = nullptr;  // q4 only: [N][K/64]
+  int N = 0, K = 0, S = 1;
+};
+
+struct PackedLayer {
+  __nv_bfloat16 *in_norm, *post_norm, *q_norm, *k_norm;
+  PackedLinear qkv, o, gateup, down;
+};
+
+struct StepPtrs {
+  const int32_t* tokens;
+  const int32_t* positions;
+  void* kv;
+  float* logits;
+  int32_t* argmax;
+  bool operator==(const StepPtrs& o) const {
+    return tokens == o.tokens && positions == o.positions && kv == o.kv && logits == o.logits &&
+           argmax == o.argmax;
+  }
+};
+
+struct Launch {
+  int cls;
+};
+
+}  // namespace
+
+struct dec_handle {
+  dec_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  int wfmt = 0;
+  // packed weights (one allocation)
+  unsigned char* wmem = nullptr;
+  size_t wbytes = 0;
+  __nv_bfloat16* embed = nullptr;
+  __nv_bfloat16* final_norm = nullptr;
+  PackedLinear lm_head;
+  std::vector<PackedLayer> layers;
+  // workspace (one allocation)
+  unsigned char* ws = nullptr;
+  float* h = nullptr;
+  float* qkv = nullptr;
+  float* attn_o = nullptr;
+  float* g = nullptr;
+  float* sumsq = nullptr;
+  float* gemv_partials = nullptr;
+  unsigned* gemv_counters = nullptr;
+  float* attn_partials = nullptr;
+  unsigned* attn_counters = nullptr;
+  float2* rope = nullptr;
+  double* inv_freq = nullptr;
+  unsigned long long* amax_key = nullptr;
+  unsigned* status = nullptr;
+  int split_len = 64, max_splits = 1;
+  // graph state
+  bool graph_mode = true;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool have_graph = false;
+  StepPtrs captured{};
+  // profiling events
+  std::vector<cudaEvent_t> events;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+double wbytes_per_elem(int fmt) { return fmt == DEC_W_BF16 ? 2.0 : 0.5 + 4.0 / kGroup; }
+
+size_t linear_bytes(int fmt, int N, int K) {
+  if (fmt == DEC_W_BF16) return align_up(static_cast<size_t>(N) * K * 2, 256);
+  return align_up(static_cast<size_t>(N) * K / 2, 256) + align_up(static_cast<size_t>(N) * (K / kGroup) * 4, 256);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dec_status validate(const dec_config* c) {
+  if (!c) {
+    set_err("config is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_layers < 1 || c->hidden < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->head_dim < 1 ||
+      c->intermediate < 1 || c->vocab < 1 || c->batch < 1 || c->max_ctx < 1) {
+    set_err("config sizes must be positive");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.f) || !std::isfinite(c->rms_eps) || !std::isfinite(c->rope_theta)) {
+    set_err("rms_eps must be > 0 and rope_theta > 1");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->linear_fmt != DEC_W_BF16 && c->linear_fmt != DEC_W_AFFINE4_G64) {
+    set_err("unknown linear_fmt %d", c->linear_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_q_heads % c->n_kv_heads != 0) {
+    set_err("n_q_heads (%d) must be a multiple of n_kv_heads (%d)", c->n_q_heads, c->n_kv_heads);
+    return DEC_ERR_INVALID_ARG;
+  }
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) {
+    set_err("query heads per KV head must be 1, 2 or 4 (got %d)", G);
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->head_dim != 64 && c->head_dim != 128) {
+    set_err("head_dim must be 64 or 128 (got %d)", c->head_dim);
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->hidden % 64 || c->intermediate % 64) {
+    set_err("hidden and intermediate must be multiples of 64");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->batch != 1) {
+    set_err("batch %d: only batch 1 is implemented", c->batch);
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (static_cast<long long>(c->max_ctx) * c->n_kv_heads * c->batch * c->head_dim > (1ll << 40)) {
+    set_err("KV cache too large");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  return DEC_OK;
+}
+
+dec_status check_linear(const dec_linear& l, int fmt, const char* name, int layer) {
+  if (!l.w || !aligned16(l.w)) {
+    set_err("layer %d %s: weight pointer NULL or not 16-byte aligned", layer, name);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (fmt == DEC_W_AFFINE4_G64 && (!l.scales || !l.biases)) {
+    set_err("layer %d %s: affine 4-bit linear needs scales and biases", layer, name);
+    return DEC_ERR_INVALID_ARG;
+  }
+  return DEC_OK;
+}
+
+// K splits of a batch-1 GEMV: enough CTAs to cover the SMs several times.
+int choose_splits(int N, int K, int fmt, int num_sms) {
+  const int cols = fmt == DEC_W_BF16 ? 8 : 32;
+  const int tiles = (N + kGemvRows - 1) / kGemvRows;
+  int S = 1;
+  while (static_cast<long long>(tiles) * S < 4ll * num_sms) {
+    const int S2 = S * 2;
+    if (K % S2 != 0) break;
+    const int KS = K / S2;
+    if (KS % cols != 0 || KS / cols < 64) break;
+    S = S2;
+  }
+  return S;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- step enqueue
+
+namespace {
+
+dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, bool pdl,
+                        std::vector<int>* classes) {
+  const dec_config& c = h->cfg;
+  const int d = c.head_dim, H = c.hidden;
+  LaunchCtx lc{stream, false};
+  auto note = [&](int cls) {
+    if (classes) classes->push_back(cls);
+  };
+  auto check = [&](cudaError_t e, const char* what) -> dec_status {
+    if (e != cudaSuccess) {
+      set_err("launch of %s failed: %s", what, cudaGetErrorString(e));
+      return DEC_ERR_CUDA;
+    }
+    return DEC_OK;
+  };
+  // profiling: events around each launch
+  int ev = 0;
+  auto ev_begin = [&]() -> cudaError_t {
+    if (!classes) return cudaSuccess;
+    return cudaEventRecord(h->events[2 * ev], stream);
+  };
+  auto ev_end = [&]() -> cudaError_t {
+    if (!classes) return cudaSuccess;
+    cudaError_t e = cudaEventRecord(h->events[2 * ev + 1], stream);
+    ++ev;
+    return e;
+  };
+  dec_status st;
+
+  EmbedParams ep{};
+  ep.embed = h->embed;
+  ep.tokens = sp.tokens;
+  ep.positions = sp.positions;
+  ep.inv_freq = h->inv_freq;
+  ep.h = h->h;
+  ep.sumsq = h->sumsq;
+  ep.rope = h->rope;
+  ep.amax_key = h->amax_key;
+  ep.status = h->status;
+  ep.V = c.vocab;
+  ep.H = H;
+  ep.half_d = d / 2;
+  ep.max_ctx = c.max_ctx;
+  note(DEC_K_EMBED);
+  ev_begin();
+  if ((st = check(launch_embed(lc, ep, c.batch), "embed")) != DEC_OK) return st;
+  ev_end();
+  lc.pdl = pdl;
+
+  auto gemv = [&](const PackedLinear& L, int in_mode, int epi, const float* x, const __nv_bfloat16* norm_w,
+                  float* out, int cls, const char* what) -> dec_status {
+    GemvParams gp{};
+    gp.w = L.w;
+    gp.sb = L.sb;
+    gp.N = L.N;
+    gp.K = L.K;
+    gp.S = L.S;
+    gp.KS = L.K / L.S;
+    gp.x = x;
+    gp.norm_w = norm_w;
+    gp.sumsq_in = h->sumsq;
+    gp.n_sumsq_in = H / kResGroup;
+    gp.eps = c.rms_eps;
+    gp.out = out;
+    gp.sumsq_out = h->sumsq;
+    gp.partials = h->gemv_partials;
+    gp.counters = h->gemv_counters;
+    gp.amax_key = h->amax_key;
+    gp.argmax_out = sp.argmax;
+    note(cls);
+    ev_begin();
+    dec_status s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
+    ev_end();
+    return s2;
+  };
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const PackedLayer& L = h->layers[l];
+    if ((st = gemv(L.qkv, kInNorm, kEpiStore, h->h, L.in_norm, h->qkv, DEC_K_QKV, "qkv")) != DEC_OK) return st;
+
+    AttnParams ap{};
+    ap.qkv = h->qkv;
+    ap.q_norm = L.q_norm;
+    ap.k_norm = L.k_norm;
+    ap.rope = h->rope;
+    ap.positions = sp.positions;
+    ap.kv = static_cast<__nv_bfloat16*>(sp.kv);
+    ap.layer = l;
+    ap.B = c.batch;
+    ap.nq = c.n_q_heads;
+    ap.nkv = c.n_kv_heads;
+    ap.max_ctx = c.max_ctx;
+    ap.split_len = h->split_len;
+    ap.max_splits = h->max_splits;
+    ap.eps = c.rms_eps;
+    ap.partials = h->attn_partials;
+    ap.counters = h->attn_counters;
+    ap.out = h->attn_o;
+    ap.status = h->status;
+    note(DEC_K_ATTN);
+    ev_begin();
+    if ((st = check(launch_attention(lc, ap, d), "attention")) != DEC_OK) return st;
+    ev_end();
+
+    if ((st = gemv(L.o, kInPlain, kEpiResid, h->attn_o, nullptr, h->h, DEC_K_OPROJ, "o_proj")) != DEC_OK) return st;
+    if ((st = gemv(L.gateup, kInNorm, kEpiSwiglu, h->h, L.post_norm, h->g, DEC_K_GATEUP, "gate_up")) != DEC_OK)
+      return st;
+    if ((st = gemv(L.down, kInPlain, kEpiResid, h->g, nullptr, h->h, DEC_K_DOWN, "down")) != DEC_OK) return st;
+  }
+  if ((st = gemv(h->lm_head, kInNorm, kEpiLmHead, h->h, h->final_norm, sp.logits, DEC_K_LMHEAD, "lm_head")) !=
+      DEC_OK)
+    return st;
+  return DEC_OK;
+}
+
+void drop_graph(dec_handle* h) {
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  h->exec = nullptr;
+  h->graph = nullptr;
+  h->have_graph = false;
+}
+
+dec_status capture_graph(dec_handle* h, const StepPtrs& sp) {
+  drop_graph(h);
+  DEC_CUDA(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  dec_status st = enqueue_step(h, sp, h->cap_stream, true, nullptr);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  if (st != DEC_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return st;
+  }
+  if (e != cudaSuccess) {
+    set_err("cudaStreamEndCapture failed: %s", cudaGetErrorString(e));
+    return DEC_ERR_CUDA;
+  }
+  h->graph = graph;
+  e = cudaGraphInstantiateWithFlags(&h->exec, graph, 0);
+  if (e != cudaSuccess) {
+    set_err("cudaGraphInstantiate failed: %s", cudaGetErrorString(e));
+    drop_graph(h);
+    return DEC_ERR_CUDA;
+  }
+  h->captured = sp;
+  h->have_graph = true;
+  return DEC_OK;
+}
+
+dec_status check_step_args(dec_handle* h, const StepPtrs& sp) {
+  if (!h) {
+    set_err("handle is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (!sp.tokens || !sp.positions || !sp.kv || !sp.argmax) {
+    set_err("token_ids, positions, kv_cache and argmax_out must be non-NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (!aligned16(sp.kv)) {
+    set_err("kv_cache must be 16-byte aligned");
+    return DEC_ERR_INVALID_ARG;
+  }
+  return DEC_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- public API
+
+extern "C" size_t dec_kv_cache_bytes(const dec_config* cfg) {
+  if (!cfg || cfg->n_layers < 1 || cfg->batch < 1 || cfg->n_kv_heads < 1 || cfg->max_ctx < 1 || cfg->head_dim < 1)
+    return 0;
+  return static_cast<size_t>(cfg->n_layers) * 2 * cfg->batch * cfg->n_kv_heads * cfg->max_ctx * cfg->head_dim * 2;
+}
+
+extern "C" const char* dec_last_error(void) { return g_err; }
+
+extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts) {
+  g_err[0] = 0;
+  if (validate(cfg) != DEC_OK) return nullptr;
+  if (!wts || !wts->layers || !wts->embed || !wts->final_norm) {
+    set_err("weights, weights->layers, embed and final_norm must be non-NULL");
+    return nullptr;
+  }
+  const dec_config c = *cfg;
+  const int fmt = c.linear_fmt;
+  const int H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate, V = c.vocab;
+  if (check_linear(wts->lm_head, fmt, "lm_head", -1) != DEC_OK || !aligned16(wts->embed)) return nullptr;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dec_layer_weights& lw = wts->layers[l];
+    if (!lw.in_norm || !lw.post_norm || !lw.q_norm || !lw.k_norm) {
+      set_err("layer %d: norm weight pointer is NULL", l);
+      return nullptr;
+    }
+    const dec_linear* lins[7] = {&lw.q, &lw.k, &lw.v, &lw.o, &lw.gate, &lw.up, &lw.down};
+    const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+    for (int i = 0; i < 7; ++i)
+      if (check_linear(*lins[i], fmt, names[i], l) != DEC_OK) return nullptr;
+  }
+
+  dec_handle* h = new dec_handle();
+  h->cfg = c;
+  h->wfmt = fmt == DEC_W_BF16 ? kWBf16 : kWQ4;
+  auto fail = [&](const char* what, cudaError_t e) -> dec_handle* {
+    set_err("%s: %s", what, cudaGetErrorString(e));
+    dec_destroy(h);
+    return nullptr;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&h->device)) != cudaSuccess) return fail("cudaGetDevice", e);
+  if ((e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess)
+    return fail("cudaDeviceGetAttribute", e);
+  if ((e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess)
+    return fail("cudaStreamCreate", e);
+
+  // ---- packed weight memory
+  const int nqkv = (nq + 2 * nkv) * d;
+  size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
+                 linear_bytes(fmt, V, H);
+  const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +
+                           linear_bytes(fmt, nqkv, H) + linear_bytes(fmt, H, nq * d) + linear_bytes(fmt, 2 * I, H) +
+                           linear_bytes(fmt, H, I);
+  total += per_layer * c.n_layers;
+  if ((e = cudaMalloc(&h->wmem, total)) != cudaSuccess) {
+    set_err("cudaMalloc of %zu bytes of packed weights failed: %s", total, cudaGetErrorString(e));
+    dec_destroy(h);
+    return nullptr;
+  }
+  h->wbytes = total;
+  unsigned char* cur = h->wmem;
+  auto take = [&](size_t bytes) {
+    unsigned char* p = cur;
+    cur += align_up(bytes, 256);
+    return p;
+  };
+  auto take_linear = [&](int N, int K) {
+    PackedLinear L;
+    L.N = N;
+    L.K = K;
+    L.S = choose_splits(N, K, fmt, h->num_sms);
+    if (fmt == DEC_W_BF16) {
+      L.w = take(static_cast<size_t>(N) * K * 2);
+    } else {
+      L.w = take(static_cast<size_t>(N) * K / 2);
+      L.sb = reinterpret_cast<uint32_t*>(take(static_cast<size_t>(N) * (K / kGroup) * 4));
+    }
+    return L;
+  };
+  h->embed = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(V) * H * 2));
+  h->final_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(H) * 2));
+  h->lm_head = take_linear(V, H);
+  h->layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    PackedLayer& L = h->layers[l];
+    L.in_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(H) * 2));
+    L.post_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(H) * 2));
+    L.q_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(d) * 2));
+    L.k_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(d) * 2));
+    L.qkv = take_linear(nqkv, H);
+    L.o = take_linear(H, nq * d);
+    L.gateup = take_linear(2 * I, H);
+    L.down = take_linear(H, I);
+  }
+
+  // ---- pack (device to device on the internal stream)
+  cudaStream_t s = h->cap_stream;
+  auto cp = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
+  auto pack_lin = [&](const PackedLinear& P, size_t row_off, const dec_linear& a, const dec_linear* b, int rows,
+                      int K, int ib) -> cudaError_t {
+    if (fmt == DEC_W_BF16) {
+      return pack_rows_bf16(s, static_cast<__nv_bfloat16*>(P.w) + row_off * K, static_cast<const __nv_bfloat16*>(a.w),
+                            b ? static_cast<const __nv_bfloat16*>(b->w) : nullptr, rows, K, ib);
+    }
+    return pack_rows_q4(s, static_cast<uint32_t*>(P.w) + row_off * (K / 8), P.sb + row_off * (K / kGroup),
+                        static_cast<const uint32_t*>(a.w), static_cast<const __nv_bfloat16*>(a.scales),
+                        static_cast<const __nv_bfloat16*>(a.biases), b ? static_cast<const uint32_t*>(b->w) : nullptr,
+                        b ? static_cast<const __nv_bfloat16*>(b->scales) : nullptr,
+                        b ? static_cast<const __nv_bfloat16*>(b->biases) : nullptr, rows, K, ib);
+  };
+  if ((e = cp(h->embed, wts->embed, static_cast<size_t>(V) * H * 2)) != cudaSuccess) return fail("copy embed", e);
+  if ((e = cp(h->final_norm, wts->final_norm, static_cast<size_t>(H) * 2)) != cudaSuccess) return fail("copy norm", e);
+  if ((e = pack_lin(h->lm_head, 0, wts->lm_head, nullptr, V, H, 0)) != cudaSuccess) return fail("pack lm_head", e);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dec_layer_weights& lw = wts->layers[l];
+    PackedLayer& L = h->layers[l];
+    if ((e = cp(L.in_norm, lw.in_norm, static_cast<size_t>(H) * 2)) != cudaSuccess) return fail("copy norm", e);
+    if ((e = cp(L.post_norm, lw.post_norm, static_cast<size_t>(H) * 2)) != cudaSuccess) return fail("copy norm", e);
+    if ((e = cp(L.q_norm, lw.q_norm, static_cast<size_t>(d) * 2)) != cudaSuccess) return fail("copy norm", e);
+    if ((e = cp(L.k_norm, lw.k_norm, static_cast<size_t>(d) * 2)) != cudaSuccess) return fail("copy norm", e);
+    if ((e = pack_lin(L.qkv, 0, lw.q, nullptr, nq * d, H, 0)) != cudaSuccess) return fail("pack q", e);
+    if ((e = pack_lin(L.qkv, static_cast<size_t>(nq) * d, lw.k, nullptr, nkv * d, H, 0)) != cudaSuccess)
+      return fail("pack k", e);
+    if ((e = pack_lin(L.qkv, static_cast<size_t>(nq + nkv) * d, lw.v, nullptr, nkv * d, H, 0)) != cudaSuccess)
+      return fail("pack v", e);
+    if ((e = pack_lin(L.o, 0, lw.o, nullptr, H, nq * d, 0)) != cudaSuccess) return fail("pack o", e);
+    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, kGemvRows / 2)) != cudaSuccess)
+      return fail("pack gate/up", e);
+    if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
+  }
+
+  // ---- attention split length: up to 16 CTAs per SM at the full context, splits of <= 512 positions
+  const int G = nq / nkv;
+  int split_len = kAttnTile;
+  auto nsplits = [&](int L) { return (c.max_ctx + L - 1) / L; };
+  while (split_len < 512 && (static_cast<long long>(c.batch) * nkv * nsplits(split_len) > 16ll * h->num_sms ||
+                             nsplits(split_len) * G > 1024))
+    split_len *= 2;
+  while (nsplits(split_len) * G > 1024) split_len *= 2;
+  h->split_len = split_len;
+  h->max_splits = nsplits(split_len);
+
+  // ---- workspace
+  const int B = c.batch;
+  int max_tiles = 0;
+  size_t max_partials = 0;
+  auto acc_lin = [&](const PackedLinear& L) {
+    const int tiles = (L.N + kGemvRows - 1) / kGemvRows;
+    max_tiles = tiles > max_tiles ? tiles : max_tiles;
+    if (L.S > 1) {
+      const size_t pp = static_cast<size_t>(L.S) * L.N * B;
+      max_partials = pp > max_partials ? pp : max_partials;
+    }
+  };
+  acc_lin(h->lm_head);
+  for (auto& L : h->layers) {
+    acc_lin(L.qkv);
+    acc_lin(L.o);
+    acc_lin(L.gateup);
+    acc_lin(L.down);
+  }
+  const size_t n_attn_part = static_cast<size_t>(B) * nkv * h->max_splits * G * (d + 2);
+  size_t ws_bytes = 0;
+  auto plan = [&](size_t bytes) {
+    size_t off = ws_bytes;
+    ws_bytes += align_up(bytes, 256);
+    return off;
+  };
+  const size_t o_h = plan(static_cast<size_t>(B) * H * 4);
+  const size_t o_qkv = plan(static_cast<size_t>(B) * nqkv * 4);
+  const size_t o_att = plan(static_cast<size_t>(B) * nq * d * 4);
+  const size_t o_g = plan(static_cast<size_t>(B) * I * 4);
+  const size_t o_ss = plan(static_cast<size_t>(B) * (H / kResGroup) * 4);
+  const size_t o_gp = plan((max_partials ? max_partials : 1) * 4);
+  const size_t o_gc = plan(static_cast<size_t>(max_tiles + 1) * 4);
+  const size_t o_ap = plan(n_attn_part * 4);
+  const size_t o_ac = plan(static_cast<size_t>(B) * nkv * 4);
+  const size_t o_rope = plan(static_cast<size_t>(B) * (d / 2) * 8);
+  const size_t o_inv = plan(static_cast<size_t>(d / 2) * 8);
+  const size_t o_key = plan(static_cast<size_t>(B) * 8);
+  const size_t o_st = plan(4);
+  if ((e = cudaMalloc(&h->ws, ws_bytes)) != cudaSuccess) {
+    set_err("cudaMalloc of %zu bytes of workspace failed: %s", ws_bytes, cudaGetErrorString(e));
+    dec_destroy(h);
+    return nullptr;
+  }
+  if ((e = cudaMemsetAsync(h->ws, 0, ws_bytes, s)) != cudaSuccess) return fail("memset workspace", e);
+  h->h = reinterpret_cast<float*>(h->ws + o_h);
+  h->qkv = reinterpret_cast<float*>(h->ws + o_qkv);
+  h->attn_o = reinterpret_cast<float*>(h->ws + o_att);
+  h->g = reinterpret_cast<float*>(h->ws + o_g);
+  h->sumsq = reinterpret_cast<float*>(h->ws + o_ss);
+  h->gemv_partials = reinterpret_cast<float*>(h->ws + o_gp);
+  h->gemv_counters = reinterpret_cast<unsigned*>(h->ws + o_gc);
+  h->attn_partials = reinterpret_cast<float*>(h->ws + o_ap);
+  h->attn_counters = reinterpret_cast<unsigned*>(h->ws + o_ac);
+  h->rope = reinterpret_cast<float2*>(h->ws + o_rope);
+  h->inv_freq = reinterpret_cast<double*>(h->ws + o_inv);
+  h->amax_key = reinterpret_cast<unsigned long long*>(h->ws + o_key);
+  h->status = reinterpret_cast<unsigned*>(h->ws + o_st);
+
+  // RoPE inverse frequencies theta^(-2i/d), i < d/2, in double on the host
+  std::vector<double> inv(d / 2);
+  for (int i = 0; i < d / 2; ++i) inv[i] = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / d);
+  if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return fail("upload inv_freq", e);
+  if ((e = prepare_attention(d, G)) != cudaSuccess) return fail("attention kernel attributes", e);
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail("packing", e);
+  return h;
+}
+
+extern "C" void dec_destroy(dec_handle* h) {
+  if (!h) return;
+  drop_graph(h);
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->wmem) cudaFree(h->wmem);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}
+
+extern "C" dec_status dec_step(dec_handle* h, const int32_t* token_ids, const int32_t* positions, void* kv_cache,
+                               float* logits_out, int32_t* argmax_out, dec_stream_t stream) {
+  const StepPtrs sp{token_ids, positions, kv_cache, logits_out, argmax_out};
+  dec_status st = check_step_args(h, sp);
+  if (st != DEC_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!h->graph_mode) {
+    st = enqueue_step(h, sp, cs, true, nullptr);
+    return st;
+  }
+  if (!h->have_graph || !(h->captured == sp)) {
+    if ((st = capture_graph(h, sp)) != DEC_OK) return st;
+  }
+  DEC_CUDA(cudaGraphLaunch(h->exec, cs));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_set_graph_mode(dec_handle* h, int enabled) {
+  if (!h) {
+    set_err("handle is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  h->graph_mode = enabled != 0;
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_get_device_status(dec_handle* h, int* out) {
+  if (!h || !out) {
+    set_err("handle and out must be non-NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  unsigned v = 0;
+  DEC_CUDA(cudaMemcpy(&v, h->status, 4, cudaMemcpyDeviceToHost));
+  const unsigned zero = 0;
+  DEC_CUDA(cudaMemcpy(h->status, &zero, 4, cudaMemcpyHostToDevice));
+  *out = static_cast<int>(v);
+  if (v & kStatusTimeout) {
+    set_err("a bounded device wait timed out");
+    return DEC_ERR_TIMEOUT;
+  }
+  if (v) {
+    set_err("device input out of range (status bits 0x%x)", v);
+    return DEC_ERR_DEVICE_INPUT;
+  }
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, float* out, dec_stream_t stream) {
+  if (!h || !out || which < 0 || which > 7 || (which < 7 && (layer < 0 || layer >= h->cfg.n_layers))) {
+    set_err("dec_debug_dequant: bad arguments");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const dec_config& c = h->cfg;
+  const int d = c.head_dim, H = c.hidden;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const PackedLinear* P;
+  int rows, K, off = 0, ib = 0, half = -1;
+  if (which == 7) {
+    P = &h->lm_head;
+    rows = c.vocab;
+    K = H;
+  } else {
+    const PackedLayer& L = h->layers[layer];
+    switch (which) {
+      case 0: P = &L.qkv; rows = c.n_q_heads * d; K = H; break;
+      case 1: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = c.n_q_heads * d; break;
+      case 2: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = (c.n_q_heads + c.n_kv_heads) * d; break;
+      case 3: P = &L.o; rows = H; K = c.n_q_heads * d; break;
+      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = kGemvRows / 2; half = 0; break;
+      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = kGemvRows / 2; half = 1; break;
+      default: P = &L.down; rows = H; K = c.intermediate; break;
+    }
+  }
+  DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_advance(const int32_t* argmax, int32_t* token_ids, int32_t* positions, int batch,
+                                  dec_stream_t stream) {
+  if (!argmax || !token_ids || !positions || batch < 1) {
+    set_err("dec_advance: bad arguments");
+    return DEC_ERR_INVALID_ARG;
+  }
+  DEC_CUDA(launch_advance(reinterpret_cast<cudaStream_t>(stream), argmax, token_ids, positions, batch));
+  return DEC_OK;
+}
+
+extern "C" int dec_launches_per_step(const dec_handle* h) { return h ? 5 * h->cfg.n_layers + 2 : 0; }
+
+extern "C" dec_status dec_profile_step(dec_handle* h, const int32_t* token_ids, const int32_t* positions,
+                                       void* kv_cache, float* logits_out, int32_t* argmax_out, dec_stream_t stream,
+                                       double* ms, int* launches, int n_classes) {
+  const StepPtrs sp{token_ids, positions, kv_cache, logits_out, argmax_out};
+  dec_status st = check_step_args(h, sp);
+  if (st != DEC_OK) return st;
+  if (!ms || !launches || n_classes < DEC_K_COUNT) {
+    set_err("dec_profile_step: ms/launches must hold DEC_K_COUNT entries");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const int n = dec_launches_per_step(h);
+  while (static_cast<int>(h->events.size()) < 2 * n) {
+    cudaEvent_t ev;
+    DEC_CUDA(cudaEventCreate(&ev));
+    h->events.push_back(ev);
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<int> classes;
+  if ((st = enqueue_step(h, sp, cs, false, &classes)) != DEC_OK) return st;
+  DEC_CUDA(cudaStreamSynchronize(cs));
+  for (size_t i = 0; i < classes.size(); ++i) {
+    float t = 0.f;
+    DEC_CUDA(cudaEventElapsedTime(&t, h->events[2 * i], h->events[2 * i + 1]));
+    ms[classes[i]] += t;
+    launches[classes[i]] += 1;
+  }
+  return DEC_OK;
+}
+
+extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cached_len) {
+  if (!h) return 0.0;
+  const dec_config& c = h->cfg;
+  const double wb = wbytes_per_elem(c.linear_fmt);
+  const double H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate, V = c.vocab;
+  const double B = c.batch;
+  switch (cls) {
+    case DEC_K_EMBED: return B * H * 2.0;
+    case DEC_K_QKV: return (nq + 2 * nkv) * d * H * wb + H * 2.0;
+    case DEC_K_ATTN: return B * nkv * 2.0 * d * 2.0 * (mean_cached_len + 1.0) + 2.0 * d * 2.0;
+    case DEC_K_OPROJ: return H * nq * d * wb;
+    case DEC_K_GATEUP: return 2.0 * I * H * wb + H * 2.0;
+    case DEC_K_DOWN: return H * I * wb;
+    case DEC_K_LMHEAD: return V * H * wb + H * 2.0;
+    default: return 0.0;
+  }
+}

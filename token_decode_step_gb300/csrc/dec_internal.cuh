@@ -1,0 +1,197 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+// Target: sm_103a (GB300).  No host-side torch types anywhere.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/dec.h"
+
+namespace dec {
+
+// ---------------------------------------------------------------- constants
+
+constexpr int kResGroup = 8;        // rows per partial sum-of-squares of the residual
+constexpr int kGemvRows = 8;        // rows per CTA of the batch-1 GEMV
+constexpr int kAttnTile = 64;       // positions per attention smem tile
+constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
+constexpr int kGroup = 64;          // affine 4-bit group size
+
+enum StatusBits : unsigned { kStatusBadToken = 1u, kStatusBadPos = 2u, kStatusTimeout = 4u };
+
+enum Epilogue : int { kEpiStore = 0, kEpiResid = 1, kEpiSwiglu = 2, kEpiLmHead = 3 };
+enum InMode : int { kInPlain = 0, kInNorm = 1 };
+enum WFmt : int { kWBf16 = 0, kWQ4 = 1 };
+
+// ---------------------------------------------------------------- kernel params
+
+// Batch-1 GEMV: y = W x over a row tile (kGemvRows rows) and one K split.
+struct GemvParams {
+  const void* w;            // bf16 [N][K] or q4 words uint32 [N][K/8]
+  const uint32_t* sb;       // q4: scale (low 16 bits) | bias (high 16 bits), [N][K/64]
+  int N, K, S, KS;          // rows, inputs, K splits, inputs per split
+  // input vector (fp32 [K]); kInNorm: x = h * rsqrt(sum(sumsq_in)/K + eps) * norm_w
+  const float* x;
+  const __nv_bfloat16* norm_w;
+  const float* sumsq_in;    // [n_sumsq_in]
+  int n_sumsq_in;
+  float eps;
+  // epilogue
+  float* out;               // store: y[N]; resid: h[N] (+=); swiglu: g[N/2]; lmhead: logits[N] or null
+  float* sumsq_out;         // resid: [N / kResGroup]
+  float* partials;          // [S][N] when S > 1
+  unsigned* counters;       // [N / kGemvRows] (+1 for lmhead) zero on entry, left zero
+  unsigned long long* amax_key;  // lmhead: packed (ordered value, ~index)
+  int32_t* argmax_out;      // lmhead
+};
+
+// Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
+struct AttnParams {
+  const float* qkv;             // [B][(nq + 2 nkv) d] projections
+  const __nv_bfloat16* q_norm;  // [d]
+  const __nv_bfloat16* k_norm;  // [d]
+  const float2* rope;           // [B][d/2] (cos, sin) at this step's positions
+  const int32_t* positions;     // [B]
+  __nv_bfloat16* kv;            // whole cache
+  int layer, B, nq, nkv, max_ctx;
+  int split_len;                // positions per split (multiple of kAttnTile)
+  int max_splits;
+  float eps;
+  float* partials;              // [B][nkv][max_splits][G][d + 2]
+  unsigned* counters;           // [B][nkv]
+  float* out;                   // [B][nq d]
+  unsigned* status;
+};
+
+struct EmbedParams {
+  const __nv_bfloat16* embed;   // [V][H]
+  const int32_t* tokens;
+  const int32_t* positions;
+  const double* inv_freq;       // [d/2]
+  float* h;                     // [B][H]
+  float* sumsq;                 // [B][H / kResGroup]
+  float2* rope;                 // [B][d/2]
+  unsigned long long* amax_key; // [B]
+  unsigned* status;
+  int V, H, half_d, max_ctx;
+};
+
+// ---------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte streaming load that bypasses L1 (weights are read once per step).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Ordered-key encoding of a float so that unsigned comparison follows float order.
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  // larger value wins; among equal values the lower index wins (larger ~idx)
+  return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(idx));
+}
+__device__ __forceinline__ int argmax_key_index(unsigned long long k) {
+  return static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
+}
+
+// bf16x2 pack of two floats (round to nearest even), first argument in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------- tensor-core helpers (mma.sync)
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t smem_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t smem_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_addr));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 fills the destination with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+}  // namespace dec
+
+// ---------------------------------------------------------------- host-side launchers
+// (defined in the kernel translation units, called by the C-ABI layer)
+
+namespace dec {
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  bool pdl;   // launch with programmatic stream serialization
+};
+
+cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B);
+cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int in_mode, int epi);
+cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim);
+size_t attention_smem_bytes(int head_dim);
+cudaError_t prepare_attention(int head_dim, int G);  // set the dynamic smem limit (before capture)
+
+// create-time packing and test hooks
+cudaError_t pack_rows_bf16(cudaStream_t s, __nv_bfloat16* dst, const __nv_bfloat16* src_a,
+                           const __nv_bfloat16* src_b, int rows_out, int K, int interleave_block);
+cudaError_t pack_rows_q4(cudaStream_t s, uint32_t* dst_w, uint32_t* dst_sb, const uint32_t* src_w_a,
+                         const __nv_bfloat16* sc_a, const __nv_bfloat16* bi_a, const uint32_t* src_w_b,
+                         const __nv_bfloat16* sc_b, const __nv_bfloat16* bi_b, int rows_out, int K,
+                         int interleave_block);
+cudaError_t debug_dequant(cudaStream_t s, float* out, const void* w, const uint32_t* sb, int wfmt,
+                          int rows_out, int K, int row_offset, int interleave_block, int which_half);
+cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
+                           int batch);
+
+}  // namespace dec

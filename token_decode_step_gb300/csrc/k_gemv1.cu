@@ -1,0 +1,278 @@
+// Batch-1 fused GEMV kernels (CUDA cores): y = W x for one 8-row tile and one K split,
+// with the RMSNorm of the input folded into the prologue and the consumer step
+// (store / residual add / SwiGLU / lm_head argmax) folded into the epilogue.
+//
+// Butter architecture.md, "SINGLE-TOKEN DECODE": rms_norm -> gemv (q, k, v),
+// gemv (o) -> add, rms_norm -> gemv (gate, up) -> silu_mul, gemv (down) -> add,
+// rms_norm -> gemv (lm_head); the same page plans a fused rms_norm_qkv kernel
+// that reads the activation once.  ANEForge "LLMs on the ANE", "lm_head on the
+// ANE": the lm_head is tiled along the vocabulary; here each CTA is a vocab tile
+// that reduces its own (max, index) and the last tile publishes the argmax.
+//
+// Weight streaming: every thread issues 16-byte L1-bypassing loads of 8 rows at
+// once; the first chunk is requested before the grid-dependency wait, so it
+// overlaps the previous kernel's tail (programmatic dependent launch).
+#include "dec_internal.cuh"
+#include "q4.cuh"
+
+namespace dec {
+
+namespace {
+
+template <int WF>
+struct ChunkTraits;
+template <>
+struct ChunkTraits<kWBf16> {
+  static constexpr int kCols = 8;  // 16 bytes of bf16
+};
+template <>
+struct ChunkTraits<kWQ4> {
+  static constexpr int kCols = 32;  // 16 bytes of 4-bit codes
+};
+
+template <int WF>
+__device__ __forceinline__ const void* chunk_ptr(const GemvParams& p, int row, int col) {
+  if constexpr (WF == kWBf16) {
+    return static_cast<const __nv_bfloat16*>(p.w) + static_cast<size_t>(row) * p.K + col;
+  } else {
+    return static_cast<const uint32_t*>(p.w) + static_cast<size_t>(row) * (p.K / 8) + col / 8;
+  }
+}
+
+// Input chunk: x[col .. col + n) as floats, normalised if requested.
+template <int IN, int N>
+__device__ __forceinline__ void load_x(const GemvParams& p, int col, float inv_rms, float (&xv)[N]) {
+  const float4* src = reinterpret_cast<const float4*>(p.x + col);
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i) {
+    float4 v = src[i];
+    xv[4 * i + 0] = v.x;
+    xv[4 * i + 1] = v.y;
+    xv[4 * i + 2] = v.z;
+    xv[4 * i + 3] = v.w;
+  }
+  if constexpr (IN == kInNorm) {
+    const uint4* wn = reinterpret_cast<const uint4*>(p.norm_w + col);
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i) {
+      uint4 u = wn[i];
+      xv[8 * i + 0] = (xv[8 * i + 0] * inv_rms) * bf16_lo(u.x);
+      xv[8 * i + 1] = (xv[8 * i + 1] * inv_rms) * bf16_hi(u.x);
+      xv[8 * i + 2] = (xv[8 * i + 2] * inv_rms) * bf16_lo(u.y);
+      xv[8 * i + 3] = (xv[8 * i + 3] * inv_rms) * bf16_hi(u.y);
+      xv[8 * i + 4] = (xv[8 * i + 4] * inv_rms) * bf16_lo(u.z);
+      xv[8 * i + 5] = (xv[8 * i + 5] * inv_rms) * bf16_hi(u.z);
+      xv[8 * i + 6] = (xv[8 * i + 6] * inv_rms) * bf16_lo(u.w);
+      xv[8 * i + 7] = (xv[8 * i + 7] * inv_rms) * bf16_hi(u.w);
+    }
+  }
+}
+
+__device__ __forceinline__ float dot_bf16x8(uint4 w, const float* x, float acc) {
+  acc = fmaf(bf16_lo(w.x), x[0], acc);
+  acc = fmaf(bf16_hi(w.x), x[1], acc);
+  acc = fmaf(bf16_lo(w.y), x[2], acc);
+  acc = fmaf(bf16_hi(w.y), x[3], acc);
+  acc = fmaf(bf16_lo(w.z), x[4], acc);
+  acc = fmaf(bf16_hi(w.z), x[5], acc);
+  acc = fmaf(bf16_lo(w.w), x[6], acc);
+  acc = fmaf(bf16_hi(w.w), x[7], acc);
+  return acc;
+}
+
+// sum over 8 codes of one word of (128 + q_k) * x_k
+__device__ __forceinline__ float dot_q4_word(uint32_t w, const float* x) {
+  float a = q4_code_plus128<0>(w) * x[0];
+  a = fmaf(q4_code_plus128<1>(w), x[1], a);
+  a = fmaf(q4_code_plus128<2>(w), x[2], a);
+  a = fmaf(q4_code_plus128<3>(w), x[3], a);
+  a = fmaf(q4_code_plus128<4>(w), x[4], a);
+  a = fmaf(q4_code_plus128<5>(w), x[5], a);
+  a = fmaf(q4_code_plus128<6>(w), x[6], a);
+  a = fmaf(q4_code_plus128<7>(w), x[7], a);
+  return a;
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+}  // namespace
+
+template <int WF, int IN, int EPI>
+__global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
+  constexpr int R = kGemvRows;
+  constexpr int CH = ChunkTraits<WF>::kCols;
+  __shared__ float red[8][R];
+  __shared__ float ys[R];
+  __shared__ float s_inv_rms;
+  __shared__ unsigned s_ticket;
+
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int row0 = tile * R;
+  const int nrows = min(R, p.N - row0);
+  const int kbeg = split * p.KS;
+  const int nchunk = p.KS / CH;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+
+  // First chunk's weights: independent of upstream kernels, so fetched before the wait.
+  uint4 wreg[R];
+  int c = tid;
+  if (c < nchunk) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + c * CH));
+  }
+
+  griddep_wait();
+
+  float inv_rms = 1.f;
+  if constexpr (IN == kInNorm) {
+    float s = 0.f;
+    for (int i = tid; i < p.n_sumsq_in; i += nt) s += p.sumsq_in[i];
+    s = warp_sum(s);
+    if (lane == 0) red[warp][0] = s;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < nt / 32; ++w) t += red[w][0];
+      s_inv_rms = rsqrtf(t / static_cast<float>(p.K) + p.eps);
+    }
+    __syncthreads();
+    inv_rms = s_inv_rms;
+  }
+
+  for (; c < nchunk; c += nt) {
+    const int col = kbeg + c * CH;
+    float xv[CH];
+    load_x<IN, CH>(p, col, inv_rms, xv);
+    if constexpr (WF == kWBf16) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = dot_bf16x8(wreg[r], xv, acc[r]);
+    } else {
+      float xsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) xsum += xv[i];
+      const int grp = col / kGroup;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = row0 + min(r, nrows - 1);
+        const uint32_t sbw = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + grp);
+        float d = dot_q4_word(wreg[r].x, xv) + dot_q4_word(wreg[r].y, xv + 8) + dot_q4_word(wreg[r].z, xv + 16) +
+                  dot_q4_word(wreg[r].w, xv + 24);
+        const float s = sb_scale(sbw), b = sb_bias(sbw);
+        // sum (s q + b) x = s * sum (128 + q) x + (b - 128 s) * sum x
+        acc[r] = fmaf(s, d, acc[r]);
+        acc[r] = fmaf(fmaf(-128.f, s, b), xsum, acc[r]);
+      }
+    }
+    const int cn = c + nt;
+    if (cn < nchunk) {
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + cn * CH));
+    }
+  }
+  griddep_launch_dependents();
+
+  // block reduction of the R row sums (fixed order: lanes, then warps 0..n-1)
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    float v = warp_sum(acc[r]);
+    if (lane == 0) red[warp][r] = v;
+  }
+  __syncthreads();
+  if (tid < R) {
+    float t = 0.f;
+    for (int w = 0; w < nt / 32; ++w) t += red[w][tid];
+    ys[tid] = t;
+  }
+
+  // split-K: the last CTA of a row tile adds the S partials in split order
+  if (p.S > 1) {
+    if (tid < R && tid < nrows) p.partials[static_cast<size_t>(split) * p.N + row0 + tid] = ys[tid];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_ticket = atomicAdd(&p.counters[tile], 1u);
+    __syncthreads();
+    if (s_ticket != static_cast<unsigned>(p.S - 1)) return;
+    __threadfence();
+    if (tid < R && tid < nrows) {
+      float t = 0.f;
+      for (int s = 0; s < p.S; ++s) t += __ldcg(p.partials + static_cast<size_t>(s) * p.N + row0 + tid);
+      ys[tid] = t;
+    }
+    if (tid == 0) p.counters[tile] = 0u;
+  }
+  __syncthreads();
+
+  if (tid != 0) return;
+  if constexpr (EPI == kEpiStore) {
+    for (int r = 0; r < nrows; ++r) p.out[row0 + r] = ys[r];
+  } else if constexpr (EPI == kEpiResid) {
+    float ss = 0.f;
+    for (int r = 0; r < R; ++r) {
+      float hn = p.out[row0 + r] + ys[r];
+      p.out[row0 + r] = hn;
+      ss = fmaf(hn, hn, ss);
+    }
+    p.sumsq_out[tile] = ss;
+  } else if constexpr (EPI == kEpiSwiglu) {
+    // rows 0..3: gate of outputs 4 tile + i; rows 4..7: up of the same outputs
+    for (int i = 0; i < R / 2; ++i) p.out[tile * (R / 2) + i] = silu_f(ys[i]) * ys[R / 2 + i];
+  } else {  // lm_head tile
+    unsigned long long best = 0ull;
+    for (int r = 0; r < nrows; ++r) {
+      if (p.out) p.out[row0 + r] = ys[r];
+      unsigned long long k = argmax_key(ys[r], row0 + r);
+      best = k > best ? k : best;
+    }
+    atomicMax(p.amax_key, best);
+    __threadfence();
+    const unsigned ntiles = gridDim.x;
+    unsigned done = atomicAdd(&p.counters[ntiles], 1u);
+    if (done == ntiles - 1) {
+      __threadfence();
+      unsigned long long k = atomicOr(p.amax_key, 0ull);
+      *p.argmax_out = argmax_key_index(k);
+      p.counters[ntiles] = 0u;
+    }
+  }
+}
+
+template <int WF, int IN, int EPI>
+static cudaError_t launch_one(const LaunchCtx& c, const GemvParams& p) {
+  constexpr int CH = ChunkTraits<WF>::kCols;
+  const int nchunk = p.KS / CH;
+  int nt = ((nchunk + 31) / 32) * 32;
+  nt = nt < 32 ? 32 : (nt > 256 ? 256 : nt);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.N + kGemvRows - 1) / kGemvRows, p.S);
+  cfg.blockDim = dim3(nt);
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemv1<WF, IN, EPI>, p);
+}
+
+cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int in_mode, int epi) {
+#define DEC_GEMV_CASE(WF, IN, EPI) \
+  if (wfmt == WF && in_mode == IN && epi == EPI) return launch_one<WF, IN, EPI>(c, p);
+  DEC_GEMV_CASE(kWBf16, kInNorm, kEpiStore)
+  DEC_GEMV_CASE(kWBf16, kInPlain, kEpiResid)
+  DEC_GEMV_CASE(kWBf16, kInNorm, kEpiSwiglu)
+  DEC_GEMV_CASE(kWBf16, kInNorm, kEpiLmHead)
+  DEC_GEMV_CASE(kWQ4, kInNorm, kEpiStore)
+  DEC_GEMV_CASE(kWQ4, kInPlain, kEpiResid)
+  DEC_GEMV_CASE(kWQ4, kInNorm, kEpiSwiglu)
+  DEC_GEMV_CASE(kWQ4, kInNorm, kEpiLmHead)
+#undef DEC_GEMV_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dec

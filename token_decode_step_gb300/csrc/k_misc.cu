@@ -1,0 +1,181 @@
+// Step prologue (embedding gather, RoPE table, status checks), create-time weight
+// packing, the dequant test hook and the greedy feedback helper.
+#include "dec_internal.cuh"
+#include "q4.cuh"
+
+namespace dec {
+
+// ---------------------------------------------------------------- embedding gather
+// Butter architecture.md, "SINGLE-TOKEN DECODE": h = embed_tokens[prev_token].
+// Also: per-8-row sums of squares of h (consumed by the first layer's fused
+// RMSNorm), the (cos, sin) table of this step's RoPE angles pos * theta^(-2i/d)
+// evaluated in double precision, reset of the argmax key, and range checks.
+__global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
+  griddep_wait();  // first kernel of a step: nothing upstream inside the graph
+  const int b = blockIdx.x;
+  int tok = p.tokens[b];
+  int pos = p.positions[b];
+  if (tok < 0 || tok >= p.V) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadToken);
+    tok = tok < 0 ? 0 : p.V - 1;
+  }
+  if (pos < 0 || pos >= p.max_ctx) {
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusBadPos);
+    pos = pos < 0 ? 0 : p.max_ctx - 1;
+  }
+  const __nv_bfloat16* row = p.embed + static_cast<size_t>(tok) * p.H;
+  float* hb = p.h + static_cast<size_t>(b) * p.H;
+  const int ngroups = p.H / kResGroup;
+  for (int gidx = threadIdx.x; gidx < ngroups; gidx += blockDim.x) {
+    uint4 u = *reinterpret_cast<const uint4*>(row + gidx * kResGroup);
+    float v[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                  bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+    float4* dst = reinterpret_cast<float4*>(hb + gidx * kResGroup);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    p.sumsq[static_cast<size_t>(b) * ngroups + gidx] = ss;
+  }
+  for (int i = threadIdx.x; i < p.half_d; i += blockDim.x) {
+    double ang = static_cast<double>(pos) * p.inv_freq[i];
+    double s, c;
+    sincos(ang, &s, &c);
+    p.rope[static_cast<size_t>(b) * p.half_d + i] = make_float2(static_cast<float>(c), static_cast<float>(s));
+  }
+  if (threadIdx.x == 0) p.amax_key[b] = 0ull;
+  griddep_launch_dependents();
+}
+
+cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_embed, p);
+}
+
+// ---------------------------------------------------------------- packing (create time)
+// Row p of the packed matrix takes, with interleave block IB > 0,
+//   block = p / (2 IB), w = p % (2 IB): w < IB ? A[block IB + w] : B[block IB + w - IB]
+// and with IB == 0 simply A[p].
+__device__ __forceinline__ void packed_source(int p, int ib, int& which, int& src_row) {
+  if (ib == 0) {
+    which = 0;
+    src_row = p;
+  } else {
+    int block = p / (2 * ib), w = p % (2 * ib);
+    which = w < ib ? 0 : 1;
+    src_row = block * ib + (w < ib ? w : w - ib);
+  }
+}
+
+__global__ void k_pack_rows_bf16(__nv_bfloat16* dst, const __nv_bfloat16* a, const __nv_bfloat16* b,
+                                 int rows_out, int K, int ib) {
+  const int p = blockIdx.x;
+  if (p >= rows_out) return;
+  int which, r;
+  packed_source(p, ib, which, r);
+  const uint4* src = reinterpret_cast<const uint4*>((which ? b : a) + static_cast<size_t>(r) * K);
+  uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(p) * K);
+  for (int i = threadIdx.x; i < K / 8; i += blockDim.x) d[i] = src[i];
+}
+
+cudaError_t pack_rows_bf16(cudaStream_t s, __nv_bfloat16* dst, const __nv_bfloat16* src_a,
+                           const __nv_bfloat16* src_b, int rows_out, int K, int interleave_block) {
+  if (rows_out == 0) return cudaSuccess;
+  k_pack_rows_bf16<<<rows_out, 128, 0, s>>>(dst, src_a, src_b, rows_out, K, interleave_block);
+  return cudaGetLastError();
+}
+
+__global__ void k_pack_rows_q4(uint32_t* dst_w, uint32_t* dst_sb, const uint32_t* wa, const __nv_bfloat16* sa,
+                               const __nv_bfloat16* ba, const uint32_t* wb, const __nv_bfloat16* sbb,
+                               const __nv_bfloat16* bb, int rows_out, int K, int ib) {
+  const int p = blockIdx.x;
+  if (p >= rows_out) return;
+  int which, r;
+  packed_source(p, ib, which, r);
+  const uint32_t* w = which ? wb : wa;
+  const __nv_bfloat16* sc = which ? sbb : sa;
+  const __nv_bfloat16* bi = which ? bb : ba;
+  const int nw = K / 8, ng = K / kGroup;
+  const uint4* src = reinterpret_cast<const uint4*>(w + static_cast<size_t>(r) * nw);
+  uint4* d = reinterpret_cast<uint4*>(dst_w + static_cast<size_t>(p) * nw);
+  for (int i = threadIdx.x; i < nw / 4; i += blockDim.x) d[i] = src[i];
+  for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+    uint32_t s16 = __bfloat16_as_ushort(sc[static_cast<size_t>(r) * ng + g]);
+    uint32_t b16 = __bfloat16_as_ushort(bi[static_cast<size_t>(r) * ng + g]);
+    dst_sb[static_cast<size_t>(p) * ng + g] = s16 | (b16 << 16);
+  }
+}
+
+cudaError_t pack_rows_q4(cudaStream_t s, uint32_t* dst_w, uint32_t* dst_sb, const uint32_t* src_w_a,
+                         const __nv_bfloat16* sc_a, const __nv_bfloat16* bi_a, const uint32_t* src_w_b,
+                         const __nv_bfloat16* sc_b, const __nv_bfloat16* bi_b, int rows_out, int K,
+                         int interleave_block) {
+  if (rows_out == 0) return cudaSuccess;
+  k_pack_rows_q4<<<rows_out, 128, 0, s>>>(dst_w, dst_sb, src_w_a, sc_a, bi_a, src_w_b, sc_b, bi_b, rows_out, K,
+                                          interleave_block);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- dequant test hook
+// out[r][k] (canonical row r of one linear) from the packed copy, with the GEMV's
+// code extraction and a single rounding: fmaf(scale, q, bias).
+__global__ void k_debug_dequant(float* out, const void* w, const uint32_t* sb, int wfmt, int rows_out, int K,
+                                int row_offset, int ib, int which_half) {
+  const int r = blockIdx.x;
+  if (r >= rows_out) return;
+  int p;
+  if (which_half < 0) {
+    p = row_offset + r;
+  } else {
+    int block = r / ib, within = r % ib;
+    p = row_offset + block * 2 * ib + which_half * ib + within;
+  }
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float v;
+    if (wfmt == kWBf16) {
+      const __nv_bfloat16* wb = static_cast<const __nv_bfloat16*>(w);
+      v = __bfloat162float(wb[static_cast<size_t>(p) * K + k]);
+    } else {
+      const uint32_t* ww = static_cast<const uint32_t*>(w);
+      uint32_t word = ww[static_cast<size_t>(p) * (K / 8) + k / 8];
+      float q = q4_code_plus128_rt(word, k % 8) - 128.0f;
+      uint32_t g = sb[static_cast<size_t>(p) * (K / kGroup) + k / kGroup];
+      v = fmaf(sb_scale(g), q, sb_bias(g));
+    }
+    out[static_cast<size_t>(r) * K + k] = v;
+  }
+}
+
+cudaError_t debug_dequant(cudaStream_t s, float* out, const void* w, const uint32_t* sb, int wfmt, int rows_out,
+                          int K, int row_offset, int interleave_block, int which_half) {
+  k_debug_dequant<<<rows_out, 256, 0, s>>>(out, w, sb, wfmt, rows_out, K, row_offset, interleave_block,
+                                           which_half);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- greedy feedback
+__global__ void k_advance(const int32_t* argmax, int32_t* tokens, int32_t* positions, int batch) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch) {
+    tokens[b] = argmax[b];
+    positions[b] += 1;
+  }
+}
+
+cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
+                           int batch) {
+  k_advance<<<(batch + 127) / 128, 128, 0, s>>>(argmax, tokens, positions, batch);
+  return cudaGetLastError();
+}
+
+}  // namespace dec
