@@ -193,6 +193,29 @@ DEC_API double dec_kernel_bytes(const dec_handle *h, int kernel_class, double me
 /* Number of kernels one dec_step launches. */
 DEC_API int dec_launches_per_step(const dec_handle *h);
 
+/* Kernel-level entry point: the fused attention that dec_step runs for each layer
+   (per-head q/k RMSNorm, rotate-half RoPE at positions[b], append of bf16 k, v at
+   slot positions[b] of `layer`, split-KV GQA attention over slots 0..positions[b]
+   with a log-sum-exp merge), on caller buffers.  ANEForge "LLMs on the ANE",
+   "Correctness" and "What's inside"; Butter architecture.md "SINGLE-TOKEN DECODE"
+   (rope, cache.append, sdpa_decode).
+     cfg        uses n_layers, batch, n_q_heads, n_kv_heads, head_dim, max_ctx,
+                rms_eps, rope_theta (same limits as dec_create; any batch >= 1).
+     qkv        device float [batch][(n_q + 2 n_kv) * head_dim]: the new token's raw
+                projections, q heads, then k heads, then v heads, head j at j*head_dim.
+     q_norm, k_norm  device bf16 [head_dim].
+     positions  device int32 [batch], as in dec_step (clamped if out of range).
+     kv_cache   as in dec_step; only slot positions[b] of `layer` is written.
+     out        device float [batch][n_q * head_dim]: attention output per query head.
+     workspace  caller-owned device scratch of at least
+                dec_attention_workspace_bytes(cfg) bytes, 256-byte aligned; its
+                contents on entry do not matter; one call at a time per workspace.
+   Enqueued on `stream`. */
+DEC_API size_t dec_attention_workspace_bytes(const dec_config *cfg);
+DEC_API dec_status dec_attention(const dec_config *cfg, int layer, const float *qkv, const void *q_norm,
+                                 const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
+                                 void *workspace, size_t workspace_bytes, dec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,6 +19,11 @@ MAX_ABS = 5e-2
 REL_L2 = 1e-2
 TIE_REL = 1e-2
 
+# attention-kernel output tolerance: max |out - ref| <= ATTN_ATOL + ATTN_RTOL * |ref|.
+# The kernel keeps ~16 significant bits of q and of the probabilities (bf16 hi + lo)
+# with fp32 accumulation, so its error is ~1e-6 of the value scale.
+ATTN_ATOL, ATTN_RTOL = 1e-4, 1e-4
+
 
 def np_model(model: dict) -> dict:
     def conv(x):
@@ -109,3 +114,19 @@ def kv_appended_close(gpu_kv: np.ndarray, ref_kv: np.ndarray, kv_init: np.ndarra
         rows = [f"{tuple(int(v) for v in idx[i])}: max err {err[i]:.3g} scale {scale[i]:.3g}" for i in worst]
         raise AssertionError(f"{int(bad.sum())} of {len(err)} appended K/V vectors differ by more than 2 bf16 "
                              f"steps: " + "; ".join(rows))
+
+
+def make_attention_case(seed, B, nq, nkv, d, positions, max_ctx, n_layers=2):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    qkv = torch.randn((B, (nq + 2 * nkv) * d), generator=g) * 0.7
+    q_norm = (1 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    k_norm = (1 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    kv = torch.randn((n_layers, 2, B, nkv, max_ctx, d), generator=g).to(torch.bfloat16)
+    pos = torch.tensor(positions, dtype=torch.int32)
+    return qkv, q_norm, k_norm, kv, pos
+
+
+def attention_cfg(dec, B, nq, nkv, d, max_ctx, n_layers=2):
+    return dec.DecConfig(n_layers=n_layers, hidden=64, n_q_heads=nq, n_kv_heads=nkv, head_dim=d, intermediate=64,
+                         vocab=1, rms_eps=1e-6, rope_theta=1e6, linear_fmt=0, batch=B, max_ctx=max_ctx)

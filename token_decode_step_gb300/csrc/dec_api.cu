@@ -502,16 +502,9 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
   }
 
-  // ---- attention split length: up to 16 CTAs per SM at the full context, splits of <= 512 positions
+  // ---- attention split length
   const int G = nq / nkv;
-  int split_len = kAttnTile;
-  auto nsplits = [&](int L) { return (c.max_ctx + L - 1) / L; };
-  while (split_len < 512 && (static_cast<long long>(c.batch) * nkv * nsplits(split_len) > 16ll * h->num_sms ||
-                             nsplits(split_len) * G > 1024))
-    split_len *= 2;
-  while (nsplits(split_len) * G > 1024) split_len *= 2;
-  h->split_len = split_len;
-  h->max_splits = nsplits(split_len);
+  attention_split_plan(c.batch, nkv, G, c.max_ctx, h->num_sms, &h->split_len, &h->max_splits);
 
   // ---- workspace
   const int B = c.batch;
@@ -726,4 +719,107 @@ extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cac
     case DEC_K_LMHEAD: return V * H * wb + H * 2.0;
     default: return 0.0;
   }
+}
+
+// ---------------------------------------------------------------- stand-alone attention kernel
+
+namespace {
+
+dec_status validate_attention_cfg(const dec_config* c, int layer) {
+  if (!c) {
+    set_err("config is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_layers < 1 || c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->max_ctx < 1 ||
+      layer < 0 || layer >= c->n_layers || !(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) {
+    set_err("attention: sizes must be positive, 0 <= layer < n_layers, rms_eps > 0, rope_theta > 1");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_q_heads % c->n_kv_heads != 0) {
+    set_err("n_q_heads (%d) must be a multiple of n_kv_heads (%d)", c->n_q_heads, c->n_kv_heads);
+    return DEC_ERR_INVALID_ARG;
+  }
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if ((G != 1 && G != 2 && G != 4) || (c->head_dim != 64 && c->head_dim != 128)) {
+    set_err("attention: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  return DEC_OK;
+}
+
+struct AttnWorkspace {
+  size_t counters, rope, partials, total;
+};
+
+AttnWorkspace attention_workspace_layout(const dec_config* c, int num_sms, int* split_len, int* max_splits) {
+  const int G = c->n_q_heads / c->n_kv_heads;
+  attention_split_plan(c->batch, c->n_kv_heads, G, c->max_ctx, num_sms, split_len, max_splits);
+  AttnWorkspace w{};
+  w.counters = 0;
+  w.rope = align_up(static_cast<size_t>(c->batch) * c->n_kv_heads * 4, 256);
+  w.partials = w.rope + align_up(static_cast<size_t>(c->batch) * (c->head_dim / 2) * 8, 256);
+  w.total = w.partials +
+            align_up(attention_partials_floats(c->batch, c->n_kv_heads, G, c->head_dim, *max_splits) * 4, 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" size_t dec_attention_workspace_bytes(const dec_config* cfg) {
+  if (validate_attention_cfg(cfg, 0) != DEC_OK) return 0;
+  int dev = 0, sms = 0, sl, ms;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess) {
+    set_err("cannot query the current CUDA device");
+    return 0;
+  }
+  return attention_workspace_layout(cfg, sms, &sl, &ms).total;
+}
+
+extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const float* qkv, const void* q_norm,
+                                    const void* k_norm, const int32_t* positions, void* kv_cache, float* out,
+                                    void* workspace, size_t workspace_bytes, dec_stream_t stream) {
+  dec_status st = validate_attention_cfg(cfg, layer);
+  if (st != DEC_OK) return st;
+  if (!qkv || !q_norm || !k_norm || !positions || !kv_cache || !out || !workspace || !aligned16(kv_cache) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u)) {
+    set_err("dec_attention: NULL pointer, kv_cache not 16-byte aligned or workspace not 256-byte aligned");
+    return DEC_ERR_INVALID_ARG;
+  }
+  int dev = 0, sms = 0, split_len = 0, max_splits = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const AttnWorkspace w = attention_workspace_layout(cfg, sms, &split_len, &max_splits);
+  if (workspace_bytes < w.total) {
+    set_err("dec_attention: workspace of %zu bytes, %zu needed", workspace_bytes, w.total);
+    return DEC_ERR_INVALID_ARG;
+  }
+  const int G = cfg->n_q_heads / cfg->n_kv_heads;
+  DEC_CUDA(prepare_attention(cfg->head_dim, G));
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  DEC_CUDA(cudaMemsetAsync(ws + w.counters, 0, static_cast<size_t>(cfg->batch) * cfg->n_kv_heads * 4, cs));
+  float2* rope = reinterpret_cast<float2*>(ws + w.rope);
+  DEC_CUDA(launch_rope_table(cs, positions, cfg->batch, cfg->head_dim, cfg->max_ctx, cfg->rope_theta, rope, nullptr));
+  AttnParams ap{};
+  ap.qkv = qkv;
+  ap.q_norm = static_cast<const __nv_bfloat16*>(q_norm);
+  ap.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
+  ap.rope = rope;
+  ap.positions = positions;
+  ap.kv = static_cast<__nv_bfloat16*>(kv_cache);
+  ap.layer = layer;
+  ap.B = cfg->batch;
+  ap.nq = cfg->n_q_heads;
+  ap.nkv = cfg->n_kv_heads;
+  ap.max_ctx = cfg->max_ctx;
+  ap.split_len = split_len;
+  ap.max_splits = max_splits;
+  ap.eps = cfg->rms_eps;
+  ap.partials = reinterpret_cast<float*>(ws + w.partials);
+  ap.counters = reinterpret_cast<unsigned*>(ws + w.counters);
+  ap.out = out;
+  ap.status = nullptr;
+  DEC_CUDA(launch_attention(LaunchCtx{cs, false}, ap, cfg->head_dim));
+  return DEC_OK;
 }

@@ -181,6 +181,12 @@ cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int 
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim);
 size_t attention_smem_bytes(int head_dim);
 cudaError_t prepare_attention(int head_dim, int G);  // set the dynamic smem limit (before capture)
+void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len, int* max_splits);
+size_t attention_partials_floats(int batch, int n_kv, int group, int head_dim, int max_splits);
+// (cos, sin) of pos * theta^(-2i/d) for every sequence, angles and inverse
+// frequencies in double on the device; out-of-range positions are clamped and flagged.
+cudaError_t launch_rope_table(cudaStream_t s, const int32_t* positions, int batch, int head_dim, int max_ctx,
+                              float theta, float2* rope, unsigned* status);
 
 // create-time packing and test hooks
 cudaError_t pack_rows_bf16(cudaStream_t s, __nv_bfloat16* dst, const __nv_bfloat16* src_a,

@@ -377,6 +377,22 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   if (tid == 0) p.counters[b * p.nkv + h] = 0u;
 }
 
+void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len,
+                          int* max_splits) {
+  // Up to 16 CTAs per SM at the full context with splits of <= 512 positions,
+  // and at most 1024 / group splits so the merge factors fit in shared memory.
+  int L = kAttnTile;
+  auto ns = [&](int len) { return (max_ctx + len - 1) / len; };
+  while (L < 512 && (static_cast<long long>(batch) * n_kv * ns(L) > 16ll * num_sms || ns(L) * group > 1024)) L *= 2;
+  while (ns(L) * group > 1024) L *= 2;
+  *split_len = L;
+  *max_splits = ns(L);
+}
+
+size_t attention_partials_floats(int batch, int n_kv, int group, int head_dim, int max_splits) {
+  return static_cast<size_t>(batch) * n_kv * max_splits * group * (head_dim + 2);
+}
+
 size_t attention_smem_bytes(int head_dim) {
   return head_dim == 64 ? AttnSmem<64>::kBytes : AttnSmem<128>::kBytes;
 }

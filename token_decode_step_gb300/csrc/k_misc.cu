@@ -62,6 +62,29 @@ cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B) {
   return cudaLaunchKernelEx(&cfg, k_embed, p);
 }
 
+// ---------------------------------------------------------------- RoPE table (stand-alone attention entry points)
+__global__ void k_rope_table(const int32_t* positions, int half_d, int max_ctx, double theta, float2* rope,
+                             unsigned* status) {
+  const int b = blockIdx.x;
+  int pos = positions[b];
+  if (pos < 0 || pos >= max_ctx) {
+    if (threadIdx.x == 0 && status) atomicOr(status, kStatusBadPos);
+    pos = pos < 0 ? 0 : max_ctx - 1;
+  }
+  for (int i = threadIdx.x; i < half_d; i += blockDim.x) {
+    const double inv = pow(theta, -2.0 * i / (2.0 * half_d));
+    double s, c;
+    sincos(static_cast<double>(pos) * inv, &s, &c);
+    rope[static_cast<size_t>(b) * half_d + i] = make_float2(static_cast<float>(c), static_cast<float>(s));
+  }
+}
+
+cudaError_t launch_rope_table(cudaStream_t s, const int32_t* positions, int batch, int head_dim, int max_ctx,
+                              float theta, float2* rope, unsigned* status) {
+  k_rope_table<<<batch, 64, 0, s>>>(positions, head_dim / 2, max_ctx, static_cast<double>(theta), rope, status);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- packing (create time)
 // Row p of the packed matrix takes, with interleave block IB > 0,
 //   block = p / (2 IB), w = p % (2 IB): w < IB ? A[block IB + w] : B[block IB + w - IB]

@@ -76,6 +76,9 @@ def _load() -> ctypes.CDLL:
                                             ctypes.c_int]),
         "dec_kernel_bytes": (ctypes.c_double, [vp, ctypes.c_int, ctypes.c_double]),
         "dec_launches_per_step": (ctypes.c_int, [vp]),
+        "dec_attention_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecConfig)]),
+        "dec_attention": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
+                                         ctypes.c_size_t, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -161,3 +164,14 @@ def dec_kernel_bytes(h: int, kernel_class: int, mean_cached_len: float) -> float
 
 def dec_launches_per_step(h: int) -> int:
     return int(lib.dec_launches_per_step(h))
+
+
+def dec_attention_workspace_bytes(cfg: DecConfig) -> int:
+    return int(lib.dec_attention_workspace_bytes(ctypes.byref(cfg)))
+
+
+def dec_attention(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_norm: int, positions: int, kv_cache: int,
+                  out: int, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return _check(lib.dec_attention(ctypes.byref(cfg), layer, qkv, q_norm, k_norm, positions, kv_cache, out,
+                                    workspace, workspace_bytes, stream), "dec_attention")
+
