@@ -216,6 +216,32 @@ DEC_API dec_status dec_attention(const dec_config *cfg, int layer, const float *
                                  const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
                                  void *workspace, size_t workspace_bytes, dec_stream_t stream);
 
+/* dec_attention without a workspace: same arguments, same computation and same
+   result as dec_attention, but it allocates nothing and takes no scratch from the
+   caller.  The pages have no counterpart; it exists for callers that cannot call
+   cudaMalloc at this point -- for example code running while a stream is being
+   captured into a CUDA graph in global capture mode (where cudaMalloc is not
+   allowed), plug-in or real-time hosts that hand over only input and output
+   buffers and forbid device allocations (cudaMalloc can synchronise the device and
+   can fail under memory pressure), or hosts whose allocator owns all free memory.
+   Its scratch (merge counters, RoPE table, split partials) is one fixed array of
+   16 MiB inside this library; every GPU that loads the library holds that array
+   until the process exits.  Shapes whose scratch exceeds it are rejected with
+   DEC_ERR_UNSUPPORTED and a message (for example batch 32, 8 KV heads, head_dim
+   128, 4 query heads per KV head and max_ctx 8224 need about 9.1 MB).
+     - The first call on each device does a one-time set-up (it looks up the
+       array's device address and sets the kernels' shared-memory limit) with that
+       device current; make that first call before any stream capture.
+     - Every call shares the one array and it keeps the last call's contents: the
+       merge counters are cleared at the start of every call, the rest is fully
+       rewritten.  Calls whose work overlaps on the GPU (other streams, other host
+       threads) race on the array; serialise them.
+   Enqueued on `stream` (a memset of the counters, a RoPE-table kernel, the
+   attention kernel). */
+DEC_API dec_status dec_attention_noalloc(const dec_config *cfg, int layer, const float *qkv, const void *q_norm,
+                                         const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
+                                         dec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,6 +29,15 @@ static void set_err(const char* fmt, ...) {
   va_end(ap);
 }
 
+namespace dec {
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+}  // namespace dec
+
 #define DEC_CUDA(call)                                                                     \
   do {                                                                                     \
     cudaError_t e_ = (call);                                                               \

@@ -200,4 +200,7 @@ cudaError_t debug_dequant(cudaStream_t s, float* out, const void* w, const uint3
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch);
 
+// Record the message returned by dec_last_error() on this thread.
+void set_last_error(const char* fmt, ...);
+
 }  // namespace dec

@@ -1,0 +1,145 @@
+// dec_attention_noalloc: the stand-alone fused attention (as dec_attention) for
+// callers that cannot allocate device memory.  Its scratch -- the split
+// partials, the merge counters and the RoPE table -- lives in one file-scope
+// device array instead of a caller workspace.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "dec_internal.cuh"
+
+using namespace dec;
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr int kMaxDevices = 64;
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+std::mutex g_setup_mu;
+unsigned char* g_scratch_addr[kMaxDevices];  // device address of g_attn_scratch, per device; null until set up
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Per-device set-up with that device current: the device address of the array
+// (in host code the name g_attn_scratch is only a host-side stand-in) and the
+// attention kernels' shared-memory limit.
+dec_status setup_device(int dev, unsigned char** addr) {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e != cudaSuccess || !p) {
+      set_last_error("dec_attention_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+      return DEC_ERR_CUDA;
+    }
+    const int dims[2] = {64, 128};
+    const int groups[3] = {1, 2, 4};
+    for (int d : dims)
+      for (int g : groups)
+        if ((e = prepare_attention(d, g)) != cudaSuccess) {
+          set_last_error("dec_attention_noalloc: kernel set-up failed: %s", cudaGetErrorString(e));
+          return DEC_ERR_CUDA;
+        }
+    g_scratch_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *addr = g_scratch_addr[dev];
+  return DEC_OK;
+}
+
+}  // namespace
+
+extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, const float* qkv, const void* q_norm,
+                                            const void* k_norm, const int32_t* positions, void* kv_cache, float* out,
+                                            dec_stream_t stream) {
+  if (!cfg) {
+    set_last_error("dec_attention_noalloc: config is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const dec_config& c = *cfg;
+  if (c.n_layers < 1 || c.batch < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.max_ctx < 1 || layer < 0 ||
+      layer >= c.n_layers || !(c.rms_eps > 0.f) || !(c.rope_theta > 1.f) || c.n_q_heads % c.n_kv_heads != 0) {
+    set_last_error("dec_attention_noalloc: sizes must be positive, 0 <= layer < n_layers, rms_eps > 0, "
+                   "rope_theta > 1, n_q_heads a multiple of n_kv_heads");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const int G = c.n_q_heads / c.n_kv_heads;
+  if ((G != 1 && G != 2 && G != 4) || (c.head_dim != 64 && c.head_dim != 128)) {
+    set_last_error("dec_attention_noalloc: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (!qkv || !q_norm || !k_norm || !positions || !kv_cache || !out ||
+      (reinterpret_cast<uintptr_t>(kv_cache) & 15u)) {
+    set_last_error("dec_attention_noalloc: NULL pointer or kv_cache not 16-byte aligned");
+    return DEC_ERR_INVALID_ARG;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    set_last_error("dec_attention_noalloc: cannot query the current device: %s", cudaGetErrorString(e));
+    return DEC_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_last_error("dec_attention_noalloc: device ordinal %d above %d", dev, kMaxDevices - 1);
+    return DEC_ERR_UNSUPPORTED;
+  }
+
+  // scratch layout: counters | RoPE table | split partials
+  int split_len = 0, max_splits = 0;
+  attention_split_plan(c.batch, c.n_kv_heads, G, c.max_ctx, sms, &split_len, &max_splits);
+  const size_t n_counters = static_cast<size_t>(c.batch) * c.n_kv_heads;
+  const size_t off_rope = round256(n_counters * 4);
+  const size_t off_part = off_rope + round256(static_cast<size_t>(c.batch) * (c.head_dim / 2) * 8);
+  const size_t total =
+      off_part + round256(attention_partials_floats(c.batch, c.n_kv_heads, G, c.head_dim, max_splits) * 4);
+  if (total > kNoAllocScratchBytes) {
+    set_last_error("dec_attention_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte "
+                   "array (reduce batch, n_kv_heads or max_ctx, or use dec_attention with a workspace)",
+                   total, kNoAllocScratchBytes);
+    return DEC_ERR_UNSUPPORTED;
+  }
+
+  unsigned char* scratch = nullptr;
+  dec_status st = setup_device(dev, &scratch);
+  if (st != DEC_OK) return st;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // the merge counters must start at zero; the rest is overwritten before it is read
+  if ((e = cudaMemsetAsync(scratch, 0, n_counters * 4, cs)) != cudaSuccess) {
+    set_last_error("dec_attention_noalloc: clearing the counters failed: %s", cudaGetErrorString(e));
+    return DEC_ERR_CUDA;
+  }
+  float2* rope = reinterpret_cast<float2*>(scratch + off_rope);
+  if ((e = launch_rope_table(cs, positions, c.batch, c.head_dim, c.max_ctx, c.rope_theta, rope, nullptr)) !=
+      cudaSuccess) {
+    set_last_error("dec_attention_noalloc: RoPE table launch failed: %s", cudaGetErrorString(e));
+    return DEC_ERR_CUDA;
+  }
+  AttnParams ap{};
+  ap.qkv = qkv;
+  ap.q_norm = static_cast<const __nv_bfloat16*>(q_norm);
+  ap.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
+  ap.rope = rope;
+  ap.positions = positions;
+  ap.kv = static_cast<__nv_bfloat16*>(kv_cache);
+  ap.layer = layer;
+  ap.B = c.batch;
+  ap.nq = c.n_q_heads;
+  ap.nkv = c.n_kv_heads;
+  ap.max_ctx = c.max_ctx;
+  ap.split_len = split_len;
+  ap.max_splits = max_splits;
+  ap.eps = c.rms_eps;
+  ap.partials = reinterpret_cast<float*>(scratch + off_part);
+  ap.counters = reinterpret_cast<unsigned*>(scratch);
+  ap.out = out;
+  ap.status = nullptr;
+  if ((e = launch_attention(LaunchCtx{cs, false}, ap, c.head_dim)) != cudaSuccess) {
+    set_last_error("dec_attention_noalloc: attention launch failed: %s", cudaGetErrorString(e));
+    return DEC_ERR_CUDA;
+  }
+  return DEC_OK;
+}

@@ -79,6 +79,8 @@ def _load() -> ctypes.CDLL:
         "dec_attention_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecConfig)]),
         "dec_attention": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
                                          ctypes.c_size_t, vp]),
+        "dec_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp,
+                                                 vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -175,3 +177,8 @@ def dec_attention(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_norm: int
     return _check(lib.dec_attention(ctypes.byref(cfg), layer, qkv, q_norm, k_norm, positions, kv_cache, out,
                                     workspace, workspace_bytes, stream), "dec_attention")
 
+
+def dec_attention_noalloc(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_norm: int, positions: int,
+                          kv_cache: int, out: int, stream: int = 0) -> int:
+    return _check(lib.dec_attention_noalloc(ctypes.byref(cfg), layer, qkv, q_norm, k_norm, positions, kv_cache,
+                                            out, stream), "dec_attention_noalloc")
