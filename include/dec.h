@@ -77,7 +77,8 @@ typedef enum {
 
 /* Model and run shape.  Supported (else DEC_ERR_UNSUPPORTED): head_dim in {64, 128};
    n_q_heads / n_kv_heads in {1, 2, 4}; hidden and intermediate multiples of 64;
-   vocab >= 1; batch 1; max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG): every
+   vocab >= 1; batch 1..16 for bf16 weights and 1..32 for affine 4-bit (batch 1
+   runs CUDA-core GEMV kernels, larger batches tensor-core kernels); max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG): every
    size positive, rms_eps > 0, rope_theta > 1, n_q_heads a multiple of n_kv_heads. */
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
@@ -215,6 +216,19 @@ DEC_API size_t dec_attention_workspace_bytes(const dec_config *cfg);
 DEC_API dec_status dec_attention(const dec_config *cfg, int layer, const float *qkv, const void *q_norm,
                                  const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
                                  void *workspace, size_t workspace_bytes, dec_stream_t stream);
+
+/* Test hooks for kernel-by-kernel parity.  dec_debug_step_prefix runs the first
+   n_launches kernels of one step (embedding = launch 1, then per layer QKV,
+   attention, O, gate/up, down, finally lm_head) as individual launches.
+   dec_debug_buffer copies a workspace buffer of the handle to device memory dst:
+   which 0: residual h float [batch][hidden]; 1: q,k,v projections float
+   [batch][(n_q + 2 n_kv) head_dim]; 2: attention output float [batch][n_q head_dim];
+   3: SwiGLU output float [batch][intermediate]; 4: residual sums of squares float
+   [batch][hidden / 8].  Both enqueue on `stream`. */
+DEC_API dec_status dec_debug_step_prefix(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
+                                         void *kv_cache, float *logits_out, int32_t *argmax_out,
+                                         dec_stream_t stream, int n_launches);
+DEC_API dec_status dec_debug_buffer(dec_handle *h, int which, void *dst, size_t bytes, dec_stream_t stream);
 
 /* dec_attention without a workspace: same arguments, same computation and same
    result as dec_attention, but it allocates nothing and takes no scratch from the

@@ -21,7 +21,7 @@ def glue():
     return torch_glue
 
 
-def _run(glue, wl, steps, check_steps=None, graph=True):
+def _run(glue, wl, steps, check_steps=None, graph=True, full_kv_check=True, cache_weights=True):
     model = synthetic.generate(wl, device="cuda")
     host = synthetic.to_host(model)
     kv_init = np_model({"kv": host["kv"]})["kv"]
@@ -33,15 +33,31 @@ def _run(glue, wl, steps, check_steps=None, graph=True):
         assert bits == 0, f"device status bits {bits}"
     finally:
         dec.close()
-    res, kv_ref = oracle_replay(wl, host, kv_init, gpu_steps, check_steps)
+    res, kv_ref = oracle_replay(wl, host, kv_init, gpu_steps, check_steps, cache_weights=cache_weights)
     worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0}
     for s, lg, am in res:
         w = check_logits(gpu_steps[s][2], lg, gpu_steps[s][3], am, f"{wl.name} step {s}")
         worst = {k: max(worst[k], w[k]) if k != "exempt" else worst[k] + w[k] for k in worst}
     if check_steps is None:
-        kv_gpu = np_model({"kv": kv.cpu()})["kv"]
-        kv_appended_close(kv_gpu, kv_ref, kv_init)
+        if full_kv_check:
+            kv_gpu = np_model({"kv": kv.cpu()})["kv"]
+            kv_appended_close(kv_gpu, kv_ref, kv_init)
+        else:  # only the slots the steps appended (the full cache is tens of GB)
+            for _, pin, _, _ in gpu_steps:
+                for b, P in enumerate(pin):
+                    g = np_model({"kv": kv[:, :, b, :, int(P)].cpu()})["kv"]
+                    appended_vectors_close(g, kv_ref[:, :, b, :, int(P)], f"{wl.name} seq {b} slot {P}")
     return worst
+
+
+def appended_vectors_close(gpu_bits, ref_bits, where):
+    """Appended K/V vectors (last axis head_dim): max |gpu - ref| <= 2 * 2^-8 * max |ref|."""
+    from oracle import numerics
+    g = numerics.bf16_bits_to_f64(gpu_bits)
+    r = numerics.bf16_bits_to_f64(ref_bits)
+    err = np.max(np.abs(g - r), axis=-1)
+    scale = np.max(np.abs(r), axis=-1)
+    assert np.all(err <= 2 * 2.0 ** -8 * scale), f"{where}: appended K/V off by {float(np.max(err / scale)):.3g}"
 
 
 def test_tiny_all_steps(glue):
@@ -66,6 +82,30 @@ CUSTOM = [
 ]
 
 
+CUSTOM_BATCHED = [
+    ("b3_bf16_ragged", dict(batch=3, prefill=(0, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=256,
+                            intermediate=512, vocab=1000, steps=3, n_layers=2)),
+    ("b12_bf16", dict(batch=12, prefill=(10, 200), head_dim=64, n_q_heads=8, n_kv_heads=2, hidden=192,
+                      intermediate=384, vocab=517, steps=2, n_layers=2)),
+    ("b5_q4", dict(batch=5, weight_format=synthetic.AFFINE4_G64, prefill=(1, 700), head_dim=128, n_q_heads=8,
+                   n_kv_heads=2, hidden=256, intermediate=640, vocab=999, steps=3, n_layers=2)),
+    ("b20_q4", dict(batch=20, weight_format=synthetic.AFFINE4_G64, prefill=(0, 1500), head_dim=64, n_q_heads=4,
+                    n_kv_heads=1, hidden=320, intermediate=768, vocab=2000, steps=2, n_layers=2)),
+    ("b32_q4_long_k", dict(batch=32, weight_format=synthetic.AFFINE4_G64, prefill=(100, 400), head_dim=128,
+                           n_q_heads=4, n_kv_heads=1, hidden=2560, intermediate=4096, vocab=333, steps=2,
+                           n_layers=1)),
+    ("b8_bf16_long_k", dict(batch=8, prefill=(50, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=4096,
+                            intermediate=6144, vocab=700, steps=2, n_layers=1)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CUSTOM_BATCHED, ids=[c[0] for c in CUSTOM_BATCHED])
+def test_custom_batched(glue, name, kw):
+    wl = synthetic.custom(name=name, seed=sum(map(ord, name)), **kw)
+    w = _run(glue, wl, wl.steps)
+    print(name, w)
+
+
 @pytest.mark.parametrize("name,kw", CUSTOM, ids=[c[0] for c in CUSTOM])
 def test_custom_shapes(glue, name, kw):
     wl = synthetic.custom(name=name, seed=hash(name) % 1000, **kw)
@@ -73,8 +113,9 @@ def test_custom_shapes(glue, name, kw):
     print(name, w)
 
 
-def test_graph_equals_eager_bitwise(glue):
-    wl = synthetic.WORKLOADS["tiny"]
+@pytest.mark.parametrize("batch", [1, 4])
+def test_graph_equals_eager_bitwise(glue, batch):
+    wl = synthetic.WORKLOADS["tiny"].replace(batch=batch)
     outs = []
     for graph in (True, False):
         model = synthetic.generate(wl, device="cuda")
@@ -105,11 +146,12 @@ def test_repeated_step_is_deterministic(glue):
     assert torch.equal(res[0], res[1]) and torch.equal(res[0], res[2])
 
 
+@pytest.mark.parametrize("batch", [1, 6])
 @pytest.mark.parametrize("fmt", [synthetic.BF16, synthetic.AFFINE4_G64])
-def test_debug_dequant_bit_exact(glue, fmt):
+def test_debug_dequant_bit_exact(glue, fmt, batch):
     from oracle import affine4, numerics
     wl = synthetic.custom(name="dq", weight_format=fmt, head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=192,
-                          intermediate=320, vocab=200, n_layers=2)
+                          intermediate=320, vocab=200, n_layers=2, batch=batch)
     model = synthetic.generate(wl, device="cuda", with_kv=False)
     host = np_model(synthetic.to_host(model))
     dec = glue.Decoder(wl, model)
@@ -160,3 +202,12 @@ def test_qwen3_0_6b_first_steps(glue):
     wl = synthetic.WORKLOADS["qwen3-0.6b"]
     w = _run(glue, wl, 6)
     print("qwen3-0.6b worst", w)
+
+
+@pytest.mark.parametrize("name", ["qwen3-4b-q4", "qwen3-8b-b1", "qwen3-8b-b8", "qwen3-8b-q4-b32"])
+def test_full_size_first_steps(glue, name):
+    """Full-size configs in the launch configuration the bench times (CUDA graph,
+    same batch and cache): the first two greedy steps against the oracle."""
+    wl = synthetic.WORKLOADS[name]
+    w = _run(glue, wl, 2, full_kv_check=False, cache_weights=False)
+    print(name, "worst", w)

@@ -52,9 +52,10 @@ void set_last_error(const char* fmt, ...) {
 namespace {
 
 struct PackedLinear {
-  void* w = nullptr;       // bf16 [N][K] or uint32 [N][K/8]
-  uint32_t* sb = nullptr;  // q4 only: [N][K/64]
+  void* w = nullptr;       // batch 1: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
+  uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
+  int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
 };
 
 struct PackedLayer {
@@ -117,6 +118,8 @@ struct dec_handle {
   StepPtrs captured{};
   // profiling events
   std::vector<cudaEvent_t> events;
+  // debug: stop an eager step after this many launches (-1: no limit)
+  int launch_limit = -1;
 };
 
 namespace {
@@ -124,6 +127,12 @@ namespace {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 double wbytes_per_elem(int fmt) { return fmt == DEC_W_BF16 ? 2.0 : 0.5 + 4.0 / kGroup; }
+
+size_t linear_bytes_tc(int fmt, int N, int K) {
+  const size_t npad = (static_cast<size_t>(N) + 15) / 16 * 16;
+  if (fmt == DEC_W_BF16) return align_up(npad * K * 2, 256);
+  return align_up(npad / 16 * (K / kGroup) * 576, 256);
+}
 
 size_t linear_bytes(int fmt, int N, int K) {
   if (fmt == DEC_W_BF16) return align_up(static_cast<size_t>(N) * K * 2, 256);
@@ -167,8 +176,9 @@ dec_status validate(const dec_config* c) {
     set_err("hidden and intermediate must be multiples of 64");
     return DEC_ERR_UNSUPPORTED;
   }
-  if (c->batch != 1) {
-    set_err("batch %d: only batch 1 is implemented", c->batch);
+  if (c->batch > 1 && gemm_tc_ny(c->linear_fmt == DEC_W_BF16 ? kWBf16 : kWQ4, c->batch) == 0) {
+    set_err("batch %d: the batched path takes at most %d sequences for this weight format", c->batch,
+            c->linear_fmt == DEC_W_BF16 ? 16 : 32);
     return DEC_ERR_UNSUPPORTED;
   }
   if (static_cast<long long>(c->max_ctx) * c->n_kv_heads * c->batch * c->head_dim > (1ll << 40)) {
@@ -203,6 +213,27 @@ int choose_splits(int N, int K, int fmt, int num_sms) {
     S = S2;
   }
   return S;
+}
+
+// Batched path: inputs staged per chunk (shared-memory bound) and K splits so that the
+// grid covers the SMs at least twice.
+int tc_chunk_max(int, int ny) { return ny == 1 ? 2048 : ny == 2 ? 1024 : 512; }
+
+void choose_tc_splits(PackedLinear& L, int wfmt, int ny, int num_sms) {
+  const int rpb = gemm_tc_rows_per_block(wfmt, ny);
+  const int blocks = (L.Npad + rpb - 1) / rpb;
+  const int kc_max = tc_chunk_max(wfmt, ny);
+  int S = 1;
+  while (static_cast<long long>(blocks) * S < 2ll * num_sms) {
+    const int S2 = S * 2;
+    if (L.K % S2 != 0 || (L.K / S2) % kGroup != 0 || L.K / S2 < 256) break;
+    S = S2;
+  }
+  L.S = S;
+  const int KS = L.K / S;
+  int kc = KS;
+  for (int div = 1; kc > kc_max || KS % kc != 0 || kc % kGroup != 0; ++div) kc = KS / div;
+  L.KC = kc;
 }
 
 }  // namespace
@@ -260,8 +291,13 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ev_end();
   lc.pdl = pdl;
 
+  int launched = 1;  // the embedding kernel
+  auto limit_hit = [&]() { return h->launch_limit >= 0 && launched >= h->launch_limit; };
+  if (limit_hit()) return DEC_OK;
   auto gemv = [&](const PackedLinear& L, int in_mode, int epi, const float* x, const __nv_bfloat16* norm_w,
                   float* out, int cls, const char* what) -> dec_status {
+    if (limit_hit()) return DEC_OK;
+    ++launched;
     GemvParams gp{};
     gp.w = L.w;
     gp.sb = L.sb;
@@ -282,7 +318,32 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     gp.argmax_out = sp.argmax;
     note(cls);
     ev_begin();
-    dec_status s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
+    dec_status s2;
+    if (c.batch == 1) {
+      s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
+    } else {
+      GemmParams tp{};
+      tp.w = L.w;
+      tp.N = L.N;
+      tp.Npad = L.Npad;
+      tp.K = L.K;
+      tp.S = L.S;
+      tp.KS = L.K / L.S;
+      tp.KC = L.KC;
+      tp.B = c.batch;
+      tp.x = x;
+      tp.norm_w = norm_w;
+      tp.sumsq_in = h->sumsq;
+      tp.n_sumsq_in = H / kResGroup;
+      tp.eps = c.rms_eps;
+      tp.out = out;
+      tp.sumsq_out = h->sumsq;
+      tp.partials = h->gemv_partials;
+      tp.counters = h->gemv_counters;
+      tp.amax_key = h->amax_key;
+      tp.argmax_out = sp.argmax;
+      s2 = check(launch_gemm_tc(lc, tp, h->wfmt, in_mode, epi), what);
+    }
     ev_end();
     return s2;
   };
@@ -310,6 +371,8 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.counters = h->attn_counters;
     ap.out = h->attn_o;
     ap.status = h->status;
+    if (limit_hit()) return DEC_OK;
+    ++launched;
     note(DEC_K_ATTN);
     ev_begin();
     if ((st = check(launch_attention(lc, ap, d), "attention")) != DEC_OK) return st;
@@ -428,11 +491,13 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
+  const bool tc = c.batch > 1;
+  const int ny = tc ? gemm_tc_ny(h->wfmt, c.batch) : 0;
+  auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
-                 linear_bytes(fmt, V, H);
+                 lbytes(V, H);
   const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +
-                           linear_bytes(fmt, nqkv, H) + linear_bytes(fmt, H, nq * d) + linear_bytes(fmt, 2 * I, H) +
-                           linear_bytes(fmt, H, I);
+                           lbytes(nqkv, H) + lbytes(H, nq * d) + lbytes(2 * I, H) + lbytes(H, I);
   total += per_layer * c.n_layers;
   if ((e = cudaMalloc(&h->wmem, total)) != cudaSuccess) {
     set_err("cudaMalloc of %zu bytes of packed weights failed: %s", total, cudaGetErrorString(e));
@@ -450,6 +515,12 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     PackedLinear L;
     L.N = N;
     L.K = K;
+    if (tc) {
+      L.Npad = (N + 15) / 16 * 16;
+      choose_tc_splits(L, h->wfmt, ny, h->num_sms);
+      L.w = take(linear_bytes_tc(fmt, N, K));
+      return L;
+    }
     L.S = choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
       L.w = take(static_cast<size_t>(N) * K * 2);
@@ -480,6 +551,19 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   auto cp = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto pack_lin = [&](const PackedLinear& P, size_t row_off, const dec_linear& a, const dec_linear* b, int rows,
                       int K, int ib) -> cudaError_t {
+    if (tc) {
+      const int npad = (rows + 15) / 16 * 16;
+      if (fmt == DEC_W_BF16)
+        return pack_frag_bf16(s, static_cast<uint32_t*>(P.w), static_cast<const __nv_bfloat16*>(a.w),
+                              b ? static_cast<const __nv_bfloat16*>(b->w) : nullptr, rows, npad, K, ib,
+                              static_cast<int>(row_off), npad);
+      return pack_frag_q4(s, static_cast<unsigned char*>(P.w), static_cast<const uint32_t*>(a.w),
+                          static_cast<const __nv_bfloat16*>(a.scales), static_cast<const __nv_bfloat16*>(a.biases),
+                          b ? static_cast<const uint32_t*>(b->w) : nullptr,
+                          b ? static_cast<const __nv_bfloat16*>(b->scales) : nullptr,
+                          b ? static_cast<const __nv_bfloat16*>(b->biases) : nullptr, rows, K, ib,
+                          static_cast<int>(row_off), npad);
+    }
     if (fmt == DEC_W_BF16) {
       return pack_rows_bf16(s, static_cast<__nv_bfloat16*>(P.w) + row_off * K, static_cast<const __nv_bfloat16*>(a.w),
                             b ? static_cast<const __nv_bfloat16*>(b->w) : nullptr, rows, K, ib);
@@ -506,7 +590,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = pack_lin(L.qkv, static_cast<size_t>(nq + nkv) * d, lw.v, nullptr, nkv * d, H, 0)) != cudaSuccess)
       return fail("pack v", e);
     if ((e = pack_lin(L.o, 0, lw.o, nullptr, H, nq * d, 0)) != cudaSuccess) return fail("pack o", e);
-    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, kGemvRows / 2)) != cudaSuccess)
+    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, tc ? 8 : kGemvRows / 2)) != cudaSuccess)
       return fail("pack gate/up", e);
     if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
   }
@@ -520,10 +604,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   int max_tiles = 0;
   size_t max_partials = 0;
   auto acc_lin = [&](const PackedLinear& L) {
-    const int tiles = (L.N + kGemvRows - 1) / kGemvRows;
+    const int tiles = (L.N + kGemvRows - 1) / kGemvRows;  // >= row blocks of the batched path too
     max_tiles = tiles > max_tiles ? tiles : max_tiles;
     if (L.S > 1) {
-      const size_t pp = static_cast<size_t>(L.S) * L.N * B;
+      const size_t pp = tc ? static_cast<size_t>(L.S) * (L.Npad / 16) * 32 * ny * 4 : static_cast<size_t>(L.S) * L.N * B;
       max_partials = pp > max_partials ? pp : max_partials;
     }
   };
@@ -580,6 +664,14 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail("upload inv_freq", e);
   if ((e = prepare_attention(d, G)) != cudaSuccess) return fail("attention kernel attributes", e);
+  if (tc) {
+    GemmParams gp{};
+    gp.B = c.batch;
+    gp.KC = tc_chunk_max(h->wfmt, ny);
+    const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
+    for (auto& cb : combos)
+      if ((e = prepare_gemm_tc(gp, h->wfmt, cb[0], cb[1])) != cudaSuccess) return fail("batched kernel attributes", e);
+  }
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail("packing", e);
   return h;
 }
@@ -662,12 +754,16 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       case 1: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = c.n_q_heads * d; break;
       case 2: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = (c.n_q_heads + c.n_kv_heads) * d; break;
       case 3: P = &L.o; rows = H; K = c.n_q_heads * d; break;
-      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = kGemvRows / 2; half = 0; break;
-      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = kGemvRows / 2; half = 1; break;
+      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = c.batch > 1 ? 8 : kGemvRows / 2; half = 0; break;
+      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = c.batch > 1 ? 8 : kGemvRows / 2; half = 1; break;
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
+  if (c.batch > 1) {
+    DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
+  } else {
+    DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
+  }
   return DEC_OK;
 }
 
@@ -830,5 +926,50 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
   ap.out = out;
   ap.status = nullptr;
   DEC_CUDA(launch_attention(LaunchCtx{cs, false}, ap, cfg->head_dim));
+  return DEC_OK;
+}
+
+// ---------------------------------------------------------------- debug hooks
+
+extern "C" dec_status dec_debug_step_prefix(dec_handle* h, const int32_t* token_ids, const int32_t* positions,
+                                            void* kv_cache, float* logits_out, int32_t* argmax_out,
+                                            dec_stream_t stream, int n_launches) {
+  const StepPtrs sp{token_ids, positions, kv_cache, logits_out, argmax_out};
+  dec_status st = check_step_args(h, sp);
+  if (st != DEC_OK) return st;
+  if (n_launches < 1) {
+    set_err("dec_debug_step_prefix: n_launches must be >= 1");
+    return DEC_ERR_INVALID_ARG;
+  }
+  h->launch_limit = n_launches;
+  st = enqueue_step(h, sp, reinterpret_cast<cudaStream_t>(stream), false, nullptr);
+  h->launch_limit = -1;
+  return st;
+}
+
+extern "C" dec_status dec_debug_buffer(dec_handle* h, int which, void* dst, size_t bytes, dec_stream_t stream) {
+  if (!h || !dst) {
+    set_err("dec_debug_buffer: NULL argument");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const dec_config& c = h->cfg;
+  const size_t B = c.batch;
+  const void* src = nullptr;
+  size_t n = 0;
+  switch (which) {
+    case 0: src = h->h; n = B * c.hidden * 4; break;
+    case 1: src = h->qkv; n = B * (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim * 4; break;
+    case 2: src = h->attn_o; n = B * c.n_q_heads * c.head_dim * 4; break;
+    case 3: src = h->g; n = B * c.intermediate * 4; break;
+    case 4: src = h->sumsq; n = B * (c.hidden / kResGroup) * 4; break;
+    default:
+      set_err("dec_debug_buffer: unknown buffer %d", which);
+      return DEC_ERR_INVALID_ARG;
+  }
+  if (bytes < n) {
+    set_err("dec_debug_buffer: %zu bytes needed", n);
+    return DEC_ERR_INVALID_ARG;
+  }
+  DEC_CUDA(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
   return DEC_OK;
 }

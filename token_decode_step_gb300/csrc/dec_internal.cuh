@@ -46,6 +46,24 @@ struct GemvParams {
   int32_t* argmax_out;      // lmhead
 };
 
+// Batched (B >= 2) projection on tensor cores over fragment-packed weight tiles.
+struct GemmParams {
+  const void* w;            // packed tiles (see k_gemm_tc.cu)
+  int N, Npad, K, S, KS, KC, B;  // rows, rows padded to 16, inputs, K splits, inputs per split,
+                                 // inputs staged at once (divides KS), tokens
+  const float* x;           // [B][K]
+  const __nv_bfloat16* norm_w;
+  const float* sumsq_in;    // [B][n_sumsq_in]
+  int n_sumsq_in;
+  float eps;
+  float* out;               // store: [B][N]; resid: h [B][N] (+=); swiglu: g [B][N/2]; lmhead: logits [B][N] or null
+  float* sumsq_out;         // resid: [B][N / kResGroup]
+  float* partials;          // [S][Npad/16][32][NY*4] when S > 1
+  unsigned* counters;       // [row blocks + 1], zero on entry, left zero
+  unsigned long long* amax_key;  // lmhead: [B]
+  int32_t* argmax_out;      // lmhead: [B]
+};
+
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
 struct AttnParams {
   const float* qkv;             // [B][(nq + 2 nkv) d] projections
@@ -179,6 +197,12 @@ struct LaunchCtx {
 cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B);
 cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int in_mode, int epi);
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim);
+// batched tensor-core projection
+int gemm_tc_ny(int wfmt, int batch);            // 8-token n-tiles per hi/lo half, 0 if unsupported
+int gemm_tc_rows_per_block(int wfmt, int ny);   // weight rows one CTA covers
+size_t gemm_tc_smem_bytes(int wfmt, int ny, int ks);
+cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi);
+cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
 size_t attention_smem_bytes(int head_dim);
 cudaError_t prepare_attention(int head_dim, int G);  // set the dynamic smem limit (before capture)
 void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len, int* max_splits);
@@ -197,6 +221,15 @@ cudaError_t pack_rows_q4(cudaStream_t s, uint32_t* dst_w, uint32_t* dst_sb, cons
                          int interleave_block);
 cudaError_t debug_dequant(cudaStream_t s, float* out, const void* w, const uint32_t* sb, int wfmt,
                           int rows_out, int K, int row_offset, int interleave_block, int which_half);
+// fragment-ordered packing for the batched path (rows padded with zeros to npad)
+cudaError_t pack_frag_bf16(cudaStream_t s, uint32_t* dst, const __nv_bfloat16* src_a, const __nv_bfloat16* src_b,
+                           int rows_out, int npad, int K, int interleave_block, int dst_row_offset, int dst_rows);
+cudaError_t pack_frag_q4(cudaStream_t s, unsigned char* dst, const uint32_t* w_a, const __nv_bfloat16* sc_a,
+                         const __nv_bfloat16* bi_a, const uint32_t* w_b, const __nv_bfloat16* sc_b,
+                         const __nv_bfloat16* bi_b, int rows_out, int K, int interleave_block, int dst_row_offset,
+                         int dst_rows);
+cudaError_t debug_dequant_frag(cudaStream_t s, float* out, const void* w, int wfmt, int rows_out, int K,
+                               int row_offset, int interleave_block, int which_half);
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch);
 

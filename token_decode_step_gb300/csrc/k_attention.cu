@@ -39,7 +39,7 @@ struct AttnSmem {
   static constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
   static constexpr int kOffNew = kOffV + 2 * kTileBytes; // new k row, new v row (bf16)
   static constexpr int kOffMisc = kOffNew + 2 * kRowBytes;
-  static constexpr int kMiscFloats = 1024 + 16;          // merge factors + per-head stats
+  static constexpr int kMiscFloats = 2048 + 16;          // merge factors and sums + per-head stats
   static constexpr int kBytes = kOffMisc + kMiscFloats * 4;
 };
 
@@ -354,24 +354,36 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   __threadfence();
 
   // ---- last CTA of (b, h): log-sum-exp merge of the nsplit partials in split order
-  float* fac = misc;  // [nsplit][G] scale factors (nsplit * G <= 1024)
-  float* tot = misc + 1024;  // [G] merged denominators
-  if (tid < G) {
+  float* fac = misc;          // [nsplit][G]: first M_s, then e^(M_s - M)
+  float* lsp = misc + 1024;   // [nsplit][G]: L_s
+  float* tot = misc + 2048;   // [G] merged denominators
+  for (int i = tid; i < nsplit * G; i += kAttnThreads) {
+    const int s = i / G, j = i % G;
+    const float* r = part + static_cast<size_t>(s) * rec + j * (D + 2);
+    fac[i] = __ldcg(r);
+    lsp[i] = __ldcg(r + 1);
+  }
+  __syncthreads();
+  if (warp < G) {  // warp j reduces head j over the splits
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(part + static_cast<size_t>(s) * rec + tid * (D + 2)));
+    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, fac[s * G + warp]);
+    M = warp_max(M);
     float L = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float f = exp2f(__ldcg(part + static_cast<size_t>(s) * rec + tid * (D + 2)) - M);
-      fac[s * G + tid] = f;
-      L += f * __ldcg(part + static_cast<size_t>(s) * rec + tid * (D + 2) + 1);
+    for (int s = lane; s < nsplit; s += 32) {
+      const float f = exp2f(fac[s * G + warp] - M);
+      fac[s * G + warp] = f;
+      L += f * lsp[s * G + warp];
     }
-    tot[tid] = L;
+    L = warp_sum(L);
+    if (lane == 0) tot[warp] = L;
   }
   __syncthreads();
   for (int i = tid; i < G * D; i += kAttnThreads) {
     const int j = i / D, e = i % D;
+    const float* src = part + j * (D + 2) + 2 + e;
     float a = 0.f;
-    for (int s = 0; s < nsplit; ++s) a += fac[s * G + j] * __ldcg(part + static_cast<size_t>(s) * rec + j * (D + 2) + 2 + e);
+#pragma unroll 8
+    for (int s = 0; s < nsplit; ++s) a = fmaf(fac[s * G + j], __ldcg(src + static_cast<size_t>(s) * rec), a);
     out_b[qoff + i] = a / tot[j];
   }
   if (tid == 0) p.counters[b * p.nkv + h] = 0u;
@@ -379,11 +391,12 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
 
 void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len,
                           int* max_splits) {
-  // Up to 16 CTAs per SM at the full context with splits of <= 512 positions,
-  // and at most 1024 / group splits so the merge factors fit in shared memory.
+  // Splits of 64 * 2^k positions: the shortest length that keeps the grid at the
+  // full context within two CTAs per SM, capped at 512 positions, and at most
+  // 1024 / group splits so the merge factors fit in shared memory.
   int L = kAttnTile;
   auto ns = [&](int len) { return (max_ctx + len - 1) / len; };
-  while (L < 512 && (static_cast<long long>(batch) * n_kv * ns(L) > 16ll * num_sms || ns(L) * group > 1024)) L *= 2;
+  while (L < 512 && (static_cast<long long>(batch) * n_kv * ns(L) > 2ll * num_sms || ns(L) * group > 1024)) L *= 2;
   while (ns(L) * group > 1024) L *= 2;
   *split_len = L;
   *max_splits = ns(L);

@@ -186,6 +186,138 @@ cudaError_t debug_dequant(cudaStream_t s, float* out, const void* w, const uint3
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------- fragment packing (batched path)
+// bf16: tile (16 rows x 16 inputs) = 32 lanes x 4 registers; lane (g, t) register r holds
+// rows g + 8 (r & 1), inputs 2t + 8 (r >> 1) and the next input, first in the low half.
+__global__ void k_pack_frag_bf16(uint32_t* dst, const __nv_bfloat16* a, const __nv_bfloat16* b, int rows_out,
+                                 int npad, int K, int ib, int row_off) {
+  const int kt_n = K / 16;
+  const size_t total = static_cast<size_t>(npad / 16) * kt_n * 128;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int reg = static_cast<int>(idx & 3), lane = static_cast<int>((idx >> 2) & 31);
+    const size_t tile = idx >> 7;
+    const int kt = static_cast<int>(tile % kt_n), rtl = static_cast<int>(tile / kt_n);
+    const int g = lane >> 2, t = lane & 3;
+    const int row = 16 * rtl + g + 8 * (reg & 1), col = 16 * kt + 2 * t + 8 * (reg >> 1);
+    uint32_t v = 0;
+    if (row < rows_out) {
+      int which, r;
+      packed_source(row, ib, which, r);
+      const __nv_bfloat16* src = (which ? b : a) + static_cast<size_t>(r) * K + col;
+      v = static_cast<uint32_t>(__bfloat16_as_ushort(src[0])) |
+          (static_cast<uint32_t>(__bfloat16_as_ushort(src[1])) << 16);
+    }
+    dst[((static_cast<size_t>(row_off / 16 + rtl) * kt_n + kt) * 32 + lane) * 4 + reg] = v;
+  }
+}
+
+cudaError_t pack_frag_bf16(cudaStream_t s, uint32_t* dst, const __nv_bfloat16* src_a, const __nv_bfloat16* src_b,
+                           int rows_out, int npad, int K, int interleave_block, int dst_row_offset, int) {
+  k_pack_frag_bf16<<<1024, 256, 0, s>>>(dst, src_a, src_b, rows_out, npad, K, interleave_block, dst_row_offset);
+  return cudaGetLastError();
+}
+
+// 4-bit: tile (16 rows x 64 inputs) = 512 bytes of codes + 64 bytes of (scale, bias).
+// Lane (g, t), k-step j: one word whose bits 4i..4i+3 and 16+4i..16+4i+3 hold A register i:
+// i = 0: row g, inputs c, c+1; i = 1: row g+8, inputs c, c+1; i = 2: row g, inputs c+8, c+9;
+// i = 3: row g+8, inputs c+8, c+9 (c = 16 j + 2 t within the group).  Then for each g the
+// bf16 scale and bias of row g followed by those of row g+8.
+__global__ void k_pack_frag_q4(unsigned char* dst, const uint32_t* wa, const __nv_bfloat16* sa,
+                               const __nv_bfloat16* ba, const uint32_t* wb, const __nv_bfloat16* sbb,
+                               const __nv_bfloat16* bb, int rows_out, int npad, int K, int ib, int row_off) {
+  const int gk_n = K / kGroup;
+  const size_t total = static_cast<size_t>(npad / 16) * gk_n * 32;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int lane = static_cast<int>(idx & 31);
+    const size_t tile = idx >> 5;
+    const int gk = static_cast<int>(tile % gk_n), rtl = static_cast<int>(tile / gk_n);
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = 16 * rtl + g, r1 = r0 + 8;
+    auto code = [&](int row, int col) -> uint32_t {
+      if (row >= rows_out) return 0u;
+      int which, r;
+      packed_source(row, ib, which, r);
+      const uint32_t w = (which ? wb : wa)[static_cast<size_t>(r) * (K / 8) + col / 8];
+      return (w >> (4 * (col % 8))) & 0xfu;
+    };
+    unsigned char* tp = dst + (static_cast<size_t>(row_off / 16 + rtl) * gk_n + gk) * 576;
+    for (int j = 0; j < 4; ++j) {
+      const int c = gk * kGroup + 16 * j + 2 * t;
+      const uint32_t word = code(r0, c) | (code(r0, c + 1) << 16) | (code(r1, c) << 4) | (code(r1, c + 1) << 20) |
+                            (code(r0, c + 8) << 8) | (code(r0, c + 9) << 24) | (code(r1, c + 8) << 12) |
+                            (code(r1, c + 9) << 28);
+      reinterpret_cast<uint32_t*>(tp + lane * 16)[j] = word;
+    }
+    if (t == 0) {
+      auto sbpair = [&](int row) -> uint32_t {
+        if (row >= rows_out) return 0u;
+        int which, r;
+        packed_source(row, ib, which, r);
+        const size_t o = static_cast<size_t>(r) * gk_n + gk;
+        return static_cast<uint32_t>(__bfloat16_as_ushort((which ? sbb : sa)[o])) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort((which ? bb : ba)[o])) << 16);
+      };
+      uint2 v;
+      v.x = sbpair(r0);
+      v.y = sbpair(r1);
+      *reinterpret_cast<uint2*>(tp + 512 + g * 8) = v;
+    }
+  }
+}
+
+cudaError_t pack_frag_q4(cudaStream_t s, unsigned char* dst, const uint32_t* w_a, const __nv_bfloat16* sc_a,
+                         const __nv_bfloat16* bi_a, const uint32_t* w_b, const __nv_bfloat16* sc_b,
+                         const __nv_bfloat16* bi_b, int rows_out, int K, int interleave_block, int dst_row_offset,
+                         int npad) {
+  k_pack_frag_q4<<<1024, 256, 0, s>>>(dst, w_a, sc_a, bi_a, w_b, sc_b, bi_b, rows_out, npad, K, interleave_block,
+                                      dst_row_offset);
+  return cudaGetLastError();
+}
+
+// dequant test hook for the fragment layouts: canonical row r, input k
+__global__ void k_debug_dequant_frag(float* out, const void* w, int wfmt, int rows_out, int K, int row_offset, int ib,
+                                     int which_half) {
+  const int r = blockIdx.x;
+  if (r >= rows_out) return;
+  int p;
+  if (which_half < 0) {
+    p = row_offset + r;
+  } else {
+    const int block = r / ib, within = r % ib;
+    p = row_offset + block * 2 * ib + which_half * ib + within;
+  }
+  const int rt = p / 16, gg = (p % 16) % 8, hi = (p % 16) / 8;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    float v;
+    if (wfmt == kWBf16) {
+      const int kt = k / 16, kk = k % 16;
+      const int lane = 4 * gg + (kk % 8) / 2, reg = hi + 2 * (kk / 8);
+      const uint32_t u =
+          static_cast<const uint32_t*>(w)[((static_cast<size_t>(rt) * (K / 16) + kt) * 32 + lane) * 4 + reg];
+      v = (kk & 1) ? bf16_hi(u) : bf16_lo(u);
+    } else {
+      const int gk = k / kGroup, kq = k % kGroup, j = kq / 16, kk = kq % 16;
+      const int lane = 4 * gg + (kk % 8) / 2;
+      const unsigned char* tp = static_cast<const unsigned char*>(w) + (static_cast<size_t>(rt) * (K / kGroup) + gk) * 576;
+      const uint32_t word = reinterpret_cast<const uint32_t*>(tp + lane * 16)[j];
+      const uint32_t q2 = q4_pair_bf16(word, 4 * (hi + 2 * (kk / 8)));
+      const float q = (kk & 1) ? bf16_hi(q2) : bf16_lo(q2);
+      const uint2 sbv = *reinterpret_cast<const uint2*>(tp + 512 + gg * 8);
+      const uint32_t sbw = hi ? sbv.y : sbv.x;
+      v = fmaf(sb_scale(sbw), q, sb_bias(sbw));
+    }
+    out[static_cast<size_t>(r) * K + k] = v;
+  }
+}
+
+cudaError_t debug_dequant_frag(cudaStream_t s, float* out, const void* w, int wfmt, int rows_out, int K,
+                               int row_offset, int interleave_block, int which_half) {
+  k_debug_dequant_frag<<<rows_out, 256, 0, s>>>(out, w, wfmt, rows_out, K, row_offset, interleave_block, which_half);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- greedy feedback
 __global__ void k_advance(const int32_t* argmax, int32_t* tokens, int32_t* positions, int batch) {
   int b = blockIdx.x * blockDim.x + threadIdx.x;

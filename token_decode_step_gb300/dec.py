@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
                                             ctypes.c_int]),
         "dec_kernel_bytes": (ctypes.c_double, [vp, ctypes.c_int, ctypes.c_double]),
         "dec_launches_per_step": (ctypes.c_int, [vp]),
+        "dec_debug_step_prefix": (ctypes.c_int, [vp, i32p, i32p, vp, vp, i32p, vp, ctypes.c_int]),
+        "dec_debug_buffer": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_size_t, vp]),
         "dec_attention_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecConfig)]),
         "dec_attention": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
                                          ctypes.c_size_t, vp]),
@@ -182,3 +184,13 @@ def dec_attention_noalloc(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_n
                           kv_cache: int, out: int, stream: int = 0) -> int:
     return _check(lib.dec_attention_noalloc(ctypes.byref(cfg), layer, qkv, q_norm, k_norm, positions, kv_cache,
                                             out, stream), "dec_attention_noalloc")
+
+
+def dec_debug_step_prefix(h: int, token_ids: int, positions: int, kv_cache: int, logits_out: int | None,
+                          argmax_out: int, stream: int, n_launches: int) -> int:
+    return _check(lib.dec_debug_step_prefix(h, token_ids, positions, kv_cache, logits_out, argmax_out, stream,
+                                            n_launches), "dec_debug_step_prefix")
+
+
+def dec_debug_buffer(h: int, which: int, dst: int, nbytes: int, stream: int = 0) -> int:
+    return _check(lib.dec_debug_buffer(h, which, dst, nbytes, stream), "dec_debug_buffer")
