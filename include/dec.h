@@ -208,7 +208,7 @@ DEC_API int dec_launches_per_step(const dec_handle *h);
      positions  device int32 [batch], as in dec_step (clamped if out of range).
      kv_cache   as in dec_step; only slot positions[b] of `layer` is written.
      out        device float [batch][n_q * head_dim]: attention output per query head.
-     workspace  caller-owned device scratch of at least
+     workspace  caller-owned device scratch (the RoPE table) of at least
                 dec_attention_workspace_bytes(cfg) bytes, 256-byte aligned; its
                 contents on entry do not matter; one call at a time per workspace.
    Enqueued on `stream`. */
@@ -238,20 +238,19 @@ DEC_API dec_status dec_debug_buffer(dec_handle *h, int which, void *dst, size_t 
    allowed), plug-in or real-time hosts that hand over only input and output
    buffers and forbid device allocations (cudaMalloc can synchronise the device and
    can fail under memory pressure), or hosts whose allocator owns all free memory.
-   Its scratch (merge counters, RoPE table, split partials) is one fixed array of
-   16 MiB inside this library; every GPU that loads the library holds that array
-   until the process exits.  Shapes whose scratch exceeds it are rejected with
-   DEC_ERR_UNSUPPORTED and a message (for example batch 32, 8 KV heads, head_dim
-   128, 4 query heads per KV head and max_ctx 8224 need about 9.1 MB).
+   Its scratch -- the RoPE (cos, sin) table that its first kernel writes and the
+   attention kernel reads -- is one fixed array of 1 MiB inside this library;
+   every GPU that loads the library holds that array until the process exits.
+   Batches whose table exceeds it (more than 2048 sequences at head_dim 128, 4096
+   at head_dim 64) are rejected with DEC_ERR_UNSUPPORTED and a message.
      - The first call on each device does a one-time set-up (it looks up the
        array's device address and sets the kernels' shared-memory limit) with that
        device current; make that first call before any stream capture.
-     - Every call shares the one array and it keeps the last call's contents: the
-       merge counters are cleared at the start of every call, the rest is fully
-       rewritten.  Calls whose work overlaps on the GPU (other streams, other host
-       threads) race on the array; serialise them.
-   Enqueued on `stream` (a memset of the counters, a RoPE-table kernel, the
-   attention kernel). */
+     - Every call shares the one array and it keeps the last call's contents;
+       each call rewrites the whole table before reading it, so nothing has to
+       start at zero.  Calls whose work overlaps on the GPU (other streams, other
+       host threads) race on the array; serialise them.
+   Enqueued on `stream` (a RoPE-table kernel, then the attention kernel). */
 DEC_API dec_status dec_attention_noalloc(const dec_config *cfg, int layer, const float *qkv, const void *q_norm,
                                          const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
                                          dec_stream_t stream);

@@ -54,7 +54,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dec):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(dec):
-    cfg = attention_cfg(dec, 64, 32, 8, 128, 65536)
+    cfg = attention_cfg(dec, 4096, 32, 8, 128, 64)  # RoPE table of 4096 sequences > 1 MiB
     x = torch.zeros((16,), device="cuda")
     with pytest.raises(dec.DecError) as ei:
         dec.dec_attention_noalloc(cfg, 0, x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(),

@@ -102,13 +102,10 @@ struct dec_handle {
   float* sumsq = nullptr;
   float* gemv_partials = nullptr;
   unsigned* gemv_counters = nullptr;
-  float* attn_partials = nullptr;
-  unsigned* attn_counters = nullptr;
   float2* rope = nullptr;
   double* inv_freq = nullptr;
   unsigned long long* amax_key = nullptr;
   unsigned* status = nullptr;
-  int split_len = 64, max_splits = 1;
   // graph state
   bool graph_mode = true;
   cudaStream_t cap_stream = nullptr;
@@ -364,11 +361,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.nq = c.n_q_heads;
     ap.nkv = c.n_kv_heads;
     ap.max_ctx = c.max_ctx;
-    ap.split_len = h->split_len;
-    ap.max_splits = h->max_splits;
     ap.eps = c.rms_eps;
-    ap.partials = h->attn_partials;
-    ap.counters = h->attn_counters;
     ap.out = h->attn_o;
     ap.status = h->status;
     if (limit_hit()) return DEC_OK;
@@ -595,10 +588,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
   }
 
-  // ---- attention split length
   const int G = nq / nkv;
-  attention_split_plan(c.batch, nkv, G, c.max_ctx, h->num_sms, &h->split_len, &h->max_splits);
-
   // ---- workspace
   const int B = c.batch;
   int max_tiles = 0;
@@ -618,7 +608,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     acc_lin(L.gateup);
     acc_lin(L.down);
   }
-  const size_t n_attn_part = static_cast<size_t>(B) * nkv * h->max_splits * G * (d + 2);
   size_t ws_bytes = 0;
   auto plan = [&](size_t bytes) {
     size_t off = ws_bytes;
@@ -632,8 +621,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const size_t o_ss = plan(static_cast<size_t>(B) * (H / kResGroup) * 4);
   const size_t o_gp = plan((max_partials ? max_partials : 1) * 4);
   const size_t o_gc = plan(static_cast<size_t>(max_tiles + 1) * 4);
-  const size_t o_ap = plan(n_attn_part * 4);
-  const size_t o_ac = plan(static_cast<size_t>(B) * nkv * 4);
   const size_t o_rope = plan(static_cast<size_t>(B) * (d / 2) * 8);
   const size_t o_inv = plan(static_cast<size_t>(d / 2) * 8);
   const size_t o_key = plan(static_cast<size_t>(B) * 8);
@@ -651,8 +638,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   h->sumsq = reinterpret_cast<float*>(h->ws + o_ss);
   h->gemv_partials = reinterpret_cast<float*>(h->ws + o_gp);
   h->gemv_counters = reinterpret_cast<unsigned*>(h->ws + o_gc);
-  h->attn_partials = reinterpret_cast<float*>(h->ws + o_ap);
-  h->attn_counters = reinterpret_cast<unsigned*>(h->ws + o_ac);
   h->rope = reinterpret_cast<float2*>(h->ws + o_rope);
   h->inv_freq = reinterpret_cast<double*>(h->ws + o_inv);
   h->amax_key = reinterpret_cast<unsigned long long*>(h->ws + o_key);
@@ -852,33 +837,15 @@ dec_status validate_attention_cfg(const dec_config* c, int layer) {
   return DEC_OK;
 }
 
-struct AttnWorkspace {
-  size_t counters, rope, partials, total;
-};
-
-AttnWorkspace attention_workspace_layout(const dec_config* c, int num_sms, int* split_len, int* max_splits) {
-  const int G = c->n_q_heads / c->n_kv_heads;
-  attention_split_plan(c->batch, c->n_kv_heads, G, c->max_ctx, num_sms, split_len, max_splits);
-  AttnWorkspace w{};
-  w.counters = 0;
-  w.rope = align_up(static_cast<size_t>(c->batch) * c->n_kv_heads * 4, 256);
-  w.partials = w.rope + align_up(static_cast<size_t>(c->batch) * (c->head_dim / 2) * 8, 256);
-  w.total = w.partials +
-            align_up(attention_partials_floats(c->batch, c->n_kv_heads, G, c->head_dim, *max_splits) * 4, 256);
-  return w;
+size_t attention_workspace_total(const dec_config* c) {
+  return align_up(static_cast<size_t>(c->batch) * (c->head_dim / 2) * 8, 256);  // RoPE (cos, sin) table
 }
 
 }  // namespace
 
 extern "C" size_t dec_attention_workspace_bytes(const dec_config* cfg) {
   if (validate_attention_cfg(cfg, 0) != DEC_OK) return 0;
-  int dev = 0, sms = 0, sl, ms;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                cudaSuccess) {
-    set_err("cannot query the current CUDA device");
-    return 0;
-  }
-  return attention_workspace_layout(cfg, sms, &sl, &ms).total;
+  return attention_workspace_total(cfg);
 }
 
 extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const float* qkv, const void* q_norm,
@@ -891,20 +858,15 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
     set_err("dec_attention: NULL pointer, kv_cache not 16-byte aligned or workspace not 256-byte aligned");
     return DEC_ERR_INVALID_ARG;
   }
-  int dev = 0, sms = 0, split_len = 0, max_splits = 0;
-  DEC_CUDA(cudaGetDevice(&dev));
-  DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const AttnWorkspace w = attention_workspace_layout(cfg, sms, &split_len, &max_splits);
-  if (workspace_bytes < w.total) {
-    set_err("dec_attention: workspace of %zu bytes, %zu needed", workspace_bytes, w.total);
+  const size_t need = attention_workspace_total(cfg);
+  if (workspace_bytes < need) {
+    set_err("dec_attention: workspace of %zu bytes, %zu needed", workspace_bytes, need);
     return DEC_ERR_INVALID_ARG;
   }
   const int G = cfg->n_q_heads / cfg->n_kv_heads;
   DEC_CUDA(prepare_attention(cfg->head_dim, G));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  DEC_CUDA(cudaMemsetAsync(ws + w.counters, 0, static_cast<size_t>(cfg->batch) * cfg->n_kv_heads * 4, cs));
-  float2* rope = reinterpret_cast<float2*>(ws + w.rope);
+  float2* rope = static_cast<float2*>(workspace);
   DEC_CUDA(launch_rope_table(cs, positions, cfg->batch, cfg->head_dim, cfg->max_ctx, cfg->rope_theta, rope, nullptr));
   AttnParams ap{};
   ap.qkv = qkv;
@@ -918,11 +880,7 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
   ap.nq = cfg->n_q_heads;
   ap.nkv = cfg->n_kv_heads;
   ap.max_ctx = cfg->max_ctx;
-  ap.split_len = split_len;
-  ap.max_splits = max_splits;
   ap.eps = cfg->rms_eps;
-  ap.partials = reinterpret_cast<float*>(ws + w.partials);
-  ap.counters = reinterpret_cast<unsigned*>(ws + w.counters);
   ap.out = out;
   ap.status = nullptr;
   DEC_CUDA(launch_attention(LaunchCtx{cs, false}, ap, cfg->head_dim));

@@ -16,6 +16,7 @@ constexpr int kResGroup = 8;        // rows per partial sum-of-squares of the re
 constexpr int kGemvRows = 8;        // rows per CTA of the batch-1 GEMV
 constexpr int kAttnTile = 64;       // positions per attention smem tile
 constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
+constexpr int kAttnCluster = 8;     // CTAs per (sequence, KV head): one thread-block cluster
 constexpr int kGroup = 64;          // affine 4-bit group size
 
 enum StatusBits : unsigned { kStatusBadToken = 1u, kStatusBadPos = 2u, kStatusTimeout = 4u };
@@ -73,11 +74,7 @@ struct AttnParams {
   const int32_t* positions;     // [B]
   __nv_bfloat16* kv;            // whole cache
   int layer, B, nq, nkv, max_ctx;
-  int split_len;                // positions per split (multiple of kAttnTile)
-  int max_splits;
   float eps;
-  float* partials;              // [B][nkv][max_splits][G][d + 2]
-  unsigned* counters;           // [B][nkv]
   float* out;                   // [B][nq d]
   unsigned* status;
 };
@@ -205,8 +202,6 @@ cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, in
 cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
 size_t attention_smem_bytes(int head_dim);
 cudaError_t prepare_attention(int head_dim, int G);  // set the dynamic smem limit (before capture)
-void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len, int* max_splits);
-size_t attention_partials_floats(int batch, int n_kv, int group, int head_dim, int max_splits);
 // (cos, sin) of pos * theta^(-2i/d) for every sequence, angles and inverse
 // frequencies in double on the device; out-of-range positions are clamped and flagged.
 cudaError_t launch_rope_table(cudaStream_t s, const int32_t* positions, int batch, int head_dim, int max_ctx,

@@ -10,17 +10,19 @@
 // TOKEN DECODE" (rope at offset = cache.length, cache.append writes into the
 // preallocated buffer, sdpa_decode over the cache).
 //
-// Grid: (max_splits, n_kv, B).  A CTA takes split s of sequence b, KV head h:
-// positions [s*L, min((s+1)*L, P+1)).  K/V tiles of 64 positions are staged in
-// shared memory with cp.async (zero-filled past the split, XOR-swizzled 16-byte
-// chunks so ldmatrix is conflict-free), double-buffered.  Each of the 4 warps
-// takes 16 positions of a tile and runs the two products on tensor cores
-// (mma.sync m16n8k16, bf16 in, fp32 accumulate): the GQA group's G query heads
-// share every K/V row, so scores and the weighted sum are small dense products.
-// Precision: q and the probabilities are split into bf16 hi + lo rows (rows
-// 0..G-1 and G..2G-1 of the 16-row A operand), which keeps ~16 significant bits
-// while K/V are bf16 already.  Softmax statistics are fp32 in the exp2 domain.
-// The last CTA to finish a (b, h) merges the splits in split order.
+// Grid (C, n_kv, B) in thread-block clusters of C CTAs along x: the cluster of
+// (sequence b, KV head h) splits that sequence's T = P+1 positions into C equal
+// runs of whole 64-position tiles (so ragged batches stay balanced), CTA r takes
+// run r.  Each CTA streams its K/V tiles into shared memory with cp.async
+// through a ring of S stages (XOR-swizzled 16-byte chunks so ldmatrix is
+// conflict-free; the first S-1 tiles are requested before the grid-dependency
+// wait) and runs both products on tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// accumulate): the group's G query heads share every K/V row.  q and the
+// probabilities enter as bf16 hi + lo rows (rows 0..G-1 and G..2G-1 of the
+// 16-row A operand), ~16 significant bits; softmax statistics are fp32 in the
+// exp2 domain.  The C partial results are merged through distributed shared
+// memory between two cluster barriers: CTA r combines a 1/C slice of the
+// outputs from all C CTAs (no global partials, no atomics).
 #include "dec_internal.cuh"
 
 namespace dec {
@@ -30,17 +32,17 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
-struct AttnSmem {
+struct AttnCfg {
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kAttnTile * kRowBytes;
-  static constexpr int kQBytes = 16 * kRowBytes;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;          // 2 stages
-  static constexpr int kOffV = kOffK + 2 * kTileBytes;   // 2 stages
-  static constexpr int kOffNew = kOffV + 2 * kTileBytes; // new k row, new v row (bf16)
-  static constexpr int kOffMisc = kOffNew + 2 * kRowBytes;
-  static constexpr int kMiscFloats = 2048 + 16;          // merge factors and sums + per-head stats
-  static constexpr int kBytes = kOffMisc + kMiscFloats * 4;
+  static constexpr int kStageBytes = 2 * kTileBytes;                  // K tile then V tile
+  static constexpr int kOffQ = 0;                                      // [16][D] bf16
+  static constexpr int kOffStages = 16 * kRowBytes;
+  static constexpr int kOffNew = kOffStages + kStages * kStageBytes;  // new k row, new v row
+  static constexpr int kOffXchg = kOffNew + 2 * kRowBytes;             // [G][D + 2] floats (G <= 4)
+  static constexpr int kOffMisc = kOffXchg + 4 * (D + 2) * 4;          // [4][G] floats
+  static constexpr int kBytes = kOffMisc + 64 * 4;
 };
 
 // byte offset of 16-byte chunk c of row r inside a swizzled tile
@@ -64,28 +66,57 @@ __device__ __forceinline__ void load_tile(uint32_t sdst, const __nv_bfloat16* pl
   }
 }
 
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared-memory address of the same variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Positions [begin, end) of CTA `rank` of a cluster of C for a sequence with T = P + 1
+// positions: runs of ceil(ceil(T / C) / 64) whole tiles; later CTAs may get none.
+__device__ __forceinline__ void attention_run(int T, int C, int rank, int* begin, int* end) {
+  const int per = (T + C - 1) / C;
+  const int len = (per + kAttnTile - 1) / kAttnTile * kAttnTile;
+  const int b0 = rank * len;
+  *begin = b0 < T ? b0 : T;
+  *end = b0 + len < T ? b0 + len : T;
+}
+
 }  // namespace
 
-template <int D, int G>
+template <int D, int G, int C>
 __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
-  using SM = AttnSmem<D>;
+  using CF = AttnCfg<D>;
+  constexpr int S = CF::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ unsigned s_ticket;
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int rank = static_cast<int>(cluster_ctarank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
   int P = p.positions[b];
   P = P < 0 ? 0 : (P >= p.max_ctx ? p.max_ctx - 1 : P);  // flagged by the embedding kernel
   const int T = P + 1;
-  const int nsplit = (T + p.split_len - 1) / p.split_len;
-  if (split >= nsplit) {
-    griddep_launch_dependents();
-    return;
-  }
-  const int pos_begin = split * p.split_len;
-  const int pos_end = min(pos_begin + p.split_len, T);
+  int pos_begin, pos_end;
+  attention_run(T, C, rank, &pos_begin, &pos_end);
   const int ntiles = (pos_end - pos_begin + kAttnTile - 1) / kAttnTile;
   const bool has_new = (P >= pos_begin && P < pos_end);
 
@@ -95,192 +126,205 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   __nv_bfloat16* vbase = p.kv + (static_cast<size_t>(p.layer) * 2 + 1) * plane + head_off;
 
   const uint32_t s_base = smem_u32(smem);
-  const uint32_t sQ = s_base + SM::kOffQ, sK = s_base + SM::kOffK, sV = s_base + SM::kOffV;
-  float* misc = reinterpret_cast<float*>(smem + SM::kOffMisc);
+  const uint32_t sStages = s_base + CF::kOffStages;
+  float* xchg = reinterpret_cast<float*>(smem + CF::kOffXchg);  // this CTA's [G][m, l, acc[D]]
+  float* misc = reinterpret_cast<float*>(smem + CF::kOffMisc);
 
-  // Tile 0 of the cached K/V does not depend on upstream kernels of this step.
-  load_tile<D>(sK, kbase, pos_begin, pos_end);
-  load_tile<D>(sV, vbase, pos_begin, pos_end);
-  cp_async_commit();
-
-  // zero the unused rows of the Q operand
-  {
-    uint32_t* q32 = reinterpret_cast<uint32_t*>(smem + SM::kOffQ);
+  // Cached K/V tiles do not depend on upstream kernels of this step: request the
+  // first S-1 before the grid-dependency wait.
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < ntiles) {
+      const int pos0 = pos_begin + s * kAttnTile;
+      load_tile<D>(sStages + s * CF::kStageBytes, kbase, pos0, pos_end);
+      load_tile<D>(sStages + s * CF::kStageBytes + CF::kTileBytes, vbase, pos0, pos_end);
+    }
+    cp_async_commit();
+  }
+  {  // zero the Q operand (rows 2G..15 stay zero)
+    uint32_t* q32 = reinterpret_cast<uint32_t*>(smem + CF::kOffQ);
     for (int i = tid; i < 16 * D / 2; i += kAttnThreads) q32[i] = 0u;
   }
 
   griddep_wait();
   __syncthreads();
 
-  // ---- q/k per-head RMSNorm + RoPE (+ KV append by the split holding slot P)
-  const int nqkv = (p.nq + 2 * p.nkv) * D;
-  const float* qkv_b = p.qkv + static_cast<size_t>(b) * nqkv;
-  const float2* rope_b = p.rope + static_cast<size_t>(b) * (D / 2);
-  constexpr int E = D / 32;  // elements per lane: lane + 32 m
-  auto norm_rope = [&](const float* src, const __nv_bfloat16* wn, float (&y)[E]) {
-    float x[E];
-    float ss = 0.f;
-#pragma unroll
-    for (int m = 0; m < E; ++m) {
-      x[m] = src[lane + 32 * m];
-      ss = fmaf(x[m], x[m], ss);
-    }
-    ss = warp_sum(ss);
-    const float inv = rsqrtf(ss / static_cast<float>(D) + p.eps);
-#pragma unroll
-    for (int m = 0; m < E; ++m) x[m] = (x[m] * inv) * bf16_to_f(wn[lane + 32 * m]);
-    // pairs (e, e + D/2): lane's elements m and m + E/2
-#pragma unroll
-    for (int m = 0; m < E / 2; ++m) {
-      const float2 cs = rope_b[lane + 32 * m];
-      const float a = x[m], c = x[m + E / 2];
-      y[m] = a * cs.x - c * cs.y;
-      y[m + E / 2] = c * cs.x + a * cs.y;
-    }
-  };
-  if (warp < G) {
-    float y[E];
-    norm_rope(qkv_b + (h * G + warp) * D, p.q_norm, y);
-    __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(smem + SM::kOffQ);
-#pragma unroll
-    for (int m = 0; m < E; ++m) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(y[m]);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(y[m] - __bfloat162float(hi));
-      q16[warp * D + lane + 32 * m] = hi;
-      q16[(G + warp) * D + lane + 32 * m] = lo;
-    }
-  }
-  if (has_new && warp == 3) {
-    float y[E];
-    norm_rope(qkv_b + p.nq * D + h * D, p.k_norm, y);
-    __nv_bfloat16* nk = reinterpret_cast<__nv_bfloat16*>(smem + SM::kOffNew);
-    __nv_bfloat16* nv = nk + D;
-    const float* vsrc = qkv_b + (p.nq + p.nkv) * D + h * D;
-#pragma unroll
-    for (int m = 0; m < E; ++m) {
-      const int e = lane + 32 * m;
-      const __nv_bfloat16 kk = __float2bfloat16_rn(y[m]);
-      const __nv_bfloat16 vv = __float2bfloat16_rn(vsrc[e]);
-      nk[e] = kk;
-      nv[e] = vv;
-      kbase[static_cast<size_t>(P) * D + e] = kk;
-      vbase[static_cast<size_t>(P) * D + e] = vv;
-    }
-  }
-  __syncthreads();
-
-  // A fragments of Q (rows g: hi for g < G, lo for G <= g < 2G; rows g+8 zero)
-  uint32_t qa[D / 16][2];
-  {
-    const uint32_t* q32 = reinterpret_cast<const uint32_t*>(smem + SM::kOffQ);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = q32[(g * D + kk * 16 + 2 * t) / 2];
-      qa[kk][1] = q32[(g * D + kk * 16 + 8 + 2 * t) / 2];
-    }
-  }
-
-  const float scale_log2 = kLog2e * rsqrtf(static_cast<float>(D));
   float m_run = -INFINITY, l_run = 0.f;
   float o[D / 8][4];
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 
-  for (int it = 0; it < ntiles; ++it) {
-    const int st = it & 1;
-    const int tile_pos0 = pos_begin + it * kAttnTile;
-    if (it + 1 < ntiles) {
-      const int nst = st ^ 1;
-      load_tile<D>(sK + nst * SM::kTileBytes, kbase, tile_pos0 + kAttnTile, pos_end);
-      load_tile<D>(sV + nst * SM::kTileBytes, vbase, tile_pos0 + kAttnTile, pos_end);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (ntiles > 0) {
+    // ---- q/k per-head RMSNorm + RoPE (+ KV append by the CTA holding slot P)
+    const int nqkv = (p.nq + 2 * p.nkv) * D;
+    const float* qkv_b = p.qkv + static_cast<size_t>(b) * nqkv;
+    const float2* rope_b = p.rope + static_cast<size_t>(b) * (D / 2);
+    constexpr int E = D / 32;  // elements per lane: lane + 32 m
+    auto norm_rope = [&](const float* src, const __nv_bfloat16* wn, float (&y)[E]) {
+      float x[E];
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < E; ++m) {
+        x[m] = src[lane + 32 * m];
+        ss = fmaf(x[m], x[m], ss);
+      }
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / static_cast<float>(D) + p.eps);
+#pragma unroll
+      for (int m = 0; m < E; ++m) x[m] = (x[m] * inv) * bf16_to_f(wn[lane + 32 * m]);
+      // pairs (e, e + D/2): lane's elements m and m + E/2
+#pragma unroll
+      for (int m = 0; m < E / 2; ++m) {
+        const float2 cs = rope_b[lane + 32 * m];
+        const float a = x[m], c = x[m + E / 2];
+        y[m] = a * cs.x - c * cs.y;
+        y[m + E / 2] = c * cs.x + a * cs.y;
+      }
+    };
+    if (warp < G) {
+      float y[E];
+      norm_rope(qkv_b + (h * G + warp) * D, p.q_norm, y);
+      __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(smem + CF::kOffQ);
+#pragma unroll
+      for (int m = 0; m < E; ++m) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(y[m]);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(y[m] - __bfloat162float(hi));
+        q16[warp * D + lane + 32 * m] = hi;
+        q16[(G + warp) * D + lane + 32 * m] = lo;
+      }
+    }
+    if (has_new && warp == 3) {
+      float y[E];
+      norm_rope(qkv_b + p.nq * D + h * D, p.k_norm, y);
+      __nv_bfloat16* nk = reinterpret_cast<__nv_bfloat16*>(smem + CF::kOffNew);
+      __nv_bfloat16* nv = nk + D;
+      const float* vsrc = qkv_b + (p.nq + p.nkv) * D + h * D;
+#pragma unroll
+      for (int m = 0; m < E; ++m) {
+        const int e = lane + 32 * m;
+        const __nv_bfloat16 kk = __float2bfloat16_rn(y[m]);
+        const __nv_bfloat16 vv = __float2bfloat16_rn(vsrc[e]);
+        nk[e] = kk;
+        nv[e] = vv;
+        kbase[static_cast<size_t>(P) * D + e] = kk;
+        vbase[static_cast<size_t>(P) * D + e] = vv;
+      }
     }
     __syncthreads();
-    if (has_new && P >= tile_pos0 && P < tile_pos0 + kAttnTile) {
-      // the cache row at P was read before this step's append: use the fresh values
-      const int r = P - tile_pos0;
-      const uint4* nk = reinterpret_cast<const uint4*>(smem + SM::kOffNew);
-      const uint4* nv = nk + D / 8;
-      if (tid < D / 8) {
-        *reinterpret_cast<uint4*>(smem + SM::kOffK + st * SM::kTileBytes + swz<D>(r, tid)) = nk[tid];
-        *reinterpret_cast<uint4*>(smem + SM::kOffV + st * SM::kTileBytes + swz<D>(r, tid)) = nv[tid];
-      }
-      __syncthreads();
-    }
 
-    const uint32_t tK = sK + st * SM::kTileBytes, tV = sV + st * SM::kTileBytes;
-    const int wrow = warp * 16;  // this warp's 16 positions within the tile
-
-    // ---- S = Q K^T (16 query rows x 16 positions)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // A fragments of Q (rows g: hi for g < G, lo for G <= g < 2G; rows g+8 zero)
+    uint32_t qa[D / 16][2];
     {
-      const int mi = lane >> 3, rr = lane & 7;
-      const int row = wrow + (mi >> 1) * 8 + rr;
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(smem + CF::kOffQ);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t bfr[4];
-        ldmatrix_x4(bfr, tK + swz<D>(row, 2 * kk + (mi & 1)));
-        mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, bfr[0], bfr[1]);
-        mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, bfr[2], bfr[3]);
+        qa[kk][0] = q32[(g * D + kk * 16 + 2 * t) / 2];
+        qa[kk][1] = q32[(g * D + kk * 16 + 8 + 2 * t) / 2];
       }
     }
-    // scores of row g at positions wrow + 8 n + 2 t + {0, 1}
-    float sv[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sv[i] += __shfl_xor_sync(0xffffffffu, sv[i], 4 * G);  // hi + lo rows
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int pos = tile_pos0 + wrow + (i >> 1) * 8 + 2 * t + (i & 1);
-      sv[i] = pos < pos_end ? sv[i] * scale_log2 : -INFINITY;
-    }
-    float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-    const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-    float pr[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = exp2f(sv[i] - mref);
-    l_run = l_run * corr + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-    m_run = m_new;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      o[j][0] *= corr;
-      o[j][1] *= corr;
-    }
-    // A operand of P: row g = hi (g < G) or lo (G <= g < 2G) part of this row's probabilities
-    uint32_t pa0 = 0u, pa2 = 0u;
-    if (g < G) {
-      pa0 = pack_bf16x2(pr[0], pr[1]);
-      pa2 = pack_bf16x2(pr[2], pr[3]);
-    } else if (g < 2 * G) {
-      float lo[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) lo[i] = pr[i] - __bfloat162float(__float2bfloat16_rn(pr[i]));
-      pa0 = pack_bf16x2(lo[0], lo[1]);
-      pa2 = pack_bf16x2(lo[2], lo[3]);
-    }
-    // ---- O += P V
-    {
-      const int mi = lane >> 3, rr = lane & 7;
-      const int row = wrow + (mi & 1) * 8 + rr;
-#pragma unroll
-      for (int jj = 0; jj < D / 16; ++jj) {
-        uint32_t bfr[4];
-        ldmatrix_x4_trans(bfr, tV + swz<D>(row, 2 * jj + (mi >> 1)));
-        mma_bf16_16816(o[2 * jj], pa0, 0u, pa2, 0u, bfr[0], bfr[1]);
-        mma_bf16_16816(o[2 * jj + 1], pa0, 0u, pa2, 0u, bfr[2], bfr[3]);
+
+    const float scale_log2 = kLog2e * rsqrtf(static_cast<float>(D));
+    for (int it = 0; it < ntiles; ++it) {
+      {  // refill the stage consumed in the previous iteration
+        const int nxt = it + S - 1;
+        if (nxt < ntiles) {
+          const int sn = nxt % S;
+          const int pos0 = pos_begin + nxt * kAttnTile;
+          load_tile<D>(sStages + sn * CF::kStageBytes, kbase, pos0, pos_end);
+          load_tile<D>(sStages + sn * CF::kStageBytes + CF::kTileBytes, vbase, pos0, pos_end);
+        }
+        cp_async_commit();
       }
+      cp_async_wait<S - 1>();  // tile `it` has landed
+      __syncthreads();
+      const int st = it % S;
+      const int tile_pos0 = pos_begin + it * kAttnTile;
+      if (has_new && P >= tile_pos0 && P < tile_pos0 + kAttnTile) {
+        // the cache row at P was read before this step's append: use the fresh values
+        const int r = P - tile_pos0;
+        const uint4* nk = reinterpret_cast<const uint4*>(smem + CF::kOffNew);
+        const uint4* nv = nk + D / 8;
+        if (tid < D / 8) {
+          unsigned char* stg = smem + CF::kOffStages + st * CF::kStageBytes;
+          *reinterpret_cast<uint4*>(stg + swz<D>(r, tid)) = nk[tid];
+          *reinterpret_cast<uint4*>(stg + CF::kTileBytes + swz<D>(r, tid)) = nv[tid];
+        }
+        __syncthreads();
+      }
+
+      const uint32_t tK = sStages + st * CF::kStageBytes, tV = tK + CF::kTileBytes;
+      const int wrow = warp * 16;  // this warp's 16 positions within the tile
+
+      // ---- S = Q K^T (16 query rows x 16 positions)
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int row = wrow + (mi >> 1) * 8 + rr;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t bfr[4];
+          ldmatrix_x4(bfr, tK + swz<D>(row, 2 * kk + (mi & 1)));
+          mma_bf16_16816(sacc[0], qa[kk][0], 0u, qa[kk][1], 0u, bfr[0], bfr[1]);
+          mma_bf16_16816(sacc[1], qa[kk][0], 0u, qa[kk][1], 0u, bfr[2], bfr[3]);
+        }
+      }
+      // scores of row g at positions wrow + 8 n + 2 t + {0, 1}
+      float sv[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sv[i] += __shfl_xor_sync(0xffffffffu, sv[i], 4 * G);  // hi + lo rows
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int pos = tile_pos0 + wrow + (i >> 1) * 8 + 2 * t + (i & 1);
+        sv[i] = pos < pos_end ? sv[i] * scale_log2 : -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+      float pr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pr[i] = exp2f(sv[i] - mref);
+      l_run = l_run * corr + (pr[0] + pr[1]) + (pr[2] + pr[3]);
+      m_run = m_new;
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        o[j][0] *= corr;
+        o[j][1] *= corr;
+      }
+      // A operand of P: row g = hi (g < G) or lo (G <= g < 2G) part of this row's probabilities
+      uint32_t pa0 = 0u, pa2 = 0u;
+      if (g < G) {
+        pa0 = pack_bf16x2(pr[0], pr[1]);
+        pa2 = pack_bf16x2(pr[2], pr[3]);
+      } else if (g < 2 * G) {
+        float lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) lo[i] = pr[i] - __bfloat162float(__float2bfloat16_rn(pr[i]));
+        pa0 = pack_bf16x2(lo[0], lo[1]);
+        pa2 = pack_bf16x2(lo[2], lo[3]);
+      }
+      // ---- O += P V
+      {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int row = wrow + (mi & 1) * 8 + rr;
+#pragma unroll
+        for (int jj = 0; jj < D / 16; ++jj) {
+          uint32_t bfr[4];
+          ldmatrix_x4_trans(bfr, tV + swz<D>(row, 2 * jj + (mi >> 1)));
+          mma_bf16_16816(o[2 * jj], pa0, 0u, pa2, 0u, bfr[0], bfr[1]);
+          mma_bf16_16816(o[2 * jj + 1], pa0, 0u, pa2, 0u, bfr[2], bfr[3]);
+        }
+      }
+      __syncthreads();  // this stage is refilled in the next iteration
     }
-    __syncthreads();  // this stage is refilled two iterations later
   }
+  cp_async_wait<0>();
+  __syncthreads();
   griddep_launch_dependents();
 
-  // ---- per-warp state -> CTA state (rows g < G hold head g after adding the lo row)
+  // ---- per-warp state -> this CTA's (m, l, acc) per head (rows g < G after adding the lo rows)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
 #pragma unroll
@@ -288,8 +332,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     o[j][0] += __shfl_xor_sync(0xffffffffu, o[j][0], 4 * G);
     o[j][1] += __shfl_xor_sync(0xffffffffu, o[j][1], 4 * G);
   }
-  // merge area (reuses the K stages): [4 warps][G] m, l, then [4][G][D] o
-  float* mw = reinterpret_cast<float*>(smem + SM::kOffK);
+  // warp partials in the (now idle) stage area: [4 warps][G] m, l, then [4][G][D] o
+  float* mw = reinterpret_cast<float*>(smem + CF::kOffStages);
   float* lw = mw + 4 * G;
   float* ow = lw + 4 * G;
   if (g < G) {
@@ -304,131 +348,94 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     }
   }
   __syncthreads();
-  // CTA-level (M, L) per head and scale factors per warp
-  float* fw = misc;                // [4][G]
-  float* cta_ml = misc + 4 * G;    // [G][2]
+  float* fw = misc;  // [4][G] warp weights
   if (tid < G) {
     float M = -INFINITY;
     for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * G + tid]);
     float L = 0.f;
     for (int w = 0; w < 4; ++w) {
-      const float f = exp2f(mw[w * G + tid] - M);
+      const float f = (M == -INFINITY) ? 0.f : exp2f(mw[w * G + tid] - M);
       fw[w * G + tid] = f;
       L += f * lw[w * G + tid];
     }
-    cta_ml[2 * tid] = M;
-    cta_ml[2 * tid + 1] = L;
+    xchg[tid * (D + 2)] = M;
+    xchg[tid * (D + 2) + 1] = L;
   }
   __syncthreads();
-
-  const int qoff = h * G * D;  // first query head of this group, in elements of out[b]
-  float* out_b = p.out + static_cast<size_t>(b) * p.nq * D;
-  if (nsplit == 1) {
-    for (int i = tid; i < G * D; i += kAttnThreads) {
-      const int j = i / D, e = i % D;
-      float a = 0.f;
-      for (int w = 0; w < 4; ++w) a += fw[w * G + j] * ow[(w * G + j) * D + e];
-      out_b[qoff + i] = a / cta_ml[2 * j + 1];
-    }
-    return;
-  }
-
-  const int rec = G * (D + 2);
-  float* part = p.partials + ((static_cast<size_t>(b) * p.nkv + h) * p.max_splits) * rec;
-  float* mine = part + static_cast<size_t>(split) * rec;
   for (int i = tid; i < G * D; i += kAttnThreads) {
     const int j = i / D, e = i % D;
     float a = 0.f;
+#pragma unroll
     for (int w = 0; w < 4; ++w) a += fw[w * G + j] * ow[(w * G + j) * D + e];
-    mine[j * (D + 2) + 2 + e] = a;
+    xchg[j * (D + 2) + 2 + e] = a;
   }
-  if (tid < G) {
-    mine[tid * (D + 2)] = cta_ml[2 * tid];
-    mine[tid * (D + 2) + 1] = cta_ml[2 * tid + 1];
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_ticket = atomicAdd(&p.counters[b * p.nkv + h], 1u);
-  __syncthreads();
-  if (s_ticket != static_cast<unsigned>(nsplit - 1)) return;
-  __threadfence();
 
-  // ---- last CTA of (b, h): log-sum-exp merge of the nsplit partials in split order
-  float* fac = misc;          // [nsplit][G]: first M_s, then e^(M_s - M)
-  float* lsp = misc + 1024;   // [nsplit][G]: L_s
-  float* tot = misc + 2048;   // [G] merged denominators
-  for (int i = tid; i < nsplit * G; i += kAttnThreads) {
-    const int s = i / G, j = i % G;
-    const float* r = part + static_cast<size_t>(s) * rec + j * (D + 2);
-    fac[i] = __ldcg(r);
-    lsp[i] = __ldcg(r + 1);
-  }
-  __syncthreads();
-  if (warp < G) {  // warp j reduces head j over the splits
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, fac[s * G + warp]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int s = lane; s < nsplit; s += 32) {
-      const float f = exp2f(fac[s * G + warp] - M);
-      fac[s * G + warp] = f;
-      L += f * lsp[s * G + warp];
+  // ---- cluster merge: CTA `rank` combines outputs [rank * n, (rank + 1) * n) of all C CTAs
+  cluster_sync();
+  {
+    constexpr int kOut = G * D;
+    constexpr int kPer = (kOut + C - 1) / C;
+    const uint32_t xa = smem_u32(xchg);
+    float* out_b = p.out + static_cast<size_t>(b) * p.nq * D + h * G * D;
+    const int i_end = (rank + 1) * kPer < kOut ? (rank + 1) * kPer : kOut;
+    for (int i = rank * kPer + tid; i < i_end; i += kAttnThreads) {
+      const int j = i / D, e = i % D;
+      float mr[C], lr[C], ar[C];
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        const uint32_t base = map_rank(xa, static_cast<uint32_t>(r));
+        mr[r] = ld_cluster_f32(base + (j * (D + 2)) * 4);
+        lr[r] = ld_cluster_f32(base + (j * (D + 2) + 1) * 4);
+        ar[r] = ld_cluster_f32(base + (j * (D + 2) + 2 + e) * 4);
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < C; ++r) M = fmaxf(M, mr[r]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        const float f = (mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M);
+        num = fmaf(f, ar[r], num);
+        den = fmaf(f, lr[r], den);
+      }
+      out_b[i] = num / den;
     }
-    L = warp_sum(L);
-    if (lane == 0) tot[warp] = L;
   }
-  __syncthreads();
-  for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int j = i / D, e = i % D;
-    const float* src = part + j * (D + 2) + 2 + e;
-    float a = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < nsplit; ++s) a = fmaf(fac[s * G + j], __ldcg(src + static_cast<size_t>(s) * rec), a);
-    out_b[qoff + i] = a / tot[j];
-  }
-  if (tid == 0) p.counters[b * p.nkv + h] = 0u;
+  cluster_sync();  // no CTA leaves while others may still read its shared memory
 }
 
-void attention_split_plan(int batch, int n_kv, int group, int max_ctx, int num_sms, int* split_len,
-                          int* max_splits) {
-  // Splits of 64 * 2^k positions: the shortest length that keeps the grid at the
-  // full context within two CTAs per SM, capped at 512 positions, and at most
-  // 1024 / group splits so the merge factors fit in shared memory.
-  int L = kAttnTile;
-  auto ns = [&](int len) { return (max_ctx + len - 1) / len; };
-  while (L < 512 && (static_cast<long long>(batch) * n_kv * ns(L) > 2ll * num_sms || ns(L) * group > 1024)) L *= 2;
-  while (ns(L) * group > 1024) L *= 2;
-  *split_len = L;
-  *max_splits = ns(L);
+namespace {
+
+template <int D, int G>
+cudaError_t launch_attn_t(const LaunchCtx& c, const AttnParams& p) {
+  constexpr int C = kAttnCluster;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, p.nkv, p.B);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = AttnCfg<D>::kBytes;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_attention<D, G, C>, p);
 }
 
-size_t attention_partials_floats(int batch, int n_kv, int group, int head_dim, int max_splits) {
-  return static_cast<size_t>(batch) * n_kv * max_splits * group * (head_dim + 2);
+template <int D, int G>
+cudaError_t prepare_attn_t() {
+  return cudaFuncSetAttribute(k_attention<D, G, kAttnCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(AttnCfg<D>::kBytes));
 }
+
+}  // namespace
 
 size_t attention_smem_bytes(int head_dim) {
-  return head_dim == 64 ? AttnSmem<64>::kBytes : AttnSmem<128>::kBytes;
-}
-
-template <int D, int G>
-static cudaError_t launch_attn_t(const LaunchCtx& c, const AttnParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.max_splits, p.nkv, p.B);
-  cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = AttnSmem<D>::kBytes;
-  cfg.stream = c.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_attention<D, G>, p);
-}
-
-template <int D, int G>
-static cudaError_t prepare_attn_t() {
-  return cudaFuncSetAttribute(k_attention<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(AttnSmem<D>::kBytes));
+  return head_dim == 64 ? AttnCfg<64>::kBytes : AttnCfg<128>::kBytes;
 }
 
 cudaError_t prepare_attention(int head_dim, int G) {

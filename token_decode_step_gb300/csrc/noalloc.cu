@@ -1,7 +1,7 @@
 // dec_attention_noalloc: the stand-alone fused attention (as dec_attention) for
-// callers that cannot allocate device memory.  Its scratch -- the split
-// partials, the merge counters and the RoPE table -- lives in one file-scope
-// device array instead of a caller workspace.
+// callers that cannot allocate device memory.  Its scratch -- the RoPE (cos, sin)
+// table that the first of its two kernels writes and the attention kernel reads
+// -- lives in one file-scope device array instead of a caller workspace.
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -12,7 +12,7 @@ using namespace dec;
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB: RoPE tables of up to 2048 sequences (head_dim 128)
 constexpr int kMaxDevices = 64;
 
 // Every GPU that loads this library holds this array until the process exits.
@@ -20,8 +20,6 @@ static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchByt
 
 std::mutex g_setup_mu;
 unsigned char* g_scratch_addr[kMaxDevices];  // device address of g_attn_scratch, per device; null until set up
-
-size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Per-device set-up with that device current: the device address of the array
 // (in host code the name g_attn_scratch is only a host-side stand-in) and the
@@ -75,9 +73,8 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
     set_last_error("dec_attention_noalloc: NULL pointer or kv_cache not 16-byte aligned");
     return DEC_ERR_INVALID_ARG;
   }
-  int dev = 0, sms = 0;
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
     set_last_error("dec_attention_noalloc: cannot query the current device: %s", cudaGetErrorString(e));
     return DEC_ERR_CUDA;
@@ -87,18 +84,12 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
     return DEC_ERR_UNSUPPORTED;
   }
 
-  // scratch layout: counters | RoPE table | split partials
-  int split_len = 0, max_splits = 0;
-  attention_split_plan(c.batch, c.n_kv_heads, G, c.max_ctx, sms, &split_len, &max_splits);
-  const size_t n_counters = static_cast<size_t>(c.batch) * c.n_kv_heads;
-  const size_t off_rope = round256(n_counters * 4);
-  const size_t off_part = off_rope + round256(static_cast<size_t>(c.batch) * (c.head_dim / 2) * 8);
-  const size_t total =
-      off_part + round256(attention_partials_floats(c.batch, c.n_kv_heads, G, c.head_dim, max_splits) * 4);
+  // scratch: the RoPE table, batch x head_dim/2 x (cos, sin)
+  const size_t total = static_cast<size_t>(c.batch) * (c.head_dim / 2) * 8;
   if (total > kNoAllocScratchBytes) {
-    set_last_error("dec_attention_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte "
-                   "array (reduce batch, n_kv_heads or max_ctx, or use dec_attention with a workspace)",
-                   total, kNoAllocScratchBytes);
+    set_last_error("dec_attention_noalloc: batch %d needs %zu bytes of scratch, above the fixed %zu-byte array "
+                   "(use dec_attention with a workspace)",
+                   c.batch, total, kNoAllocScratchBytes);
     return DEC_ERR_UNSUPPORTED;
   }
 
@@ -107,12 +98,7 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
   if (st != DEC_OK) return st;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // the merge counters must start at zero; the rest is overwritten before it is read
-  if ((e = cudaMemsetAsync(scratch, 0, n_counters * 4, cs)) != cudaSuccess) {
-    set_last_error("dec_attention_noalloc: clearing the counters failed: %s", cudaGetErrorString(e));
-    return DEC_ERR_CUDA;
-  }
-  float2* rope = reinterpret_cast<float2*>(scratch + off_rope);
+  float2* rope = reinterpret_cast<float2*>(scratch);  // fully rewritten by every call
   if ((e = launch_rope_table(cs, positions, c.batch, c.head_dim, c.max_ctx, c.rope_theta, rope, nullptr)) !=
       cudaSuccess) {
     set_last_error("dec_attention_noalloc: RoPE table launch failed: %s", cudaGetErrorString(e));
@@ -130,11 +116,7 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
   ap.nq = c.n_q_heads;
   ap.nkv = c.n_kv_heads;
   ap.max_ctx = c.max_ctx;
-  ap.split_len = split_len;
-  ap.max_splits = max_splits;
   ap.eps = c.rms_eps;
-  ap.partials = reinterpret_cast<float*>(scratch + off_part);
-  ap.counters = reinterpret_cast<unsigned*>(scratch);
   ap.out = out;
   ap.status = nullptr;
   if ((e = launch_attention(LaunchCtx{cs, false}, ap, c.head_dim)) != cudaSuccess) {
