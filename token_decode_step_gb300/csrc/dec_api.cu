@@ -100,6 +100,10 @@ struct dec_handle {
   float* attn_o = nullptr;
   float* g = nullptr;
   float* sumsq = nullptr;
+  // batched path: next-consumer inputs as bf16 hi, lo planes
+  __nv_bfloat16* xh_u = nullptr;  // [2][B][H]: h times the next norm weight
+  __nv_bfloat16* xh_o = nullptr;  // [2][B][nq d]: attention output
+  __nv_bfloat16* xh_g = nullptr;  // [2][B][I]: SwiGLU output
   float* gemv_partials = nullptr;
   unsigned* gemv_counters = nullptr;
   float2* rope = nullptr;
@@ -214,12 +218,12 @@ int choose_splits(int N, int K, int fmt, int num_sms) {
 
 // Batched path: inputs staged per chunk (shared-memory bound) and K splits so that the
 // grid covers the SMs at least twice.
-int tc_chunk_max(int, int ny) { return ny == 1 ? 2048 : ny == 2 ? 1024 : 512; }
+
 
 void choose_tc_splits(PackedLinear& L, int wfmt, int ny, int num_sms) {
   const int rpb = gemm_tc_rows_per_block(wfmt, ny);
   const int blocks = (L.Npad + rpb - 1) / rpb;
-  const int kc_max = tc_chunk_max(wfmt, ny);
+  const int kc_max = gemm_tc_chunk(ny);
   int S = 1;
   while (static_cast<long long>(blocks) * S < 2ll * num_sms) {
     const int S2 = S * 2;
@@ -278,6 +282,8 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.rope = h->rope;
   ep.amax_key = h->amax_key;
   ep.status = h->status;
+  ep.norm_w0 = h->layers[0].in_norm;
+  ep.xhl_out = c.batch > 1 ? h->xh_u : nullptr;
   ep.V = c.vocab;
   ep.H = H;
   ep.half_d = d / 2;
@@ -291,8 +297,10 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   int launched = 1;  // the embedding kernel
   auto limit_hit = [&]() { return h->launch_limit >= 0 && launched >= h->launch_limit; };
   if (limit_hit()) return DEC_OK;
+  // x, norm_w: the batch-1 input; xin, xout, next_norm: the batched path's hi/lo planes
   auto gemv = [&](const PackedLinear& L, int in_mode, int epi, const float* x, const __nv_bfloat16* norm_w,
-                  float* out, int cls, const char* what) -> dec_status {
+                  float* out, int cls, const char* what, const __nv_bfloat16* xin, __nv_bfloat16* xout,
+                  const __nv_bfloat16* next_norm) -> dec_status {
     if (limit_hit()) return DEC_OK;
     ++launched;
     GemvParams gp{};
@@ -328,8 +336,9 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       tp.KS = L.K / L.S;
       tp.KC = L.KC;
       tp.B = c.batch;
-      tp.x = x;
-      tp.norm_w = norm_w;
+      tp.xhl = xin;
+      tp.xhl_out = xout;
+      tp.next_norm_w = next_norm;
       tp.sumsq_in = h->sumsq;
       tp.n_sumsq_in = H / kResGroup;
       tp.eps = c.rms_eps;
@@ -347,7 +356,9 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
 
   for (int l = 0; l < c.n_layers; ++l) {
     const PackedLayer& L = h->layers[l];
-    if ((st = gemv(L.qkv, kInNorm, kEpiStore, h->h, L.in_norm, h->qkv, DEC_K_QKV, "qkv")) != DEC_OK) return st;
+    if ((st = gemv(L.qkv, kInNorm, kEpiStore, h->h, L.in_norm, h->qkv, DEC_K_QKV, "qkv", h->xh_u, nullptr,
+                   nullptr)) != DEC_OK)
+      return st;
 
     AttnParams ap{};
     ap.qkv = h->qkv;
@@ -364,6 +375,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.eps = c.rms_eps;
     ap.out = h->attn_o;
     ap.status = h->status;
+    ap.out_hl = c.batch > 1 ? h->xh_o : nullptr;
     if (limit_hit()) return DEC_OK;
     ++launched;
     note(DEC_K_ATTN);
@@ -371,13 +383,19 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     if ((st = check(launch_attention(lc, ap, d), "attention")) != DEC_OK) return st;
     ev_end();
 
-    if ((st = gemv(L.o, kInPlain, kEpiResid, h->attn_o, nullptr, h->h, DEC_K_OPROJ, "o_proj")) != DEC_OK) return st;
-    if ((st = gemv(L.gateup, kInNorm, kEpiSwiglu, h->h, L.post_norm, h->g, DEC_K_GATEUP, "gate_up")) != DEC_OK)
+    const __nv_bfloat16* after = (l + 1 < c.n_layers) ? h->layers[l + 1].in_norm : h->final_norm;
+    if ((st = gemv(L.o, kInPlain, kEpiResid, h->attn_o, nullptr, h->h, DEC_K_OPROJ, "o_proj", h->xh_o, h->xh_u,
+                   L.post_norm)) != DEC_OK)
       return st;
-    if ((st = gemv(L.down, kInPlain, kEpiResid, h->g, nullptr, h->h, DEC_K_DOWN, "down")) != DEC_OK) return st;
+    if ((st = gemv(L.gateup, kInNorm, kEpiSwiglu, h->h, L.post_norm, h->g, DEC_K_GATEUP, "gate_up", h->xh_u,
+                   h->xh_g, nullptr)) != DEC_OK)
+      return st;
+    if ((st = gemv(L.down, kInPlain, kEpiResid, h->g, nullptr, h->h, DEC_K_DOWN, "down", h->xh_g, h->xh_u, after)) !=
+        DEC_OK)
+      return st;
   }
-  if ((st = gemv(h->lm_head, kInNorm, kEpiLmHead, h->h, h->final_norm, sp.logits, DEC_K_LMHEAD, "lm_head")) !=
-      DEC_OK)
+  if ((st = gemv(h->lm_head, kInNorm, kEpiLmHead, h->h, h->final_norm, sp.logits, DEC_K_LMHEAD, "lm_head",
+                 h->xh_u, nullptr, nullptr)) != DEC_OK)
     return st;
   return DEC_OK;
 }
@@ -619,6 +637,9 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const size_t o_att = plan(static_cast<size_t>(B) * nq * d * 4);
   const size_t o_g = plan(static_cast<size_t>(B) * I * 4);
   const size_t o_ss = plan(static_cast<size_t>(B) * (H / kResGroup) * 4);
+  const size_t o_xu = plan(static_cast<size_t>(2) * B * H * 2);
+  const size_t o_xo = plan(static_cast<size_t>(2) * B * nq * d * 2);
+  const size_t o_xg = plan(static_cast<size_t>(2) * B * I * 2);
   const size_t o_gp = plan((max_partials ? max_partials : 1) * 4);
   const size_t o_gc = plan(static_cast<size_t>(max_tiles + 1) * 4);
   const size_t o_rope = plan(static_cast<size_t>(B) * (d / 2) * 8);
@@ -636,6 +657,9 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   h->attn_o = reinterpret_cast<float*>(h->ws + o_att);
   h->g = reinterpret_cast<float*>(h->ws + o_g);
   h->sumsq = reinterpret_cast<float*>(h->ws + o_ss);
+  h->xh_u = reinterpret_cast<__nv_bfloat16*>(h->ws + o_xu);
+  h->xh_o = reinterpret_cast<__nv_bfloat16*>(h->ws + o_xo);
+  h->xh_g = reinterpret_cast<__nv_bfloat16*>(h->ws + o_xg);
   h->gemv_partials = reinterpret_cast<float*>(h->ws + o_gp);
   h->gemv_counters = reinterpret_cast<unsigned*>(h->ws + o_gc);
   h->rope = reinterpret_cast<float2*>(h->ws + o_rope);
@@ -652,7 +676,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if (tc) {
     GemmParams gp{};
     gp.B = c.batch;
-    gp.KC = tc_chunk_max(h->wfmt, ny);
+    gp.KC = gemm_tc_chunk(ny);
     const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
     for (auto& cb : combos)
       if ((e = prepare_gemm_tc(gp, h->wfmt, cb[0], cb[1])) != cudaSuccess) return fail("batched kernel attributes", e);

@@ -18,6 +18,7 @@ constexpr int kAttnTile = 64;       // positions per attention smem tile
 constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
 constexpr int kAttnCluster = 8;     // CTAs per (sequence, KV head): one thread-block cluster
 constexpr int kGroup = 64;          // affine 4-bit group size
+constexpr int kGemmPrefetch = 4;    // 64-input weight units in flight per lane (batched path)
 
 enum StatusBits : unsigned { kStatusBadToken = 1u, kStatusBadPos = 2u, kStatusTimeout = 4u };
 
@@ -52,13 +53,14 @@ struct GemmParams {
   const void* w;            // packed tiles (see k_gemm_tc.cu)
   int N, Npad, K, S, KS, KC, B;  // rows, rows padded to 16, inputs, K splits, inputs per split,
                                  // inputs staged at once (divides KS), tokens
-  const float* x;           // [B][K]
-  const __nv_bfloat16* norm_w;
-  const float* sumsq_in;    // [B][n_sumsq_in]
+  const __nv_bfloat16* xhl; // input as bf16 hi, lo planes [2][B][K] (norm inputs already times the norm weight)
+  const float* sumsq_in;    // norm inputs: [B][n_sumsq_in] partial sums of squares of the residual
   int n_sumsq_in;
   float eps;
   float* out;               // store: [B][N]; resid: h [B][N] (+=); swiglu: g [B][N/2]; lmhead: logits [B][N] or null
   float* sumsq_out;         // resid: [B][N / kResGroup]
+  __nv_bfloat16* xhl_out;   // resid: h * next_norm_w, swiglu: g, as hi, lo planes (the next consumer's input)
+  const __nv_bfloat16* next_norm_w;  // resid: [N]
   float* partials;          // [S][Npad/16][32][NY*4] when S > 1
   unsigned* counters;       // [row blocks + 1], zero on entry, left zero
   unsigned long long* amax_key;  // lmhead: [B]
@@ -76,6 +78,7 @@ struct AttnParams {
   int layer, B, nq, nkv, max_ctx;
   float eps;
   float* out;                   // [B][nq d]
+  __nv_bfloat16* out_hl;        // optional: the output again as bf16 hi, lo planes [2][B][nq d]
   unsigned* status;
 };
 
@@ -89,6 +92,8 @@ struct EmbedParams {
   float2* rope;                 // [B][d/2]
   unsigned long long* amax_key; // [B]
   unsigned* status;
+  const __nv_bfloat16* norm_w0;  // optional: first layer's input norm weight, for xhl_out
+  __nv_bfloat16* xhl_out;        // optional: h * norm_w0 as bf16 hi, lo planes [2][B][H]
   int V, H, half_d, max_ctx;
 };
 
@@ -197,7 +202,8 @@ cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_d
 // batched tensor-core projection
 int gemm_tc_ny(int wfmt, int batch);            // 8-token n-tiles per hi/lo half, 0 if unsupported
 int gemm_tc_rows_per_block(int wfmt, int ny);   // weight rows one CTA covers
-size_t gemm_tc_smem_bytes(int wfmt, int ny, int ks);
+size_t gemm_tc_smem_bytes(int wfmt, int ny, int kc);
+int gemm_tc_chunk(int ny);                      // inputs staged per chunk
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi);
 cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
 size_t attention_smem_bytes(int head_dim);

@@ -398,7 +398,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
         num = fmaf(f, ar[r], num);
         den = fmaf(f, lr[r], den);
       }
-      out_b[i] = num / den;
+      const float ov = num / den;
+      out_b[i] = ov;
+      if (p.out_hl) {  // batched path: the O projection's input as hi + lo planes
+        const size_t o = static_cast<size_t>(b) * p.nq * D + h * G * D + i;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(ov);
+        p.out_hl[o] = hi;
+        p.out_hl[static_cast<size_t>(p.B) * p.nq * D + o] = __float2bfloat16_rn(ov - __bfloat162float(hi));
+      }
     }
   }
   cluster_sync();  // no CTA leaves while others may still read its shared memory

@@ -1,8 +1,8 @@
 // Batched (B >= 2) fused projections on tensor cores: Y[b][n] = sum_k W[n][k] X[b][k]
 // with mma.sync m16n8k16 (weights as the 16-row A operand, tokens as the 8-column
-// B operand, fp32 accumulation), RMSNorm folded into the X staging and the same
-// epilogues as the batch-1 GEMV (store / residual + sum of squares / SwiGLU /
-// lm_head argmax).
+// B operand, fp32 accumulation) and the same fused steps as the batch-1 GEMV:
+// RMSNorm of the input, then store / residual add + sum of squares / SwiGLU /
+// lm_head argmax.
 //
 // Sources: Butter architecture.md "SINGLE-TOKEN DECODE" (the gemv sequence);
 // oxinfer crate page "MLX checkpoints" (affine 4-bit, w = scale*q + bias, the
@@ -19,13 +19,15 @@
 //         512 bytes of codes (lane-major, one 32-bit word per 16-input k-step,
 //         arranged so that (word >> 4i) & 0x000F000F yields A register i), then
 //         for each g the bf16 (scale, bias) of rows g and g+8.
-// Activations: staged in shared memory as bf16 hi + lo rows (x = hi + lo, ~16
-// significant bits; one row per token and half, padded by 16 bytes to keep
-// ldmatrix conflict-free), so every 8 tokens take two n-tiles.  bf16 weights are
-// the A operand as they are; 4-bit weights enter as their exact integer codes q
-// (bf16), and the group scale and bias are applied in fp32 after each group:
-// y += s * sum(q x) + b * sum(x).
-#include <cuda_fp16.h>
+// Activations: the producing kernel already wrote them as bf16 hi + lo planes
+// ([2][B][K], x = hi + lo, ~16 significant bits), for norm inputs multiplied by
+// the norm weight; the per-token 1/rms is applied to the products afterwards
+// (the product is linear in x).  Chunks of KC inputs are copied into shared
+// memory with cp.async, double-buffered, one padded row per token and half
+// (16-byte padding keeps ldmatrix conflict-free), so every 8 tokens take two
+// n-tiles.  4-bit weights enter as exact integer codes q (bf16) and the group
+// scale and bias are applied in fp32 after each group: y += s*sum(q x) + b*sum(x).
+#include <type_traits>
 
 #include "dec_internal.cuh"
 #include "q4.cuh"
@@ -34,193 +36,213 @@ namespace dec {
 
 namespace {
 
-constexpr int kWarps = 8;
-
-__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t smem_addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1]) : "r"(smem_addr));
-}
-
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// (hi, lo) bf16 split of a float: hi = bf16(v), lo = bf16(v - hi)
+__device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
 
 }  // namespace
 
 size_t gemm_tc_smem_bytes(int wfmt, int ny, int kc) {
-  const int nt = 2 * ny;
-  size_t b = static_cast<size_t>(nt) * 8 * (kc + 8) * 2;
-  if (wfmt == kWQ4) b += static_cast<size_t>(kc / kGroup) * ny * 8 * 4;
+  size_t b = 2ull * (2 * ny * 8) * (kc + 8) * 2;              // two chunk buffers
+  if (wfmt == kWQ4) b += 2ull * (kc / kGroup) * ny * 8 * 4;  // two group-sum buffers
   return b;
 }
 
-template <int WF, int NY, int TPW, int IN, int EPI>
-__global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
+template <int WF, int NY, int TPW, int WARPS, int IN, int EPI>
+__global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
   constexpr int NT = 2 * NY;  // n-tiles of the MMA: hi rows of every token, then lo rows
-  constexpr int XR = NT * 8;              // staged activation rows
+  constexpr int XR = NT * 8;  // staged rows per chunk buffer
+  constexpr int NTH = WARPS * 32;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float s_inv[32];
   __shared__ unsigned s_ticket;
 
-  const int KC = p.KC, KSP = p.KC + 8;  // staged chunk of the split, padded rows
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-  float* xsum = reinterpret_cast<float*>(smem + static_cast<size_t>(XR) * KSP * 2);  // [KS/64][NY*8]
+  const int KC = p.KC, KSP = p.KC + 8;  // staged chunk, padded row length
+  const size_t buf_elems = static_cast<size_t>(XR) * KSP;
+  uint16_t* xs0 = reinterpret_cast<uint16_t*>(smem);
+  float* xsum0 = reinterpret_cast<float*>(smem + 2 * buf_elems * 2);  // two [KC/64][NY*8] buffers
 
   const int rb = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int kbeg0 = split * p.KS;
   const int n_rt = p.Npad / 16;
-  const int rt0 = (rb * kWarps + warp) * TPW;
+  const int rt0 = (rb * WARPS + warp) * TPW;
+  const int nchunks = p.KS / KC;
+
+  bool valid[TPW];
+#pragma unroll
+  for (int i = 0; i < TPW; ++i) valid[i] = (rt0 + i) < n_rt;
+
+  {  // rows of absent tokens (and their lo rows) stay zero in both buffers
+    uint4* z = reinterpret_cast<uint4*>(smem);
+    const int nz = static_cast<int>(2 * buf_elems * 2 / 16);
+    for (int i = tid; i < nz; i += NTH) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // The K split is walked in units of 64 inputs (4 bf16 k-tiles, or one 4-bit group);
+  // each lane keeps the weights of PF units in flight in a register ring, across the
+  // chunk boundaries of the staged activations.
+  constexpr int PF = kGemmPrefetch;
+  using Unit = typename std::conditional<WF == kWBf16, uint4[TPW][4], uint4[TPW][2]>::type;
+  const int nunits = p.KS / 64, upc = KC / 64;
+  const int ktiles = p.K / 16, gtiles = p.K / kGroup;
+  auto load_unit = [&](int u, Unit& dst) {
+    const int ug = kbeg0 / 64 + u;  // 64-input unit index along the whole K
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+      if constexpr (WF == kWBf16) {
+        const uint4* wb = static_cast<const uint4*>(p.w) + (static_cast<size_t>(rt0 + i) * ktiles + 4 * ug) * 32 + lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[i][q] = valid[i] ? ld_stream16(wb + q * 32) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const unsigned char* tile = static_cast<const unsigned char*>(p.w) + (static_cast<size_t>(rt0 + i) * gtiles + ug) * 576;
+        dst[i][0] = valid[i] ? ld_stream16(tile + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const uint2 sb = valid[i] ? __ldg(reinterpret_cast<const uint2*>(tile + 512 + g * 8)) : make_uint2(0u, 0u);
+        dst[i][1] = make_uint4(sb.x, sb.y, 0u, 0u);
+      }
+    }
+  };
+  // weights do not depend on upstream kernels: the first PF units are requested
+  // before the grid-dependency wait
+  Unit ring[PF];
+#pragma unroll
+  for (int j = 0; j < PF; ++j)
+    if (j < nunits) load_unit(j, ring[j]);
 
   griddep_wait();
 
-  // ---- per-token inverse RMS (fused RMSNorm), then stage X for this K split
-  if constexpr (IN == kInNorm) {
-    for (int b = warp; b < p.B; b += kWarps) {
+  if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (fused RMSNorm)
+    for (int b = warp; b < p.B; b += WARPS) {
       float s = 0.f;
       for (int i = lane; i < p.n_sumsq_in; i += 32) s += p.sumsq_in[static_cast<size_t>(b) * p.n_sumsq_in + i];
       s = warp_sum(s);
       if (lane == 0) s_inv[b] = rsqrtf(s / static_cast<float>(p.K) + p.eps);
     }
   }
-  // ---- main loop: each warp owns TPW row tiles over the whole K split, staged chunk by chunk
+  __syncthreads();
+
+  // copy chunk c (inputs kbeg0 + c KC ..) of both planes into buffer c & 1
+  auto issue_chunk = [&](int c) {
+    const uint32_t dst0 = smem_u32(xs0 + (c & 1) * buf_elems);
+    const int per_row = KC / 8;  // 16-byte pieces
+    const int kb = kbeg0 + c * KC;
+    for (int idx = tid; idx < 2 * p.B * per_row; idx += NTH) {
+      const int r = idx / per_row, j = idx % per_row;
+      const int plane = r / p.B, b = r % p.B;
+      const __nv_bfloat16* src = p.xhl + (static_cast<size_t>(plane) * p.B + b) * p.K + kb + 8 * j;
+      const int srow = plane * NY * 8 + b;
+      cp_async16(dst0 + (srow * KSP + 8 * j) * 2, src, 16);
+    }
+    cp_async_commit();
+  };
+
   float acc[TPW][NT][4];
 #pragma unroll
   for (int i = 0; i < TPW; ++i)
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[i][n][0] = acc[i][n][1] = acc[i][n][2] = acc[i][n][3] = 0.f;
-  bool valid[TPW];
-#pragma unroll
-  for (int i = 0; i < TPW; ++i) valid[i] = (rt0 + i) < n_rt;
 
-  {  // rows of absent tokens (and their lo rows) stay zero for every chunk
-    uint4* z = reinterpret_cast<uint4*>(smem);
-    const int nz = XR * KSP * 2 / 16;
-    for (int i = tid; i < nz; i += kWarps * 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
-  for (int kbeg = kbeg0; kbeg < kbeg0 + p.KS; kbeg += KC) {
-    if (kbeg != kbeg0) __syncthreads();  // previous chunk fully consumed
-    const int k4 = KC / 4;
-    for (int idx = tid; idx < p.B * k4; idx += kWarps * 32) {
-      const int b = idx / k4, kq = idx % k4;
-      const int col = kbeg + 4 * kq;
-      float4 v = *reinterpret_cast<const float4*>(p.x + static_cast<size_t>(b) * p.K + col);
-      if constexpr (IN == kInNorm) {
-        const uint2 wn = *reinterpret_cast<const uint2*>(p.norm_w + col);
-        const float r = s_inv[b];
-        v.x = (v.x * r) * bf16_lo(wn.x);
-        v.y = (v.y * r) * bf16_hi(wn.x);
-        v.z = (v.z * r) * bf16_lo(wn.y);
-        v.w = (v.w * r) * bf16_hi(wn.y);
-      }
-      uint16_t* dst = xs + static_cast<size_t>(b) * KSP + 4 * kq;
-      const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
-      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-      const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-      const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-      uint2 hv, lv;
-      hv.x = *reinterpret_cast<const uint32_t*>(&h01);
-      hv.y = *reinterpret_cast<const uint32_t*>(&h23);
-      lv.x = *reinterpret_cast<const uint32_t*>(&l01);
-      lv.y = *reinterpret_cast<const uint32_t*>(&l23);
-      *reinterpret_cast<uint2*>(dst) = hv;
-      *reinterpret_cast<uint2*>(dst + static_cast<size_t>(NY) * 8 * KSP) = lv;
-    }
-    __syncthreads();
-    if constexpr (WF == kWQ4) {
-      // per (group, token) sum of the staged inputs (hi + lo), for the bias term: together
-      // with the MMA over the same staged values this is sum_k (s q_k + b) x_k
-      const int ng = KC / kGroup;
-      for (int idx = tid; idx < ng * NY * 8; idx += kWarps * 32) {
-        const int grp = idx / (NY * 8), b = idx % (NY * 8);
-        const __nv_bfloat16* hi = reinterpret_cast<const __nv_bfloat16*>(xs) + static_cast<size_t>(b) * KSP + grp * kGroup;
-        const __nv_bfloat16* lo = hi + static_cast<size_t>(NY) * 8 * KSP;
-        float s = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < kGroup; ++i) s += __bfloat162float(hi[i]) + __bfloat162float(lo[i]);
-        xsum[idx] = s;
-      }
-      __syncthreads();
-    }
-    const uint32_t xs_base = smem_u32(xs);
-    // ldmatrix lane address for n-tile pair np at input column c (within the split)
-    auto b_frags = [&](int c, uint32_t (&bf)[NT][2]) {
-      const int mi = lane >> 3, rr = lane & 7;
+  issue_chunk(0);
+  const uint16_t* xs = xs0;
+  float* xsum = xsum0;
+  uint32_t xs_base = smem_u32(xs0);
+  // ldmatrix: B fragments of every n-tile at input column cc (within the chunk)
+  auto b_frags = [&](int cc, uint32_t (&bf)[NT][2]) {
+    const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-      for (int np = 0; np < NT / 2; ++np) {
-        const int row = (2 * np + (mi >> 1)) * 8 + rr;
-        uint32_t r[4];
-        ldmatrix_x4(r, xs_base + (row * KSP + c + 8 * (mi & 1)) * 2);
-        bf[2 * np][0] = r[0];
-        bf[2 * np][1] = r[1];
-        bf[2 * np + 1][0] = r[2];
-        bf[2 * np + 1][1] = r[3];
-      }
-      if constexpr (NT % 2 == 1) {
-        const int row = (NT - 1) * 8 + rr;
-        uint32_t r[2];
-        ldmatrix_x2(r, xs_base + (row * KSP + c + 8 * ((lane >> 3) & 1)) * 2);
-        bf[NT - 1][0] = r[0];
-        bf[NT - 1][1] = r[1];
-      }
-    };
+    for (int np = 0; np < NT / 2; ++np) {
+      const int row = (2 * np + (mi >> 1)) * 8 + rr;
+      uint32_t r[4];
+      ldmatrix_x4(r, xs_base + (row * KSP + cc + 8 * (mi & 1)) * 2);
+      bf[2 * np][0] = r[0];
+      bf[2 * np][1] = r[1];
+      bf[2 * np + 1][0] = r[2];
+      bf[2 * np + 1][1] = r[3];
+    }
+  };
 
-    if constexpr (WF == kWBf16) {
-      const int nk = KC / 16, kt0 = kbeg / 16, ktiles = p.K / 16;
-      const uint4* wbase = static_cast<const uint4*>(p.w);
-      for (int kk = 0; kk < nk; kk += 4) {
-        uint4 a[TPW][4];
+  for (int u0 = 0; u0 < nunits; u0 += PF) {
 #pragma unroll
-        for (int i = 0; i < TPW; ++i)
+    for (int j = 0; j < PF; ++j) {
+      const int u = u0 + j;
+      if (u >= nunits) break;
+      const int c = u / upc, uc = u % upc;  // chunk and unit within it
+      if (uc == 0) {  // activations of chunk c: wait for them, prefetch chunk c + 1
+        if (c + 1 < nchunks) {
+          issue_chunk(c + 1);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+        __syncthreads();
+        xs = xs0 + (c & 1) * buf_elems;
+        xs_base = smem_u32(xs);
+        xsum = xsum0 + (c & 1) * (KC / kGroup) * NY * 8;
+        if constexpr (WF == kWQ4) {
+          // per (group, token) sum of the staged inputs (hi + lo), for the bias term: with
+          // the MMA over the same staged values this is sum_k (s q_k + b) x_k
+          const int ng = KC / kGroup;
+          for (int idx = tid; idx < ng * NY * 8; idx += NTH) {
+            const int grp = idx / (NY * 8), b = idx % (NY * 8);
+            const uint4* hi = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(b) * KSP + grp * kGroup);
+            const uint4* lo = reinterpret_cast<const uint4*>(xs + static_cast<size_t>(NY * 8 + b) * KSP + grp * kGroup);
+            float sum = 0.f;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            a[i][u] = valid[i] ? ld_stream16(wbase + (static_cast<size_t>(rt0 + i) * ktiles + kt0 + kk + u) * 32 + lane)
-                               : make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < kGroup / 8; ++q) {
+              const uint4 va = hi[q], vd = lo[q];
+              sum += (bf16_lo(va.x) + bf16_hi(va.x)) + (bf16_lo(va.y) + bf16_hi(va.y)) +
+                     (bf16_lo(va.z) + bf16_hi(va.z)) + (bf16_lo(va.w) + bf16_hi(va.w));
+              sum += (bf16_lo(vd.x) + bf16_hi(vd.x)) + (bf16_lo(vd.y) + bf16_hi(vd.y)) +
+                     (bf16_lo(vd.z) + bf16_hi(vd.z)) + (bf16_lo(vd.w) + bf16_hi(vd.w));
+            }
+            xsum[idx] = sum;
+          }
+          __syncthreads();
+        }
+      }
+
+      if constexpr (WF == kWBf16) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int q = 0; q < 4; ++q) {
           uint32_t bf[NT][2];
-          b_frags((kk + u) * 16, bf);
+          b_frags(uc * 64 + q * 16, bf);
 #pragma unroll
           for (int i = 0; i < TPW; ++i)
 #pragma unroll
             for (int n = 0; n < NT; ++n)
-              mma_bf16_16816(acc[i][n], a[i][u].x, a[i][u].y, a[i][u].z, a[i][u].w, bf[n][0], bf[n][1]);
+              mma_bf16_16816(acc[i][n], ring[j][i][q].x, ring[j][i][q].y, ring[j][i][q].z, ring[j][i][q].w, bf[n][0],
+                             bf[n][1]);
         }
-      }
-    } else {
-      const int ngrp = KC / kGroup, g0 = kbeg / kGroup, gtiles = p.K / kGroup;
-      const unsigned char* wbase = static_cast<const unsigned char*>(p.w);
-      for (int grp = 0; grp < ngrp; ++grp) {
-        uint4 nib[TPW];
-        uint2 sbv[TPW];
-#pragma unroll
-        for (int i = 0; i < TPW; ++i) {
-          const unsigned char* tile = wbase + (static_cast<size_t>(rt0 + i) * gtiles + g0 + grp) * 576;
-          nib[i] = valid[i] ? ld_stream16(tile + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
-          sbv[i] = valid[i] ? __ldg(reinterpret_cast<const uint2*>(tile + 512 + g * 8)) : make_uint2(0u, 0u);
-        }
+      } else {
         float gacc[TPW][NT][4];
 #pragma unroll
         for (int i = 0; i < TPW; ++i)
 #pragma unroll
           for (int n = 0; n < NT; ++n) gacc[i][n][0] = gacc[i][n][1] = gacc[i][n][2] = gacc[i][n][3] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int q = 0; q < 4; ++q) {
           uint32_t bf[NT][2];
-          b_frags(grp * kGroup + u * 16, bf);
+          b_frags(uc * kGroup + q * 16, bf);
 #pragma unroll
           for (int i = 0; i < TPW; ++i) {
-            const uint32_t word = u == 0 ? nib[i].x : u == 1 ? nib[i].y : u == 2 ? nib[i].z : nib[i].w;
+            const uint4 nib = ring[j][i][0];
+            const uint32_t word = q == 0 ? nib.x : q == 1 ? nib.y : q == 2 ? nib.z : nib.w;
             const uint32_t a0 = q4_pair_bf16(word, 0), a1 = q4_pair_bf16(word, 4);
             const uint32_t a2 = q4_pair_bf16(word, 8), a3 = q4_pair_bf16(word, 12);
 #pragma unroll
             for (int n = 0; n < NT; ++n) mma_bf16_16816(gacc[i][n], a0, a1, a2, a3, bf[n][0], bf[n][1]);
           }
         }
-        const float* xg = xsum + grp * NY * 8;
+        const float* xg = xsum + uc * NY * 8;
 #pragma unroll
         for (int i = 0; i < TPW; ++i) {
-          const float s_lo = bf16_lo(sbv[i].x), b_lo = bf16_hi(sbv[i].x);  // row g
-          const float s_hi = bf16_lo(sbv[i].y), b_hi = bf16_hi(sbv[i].y);  // row g + 8
+          const uint4 sb = ring[j][i][1];
+          const float s_lo = bf16_lo(sb.x), b_lo = bf16_hi(sb.x);  // row g
+          const float s_hi = bf16_lo(sb.y), b_hi = bf16_hi(sb.y);  // row g + 8
 #pragma unroll
           for (int n = 0; n < NY; ++n)  // hi n-tile n and lo n-tile n + NY hold the same tokens
 #pragma unroll
@@ -231,6 +253,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
             }
         }
       }
+      if (u + PF < nunits) load_unit(u + PF, ring[j]);  // refill the slot just consumed
+      if (uc == upc - 1) __syncthreads();               // buffer c & 1 is refilled with chunk c + 2
     }
   }
   griddep_launch_dependents();
@@ -280,7 +304,20 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
     if (tid == 0) p.counters[rb] = 0u;
   }
 
+  if constexpr (IN == kInNorm) {  // the norm's 1/rms, per token
+#pragma unroll
+    for (int n = 0; n < NY; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 8 * n + 2 * t + (e & 1);
+        const float r = tok < p.B ? s_inv[tok] : 0.f;
+#pragma unroll
+        for (int i = 0; i < TPW; ++i) y[i][n][e] *= r;
+      }
+  }
+
   // ---- epilogue
+  const size_t plane_out = static_cast<size_t>(p.B) * (EPI == kEpiSwiglu ? p.N / 2 : p.N);
 #pragma unroll
   for (int i = 0; i < TPW; ++i) {
     if (!valid[i]) continue;
@@ -299,6 +336,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
             float* hp = p.out + static_cast<size_t>(tok) * p.N + row;
             hn = *hp + y[i][n][e];
             *hp = hn;
+            // the next consumer's input: h times its norm weight, as hi + lo planes
+            __nv_bfloat16 hi, lo;
+            split_hl(hn * bf16_to_f(p.next_norm_w[row]), hi, lo);
+            const size_t o = static_cast<size_t>(tok) * p.N + row;
+            p.xhl_out[o] = hi;
+            p.xhl_out[plane_out + o] = lo;
           }
           float ss = hn * hn;  // sum over the 8 rows g of this half-tile (lanes with equal t)
           ss += __shfl_xor_sync(0xffffffffu, ss, 4);
@@ -307,8 +350,15 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
           if (g == 0 && tok < p.B) p.sumsq_out[static_cast<size_t>(tok) * (p.N / kResGroup) + 2 * rt + (e >> 1)] = ss;
         } else if constexpr (EPI == kEpiSwiglu) {
           // rows 0..7 of a tile are gate rows, rows 8..15 the matching up rows
-          if (e < 2 && tok < p.B)
-            p.out[static_cast<size_t>(tok) * (p.N / 2) + 8 * rt + g] = silu_f(y[i][n][e]) * y[i][n][e + 2];
+          if (e < 2 && tok < p.B) {
+            const float gv = silu_f(y[i][n][e]) * y[i][n][e + 2];
+            const size_t o = static_cast<size_t>(tok) * (p.N / 2) + 8 * rt + g;
+            p.out[o] = gv;
+            __nv_bfloat16 hi, lo;
+            split_hl(gv, hi, lo);
+            p.xhl_out[o] = hi;
+            p.xhl_out[plane_out + o] = lo;
+          }
         } else {  // lm_head
           if (row < p.N && tok < p.B && p.out) p.out[static_cast<size_t>(tok) * p.N + row] = y[i][n][e];
         }
@@ -348,16 +398,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemm_tc(GemmParams p) {
 
 namespace {
 
-template <int WF, int NY, int TPW, int IN, int EPI>
+template <int WF, int NY, int TPW, int WARPS, int IN, int EPI>
 cudaError_t launch_t(const LaunchCtx& c, const GemmParams& p, bool prepare) {
-  auto kern = k_gemm_tc<WF, NY, TPW, IN, EPI>;
+  auto kern = k_gemm_tc<WF, NY, TPW, WARPS, IN, EPI>;
   const size_t smem = gemm_tc_smem_bytes(WF, NY, p.KC);
   if (prepare) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   const int n_rt = p.Npad / 16;
-  const int per_blk = kWarps * TPW;
+  const int per_blk = WARPS * TPW;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((n_rt + per_blk - 1) / per_blk, p.S);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3(WARPS * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
@@ -368,24 +418,27 @@ cudaError_t launch_t(const LaunchCtx& c, const GemmParams& p, bool prepare) {
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int WF, int NY, int TPW>
+template <int WF, int NY, int TPW, int WARPS>
 cudaError_t dispatch_epi(const LaunchCtx& c, const GemmParams& p, int in_mode, int epi, bool prepare) {
-  if (in_mode == kInNorm && epi == kEpiStore) return launch_t<WF, NY, TPW, kInNorm, kEpiStore>(c, p, prepare);
-  if (in_mode == kInPlain && epi == kEpiResid) return launch_t<WF, NY, TPW, kInPlain, kEpiResid>(c, p, prepare);
-  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_t<WF, NY, TPW, kInNorm, kEpiSwiglu>(c, p, prepare);
-  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_t<WF, NY, TPW, kInNorm, kEpiLmHead>(c, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiStore) return launch_t<WF, NY, TPW, WARPS, kInNorm, kEpiStore>(c, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiResid) return launch_t<WF, NY, TPW, WARPS, kInPlain, kEpiResid>(c, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_t<WF, NY, TPW, WARPS, kInNorm, kEpiSwiglu>(c, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_t<WF, NY, TPW, WARPS, kInNorm, kEpiLmHead>(c, p, prepare);
   return cudaErrorInvalidValue;
 }
 
+// Tile shapes: bf16 - 8 warps of one 16-row tile (128 rows per CTA); 4-bit - 8 warps
+// of two tiles up to 16 tokens, 16 warps of one tile for 17..32 tokens (256 rows
+// share each staged chunk of activations).
 cudaError_t dispatch(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi, bool prepare) {
   const int ny = gemm_tc_ny(wfmt, p.B);
   if (wfmt == kWBf16) {
-    if (ny == 1) return dispatch_epi<kWBf16, 1, 1>(c, p, in_mode, epi, prepare);
-    if (ny == 2) return dispatch_epi<kWBf16, 2, 1>(c, p, in_mode, epi, prepare);
+    if (ny == 1) return dispatch_epi<kWBf16, 1, 1, 8>(c, p, in_mode, epi, prepare);
+    if (ny == 2) return dispatch_epi<kWBf16, 2, 1, 8>(c, p, in_mode, epi, prepare);
   } else {
-    if (ny == 1) return dispatch_epi<kWQ4, 1, 2>(c, p, in_mode, epi, prepare);
-    if (ny == 2) return dispatch_epi<kWQ4, 2, 2>(c, p, in_mode, epi, prepare);
-    if (ny == 4) return dispatch_epi<kWQ4, 4, 1>(c, p, in_mode, epi, prepare);
+    if (ny == 1) return dispatch_epi<kWQ4, 1, 2, 8>(c, p, in_mode, epi, prepare);
+    if (ny == 2) return dispatch_epi<kWQ4, 2, 2, 8>(c, p, in_mode, epi, prepare);
+    if (ny == 4) return dispatch_epi<kWQ4, 4, 1, 16>(c, p, in_mode, epi, prepare);
   }
   return cudaErrorInvalidValue;
 }
@@ -398,7 +451,9 @@ int gemm_tc_ny(int wfmt, int batch) {
   return ny <= 1 ? 1 : ny <= 2 ? 2 : ny <= 4 ? 4 : 0;
 }
 
-int gemm_tc_rows_per_block(int wfmt, int ny) { return kWarps * 16 * (wfmt == kWQ4 && ny <= 2 ? 2 : 1); }
+int gemm_tc_rows_per_block(int wfmt, int) { return wfmt == kWQ4 ? 256 : 128; }
+
+int gemm_tc_chunk(int ny) { return ny == 1 ? 1024 : 512; }
 
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi) {
   return dispatch(c, p, wfmt, in_mode, epi, false);

@@ -37,6 +37,17 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
     dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     p.sumsq[static_cast<size_t>(b) * ngroups + gidx] = ss;
+    if (p.xhl_out) {  // batched path: the first projection's input h * in_norm as hi + lo planes
+      const size_t plane = static_cast<size_t>(gridDim.x) * p.H;
+      __nv_bfloat16* hi = p.xhl_out + static_cast<size_t>(b) * p.H + gidx * kResGroup;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float u = v[i] * __bfloat162float(p.norm_w0[gidx * kResGroup + i]);
+        const __nv_bfloat16 uh = __float2bfloat16_rn(u);
+        hi[i] = uh;
+        hi[plane + i] = __float2bfloat16_rn(u - __bfloat162float(uh));
+      }
+    }
   }
   for (int i = threadIdx.x; i < p.half_d; i += blockDim.x) {
     double ang = static_cast<double>(pos) * p.inv_freq[i];
