@@ -230,6 +230,17 @@ DEC_API dec_status dec_debug_step_prefix(dec_handle *h, const int32_t *token_ids
                                          dec_stream_t stream, int n_launches);
 DEC_API dec_status dec_debug_buffer(dec_handle *h, int which, void *dst, size_t bytes, dec_stream_t stream);
 
+/* Test hook: with stamps != NULL, every kernel of later steps records %globaltimer
+   values (nanoseconds) in stamps[3 i + 0..2] for launch i of the step (same order
+   as dec_debug_step_prefix): 0 = first CTA started (atomic min), 1 = first CTA past
+   its wait for the previous kernel (min), 2 = last CTA finished (max).  The caller
+   owns the device buffer (3 * dec_launches_per_step() entries) and resets it to
+   (~0, ~0, 0) triples before a step.  NULL turns the stamps off.  The step graph
+   is re-captured on the next dec_step.  The stamps exist only in a library built
+   with DEC_TIMELINE=1 (they cost the GEMV kernels registers); elsewhere a non-NULL
+   `stamps` returns DEC_ERR_UNSUPPORTED. */
+DEC_API dec_status dec_set_timeline(dec_handle *h, unsigned long long *stamps);
+
 /* dec_attention without a workspace: same arguments, same computation and same
    result as dec_attention, but it allocates nothing and takes no scratch from the
    caller.  The pages have no counterpart; it exists for callers that cannot call

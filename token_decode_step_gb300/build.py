@@ -43,8 +43,19 @@ def _stale(obj: pathlib.Path, src: pathlib.Path) -> bool:
 
 
 def build(verbose: bool = False, force: bool = False, extra: list[str] | None = None) -> pathlib.Path:
+    """Compile every stale translation unit and link libdec.so.
+
+    DEC_TIMELINE=1 in the environment compiles in the per-launch %globaltimer
+    stamps of dec_set_timeline.  A change of flags rebuilds everything.
+    """
     BUILD.mkdir(exist_ok=True)
-    extra = extra or []
+    extra = list(extra or [])
+    if os.environ.get("DEC_TIMELINE", "0") == "1":
+        extra.append("-DDEC_TIMELINE=1")
+    stamp = BUILD / "flags.txt"
+    flags = " ".join(ARCH + FLAGS + extra)
+    if not stamp.exists() or stamp.read_text() != flags:
+        force = True
     cmds = []
     objs = []
     for src in sources():
@@ -67,6 +78,7 @@ def build(verbose: bool = False, force: bool = False, extra: list[str] | None = 
         tmp = LIB.with_suffix(".so.tmp")
         run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", str(tmp), *map(str, objs)])
         os.replace(tmp, LIB)
+    stamp.write_text(flags)
     return LIB
 
 

@@ -121,6 +121,8 @@ struct dec_handle {
   std::vector<cudaEvent_t> events;
   // debug: stop an eager step after this many launches (-1: no limit)
   int launch_limit = -1;
+  // debug: per-launch %globaltimer stamps (device, 3 per launch) or null
+  unsigned long long* timeline = nullptr;
 };
 
 namespace {
@@ -201,12 +203,13 @@ dec_status check_linear(const dec_linear& l, int fmt, const char* name, int laye
   return DEC_OK;
 }
 
-// K splits of a batch-1 GEMV: enough CTAs to cover the SMs several times.
+// K splits of a batch-1 GEMV: split only while there are fewer CTAs than SMs (every
+// split costs a round trip through the partial sums).
 int choose_splits(int N, int K, int fmt, int num_sms) {
   const int cols = fmt == DEC_W_BF16 ? 8 : 32;
   const int tiles = (N + kGemvRows - 1) / kGemvRows;
   int S = 1;
-  while (static_cast<long long>(tiles) * S < 4ll * num_sms) {
+  while (static_cast<long long>(tiles) * S < num_sms) {
     const int S2 = S * 2;
     if (K % S2 != 0) break;
     const int KS = K / S2;
@@ -284,6 +287,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.status = h->status;
   ep.norm_w0 = h->layers[0].in_norm;
   ep.xhl_out = c.batch > 1 ? h->xh_u : nullptr;
+  ep.tl = Timeline{h->timeline, 0};
   ep.V = c.vocab;
   ep.H = H;
   ep.half_d = d / 2;
@@ -321,6 +325,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     gp.counters = h->gemv_counters;
     gp.amax_key = h->amax_key;
     gp.argmax_out = sp.argmax;
+    gp.tl = Timeline{h->timeline, launched - 1};
     note(cls);
     ev_begin();
     dec_status s2;
@@ -348,6 +353,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       tp.counters = h->gemv_counters;
       tp.amax_key = h->amax_key;
       tp.argmax_out = sp.argmax;
+      tp.tl = gp.tl;
       s2 = check(launch_gemm_tc(lc, tp, h->wfmt, in_mode, epi), what);
     }
     ev_end();
@@ -378,6 +384,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.out_hl = c.batch > 1 ? h->xh_o : nullptr;
     if (limit_hit()) return DEC_OK;
     ++launched;
+    ap.tl = Timeline{h->timeline, launched - 1};
     note(DEC_K_ATTN);
     ev_begin();
     if ((st = check(launch_attention(lc, ap, d), "attention")) != DEC_OK) return st;
@@ -953,5 +960,21 @@ extern "C" dec_status dec_debug_buffer(dec_handle* h, int which, void* dst, size
     return DEC_ERR_INVALID_ARG;
   }
   DEC_CUDA(cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_set_timeline(dec_handle* h, unsigned long long* stamps) {
+  if (!h) {
+    set_err("handle is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+#if !(defined(DEC_TIMELINE) && DEC_TIMELINE)
+  if (stamps) {
+    set_err("timeline stamps are compiled in only when the library is built with DEC_TIMELINE=1");
+    return DEC_ERR_UNSUPPORTED;
+  }
+#endif
+  h->timeline = stamps;
+  drop_graph(h);  // the next step captures the kernels with the new pointer
   return DEC_OK;
 }

@@ -28,8 +28,16 @@ enum WFmt : int { kWBf16 = 0, kWQ4 = 1 };
 
 // ---------------------------------------------------------------- kernel params
 
+// Test hook: %globaltimer stamps of one launch in buf[3 idx ..]: 0 = first CTA start
+// (atomic min), 1 = first CTA past the grid-dependency wait (min), 2 = last CTA end (max).
+struct Timeline {
+  unsigned long long* buf;
+  int idx;
+};
+
 // Batch-1 GEMV: y = W x over a row tile (kGemvRows rows) and one K split.
 struct GemvParams {
+  Timeline tl;
   const void* w;            // bf16 [N][K] or q4 words uint32 [N][K/8]
   const uint32_t* sb;       // q4: scale (low 16 bits) | bias (high 16 bits), [N][K/64]
   int N, K, S, KS;          // rows, inputs, K splits, inputs per split
@@ -50,6 +58,7 @@ struct GemvParams {
 
 // Batched (B >= 2) projection on tensor cores over fragment-packed weight tiles.
 struct GemmParams {
+  Timeline tl;
   const void* w;            // packed tiles (see k_gemm_tc.cu)
   int N, Npad, K, S, KS, KC, B;  // rows, rows padded to 16, inputs, K splits, inputs per split,
                                  // inputs staged at once (divides KS), tokens
@@ -69,6 +78,7 @@ struct GemmParams {
 
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
 struct AttnParams {
+  Timeline tl;
   const float* qkv;             // [B][(nq + 2 nkv) d] projections
   const __nv_bfloat16* q_norm;  // [d]
   const __nv_bfloat16* k_norm;  // [d]
@@ -83,6 +93,7 @@ struct AttnParams {
 };
 
 struct EmbedParams {
+  Timeline tl;
   const __nv_bfloat16* embed;   // [V][H]
   const int32_t* tokens;
   const int32_t* positions;
@@ -101,6 +112,25 @@ struct EmbedParams {
 
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Compiled in only when the library is built with DEC_TIMELINE=1: the stamps keep a
+// predicate and a pointer live across the weight loop and cost the batch-1 GEMV 16
+// registers, so the default build leaves them out.
+__device__ __forceinline__ void tl_mark(const Timeline& tl, int slot) {
+#if defined(DEC_TIMELINE) && DEC_TIMELINE
+  if (tl.buf && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (slot == 2)
+      atomicMax(tl.buf + 3 * tl.idx + 2, t);
+    else
+      atomicMin(tl.buf + 3 * tl.idx + slot, t);
+  }
+#else
+  (void)tl;
+  (void)slot;
+#endif
 }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

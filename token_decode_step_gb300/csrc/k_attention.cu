@@ -33,7 +33,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct AttnCfg {
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = D == 128 ? 3 : 4;  // two CTAs per SM (6 stages measured slower when batched)
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kAttnTile * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;                  // K tile then V tile
@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   constexpr int S = CF::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
 
+  tl_mark(p.tl, 0);
   const int h = blockIdx.y, b = blockIdx.z;
   const int rank = static_cast<int>(cluster_ctarank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   }
 
   griddep_wait();
+  tl_mark(p.tl, 1);
   __syncthreads();
 
   float m_run = -INFINITY, l_run = 0.f;
@@ -409,6 +411,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     }
   }
   cluster_sync();  // no CTA leaves while others may still read its shared memory
+  tl_mark(p.tl, 2);
 }
 
 namespace {

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
 #pragma unroll
   for (int i = 0; i < TPW; ++i) valid[i] = (rt0 + i) < n_rt;
 
+  tl_mark(p.tl, 0);
   {  // rows of absent tokens (and their lo rows) stay zero in both buffers
     uint4* z = reinterpret_cast<uint4*>(smem);
     const int nz = static_cast<int>(2 * buf_elems * 2 / 16);
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
     if (j < nunits) load_unit(j, ring[j]);
 
   griddep_wait();
+  tl_mark(p.tl, 1);
 
   if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (fused RMSNorm)
     for (int b = warp; b < p.B; b += WARPS) {
@@ -282,7 +284,10 @@ __global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
     __syncthreads();
     if (tid == 0) s_ticket = atomicAdd(&p.counters[rb], 1u);
     __syncthreads();
-    if (s_ticket != static_cast<unsigned>(p.S - 1)) return;
+    if (s_ticket != static_cast<unsigned>(p.S - 1)) {
+      tl_mark(p.tl, 2);
+      return;
+    }
     __threadfence();
 #pragma unroll
     for (int i = 0; i < TPW; ++i) {
@@ -381,6 +386,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
       }
     }
   }
+  tl_mark(p.tl, 2);
   if constexpr (EPI == kEpiLmHead) {
     __threadfence();
     __syncthreads();

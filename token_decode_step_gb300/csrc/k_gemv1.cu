@@ -39,7 +39,7 @@ __device__ __forceinline__ const void* chunk_ptr(const GemvParams& p, int row, i
   }
 }
 
-// Input chunk: x[col .. col + n) as floats, normalised if requested.
+// Input chunk: x[col .. col + n) as floats, normalised (RMSNorm of the residual) if requested.
 template <int IN, int N>
 __device__ __forceinline__ void load_x(const GemvParams& p, int col, float inv_rms, float (&xv)[N]) {
   const float4* src = reinterpret_cast<const float4*>(p.x + col);
@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = 0.f;
 
+  tl_mark(p.tl, 0);
   // First chunk's weights: independent of upstream kernels, so fetched before the wait.
   uint4 wreg[R];
   int c = tid;
@@ -125,8 +126,15 @@ __global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
 #pragma unroll
     for (int r = 0; r < R; ++r) wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + c * CH));
   }
+  // Residual rows of this tile: last written two or more kernels upstream, which
+  // completed before the previous kernel could pass its own wait and start this one.
+  float h_pre = 0.f;
+  if constexpr (EPI == kEpiResid) {
+    if (tid < R) h_pre = __ldcg(p.out + row0 + tid);
+  }
 
   griddep_wait();
+  tl_mark(p.tl, 1);
 
   float inv_rms = 1.f;
   if constexpr (IN == kInNorm) {
@@ -197,7 +205,10 @@ __global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
     __syncthreads();
     if (tid == 0) s_ticket = atomicAdd(&p.counters[tile], 1u);
     __syncthreads();
-    if (s_ticket != static_cast<unsigned>(p.S - 1)) return;
+    if (s_ticket != static_cast<unsigned>(p.S - 1)) {
+      tl_mark(p.tl, 2);
+      return;
+    }
     __threadfence();
     if (tid < R && tid < nrows) {
       float t = 0.f;
@@ -208,38 +219,49 @@ __global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
   }
   __syncthreads();
 
-  if (tid != 0) return;
+  // epilogue: lane r of warp 0 owns row row0 + r
+  if (warp != 0) return;
+  const bool mine = lane < R;
+  const float y = mine ? ys[lane] : 0.f;
   if constexpr (EPI == kEpiStore) {
-    for (int r = 0; r < nrows; ++r) p.out[row0 + r] = ys[r];
+    if (lane < nrows) p.out[row0 + lane] = y;
   } else if constexpr (EPI == kEpiResid) {
-    float ss = 0.f;
-    for (int r = 0; r < R; ++r) {
-      float hn = p.out[row0 + r] + ys[r];
-      p.out[row0 + r] = hn;
-      ss = fmaf(hn, hn, ss);
+    float hn = 0.f;
+    if (mine) {
+      hn = h_pre + y;
+      p.out[row0 + lane] = hn;
     }
-    p.sumsq_out[tile] = ss;
+    float ss = hn * hn;  // the tile's 8 rows are one group of the norm's sums of squares
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    if (lane == 0) p.sumsq_out[tile] = ss;
   } else if constexpr (EPI == kEpiSwiglu) {
     // rows 0..3: gate of outputs 4 tile + i; rows 4..7: up of the same outputs
-    for (int i = 0; i < R / 2; ++i) p.out[tile * (R / 2) + i] = silu_f(ys[i]) * ys[R / 2 + i];
+    const float up = __shfl_down_sync(0xffffffffu, y, R / 2);
+    if (lane < R / 2) p.out[tile * (R / 2) + lane] = silu_f(y) * up;
   } else {  // lm_head tile
-    unsigned long long best = 0ull;
-    for (int r = 0; r < nrows; ++r) {
-      if (p.out) p.out[row0 + r] = ys[r];
-      unsigned long long k = argmax_key(ys[r], row0 + r);
-      best = k > best ? k : best;
+    if (lane < nrows && p.out) p.out[row0 + lane] = y;
+    unsigned long long k = lane < nrows ? argmax_key(y, row0 + lane) : 0ull;
+#pragma unroll
+    for (int o = 1; o < R; o <<= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+      k = other > k ? other : k;
     }
-    atomicMax(p.amax_key, best);
-    __threadfence();
-    const unsigned ntiles = gridDim.x;
-    unsigned done = atomicAdd(&p.counters[ntiles], 1u);
-    if (done == ntiles - 1) {
+    if (lane == 0) {
+      atomicMax(p.amax_key, k);
       __threadfence();
-      unsigned long long k = atomicOr(p.amax_key, 0ull);
-      *p.argmax_out = argmax_key_index(k);
-      p.counters[ntiles] = 0u;
+      const unsigned ntiles = gridDim.x;
+      const unsigned done = atomicAdd(&p.counters[ntiles], 1u);
+      if (done == ntiles - 1) {
+        __threadfence();
+        const unsigned long long best = atomicOr(p.amax_key, 0ull);
+        *p.argmax_out = argmax_key_index(best);
+        p.counters[ntiles] = 0u;
+      }
     }
   }
+  if (lane == 0) tl_mark(p.tl, 2);
 }
 
 template <int WF, int IN, int EPI>

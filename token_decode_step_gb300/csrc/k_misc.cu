@@ -11,7 +11,9 @@ namespace dec {
 // RMSNorm), the (cos, sin) table of this step's RoPE angles pos * theta^(-2i/d)
 // evaluated in double precision, reset of the argmax key, and range checks.
 __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
+  tl_mark(p.tl, 0);
   griddep_wait();  // first kernel of a step: nothing upstream inside the graph
+  tl_mark(p.tl, 1);
   const int b = blockIdx.x;
   int tok = p.tokens[b];
   int pos = p.positions[b];
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   }
   if (threadIdx.x == 0) p.amax_key[b] = 0ull;
   griddep_launch_dependents();
+  tl_mark(p.tl, 2);
 }
 
 cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B) {

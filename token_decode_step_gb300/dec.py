@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "dec_launches_per_step": (ctypes.c_int, [vp]),
         "dec_debug_step_prefix": (ctypes.c_int, [vp, i32p, i32p, vp, vp, i32p, vp, ctypes.c_int]),
         "dec_debug_buffer": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_size_t, vp]),
+        "dec_set_timeline": (ctypes.c_int, [vp, vp]),
         "dec_attention_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecConfig)]),
         "dec_attention": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp, vp,
                                          ctypes.c_size_t, vp]),
@@ -194,3 +195,7 @@ def dec_debug_step_prefix(h: int, token_ids: int, positions: int, kv_cache: int,
 
 def dec_debug_buffer(h: int, which: int, dst: int, nbytes: int, stream: int = 0) -> int:
     return _check(lib.dec_debug_buffer(h, which, dst, nbytes, stream), "dec_debug_buffer")
+
+
+def dec_set_timeline(h: int, stamps: int | None) -> int:
+    return _check(lib.dec_set_timeline(h, stamps), "dec_set_timeline")
