@@ -53,6 +53,10 @@ CASES = [
     (2, 32, 8, 128, [4095, 513], 4160),
     (4, 4, 4, 128, [2000, 1, 64, 127], 2080),
     (2, 8, 4, 64, [8191, 3], 8224),
+    # more (sequence, KV head) pairs than fit one CTA per SM in clusters of 8: the
+    # shallow two-CTAs-per-SM ring
+    (6, 16, 4, 128, [1500, 0, 63, 64, 777, 1200], 1536),
+    (12, 4, 2, 64, [5, 300, 17, 1000, 64, 129, 2, 999, 640, 31, 1023, 256], 1024),
 ]
 
 

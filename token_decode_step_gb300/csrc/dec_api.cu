@@ -86,6 +86,9 @@ struct dec_handle {
   int device = 0;
   int num_sms = 0;
   int wfmt = 0;
+  // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
+  // layer's K/V at max_ctx takes at most a quarter of L2)
+  bool kv_prefetch = false;
   // packed weights (one allocation)
   unsigned char* wmem = nullptr;
   size_t wbytes = 0;
@@ -301,6 +304,11 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   int launched = 1;  // the embedding kernel
   auto limit_hit = [&]() { return h->launch_limit >= 0 && launched >= h->launch_limit; };
   if (limit_hit()) return DEC_OK;
+  // the K/V prefetch of the next GEMV launch (set around the QKV projection only)
+  struct {
+    const unsigned char* kv = nullptr;
+    unsigned long long plane_bytes = 0;
+  } kv_pf;
   // x, norm_w: the batch-1 input; xin, xout, next_norm: the batched path's hi/lo planes
   auto gemv = [&](const PackedLinear& L, int in_mode, int epi, const float* x, const __nv_bfloat16* norm_w,
                   float* out, int cls, const char* what, const __nv_bfloat16* xin, __nv_bfloat16* xout,
@@ -326,6 +334,16 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     gp.amax_key = h->amax_key;
     gp.argmax_out = sp.argmax;
     gp.tl = Timeline{h->timeline, launched - 1};
+    if (kv_pf.kv) {
+      gp.pf_kv = kv_pf.kv;
+      gp.pf_positions = sp.positions;
+      gp.pf_plane_bytes = kv_pf.plane_bytes;
+      gp.pf_head_bytes = static_cast<unsigned long long>(c.max_ctx) * d * 2;
+      gp.pf_B = c.batch;
+      gp.pf_nkv = c.n_kv_heads;
+      gp.pf_row_bytes = d * 2;
+      gp.pf_max_ctx = c.max_ctx;
+    }
     note(cls);
     ev_begin();
     dec_status s2;
@@ -362,9 +380,15 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
 
   for (int l = 0; l < c.n_layers; ++l) {
     const PackedLayer& L = h->layers[l];
+    if (h->kv_prefetch) {
+      const unsigned long long plane = static_cast<unsigned long long>(c.batch) * c.n_kv_heads * c.max_ctx * d * 2;
+      kv_pf.kv = static_cast<const unsigned char*>(sp.kv) + 2ull * l * plane;
+      kv_pf.plane_bytes = plane;
+    }
     if ((st = gemv(L.qkv, kInNorm, kEpiStore, h->h, L.in_norm, h->qkv, DEC_K_QKV, "qkv", h->xh_u, nullptr,
                    nullptr)) != DEC_OK)
       return st;
+    kv_pf.kv = nullptr;
 
     AttnParams ap{};
     ap.qkv = h->qkv;
@@ -506,6 +530,13 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     return fail("cudaDeviceGetAttribute", e);
   if ((e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking)) != cudaSuccess)
     return fail("cudaStreamCreate", e);
+  {
+    int l2 = 0;
+    if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device)) != cudaSuccess)
+      return fail("cudaDeviceGetAttribute", e);
+    const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim * 2;
+    h->kv_prefetch = c.batch == 1 && kv_layer <= l2 / 4.0;
+  }
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;

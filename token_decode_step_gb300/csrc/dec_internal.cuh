@@ -16,7 +16,6 @@ constexpr int kResGroup = 8;        // rows per partial sum-of-squares of the re
 constexpr int kGemvRows = 8;        // rows per CTA of the batch-1 GEMV
 constexpr int kAttnTile = 64;       // positions per attention smem tile
 constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
-constexpr int kAttnCluster = 8;     // CTAs per (sequence, KV head): one thread-block cluster
 constexpr int kGroup = 64;          // affine 4-bit group size
 constexpr int kGemmPrefetch = 4;    // 64-input weight units in flight per lane (batched path)
 
@@ -54,6 +53,12 @@ struct GemvParams {
   unsigned* counters;       // [N / kGemvRows] (+1 for lmhead) zero on entry, left zero
   unsigned long long* amax_key;  // lmhead: packed (ordered value, ~index)
   int32_t* argmax_out;      // lmhead
+  // Optional L2 prefetch of the cached K/V rows (positions 0..P-1) that the next
+  // attention kernel reads: the CTAs split them into contiguous byte ranges.
+  const unsigned char* pf_kv;     // this layer's K plane, V plane at + pf_plane_bytes; null: off
+  const int32_t* pf_positions;    // [pf_B] cached positions P per sequence
+  unsigned long long pf_plane_bytes, pf_head_bytes;  // one plane of a layer; one (sequence, head) run
+  int pf_B, pf_nkv, pf_row_bytes, pf_max_ctx;
 };
 
 // Batched (B >= 2) projection on tensor cores over fragment-packed weight tiles.
@@ -132,6 +137,11 @@ __device__ __forceinline__ void tl_mark(const Timeline& tl, int slot) {
   (void)slot;
 #endif
 }
+// Bulk prefetch of [src, src + bytes) into L2 (src and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -12,17 +12,21 @@
 //
 // Grid (C, n_kv, B) in thread-block clusters of C CTAs along x: the cluster of
 // (sequence b, KV head h) splits that sequence's T = P+1 positions into C equal
-// runs of whole 64-position tiles (so ragged batches stay balanced), CTA r takes
-// run r.  Each CTA streams its K/V tiles into shared memory with cp.async
-// through a ring of S stages (XOR-swizzled 16-byte chunks so ldmatrix is
+// runs (multiples of 16 positions, so ragged batches stay balanced), CTA r takes
+// run r.  Each CTA streams its K/V tiles of 64 positions into shared memory with
+// cp.async through a ring of S stages (XOR-swizzled 16-byte chunks so ldmatrix is
 // conflict-free; the first S-1 tiles are requested before the grid-dependency
-// wait) and runs both products on tensor cores (mma.sync m16n8k16, bf16 in, fp32
+// wait, which for small batches is the whole run) and runs both products on
+// tensor cores (mma.sync m16n8k16, bf16 in, fp32
 // accumulate): the group's G query heads share every K/V row.  q and the
 // probabilities enter as bf16 hi + lo rows (rows 0..G-1 and G..2G-1 of the
 // 16-row A operand), ~16 significant bits; softmax statistics are fp32 in the
 // exp2 domain.  The C partial results are merged through distributed shared
-// memory between two cluster barriers: CTA r combines a 1/C slice of the
-// outputs from all C CTAs (no global partials, no atomics).
+// memory: every CTA stores its share of CTA r's 1/C slice of the outputs into CTA r's
+// shared memory, one cluster barrier, then CTA r combines the slice (no global
+// partials, no atomics, no remote loads).
+#include <mutex>
+
 #include "dec_internal.cuh"
 
 namespace dec {
@@ -31,17 +35,23 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// Two shapes of the stage ring: shallow (about 100 KB, two CTAs per SM, for grids
+// above the SM count; deeper rings measured slower there) and deep (about 200 KB, one
+// CTA per SM, for grids that fit on the SMs at once: up to 5 or 11 tiles are in
+// flight before the wait).
+template <int D, bool DEEP>
 struct AttnCfg {
-  static constexpr int kStages = D == 128 ? 3 : 4;  // two CTAs per SM (6 stages measured slower when batched)
+  static constexpr int kStages = DEEP ? (D == 128 ? 6 : 12) : (D == 128 ? 3 : 4);
   static constexpr int kRowBytes = D * 2;
   static constexpr int kTileBytes = kAttnTile * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;                  // K tile then V tile
   static constexpr int kOffQ = 0;                                      // [16][D] bf16
   static constexpr int kOffStages = 16 * kRowBytes;
   static constexpr int kOffNew = kOffStages + kStages * kStageBytes;  // new k row, new v row
-  static constexpr int kOffXchg = kOffNew + 2 * kRowBytes;             // [G][D + 2] floats (G <= 4)
-  static constexpr int kOffMisc = kOffXchg + 4 * (D + 2) * 4;          // [4][G] floats
+  // cluster merge receive area: up to 16 records of (m[G], l[G], acc[ceil(G D / C)]), G <= 4
+  static constexpr int kXchgFloats = 16 * 2 * 4 + 4 * D + 16;
+  static constexpr int kOffXchg = kOffNew + 2 * kRowBytes;
+  static constexpr int kOffMisc = kOffXchg + kXchgFloats * 4;          // [4][G] floats
   static constexpr int kBytes = kOffMisc + 64 * 4;
 };
 
@@ -70,6 +80,13 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// split form: arrive early without ordering memory, wait before the first remote access
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -83,17 +100,16 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) 
   return r;
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Positions [begin, end) of CTA `rank` of a cluster of C for a sequence with T = P + 1
-// positions: runs of ceil(ceil(T / C) / 64) whole tiles; later CTAs may get none.
+// positions: runs of ceil(T / C) rounded up to 16 positions; later CTAs may get fewer
+// or none.
 __device__ __forceinline__ void attention_run(int T, int C, int rank, int* begin, int* end) {
   const int per = (T + C - 1) / C;
-  const int len = (per + kAttnTile - 1) / kAttnTile * kAttnTile;
+  const int len = (per + 15) / 16 * 16;
   const int b0 = rank * len;
   *begin = b0 < T ? b0 : T;
   *end = b0 + len < T ? b0 + len : T;
@@ -101,15 +117,18 @@ __device__ __forceinline__ void attention_run(int T, int C, int rank, int* begin
 
 }  // namespace
 
-template <int D, int G, int C>
+template <int D, int G, int C, bool DEEP>
 __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
-  using CF = AttnCfg<D>;
+  using CF = AttnCfg<D, DEEP>;
   constexpr int S = CF::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
 
   tl_mark(p.tl, 0);
   const int h = blockIdx.y, b = blockIdx.z;
   const int rank = static_cast<int>(cluster_ctarank());
+  // The merge writes into the other CTAs' shared memory: first barrier phase, completed
+  // before the first remote store, so every CTA of the cluster is known to be running.
+  cluster_arrive_relaxed();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
@@ -128,7 +147,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
 
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sStages = s_base + CF::kOffStages;
-  float* xchg = reinterpret_cast<float*>(smem + CF::kOffXchg);  // this CTA's [G][m, l, acc[D]]
+  float* xchg = reinterpret_cast<float*>(smem + CF::kOffXchg);  // receive area of the cluster merge
   float* misc = reinterpret_cast<float*>(smem + CF::kOffMisc);
 
   // Cached K/V tiles do not depend on upstream kernels of this step: request the
@@ -146,6 +165,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     uint32_t* q32 = reinterpret_cast<uint32_t*>(smem + CF::kOffQ);
     for (int i = tid; i < 16 * D / 2; i += kAttnThreads) q32[i] = 0u;
   }
+  // Norm weights and this sequence's RoPE factors (written by the embedding kernel,
+  // two or more launches upstream) do not depend on the previous kernel either.
+  constexpr int E = D / 32;  // elements per lane: lane + 32 m
+  float wq[E], wk[E];
+  float2 cs[E / 2];
+#pragma unroll
+  for (int m = 0; m < E; ++m) {
+    wq[m] = bf16_to_f(p.q_norm[lane + 32 * m]);
+    wk[m] = bf16_to_f(p.k_norm[lane + 32 * m]);
+  }
+  {
+    const float2* rope_b = p.rope + static_cast<size_t>(b) * (D / 2);
+#pragma unroll
+    for (int m = 0; m < E / 2; ++m) cs[m] = rope_b[lane + 32 * m];
+  }
 
   griddep_wait();
   tl_mark(p.tl, 1);
@@ -160,32 +194,44 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     // ---- q/k per-head RMSNorm + RoPE (+ KV append by the CTA holding slot P)
     const int nqkv = (p.nq + 2 * p.nkv) * D;
     const float* qkv_b = p.qkv + static_cast<size_t>(b) * nqkv;
-    const float2* rope_b = p.rope + static_cast<size_t>(b) * (D / 2);
-    constexpr int E = D / 32;  // elements per lane: lane + 32 m
-    auto norm_rope = [&](const float* src, const __nv_bfloat16* wn, float (&y)[E]) {
-      float x[E];
-      float ss = 0.f;
+    // rows of this step's q (warps < G, one head each) and, in the CTA holding slot P,
+    // the new k and v (warp kvw); all loads are issued before any arithmetic
+    constexpr int kvw = G < 4 ? G : 3;
+    const bool do_q = warp < G, do_kv = has_new && warp == kvw;
+    float xq[E], xk[E], xv[E];
+    if (do_q) {
+      const float* src = qkv_b + (h * G + warp) * D;
+#pragma unroll
+      for (int m = 0; m < E; ++m) xq[m] = src[lane + 32 * m];
+    }
+    if (do_kv) {
+      const float* ksrc = qkv_b + p.nq * D + h * D;
+      const float* vsrc = qkv_b + (p.nq + p.nkv) * D + h * D;
 #pragma unroll
       for (int m = 0; m < E; ++m) {
-        x[m] = src[lane + 32 * m];
-        ss = fmaf(x[m], x[m], ss);
+        xk[m] = ksrc[lane + 32 * m];
+        xv[m] = vsrc[lane + 32 * m];
       }
+    }
+    auto norm_rope = [&](float (&x)[E], const float (&wn)[E], float (&y)[E]) {
+      float ss = 0.f;
+#pragma unroll
+      for (int m = 0; m < E; ++m) ss = fmaf(x[m], x[m], ss);
       ss = warp_sum(ss);
       const float inv = rsqrtf(ss / static_cast<float>(D) + p.eps);
 #pragma unroll
-      for (int m = 0; m < E; ++m) x[m] = (x[m] * inv) * bf16_to_f(wn[lane + 32 * m]);
+      for (int m = 0; m < E; ++m) x[m] = (x[m] * inv) * wn[m];
       // pairs (e, e + D/2): lane's elements m and m + E/2
 #pragma unroll
       for (int m = 0; m < E / 2; ++m) {
-        const float2 cs = rope_b[lane + 32 * m];
         const float a = x[m], c = x[m + E / 2];
-        y[m] = a * cs.x - c * cs.y;
-        y[m + E / 2] = c * cs.x + a * cs.y;
+        y[m] = a * cs[m].x - c * cs[m].y;
+        y[m + E / 2] = c * cs[m].x + a * cs[m].y;
       }
     };
-    if (warp < G) {
+    if (do_q) {
       float y[E];
-      norm_rope(qkv_b + (h * G + warp) * D, p.q_norm, y);
+      norm_rope(xq, wq, y);
       __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(smem + CF::kOffQ);
 #pragma unroll
       for (int m = 0; m < E; ++m) {
@@ -195,17 +241,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
         q16[(G + warp) * D + lane + 32 * m] = lo;
       }
     }
-    if (has_new && warp == 3) {
+    if (do_kv) {
       float y[E];
-      norm_rope(qkv_b + p.nq * D + h * D, p.k_norm, y);
+      norm_rope(xk, wk, y);
       __nv_bfloat16* nk = reinterpret_cast<__nv_bfloat16*>(smem + CF::kOffNew);
       __nv_bfloat16* nv = nk + D;
-      const float* vsrc = qkv_b + (p.nq + p.nkv) * D + h * D;
 #pragma unroll
       for (int m = 0; m < E; ++m) {
         const int e = lane + 32 * m;
         const __nv_bfloat16 kk = __float2bfloat16_rn(y[m]);
-        const __nv_bfloat16 vv = __float2bfloat16_rn(vsrc[e]);
+        const __nv_bfloat16 vv = __float2bfloat16_rn(xv[m]);
         nk[e] = kk;
         nv[e] = vv;
         kbase[static_cast<size_t>(P) * D + e] = kk;
@@ -324,7 +369,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   }
   cp_async_wait<0>();
   __syncthreads();
-  griddep_launch_dependents();
 
   // ---- per-warp state -> this CTA's (m, l, acc) per head (rows g < G after adding the lo rows)
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -350,7 +394,17 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     }
   }
   __syncthreads();
+  // ---- cluster merge, pushed: CTA `rank` owns outputs [rank kPer, (rank + 1) kPer) of
+  // the G D; every CTA stores its (m, l) per head and its combined partial outputs of
+  // each owner's slice into the owner's receive area (record `rank`: m[G], l[G],
+  // acc[kPer]), then one cluster barrier, then each owner merges from its own memory.
+  constexpr int kOut = G * D;
+  constexpr int kPer = (kOut + C - 1) / C;
+  constexpr int kRec = 2 * G + kPer;
+  static_assert(C * kRec <= CF::kXchgFloats, "receive area too small");
+  const uint32_t recv_local = smem_u32(xchg);
   float* fw = misc;  // [4][G] warp weights
+  cluster_wait();
   if (tid < G) {
     float M = -INFINITY;
     for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * G + tid]);
@@ -360,45 +414,39 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
       fw[w * G + tid] = f;
       L += f * lw[w * G + tid];
     }
-    xchg[tid * (D + 2)] = M;
-    xchg[tid * (D + 2) + 1] = L;
+#pragma unroll 1
+    for (int r = 0; r < C; ++r) {
+      const uint32_t rec = map_rank(recv_local + (rank * kRec) * 4, static_cast<uint32_t>(r));
+      st_cluster_f32(rec + tid * 4, M);
+      st_cluster_f32(rec + (G + tid) * 4, L);
+    }
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += kAttnThreads) {
+  for (int i = tid; i < kOut; i += kAttnThreads) {
     const int j = i / D, e = i % D;
     float a = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) a += fw[w * G + j] * ow[(w * G + j) * D + e];
-    xchg[j * (D + 2) + 2 + e] = a;
+    const int owner = i / kPer;
+    const uint32_t rec = map_rank(recv_local + (rank * kRec) * 4, static_cast<uint32_t>(owner));
+    st_cluster_f32(rec + (2 * G + i - owner * kPer) * 4, a);
   }
-
-  // ---- cluster merge: CTA `rank` combines outputs [rank * n, (rank + 1) * n) of all C CTAs
   cluster_sync();
   {
-    constexpr int kOut = G * D;
-    constexpr int kPer = (kOut + C - 1) / C;
-    const uint32_t xa = smem_u32(xchg);
     float* out_b = p.out + static_cast<size_t>(b) * p.nq * D + h * G * D;
     const int i_end = (rank + 1) * kPer < kOut ? (rank + 1) * kPer : kOut;
     for (int i = rank * kPer + tid; i < i_end; i += kAttnThreads) {
-      const int j = i / D, e = i % D;
-      float mr[C], lr[C], ar[C];
-#pragma unroll
-      for (int r = 0; r < C; ++r) {
-        const uint32_t base = map_rank(xa, static_cast<uint32_t>(r));
-        mr[r] = ld_cluster_f32(base + (j * (D + 2)) * 4);
-        lr[r] = ld_cluster_f32(base + (j * (D + 2) + 1) * 4);
-        ar[r] = ld_cluster_f32(base + (j * (D + 2) + 2 + e) * 4);
-      }
+      const int j = i / D, k = i - rank * kPer;
       float M = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < C; ++r) M = fmaxf(M, mr[r]);
+      for (int r = 0; r < C; ++r) M = fmaxf(M, xchg[r * kRec + j]);
       float num = 0.f, den = 0.f;
 #pragma unroll
       for (int r = 0; r < C; ++r) {
-        const float f = (mr[r] == -INFINITY) ? 0.f : exp2f(mr[r] - M);
-        num = fmaf(f, ar[r], num);
-        den = fmaf(f, lr[r], den);
+        const float mr = xchg[r * kRec + j];
+        const float f = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+        num = fmaf(f, xchg[r * kRec + 2 * G + k], num);
+        den = fmaf(f, xchg[r * kRec + G + j], den);
       }
       const float ov = num / den;
       out_b[i] = ov;
@@ -410,61 +458,148 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
       }
     }
   }
-  cluster_sync();  // no CTA leaves while others may still read its shared memory
+  // no shared::cluster access follows the barrier: CTAs leave independently
+  // Dependents are released only now: when their CTAs start earlier, on the SMs this
+  // kernel runs on, their weight loads crowd the load/store pipe and the merge above
+  // measured several times slower.
+  griddep_launch_dependents();
   tl_mark(p.tl, 2);
 }
 
 namespace {
 
-template <int D, int G>
-cudaError_t launch_attn_t(const LaunchCtx& c, const AttnParams& p) {
-  constexpr int C = kAttnCluster;
+// Launch shapes: 0 = clusters of 8, shallow ring; 1 = clusters of 8, deep ring;
+// 2 = clusters of 16 (a non-portable size), deep ring.
+constexpr int kShapes = 3;
+
+template <int D, int G, int C, bool DEEP>
+cudaLaunchConfig_t attn_config(const AttnParams& p, cudaStream_t stream, bool pdl, cudaLaunchAttribute (&attr)[2]) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, p.nkv, p.B);
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = AttnCfg<D>::kBytes;
-  cfg.stream = c.stream;
-  cudaLaunchAttribute attr[2];
+  cfg.dynamicSmemBytes = AttnCfg<D, DEEP>::kBytes;
+  cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attention<D, G, C>, p);
+  return cfg;
+}
+
+template <int D, int G, int C, bool DEEP>
+cudaError_t launch_attn_t(const LaunchCtx& c, const AttnParams& p) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = attn_config<D, G, C, DEEP>(p, c.stream, c.pdl, attr);
+  return cudaLaunchKernelEx(&cfg, k_attention<D, G, C, DEEP>, p);
+}
+
+// Shared-memory limit (and the non-portable cluster size), then the number of
+// clusters of this shape that fit on the device at once.
+template <int D, int G, int C, bool DEEP>
+cudaError_t prepare_attn_t(int* max_clusters) {
+  auto kern = k_attention<D, G, C, DEEP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(AttnCfg<D, DEEP>::kBytes));
+  if (e != cudaSuccess) return e;
+  if (C > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+    return e;
+  AttnParams probe = {};
+  probe.B = 1;
+  probe.nkv = 1;
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = attn_config<D, G, C, DEEP>(probe, nullptr, false, attr);
+  cfg.numAttrs = 1;  // the cluster dimension only
+  return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
 }
 
 template <int D, int G>
-cudaError_t prepare_attn_t() {
-  return cudaFuncSetAttribute(k_attention<D, G, kAttnCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(AttnCfg<D>::kBytes));
+cudaError_t prepare_all(int (&max_clusters)[kShapes]) {
+  cudaError_t e;
+  if ((e = prepare_attn_t<D, G, 8, false>(&max_clusters[0])) != cudaSuccess) return e;
+  if ((e = prepare_attn_t<D, G, 8, true>(&max_clusters[1])) != cudaSuccess) return e;
+  return prepare_attn_t<D, G, 16, true>(&max_clusters[2]);
 }
+
+template <int D, int G>
+cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
+  if (shape == 2) return launch_attn_t<D, G, 16, true>(c, p);
+  if (shape == 1) return launch_attn_t<D, G, 8, true>(c, p);
+  return launch_attn_t<D, G, 8, false>(c, p);
+}
+
+// Per device and (head_dim, group): SM count and co-resident clusters per shape,
+// filled by prepare_attention (before any capture), read by launch_attention.
+constexpr int kMaxAttnDevices = 64;
+struct AttnCaps {
+  int num_sms = 0;
+  int max_clusters[kShapes] = {0, 0, 0};
+};
+AttnCaps g_caps[kMaxAttnDevices][2][3];
+std::mutex g_caps_mu;
+
+int dim_index(int head_dim) { return head_dim == 64 ? 0 : 1; }
+int group_index(int G) { return G == 1 ? 0 : G == 2 ? 1 : 2; }
 
 }  // namespace
 
 size_t attention_smem_bytes(int head_dim) {
-  return head_dim == 64 ? AttnCfg<64>::kBytes : AttnCfg<128>::kBytes;
+  return head_dim == 64 ? AttnCfg<64, false>::kBytes : AttnCfg<128, false>::kBytes;
+}
+
+// The widest shape whose grid runs in one wave: 16-CTA clusters when B n_kv of them
+// fit at once, else 8-CTA clusters with the deep ring when one CTA per SM suffices,
+// else the shallow ring.
+int attention_shape(int B, int nkv, int head_dim, int G) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttnDevices) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  if (G != 1 && G != 2 && G != 4) return 0;
+  AttnCaps caps;
+  {
+    std::lock_guard<std::mutex> lock(g_caps_mu);
+    caps = g_caps[dev][dim_index(head_dim)][group_index(G)];
+  }
+  const long long clusters = static_cast<long long>(B) * nkv;
+  if (caps.num_sms <= 0) return 0;
+  if (clusters * 16 <= caps.num_sms && clusters <= caps.max_clusters[2]) return 2;
+  if (clusters * 8 <= caps.num_sms && clusters <= caps.max_clusters[1]) return 1;
+  return 0;
 }
 
 cudaError_t prepare_attention(int head_dim, int G) {
+  int dev = 0, sms = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  AttnCaps caps;
+  caps.num_sms = sms;
 #define DEC_ATTN_PREP(D_, G_) \
-  if (head_dim == D_ && G == G_) return prepare_attn_t<D_, G_>();
+  if (head_dim == D_ && G == G_) e = prepare_all<D_, G_>(caps.max_clusters); else
   DEC_ATTN_PREP(64, 1)
   DEC_ATTN_PREP(64, 2)
   DEC_ATTN_PREP(64, 4)
   DEC_ATTN_PREP(128, 1)
   DEC_ATTN_PREP(128, 2)
   DEC_ATTN_PREP(128, 4)
+  e = cudaErrorInvalidValue;
 #undef DEC_ATTN_PREP
-  return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxAttnDevices) {
+    std::lock_guard<std::mutex> lock(g_caps_mu);
+    g_caps[dev][dim_index(head_dim)][group_index(G)] = caps;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim) {
   const int G = p.nq / p.nkv;
+  const int shape = attention_shape(p.B, p.nkv, head_dim, G);
 #define DEC_ATTN_CASE(D_, G_) \
-  if (head_dim == D_ && G == G_) return launch_attn_t<D_, G_>(c, p);
+  if (head_dim == D_ && G == G_) return launch_shape<D_, G_>(c, p, shape);
   DEC_ATTN_CASE(64, 1)
   DEC_ATTN_CASE(64, 2)
   DEC_ATTN_CASE(64, 4)

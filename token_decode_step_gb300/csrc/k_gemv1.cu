@@ -95,10 +95,39 @@ __device__ __forceinline__ float dot_q4_word(uint32_t w, const float* x) {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// This CTA's share of the next attention's cached K/V rows, prefetched into L2 by the
+// lanes of one warp.  The 2 B n_kv runs (plane, sequence, head) of P_b rows each are
+// dealt to the CTAs round-robin; the CTAs of a run split it into equal 16-byte-aligned
+// byte ranges, issued in pieces of at most 32 KB.
+__device__ __noinline__ void prefetch_kv_share(const GemvParams& p, int lane) {
+  const int ncta = static_cast<int>(gridDim.x * gridDim.y);
+  const int cta = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+  const int nruns = 2 * p.pf_B * p.pf_nkv;
+  const int run = cta % nruns, slice = cta / nruns;
+  const int nslices = (ncta - run + nruns - 1) / nruns;
+  const int plane = run / (p.pf_B * p.pf_nkv), bh = run % (p.pf_B * p.pf_nkv), b = bh / p.pf_nkv;
+  int P = p.pf_positions[b];
+  P = P < 0 ? 0 : (P >= p.pf_max_ctx ? p.pf_max_ctx - 1 : P);
+  const unsigned long long bytes = static_cast<unsigned long long>(P) * p.pf_row_bytes;
+  const unsigned long long per = ((bytes + nslices - 1) / nslices + 15) / 16 * 16;
+  const unsigned long long off = per * slice;
+  if (off >= bytes) return;
+  const unsigned long long n = bytes - off < per ? bytes - off : per;
+  const unsigned char* src = p.pf_kv + plane * p.pf_plane_bytes + bh * p.pf_head_bytes + off;
+  constexpr unsigned long long kPiece = 32768;
+  const unsigned long long npieces = (n + kPiece - 1) / kPiece;
+  for (unsigned long long i = lane; i < npieces; i += 32) {
+    const unsigned long long o = i * kPiece;
+    const unsigned long long m = n - o < kPiece ? n - o : kPiece;
+    prefetch_l2_bulk(src + o, static_cast<uint32_t>(m));
+  }
+}
+
 }  // namespace
 
+// Four CTAs of 256 threads per SM for bf16 (64 registers), two for the 4-bit decode.
 template <int WF, int IN, int EPI>
-__global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
+__global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParams p) {
   constexpr int R = kGemvRows;
   constexpr int CH = ChunkTraits<WF>::kCols;
   __shared__ float red[8][R];
@@ -126,6 +155,7 @@ __global__ void __launch_bounds__(256) k_gemv1(GemvParams p) {
 #pragma unroll
     for (int r = 0; r < R; ++r) wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + c * CH));
   }
+  if (p.pf_kv && warp == (nt >> 5) - 1) prefetch_kv_share(p, lane);
   // Residual rows of this tile: last written two or more kernels upstream, which
   // completed before the previous kernel could pass its own wait and start this one.
   float h_pre = 0.f;

@@ -1,0 +1,59 @@
+"""A short decode run on a reduced copy of a synthetic workload, for profiler captures.
+
+The model keeps the workload's layer shapes, batch and context but only
+`--layers` decoder layers (and optionally a smaller vocabulary), so that one
+kernel of a given shape can be captured by a profiler with a few GB on the
+device.  Steps run eagerly by default (one launch per kernel, in the order of
+dec_debug_step_prefix: embed, then qkv, attention, o_proj, gate_up, down per
+layer, then lm_head); `--graph` replays the captured step graph instead.
+
+    python -m token_decode_step_gb300.profile_case --config qwen3-8b-b1 --layers 2
+"""
+
+from __future__ import annotations
+
+import argparse
+import pathlib
+import sys
+
+import torch
+
+sys.path.insert(0, str(pathlib.Path(__file__).resolve().parent.parent))
+
+import synthetic  # noqa: E402
+from token_decode_step_gb300.torch_glue import Decoder  # noqa: E402
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--config", default="qwen3-8b-b1", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=2)
+    ap.add_argument("--vocab", type=int, default=0, help="0 keeps the workload's vocabulary")
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--graph", action="store_true")
+    a = ap.parse_args(argv)
+
+    kw = {"n_layers": a.layers, "steps": a.steps}
+    if a.vocab:
+        kw["vocab"] = a.vocab
+    wl = synthetic.WORKLOADS[a.config].replace(**kw)
+    model = synthetic.generate(wl, device="cuda")
+    d = Decoder(wl, model)
+    d.set_graph_mode(a.graph)
+    B = wl.batch
+    logits = torch.empty((B, wl.vocab), device="cuda")
+    amax = torch.empty((B,), dtype=torch.int32, device="cuda")
+    tok, pos = model["tokens"].clone(), model["positions"].clone()
+    for _ in range(a.steps):
+        d.step(tok, pos, model["kv"], logits, amax)
+        d.advance(amax, tok, pos)
+    torch.cuda.synchronize()
+    st = d.device_status()
+    d.close()
+    print(f"profile_case {a.config} layers={a.layers} vocab={wl.vocab} steps={a.steps} "
+          f"graph={a.graph} status={st}")
+    return 0 if st == (0, 0) else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
