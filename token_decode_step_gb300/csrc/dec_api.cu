@@ -56,6 +56,7 @@ struct PackedLinear {
   uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
   int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
+  size_t w_bytes = 0, sb_bytes = 0;  // sizes of the two regions (sb_bytes 0 when sb is null)
 };
 
 struct PackedLayer {
@@ -89,6 +90,10 @@ struct dec_handle {
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
+  // the attention kernel prefetches the O projection's weights into L2 (when they take
+  // at most a quarter of L2)
+  bool w_prefetch = false;
+  int l2_bytes = 0;
   // packed weights (one allocation)
   unsigned char* wmem = nullptr;
   size_t wbytes = 0;
@@ -206,13 +211,14 @@ dec_status check_linear(const dec_linear& l, int fmt, const char* name, int laye
   return DEC_OK;
 }
 
-// K splits of a batch-1 GEMV: split only while there are fewer CTAs than SMs (every
-// split costs a round trip through the partial sums).
+// K splits of a batch-1 GEMV: split only while the CTAs would cover fewer than half the
+// SMs.  Every split costs a round trip through the partial sums (fence, ticket, reload:
+// about 2 us measured on the 1024-row projections, more than the idle SMs give back).
 int choose_splits(int N, int K, int fmt, int num_sms) {
   const int cols = fmt == DEC_W_BF16 ? 8 : 32;
   const int tiles = (N + kGemvRows - 1) / kGemvRows;
   int S = 1;
-  while (static_cast<long long>(tiles) * S < num_sms) {
+  while (static_cast<long long>(tiles) * S * 2 < num_sms) {
     const int S2 = S * 2;
     if (K % S2 != 0) break;
     const int KS = K / S2;
@@ -406,6 +412,12 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.out = h->attn_o;
     ap.status = h->status;
     ap.out_hl = c.batch > 1 ? h->xh_o : nullptr;
+    if (h->w_prefetch) {  // HBM is mostly idle during the attention: stage the O projection in L2
+      ap.pf_w0 = static_cast<const unsigned char*>(L.o.w);
+      ap.pf_w0_bytes = L.o.w_bytes;
+      ap.pf_w1 = reinterpret_cast<const unsigned char*>(L.o.sb);
+      ap.pf_w1_bytes = L.o.sb_bytes;
+    }
     if (limit_hit()) return DEC_OK;
     ++launched;
     ap.tl = Timeline{h->timeline, launched - 1};
@@ -536,6 +548,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       return fail("cudaDeviceGetAttribute", e);
     const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim * 2;
     h->kv_prefetch = c.batch == 1 && kv_layer <= l2 / 4.0;
+    h->l2_bytes = l2;
   }
 
   // ---- packed weight memory
@@ -543,6 +556,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const bool tc = c.batch > 1;
   const int ny = tc ? gemm_tc_ny(h->wfmt, c.batch) : 0;
   auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
+  h->w_prefetch = static_cast<double>(lbytes(H, nq * d)) <= h->l2_bytes / 4.0;
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
   const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +
@@ -567,15 +581,19 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if (tc) {
       L.Npad = (N + 15) / 16 * 16;
       choose_tc_splits(L, h->wfmt, ny, h->num_sms);
-      L.w = take(linear_bytes_tc(fmt, N, K));
+      L.w_bytes = linear_bytes_tc(fmt, N, K);
+      L.w = take(L.w_bytes);
       return L;
     }
     L.S = choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
-      L.w = take(static_cast<size_t>(N) * K * 2);
+      L.w_bytes = static_cast<size_t>(N) * K * 2;
+      L.w = take(L.w_bytes);
     } else {
-      L.w = take(static_cast<size_t>(N) * K / 2);
-      L.sb = reinterpret_cast<uint32_t*>(take(static_cast<size_t>(N) * (K / kGroup) * 4));
+      L.w_bytes = static_cast<size_t>(N) * K / 2;
+      L.sb_bytes = static_cast<size_t>(N) * (K / kGroup) * 4;
+      L.w = take(L.w_bytes);
+      L.sb = reinterpret_cast<uint32_t*>(take(L.sb_bytes));
     }
     return L;
   };
