@@ -90,10 +90,7 @@ struct dec_handle {
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
-  // the attention kernel prefetches the O projection's weights into L2 (when they take
-  // at most a quarter of L2)
-  bool w_prefetch = false;
-  int l2_bytes = 0;
+
   // packed weights (one allocation)
   unsigned char* wmem = nullptr;
   size_t wbytes = 0;
@@ -412,12 +409,6 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.out = h->attn_o;
     ap.status = h->status;
     ap.out_hl = c.batch > 1 ? h->xh_o : nullptr;
-    if (h->w_prefetch) {  // HBM is mostly idle during the attention: stage the O projection in L2
-      ap.pf_w0 = static_cast<const unsigned char*>(L.o.w);
-      ap.pf_w0_bytes = L.o.w_bytes;
-      ap.pf_w1 = reinterpret_cast<const unsigned char*>(L.o.sb);
-      ap.pf_w1_bytes = L.o.sb_bytes;
-    }
     if (limit_hit()) return DEC_OK;
     ++launched;
     ap.tl = Timeline{h->timeline, launched - 1};
@@ -548,7 +539,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       return fail("cudaDeviceGetAttribute", e);
     const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim * 2;
     h->kv_prefetch = c.batch == 1 && kv_layer <= l2 / 4.0;
-    h->l2_bytes = l2;
   }
 
   // ---- packed weight memory
@@ -556,7 +546,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const bool tc = c.batch > 1;
   const int ny = tc ? gemm_tc_ny(h->wfmt, c.batch) : 0;
   auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
-  h->w_prefetch = static_cast<double>(lbytes(H, nq * d)) <= h->l2_bytes / 4.0;
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
   const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +

@@ -95,11 +95,6 @@ struct AttnParams {
   float* out;                   // [B][nq d]
   __nv_bfloat16* out_hl;        // optional: the output again as bf16 hi, lo planes [2][B][nq d]
   unsigned* status;
-  // optional L2 prefetch of up to two byte ranges (the next kernel's weights), split
-  // evenly over the CTAs; null: none
-  const unsigned char* pf_w0;
-  const unsigned char* pf_w1;
-  unsigned long long pf_w0_bytes, pf_w1_bytes;
 };
 
 struct EmbedParams {

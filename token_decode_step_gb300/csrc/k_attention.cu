@@ -104,21 +104,6 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// This CTA's 1/n share of [base, base + bytes) prefetched into L2 by the lanes of one
-// warp, in 16-byte-aligned pieces of at most 32 KB.
-__device__ __forceinline__ void prefetch_share(const unsigned char* base, unsigned long long bytes, int cta, int n,
-                                               int lane) {
-  const unsigned long long per = ((bytes + n - 1) / n + 15) / 16 * 16;
-  const unsigned long long off = per * cta;
-  if (!base || off >= bytes) return;
-  const unsigned long long len = bytes - off < per ? bytes - off : per;
-  constexpr unsigned long long kPiece = 32768;
-  for (unsigned long long i = lane; i * kPiece < len; i += 32) {
-    const unsigned long long o = i * kPiece;
-    prefetch_l2_bulk(base + off + o, static_cast<uint32_t>(len - o < kPiece ? len - o : kPiece));
-  }
-}
-
 // Positions [begin, end) of CTA `rank` of a cluster of C for a sequence with T = P + 1
 // positions: runs of ceil(T / C) rounded up to 16 positions; later CTAs may get fewer
 // or none.
@@ -159,13 +144,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   const size_t head_off = (static_cast<size_t>(b) * p.nkv + h) * p.max_ctx * D;
   __nv_bfloat16* kbase = p.kv + (static_cast<size_t>(p.layer) * 2 + 0) * plane + head_off;
   __nv_bfloat16* vbase = p.kv + (static_cast<size_t>(p.layer) * 2 + 1) * plane + head_off;
-
-  if (warp == kAttnThreads / 32 - 1 && (p.pf_w0 || p.pf_w1)) {
-    const int ncta = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
-    const int cta = static_cast<int>((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x);
-    prefetch_share(p.pf_w0, p.pf_w0_bytes, cta, ncta, lane);
-    prefetch_share(p.pf_w1, p.pf_w1_bytes, cta, ncta, lane);
-  }
 
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sStages = s_base + CF::kOffStages;

@@ -12,6 +12,16 @@
 // Weight streaming: every thread issues 16-byte L1-bypassing loads of 8 rows at
 // once; the first chunk is requested before the grid-dependency wait, so it
 // overlaps the previous kernel's tail (programmatic dependent launch).
+//
+// The input RMSNorm is linear in the product: y = rsqrt(mean(h^2) + eps) * W (h * w),
+// so the loop runs on h * w and the scale is applied to the row sums at the end; the
+// partial sums of squares are loaded right after the wait and reduced with the row
+// sums, off the path to the first multiply.
+//
+// 4-bit decode: the codes of a word are split into even and odd bytes (two logic
+// ops), each byte is moved into bits 16..19 of 128.0f by one byte permute (giving
+// 128 + q exactly), and the products accumulate in pairs with the packed fp32 FMA
+// (fma.rn.f32x2).  Per group: sum (s q + b) x = s sum (128 + q) x + (b - 128 s) sum x.
 #include "dec_internal.cuh"
 #include "q4.cuh"
 
@@ -39,9 +49,9 @@ __device__ __forceinline__ const void* chunk_ptr(const GemvParams& p, int row, i
   }
 }
 
-// Input chunk: x[col .. col + n) as floats, normalised (RMSNorm of the residual) if requested.
+// Input chunk: x[col .. col + n) as floats, times the norm weight for kInNorm.
 template <int IN, int N>
-__device__ __forceinline__ void load_x(const GemvParams& p, int col, float inv_rms, float (&xv)[N]) {
+__device__ __forceinline__ void load_x(const GemvParams& p, int col, float (&xv)[N]) {
   const float4* src = reinterpret_cast<const float4*>(p.x + col);
 #pragma unroll
   for (int i = 0; i < N / 4; ++i) {
@@ -56,14 +66,14 @@ __device__ __forceinline__ void load_x(const GemvParams& p, int col, float inv_r
 #pragma unroll
     for (int i = 0; i < N / 8; ++i) {
       uint4 u = wn[i];
-      xv[8 * i + 0] = (xv[8 * i + 0] * inv_rms) * bf16_lo(u.x);
-      xv[8 * i + 1] = (xv[8 * i + 1] * inv_rms) * bf16_hi(u.x);
-      xv[8 * i + 2] = (xv[8 * i + 2] * inv_rms) * bf16_lo(u.y);
-      xv[8 * i + 3] = (xv[8 * i + 3] * inv_rms) * bf16_hi(u.y);
-      xv[8 * i + 4] = (xv[8 * i + 4] * inv_rms) * bf16_lo(u.z);
-      xv[8 * i + 5] = (xv[8 * i + 5] * inv_rms) * bf16_hi(u.z);
-      xv[8 * i + 6] = (xv[8 * i + 6] * inv_rms) * bf16_lo(u.w);
-      xv[8 * i + 7] = (xv[8 * i + 7] * inv_rms) * bf16_hi(u.w);
+      xv[8 * i + 0] *= bf16_lo(u.x);
+      xv[8 * i + 1] *= bf16_hi(u.x);
+      xv[8 * i + 2] *= bf16_lo(u.y);
+      xv[8 * i + 3] *= bf16_hi(u.y);
+      xv[8 * i + 4] *= bf16_lo(u.z);
+      xv[8 * i + 5] *= bf16_hi(u.z);
+      xv[8 * i + 6] *= bf16_lo(u.w);
+      xv[8 * i + 7] *= bf16_hi(u.w);
     }
   }
 }
@@ -80,17 +90,28 @@ __device__ __forceinline__ float dot_bf16x8(uint4 w, const float* x, float acc) 
   return acc;
 }
 
-// sum over 8 codes of one word of (128 + q_k) * x_k
-__device__ __forceinline__ float dot_q4_word(uint32_t w, const float* x) {
-  float a = q4_code_plus128<0>(w) * x[0];
-  a = fmaf(q4_code_plus128<1>(w), x[1], a);
-  a = fmaf(q4_code_plus128<2>(w), x[2], a);
-  a = fmaf(q4_code_plus128<3>(w), x[3], a);
-  a = fmaf(q4_code_plus128<4>(w), x[4], a);
-  a = fmaf(q4_code_plus128<5>(w), x[5], a);
-  a = fmaf(q4_code_plus128<6>(w), x[6], a);
-  a = fmaf(q4_code_plus128<7>(w), x[7], a);
-  return a;
+// (d0, d1) += (a0 * x0, a1 * x1) with one packed fp32 FMA; a0, a1 are float bit patterns
+__device__ __forceinline__ void ffma2(float& d0, float& d1, uint32_t a0, uint32_t a1, float x0, float x1) {
+  asm("{\n\t.reg .b64 a, x, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 x, {%4, %5};\n\t"
+      "mov.b64 d, {%0, %1};\n\t"
+      "fma.rn.f32x2 d, a, x, d;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(a0), "r"(a1), "f"(x0), "f"(x1));
+}
+
+// (d0, d1) += sum over the 8 codes of one word of (128 + q_k) x_k: even codes in d0,
+// odd codes in d1.  Byte j of `lo` is code 2j, byte j of `hi` code 2j + 1; the permute
+// selector 0x7j44 builds [0, 0, byte j, 0x43] = 128 + code as a float.
+__device__ __forceinline__ void dot_q4_word(uint32_t w, const float* x, float& d0, float& d1) {
+  const uint32_t lo = w & 0x0f0f0f0fu, hi = (w >> 4) & 0x0f0f0f0fu;
+  constexpr uint32_t kMagic = 0x43000000u;
+  ffma2(d0, d1, __byte_perm(lo, kMagic, 0x7044), __byte_perm(hi, kMagic, 0x7044), x[0], x[1]);
+  ffma2(d0, d1, __byte_perm(lo, kMagic, 0x7144), __byte_perm(hi, kMagic, 0x7144), x[2], x[3]);
+  ffma2(d0, d1, __byte_perm(lo, kMagic, 0x7244), __byte_perm(hi, kMagic, 0x7244), x[4], x[5]);
+  ffma2(d0, d1, __byte_perm(lo, kMagic, 0x7344), __byte_perm(hi, kMagic, 0x7344), x[6], x[7]);
 }
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
@@ -130,9 +151,8 @@ template <int WF, int IN, int EPI>
 __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParams p) {
   constexpr int R = kGemvRows;
   constexpr int CH = ChunkTraits<WF>::kCols;
-  __shared__ float red[8][R];
+  __shared__ float red[8][R + 1];  // per warp: R row sums, then the sum of squares
   __shared__ float ys[R];
-  __shared__ float s_inv_rms;
   __shared__ unsigned s_ticket;
 
   const int tile = blockIdx.x, split = blockIdx.y;
@@ -148,13 +168,20 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
   for (int r = 0; r < R; ++r) acc[r] = 0.f;
 
   tl_mark(p.tl, 0);
-  // First chunk's weights: independent of upstream kernels, so fetched before the wait.
+  // First chunk's weights (and 4-bit scale/bias words): independent of upstream
+  // kernels, so fetched before the wait.
   uint4 wreg[R];
-  int c = tid;
-  if (c < nchunk) {
+  uint32_t sbw[WF == kWQ4 ? R : 1];
+  auto load_chunk = [&](int cc) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + c * CH));
-  }
+    for (int r = 0; r < R; ++r) {
+      const int row = row0 + min(r, nrows - 1);
+      wreg[r] = ld_stream16(chunk_ptr<WF>(p, row, kbeg + cc * CH));
+      if constexpr (WF == kWQ4) sbw[r] = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + (kbeg + cc * CH) / kGroup);
+    }
+  };
+  int c = tid;
+  if (c < nchunk) load_chunk(c);
   if (p.pf_kv && warp == (nt >> 5) - 1) prefetch_kv_share(p, lane);
   // Residual rows of this tile: last written two or more kernels upstream, which
   // completed before the previous kernel could pass its own wait and start this one.
@@ -166,26 +193,16 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
   griddep_wait();
   tl_mark(p.tl, 1);
 
-  float inv_rms = 1.f;
+  // this thread's share of the input's partial sums of squares (reduced after the loop)
+  float ssq = 0.f;
   if constexpr (IN == kInNorm) {
-    float s = 0.f;
-    for (int i = tid; i < p.n_sumsq_in; i += nt) s += p.sumsq_in[i];
-    s = warp_sum(s);
-    if (lane == 0) red[warp][0] = s;
-    __syncthreads();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < nt / 32; ++w) t += red[w][0];
-      s_inv_rms = rsqrtf(t / static_cast<float>(p.K) + p.eps);
-    }
-    __syncthreads();
-    inv_rms = s_inv_rms;
+    for (int i = tid; i < p.n_sumsq_in; i += nt) ssq += p.sumsq_in[i];
   }
 
   for (; c < nchunk; c += nt) {
     const int col = kbeg + c * CH;
     float xv[CH];
-    load_x<IN, CH>(p, col, inv_rms, xv);
+    load_x<IN, CH>(p, col, xv);
     if constexpr (WF == kWBf16) {
 #pragma unroll
       for (int r = 0; r < R; ++r) acc[r] = dot_bf16x8(wreg[r], xv, acc[r]);
@@ -193,38 +210,43 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
       float xsum = 0.f;
 #pragma unroll
       for (int i = 0; i < CH; ++i) xsum += xv[i];
-      const int grp = col / kGroup;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const int row = row0 + min(r, nrows - 1);
-        const uint32_t sbw = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + grp);
-        float d = dot_q4_word(wreg[r].x, xv) + dot_q4_word(wreg[r].y, xv + 8) + dot_q4_word(wreg[r].z, xv + 16) +
-                  dot_q4_word(wreg[r].w, xv + 24);
-        const float s = sb_scale(sbw), b = sb_bias(sbw);
-        // sum (s q + b) x = s * sum (128 + q) x + (b - 128 s) * sum x
-        acc[r] = fmaf(s, d, acc[r]);
+        float d0 = 0.f, d1 = 0.f;
+        dot_q4_word(wreg[r].x, xv, d0, d1);
+        dot_q4_word(wreg[r].y, xv + 8, d0, d1);
+        dot_q4_word(wreg[r].z, xv + 16, d0, d1);
+        dot_q4_word(wreg[r].w, xv + 24, d0, d1);
+        const float s = sb_scale(sbw[r]), b = sb_bias(sbw[r]);
+        acc[r] = fmaf(s, d0 + d1, acc[r]);
         acc[r] = fmaf(fmaf(-128.f, s, b), xsum, acc[r]);
       }
     }
     const int cn = c + nt;
-    if (cn < nchunk) {
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-        wreg[r] = ld_stream16(chunk_ptr<WF>(p, row0 + min(r, nrows - 1), kbeg + cn * CH));
-    }
+    if (cn < nchunk) load_chunk(cn);
   }
   griddep_launch_dependents();
 
-  // block reduction of the R row sums (fixed order: lanes, then warps 0..n-1)
+  // block reduction of the R row sums and the sum of squares (fixed order: lanes,
+  // then warps 0..n-1)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     float v = warp_sum(acc[r]);
     if (lane == 0) red[warp][r] = v;
   }
+  if constexpr (IN == kInNorm) {
+    ssq = warp_sum(ssq);
+    if (lane == 0) red[warp][R] = ssq;
+  }
   __syncthreads();
   if (tid < R) {
     float t = 0.f;
     for (int w = 0; w < nt / 32; ++w) t += red[w][tid];
+    if constexpr (IN == kInNorm) {
+      float q = 0.f;
+      for (int w = 0; w < nt / 32; ++w) q += red[w][R];
+      t *= rsqrtf(q / static_cast<float>(p.K) + p.eps);
+    }
     ys[tid] = t;
   }
 
