@@ -153,162 +153,192 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
   constexpr int CH = ChunkTraits<WF>::kCols;
   __shared__ float red[8][R + 1];  // per warp: R row sums, then the sum of squares
   __shared__ float ys[R];
+  __shared__ float s_inv;
   __shared__ unsigned s_ticket;
 
-  const int tile = blockIdx.x, split = blockIdx.y;
-  const int row0 = tile * R;
-  const int nrows = min(R, p.N - row0);
-  const int kbeg = split * p.KS;
+  // Work units (row tile, K split), unit u = split * ntiles + tile; the CTAs take the
+  // units round-robin and request the next unit's first chunk before reducing the
+  // current one.
+  const int ntiles = (p.N + R - 1) / R;
+  const int nunits = ntiles * p.S;
   const int nchunk = p.KS / CH;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
 
-  float acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
-
   tl_mark(p.tl, 0);
-  // First chunk's weights (and 4-bit scale/bias words): independent of upstream
-  // kernels, so fetched before the wait.
   uint4 wreg[R];
   uint32_t sbw[WF == kWQ4 ? R : 1];
-  auto load_chunk = [&](int cc) {
+  auto load_chunk = [&](int u, int cc) {
+    const int tile = u % ntiles, row0 = tile * R, nrows = min(R, p.N - row0);
+    const int col = (u / ntiles) * p.KS + cc * CH;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int row = row0 + min(r, nrows - 1);
-      wreg[r] = ld_stream16(chunk_ptr<WF>(p, row, kbeg + cc * CH));
-      if constexpr (WF == kWQ4) sbw[r] = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + (kbeg + cc * CH) / kGroup);
+      wreg[r] = ld_stream16(chunk_ptr<WF>(p, row, col));
+      if constexpr (WF == kWQ4) sbw[r] = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + col / kGroup);
     }
   };
-  int c = tid;
-  if (c < nchunk) load_chunk(c);
+  // The first unit's first chunk (weights and 4-bit scale/bias words) does not depend
+  // on upstream kernels: requested before the grid-dependency wait.
+  int u = blockIdx.x;
+  if (u < nunits && tid < nchunk) load_chunk(u, tid);
   if (p.pf_kv && warp == (nt >> 5) - 1) prefetch_kv_share(p, lane);
-  // Residual rows of this tile: last written two or more kernels upstream, which
+  // Residual rows of the first tile: last written two or more kernels upstream, which
   // completed before the previous kernel could pass its own wait and start this one.
   float h_pre = 0.f;
   if constexpr (EPI == kEpiResid) {
-    if (tid < R) h_pre = __ldcg(p.out + row0 + tid);
+    if (tid < R && u < nunits) h_pre = __ldcg(p.out + (u % ntiles) * R + tid);
   }
 
   griddep_wait();
   tl_mark(p.tl, 1);
 
-  // this thread's share of the input's partial sums of squares (reduced after the loop)
+  // this thread's share of the input's partial sums of squares, reduced with the first
+  // unit's row sums
   float ssq = 0.f;
   if constexpr (IN == kInNorm) {
     for (int i = tid; i < p.n_sumsq_in; i += nt) ssq += p.sumsq_in[i];
   }
 
-  for (; c < nchunk; c += nt) {
-    const int col = kbeg + c * CH;
-    float xv[CH];
-    load_x<IN, CH>(p, col, xv);
-    if constexpr (WF == kWBf16) {
+  // 4-bit, one chunk per thread, no K split: a thread's input chunk (and its sum) is the
+  // same in every unit and loaded once (bf16 reloads its 8 inputs: registers are tight).
+  const bool x_fixed = WF == kWQ4 && p.S == 1 && nchunk <= nt;
+  float xv[CH];
+  float xsum = 0.f;
+  __shared__ unsigned long long s_best;  // lm_head: this CTA's best (value, index) key
+  if (tid == 0) s_best = 0ull;          // written and read by thread 0 only
+
+  for (bool first = true; u < nunits; u += gridDim.x, first = false) {
+    const int tile = u % ntiles, split = u / ntiles;
+    const int row0 = tile * R;
+    const int nrows = min(R, p.N - row0);
+    const int kbeg = split * p.KS;
+    const int un = u + gridDim.x;  // this CTA's next unit
+
+    float acc[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) acc[r] = dot_bf16x8(wreg[r], xv, acc[r]);
-    } else {
-      float xsum = 0.f;
+    for (int r = 0; r < R; ++r) acc[r] = 0.f;
+    for (int c = tid; c < nchunk; c += nt) {
+      const int col = kbeg + c * CH;
+      if (first || !x_fixed) {
+        load_x<IN, CH>(p, col, xv);
+        if constexpr (WF == kWQ4) {
+          xsum = 0.f;
 #pragma unroll
-      for (int i = 0; i < CH; ++i) xsum += xv[i];
+          for (int i = 0; i < CH; ++i) xsum += xv[i];
+        }
+      }
+      if constexpr (WF == kWBf16) {
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float d0 = 0.f, d1 = 0.f;
-        dot_q4_word(wreg[r].x, xv, d0, d1);
-        dot_q4_word(wreg[r].y, xv + 8, d0, d1);
-        dot_q4_word(wreg[r].z, xv + 16, d0, d1);
-        dot_q4_word(wreg[r].w, xv + 24, d0, d1);
-        const float s = sb_scale(sbw[r]), b = sb_bias(sbw[r]);
-        acc[r] = fmaf(s, d0 + d1, acc[r]);
-        acc[r] = fmaf(fmaf(-128.f, s, b), xsum, acc[r]);
+        for (int r = 0; r < R; ++r) acc[r] = dot_bf16x8(wreg[r], xv, acc[r]);
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float d0 = 0.f, d1 = 0.f;
+          dot_q4_word(wreg[r].x, xv, d0, d1);
+          dot_q4_word(wreg[r].y, xv + 8, d0, d1);
+          dot_q4_word(wreg[r].z, xv + 16, d0, d1);
+          dot_q4_word(wreg[r].w, xv + 24, d0, d1);
+          const float s = sb_scale(sbw[r]), b = sb_bias(sbw[r]);
+          acc[r] = fmaf(s, d0 + d1, acc[r]);
+          acc[r] = fmaf(fmaf(-128.f, s, b), xsum, acc[r]);
+        }
+      }
+      if (c + nt < nchunk) {
+        load_chunk(u, c + nt);
+      } else if (un < nunits) {
+        load_chunk(un, tid);  // tid < nchunk here
       }
     }
-    const int cn = c + nt;
-    if (cn < nchunk) load_chunk(cn);
-  }
-  griddep_launch_dependents();
+    if (un >= nunits) griddep_launch_dependents();
 
-  // block reduction of the R row sums and the sum of squares (fixed order: lanes,
-  // then warps 0..n-1)
+    // block reduction of the R row sums (and, once, the sum of squares); fixed order:
+    // lanes, then warps 0..n-1
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    float v = warp_sum(acc[r]);
-    if (lane == 0) red[warp][r] = v;
-  }
-  if constexpr (IN == kInNorm) {
-    ssq = warp_sum(ssq);
-    if (lane == 0) red[warp][R] = ssq;
-  }
-  __syncthreads();
-  if (tid < R) {
-    float t = 0.f;
-    for (int w = 0; w < nt / 32; ++w) t += red[w][tid];
-    if constexpr (IN == kInNorm) {
-      float q = 0.f;
-      for (int w = 0; w < nt / 32; ++w) q += red[w][R];
-      t *= rsqrtf(q / static_cast<float>(p.K) + p.eps);
+    for (int r = 0; r < R; ++r) {
+      float v = warp_sum(acc[r]);
+      if (lane == 0) red[warp][r] = v;
     }
-    ys[tid] = t;
-  }
-
-  // split-K: the last CTA of a row tile adds the S partials in split order
-  if (p.S > 1) {
-    if (tid < R && tid < nrows) p.partials[static_cast<size_t>(split) * p.N + row0 + tid] = ys[tid];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_ticket = atomicAdd(&p.counters[tile], 1u);
-    __syncthreads();
-    if (s_ticket != static_cast<unsigned>(p.S - 1)) {
-      tl_mark(p.tl, 2);
-      return;
+    if (IN == kInNorm && first) {
+      const float v = warp_sum(ssq);
+      if (lane == 0) red[warp][R] = v;
     }
-    __threadfence();
-    if (tid < R && tid < nrows) {
+    __syncthreads();
+    if (tid < R) {
+      if (IN == kInNorm && first) {
+        float q = 0.f;
+        for (int w = 0; w < nt / 32; ++w) q += red[w][R];
+        if (tid == 0) s_inv = rsqrtf(q / static_cast<float>(p.K) + p.eps);
+      }
       float t = 0.f;
-      for (int s = 0; s < p.S; ++s) t += __ldcg(p.partials + static_cast<size_t>(s) * p.N + row0 + tid);
+      for (int w = 0; w < nt / 32; ++w) t += red[w][tid];
       ys[tid] = t;
     }
-    if (tid == 0) p.counters[tile] = 0u;
-  }
-  __syncthreads();
 
-  // epilogue: lane r of warp 0 owns row row0 + r
-  if (warp != 0) return;
-  const bool mine = lane < R;
-  const float y = mine ? ys[lane] : 0.f;
-  if constexpr (EPI == kEpiStore) {
-    if (lane < nrows) p.out[row0 + lane] = y;
-  } else if constexpr (EPI == kEpiResid) {
-    float hn = 0.f;
-    if (mine) {
-      hn = h_pre + y;
-      p.out[row0 + lane] = hn;
-    }
-    float ss = hn * hn;  // the tile's 8 rows are one group of the norm's sums of squares
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-    if (lane == 0) p.sumsq_out[tile] = ss;
-  } else if constexpr (EPI == kEpiSwiglu) {
-    // rows 0..3: gate of outputs 4 tile + i; rows 4..7: up of the same outputs
-    const float up = __shfl_down_sync(0xffffffffu, y, R / 2);
-    if (lane < R / 2) p.out[tile * (R / 2) + lane] = silu_f(y) * up;
-  } else {  // lm_head tile
-    if (lane < nrows && p.out) p.out[row0 + lane] = y;
-    unsigned long long k = lane < nrows ? argmax_key(y, row0 + lane) : 0ull;
-#pragma unroll
-    for (int o = 1; o < R; o <<= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
-      k = other > k ? other : k;
-    }
-    if (lane == 0) {
-      atomicMax(p.amax_key, k);
+    // split-K: the last CTA to finish a row tile adds the S partials in split order
+    if (p.S > 1) {
+      __syncthreads();
+      if (tid < R && tid < nrows) {
+        const float sc = IN == kInNorm ? s_inv : 1.f;
+        p.partials[static_cast<size_t>(split) * p.N + row0 + tid] = ys[tid] * sc;
+      }
       __threadfence();
-      const unsigned ntiles = gridDim.x;
+      __syncthreads();
+      if (tid == 0) s_ticket = atomicAdd(&p.counters[tile], 1u);
+      __syncthreads();
+      if (s_ticket != static_cast<unsigned>(p.S - 1)) continue;
+      __threadfence();
+      if (tid < R && tid < nrows) {
+        float t = 0.f;
+        for (int s = 0; s < p.S; ++s) t += __ldcg(p.partials + static_cast<size_t>(s) * p.N + row0 + tid);
+        ys[tid] = t;
+      }
+      if (tid == 0) p.counters[tile] = 0u;
+    }
+    __syncthreads();
+
+    // epilogue: lane r of warp 0 owns row row0 + r; the other warps go on to the next unit
+    if (warp != 0) continue;
+    const bool mine = lane < R;
+    float y = mine ? ys[lane] : 0.f;
+    if (IN == kInNorm && p.S == 1) y *= s_inv;
+    if constexpr (EPI == kEpiStore) {
+      if (lane < nrows) p.out[row0 + lane] = y;
+    } else if constexpr (EPI == kEpiResid) {
+      float hn = 0.f;
+      if (mine) {
+        hn = (first ? h_pre : __ldcg(p.out + row0 + lane)) + y;
+        p.out[row0 + lane] = hn;
+      }
+      float ss = hn * hn;  // the tile's 8 rows are one group of the norm's sums of squares
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      if (lane == 0) p.sumsq_out[tile] = ss;
+    } else if constexpr (EPI == kEpiSwiglu) {
+      // rows 0..3: gate of outputs 4 tile + i; rows 4..7: up of the same outputs
+      const float up = __shfl_down_sync(0xffffffffu, y, R / 2);
+      if (lane < R / 2) p.out[tile * (R / 2) + lane] = silu_f(y) * up;
+    } else {  // lm_head tile: keep the CTA's best key, published once after the last unit
+      if (lane < nrows && p.out) p.out[row0 + lane] = y;
+      unsigned long long k = lane < nrows ? argmax_key(y, row0 + lane) : 0ull;
+#pragma unroll
+      for (int o = 1; o < R; o <<= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+        k = other > k ? other : k;
+      }
+      if (lane == 0 && k > s_best) s_best = k;
+    }
+  }
+  if constexpr (EPI == kEpiLmHead) {  // two-stage argmax: CTA keys, then the last CTA publishes
+    if (tid == 0) {
+      atomicMax(p.amax_key, s_best);
+      __threadfence();
       const unsigned done = atomicAdd(&p.counters[ntiles], 1u);
-      if (done == ntiles - 1) {
+      if (done == gridDim.x - 1) {
         __threadfence();
-        const unsigned long long best = atomicOr(p.amax_key, 0ull);
-        *p.argmax_out = argmax_key_index(best);
+        const unsigned long long top = atomicOr(p.amax_key, 0ull);
+        *p.argmax_out = argmax_key_index(top);
         p.counters[ntiles] = 0u;
       }
     }
@@ -322,8 +352,17 @@ static cudaError_t launch_one(const LaunchCtx& c, const GemvParams& p) {
   const int nchunk = p.KS / CH;
   int nt = ((nchunk + 31) / 32) * 32;
   nt = nt < 32 ? 32 : (nt > 256 ? 256 : nt);
+  // one wave of CTAs (every CTA resident at once), each looping over its units
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv1<WF, IN, EPI>, nt, 0)) != cudaSuccess)
+    return e;
+  const long long units = static_cast<long long>((p.N + kGemvRows - 1) / kGemvRows) * p.S;
+  const long long cap = static_cast<long long>(per_sm > 0 ? per_sm : 1) * sms;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.N + kGemvRows - 1) / kGemvRows, p.S);
+  cfg.gridDim = dim3(static_cast<unsigned>(units < cap ? units : cap));
   cfg.blockDim = dim3(nt);
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
