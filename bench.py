@@ -35,7 +35,13 @@ METRIC = "decode tokens/s and achieved HBM GB/s (fraction of GB300 peak) per ste
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # dominant kernel class, keyed by workload and class, valid only for the kernel
 # sources whose digest is recorded with it (see profiles/).
-NCU_TRAFFIC: dict = {}
+# Captured with token_decode_step_gb300.profile_case (2 layers, same shapes as the bench
+# workload) under `ncu --set full`; profiles/ holds the summaries and commands.
+NCU_TRAFFIC: dict = {
+    "qwen3-0.6b": {"attention": {"bytes": 4253696, "csrc": "5d874a29ddfcd8e3"}},
+    "qwen3-8b-b1": {"gate_up": {"bytes": 201391360 + 2978304, "csrc": "5d874a29ddfcd8e3"}},
+    "qwen3-4b-q4": {"gate_up": {"bytes": 28077568, "csrc": "5d874a29ddfcd8e3"}},
+}
 
 
 def csrc_digest() -> str:
@@ -53,31 +59,50 @@ def measured_peaks() -> tuple[dict, str]:
 
 
 class ClockSampler:
-    """nvidia-smi SM clock / throttle sampling while the timed region runs."""
+    """nvidia-smi SM clock / throttle sampling around the timed region.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    Sampling starts (and its first sample is awaited) before the timed region;
+    begin() and end() mark the region on the host clock and summary() keeps the
+    samples stamped inside it.  If the region is shorter than one sampling period,
+    the first sample after begin() stands in and `samples_in_region` says so.
+    """
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 3.0
+            while not self.lines and time.time() < deadline:
+                time.sleep(0.01)
         except FileNotFoundError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
+        # one more period so that a sample stamped inside the region has been read
+        time.sleep(2 * self.PERIOD_MS / 1000.0)
 
     def __exit__(self, *a):
         if self.proc:
@@ -87,13 +112,30 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    @staticmethod
+    def _stamp(text: str) -> float | None:
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self) -> dict:
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        rows = []
+        for arrival, ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
+            t = self._stamp(parts[0])
+            rows.append((t if t is not None else arrival, parts[1:]))
+        inside = [r for r in rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        n_in = len(inside)
+        if not inside and self.t0 is not None:
+            after = [r for r in rows if r[0] >= self.t0]
+            inside = after[:1]
+        sm, smax, reasons = [], None, set()
+        for _, parts in inside:
             try:
                 sm.append(float(parts[0]))
                 smax = float(parts[1])
@@ -103,7 +145,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_region": n_in}
 
 
 def run_ours(args, rank: int, world: int) -> dict | None:
@@ -146,11 +188,13 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        clk.begin()
         ev0.record(stream)
         for _ in range(args.steps):
             one_step()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
+        clk.end()
     if world > 1:
         torch.distributed.barrier()
     ms = ev0.elapsed_time(ev1)

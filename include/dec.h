@@ -178,10 +178,12 @@ enum {
     DEC_K_DOWN = 5, DEC_K_LMHEAD = 6, DEC_K_COUNT = 7
 };
 
-/* Run one step with individual launches, each bracketed by CUDA events recorded
-   on `stream`, then synchronise `stream` and add each launch's elapsed time (ms)
-   to ms[class] and 1 to launches[class] (host arrays of n_classes >= DEC_K_COUNT
-   entries).  Same arguments and results as dec_step. */
+/* Run one step with individual launches, one after another, each bracketed by CUDA
+   events recorded on `stream` (the stream is first held by a short sleeping kernel on
+   an internal stream, so that every launch is enqueued before the first runs and the
+   times hold no host launch gaps), then synchronise `stream` and add each launch's
+   elapsed time (ms) to ms[class] and 1 to launches[class] (host arrays of
+   n_classes >= DEC_K_COUNT entries).  Same arguments and results as dec_step. */
 DEC_API dec_status dec_profile_step(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
                             void *kv_cache, float *logits_out, int32_t *argmax_out,
                             dec_stream_t stream, double *ms, int *launches, int n_classes);

@@ -122,8 +122,11 @@ struct dec_handle {
   cudaGraphExec_t exec = nullptr;
   bool have_graph = false;
   StepPtrs captured{};
-  // profiling events
+  // profiling: events around every launch; the stream is held (by a sleeping kernel
+  // on hold_stream) until the host has enqueued the whole step
   std::vector<cudaEvent_t> events;
+  cudaStream_t hold_stream = nullptr;
+  cudaEvent_t hold_ev = nullptr;
   // debug: stop an eager step after this many launches (-1: no limit)
   int launch_limit = -1;
   // debug: per-launch %globaltimer stamps (device, 3 per launch) or null
@@ -734,6 +737,8 @@ extern "C" void dec_destroy(dec_handle* h) {
   if (!h) return;
   drop_graph(h);
   for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  if (h->hold_ev) cudaEventDestroy(h->hold_ev);
+  if (h->hold_stream) cudaStreamDestroy(h->hold_stream);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->wmem) cudaFree(h->wmem);
   if (h->ws) cudaFree(h->ws);
@@ -850,6 +855,12 @@ extern "C" dec_status dec_profile_step(dec_handle* h, const int32_t* token_ids, 
     h->events.push_back(ev);
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!h->hold_stream) DEC_CUDA(cudaStreamCreateWithFlags(&h->hold_stream, cudaStreamNonBlocking));
+  if (!h->hold_ev) DEC_CUDA(cudaEventCreateWithFlags(&h->hold_ev, cudaEventDisableTiming));
+  // about 10 us of host time per launch to enqueue, plus a margin
+  DEC_CUDA(launch_hold(h->hold_stream, 200000ull + 10000ull * static_cast<unsigned long long>(n)));
+  DEC_CUDA(cudaEventRecord(h->hold_ev, h->hold_stream));
+  DEC_CUDA(cudaStreamWaitEvent(cs, h->hold_ev, 0));
   std::vector<int> classes;
   if ((st = enqueue_step(h, sp, cs, false, &classes)) != DEC_OK) return st;
   DEC_CUDA(cudaStreamSynchronize(cs));

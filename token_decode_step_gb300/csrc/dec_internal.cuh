@@ -271,6 +271,7 @@ cudaError_t pack_frag_q4(cudaStream_t s, unsigned char* dst, const uint32_t* w_a
                          int dst_rows);
 cudaError_t debug_dequant_frag(cudaStream_t s, float* out, const void* w, int wfmt, int rows_out, int K,
                                int row_offset, int interleave_block, int which_half);
+cudaError_t launch_hold(cudaStream_t s, unsigned long long ns);
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch);
 

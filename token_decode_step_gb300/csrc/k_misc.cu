@@ -341,6 +341,25 @@ __global__ void k_advance(const int32_t* argmax, int32_t* tokens, int32_t* posit
   }
 }
 
+// Profiling aid: one thread sleeps until `ns` nanoseconds of %globaltimer have passed
+// (at most 2 ns / 256 sleeps of 256 ns), so that a stream held on it fills up with the
+// host's launches before the first of them runs.
+__global__ void k_hold(unsigned long long ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  const unsigned long long max_iter = ns / 128 + 1;
+  for (unsigned long long i = 0; i < max_iter; ++i) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 >= ns) break;
+    __nanosleep(256);
+  }
+}
+
+cudaError_t launch_hold(cudaStream_t s, unsigned long long ns) {
+  k_hold<<<1, 1, 0, s>>>(ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch) {
   k_advance<<<(batch + 127) / 128, 128, 0, s>>>(argmax, tokens, positions, batch);
