@@ -248,32 +248,66 @@ def run_ours(args, rank: int, world: int) -> dict | None:
             "clocks": clk.summary()}
 
 
-def cpu_oracle_sample(config: str, budget_s: float) -> dict:
-    """Time the CPU oracle (as it stands) on whole decode steps of the workload,
-    stopping after the first step that ends past budget_s."""
+def cpu_oracle_sample(config: str, warmup: int, steps: int, budget_s: float) -> dict:
+    """Time the CPU oracle (as it stands) on whole greedy decode steps of the workload.
+
+    A bounded sample: batched workloads run their first sequence only (its own KV
+    cache and prompt token); `warmup` untimed steps (the first converts the weights
+    to float64), then up to `steps` timed steps, stopping after the first one that
+    ends past `budget_s`.
+    """
     import numpy as np
     import oracle
     import synthetic
-    wl = synthetic.WORKLOADS[config].replace(steps=8)
+    import torch
+    wl = synthetic.WORKLOADS[config].replace(steps=warmup + steps + 1)
     model = synthetic.generate(wl, device="cpu")
     m = oracle.OracleModel.from_synthetic(wl, model, cache_weights=True)
-    kv = model["kv"].view(__import__("torch").int16).numpy().view(np.uint16).copy()
-    tokens = model["tokens"].numpy().copy()
-    pos = model["positions"].numpy().copy()
-    done = 0
-    t0 = time.perf_counter()
-    while True:
+    bs = 1 if wl.batch > 1 else wl.batch
+    kv = model["kv"][:, :, :bs].contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    tokens = model["tokens"][:bs].numpy().copy()
+    pos = model["positions"][:bs].numpy().copy()
+
+    def step():
+        nonlocal tokens, pos
         _, am = oracle.decode_step(m, kv, tokens, pos)
         tokens = am.astype(np.int32)
         pos = pos + 1
+
+    for _ in range(warmup):
+        step()
+    done = 0
+    t0 = time.perf_counter()
+    while done < steps:
+        step()
         done += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or done >= wl.steps:
+        if time.perf_counter() - t0 >= budget_s:
             break
+    el = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": wl.batch * done / el, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} greedy step(s) of {config} (batch {wl.batch}) from the initial cache, "
-                      f"first-use float64 weight conversion included, {el:.1f} s"}
+    seqs = f"sequence 0 of {wl.batch}" if bs < wl.batch else f"batch {wl.batch}"
+    return {"value": bs * done / el, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} timed greedy step(s) of {config} ({seqs}) after {warmup} untimed "
+                      f"(the first converts the weights to float64), {el:.1f} s"}
+
+
+def workload_config(wl, world: int) -> dict:
+    return {
+        "workload": wl.name, "batch": wl.batch, "layers": wl.n_layers, "hidden": wl.hidden,
+        "cached_positions": wl.prefill if not isinstance(wl.prefill, tuple) else list(wl.prefill),
+        "weight_format": wl.weight_format, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "l2": ("inputs larger than L2 (per-step weights exceed 129 MB); no flush" if weight_bytes(wl) > 129e6 else
+               "inputs smaller than L2 and not flushed: a cache-warm number"),
+        "timing": "CUDA events on the launching stream, CUDA-graph replay per step",
+    }
+
+
+def weight_bytes(wl) -> float:
+    """Bytes of every linear layer of the workload (bf16: 2 per weight, 4-bit: 0.5625)."""
+    per = 2.0 if wl.weight_format == "bf16" else 0.5 + 4.0 / 64
+    sh = wl.shapes()
+    n = sum(a * b for k, (a, b) in sh.items() if k != "lm_head") * wl.n_layers + sh["lm_head"][0] * sh["lm_head"][1]
+    return n * per
 
 
 def main():
@@ -287,6 +321,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="reference arm: stop the timed oracle steps after this many seconds")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -297,12 +333,20 @@ def main():
         # the reference arm is the CPU oracle, timed as it stands on the host cores (rank 0 only)
         if rank != 0:
             return
-        s = cpu_oracle_sample(args.config, args.cpu_budget)
+        import synthetic
+        t0 = time.perf_counter()
+        s = cpu_oracle_sample(args.config, args.warmup, args.steps, args.ref_budget)
+        cfg = workload_config(synthetic.WORKLOADS[args.config], world)
+        cfg["timing"] = "host wall clock over the timed oracle steps"
         print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": s["value"], "unit": "tok/s", "n_gpus": 0,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "data": "synthetic",
-            "config": {"workload": args.config}, "cpu_baseline": s,
-            "e2e": {"value": s["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "impl": "reference", "metric": METRIC, "value": round(s["value"], 4), "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000.0 / s["value"], 2) if s["value"] else None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, random-init weights; see synthetic/workloads.py)",
+            "config": cfg, "cpu_baseline": s,
+            "e2e": {"value": round(s["value"], 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.perf_counter() - t0, 1),
         }))
         return
 
@@ -342,13 +386,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if wl.weight_format == "bf16" else "int4-affine-g64",
         "data": "synthetic (seeded, random-init weights; see synthetic/workloads.py)",
-        "config": {
-            "workload": args.config, "batch": B, "layers": wl.n_layers, "hidden": wl.hidden,
-            "cached_positions": wl.prefill if not isinstance(wl.prefill, tuple) else list(wl.prefill),
-            "weight_format": wl.weight_format, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "inputs larger than L2 (per-step weights exceed 129 MB); no flush",
-            "timing": "CUDA events on the launching stream, CUDA-graph replay per step",
-        },
+        "config": workload_config(wl, world),
         "step_hbm_gbs": round(step_gbs, 1),
         "step_hbm_frac": round(step_gbs / hbm_peak, 4),
         "step_bytes": int(r["bytes_step"]),
@@ -375,7 +413,7 @@ def main():
         if tr and tr.get("csrc") == csrc_digest():
             line["roofline"]["traffic"] = tr["bytes"]
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(args.config, args.cpu_budget)
+        line["cpu_baseline"] = cpu_oracle_sample(args.config, 1, 1000, args.cpu_budget)
     print(json.dumps(line))
 
 
