@@ -469,8 +469,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
 namespace {
 
 // Launch shapes: 0 = clusters of 8, shallow ring; 1 = clusters of 8, deep ring;
-// 2 = clusters of 16 (a non-portable size), deep ring.
-constexpr int kShapes = 3;
+// 2 = clusters of 16, deep ring; 3 = clusters of 12, deep ring (16 and 12 are
+// non-portable sizes).
+constexpr int kShapes = 4;
 
 template <int D, int G, int C, bool DEEP>
 cudaLaunchConfig_t attn_config(const AttnParams& p, cudaStream_t stream, bool pdl, cudaLaunchAttribute (&attr)[2]) {
@@ -521,11 +522,13 @@ cudaError_t prepare_all(int (&max_clusters)[kShapes]) {
   cudaError_t e;
   if ((e = prepare_attn_t<D, G, 8, false>(&max_clusters[0])) != cudaSuccess) return e;
   if ((e = prepare_attn_t<D, G, 8, true>(&max_clusters[1])) != cudaSuccess) return e;
-  return prepare_attn_t<D, G, 16, true>(&max_clusters[2]);
+  if ((e = prepare_attn_t<D, G, 16, true>(&max_clusters[2])) != cudaSuccess) return e;
+  return prepare_attn_t<D, G, 12, true>(&max_clusters[3]);
 }
 
 template <int D, int G>
 cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
+  if (shape == 3) return launch_attn_t<D, G, 12, true>(c, p);
   if (shape == 2) return launch_attn_t<D, G, 16, true>(c, p);
   if (shape == 1) return launch_attn_t<D, G, 8, true>(c, p);
   return launch_attn_t<D, G, 8, false>(c, p);
@@ -536,7 +539,7 @@ cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
 constexpr int kMaxAttnDevices = 64;
 struct AttnCaps {
   int num_sms = 0;
-  int max_clusters[kShapes] = {0, 0, 0};
+  int max_clusters[kShapes] = {0, 0, 0, 0};
 };
 AttnCaps g_caps[kMaxAttnDevices][2][3];
 std::mutex g_caps_mu;
@@ -550,9 +553,9 @@ size_t attention_smem_bytes(int head_dim) {
   return head_dim == 64 ? AttnCfg<64, false>::kBytes : AttnCfg<128, false>::kBytes;
 }
 
-// The widest shape whose grid runs in one wave: 16-CTA clusters when B n_kv of them
-// fit at once, else 8-CTA clusters with the deep ring when one CTA per SM suffices,
-// else the shallow ring.
+// The widest shape whose grid runs in one wave with one CTA per SM: 16-, then 12-, then
+// 8-CTA clusters with the deep ring when B n_kv of them fit at once (the occupancy
+// query counts what the GPCs can place), else 8-CTA clusters with the shallow ring.
 int attention_shape(int B, int nkv, int head_dim, int G) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttnDevices) return 0;
@@ -566,6 +569,7 @@ int attention_shape(int B, int nkv, int head_dim, int G) {
   const long long clusters = static_cast<long long>(B) * nkv;
   if (caps.num_sms <= 0) return 0;
   if (clusters * 16 <= caps.num_sms && clusters <= caps.max_clusters[2]) return 2;
+  if (clusters * 12 <= caps.num_sms && clusters <= caps.max_clusters[3]) return 3;
   if (clusters * 8 <= caps.num_sms && clusters <= caps.max_clusters[1]) return 1;
   return 0;
 }
