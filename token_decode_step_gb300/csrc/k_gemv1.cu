@@ -116,6 +116,29 @@ __device__ __forceinline__ void dot_q4_word(uint32_t w, const float* x, float& d
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// Warp sums of 8 values at once by halving exchanges: after the xor-16, -8 and -4 steps
+// each lane holds a partial of value (lane >> 2) & 7 only, then xor-2 and xor-1 finish
+// it (9 shuffles instead of 40).  Every lane returns the full sum of its value; the sum
+// order is fixed.
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+  float a[4], b[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[i + 4] : v[i], send = b4 ? v[i] : v[i + 4];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? a[i + 2] : a[i], send = b3 ? a[i] : a[i + 2];
+    b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  float c = (b2 ? b[1] : b[0]) + __shfl_xor_sync(0xffffffffu, b2 ? b[0] : b[1], 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
 // This CTA's share of the next attention's cached K/V rows, prefetched into L2 by the
 // lanes of one warp.  The 2 B n_kv runs (plane, sequence, head) of P_b rows each are
 // dealt to the CTAs round-robin; the CTAs of a run split it into equal 16-byte-aligned
@@ -254,10 +277,10 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
 
     // block reduction of the R row sums (and, once, the sum of squares); fixed order:
     // lanes, then warps 0..n-1
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float v = warp_sum(acc[r]);
-      if (lane == 0) red[warp][r] = v;
+    static_assert(R == 8, "warp_sum8 reduces 8 rows");
+    {
+      const float v = warp_sum8(acc, lane);
+      if ((lane & 3) == 0) red[warp][lane >> 2] = v;
     }
     if (IN == kInNorm && first) {
       const float v = warp_sum(ssq);
