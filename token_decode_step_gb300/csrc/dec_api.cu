@@ -228,18 +228,20 @@ int choose_splits(int N, int K, int fmt, int num_sms) {
   return S;
 }
 
-// Batched path: inputs staged per chunk (shared-memory bound) and K splits so that the
-// grid covers the SMs at least twice.
-
-
+// Batched path: inputs staged per chunk (shared-memory bound) and K splits until the grid
+// covers the SMs once (bf16) or twice (4-bit, whose CTAs are issue-bound), keeping at
+// least 512 (bf16) or 1024 (4-bit) inputs per split: finer splits measured slower, the
+// partial-sum round trip (fence, ticket, reload) outweighing the extra CTAs.
 void choose_tc_splits(PackedLinear& L, int wfmt, int ny, int num_sms) {
   const int rpb = gemm_tc_rows_per_block(wfmt, ny);
   const int blocks = (L.Npad + rpb - 1) / rpb;
   const int kc_max = gemm_tc_chunk(ny);
+  const long long cover = wfmt == kWQ4 ? 2ll * num_sms : num_sms;
+  const int min_ks = wfmt == kWQ4 ? 1024 : 512;
   int S = 1;
-  while (static_cast<long long>(blocks) * S < 2ll * num_sms) {
+  while (static_cast<long long>(blocks) * S < cover) {
     const int S2 = S * 2;
-    if (L.K % S2 != 0 || (L.K / S2) % kGroup != 0 || L.K / S2 < 256) break;
+    if (L.K % S2 != 0 || (L.K / S2) % kGroup != 0 || L.K / S2 < min_ks) break;
     S = S2;
   }
   L.S = S;

@@ -53,7 +53,7 @@ size_t gemm_tc_smem_bytes(int wfmt, int ny, int kc) {
 }
 
 template <int WF, int NY, int TPW, int WARPS, int IN, int EPI>
-__global__ void __launch_bounds__(WARPS * 32) k_gemm_tc(GemmParams p) {
+__global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(GemmParams p) {
   constexpr int NT = 2 * NY;  // n-tiles of the MMA: hi rows of every token, then lo rows
   constexpr int XR = NT * 8;  // staged rows per chunk buffer
   constexpr int NTH = WARPS * 32;
