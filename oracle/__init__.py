@@ -20,6 +20,9 @@ Sources (page title and section):
     gemv + add, rms_norm, gate/up gemv, silu_mul, down gemv + add, final
     rms_norm, lm_head gemv) and section on GPU sampling (greedy = argmax over
     the vocab axis).
+  * The same Butter section on GPU sampling for oracle/sampling.py: temperature,
+    top-k, top-p, then an inverse-CDF draw from a counter-based generator
+    (Philox4x32-10 from its publication; its known-answer vectors pin it).
   * oxinfer (docs.rs crate page), section "MLX checkpoints": packed 4-bit
     weights, eight per uint32, bf16 scale and bias per group of 64,
     w = scale * q + bias.
@@ -44,6 +47,7 @@ plus an independent scalar-loop restatement on a tiny shape.
 
 from .numerics import bf16_bits_to_f64, f64_to_bf16_bits, round_to_bf16  # noqa: F401
 from .affine4 import dequant_affine4_g64, dequant_affine4_g64_f32  # noqa: F401
+from . import sampling  # noqa: F401
 from .decoder import (  # noqa: F401
     OracleModel, rmsnorm, rope_rotate_half, softmax, gqa_attention, lse_merge, silu,
     argmax_lowest, decode_step, tie_exempt,
