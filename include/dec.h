@@ -268,6 +268,33 @@ DEC_API dec_status dec_attention_noalloc(const dec_config *cfg, int layer, const
                                          const void *k_norm, const int32_t *positions, void *kv_cache, float *out,
                                          dec_stream_t stream);
 
+/* ---- On-device sampling (Butter architecture.md, GPU sampling section: the sampling
+   kernel after the lm_head; temperature, top-k, top-p, inverse-CDF draw, 4-byte
+   token out).  Per row b of logits [batch][vocab] (float32, device):
+     temperature <= 0: tokens[b] = argmax (lowest index on ties);
+     else: the k most likely tokens, k = top_k if 1 <= top_k <= 1024, else 1024 (at
+     most vocab), ordered by (logit descending, index ascending); p_j = exp((l_j -
+     l_0) / temperature); if top_p < 1, the shortest prefix whose cumulative p reaches
+     top_p times the sum; tokens[b] = the first kept candidate whose cumulative p
+     exceeds u times the kept sum, where u = (x0 >> 8) * 2^-24 and x0 is the first
+     word of Philox4x32-10 with key (seed low, seed high 32 bits) and counter (offset
+     low, offset high, b, 0).  When offset_device is not NULL the offset is read from
+     that device word when the kernel runs (so a captured graph can advance it).
+   Logits of -0 rank as +0 and NaN below every number.  One kernel launch on
+   `stream`, no allocation.  Errors: NULL logits/tokens/params, batch or vocab < 1,
+   top_p not in (0, 1] or a non-finite temperature -> DEC_ERR_INVALID_ARG. */
+typedef struct dec_sampling_params {
+    float temperature;
+    int top_k;
+    float top_p;
+    unsigned long long seed;
+    unsigned long long offset;
+    const unsigned long long *offset_device;
+} dec_sampling_params;
+
+DEC_API dec_status dec_sample(const float *logits, int batch, int vocab, const dec_sampling_params *params,
+                              int32_t *tokens, dec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

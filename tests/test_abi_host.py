@@ -91,3 +91,21 @@ def test_step_rejects_null_handle(dec):
     st = dec.lib.dec_step(None, 16, 16, 16, None, 16, None)
     assert st == dec.DEC_ERR_INVALID_ARG
     assert "handle" in dec.dec_last_error()
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(logits=None), "NULL"),
+    (dict(tokens=None), "NULL"),
+    (dict(batch=0), "batch"),
+    (dict(top_p=0.0), "top_p"),
+    (dict(top_p=1.5), "top_p"),
+    (dict(temperature=float("nan")), "temperature"),
+])
+def test_sample_rejects_bad_arguments(dec, kw, msg):
+    args = dict(logits=16, batch=1, vocab=8, tokens=16, temperature=1.0, top_p=1.0)
+    args.update(kw)
+    prm = dec.SamplingParams(temperature=args["temperature"], top_k=0, top_p=args["top_p"], seed=1, offset=0,
+                             offset_device=None)
+    st = dec.lib.dec_sample(args["logits"], args["batch"], args["vocab"], prm, args["tokens"], None)
+    assert st == dec.DEC_ERR_INVALID_ARG
+    assert msg in dec.dec_last_error()

@@ -1029,3 +1029,29 @@ extern "C" dec_status dec_set_timeline(dec_handle* h, unsigned long long* stamps
   drop_graph(h);  // the next step captures the kernels with the new pointer
   return DEC_OK;
 }
+
+// ---------------------------------------------------------------- sampling
+
+extern "C" dec_status dec_sample(const float* logits, int batch, int vocab, const dec_sampling_params* params,
+                                 int32_t* tokens, dec_stream_t stream) {
+  if (!logits || !tokens || !params || batch < 1 || vocab < 1) {
+    set_err("dec_sample: NULL logits/tokens/params or batch/vocab < 1");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (!(params->top_p > 0.f && params->top_p <= 1.f) || !std::isfinite(params->temperature)) {
+    set_err("dec_sample: top_p must be in (0, 1] and temperature finite");
+    return DEC_ERR_INVALID_ARG;
+  }
+  SampleParams sp{};
+  sp.logits = logits;
+  sp.V = vocab;
+  sp.temperature = params->temperature;
+  sp.top_k = params->top_k;
+  sp.top_p = params->top_p;
+  sp.seed = params->seed;
+  sp.offset = params->offset;
+  sp.offset_dev = params->offset_device;
+  sp.tokens = tokens;
+  DEC_CUDA(launch_sample(reinterpret_cast<cudaStream_t>(stream), sp, batch));
+  return DEC_OK;
+}

@@ -97,6 +97,19 @@ struct AttnParams {
   unsigned* status;
 };
 
+// On-device sampling of one token per row of logits (k_sample.cu).
+constexpr int kSampleMaxK = 1024;  // candidates kept before top-p and the draw
+struct SampleParams {
+  const float* logits;  // [B][V]
+  int V;
+  float temperature;    // <= 0: greedy
+  int top_k;            // 1..kSampleMaxK, else kSampleMaxK
+  float top_p;          // (0, 1]; 1: no cut
+  unsigned long long seed, offset;
+  const unsigned long long* offset_dev;  // if not null, the offset is read here
+  int32_t* tokens;      // [B]
+};
+
 struct EmbedParams {
   Timeline tl;
   const __nv_bfloat16* embed;   // [V][H]
@@ -272,6 +285,7 @@ cudaError_t pack_frag_q4(cudaStream_t s, unsigned char* dst, const uint32_t* w_a
 cudaError_t debug_dequant_frag(cudaStream_t s, float* out, const void* w, int wfmt, int rows_out, int K,
                                int row_offset, int interleave_block, int which_half);
 cudaError_t launch_hold(cudaStream_t s, unsigned long long ns);
+cudaError_t launch_sample(cudaStream_t s, const SampleParams& p, int batch);
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch);
 

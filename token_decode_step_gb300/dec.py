@@ -28,6 +28,14 @@ DEC_K_EMBED, DEC_K_QKV, DEC_K_ATTN, DEC_K_OPROJ, DEC_K_GATEUP, DEC_K_DOWN, DEC_K
 KERNEL_CLASS_NAMES = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
 
 
+class SamplingParams(ctypes.Structure):
+    """dec_sampling_params (include/dec.h)."""
+    _fields_ = [
+        ("temperature", ctypes.c_float), ("top_k", ctypes.c_int), ("top_p", ctypes.c_float),
+        ("seed", ctypes.c_ulonglong), ("offset", ctypes.c_ulonglong), ("offset_device", ctypes.c_void_p),
+    ]
+
+
 class DecConfig(ctypes.Structure):
     _fields_ = [
         ("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int),
@@ -84,6 +92,7 @@ def _load() -> ctypes.CDLL:
                                          ctypes.c_size_t, vp]),
         "dec_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                                  vp]),
+        "dec_sample": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(SamplingParams), vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -185,6 +194,10 @@ def dec_attention_noalloc(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_n
                           kv_cache: int, out: int, stream: int = 0) -> int:
     return _check(lib.dec_attention_noalloc(ctypes.byref(cfg), layer, qkv, q_norm, k_norm, positions, kv_cache,
                                             out, stream), "dec_attention_noalloc")
+
+
+def dec_sample(logits: int, batch: int, vocab: int, params: SamplingParams, tokens: int, stream: int = 0) -> int:
+    return _check(lib.dec_sample(logits, batch, vocab, ctypes.byref(params), tokens, stream), "dec_sample")
 
 
 def dec_debug_step_prefix(h: int, token_ids: int, positions: int, kv_cache: int, logits_out: int | None,
