@@ -238,6 +238,25 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         e2e_step()
     e2e_s = time.perf_counter() - t0
 
+    # the sampling kernel (dec_sample, the step after the argmax) on this step's logits;
+    # a separate entry point, not part of the timed step
+    prm = D.SamplingParams(temperature=0.8, top_k=50, top_p=0.9, seed=1, offset=0, offset_device=None)
+    stok = torch.empty((B,), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        D.dec_sample(logits.data_ptr(), B, V, prm, stok.data_ptr(), stream.cuda_stream)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_samp = 20
+    s0.record(stream)
+    for i in range(n_samp):
+        prm.offset = i
+        D.dec_sample(logits.data_ptr(), B, V, prm, stok.data_ptr(), stream.cuda_stream)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    samp_us = s0.elapsed_time(s1) * 1000.0 / n_samp
+    sampling = {"us_per_call": round(samp_us, 2), "rows": B, "vocab": V,
+                "params": "temperature 0.8, top_k 50, top_p 0.9", "logit_bytes": B * V * 4,
+                "logit_gbs": round(B * V * 4 / (samp_us * 1e-6) / 1e9, 1)}
+
     per_step = [1, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, 1]  # launches per class
     bytes_step = sum(n * dec.kernel_bytes(c, mean_p) for c, n in enumerate(per_step))
     cls_bytes = [dec.kernel_bytes(c, prof_mean_p) for c in range(D.DEC_K_COUNT)]
@@ -245,7 +264,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     dec.close()
     return {"ms": ms, "mean_p": mean_p, "bytes_step": bytes_step, "cls_ms": cls_ms, "cls_n": cls_n,
             "cls_bytes": cls_bytes, "e2e_s": e2e_s, "launches": launches, "wl": wl0, "B": B,
-            "clocks": clk.summary()}
+            "clocks": clk.summary(), "sampling": sampling}
 
 
 def cpu_oracle_sample(config: str, warmup: int, steps: int, budget_s: float) -> dict:
@@ -399,6 +418,7 @@ def main():
         "kernel_share": {D.KERNEL_CLASS_NAMES[c]: round(cls_ms[c] / max(1e-12, sum(cls_ms)), 4)
                          for c in range(D.DEC_K_COUNT)},
     }
+    line["sampling"] = r["sampling"]
     e2e_tok_s = B * args.e2e_steps / r["e2e_s"]
     line["e2e"] = {"value": round(e2e_tok_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 8 * B,
                    "d2h_bytes_per_step": 4 * B}

@@ -6,7 +6,8 @@
 // top-p by a cumulative-softmax threshold, an inverse-CDF sample with an RNG state,
 // a 4-byte token id as the only output).
 //
-// Steps in a CTA of 1024 threads:
+// Steps, for one row per 8-CTA thread-block cluster of 1024 threads each (CTA r scans
+// 1/8 of the row; counts and candidates meet in rank 0's shared memory):
 //  1. order keys: every float32 logit maps to a uint32 whose unsigned order is the
 //     float order (-0 taken as +0, NaN below everything);
 //  2. the k-th largest key by a 4-pass radix select (8-bit digits, shared-memory
@@ -24,6 +25,7 @@ namespace dec {
 namespace {
 
 constexpr int kSampleThreads = 1024;
+constexpr int kSampleCluster = 8;  // CTAs per row
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -34,6 +36,24 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+constexpr int kSampleUnroll = 8;   // loads in flight per thread in each pass over a row
+
+// keys of elements base + u * kSampleThreads + threadIdx.x, u < kSampleUnroll (0 past the end):
+// all loads issued before any is used
+__device__ __forceinline__ void load_keys(const float* lg, int V, int base, uint32_t (&keys)[kSampleUnroll]) {
+  float v[kSampleUnroll];
+#pragma unroll
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    const int i = base + u * kSampleThreads + static_cast<int>(threadIdx.x);
+    v[u] = i < V ? __ldg(lg + i) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    const int i = base + u * kSampleThreads + static_cast<int>(threadIdx.x);
+    keys[u] = i < V ? order_key(v[u]) : 0u;
+  }
 }
 
 // Philox4x32-10: returns the first output word for (counter, key).
@@ -77,22 +97,83 @@ __device__ float block_scan(float v, float* warp_tot) {
   return warp > 0 ? v + warp_tot[warp - 1] : v;
 }
 
+// shared::cluster helpers (rank 0 holds the row's histograms and candidates)
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void* smem_ptr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(smem_ptr)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_red_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void cl_st_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void cl_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cl_ld_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One row per thread-block cluster of kSampleCluster CTAs: CTA r scans the contiguous
+// slice [r per, (r + 1) per) of the row; the histograms, the selection state and the
+// candidates live in rank 0's shared memory, which finishes the row alone.
 __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleParams p) {
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cl_rank();
   const float* lg = p.logits + static_cast<size_t>(row) * p.V;
+  const int per = (p.V + kSampleCluster - 1) / kSampleCluster;
+  const int lo = static_cast<int>(rank) * per, hi = min(p.V, lo + per);
+
   __shared__ unsigned hist[256];
-  __shared__ unsigned long long cand[kSampleThreads];  // (key << 32) | (~index)
+  __shared__ unsigned ghist[4][256];                   // rank 0: the cluster's histogram per pass
+  __shared__ unsigned long long cand[kSampleThreads];  // rank 0: (key << 32) | (~index)
+  __shared__ unsigned long long best_all[kSampleCluster];  // rank 0: greedy, per CTA
+  __shared__ unsigned eq_cnt[kSampleCluster];          // rank 0: threshold ties per CTA
   __shared__ float warp_tot[32];
   __shared__ unsigned warp_cnt[32];
-  __shared__ unsigned s_prefix, s_remaining, s_ngt, s_eq_base;
+  __shared__ unsigned s_prefix, s_remaining, s_count_eq, s_slot, s_eq_base;  // rank 0's are the cluster's
   __shared__ int s_m, s_token;
   __shared__ unsigned long long s_best[32];
+  __shared__ float s_cum[kSampleThreads];
+
+  // rank 0 clears its cluster state, then the first barrier (also: every CTA is running
+  // before any remote access)
+  if (rank == 0) {
+    for (int i = tid; i < 4 * 256; i += kSampleThreads) (&ghist[0][0])[i] = 0u;
+    if (tid == 0) s_slot = 0u;
+  }
+  cand[tid] = 0ull;
+  cl_sync();
+  const uint32_t r0 = 0u;
 
   if (!(p.temperature > 0.f)) {  // greedy: the argmax, lowest index on ties
     unsigned long long best = 0ull;
-    for (int i = tid; i < p.V; i += kSampleThreads) {
-      const unsigned long long c = (static_cast<unsigned long long>(order_key(lg[i])) << 32) | (0xffffffffu - i);
-      best = c > best ? c : best;
+    for (int base = lo; base < hi; base += kSampleThreads * kSampleUnroll) {
+      uint32_t keys[kSampleUnroll];
+      load_keys(lg, hi, base, keys);
+#pragma unroll
+      for (int u = 0; u < kSampleUnroll; ++u) {
+        const int i = base + u * kSampleThreads + tid;
+        const unsigned long long c = (static_cast<unsigned long long>(keys[u]) << 32) | (0xffffffffu - i);
+        if (i < hi) best = c > best ? c : best;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -104,6 +185,12 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleParams p) {
     if (tid == 0) {
       unsigned long long b = 0ull;
       for (int w = 0; w < kSampleThreads / 32; ++w) b = s_best[w] > b ? s_best[w] : b;
+      cl_st_u64(cl_map(&best_all[rank], r0), b);
+    }
+    cl_sync();
+    if (rank == 0 && tid == 0) {
+      unsigned long long b = 0ull;
+      for (int r = 0; r < kSampleCluster; ++r) b = best_all[r] > b ? best_all[r] : b;
       p.tokens[row] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(b));
     }
     return;
@@ -112,67 +199,107 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleParams p) {
   int k = (p.top_k >= 1 && p.top_k <= kSampleMaxK) ? p.top_k : kSampleMaxK;
   k = k < p.V ? k : p.V;
 
-  // ---- 2. radix select of the k-th largest key
-  if (tid == 0) {
-    s_prefix = 0u;
-    s_remaining = static_cast<unsigned>(k);
-  }
-  unsigned mask = 0u;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  // ---- 2. radix select of the k-th largest key over the cluster
+  unsigned prefix = 0u, remaining = static_cast<unsigned>(k), count_eq = 0u, mask = 0u;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kSampleThreads) hist[i] = 0u;
     __syncthreads();
-    const unsigned prefix = s_prefix;
-    for (int i = tid; i < p.V; i += kSampleThreads) {
-      const uint32_t key = order_key(lg[i]);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    for (int base = lo; base < hi; base += kSampleThreads * kSampleUnroll) {
+      uint32_t keys[kSampleUnroll];
+      load_keys(lg, hi, base, keys);
+#pragma unroll
+      for (int u = 0; u < kSampleUnroll; ++u) {
+        // lanes with the same digit add once (logits crowd a few bins: unaggregated
+        // shared atomics on one address serialise)
+        const int i = base + u * kSampleThreads + tid;
+        const bool in = i < hi && (keys[u] & mask) == prefix;
+        const unsigned digit = in ? (keys[u] >> shift) & 255u : 256u;
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<unsigned>(__popc(peers)));
+      }
     }
     __syncthreads();
-    if (tid == 0) {  // the digit where the count from the top reaches the remaining rank
-      unsigned above = 0u, rem = s_remaining;
+    if (tid < 256 && hist[tid]) cl_red_add(cl_map(&ghist[pass][tid], r0), hist[tid]);
+    cl_sync();
+    if (rank == 0 && tid == 0) {  // the digit where the count from the top reaches the remaining rank
+      unsigned above = 0u;
       int d = 255;
       for (; d > 0; --d) {
-        if (above + hist[d] >= rem) break;
-        above += hist[d];
+        if (above + ghist[pass][d] >= remaining) break;
+        above += ghist[pass][d];
       }
       s_prefix = prefix | (static_cast<unsigned>(d) << shift);
-      s_remaining = rem - above;
+      s_remaining = remaining - above;
+      s_count_eq = ghist[pass][d];  // after the last pass: the elements equal to the threshold
     }
+    cl_sync();
+    prefix = cl_ld_u32(cl_map(&s_prefix, r0));
+    remaining = cl_ld_u32(cl_map(&s_remaining, r0));
+    count_eq = cl_ld_u32(cl_map(&s_count_eq, r0));
     mask |= 0xffu << shift;
-    __syncthreads();
   }
-  const uint32_t thr = s_prefix;
-  const unsigned need_eq = s_remaining;  // ties at the threshold taken, lowest indices first
-
-  // ---- 3. gather: keys above the threshold (any order), ties in index order
-  if (tid == 0) {
-    s_ngt = 0u;
-    s_eq_base = 0u;
-  }
-  cand[tid] = 0ull;
-  __syncthreads();
+  const uint32_t thr = prefix;
+  const unsigned need_eq = remaining;  // ties at the threshold taken, lowest indices first
   const unsigned ngt_total = static_cast<unsigned>(k) - need_eq;
-  for (int base = 0; base < p.V; base += kSampleThreads) {
-    const int i = base + tid;
-    const uint32_t key = i < p.V ? order_key(lg[i]) : 0u;
-    const bool gt = i < p.V && key > thr, eq = i < p.V && key == thr;
-    const unsigned long long c = (static_cast<unsigned long long>(key) << 32) | (0xffffffffu - i);
-    if (gt) cand[atomicAdd(&s_ngt, 1u)] = c;
-    const unsigned bal = __ballot_sync(0xffffffffu, eq);
-    if (lane == 0) warp_cnt[warp] = __popc(bal);
-    __syncthreads();
-    unsigned before = s_eq_base;
-    for (int w = 0; w < warp; ++w) before += warp_cnt[w];
-    before += __popc(bal & ((1u << lane) - 1u));
-    if (eq && before < need_eq) cand[ngt_total + before] = c;
+  const uint32_t slot_addr = cl_map(&s_slot, r0);
+
+  // ---- 3. gather into rank 0: keys above the threshold (any slot), ties in index order
+  if (count_eq == need_eq) {  // every tie is kept: slots by an atomic counter (the sort fixes the order)
+    for (int base = lo; base < hi; base += kSampleThreads * kSampleUnroll) {
+      uint32_t keys[kSampleUnroll];
+      load_keys(lg, hi, base, keys);
+#pragma unroll
+      for (int u = 0; u < kSampleUnroll; ++u) {
+        const int i = base + u * kSampleThreads + tid;
+        if (i < hi && keys[u] >= thr) {
+          const uint32_t slot = cl_atom_add(slot_addr, 1u);
+          cl_st_u64(cl_map(&cand[slot], r0), (static_cast<unsigned long long>(keys[u]) << 32) | (0xffffffffu - i));
+        }
+      }
+    }
+  } else {  // ties straddle the k-th place: the lowest indices among them, slices in rank order
+    unsigned my_eq = 0u;
+    for (int i = lo + tid; i < hi; i += kSampleThreads) my_eq += order_key(lg[i]) == thr ? 1u : 0u;
+    my_eq = __reduce_add_sync(0xffffffffu, my_eq);
+    if (lane == 0) warp_cnt[warp] = my_eq;
     __syncthreads();
     if (tid == 0) {
       unsigned t = 0u;
       for (int w = 0; w < kSampleThreads / 32; ++w) t += warp_cnt[w];
-      s_eq_base += t;
+      cl_st_u32(cl_map(&eq_cnt[rank], r0), t);
+    }
+    cl_sync();
+    if (tid == 0) {
+      unsigned b = 0u;
+      for (uint32_t r = 0; r < rank; ++r) b += cl_ld_u32(cl_map(&eq_cnt[r], r0));
+      s_eq_base = b;
     }
     __syncthreads();
-    if (s_eq_base >= need_eq && s_ngt >= ngt_total) break;  // uniform: shared values after a barrier
+    for (int base = lo; base < hi; base += kSampleThreads) {
+      const int i = base + tid;
+      const uint32_t key = i < hi ? order_key(lg[i]) : 0u;
+      const bool gt = i < hi && key > thr, eq = i < hi && key == thr;
+      const unsigned long long c = (static_cast<unsigned long long>(key) << 32) | (0xffffffffu - i);
+      if (gt) cl_st_u64(cl_map(&cand[cl_atom_add(slot_addr, 1u)], r0), c);
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) warp_cnt[warp] = __popc(bal);
+      __syncthreads();
+      unsigned before = s_eq_base;
+      for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+      before += __popc(bal & ((1u << lane) - 1u));
+      if (eq && before < need_eq) cl_st_u64(cl_map(&cand[ngt_total + before], r0), c);
+      __syncthreads();
+      if (tid == 0) {
+        unsigned t = 0u;
+        for (int w = 0; w < kSampleThreads / 32; ++w) t += warp_cnt[w];
+        s_eq_base += t;
+      }
+      __syncthreads();
+    }
   }
+  cl_sync();  // every candidate is in rank 0; no remote access follows
+  if (rank != 0) return;
 
   // ---- 4. bitonic sort, descending (logit descending, then index ascending)
   int P = 1;
@@ -198,7 +325,6 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleParams p) {
   float pj = 0.f;
   if (tid < k) pj = expf((key_value(static_cast<uint32_t>(cand[tid] >> 32)) - l0) / p.temperature);
   const float cum = block_scan(pj, warp_tot);
-  __shared__ float s_cum[kSampleThreads];
   s_cum[tid] = cum;
   if (tid == 0) s_m = k;
   __syncthreads();
@@ -227,8 +353,18 @@ __global__ void __launch_bounds__(kSampleThreads) k_sample(SampleParams p) {
 }  // namespace
 
 cudaError_t launch_sample(cudaStream_t s, const SampleParams& p, int batch) {
-  k_sample<<<batch, kSampleThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSampleCluster, batch);
+  cfg.blockDim = dim3(kSampleThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSampleCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_sample, p);
 }
 
 }  // namespace dec
