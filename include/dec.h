@@ -77,14 +77,24 @@ typedef enum {
 
 /* Model and run shape.  Supported (else DEC_ERR_UNSUPPORTED): head_dim in {64, 128};
    n_q_heads / n_kv_heads in {1, 2, 4}; hidden and intermediate multiples of 64;
-   vocab >= 1; batch 1..16 for bf16 weights and 1..32 for affine 4-bit (batch 1
-   runs CUDA-core GEMV kernels, larger batches tensor-core kernels); max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG): every
-   size positive, rms_eps > 0, rope_theta > 1, n_q_heads a multiple of n_kv_heads. */
+   vocab >= 1; rows = batch * tokens_per_seq at most 16 for bf16 weights and 32 for
+   affine 4-bit (one row runs CUDA-core GEMV kernels, more rows tensor-core kernels);
+   tokens_per_seq 0..8 (0 means 1); max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG):
+   every size positive, rms_eps > 0, rope_theta > 1, n_q_heads a multiple of n_kv_heads.
+
+   tokens_per_seq T > 1 makes dec_step a multi-token verify step (speculative decoding's
+   check of drafted tokens in one forward: ANEForge "LLMs on the ANE", "Speculative
+   decoding"; Butter architecture.md, phase 8): row r = b T + t carries token_ids[r] at position
+   positions[b] + t of sequence b, attends causally to that sequence's slots 0 ..
+   positions[b] + t, and its K/V are written at that slot; logits_out and argmax_out
+   hold one row per (b, t).  The result of row (b, t) is that of a one-token step of
+   sequence b at position positions[b] + t after the rows (b, 0..t-1). */
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
     float rms_eps, rope_theta;
     int linear_fmt;            /* dec_wfmt, applies to every linear including lm_head */
     int batch, max_ctx;        /* sequences per step; cache slots per sequence */
+    int tokens_per_seq;        /* new tokens per sequence and step: 1 (decode) .. 8 (verify); 0 = 1 */
 } dec_config;
 
 /* One linear layer, row-major [out][in] in device memory.  bf16: w only (scales,
@@ -123,15 +133,17 @@ typedef struct dec_handle dec_handle;
 DEC_API dec_handle *dec_create(const dec_config *cfg, const dec_weights *weights);
 
 /* One decode step (Butter "SINGLE-TOKEN DECODE" sequence), enqueued on `stream`.
-     token_ids  device int32 [batch]: input token per sequence.
-     positions  device int32 [batch]: P_b = cached positions of sequence b; the
-                step writes K/V slot P_b, attends over slots 0..P_b and applies
-                RoPE at angle P_b.  The caller advances positions.
+   With T = tokens_per_seq (1 unless set), rows = batch * T:
+     token_ids  device int32 [rows]: input token per row (row b T + t: token t of
+                sequence b).
+     positions  device int32 [batch]: P_b = cached positions of sequence b; row
+                (b, t) writes K/V slot P_b + t, attends over slots 0..P_b + t and
+                applies RoPE at angle P_b + t.  The caller advances positions.
      kv_cache   device, dec_kv_cache_bytes(cfg) bytes, bf16
                 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim] (plane 0 = K,
                 plane 1 = V, post-norm post-RoPE keys), caller-owned.
-     logits_out device float [batch][vocab], or NULL to skip writing logits.
-     argmax_out device int32 [batch]: greedy token (lowest index on equal
+     logits_out device float [rows][vocab], or NULL to skip writing logits.
+     argmax_out device int32 [rows]: greedy token (lowest index on equal
                 logits).  May alias token_ids (read happens first).
    Out-of-range token ids or positions are clamped on the device and flagged in
    the status word (dec_get_device_status); nothing outside the buffers is
@@ -193,7 +205,8 @@ DEC_API dec_status dec_profile_step(dec_handle *h, const int32_t *token_ids, con
    excluded.  Host-side arithmetic on the handle's config. */
 DEC_API double dec_kernel_bytes(const dec_handle *h, int kernel_class, double mean_cached_len);
 
-/* Number of kernels one dec_step launches. */
+/* Number of kernels one dec_step launches: 2 + 5 n_layers, or 2 + 6 n_layers for a
+   verify step (tokens_per_seq > 1: a K/V append kernel precedes each attention). */
 DEC_API int dec_launches_per_step(const dec_handle *h);
 
 /* Kernel-level entry point: the fused attention that dec_step runs for each layer
@@ -203,7 +216,8 @@ DEC_API int dec_launches_per_step(const dec_handle *h);
    "Correctness" and "What's inside"; Butter architecture.md "SINGLE-TOKEN DECODE"
    (rope, cache.append, sdpa_decode).
      cfg        uses n_layers, batch, n_q_heads, n_kv_heads, head_dim, max_ctx,
-                rms_eps, rope_theta (same limits as dec_create; any batch >= 1).
+                rms_eps, rope_theta (same limits as dec_create; any batch >= 1);
+                tokens_per_seq must be 0 or 1.
      qkv        device float [batch][(n_q + 2 n_kv) * head_dim]: the new token's raw
                 projections, q heads, then k heads, then v heads, head j at j*head_dim.
      q_norm, k_norm  device bf16 [head_dim].
@@ -221,12 +235,13 @@ DEC_API dec_status dec_attention(const dec_config *cfg, int layer, const float *
 
 /* Test hooks for kernel-by-kernel parity.  dec_debug_step_prefix runs the first
    n_launches kernels of one step (embedding = launch 1, then per layer QKV,
-   attention, O, gate/up, down, finally lm_head) as individual launches.
-   dec_debug_buffer copies a workspace buffer of the handle to device memory dst:
-   which 0: residual h float [batch][hidden]; 1: q,k,v projections float
-   [batch][(n_q + 2 n_kv) head_dim]; 2: attention output float [batch][n_q head_dim];
-   3: SwiGLU output float [batch][intermediate]; 4: residual sums of squares float
-   [batch][hidden / 8].  Both enqueue on `stream`. */
+   (K/V append for a verify step,) attention, O, gate/up, down, finally lm_head) as
+   individual launches.  dec_debug_buffer copies a workspace buffer of the handle to
+   device memory dst (rows = batch * tokens_per_seq):
+   which 0: residual h float [rows][hidden]; 1: q,k,v projections float
+   [rows][(n_q + 2 n_kv) head_dim]; 2: attention output float [rows][n_q head_dim];
+   3: SwiGLU output float [rows][intermediate]; 4: residual sums of squares float
+   [rows][hidden / 8].  Both enqueue on `stream`. */
 DEC_API dec_status dec_debug_step_prefix(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
                                          void *kv_cache, float *logits_out, int32_t *argmax_out,
                                          dec_stream_t stream, int n_launches);

@@ -50,5 +50,5 @@ from .affine4 import dequant_affine4_g64, dequant_affine4_g64_f32  # noqa: F401
 from . import sampling  # noqa: F401
 from .decoder import (  # noqa: F401
     OracleModel, rmsnorm, rope_rotate_half, softmax, gqa_attention, lse_merge, silu,
-    argmax_lowest, decode_step, tie_exempt,
+    argmax_lowest, decode_step, tie_exempt, verify_step,
 )

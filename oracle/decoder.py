@@ -237,3 +237,24 @@ def decode_step(m: OracleModel, kv: np.ndarray, tokens, positions):
     logits = m.linear(rmsnorm(h, m.vec("final_norm"), eps), "lm_head")
     am = np.array([argmax_lowest(logits[b]) for b in range(B)], dtype=np.int64)
     return logits, am
+
+
+def verify_step(m: OracleModel, kv: np.ndarray, tokens, positions):
+    """Multi-token verify step (speculative decoding's check of drafted tokens): for
+    each sequence b, tokens[b][0..T-1] at positions P_b .. P_b + T - 1.  Row (b, t) is,
+    by definition, the one-token step of sequence b at position P_b + t after the rows
+    (b, 0..t-1) were appended: T decode steps with the given tokens fed in (teacher
+    forcing), each appending its K/V.  Returns (logits float64 [B, T, V], argmax int64
+    [B, T]).  Sources: ANEForge "LLMs on the ANE", section "Speculative decoding" (a
+    draft proposes K tokens, the target verifies all K in one forward); Butter
+    architecture.md, phase 8 speculative decoding (one verifier pass scores all K
+    candidates, batched along the sequence)."""
+    tokens = np.asarray(tokens)
+    positions = np.asarray(positions)
+    T = tokens.shape[1]
+    logits, am = [], []
+    for t in range(T):
+        lg, a = decode_step(m, kv, tokens[:, t], positions + t)
+        logits.append(lg)
+        am.append(a)
+    return np.stack(logits, axis=1), np.stack(am, axis=1)

@@ -62,6 +62,9 @@ def test_kv_cache_bytes(dec):
     (dict(rms_eps=0.0), 1, "rms_eps"),
     (dict(linear_fmt=7), 1, "linear_fmt"),
     (dict(vocab=0), 1, "positive"),
+    (dict(tokens_per_seq=9), 2, "tokens_per_seq"),
+    (dict(tokens_per_seq=-1), 1, "tokens_per_seq"),
+    (dict(batch=5, tokens_per_seq=4), 2, "rows"),
 ])
 def test_create_rejects_bad_config(dec, kw, status, msg):
     with pytest.raises(dec.DecError) as ei:

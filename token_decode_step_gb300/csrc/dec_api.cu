@@ -87,6 +87,8 @@ struct dec_handle {
   int device = 0;
   int num_sms = 0;
   int wfmt = 0;
+  int tps = 1;   // tokens per sequence (1: decode; 2..8: verify)
+  int rows = 1;  // batch * tps: rows of every projection
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
@@ -187,9 +189,14 @@ dec_status validate(const dec_config* c) {
     set_err("hidden and intermediate must be multiples of 64");
     return DEC_ERR_UNSUPPORTED;
   }
-  if (c->batch > 1 && gemm_tc_ny(c->linear_fmt == DEC_W_BF16 ? kWBf16 : kWQ4, c->batch) == 0) {
-    set_err("batch %d: the batched path takes at most %d sequences for this weight format", c->batch,
-            c->linear_fmt == DEC_W_BF16 ? 16 : 32);
+  if (c->tokens_per_seq < 0 || c->tokens_per_seq > kMaxTokensPerSeq) {
+    set_err("tokens_per_seq must be 0..%d (got %d)", kMaxTokensPerSeq, c->tokens_per_seq);
+    return c->tokens_per_seq < 0 ? DEC_ERR_INVALID_ARG : DEC_ERR_UNSUPPORTED;
+  }
+  const int rows = c->batch * (c->tokens_per_seq > 1 ? c->tokens_per_seq : 1);
+  if (rows > 1 && gemm_tc_ny(c->linear_fmt == DEC_W_BF16 ? kWBf16 : kWQ4, rows) == 0) {
+    set_err("batch %d x tokens_per_seq: %d rows, the batched path takes at most %d for this weight format",
+            c->batch, rows, c->linear_fmt == DEC_W_BF16 ? 16 : 32);
     return DEC_ERR_UNSUPPORTED;
   }
   if (static_cast<long long>(c->max_ctx) * c->n_kv_heads * c->batch * c->head_dim > (1ll << 40)) {
@@ -297,7 +304,8 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.amax_key = h->amax_key;
   ep.status = h->status;
   ep.norm_w0 = h->layers[0].in_norm;
-  ep.xhl_out = c.batch > 1 ? h->xh_u : nullptr;
+  ep.xhl_out = h->rows > 1 ? h->xh_u : nullptr;
+  ep.T = h->tps;
   ep.tl = Timeline{h->timeline, 0};
   ep.V = c.vocab;
   ep.H = H;
@@ -305,7 +313,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.max_ctx = c.max_ctx;
   note(DEC_K_EMBED);
   ev_begin();
-  if ((st = check(launch_embed(lc, ep, c.batch), "embed")) != DEC_OK) return st;
+  if ((st = check(launch_embed(lc, ep, h->rows), "embed")) != DEC_OK) return st;
   ev_end();
   lc.pdl = pdl;
 
@@ -355,7 +363,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     note(cls);
     ev_begin();
     dec_status s2;
-    if (c.batch == 1) {
+    if (h->rows == 1) {
       s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
       GemmParams tp{};
@@ -366,7 +374,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       tp.S = L.S;
       tp.KS = L.K / L.S;
       tp.KC = L.KC;
-      tp.B = c.batch;
+      tp.B = h->rows;
       tp.xhl = xin;
       tp.xhl_out = xout;
       tp.next_norm_w = next_norm;
@@ -406,14 +414,26 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.positions = sp.positions;
     ap.kv = static_cast<__nv_bfloat16*>(sp.kv);
     ap.layer = l;
-    ap.B = c.batch;
+    ap.B = h->rows;
+    ap.T = h->tps;
     ap.nq = c.n_q_heads;
     ap.nkv = c.n_kv_heads;
     ap.max_ctx = c.max_ctx;
     ap.eps = c.rms_eps;
     ap.out = h->attn_o;
     ap.status = h->status;
-    ap.out_hl = c.batch > 1 ? h->xh_o : nullptr;
+    ap.out_hl = h->rows > 1 ? h->xh_o : nullptr;
+    if (h->tps > 1) {
+      // verify step: every row's K/V go into the cache before any row attends, so
+      // that row (b, t) sees the rows (b, 0..t-1) of this step
+      if (limit_hit()) return DEC_OK;
+      ++launched;
+      ap.tl = Timeline{h->timeline, launched - 1};
+      note(DEC_K_ATTN);
+      ev_begin();
+      if ((st = check(launch_kv_append(lc, ap, d), "kv append")) != DEC_OK) return st;
+      ev_end();
+    }
     if (limit_hit()) return DEC_OK;
     ++launched;
     ap.tl = Timeline{h->timeline, launched - 1};
@@ -526,6 +546,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   dec_handle* h = new dec_handle();
   h->cfg = c;
+  h->tps = c.tokens_per_seq > 1 ? c.tokens_per_seq : 1;
+  h->rows = c.batch * h->tps;
   h->wfmt = fmt == DEC_W_BF16 ? kWBf16 : kWQ4;
   auto fail = [&](const char* what, cudaError_t e) -> dec_handle* {
     set_err("%s: %s", what, cudaGetErrorString(e));
@@ -543,13 +565,13 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device)) != cudaSuccess)
       return fail("cudaDeviceGetAttribute", e);
     const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim * 2;
-    h->kv_prefetch = c.batch == 1 && kv_layer <= l2 / 4.0;
+    h->kv_prefetch = h->rows == 1 && kv_layer <= l2 / 4.0;
   }
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  const bool tc = c.batch > 1;
-  const int ny = tc ? gemm_tc_ny(h->wfmt, c.batch) : 0;
+  const bool tc = h->rows > 1;
+  const int ny = tc ? gemm_tc_ny(h->wfmt, h->rows) : 0;
   auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
@@ -657,8 +679,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   }
 
   const int G = nq / nkv;
-  // ---- workspace
-  const int B = c.batch;
+  // ---- workspace (one row per token of the step)
+  const int B = h->rows;
   int max_tiles = 0;
   size_t max_partials = 0;
   auto acc_lin = [&](const PackedLinear& L) {
@@ -725,7 +747,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if ((e = prepare_attention(d, G)) != cudaSuccess) return fail("attention kernel attributes", e);
   if (tc) {
     GemmParams gp{};
-    gp.B = c.batch;
+    gp.B = h->rows;
     gp.KC = gemm_tc_chunk(ny);
     const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
     for (auto& cb : combos)
@@ -815,12 +837,12 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       case 1: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = c.n_q_heads * d; break;
       case 2: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = (c.n_q_heads + c.n_kv_heads) * d; break;
       case 3: P = &L.o; rows = H; K = c.n_q_heads * d; break;
-      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = c.batch > 1 ? 8 : kGemvRows / 2; half = 0; break;
-      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = c.batch > 1 ? 8 : kGemvRows / 2; half = 1; break;
+      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = h->rows > 1 ? 8 : kGemvRows / 2; half = 0; break;
+      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = h->rows > 1 ? 8 : kGemvRows / 2; half = 1; break;
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  if (c.batch > 1) {
+  if (h->rows > 1) {
     DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
   } else {
     DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
@@ -838,7 +860,9 @@ extern "C" dec_status dec_advance(const int32_t* argmax, int32_t* token_ids, int
   return DEC_OK;
 }
 
-extern "C" int dec_launches_per_step(const dec_handle* h) { return h ? 5 * h->cfg.n_layers + 2 : 0; }
+extern "C" int dec_launches_per_step(const dec_handle* h) {
+  return h ? (h->tps > 1 ? 6 : 5) * h->cfg.n_layers + 2 : 0;
+}
 
 extern "C" dec_status dec_profile_step(dec_handle* h, const int32_t* token_ids, const int32_t* positions,
                                        void* kv_cache, float* logits_out, int32_t* argmax_out, dec_stream_t stream,
@@ -880,11 +904,12 @@ extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cac
   const dec_config& c = h->cfg;
   const double wb = wbytes_per_elem(c.linear_fmt);
   const double H = c.hidden, d = c.head_dim, nq = c.n_q_heads, nkv = c.n_kv_heads, I = c.intermediate, V = c.vocab;
-  const double B = c.batch;
+  const double B = h->rows, T = h->tps;
   switch (cls) {
     case DEC_K_EMBED: return B * H * 2.0;
     case DEC_K_QKV: return (nq + 2 * nkv) * d * H * wb + H * 2.0;
-    case DEC_K_ATTN: return B * nkv * 2.0 * d * 2.0 * (mean_cached_len + 1.0) + 2.0 * d * 2.0;
+    // every row reads its sequence's slots 0 .. P + t (t < T: its place among the step's rows)
+    case DEC_K_ATTN: return B * nkv * 2.0 * d * 2.0 * (mean_cached_len + 1.0 + (T - 1.0) / 2.0) + 2.0 * d * 2.0;
     case DEC_K_OPROJ: return H * nq * d * wb;
     case DEC_K_GATEUP: return 2.0 * I * H * wb + H * 2.0;
     case DEC_K_DOWN: return H * I * wb;
@@ -910,6 +935,10 @@ dec_status validate_attention_cfg(const dec_config* c, int layer) {
   if (c->n_q_heads % c->n_kv_heads != 0) {
     set_err("n_q_heads (%d) must be a multiple of n_kv_heads (%d)", c->n_q_heads, c->n_kv_heads);
     return DEC_ERR_INVALID_ARG;
+  }
+  if (c->tokens_per_seq > 1) {
+    set_err("attention: the stand-alone entry points take tokens_per_seq 0 or 1");
+    return DEC_ERR_UNSUPPORTED;
   }
   const int G = c->n_q_heads / c->n_kv_heads;
   if ((G != 1 && G != 2 && G != 4) || (c->head_dim != 64 && c->head_dim != 128)) {
@@ -993,7 +1022,7 @@ extern "C" dec_status dec_debug_buffer(dec_handle* h, int which, void* dst, size
     return DEC_ERR_INVALID_ARG;
   }
   const dec_config& c = h->cfg;
-  const size_t B = c.batch;
+  const size_t B = h->rows;
   const void* src = nullptr;
   size_t n = 0;
   switch (which) {

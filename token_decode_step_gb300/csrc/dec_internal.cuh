@@ -16,6 +16,7 @@ constexpr int kResGroup = 8;        // rows per partial sum-of-squares of the re
 constexpr int kGemvRows = 8;        // rows per CTA of the batch-1 GEMV
 constexpr int kAttnTile = 64;       // positions per attention smem tile
 constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
+constexpr int kMaxTokensPerSeq = 8; // verify step: new tokens per sequence
 constexpr int kGroup = 64;          // affine 4-bit group size
 constexpr int kGemmPrefetch = 4;    // 64-input weight units in flight per lane (batched path)
 
@@ -84,11 +85,14 @@ struct GemmParams {
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
 struct AttnParams {
   Timeline tl;
+  // B rows = sequences x T tokens per sequence; row r is token r % T of sequence r / T
+  // at position positions[r / T] + r % T (T <= 1: one row per sequence)
+  int T;
   const float* qkv;             // [B][(nq + 2 nkv) d] projections
   const __nv_bfloat16* q_norm;  // [d]
   const __nv_bfloat16* k_norm;  // [d]
   const float2* rope;           // [B][d/2] (cos, sin) at this step's positions
-  const int32_t* positions;     // [B]
+  const int32_t* positions;     // [B / T] cached positions per sequence
   __nv_bfloat16* kv;            // whole cache
   int layer, B, nq, nkv, max_ctx;
   float eps;
@@ -124,6 +128,7 @@ struct EmbedParams {
   const __nv_bfloat16* norm_w0;  // optional: first layer's input norm weight, for xhl_out
   __nv_bfloat16* xhl_out;        // optional: h * norm_w0 as bf16 hi, lo planes [2][B][H]
   int V, H, half_d, max_ctx;
+  int T;                         // tokens per sequence: row b at position positions[b / T] + b % T
 };
 
 // ---------------------------------------------------------------- device helpers
@@ -252,6 +257,7 @@ struct LaunchCtx {
 cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B);
 cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int in_mode, int epi);
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim);
+cudaError_t launch_kv_append(const LaunchCtx& c, const AttnParams& p, int head_dim);
 // batched tensor-core projection
 int gemm_tc_ny(int wfmt, int batch);            // 8-token n-tiles per hi/lo half, 0 if unsupported
 int gemm_tc_rows_per_block(int wfmt, int ny);   // weight rows one CTA covers

@@ -132,16 +132,20 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
-  int P = p.positions[b];
+  // row b is token b % tps of sequence b / tps (tps = 1: the one new token)
+  const int tps = p.T > 1 ? p.T : 1, seq = b / tps;
+  int P = p.positions[seq] + b % tps;
   P = P < 0 ? 0 : (P >= p.max_ctx ? p.max_ctx - 1 : P);  // flagged by the embedding kernel
   const int T = P + 1;
   int pos_begin, pos_end;
   attention_run(T, C, rank, &pos_begin, &pos_end);
   const int ntiles = (pos_end - pos_begin + kAttnTile - 1) / kAttnTile;
-  const bool has_new = (P >= pos_begin && P < pos_end);
+  // one token: this kernel appends slot P itself (and patches the stale copy it read);
+  // a verify step appended every row's slot in the previous kernel
+  const bool has_new = tps == 1 && (P >= pos_begin && P < pos_end);
 
-  const size_t plane = static_cast<size_t>(p.B) * p.nkv * p.max_ctx * D;
-  const size_t head_off = (static_cast<size_t>(b) * p.nkv + h) * p.max_ctx * D;
+  const size_t plane = static_cast<size_t>(p.B / tps) * p.nkv * p.max_ctx * D;
+  const size_t head_off = (static_cast<size_t>(seq) * p.nkv + h) * p.max_ctx * D;
   __nv_bfloat16* kbase = p.kv + (static_cast<size_t>(p.layer) * 2 + 0) * plane + head_off;
   __nv_bfloat16* vbase = p.kv + (static_cast<size_t>(p.layer) * 2 + 1) * plane + head_off;
 
@@ -150,17 +154,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   float* xchg = reinterpret_cast<float*>(smem + CF::kOffXchg);  // receive area of the cluster merge
   float* misc = reinterpret_cast<float*>(smem + CF::kOffMisc);
 
-  // Cached K/V tiles do not depend on upstream kernels of this step: request the
-  // first S-1 before the grid-dependency wait.
+  // Cached K/V tiles do not depend on upstream kernels of a one-token step: request the
+  // first S-1 before the grid-dependency wait (a verify step's are requested after it,
+  // since the previous kernel appended this step's slots).
+  auto first_tiles = [&]() {
 #pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
-    if (s < ntiles) {
-      const int pos0 = pos_begin + s * kAttnTile;
-      load_tile<D>(sStages + s * CF::kStageBytes, kbase, pos0, pos_end);
-      load_tile<D>(sStages + s * CF::kStageBytes + CF::kTileBytes, vbase, pos0, pos_end);
+    for (int s = 0; s < S - 1; ++s) {
+      if (s < ntiles) {
+        const int pos0 = pos_begin + s * kAttnTile;
+        load_tile<D>(sStages + s * CF::kStageBytes, kbase, pos0, pos_end);
+        load_tile<D>(sStages + s * CF::kStageBytes + CF::kTileBytes, vbase, pos0, pos_end);
+      }
+      cp_async_commit();
     }
-    cp_async_commit();
-  }
+  };
+  if (tps == 1) first_tiles();
   {  // zero the Q operand (rows 2G..15 stay zero)
     uint32_t* q32 = reinterpret_cast<uint32_t*>(smem + CF::kOffQ);
     for (int i = tid; i < 16 * D / 2; i += kAttnThreads) q32[i] = 0u;
@@ -183,6 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
 
   griddep_wait();
   tl_mark(p.tl, 1);
+  if (tps > 1) first_tiles();
   __syncthreads();
 
   float m_run = -INFINITY, l_run = 0.f;
@@ -466,6 +475,55 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   tl_mark(p.tl, 2);
 }
 
+// Verify step: the K/V of every row (token t of sequence b) into slot positions[b] + t,
+// before any row attends.  One warp per (row, KV head): per-head RMSNorm and RoPE of
+// k as in the attention prologue, bf16 rounding of k and v.
+template <int D>
+__global__ void __launch_bounds__(32) k_kv_append(AttnParams p) {
+  tl_mark(p.tl, 0);
+  const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
+  const int tps = p.T > 1 ? p.T : 1, seq = b / tps;
+  int P = p.positions[seq] + b % tps;
+  P = P < 0 ? 0 : (P >= p.max_ctx ? p.max_ctx - 1 : P);  // flagged by the embedding kernel
+  constexpr int E = D / 32;
+  float wk[E];
+  float2 cs[E / 2];
+#pragma unroll
+  for (int m = 0; m < E; ++m) wk[m] = bf16_to_f(p.k_norm[lane + 32 * m]);
+#pragma unroll
+  for (int m = 0; m < E / 2; ++m) cs[m] = p.rope[static_cast<size_t>(b) * (D / 2) + lane + 32 * m];
+  griddep_wait();
+  tl_mark(p.tl, 1);
+  const float* qkv_b = p.qkv + static_cast<size_t>(b) * (p.nq + 2 * p.nkv) * D;
+  float x[E], v[E];
+#pragma unroll
+  for (int m = 0; m < E; ++m) {
+    x[m] = qkv_b[p.nq * D + h * D + lane + 32 * m];
+    v[m] = qkv_b[(p.nq + p.nkv) * D + h * D + lane + 32 * m];
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < E; ++m) ss = fmaf(x[m], x[m], ss);
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / static_cast<float>(D) + p.eps);
+#pragma unroll
+  for (int m = 0; m < E; ++m) x[m] = (x[m] * inv) * wk[m];
+  const size_t plane = static_cast<size_t>(p.B / tps) * p.nkv * p.max_ctx * D;
+  const size_t slot = ((static_cast<size_t>(seq) * p.nkv + h) * p.max_ctx + P) * D;
+  __nv_bfloat16* kd = p.kv + static_cast<size_t>(p.layer) * 2 * plane + slot;
+  __nv_bfloat16* vd = kd + plane;
+#pragma unroll
+  for (int m = 0; m < E / 2; ++m) {  // rotate-half pairs (e, e + D/2)
+    const float a = x[m], c = x[m + E / 2];
+    kd[lane + 32 * m] = __float2bfloat16_rn(a * cs[m].x - c * cs[m].y);
+    kd[lane + 32 * (m + E / 2)] = __float2bfloat16_rn(c * cs[m].x + a * cs[m].y);
+  }
+#pragma unroll
+  for (int m = 0; m < E; ++m) vd[lane + 32 * m] = __float2bfloat16_rn(v[m]);
+  griddep_launch_dependents();
+  tl_mark(p.tl, 2);
+}
+
 namespace {
 
 // Launch shapes: 0 = clusters of 8, shallow ring; 1 = clusters of 8, deep ring;
@@ -597,6 +655,21 @@ cudaError_t prepare_attention(int head_dim, int G) {
     g_caps[dev][dim_index(head_dim)][group_index(G)] = caps;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_kv_append(const LaunchCtx& c, const AttnParams& p, int head_dim) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.nkv, p.B);
+  cfg.blockDim = dim3(32);
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (head_dim == 64) return cudaLaunchKernelEx(&cfg, k_kv_append<64>, p);
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, k_kv_append<128>, p);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim) {

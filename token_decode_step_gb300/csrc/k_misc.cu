@@ -15,8 +15,9 @@ __global__ void __launch_bounds__(256) k_embed(EmbedParams p) {
   griddep_wait();  // first kernel of a step: nothing upstream inside the graph
   tl_mark(p.tl, 1);
   const int b = blockIdx.x;
+  const int T = p.T > 1 ? p.T : 1;
   int tok = p.tokens[b];
-  int pos = p.positions[b];
+  int pos = p.positions[b / T] + b % T;
   if (tok < 0 || tok >= p.V) {
     if (threadIdx.x == 0) atomicOr(p.status, kStatusBadToken);
     tok = tok < 0 ? 0 : p.V - 1;

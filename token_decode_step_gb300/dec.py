@@ -42,6 +42,7 @@ class DecConfig(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("intermediate", ctypes.c_int),
         ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
         ("linear_fmt", ctypes.c_int), ("batch", ctypes.c_int), ("max_ctx", ctypes.c_int),
+        ("tokens_per_seq", ctypes.c_int),
     ]
 
 

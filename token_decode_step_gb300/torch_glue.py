@@ -20,14 +20,15 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
-def make_config(shape, batch: int | None = None, max_ctx: int | None = None) -> dec.DecConfig:
+def make_config(shape, batch: int | None = None, max_ctx: int | None = None,
+                tokens_per_seq: int = 1) -> dec.DecConfig:
     """dec_config from any object with the model-shape attributes (n_layers, hidden, ...)."""
     fmt = dec.DEC_W_BF16 if shape.weight_format == "bf16" else dec.DEC_W_AFFINE4_G64
     return dec.DecConfig(
         n_layers=shape.n_layers, hidden=shape.hidden, n_q_heads=shape.n_q_heads, n_kv_heads=shape.n_kv_heads,
         head_dim=shape.head_dim, intermediate=shape.intermediate, vocab=shape.vocab, rms_eps=shape.rms_eps,
         rope_theta=shape.rope_theta, linear_fmt=fmt, batch=batch if batch is not None else shape.batch,
-        max_ctx=max_ctx if max_ctx is not None else shape.max_ctx)
+        max_ctx=max_ctx if max_ctx is not None else shape.max_ctx, tokens_per_seq=tokens_per_seq)
 
 
 def _linear(x) -> dec.DecLinear:
@@ -41,8 +42,9 @@ class Decoder:
     include/dec.h (embed, final_norm, lm_head, layers[i][in_norm, post_norm, q_norm,
     k_norm, q, k, v, o, gate, up, down])."""
 
-    def __init__(self, shape, weights: dict, batch: int | None = None, max_ctx: int | None = None):
-        self.cfg = make_config(shape, batch, max_ctx)
+    def __init__(self, shape, weights: dict, batch: int | None = None, max_ctx: int | None = None,
+                 tokens_per_seq: int = 1):
+        self.cfg = make_config(shape, batch, max_ctx, tokens_per_seq)
         L = self.cfg.n_layers
         layers = (dec.DecLayerWeights * L)()
         for i, lw in enumerate(weights["layers"][:L]):
