@@ -113,6 +113,30 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
 #pragma unroll
   for (int j = 0; j < PF; ++j)
     if (j < nunits) load_unit(j, ring[j]);
+  // Residual epilogue inputs: the residual rows (last written two or more kernels
+  // upstream, which completed before the previous kernel could pass its own wait and
+  // start this one) and the next norm's weights, requested before the wait too.
+  constexpr int RH = EPI == kEpiResid ? 1 : 0;
+  float h_pre[RH ? TPW : 1][RH ? NY : 1][4];
+  float nw_pre[RH ? TPW : 1][2];
+  if constexpr (RH) {
+#pragma unroll
+    for (int i = 0; i < TPW; ++i) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int row = 16 * (rt0 + i) + g + 8 * hf;
+        nw_pre[i][hf] = (valid[i] && row < p.N) ? bf16_to_f(p.next_norm_w[row]) : 0.f;
+      }
+#pragma unroll
+      for (int n = 0; n < NY; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = 16 * (rt0 + i) + g + 8 * (e >> 1), tok = 8 * n + 2 * t + (e & 1);
+          h_pre[i][n][e] = (valid[i] && row < p.N && tok < p.B) ? __ldcg(p.out + static_cast<size_t>(tok) * p.N + row)
+                                                                   : 0.f;
+        }
+    }
+  }
 
   griddep_wait();
   tl_mark(p.tl, 1);
@@ -294,15 +318,26 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
       if (!valid[i]) continue;
 #pragma unroll
       for (int n = 0; n < NY; ++n) y[i][n][0] = y[i][n][1] = y[i][n][2] = y[i][n][3] = 0.f;
-      for (int s = 0; s < p.S; ++s) {
-        const float* src = p.partials + ((static_cast<size_t>(s) * n_rt + rt0 + i) * 32 + lane) * (NY * 4);
+      // four splits' partials requested at a time, then added in split order
+      for (int s0 = 0; s0 < p.S; s0 += 4) {
+        float4 v[4][NY];
 #pragma unroll
-        for (int n = 0; n < NY; ++n) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * n));
-          y[i][n][0] += v.x;
-          y[i][n][1] += v.y;
-          y[i][n][2] += v.z;
-          y[i][n][3] += v.w;
+        for (int j = 0; j < 4; ++j) {
+          if (s0 + j >= p.S) break;
+          const float* src = p.partials + ((static_cast<size_t>(s0 + j) * n_rt + rt0 + i) * 32 + lane) * (NY * 4);
+#pragma unroll
+          for (int n = 0; n < NY; ++n) v[j][n] = __ldcg(reinterpret_cast<const float4*>(src + 4 * n));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (s0 + j >= p.S) break;
+#pragma unroll
+          for (int n = 0; n < NY; ++n) {
+            y[i][n][0] += v[j][n].x;
+            y[i][n][1] += v[j][n].y;
+            y[i][n][2] += v[j][n].z;
+            y[i][n][3] += v[j][n].w;
+          }
         }
       }
     }
@@ -338,12 +373,11 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
         } else if constexpr (EPI == kEpiResid) {
           float hn = 0.f;
           if (tok < p.B) {
-            float* hp = p.out + static_cast<size_t>(tok) * p.N + row;
-            hn = *hp + y[i][n][e];
-            *hp = hn;
+            hn = h_pre[i][n][e] + y[i][n][e];
+            p.out[static_cast<size_t>(tok) * p.N + row] = hn;
             // the next consumer's input: h times its norm weight, as hi + lo planes
             __nv_bfloat16 hi, lo;
-            split_hl(hn * bf16_to_f(p.next_norm_w[row]), hi, lo);
+            split_hl(hn * nw_pre[i][e >> 1], hi, lo);
             const size_t o = static_cast<size_t>(tok) * p.N + row;
             p.xhl_out[o] = hi;
             p.xhl_out[plane_out + o] = lo;

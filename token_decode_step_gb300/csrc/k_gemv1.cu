@@ -312,8 +312,15 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
       if (s_ticket != static_cast<unsigned>(p.S - 1)) continue;
       __threadfence();
       if (tid < R && tid < nrows) {
-        float t = 0.f;
-        for (int s = 0; s < p.S; ++s) t += __ldcg(p.partials + static_cast<size_t>(s) * p.N + row0 + tid);
+        float t = 0.f;  // four splits requested at a time, added in split order
+        for (int s0 = 0; s0 < p.S; s0 += 4) {
+          float v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = s0 + j < p.S ? __ldcg(p.partials + static_cast<size_t>(s0 + j) * p.N + row0 + tid) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) t += v[j];
+        }
         ys[tid] = t;
       }
       if (tid == 0) p.counters[tile] = 0u;
