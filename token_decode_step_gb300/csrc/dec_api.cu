@@ -222,7 +222,7 @@ dec_status check_linear(const dec_linear& l, int fmt, const char* name, int laye
 // SMs.  Every split costs a round trip through the partial sums (fence, ticket, reload:
 // about 2 us measured on the 1024-row projections, more than the idle SMs give back).
 int choose_splits(int N, int K, int fmt, int num_sms) {
-  const int cols = fmt == DEC_W_BF16 ? 8 : 32;
+  const int cols = fmt == DEC_W_BF16 ? 8 : 16;  // inputs per thread chunk (k_gemv1.cu)
   const int tiles = (N + kGemvRows - 1) / kGemvRows;
   int S = 1;
   while (static_cast<long long>(tiles) * S * 2 < num_sms) {

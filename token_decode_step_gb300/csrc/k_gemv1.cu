@@ -22,6 +22,8 @@
 // ops), each byte is moved into bits 16..19 of 128.0f by one byte permute (giving
 // 128 + q exactly), and the products accumulate in pairs with the packed fp32 FMA
 // (fma.rn.f32x2).  Per group: sum (s q + b) x = s sum (128 + q) x + (b - 128 s) sum x.
+#include <type_traits>
+
 #include "dec_internal.cuh"
 #include "q4.cuh"
 
@@ -37,7 +39,7 @@ struct ChunkTraits<kWBf16> {
 };
 template <>
 struct ChunkTraits<kWQ4> {
-  static constexpr int kCols = 32;  // 16 bytes of 4-bit codes
+  static constexpr int kCols = 16;  // 8 bytes of 4-bit codes (a quarter group): two words per row
 };
 
 template <int WF>
@@ -169,9 +171,9 @@ __device__ __noinline__ void prefetch_kv_share(const GemvParams& p, int lane) {
 
 }  // namespace
 
-// Four CTAs of 256 threads per SM for bf16 (64 registers), two for the 4-bit decode.
+// Four CTAs of 256 threads per SM for bf16 (64 registers), three for the 4-bit decode.
 template <int WF, int IN, int EPI>
-__global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParams p) {
+__global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 3)) k_gemv1(GemvParams p) {
   constexpr int R = kGemvRows;
   constexpr int CH = ChunkTraits<WF>::kCols;
   __shared__ float red[8][R + 1];  // per warp: R row sums, then the sum of squares
@@ -189,7 +191,8 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
   const int lane = tid & 31, warp = tid >> 5;
 
   tl_mark(p.tl, 0);
-  uint4 wreg[R];
+  using WReg = typename std::conditional<WF == kWBf16, uint4, uint2>::type;
+  WReg wreg[R];
   uint32_t sbw[WF == kWQ4 ? R : 1];
   auto load_chunk = [&](int u, int cc) {
     const int tile = u % ntiles, row0 = tile * R, nrows = min(R, p.N - row0);
@@ -197,7 +200,11 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int row = row0 + min(r, nrows - 1);
-      wreg[r] = ld_stream16(chunk_ptr<WF>(p, row, col));
+      if constexpr (WF == kWBf16) {
+        wreg[r] = ld_stream16(chunk_ptr<WF>(p, row, col));
+      } else {
+        wreg[r] = ld_stream8(chunk_ptr<WF>(p, row, col));
+      }
       if constexpr (WF == kWQ4) sbw[r] = __ldg(p.sb + static_cast<size_t>(row) * (p.K / kGroup) + col / kGroup);
     }
   };
@@ -260,8 +267,6 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 2)) k_gemv1(GemvParam
           float d0 = 0.f, d1 = 0.f;
           dot_q4_word(wreg[r].x, xv, d0, d1);
           dot_q4_word(wreg[r].y, xv + 8, d0, d1);
-          dot_q4_word(wreg[r].z, xv + 16, d0, d1);
-          dot_q4_word(wreg[r].w, xv + 24, d0, d1);
           const float s = sb_scale(sbw[r]), b = sb_bias(sbw[r]);
           acc[r] = fmaf(s, d0 + d1, acc[r]);
           acc[r] = fmaf(fmaf(-128.f, s, b), xsum, acc[r]);
