@@ -38,9 +38,11 @@ METRIC = "decode tokens/s and achieved HBM GB/s (fraction of GB300 peak) per ste
 # Captured with token_decode_step_gb300.profile_case (2 layers, same shapes as the bench
 # workload) under `ncu --set full`; profiles/ holds the summaries and commands.
 NCU_TRAFFIC: dict = {
-    "qwen3-0.6b": {"attention": {"bytes": 4253696, "csrc": "5d874a29ddfcd8e3"}},
-    "qwen3-8b-b1": {"gate_up": {"bytes": 201391360 + 2978304, "csrc": "5d874a29ddfcd8e3"}},
-    "qwen3-4b-q4": {"gate_up": {"bytes": 28077568, "csrc": "5d874a29ddfcd8e3"}},
+    "qwen3-0.6b": {"attention": {"bytes": 4263424, "csrc": "b1d10eee8cb9e9f5"}},
+    "qwen3-8b-b1": {"gate_up": {"bytes": 201392128 + 3184640, "csrc": "b1d10eee8cb9e9f5"}},
+    "qwen3-4b-q4": {"gate_up": {"bytes": 28074752, "csrc": "b1d10eee8cb9e9f5"}},
+    "qwen3-8b-b8": {"gate_up": {"bytes": 201518080 + 2957312, "csrc": "b1d10eee8cb9e9f5"}},
+    "qwen3-8b-q4-b32": {"attention": {"bytes": 607689472 + 4173568, "csrc": "b1d10eee8cb9e9f5"}},
 }
 
 
