@@ -57,6 +57,8 @@ CASES = [
     # shallow two-CTAs-per-SM ring
     (6, 16, 4, 128, [1500, 0, 63, 64, 777, 1200], 1536),
     (12, 4, 2, 64, [5, 300, 17, 1000, 64, 129, 2, 999, 640, 31, 1023, 256], 1024),
+    # clusters of 8 would take two waves of two CTAs per SM, clusters of 4 take one
+    (10, 16, 4, 128, [900, 1, 2047, 333, 64, 65, 1500, 0, 1000, 2000], 2048),
 ]
 
 

@@ -528,8 +528,8 @@ namespace {
 
 // Launch shapes: 0 = clusters of 8, shallow ring; 1 = clusters of 8, deep ring;
 // 2 = clusters of 16, deep ring; 3 = clusters of 12, deep ring (16 and 12 are
-// non-portable sizes).
-constexpr int kShapes = 4;
+// non-portable sizes); 4 = clusters of 4, shallow ring.
+constexpr int kShapes = 5;
 
 template <int D, int G, int C, bool DEEP>
 cudaLaunchConfig_t attn_config(const AttnParams& p, cudaStream_t stream, bool pdl, cudaLaunchAttribute (&attr)[2]) {
@@ -581,11 +581,13 @@ cudaError_t prepare_all(int (&max_clusters)[kShapes]) {
   if ((e = prepare_attn_t<D, G, 8, false>(&max_clusters[0])) != cudaSuccess) return e;
   if ((e = prepare_attn_t<D, G, 8, true>(&max_clusters[1])) != cudaSuccess) return e;
   if ((e = prepare_attn_t<D, G, 16, true>(&max_clusters[2])) != cudaSuccess) return e;
-  return prepare_attn_t<D, G, 12, true>(&max_clusters[3]);
+  if ((e = prepare_attn_t<D, G, 12, true>(&max_clusters[3])) != cudaSuccess) return e;
+  return prepare_attn_t<D, G, 4, false>(&max_clusters[4]);
 }
 
 template <int D, int G>
 cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
+  if (shape == 4) return launch_attn_t<D, G, 4, false>(c, p);
   if (shape == 3) return launch_attn_t<D, G, 12, true>(c, p);
   if (shape == 2) return launch_attn_t<D, G, 16, true>(c, p);
   if (shape == 1) return launch_attn_t<D, G, 8, true>(c, p);
@@ -597,7 +599,7 @@ cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
 constexpr int kMaxAttnDevices = 64;
 struct AttnCaps {
   int num_sms = 0;
-  int max_clusters[kShapes] = {0, 0, 0, 0};
+  int max_clusters[kShapes] = {0, 0, 0, 0, 0};
 };
 AttnCaps g_caps[kMaxAttnDevices][2][3];
 std::mutex g_caps_mu;
@@ -613,7 +615,9 @@ size_t attention_smem_bytes(int head_dim) {
 
 // The widest shape whose grid runs in one wave with one CTA per SM: 16-, then 12-, then
 // 8-CTA clusters with the deep ring when B n_kv of them fit at once (the occupancy
-// query counts what the GPCs can place), else 8-CTA clusters with the shallow ring.
+// query counts what the GPCs can place); with two CTAs per SM, 4-CTA clusters when they
+// make one wave and 8-CTA clusters would not; else 8-CTA clusters (many short CTAs keep
+// ragged batches balanced).
 int attention_shape(int B, int nkv, int head_dim, int G) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttnDevices) return 0;
@@ -629,6 +633,9 @@ int attention_shape(int B, int nkv, int head_dim, int G) {
   if (clusters * 16 <= caps.num_sms && clusters <= caps.max_clusters[2]) return 2;
   if (clusters * 12 <= caps.num_sms && clusters <= caps.max_clusters[3]) return 3;
   if (clusters * 8 <= caps.num_sms && clusters <= caps.max_clusters[1]) return 1;
+  // two CTAs per SM: clusters of 4 when those fit in one wave and clusters of 8 would not
+  if (clusters * 8 > 2ll * caps.num_sms && clusters * 4 <= 2ll * caps.num_sms && clusters <= caps.max_clusters[4])
+    return 4;
   return 0;
 }
 
