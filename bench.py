@@ -150,6 +150,22 @@ class ClockSampler:
                 "samples": len(sm), "samples_in_region": n_in}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own, all receive the maximum
+    (replicas run independently; the job is done when the last one is)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, batch: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput: the tokens of every rank over the slowest rank's time."""
+    return world * batch * steps / (ms_max / 1e3)
+
+
 def run_ours(args, rank: int, world: int) -> dict | None:
     import torch
     import synthetic
@@ -199,11 +215,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         clk.end()
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     mean_p = pos_start + (args.steps - 1) / 2.0  # mean cached length over the timed steps
 
     # per-kernel-class durations: the same step with per-launch CUDA events (no graph)
@@ -412,7 +424,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     steps = args.steps
-    tok_s = world * B * steps / (r["ms"] / 1e3)
+    tok_s = job_tokens_per_s(world, B, steps, r["ms"])
     step_ms = r["ms"] / steps
     step_gbs = r["bytes_step"] / (step_ms / 1e3) / 1e9
 
