@@ -26,6 +26,9 @@ Sources (page title and section):
   * oxinfer (docs.rs crate page), section "MLX checkpoints": packed 4-bit
     weights, eight per uint32, bf16 scale and bias per group of 64,
     w = scale * q + bias.
+  * Butter architecture.md, model-layer section (per-layer cache types include an
+    AffineQuantizedKVCache) for oracle/kvcache.py: the cache may hold affine 8-bit
+    codes with a bf16 scale and bias per group of 64 instead of bf16 rows.
 
 Readings where the pages are silent (each is listed in the design doc):
   * RoPE pairs element i with element i + d/2 (rotate-half), angle
@@ -36,7 +39,9 @@ Readings where the pages are silent (each is listed in the design doc):
   * The new token attends to cached slots 0..P inclusive (P = cached length),
     after its own K/V were written at slot P; scale 1/sqrt(head_dim).
   * The cache stores bf16: the appended K and V are rounded to bf16
-    (round-to-nearest-even) before they are used.
+    (round-to-nearest-even) before they are used; or, in the affine 8-bit format,
+    they are quantized (min-max per group of 64, decisions in float32, see
+    oracle/kvcache.py) and read back as scale * code + bias.
   * argmax ties go to the lowest index.
 
 Parity-unpinned pieces: none of the functions below lacks a pin (see
@@ -48,6 +53,7 @@ plus an independent scalar-loop restatement on a tiny shape.
 from .numerics import bf16_bits_to_f64, f64_to_bf16_bits, round_to_bf16  # noqa: F401
 from .affine4 import dequant_affine4_g64, dequant_affine4_g64_f32  # noqa: F401
 from . import sampling  # noqa: F401
+from .kvcache import Affine8Cache, quantize_affine8_g64, dequant_affine8_g64  # noqa: F401
 from .decoder import (  # noqa: F401
     OracleModel, rmsnorm, rope_rotate_half, softmax, gqa_attention, lse_merge, silu,
     argmax_lowest, decode_step, tie_exempt, verify_step,

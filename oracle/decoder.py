@@ -18,7 +18,8 @@ from dataclasses import dataclass, field
 import numpy as np
 
 from .affine4 import dequant_affine4_g64
-from .numerics import bf16_bits_to_f64, f64_to_bf16_bits
+from .kvcache import Affine8Cache, kv_read, kv_store
+from .numerics import bf16_bits_to_f64
 
 
 # --------------------------------------------------------------------------- ops
@@ -189,8 +190,9 @@ class OracleModel:
 def decode_step(m: OracleModel, kv: np.ndarray, tokens, positions):
     """One greedy decode step for B independent sequences.
 
-    kv: uint16 bf16 bit patterns [L][2][B][n_kv][max_ctx][d]; slot P_b of every
-    layer is overwritten with the new token's K and V (rounded to bf16).
+    kv: uint16 bf16 bit patterns [L][2][B][n_kv][max_ctx][d], or an Affine8Cache;
+    slot P_b of every layer is overwritten with the new token's K and V in the
+    cache's format (rounded to bf16, or quantized to affine 8-bit codes).
     tokens[b]: input token id; positions[b] = P_b = number of cached positions.
     Returns (logits float64 [B, V], argmax int64 [B]).
 
@@ -208,7 +210,8 @@ def decode_step(m: OracleModel, kv: np.ndarray, tokens, positions):
     tokens = [int(t) for t in np.asarray(tokens).reshape(-1)]
     positions = [int(p) for p in np.asarray(positions).reshape(-1)]
     B = len(tokens)
-    assert kv.shape[:3] == (L, 2, B) and kv.dtype == np.uint16
+    assert kv.shape[:3] == (L, 2, B)
+    assert isinstance(kv, Affine8Cache) or kv.dtype == np.uint16
     for P in positions:
         assert 0 <= P < kv.shape[4], "position outside the cache"
 
@@ -225,10 +228,10 @@ def decode_step(m: OracleModel, kv: np.ndarray, tokens, positions):
             P = positions[b]
             qb = rope_rotate_half(q[b], P, theta)
             kb = rope_rotate_half(k[b], P, theta)
-            kv[l, 0, b, :, P, :] = f64_to_bf16_bits(kb)
-            kv[l, 1, b, :, P, :] = f64_to_bf16_bits(v[b])
-            Kc = bf16_bits_to_f64(kv[l, 0, b, :, : P + 1, :])
-            Vc = bf16_bits_to_f64(kv[l, 1, b, :, : P + 1, :])
+            kv_store(kv, l, 0, b, P, kb)
+            kv_store(kv, l, 1, b, P, v[b])
+            Kc = kv_read(kv, l, 0, b, P + 1)
+            Vc = kv_read(kv, l, 1, b, P + 1)
             o[b] = gqa_attention(qb, Kc, Vc).reshape(-1)
         h = h + m.linear(o, "layers", l, "o")
         xn = rmsnorm(h, m.vec("layers", l, "post_norm"), eps)

@@ -26,16 +26,23 @@ no trained weights):
 * ``qwen3-8b-q4-b32`` the 8B shapes in the affine 4-bit format, batch 32,
                    cached lengths uniform in [512, 8192] per sequence, 32
                    steps, seed 4.
+* ``*-kv8``        the same workload (same seed and draws up to the cache) with
+                   the KV cache in the affine 8-bit format (``tiny-kv8``,
+                   ``qwen3-8b-b1-kv8``, ``qwen3-8b-q4-b32-kv8``).
 
 Value distributions: linear and embedding weights N(0, 0.02); norm weights
 1 + N(0, 0.1); cached K/V N(0, 1); for 4-bit linears, uniform random 32-bit
 words (so every nibble is uniform in 0..15), scales U(0.001, 0.01) and biases
 N(0, 0.02).  Every floating value is drawn in fp32 and rounded to bf16 with
-round-to-nearest-even (torch's conversion).
+round-to-nearest-even (torch's conversion).  An affine 8-bit cache is drawn in
+its stored form: codes uniform in 0..255, per group of 64 a scale U(0.015,
+0.023) and a bias -scale * U(110, 145), both rounded to bf16 (values spread over
+about [-2.8, 2.8] like a quantized N(0, 1) row).
 
 Draw order: embed; per layer in_norm, q, k, v, o, q_norm, k_norm, post_norm,
 gate, up, down; final_norm; lm_head; KV (layer by layer, K plane then V plane);
-prompt tokens; cached lengths.  A 4-bit linear draws words, scales, biases.
+prompt tokens; cached lengths.  A 4-bit linear draws words, scales, biases; an
+affine 8-bit cache draws, per layer and plane, codes, scales, bias factors.
 
 Layouts (all row-major, linears are [out][in]):
   bf16 linear      int16/bfloat16 tensor [out, in]
@@ -43,7 +50,9 @@ Layouts (all row-major, linears are [out][in]):
                    element 8j+k, bits 4k..4k+3), scales=bf16 [out, in/64],
                    biases=bf16 [out, in/64])
   KV cache         bf16 [L][2][B][n_kv][max_ctx][head_dim]  (plane 0 = K,
-                   plane 1 = V)
+                   plane 1 = V); affine 8-bit: dict(codes=uint8
+                   [L][2][B][n_kv][max_ctx][head_dim], params=bf16
+                   [L][2][B][n_kv][max_ctx][head_dim/64][2] (scale, bias))
 """
 
 from __future__ import annotations
@@ -55,6 +64,7 @@ import torch
 
 BF16 = "bf16"
 AFFINE4_G64 = "affine4_g64"
+AFFINE8_G64 = "affine8_g64"  # KV cache format
 GROUP = 64
 
 
@@ -77,6 +87,7 @@ class Workload:
     rope_theta: float = 1e6
     weight_std: float = 0.02
     norm_std: float = 0.1
+    kv_format: str = BF16
 
     @property
     def max_prefill(self) -> int:
@@ -116,6 +127,8 @@ WORKLOADS: dict[str, Workload] = {
     "qwen3-8b-q4-b32": Workload("qwen3-8b-q4-b32", 4, 36, 4096, 32, 8, 128, 12288, 151936, AFFINE4_G64, 32,
                                 (512, 8192), 32),
 }
+for _name in ("tiny", "qwen3-8b-b1", "qwen3-8b-q4-b32"):
+    WORKLOADS[_name + "-kv8"] = WORKLOADS[_name].replace(name=_name + "-kv8", kv_format=AFFINE8_G64)
 
 
 def _normal_bf16(g: torch.Generator, shape, std: float, mean: float, device) -> torch.Tensor:
@@ -141,6 +154,33 @@ def _linear(g: torch.Generator, wl: Workload, out: int, inp: int, fmt: str, devi
     scales = _uniform_bf16(g, (out, inp // GROUP), 0.001, 0.01, device)
     biases = _normal_bf16(g, (out, inp // GROUP), wl.weight_std, 0.0, device)
     return {"w": words, "scales": scales, "biases": biases}
+
+
+def _kv_affine8(g: torch.Generator, wl: Workload, device) -> dict:
+    shape = wl.kv_shape()
+    codes = torch.empty(shape, dtype=torch.uint8, device=device)
+    params = torch.empty(shape[:5] + (wl.head_dim // GROUP, 2), dtype=torch.bfloat16, device=device)
+    for l in range(wl.n_layers):
+        for p in range(2):
+            codes[l, p].copy_(torch.randint(0, 256, shape[2:], generator=g, device=device, dtype=torch.int32))
+            sc = torch.rand(params.shape[2:6], generator=g, device=device, dtype=torch.float32) * 0.008 + 0.015
+            off = torch.rand(params.shape[2:6], generator=g, device=device, dtype=torch.float32) * 35.0 + 110.0
+            sc16 = sc.to(torch.bfloat16)
+            params[l, p, ..., 0].copy_(sc16)
+            params[l, p, ..., 1].copy_((-sc16.float() * off).to(torch.bfloat16))
+    return {"codes": codes, "params": params}
+
+
+def kv_buffer(kv) -> torch.Tensor:
+    """The cache as the one flat buffer the library reads: a bf16 cache as it is; an
+    affine 8-bit cache as its codes, zero padding to a multiple of 256 bytes, then its
+    (scale, bias) pairs."""
+    if isinstance(kv, torch.Tensor):
+        return kv
+    codes = kv["codes"].reshape(-1)
+    params = kv["params"].contiguous().view(torch.uint8).reshape(-1)
+    pad = (-codes.numel()) % 256
+    return torch.cat([codes, torch.zeros(pad, dtype=torch.uint8, device=codes.device), params])
 
 
 def generate(wl: Workload, device: str | torch.device = "cpu", with_kv: bool = True) -> dict:
@@ -174,7 +214,9 @@ def generate(wl: Workload, device: str | torch.device = "cpu", with_kv: bool = T
     model["final_norm"] = _normal_bf16(g, (H,), wl.norm_std, 1.0, device)
     model["lm_head"] = _linear(g, wl, *sh["lm_head"], fmt, device)
 
-    if with_kv:
+    if with_kv and wl.kv_format == AFFINE8_G64:
+        model["kv"] = _kv_affine8(g, wl, device)
+    elif with_kv:
         kv = torch.empty(wl.kv_shape(), dtype=torch.bfloat16, device=device)
         for l in range(wl.n_layers):
             for p in range(2):
