@@ -187,7 +187,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     B, V = wl.batch, wl.vocab
     tokens = model["tokens"].clone()
     positions = model["positions"].clone()
-    kv = model["kv"]
+    kv = synthetic.kv_buffer(model["kv"])  # the one flat cache buffer the library reads
     logits = torch.empty((B, V), dtype=torch.float32, device=dev)
     argmax = torch.empty((B,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -322,7 +322,12 @@ def cpu_oracle_sample(config: str, warmup: int, steps: int, budget_s: float) -> 
     model = synthetic.generate(wl, device="cpu")
     m = oracle.OracleModel.from_synthetic(wl, model, cache_weights=True)
     bs = 1 if wl.batch > 1 else wl.batch
-    kv = model["kv"][:, :, :bs].contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    if isinstance(model["kv"], dict):  # affine 8-bit cache
+        kv = oracle.Affine8Cache(model["kv"]["codes"][:, :, :bs].contiguous().numpy().copy(),
+                                 model["kv"]["params"][:, :, :bs].contiguous().view(torch.int16).numpy()
+                                 .view(np.uint16).copy())
+    else:
+        kv = model["kv"][:, :, :bs].contiguous().view(torch.int16).numpy().view(np.uint16).copy()
     tokens = model["tokens"][:bs].numpy().copy()
     pos = model["positions"][:bs].numpy().copy()
 
@@ -353,7 +358,7 @@ def workload_config(wl, world: int) -> dict:
     return {
         "workload": wl.name, "batch": wl.batch, "layers": wl.n_layers, "hidden": wl.hidden,
         "cached_positions": wl.prefill if not isinstance(wl.prefill, tuple) else list(wl.prefill),
-        "weight_format": wl.weight_format, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "weight_format": wl.weight_format, "kv_format": wl.kv_format, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         "l2": ("inputs larger than L2 (per-step weights exceed 129 MB); no flush" if weight_bytes(wl) > 129e6 else
                "inputs smaller than L2 and not flushed: a cache-warm number"),
         "timing": "CUDA events on the launching stream, CUDA-graph replay per step",

@@ -28,6 +28,9 @@
  *     sampling (greedy argmax on the device, 4-byte result).
  *   - oxinfer crate page, "MLX checkpoints": affine 4-bit weights, eight per
  *     uint32, one bf16 scale and bias per group of 64, w = scale*q + bias.
+ *   - Butter, architecture.md, model-layer section (per-layer cache types: KVCache,
+ *     AffineQuantizedKVCache): the KV cache may hold affine 8-bit codes (the same
+ *     affine form, one bf16 scale and bias per 64 values of a row) instead of bf16.
  *
  * Conventions for every entry point:
  *   - Device pointers are CUDA device memory of the current device.  Host
@@ -75,12 +78,18 @@ typedef enum {
                                   bits 4k..4k+3), scales, biases = bf16 [out][in/64] */
 } dec_wfmt;
 
+typedef enum {
+    DEC_KV_BF16 = 0,           /* bf16 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim] */
+    DEC_KV_AFFINE8_G64 = 1     /* affine 8-bit, see dec_kv_cache_bytes() for the layout */
+} dec_kvfmt;
+
 /* Model and run shape.  Supported (else DEC_ERR_UNSUPPORTED): head_dim in {64, 128};
    n_q_heads / n_kv_heads in {1, 2, 4}; hidden and intermediate multiples of 64;
    vocab >= 1; rows = batch * tokens_per_seq at most 16 for bf16 weights and 32 for
    affine 4-bit (one row runs CUDA-core GEMV kernels, more rows tensor-core kernels);
-   tokens_per_seq 0..8 (0 means 1); max_ctx >= 1.  Required (else DEC_ERR_INVALID_ARG):
-   every size positive, rms_eps > 0, rope_theta > 1, n_q_heads a multiple of n_kv_heads.
+   tokens_per_seq 0..8 (0 means 1); max_ctx >= 1, and a multiple of 16 for the affine
+   8-bit cache.  Required (else DEC_ERR_INVALID_ARG): every size positive, rms_eps > 0,
+   rope_theta > 1, n_q_heads a multiple of n_kv_heads, kv_fmt a dec_kvfmt.
 
    tokens_per_seq T > 1 makes dec_step a multi-token verify step (speculative decoding's
    check of drafted tokens in one forward: ANEForge "LLMs on the ANE", "Speculative
@@ -95,6 +104,7 @@ typedef struct {
     int linear_fmt;            /* dec_wfmt, applies to every linear including lm_head */
     int batch, max_ctx;        /* sequences per step; cache slots per sequence */
     int tokens_per_seq;        /* new tokens per sequence and step: 1 (decode) .. 8 (verify); 0 = 1 */
+    int kv_fmt;                /* dec_kvfmt of the KV cache (0 = bf16) */
 } dec_config;
 
 /* One linear layer, row-major [out][in] in device memory.  bf16: w only (scales,
@@ -139,9 +149,9 @@ DEC_API dec_handle *dec_create(const dec_config *cfg, const dec_weights *weights
      positions  device int32 [batch]: P_b = cached positions of sequence b; row
                 (b, t) writes K/V slot P_b + t, attends over slots 0..P_b + t and
                 applies RoPE at angle P_b + t.  The caller advances positions.
-     kv_cache   device, dec_kv_cache_bytes(cfg) bytes, bf16
-                [n_layers][2][batch][n_kv_heads][max_ctx][head_dim] (plane 0 = K,
-                plane 1 = V, post-norm post-RoPE keys), caller-owned.
+     kv_cache   device, dec_kv_cache_bytes(cfg) bytes in the cfg's kv_fmt (layouts at
+                dec_kv_cache_bytes), caller-owned, 16-byte aligned.  New K/V rows
+                are rounded to bf16, or quantized as dec_kv_quantize() does.
      logits_out device float [rows][vocab], or NULL to skip writing logits.
      argmax_out device int32 [rows]: greedy token (lowest index on equal
                 logits).  May alias token_ids (read happens first).
@@ -157,8 +167,29 @@ DEC_API dec_status dec_step(dec_handle *h, const int32_t *token_ids, const int32
    The caller must make sure no step of this handle is still running. */
 DEC_API void dec_destroy(dec_handle *h);
 
-/* Bytes of the KV cache for cfg (0 if cfg is NULL or invalid). */
+/* Bytes of the KV cache for cfg (0 if cfg is NULL or invalid).  Plane 0 holds the keys
+   (after the per-head norm and RoPE), plane 1 the values; slot s of a sequence holds its
+   position s.
+     DEC_KV_BF16: bf16 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim].
+     DEC_KV_AFFINE8_G64: the codes, uint8 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim],
+       then, from the first multiple of 256 bytes after them, the (scale, bias) pairs, bf16
+       [n_layers][2][batch][n_kv_heads][max_ctx][head_dim/64][2]: element i of a row reads
+       scale[i/64] * code[i] + bias[i/64]. */
 DEC_API size_t dec_kv_cache_bytes(const dec_config *cfg);
+
+/* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
+   caller buffers.  For each group of 64 consecutive values x of a row, in float32:
+   mn, mx = min, max; scale = bf16(fl(fl(mx - mn) / 255)); bias = bf16(mn) (round to
+   nearest even); code = clamp(rint(fl(fl(x - bias) / scale)), 0, 255), rint rounding
+   halves to even, code 0 where scale = 0.  (Butter architecture.md, model-layer section:
+   AffineQuantizedKVCache; the affine form of oxinfer's "MLX checkpoints" section.)
+     src     device float [rows][head_dim], finite values
+     codes   device uint8 [rows][head_dim]
+     params  device bf16 [rows][head_dim/64][2]: (scale, bias) per group
+   head_dim 64 or 128 (else DEC_ERR_UNSUPPORTED); rows >= 0; NULL pointers with rows > 0
+   -> DEC_ERR_INVALID_ARG.  One kernel launch on `stream`. */
+DEC_API dec_status dec_kv_quantize(const float *src, int rows, int head_dim, uint8_t *codes, void *params,
+                                   dec_stream_t stream);
 
 /* Message of the last failing call on this thread ("" if none). */
 DEC_API const char *dec_last_error(void);
@@ -210,7 +241,7 @@ DEC_API double dec_kernel_bytes(const dec_handle *h, int kernel_class, double me
 DEC_API int dec_launches_per_step(const dec_handle *h);
 
 /* Kernel-level entry point: the fused attention that dec_step runs for each layer
-   (per-head q/k RMSNorm, rotate-half RoPE at positions[b], append of bf16 k, v at
+   (per-head q/k RMSNorm, rotate-half RoPE at positions[b], append of k, v (in the cache format) at
    slot positions[b] of `layer`, split-KV GQA attention over slots 0..positions[b]
    with a log-sum-exp merge), on caller buffers.  ANEForge "LLMs on the ANE",
    "Correctness" and "What's inside"; Butter architecture.md "SINGLE-TOKEN DECODE"
@@ -222,7 +253,8 @@ DEC_API int dec_launches_per_step(const dec_handle *h);
                 projections, q heads, then k heads, then v heads, head j at j*head_dim.
      q_norm, k_norm  device bf16 [head_dim].
      positions  device int32 [batch], as in dec_step (clamped if out of range).
-     kv_cache   as in dec_step; only slot positions[b] of `layer` is written.
+     kv_cache   as in dec_step (either kv_fmt); only slot positions[b] of `layer` is
+                written.
      out        device float [batch][n_q * head_dim]: attention output per query head.
      workspace  caller-owned device scratch (the RoPE table) of at least
                 dec_attention_workspace_bytes(cfg) bytes, 256-byte aligned; its

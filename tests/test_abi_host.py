@@ -52,6 +52,33 @@ def _cfg(dec, **kw):
 def test_kv_cache_bytes(dec):
     assert dec.dec_kv_cache_bytes(_cfg(dec)) == 2 * 2 * 1 * 2 * 144 * 64 * 2
     assert dec.lib.dec_kv_cache_bytes(None) == 0
+    # affine 8-bit: the codes, padded to 256 bytes, then a (scale, bias) bf16 pair per 64
+    codes = 2 * 2 * 3 * 2 * 144 * 128
+    pad = (-codes) % 256
+    assert dec.dec_kv_cache_bytes(_cfg(dec, kv_fmt=1, batch=3, head_dim=128)) == codes + pad + codes // 64 * 4
+    codes = 2 * 2 * 1 * 2 * 144 * 64
+    assert dec.dec_kv_cache_bytes(_cfg(dec, kv_fmt=1)) == codes + (-codes) % 256 + codes // 16
+    assert dec.dec_kv_cache_bytes(_cfg(dec, kv_fmt=5)) == 0
+
+
+def test_kv_cache_bytes_match_the_synthetic_buffer(dec):
+    import synthetic
+    from token_decode_step_gb300 import torch_glue
+    wl = synthetic.WORKLOADS["tiny-kv8"].replace(batch=2)
+    buf = synthetic.kv_buffer(synthetic.generate(wl)["kv"])
+    assert dec.dec_kv_cache_bytes(torch_glue.make_config(wl)) == buf.numel()
+
+
+def test_kv_quantize_rejects_bad_arguments(dec):
+    with pytest.raises(dec.DecError) as ei:
+        dec.dec_kv_quantize(0, 4, 96, 0, 0, 0)
+    assert "head_dim" in str(ei.value)
+    with pytest.raises(dec.DecError) as ei:
+        dec.dec_kv_quantize(0, 4, 64, 0, 0, 0)
+    assert "NULL" in str(ei.value)
+    with pytest.raises(dec.DecError):
+        dec.dec_kv_quantize(0, -1, 64, 0, 0, 0)
+    dec.dec_kv_quantize(0, 0, 64, 0, 0, 0)  # nothing to quantize: no launch, no error
 
 
 @pytest.mark.parametrize("kw,status,msg", [
@@ -65,6 +92,8 @@ def test_kv_cache_bytes(dec):
     (dict(tokens_per_seq=9), 2, "tokens_per_seq"),
     (dict(tokens_per_seq=-1), 1, "tokens_per_seq"),
     (dict(batch=5, tokens_per_seq=4), 2, "rows"),
+    (dict(kv_fmt=3), 1, "kv_fmt"),
+    (dict(kv_fmt=1, max_ctx=150), 2, "multiple of 16"),
 ])
 def test_create_rejects_bad_config(dec, kw, status, msg):
     with pytest.raises(dec.DecError) as ei:

@@ -189,6 +189,14 @@ dec_status validate(const dec_config* c) {
     set_err("hidden and intermediate must be multiples of 64");
     return DEC_ERR_UNSUPPORTED;
   }
+  if (c->kv_fmt != DEC_KV_BF16 && c->kv_fmt != DEC_KV_AFFINE8_G64) {
+    set_err("unknown kv_fmt %d", c->kv_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->kv_fmt == DEC_KV_AFFINE8_G64 && c->max_ctx % 16 != 0) {
+    set_err("the affine 8-bit KV cache needs max_ctx to be a multiple of 16 (got %d)", c->max_ctx);
+    return DEC_ERR_UNSUPPORTED;
+  }
   if (c->tokens_per_seq < 0 || c->tokens_per_seq > kMaxTokensPerSeq) {
     set_err("tokens_per_seq must be 0..%d (got %d)", kMaxTokensPerSeq, c->tokens_per_seq);
     return c->tokens_per_seq < 0 ? DEC_ERR_INVALID_ARG : DEC_ERR_UNSUPPORTED;
@@ -321,6 +329,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   auto limit_hit = [&]() { return h->launch_limit >= 0 && launched >= h->launch_limit; };
   if (limit_hit()) return DEC_OK;
   // the K/V prefetch of the next GEMV launch (set around the QKV projection only)
+  const int kv_elem = c.kv_fmt == DEC_KV_AFFINE8_G64 ? 1 : 2;  // bytes per cached element
   struct {
     const unsigned char* kv = nullptr;
     unsigned long long plane_bytes = 0;
@@ -354,10 +363,10 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       gp.pf_kv = kv_pf.kv;
       gp.pf_positions = sp.positions;
       gp.pf_plane_bytes = kv_pf.plane_bytes;
-      gp.pf_head_bytes = static_cast<unsigned long long>(c.max_ctx) * d * 2;
+      gp.pf_head_bytes = static_cast<unsigned long long>(c.max_ctx) * d * kv_elem;
       gp.pf_B = c.batch;
       gp.pf_nkv = c.n_kv_heads;
-      gp.pf_row_bytes = d * 2;
+      gp.pf_row_bytes = d * kv_elem;
       gp.pf_max_ctx = c.max_ctx;
     }
     note(cls);
@@ -396,8 +405,9 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
 
   for (int l = 0; l < c.n_layers; ++l) {
     const PackedLayer& L = h->layers[l];
-    if (h->kv_prefetch) {
-      const unsigned long long plane = static_cast<unsigned long long>(c.batch) * c.n_kv_heads * c.max_ctx * d * 2;
+    if (h->kv_prefetch) {  // bf16 rows, or the codes of the affine 8-bit cache
+      const unsigned long long plane =
+          static_cast<unsigned long long>(c.batch) * c.n_kv_heads * c.max_ctx * d * kv_elem;
       kv_pf.kv = static_cast<const unsigned char*>(sp.kv) + 2ull * l * plane;
       kv_pf.plane_bytes = plane;
     }
@@ -412,7 +422,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.k_norm = L.k_norm;
     ap.rope = h->rope;
     ap.positions = sp.positions;
-    ap.kv = static_cast<__nv_bfloat16*>(sp.kv);
+    attn_set_cache(ap, c, sp.kv);
     ap.layer = l;
     ap.B = h->rows;
     ap.T = h->tps;
@@ -516,7 +526,11 @@ dec_status check_step_args(dec_handle* h, const StepPtrs& sp) {
 extern "C" size_t dec_kv_cache_bytes(const dec_config* cfg) {
   if (!cfg || cfg->n_layers < 1 || cfg->batch < 1 || cfg->n_kv_heads < 1 || cfg->max_ctx < 1 || cfg->head_dim < 1)
     return 0;
-  return static_cast<size_t>(cfg->n_layers) * 2 * cfg->batch * cfg->n_kv_heads * cfg->max_ctx * cfg->head_dim * 2;
+  const size_t rows = static_cast<size_t>(cfg->n_layers) * 2 * cfg->batch * cfg->n_kv_heads * cfg->max_ctx;
+  if (cfg->kv_fmt == DEC_KV_BF16) return rows * cfg->head_dim * 2;
+  if (cfg->kv_fmt == DEC_KV_AFFINE8_G64 && cfg->head_dim % 64 == 0)
+    return kv_q8_params_offset(*cfg) + rows * (cfg->head_dim / 64) * 4;
+  return 0;
 }
 
 extern "C" const char* dec_last_error(void) { return g_err; }
@@ -564,7 +578,9 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     int l2 = 0;
     if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, h->device)) != cudaSuccess)
       return fail("cudaDeviceGetAttribute", e);
-    const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim * 2;
+    // (the affine 8-bit cache prefetches its codes only)
+    const double kv_layer = 2.0 * c.batch * c.n_kv_heads * static_cast<double>(c.max_ctx) * c.head_dim *
+                            (c.kv_fmt == DEC_KV_AFFINE8_G64 ? 1 : 2);
     h->kv_prefetch = h->rows == 1 && kv_layer <= l2 / 4.0;
   }
 
@@ -744,7 +760,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   for (int i = 0; i < d / 2; ++i) inv[i] = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / d);
   if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail("upload inv_freq", e);
-  if ((e = prepare_attention(d, G)) != cudaSuccess) return fail("attention kernel attributes", e);
+  if ((e = prepare_attention(d, G, c.kv_fmt)) != cudaSuccess) return fail("attention kernel attributes", e);
   if (tc) {
     GemmParams gp{};
     gp.B = h->rows;
@@ -908,8 +924,12 @@ extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cac
   switch (cls) {
     case DEC_K_EMBED: return B * H * 2.0;
     case DEC_K_QKV: return (nq + 2 * nkv) * d * H * wb + H * 2.0;
-    // every row reads its sequence's slots 0 .. P + t (t < T: its place among the step's rows)
-    case DEC_K_ATTN: return B * nkv * 2.0 * d * 2.0 * (mean_cached_len + 1.0 + (T - 1.0) / 2.0) + 2.0 * d * 2.0;
+    // every row reads its sequence's slots 0 .. P + t (t < T: its place among the step's rows);
+    // a slot is a bf16 row, or a row of codes and a (scale, bias) pair per 64
+    case DEC_K_ATTN: {
+      const double row = c.kv_fmt == DEC_KV_AFFINE8_G64 ? d + 4.0 * (d / 64.0) : 2.0 * d;
+      return B * nkv * 2.0 * row * (mean_cached_len + 1.0 + (T - 1.0) / 2.0) + 2.0 * row;
+    }
     case DEC_K_OPROJ: return H * nq * d * wb;
     case DEC_K_GATEUP: return 2.0 * I * H * wb + H * 2.0;
     case DEC_K_DOWN: return H * I * wb;
@@ -938,6 +958,14 @@ dec_status validate_attention_cfg(const dec_config* c, int layer) {
   }
   if (c->tokens_per_seq > 1) {
     set_err("attention: the stand-alone entry points take tokens_per_seq 0 or 1");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->kv_fmt != DEC_KV_BF16 && c->kv_fmt != DEC_KV_AFFINE8_G64) {
+    set_err("attention: unknown kv_fmt %d", c->kv_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->kv_fmt == DEC_KV_AFFINE8_G64 && c->max_ctx % 16 != 0) {
+    set_err("attention: the affine 8-bit KV cache needs max_ctx to be a multiple of 16 (got %d)", c->max_ctx);
     return DEC_ERR_UNSUPPORTED;
   }
   const int G = c->n_q_heads / c->n_kv_heads;
@@ -975,7 +1003,7 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
     return DEC_ERR_INVALID_ARG;
   }
   const int G = cfg->n_q_heads / cfg->n_kv_heads;
-  DEC_CUDA(prepare_attention(cfg->head_dim, G));
+  DEC_CUDA(prepare_attention(cfg->head_dim, G, cfg->kv_fmt));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   float2* rope = static_cast<float2*>(workspace);
   DEC_CUDA(launch_rope_table(cs, positions, cfg->batch, cfg->head_dim, cfg->max_ctx, cfg->rope_theta, rope, nullptr));
@@ -985,7 +1013,7 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
   ap.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
   ap.rope = rope;
   ap.positions = positions;
-  ap.kv = static_cast<__nv_bfloat16*>(kv_cache);
+  attn_set_cache(ap, *cfg, kv_cache);
   ap.layer = layer;
   ap.B = cfg->batch;
   ap.nq = cfg->n_q_heads;
@@ -995,6 +1023,23 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
   ap.out = out;
   ap.status = nullptr;
   DEC_CUDA(launch_attention(LaunchCtx{cs, false}, ap, cfg->head_dim));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_kv_quantize(const float* src, int rows, int head_dim, uint8_t* codes, void* params,
+                                      dec_stream_t stream) {
+  g_err[0] = 0;
+  if (head_dim != 64 && head_dim != 128) {
+    set_err("dec_kv_quantize: head_dim must be 64 or 128 (got %d)", head_dim);
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (rows < 0 || (rows > 0 && (!src || !codes || !params)) ||
+      (reinterpret_cast<uintptr_t>(params) & 3u)) {
+    set_err("dec_kv_quantize: rows < 0, a NULL buffer, or params not 4-byte aligned");
+    return DEC_ERR_INVALID_ARG;
+  }
+  DEC_CUDA(launch_kv_quantize(reinterpret_cast<cudaStream_t>(stream), src, rows, head_dim, codes,
+                              static_cast<__nv_bfloat16*>(params)));
   return DEC_OK;
 }
 

@@ -93,7 +93,10 @@ struct AttnParams {
   const __nv_bfloat16* k_norm;  // [d]
   const float2* rope;           // [B][d/2] (cos, sin) at this step's positions
   const int32_t* positions;     // [B / T] cached positions per sequence
-  __nv_bfloat16* kv;            // whole cache
+  int kv_fmt;                   // DEC_KV_BF16 or DEC_KV_AFFINE8_G64
+  __nv_bfloat16* kv;            // bf16 cache
+  unsigned char* q8_codes;      // affine 8-bit cache: codes [L][2][B/T][nkv][max_ctx][d]
+  unsigned char* q8_params;     //   and (scale, bias) bf16 pairs [L][2][B/T][nkv][max_ctx][d/64]
   int layer, B, nq, nkv, max_ctx;
   float eps;
   float* out;                   // [B][nq d]
@@ -272,7 +275,34 @@ int gemm_tc_chunk(int ny);                      // inputs staged per chunk
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi);
 cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
 size_t attention_smem_bytes(int head_dim);
-cudaError_t prepare_attention(int head_dim, int G);  // set the dynamic smem limit (before capture)
+// set the dynamic smem limits and record the shapes' occupancy (before capture)
+cudaError_t prepare_attention(int head_dim, int G, int kv_fmt);
+// affine 8-bit cache kernels (k_attention_q8.cu)
+cudaError_t prepare_attention_q8(int head_dim, int G, int (&max_clusters)[5]);
+cudaError_t launch_attention_q8(const LaunchCtx& c, const AttnParams& p, int head_dim, int shape);
+cudaError_t launch_kv_append_q8(const cudaLaunchConfig_t& cfg, const AttnParams& p, int head_dim);
+cudaError_t launch_kv_quantize(cudaStream_t s, const float* src, int rows, int head_dim, unsigned char* codes,
+                               __nv_bfloat16* params);
+
+// Byte offset of the (scale, bias) pairs of an affine 8-bit cache: the codes, rounded up
+// to 256 bytes.
+inline size_t kv_q8_params_offset(const dec_config& c) {
+  const size_t codes = static_cast<size_t>(c.n_layers) * 2 * c.batch * c.n_kv_heads * c.max_ctx * c.head_dim;
+  return (codes + 255) / 256 * 256;
+}
+
+// The attention's view of a caller's cache in the config's format.
+inline void attn_set_cache(AttnParams& ap, const dec_config& c, void* kv_cache) {
+  ap.kv_fmt = c.kv_fmt;
+  if (c.kv_fmt == DEC_KV_AFFINE8_G64) {
+    ap.kv = nullptr;
+    ap.q8_codes = static_cast<unsigned char*>(kv_cache);
+    ap.q8_params = static_cast<unsigned char*>(kv_cache) + kv_q8_params_offset(c);
+  } else {
+    ap.kv = static_cast<__nv_bfloat16*>(kv_cache);
+    ap.q8_codes = ap.q8_params = nullptr;
+  }
+}
 // (cos, sin) of pos * theta^(-2i/d) for every sequence, angles and inverse
 // frequencies in double on the device; out-of-range positions are clamped and flagged.
 cudaError_t launch_rope_table(cudaStream_t s, const int32_t* positions, int batch, int head_dim, int max_ctx,

@@ -27,13 +27,14 @@
 // partials, no atomics, no remote loads).
 #include <mutex>
 
+#include "attn_common.cuh"
 #include "dec_internal.cuh"
 
 namespace dec {
 
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+using attn::kLog2e;
 
 // Two shapes of the stage ring: shallow (about 100 KB, two CTAs per SM, for grids
 // above the SM count; deeper rings measured slower there) and deep (about 200 KB, one
@@ -48,8 +49,8 @@ struct AttnCfg {
   static constexpr int kOffQ = 0;                                      // [16][D] bf16
   static constexpr int kOffStages = 16 * kRowBytes;
   static constexpr int kOffNew = kOffStages + kStages * kStageBytes;  // new k row, new v row
-  // cluster merge receive area: up to 16 records of (m[G], l[G], acc[ceil(G D / C)]), G <= 4
-  static constexpr int kXchgFloats = 16 * 2 * 4 + 4 * D + 16;
+  // cluster merge receive area
+  static constexpr int kXchgFloats = attn::Xchg<D>::kFloats;
   static constexpr int kOffXchg = kOffNew + 2 * kRowBytes;
   static constexpr int kOffMisc = kOffXchg + kXchgFloats * 4;          // [4][G] floats
   static constexpr int kBytes = kOffMisc + 64 * 4;
@@ -76,45 +77,6 @@ __device__ __forceinline__ void load_tile(uint32_t sdst, const __nv_bfloat16* pl
   }
 }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// split form: arrive early without ordering memory, wait before the first remote access
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// shared-memory address of the same variable in CTA `rank` of this cluster
-__device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-// Positions [begin, end) of CTA `rank` of a cluster of C for a sequence with T = P + 1
-// positions: runs of ceil(T / C) rounded up to 16 positions; later CTAs may get fewer
-// or none.
-__device__ __forceinline__ void attention_run(int T, int C, int rank, int* begin, int* end) {
-  const int per = (T + C - 1) / C;
-  const int len = (per + 15) / 16 * 16;
-  const int b0 = rank * len;
-  *begin = b0 < T ? b0 : T;
-  *end = b0 + len < T ? b0 + len : T;
-}
-
 }  // namespace
 
 template <int D, int G, int C, bool DEEP>
@@ -125,10 +87,10 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
 
   tl_mark(p.tl, 0);
   const int h = blockIdx.y, b = blockIdx.z;
-  const int rank = static_cast<int>(cluster_ctarank());
+  const int rank = static_cast<int>(attn::cluster_ctarank());
   // The merge writes into the other CTAs' shared memory: first barrier phase, completed
   // before the first remote store, so every CTA of the cluster is known to be running.
-  cluster_arrive_relaxed();
+  attn::cluster_arrive_relaxed();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
@@ -138,7 +100,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
   P = P < 0 ? 0 : (P >= p.max_ctx ? p.max_ctx - 1 : P);  // flagged by the embedding kernel
   const int T = P + 1;
   int pos_begin, pos_end;
-  attention_run(T, C, rank, &pos_begin, &pos_end);
+  attn::attention_run(T, C, rank, &pos_begin, &pos_end);
   const int ntiles = (pos_end - pos_begin + kAttnTile - 1) / kAttnTile;
   // one token: this kernel appends slot P itself (and patches the stale copy it read);
   // a verify step appended every row's slot in the previous kernel
@@ -403,71 +365,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention(AttnParams p) {
     }
   }
   __syncthreads();
-  // ---- cluster merge, pushed: CTA `rank` owns outputs [rank kPer, (rank + 1) kPer) of
-  // the G D; every CTA stores its (m, l) per head and its combined partial outputs of
-  // each owner's slice into the owner's receive area (record `rank`: m[G], l[G],
-  // acc[kPer]), then one cluster barrier, then each owner merges from its own memory.
-  constexpr int kOut = G * D;
-  constexpr int kPer = (kOut + C - 1) / C;
-  constexpr int kRec = 2 * G + kPer;
-  static_assert(C * kRec <= CF::kXchgFloats, "receive area too small");
-  const uint32_t recv_local = smem_u32(xchg);
-  float* fw = misc;  // [4][G] warp weights
-  cluster_wait();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * G + tid]);
-    float L = 0.f;
-    for (int w = 0; w < 4; ++w) {
-      const float f = (M == -INFINITY) ? 0.f : exp2f(mw[w * G + tid] - M);
-      fw[w * G + tid] = f;
-      L += f * lw[w * G + tid];
-    }
-#pragma unroll 1
-    for (int r = 0; r < C; ++r) {
-      const uint32_t rec = map_rank(recv_local + (rank * kRec) * 4, static_cast<uint32_t>(r));
-      st_cluster_f32(rec + tid * 4, M);
-      st_cluster_f32(rec + (G + tid) * 4, L);
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < kOut; i += kAttnThreads) {
-    const int j = i / D, e = i % D;
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) a += fw[w * G + j] * ow[(w * G + j) * D + e];
-    const int owner = i / kPer;
-    const uint32_t rec = map_rank(recv_local + (rank * kRec) * 4, static_cast<uint32_t>(owner));
-    st_cluster_f32(rec + (2 * G + i - owner * kPer) * 4, a);
-  }
-  cluster_sync();
-  {
-    float* out_b = p.out + static_cast<size_t>(b) * p.nq * D + h * G * D;
-    const int i_end = (rank + 1) * kPer < kOut ? (rank + 1) * kPer : kOut;
-    for (int i = rank * kPer + tid; i < i_end; i += kAttnThreads) {
-      const int j = i / D, k = i - rank * kPer;
-      float M = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < C; ++r) M = fmaxf(M, xchg[r * kRec + j]);
-      float num = 0.f, den = 0.f;
-#pragma unroll
-      for (int r = 0; r < C; ++r) {
-        const float mr = xchg[r * kRec + j];
-        const float f = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
-        num = fmaf(f, xchg[r * kRec + 2 * G + k], num);
-        den = fmaf(f, xchg[r * kRec + G + j], den);
-      }
-      const float ov = num / den;
-      out_b[i] = ov;
-      if (p.out_hl) {  // batched path: the O projection's input as hi + lo planes
-        const size_t o = static_cast<size_t>(b) * p.nq * D + h * G * D + i;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(ov);
-        p.out_hl[o] = hi;
-        p.out_hl[static_cast<size_t>(p.B) * p.nq * D + o] = __float2bfloat16_rn(ov - __bfloat162float(hi));
-      }
-    }
-  }
-  // no shared::cluster access follows the barrier: CTAs leave independently
+  attn::merge_store<D, G, C>(p, mw, lw, ow, xchg, misc, rank, b, h, tid);
   // Dependents are released only now: when their CTAs start earlier, on the SMs this
   // kernel runs on, their weight loads crowd the load/store pipe and the merge above
   // measured several times slower.
@@ -526,84 +424,23 @@ __global__ void __launch_bounds__(32) k_kv_append(AttnParams p) {
 
 namespace {
 
-// Launch shapes: 0 = clusters of 8, shallow ring; 1 = clusters of 8, deep ring;
-// 2 = clusters of 16, deep ring; 3 = clusters of 12, deep ring (16 and 12 are
-// non-portable sizes); 4 = clusters of 4, shallow ring.
-constexpr int kShapes = 5;
-
 template <int D, int G, int C, bool DEEP>
-cudaLaunchConfig_t attn_config(const AttnParams& p, cudaStream_t stream, bool pdl, cudaLaunchAttribute (&attr)[2]) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, p.nkv, p.B);
-  cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = AttnCfg<D, DEEP>::kBytes;
-  cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cfg;
-}
+struct Bf16Kern {
+  static constexpr size_t kSmem = AttnCfg<D, DEEP>::kBytes;
+  static auto kernel() { return k_attention<D, G, C, DEEP>; }
+};
 
-template <int D, int G, int C, bool DEEP>
-cudaError_t launch_attn_t(const LaunchCtx& c, const AttnParams& p) {
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = attn_config<D, G, C, DEEP>(p, c.stream, c.pdl, attr);
-  return cudaLaunchKernelEx(&cfg, k_attention<D, G, C, DEEP>, p);
-}
-
-// Shared-memory limit (and the non-portable cluster size), then the number of
-// clusters of this shape that fit on the device at once.
-template <int D, int G, int C, bool DEEP>
-cudaError_t prepare_attn_t(int* max_clusters) {
-  auto kern = k_attention<D, G, C, DEEP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(AttnCfg<D, DEEP>::kBytes));
-  if (e != cudaSuccess) return e;
-  if (C > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-    return e;
-  AttnParams probe = {};
-  probe.B = 1;
-  probe.nkv = 1;
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = attn_config<D, G, C, DEEP>(probe, nullptr, false, attr);
-  cfg.numAttrs = 1;  // the cluster dimension only
-  return cudaOccupancyMaxActiveClusters(max_clusters, kern, &cfg);
-}
-
-template <int D, int G>
-cudaError_t prepare_all(int (&max_clusters)[kShapes]) {
-  cudaError_t e;
-  if ((e = prepare_attn_t<D, G, 8, false>(&max_clusters[0])) != cudaSuccess) return e;
-  if ((e = prepare_attn_t<D, G, 8, true>(&max_clusters[1])) != cudaSuccess) return e;
-  if ((e = prepare_attn_t<D, G, 16, true>(&max_clusters[2])) != cudaSuccess) return e;
-  if ((e = prepare_attn_t<D, G, 12, true>(&max_clusters[3])) != cudaSuccess) return e;
-  return prepare_attn_t<D, G, 4, false>(&max_clusters[4]);
-}
-
-template <int D, int G>
-cudaError_t launch_shape(const LaunchCtx& c, const AttnParams& p, int shape) {
-  if (shape == 4) return launch_attn_t<D, G, 4, false>(c, p);
-  if (shape == 3) return launch_attn_t<D, G, 12, true>(c, p);
-  if (shape == 2) return launch_attn_t<D, G, 16, true>(c, p);
-  if (shape == 1) return launch_attn_t<D, G, 8, true>(c, p);
-  return launch_attn_t<D, G, 8, false>(c, p);
-}
-
-// Per device and (head_dim, group): SM count and co-resident clusters per shape,
-// filled by prepare_attention (before any capture), read by launch_attention.
+// Per device, KV format, head_dim and group: SM count and co-resident clusters per
+// shape, filled by prepare_attention (before any capture), read by launch_attention.
 constexpr int kMaxAttnDevices = 64;
 struct AttnCaps {
   int num_sms = 0;
-  int max_clusters[kShapes] = {0, 0, 0, 0, 0};
+  int max_clusters[attn::kShapes] = {0, 0, 0, 0, 0};
 };
-AttnCaps g_caps[kMaxAttnDevices][2][3];
+AttnCaps g_caps[kMaxAttnDevices][2][2][3];
 std::mutex g_caps_mu;
 
+int fmt_index(int kv_fmt) { return kv_fmt == DEC_KV_AFFINE8_G64 ? 1 : 0; }
 int dim_index(int head_dim) { return head_dim == 64 ? 0 : 1; }
 int group_index(int G) { return G == 1 ? 0 : G == 2 ? 1 : 2; }
 
@@ -618,7 +455,7 @@ size_t attention_smem_bytes(int head_dim) {
 // query counts what the GPCs can place); with two CTAs per SM, 4-CTA clusters when they
 // make one wave and 8-CTA clusters would not; else 8-CTA clusters (many short CTAs keep
 // ragged batches balanced).
-int attention_shape(int B, int nkv, int head_dim, int G) {
+int attention_shape(int B, int nkv, int head_dim, int G, int kv_fmt) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxAttnDevices) return 0;
   if (head_dim != 64 && head_dim != 128) return 0;
@@ -626,7 +463,7 @@ int attention_shape(int B, int nkv, int head_dim, int G) {
   AttnCaps caps;
   {
     std::lock_guard<std::mutex> lock(g_caps_mu);
-    caps = g_caps[dev][dim_index(head_dim)][group_index(G)];
+    caps = g_caps[dev][fmt_index(kv_fmt)][dim_index(head_dim)][group_index(G)];
   }
   const long long clusters = static_cast<long long>(B) * nkv;
   if (caps.num_sms <= 0) return 0;
@@ -639,27 +476,19 @@ int attention_shape(int B, int nkv, int head_dim, int G) {
   return 0;
 }
 
-cudaError_t prepare_attention(int head_dim, int G) {
+cudaError_t prepare_attention(int head_dim, int G, int kv_fmt) {
   int dev = 0, sms = 0;
   cudaError_t e;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   AttnCaps caps;
   caps.num_sms = sms;
-#define DEC_ATTN_PREP(D_, G_) \
-  if (head_dim == D_ && G == G_) e = prepare_all<D_, G_>(caps.max_clusters); else
-  DEC_ATTN_PREP(64, 1)
-  DEC_ATTN_PREP(64, 2)
-  DEC_ATTN_PREP(64, 4)
-  DEC_ATTN_PREP(128, 1)
-  DEC_ATTN_PREP(128, 2)
-  DEC_ATTN_PREP(128, 4)
-  e = cudaErrorInvalidValue;
-#undef DEC_ATTN_PREP
+  e = kv_fmt == DEC_KV_AFFINE8_G64 ? prepare_attention_q8(head_dim, G, caps.max_clusters)
+                                   : attn::prepare_dims<Bf16Kern>(head_dim, G, caps.max_clusters);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxAttnDevices) {
     std::lock_guard<std::mutex> lock(g_caps_mu);
-    g_caps[dev][dim_index(head_dim)][group_index(G)] = caps;
+    g_caps[dev][fmt_index(kv_fmt)][dim_index(head_dim)][group_index(G)] = caps;
   }
   return cudaSuccess;
 }
@@ -674,24 +503,16 @@ cudaError_t launch_kv_append(const LaunchCtx& c, const AttnParams& p, int head_d
   attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.kv_fmt == DEC_KV_AFFINE8_G64) return launch_kv_append_q8(cfg, p, head_dim);
   if (head_dim == 64) return cudaLaunchKernelEx(&cfg, k_kv_append<64>, p);
   if (head_dim == 128) return cudaLaunchKernelEx(&cfg, k_kv_append<128>, p);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim) {
-  const int G = p.nq / p.nkv;
-  const int shape = attention_shape(p.B, p.nkv, head_dim, G);
-#define DEC_ATTN_CASE(D_, G_) \
-  if (head_dim == D_ && G == G_) return launch_shape<D_, G_>(c, p, shape);
-  DEC_ATTN_CASE(64, 1)
-  DEC_ATTN_CASE(64, 2)
-  DEC_ATTN_CASE(64, 4)
-  DEC_ATTN_CASE(128, 1)
-  DEC_ATTN_CASE(128, 2)
-  DEC_ATTN_CASE(128, 4)
-#undef DEC_ATTN_CASE
-  return cudaErrorInvalidValue;
+  const int shape = attention_shape(p.B, p.nkv, head_dim, p.nq / p.nkv, p.kv_fmt);
+  if (p.kv_fmt == DEC_KV_AFFINE8_G64) return launch_attention_q8(c, p, head_dim, shape);
+  return attn::launch_dims<Bf16Kern>(c, p, head_dim, shape);
 }
 
 }  // namespace dec

@@ -35,12 +35,14 @@ dec_status setup_device(int dev, unsigned char** addr) {
     }
     const int dims[2] = {64, 128};
     const int groups[3] = {1, 2, 4};
-    for (int d : dims)
-      for (int g : groups)
-        if ((e = prepare_attention(d, g)) != cudaSuccess) {
-          set_last_error("dec_attention_noalloc: kernel set-up failed: %s", cudaGetErrorString(e));
-          return DEC_ERR_CUDA;
-        }
+    const int fmts[2] = {DEC_KV_BF16, DEC_KV_AFFINE8_G64};
+    for (int f : fmts)
+      for (int d : dims)
+        for (int g : groups)
+          if ((e = prepare_attention(d, g, f)) != cudaSuccess) {
+            set_last_error("dec_attention_noalloc: kernel set-up failed: %s", cudaGetErrorString(e));
+            return DEC_ERR_CUDA;
+          }
     g_scratch_addr[dev] = static_cast<unsigned char*>(p);
   }
   *addr = g_scratch_addr[dev];
@@ -66,6 +68,14 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
   const int G = c.n_q_heads / c.n_kv_heads;
   if ((G != 1 && G != 2 && G != 4) || (c.head_dim != 64 && c.head_dim != 128)) {
     set_last_error("dec_attention_noalloc: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c.kv_fmt != DEC_KV_BF16 && c.kv_fmt != DEC_KV_AFFINE8_G64) {
+    set_last_error("dec_attention_noalloc: unknown kv_fmt %d", c.kv_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c.kv_fmt == DEC_KV_AFFINE8_G64 && c.max_ctx % 16 != 0) {
+    set_last_error("dec_attention_noalloc: the affine 8-bit KV cache needs max_ctx to be a multiple of 16");
     return DEC_ERR_UNSUPPORTED;
   }
   if (!qkv || !q_norm || !k_norm || !positions || !kv_cache || !out ||
@@ -110,7 +120,7 @@ extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, co
   ap.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
   ap.rope = rope;
   ap.positions = positions;
-  ap.kv = static_cast<__nv_bfloat16*>(kv_cache);
+  attn_set_cache(ap, c, kv_cache);
   ap.layer = layer;
   ap.B = c.batch;
   ap.nq = c.n_q_heads;

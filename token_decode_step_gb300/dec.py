@@ -24,6 +24,9 @@ DEC_ERR_DEVICE_INPUT = 6
 DEC_W_BF16 = 0
 DEC_W_AFFINE4_G64 = 1
 
+DEC_KV_BF16 = 0
+DEC_KV_AFFINE8_G64 = 1
+
 DEC_K_EMBED, DEC_K_QKV, DEC_K_ATTN, DEC_K_OPROJ, DEC_K_GATEUP, DEC_K_DOWN, DEC_K_LMHEAD, DEC_K_COUNT = range(8)
 KERNEL_CLASS_NAMES = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
 
@@ -42,7 +45,7 @@ class DecConfig(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("intermediate", ctypes.c_int),
         ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
         ("linear_fmt", ctypes.c_int), ("batch", ctypes.c_int), ("max_ctx", ctypes.c_int),
-        ("tokens_per_seq", ctypes.c_int),
+        ("tokens_per_seq", ctypes.c_int), ("kv_fmt", ctypes.c_int),
     ]
 
 
@@ -94,6 +97,7 @@ def _load() -> ctypes.CDLL:
         "dec_attention_noalloc": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.c_int, vp, vp, vp, vp, vp, vp,
                                                  vp]),
         "dec_sample": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(SamplingParams), vp, vp]),
+        "dec_kv_quantize": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -199,6 +203,10 @@ def dec_attention_noalloc(cfg: DecConfig, layer: int, qkv: int, q_norm: int, k_n
 
 def dec_sample(logits: int, batch: int, vocab: int, params: SamplingParams, tokens: int, stream: int = 0) -> int:
     return _check(lib.dec_sample(logits, batch, vocab, ctypes.byref(params), tokens, stream), "dec_sample")
+
+
+def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
+    return _check(lib.dec_kv_quantize(src, rows, head_dim, codes, params, stream), "dec_kv_quantize")
 
 
 def dec_debug_step_prefix(h: int, token_ids: int, positions: int, kv_cache: int, logits_out: int | None,

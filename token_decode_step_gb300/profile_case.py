@@ -44,8 +44,9 @@ def main(argv=None) -> int:
     logits = torch.empty((B, wl.vocab), device="cuda")
     amax = torch.empty((B,), dtype=torch.int32, device="cuda")
     tok, pos = model["tokens"].clone(), model["positions"].clone()
+    kv = synthetic.kv_buffer(model["kv"])
     for _ in range(a.steps):
-        d.step(tok, pos, model["kv"], logits, amax)
+        d.step(tok, pos, kv, logits, amax)
         d.advance(amax, tok, pos)
     torch.cuda.synchronize()
     st = d.device_status()

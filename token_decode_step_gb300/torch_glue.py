@@ -22,13 +22,26 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 
 def make_config(shape, batch: int | None = None, max_ctx: int | None = None,
                 tokens_per_seq: int = 1) -> dec.DecConfig:
-    """dec_config from any object with the model-shape attributes (n_layers, hidden, ...)."""
+    """dec_config from any object with the model-shape attributes (n_layers, hidden, ...,
+    and optionally kv_format "bf16" / "affine8_g64")."""
     fmt = dec.DEC_W_BF16 if shape.weight_format == "bf16" else dec.DEC_W_AFFINE4_G64
-    return dec.DecConfig(
+    kv_fmt = dec.DEC_KV_AFFINE8_G64 if getattr(shape, "kv_format", "bf16") == "affine8_g64" else dec.DEC_KV_BF16
+    return dec.DecConfig(kv_fmt=kv_fmt, **_shape_fields(shape, fmt, batch, max_ctx, tokens_per_seq))
+
+
+def _shape_fields(shape, fmt, batch, max_ctx, tokens_per_seq) -> dict:
+    return dict(
         n_layers=shape.n_layers, hidden=shape.hidden, n_q_heads=shape.n_q_heads, n_kv_heads=shape.n_kv_heads,
         head_dim=shape.head_dim, intermediate=shape.intermediate, vocab=shape.vocab, rms_eps=shape.rms_eps,
         rope_theta=shape.rope_theta, linear_fmt=fmt, batch=batch if batch is not None else shape.batch,
         max_ctx=max_ctx if max_ctx is not None else shape.max_ctx, tokens_per_seq=tokens_per_seq)
+
+
+def kv_quantize(src: torch.Tensor, codes: torch.Tensor, params: torch.Tensor) -> None:
+    """dec_kv_quantize on CUDA tensors: src float32 [rows, d], codes uint8 [rows, d], params
+    bf16 [rows, d/64, 2]."""
+    rows, d = src.shape
+    dec.dec_kv_quantize(_ptr(src), rows, d, _ptr(codes), _ptr(params), torch.cuda.current_stream().cuda_stream)
 
 
 def _linear(x) -> dec.DecLinear:
