@@ -95,8 +95,10 @@ class Workload:
 
     @property
     def max_ctx(self) -> int:
-        """Cache slots per sequence: every cached position plus one per step."""
-        return self.max_prefill + self.steps
+        """Cache slots per sequence: every cached position plus one per step (rounded up to
+        a multiple of 16 for the affine 8-bit cache, which needs that)."""
+        n = self.max_prefill + self.steps
+        return (n + 15) // 16 * 16 if self.kv_format == AFFINE8_G64 else n
 
     def shapes(self) -> dict[str, tuple[int, int]]:
         H, d = self.hidden, self.head_dim

@@ -59,6 +59,8 @@ CASES = [
     (12, 4, 2, 64, [5, 300, 17, 1000, 64, 129, 2, 999, 640, 31, 1023, 256], 1024),
     # clusters of 8 would take two waves of two CTAs per SM, clusters of 4 take one
     (10, 16, 4, 128, [900, 1, 2047, 333, 64, 65, 1500, 0, 1000, 2000], 2048),
+    # the batch-32 8B shapes: 256 clusters of 4, several waves of two CTAs per SM
+    (32, 32, 8, 128, [int(x) for x in np.random.default_rng(32).integers(512, 8193, 32)], 8224),
 ]
 
 

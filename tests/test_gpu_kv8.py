@@ -129,6 +129,8 @@ ATT_CASES = [
     (6, 16, 4, 128, [1500, 0, 63, 64, 777, 1200], 1536),
     (12, 4, 2, 64, [5, 300, 17, 1000, 64, 129, 2, 999, 640, 31, 1023, 256], 1024),
     (10, 16, 4, 128, [900, 1, 2047, 333, 64, 65, 1500, 0, 1000, 2000], 2048),
+    # the batch-32 8B shapes: 256 clusters (several waves of two CTAs per SM), long contexts
+    (32, 32, 8, 128, [int(x) for x in np.random.default_rng(32).integers(512, 8193, 32)], 8224),
 ]
 
 
@@ -258,15 +260,9 @@ KV8_CUSTOM = [
 
 @pytest.mark.parametrize("name,kw", KV8_CUSTOM, ids=[c[0] for c in KV8_CUSTOM])
 def test_kv8_custom_shapes(glue, name, kw):
-    kw = dict(kw)
-    pre = kw["prefill"]
-    steps = kw["steps"]
-    hi = pre[1] if isinstance(pre, tuple) else pre
-    # max_ctx = largest prefill + steps must be a multiple of 16 for this format
-    pad = (-(hi + steps)) % 16
-    kw["steps"] = steps + pad
     wl = synthetic.custom(name=name, seed=sum(map(ord, name)), kv_format=synthetic.AFFINE8_G64, **kw)
-    w = _run_kv8(glue, wl, steps)
+    assert wl.max_ctx % 16 == 0
+    w = _run_kv8(glue, wl, wl.steps)
     print(name, w)
 
 
@@ -292,8 +288,7 @@ def test_kv8_graph_equals_eager_bitwise(glue):
              intermediate=512, prefill=(0, 141), n_layers=2)),
 ])
 def test_kv8_verify_matches_oracle(glue, T, kw):
-    wl = synthetic.custom(name=f"kv8_verify_{T}", seed=40 + T, steps=(-(kw["prefill"][1])) % 16 or 16,
-                          kv_format=synthetic.AFFINE8_G64, **kw)
+    wl = synthetic.custom(name=f"kv8_verify_{T}", seed=40 + T, steps=T, kv_format=synthetic.AFFINE8_G64, **kw)
     assert wl.max_ctx % 16 == 0 and wl.max_ctx >= wl.max_prefill + T
     model = synthetic.generate(wl, device="cuda")
     host = synthetic.to_host(model)

@@ -40,20 +40,24 @@ namespace {
 
 using attn::kLog2e;
 
+constexpr int kQ8Tile = 128;  // positions per stage: four warps of two 16-position chunks
+constexpr int kQ8Warp = 32;   // positions per warp and stage
+
 template <int D, bool DEEP>
 struct Q8Cfg {
   static constexpr int NG = D / 64;                        // groups of 64 per row
-  static constexpr int kStages = DEEP ? (D == 128 ? 11 : 20) : (D == 128 ? 5 : 9);
-  static constexpr int kCodeTile = kAttnTile * D;          // one plane's codes
-  static constexpr int kParTile = kAttnTile * NG * 4;      // one plane's (scale, bias) pairs
+  static constexpr int kStages = DEEP ? (D == 128 ? 5 : 10) : (D == 128 ? 3 : 5);
+  static constexpr int kCodeTile = kQ8Tile * D;            // one plane's codes
+  static constexpr int kParTile = kQ8Tile * NG * 4;        // one plane's (scale, bias) pairs
   static constexpr int kStageBytes = 2 * kCodeTile + 2 * kParTile;  // K codes, V codes, K pairs, V pairs
   static constexpr int kOffQ = 0;                          // [16][D] f16 A operand
   static constexpr int kOffStages = 16 * D * 2;
   static constexpr int kOffNew = kOffStages + kStages * kStageBytes;  // new row: K, V codes; K, V pairs
   static constexpr int kNewBytes = (2 * D + 2 * NG * 4 + 15) / 16 * 16;
-  static constexpr int kOffWp = kOffNew + kNewBytes;       // per warp: [16 positions][NG] float4
-  static constexpr int kWpBytes = 4 * 16 * NG * 16;
-  static constexpr int kOffXchg = kOffWp + kWpBytes;
+  // per warp [32 positions][NG] float4, over the Q operand (in registers before the first stage)
+  static constexpr int kOffWp = kOffQ;
+  static_assert(4 * kQ8Warp * NG * 16 <= kOffStages, "per-warp floats must fit the Q operand's space");
+  static constexpr int kOffXchg = kOffNew + kNewBytes;
   static constexpr int kOffMisc = kOffXchg + attn::Xchg<D>::kFloats * 4;  // merge weights, query group sums
   static constexpr int kBytes = kOffMisc + 64 * 4;
 };
@@ -126,7 +130,7 @@ __device__ __forceinline__ void store_row_q8(const float (&x)[D / 32], unsigned 
   }
 }
 
-// One stage: K and V codes of positions pos0..pos0+63 (zero past valid_end) into swizzled
+// One stage: K and V codes of positions pos0..pos0+127 (zero past valid_end) into swizzled
 // tiles, then their (scale, bias) pairs (zero past valid_end, so masked positions stay finite).
 template <int D>
 __device__ __forceinline__ void load_tile_q8(uint32_t stage, const unsigned char* kc, const unsigned char* vc,
@@ -135,7 +139,7 @@ __device__ __forceinline__ void load_tile_q8(uint32_t stage, const unsigned char
   using CF = Q8Cfg<D, false>;
   constexpr int NG = CF::NG;
   constexpr int kPieces = D / 16;
-  constexpr int kTotal = kAttnTile * kPieces;
+  constexpr int kTotal = kQ8Tile * kPieces;
 #pragma unroll
   for (int j = 0; j < kTotal / kAttnThreads; ++j) {
     const int idx = threadIdx.x + j * kAttnThreads;
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
   const int T = P + 1;
   int pos_begin, pos_end;
   attn::attention_run(T, C, rank, &pos_begin, &pos_end);
-  const int ntiles = (pos_end - pos_begin + kAttnTile - 1) / kAttnTile;
+  const int ntiles = (pos_end - pos_begin + kQ8Tile - 1) / kQ8Tile;
   const bool has_new = tps == 1 && (P >= pos_begin && P < pos_end);
 
   // (layer, plane, sequence, head) rows of the codes and of the pairs
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
       if (s < ntiles)
-        load_tile_q8<D>(sStages + s * CF::kStageBytes, kc, vc, kp, vp, pos_begin + s * kAttnTile, pos_end);
+        load_tile_q8<D>(sStages + s * CF::kStageBytes, kc, vc, kp, vp, pos_begin + s * kQ8Tile, pos_end);
       cp_async_commit();
     }
   };
@@ -236,9 +240,11 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
   __syncthreads();
 
   float m_run = -INFINITY, l_run = 0.f;
-  float o[D / 8][4];
+  // O^T accumulators, one m16n8 tile per 16 dimensions s: rows g / g + 8 = dimensions
+  // 16 s + 2 g / 16 s + 2 g + 1, columns 2t, 2t + 1 = head-rows (hi rows 0..G-1, lo rows G..2G-1)
+  float o[D / 16][4];
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  for (int j = 0; j < D / 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float bacc[NG];  // sum over positions of p (bias - 1024 scale) of V, per group
 #pragma unroll
   for (int gr = 0; gr < NG; ++gr) bacc[gr] = 0.f;
@@ -348,16 +354,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
       {  // refill the stage consumed in the previous iteration
         const int nxt = it + S - 1;
         if (nxt < ntiles)
-          load_tile_q8<D>(sStages + (nxt % S) * CF::kStageBytes, kc, vc, kp, vp, pos_begin + nxt * kAttnTile,
+          load_tile_q8<D>(sStages + (nxt % S) * CF::kStageBytes, kc, vc, kp, vp, pos_begin + nxt * kQ8Tile,
                           pos_end);
         cp_async_commit();
       }
       cp_async_wait<S - 1>();  // stage `it` has landed
       __syncthreads();
       const int st = it % S;
-      const int tile_pos0 = pos_begin + it * kAttnTile;
+      const int tile_pos0 = pos_begin + it * kQ8Tile;
       unsigned char* stg = smem + CF::kOffStages + st * CF::kStageBytes;
-      if (has_new && P >= tile_pos0 && P < tile_pos0 + kAttnTile) {
+      if (has_new && P >= tile_pos0 && P < tile_pos0 + kQ8Tile) {
         // the cache row at P was read before this step's append: use the fresh values
         const int r = P - tile_pos0;
         if (tid < D / 16) {
@@ -371,152 +377,177 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         }
         __syncthreads();
       }
-      const int wrow = warp * 16;  // this warp's 16 positions within the stage
-
-      // ---- this warp's (scale, bias - 1024 scale) of K and V as floats, and the prescale
-      float4* wp = reinterpret_cast<float4*>(smem + CF::kOffWp) + warp * 16 * NG;
-      float sv_max = 0.f;
-      if (lane < 16 * NG) {
-        const int pl = lane / NG, gr = lane % NG;
-        const uint32_t pk = reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile)[(wrow + pl) * NG + gr];
-        const uint32_t pv =
-            reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile + CF::kParTile)[(wrow + pl) * NG + gr];
-        const float sk = __uint_as_float(pk << 16), bk = __uint_as_float(pk & 0xffff0000u);
-        const float sv = __uint_as_float(pv << 16), bv = __uint_as_float(pv & 0xffff0000u);
-        wp[pl * NG + gr] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(-1024.f, sv, bv));
-        sv_max = fabsf(sv);
-      }
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o2));
-      __syncwarp();
-      // |p scale_V| 2^e < 2^14 for p <= 1: e = 13 - floor(log2 max|scale_V|)
-      int e_tile = 100;
-      if (sv_max > 0.f) {
-        const int ex = static_cast<int>((__float_as_uint(sv_max) >> 23) & 0xffu) - 127;
-        e_tile = 13 - ex < 100 ? 13 - ex : 100;
-        e_tile = e_tile > -100 ? e_tile : -100;
-      }
-      int de = 0;
-      if (e_tile < e_run) {
-        de = e_tile - e_run;
-        e_run = e_tile;
-      }
-      const float f_e = pow2i(e_run);
-      const float f_de = de < -126 ? 0.f : pow2i(de);
-
-      const uint32_t tK = sStages + st * CF::kStageBytes, tV = tK + CF::kCodeTile;
-
-      // ---- S = Q K^T: rows g (group 0) / g + 8 (group 1) x 16 positions
-      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int row = wrow + (mi >> 1) * 8 + rr;  // matrices (block 0, piece), (0, piece+1), (1, piece), (1, piece+1)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk += 2) {
-          uint32_t r4[4];
-          ldmatrix_x4(r4, tK + swz8<D>(row, kk + (mi & 1)));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-              const uint32_t w = r4[blk * 2 + u];
-              const uint32_t b0 = __byte_perm(w, 0x64646464u, 0x4140);
-              const uint32_t b1 = __byte_perm(w, 0x64646464u, 0x4342);
-              mma_f16_16816(sacc[blk], qa[kk + u][0], qa[kk + u][1], qa[kk + u][2], qa[kk + u][3], b0, b1);
-            }
-          }
-        }
-      }
-      // scores of head (g % G) at positions wrow + 8 blk + 2 t + i, with the V factors
-      float sv[4], vs[4][NG], vb[4][NG];
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int idx = blk * 2 + i, pl = 8 * blk + 2 * t + i;
-          float sc = 0.f;
+      const int wrow = warp * kQ8Warp;  // this warp's 32 positions (two chunks of 16) within the stage
+      if (tile_pos0 + wrow < pos_end) {  // (warp-uniform: a stage's tail beyond the run is skipped)
+        // ---- (scale, bias - 1024 scale) of K and V as floats for this warp's positions, and the prescale
+        float4* wp = reinterpret_cast<float4*>(smem + CF::kOffWp) + warp * kQ8Warp * NG;
+        float sv_max = 0.f;
+        {
+          const uint32_t* pkk = reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile) + (wrow + lane) * NG;
+          const uint32_t* pvv =
+              reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile + CF::kParTile) + (wrow + lane) * NG;
 #pragma unroll
           for (int gr = 0; gr < NG; ++gr) {
-            float s = sacc[blk][2 * gr + i];
-            s += __shfl_xor_sync(0xffffffffu, s, 4 * G);  // hi + lo rows
-            const float4 f = wp[pl * NG + gr];
-            sc = fmaf(f.x, s, fmaf(f.y, qsl[gr], sc));
-            vs[idx][gr] = f.z;
-            vb[idx][gr] = f.w;
-          }
-          const int pos = tile_pos0 + wrow + pl;
-          sv[idx] = pos < pos_end ? sc * scale_log2 : -INFINITY;
-        }
-      }
-      float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      const float mref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-      float pr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pr[i] = exp2f(sv[i] - mref);
-      l_run = l_run * corr + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-      m_run = m_new;
-      const float co = corr * f_de;
-      if (!__all_sync(0xffffffffu, co == 1.f)) {
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {  // the live half: rows of the block's group
-          if (NG == 2 && (j >> 3)) {
-            o[j][2] *= co;
-            o[j][3] *= co;
-          } else {
-            o[j][0] *= co;
-            o[j][1] *= co;
+            const uint32_t pk = pkk[gr], pv = pvv[gr];
+            const float sk = __uint_as_float(pk << 16), bk = __uint_as_float(pk & 0xffff0000u);
+            const float sv = __uint_as_float(pv << 16), bv = __uint_as_float(pv & 0xffff0000u);
+            wp[lane * NG + gr] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(-1024.f, sv, bv));
+            sv_max = fmaxf(sv_max, fabsf(sv));
           }
         }
-      }
 #pragma unroll
-      for (int gr = 0; gr < NG; ++gr) {
-        bacc[gr] *= corr;
+        for (int o2 = 16; o2 > 0; o2 >>= 1) sv_max = fmaxf(sv_max, __shfl_xor_sync(0xffffffffu, sv_max, o2));
+        __syncwarp();
+        // |p scale_V| 2^e < 2^14 for p <= 1: e = 13 - floor(log2 max|scale_V|)
+        int e_tile = 100;
+        if (sv_max > 0.f) {
+          const int ex = static_cast<int>((__float_as_uint(sv_max) >> 23) & 0xffu) - 127;
+          e_tile = 13 - ex < 100 ? 13 - ex : 100;
+          e_tile = e_tile > -100 ? e_tile : -100;
+        }
+        int de = 0;
+        if (e_tile < e_run) {
+          de = e_tile - e_run;
+          e_run = e_tile;
+        }
+        const float f_e = pow2i(e_run);
+        const float f_de = de < -126 ? 0.f : pow2i(de);
+
+        const uint32_t tK = sStages + st * CF::kStageBytes, tV = tK + CF::kCodeTile;
+
+        // ---- S = Q K^T for both chunks: rows g (group 0) / g + 8 (group 1) x 16 positions each
+        float sacc[2][2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) bacc[gr] = fmaf(pr[i], vb[i][gr], bacc[gr]);
-      }
-      // A operand of P: (row g, k) = group 0, (row g + 8, k) = group 1; k = 2t.. block 0,
-      // 2t + 8.. block 1; hi rows the f16 value of p scale_V 2^e, lo rows its remainder
-      uint32_t pa[4];
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
+          for (int blk = 0; blk < 2; ++blk) sacc[c][blk][0] = sacc[c][blk][1] = sacc[c][blk][2] = sacc[c][blk][3] = 0.f;
+        {
+          const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-        for (int gr = 0; gr < 2; ++gr) {
-          uint32_t reg = 0u;
-          if (gr < NG) {
-            const float w0 = pr[2 * blk] * f_e * vs[2 * blk][gr < NG ? gr : 0];
-            const float w1 = pr[2 * blk + 1] * f_e * vs[2 * blk + 1][gr < NG ? gr : 0];
-            const __half2 hi = __floats2half2_rn(w0, w1);
-            if (lo_part) {
-              const float2 hf = __half22float2(hi);
-              reg = h2_bits(__floats2half2_rn(w0 - hf.x, w1 - hf.y));
-            } else {
-              reg = h2_bits(hi);
+          for (int kk = 0; kk < D / 16; kk += 2) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              // matrices (block 0, piece), (0, piece + 1), (1, piece), (1, piece + 1) of chunk c
+              const int row = wrow + 16 * c + (mi >> 1) * 8 + rr;
+              uint32_t r4[4];
+              ldmatrix_x4(r4, tK + swz8<D>(row, kk + (mi & 1)));
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                  const uint32_t w = r4[blk * 2 + u];
+                  mma_f16_16816(sacc[c][blk], qa[kk + u][0], qa[kk + u][1], qa[kk + u][2], qa[kk + u][3],
+                                __byte_perm(w, 0x64646464u, 0x4140), __byte_perm(w, 0x64646464u, 0x4342));
+                }
+              }
             }
-            if (!live_row) reg = 0u;
           }
-          pa[blk * 2 + gr] = reg;
         }
-      }
-      // ---- O += P V: per 16-dimension piece, the even then the odd dimensions
-      {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int row = wrow + (mi & 1) * 8 + rr;  // matrices (pos 0-7, piece), (8-15, piece), (0-7, +1), (8-15, +1)
+        // scores of head (g % G) at positions wrow + 16 c + 8 blk + 2 t + i, with the V factors
+        float sv[8], vs[8][NG], vb[8][NG];
 #pragma unroll
-        for (int jj = 0; jj < D / 16; jj += 2) {
-          uint32_t r4[4];
-          ldmatrix_x4_trans(r4, tV + swz8<D>(row, jj + (mi >> 1)));
+        for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint32_t lo8 = r4[2 * u], hi8 = r4[2 * u + 1];
-            const int j = 2 * (jj + u);
-            mma_f16_16816(o[j], pa[0], pa[1], pa[2], pa[3], __byte_perm(lo8, 0x64646464u, 0x4240),
-                          __byte_perm(hi8, 0x64646464u, 0x4240));
-            mma_f16_16816(o[j + 1], pa[0], pa[1], pa[2], pa[3], __byte_perm(lo8, 0x64646464u, 0x4341),
-                          __byte_perm(hi8, 0x64646464u, 0x4341));
+          for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int idx = c * 4 + blk * 2 + i, pl = 16 * c + 8 * blk + 2 * t + i;
+              float sc = 0.f;
+#pragma unroll
+              for (int gr = 0; gr < NG; ++gr) {
+                float s2 = sacc[c][blk][2 * gr + i];
+                s2 += __shfl_xor_sync(0xffffffffu, s2, 4 * G);  // hi + lo rows
+                const float4 f = wp[pl * NG + gr];
+                sc = fmaf(f.x, s2, fmaf(f.y, qsl[gr], sc));
+                vs[idx][gr] = f.z;
+                vb[idx][gr] = f.w;
+              }
+              const int pos = tile_pos0 + wrow + pl;
+              sv[idx] = pos < pos_end ? sc * scale_log2 : -INFINITY;
+            }
+          }
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sv[i]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float mref = (m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+        float pr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pr[i] = exp2f(sv[i] - mref);
+        l_run = l_run * corr + (((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7])));
+        m_run = m_new;
+        if (!__all_sync(0xffffffffu, corr * f_de == 1.f)) {
+          // this lane's accumulator columns are head-rows 2t and 2t + 1, whose factors the
+          // lanes of those rows hold
+          const float ca = __shfl_sync(0xffffffffu, corr, 8 * t) * f_de;
+          const float cb = __shfl_sync(0xffffffffu, corr, 8 * t + 4) * f_de;
+#pragma unroll
+          for (int j = 0; j < D / 16; ++j) {
+            o[j][0] *= ca;
+            o[j][1] *= cb;
+            o[j][2] *= ca;
+            o[j][3] *= cb;
+          }
+        }
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+          bacc[gr] *= corr;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bacc[gr] = fmaf(pr[i], vb[i][gr], bacc[gr]);
+        }
+        // B operands of P^T per chunk and group: (k, column g) = head-row g at positions 2t..
+        // (pa[c][gr], block 0) and 2t + 8.. (pa[c][2 + gr], block 1); hi rows the f16 value of
+        // p scale_V 2^e, lo rows its remainder
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+#pragma unroll
+            for (int gr = 0; gr < 2; ++gr) {
+              uint32_t reg = 0u;
+              if (gr < NG) {
+                const int i0 = c * 4 + blk * 2;
+                const float w0 = pr[i0] * f_e * vs[i0][gr < NG ? gr : 0];
+                const float w1 = pr[i0 + 1] * f_e * vs[i0 + 1][gr < NG ? gr : 0];
+                const __half2 hi = __floats2half2_rn(w0, w1);
+                if (lo_part) {
+                  const float2 hf = __half22float2(hi);
+                  reg = h2_bits(__floats2half2_rn(w0 - hf.x, w1 - hf.y));
+                } else {
+                  reg = h2_bits(hi);
+                }
+                if (!live_row) reg = 0u;
+              }
+              pa[c][blk * 2 + gr] = reg;
+            }
+          }
+        }
+        // ---- O^T += V^T P^T: per chunk and 16-dimension piece s, A = the piece's codes (rows: its
+        // even dimensions, then its odd ones; k = the chunk's 16 positions), B = that group's P^T
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            // matrices (pos 0-7, piece), (8-15, piece), (0-7, piece + 1), (8-15, piece + 1) of chunk c
+            const int row = wrow + 16 * c + (mi & 1) * 8 + rr;
+#pragma unroll
+            for (int jj = 0; jj < D / 16; jj += 2) {
+              uint32_t r4[4];
+              ldmatrix_x4_trans(r4, tV + swz8<D>(row, jj + (mi >> 1)));
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const uint32_t lo8 = r4[2 * u], hi8 = r4[2 * u + 1];
+                const int sj = jj + u, gr = (NG == 2 && sj >= D / 32) ? 1 : 0;
+                mma_f16_16816(o[sj], __byte_perm(lo8, 0x64646464u, 0x4240), __byte_perm(lo8, 0x64646464u, 0x4341),
+                              __byte_perm(hi8, 0x64646464u, 0x4240), __byte_perm(hi8, 0x64646464u, 0x4341),
+                              pa[c][gr], pa[c][2 + gr]);
+              }
+            }
           }
         }
       }
@@ -538,18 +569,36 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
   float* mw = reinterpret_cast<float*>(smem + CF::kOffStages);
   float* lw = mw + 4 * G;
   float* ow = lw + 4 * G;
+  {
+    // head-rows 2t, 2t + 1 of this lane: add the lo rows (head-row + G), undo the prescale,
+    // add the bias part of the head's group (held by the lanes of row = head)
+    const int h0 = 2 * t, h1 = 2 * t + 1;
+    float ba[2][NG];
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j) {
-    // block j: dimensions 16 (j / 2) + 2 n + (j % 2), n = 2t, 2t + 1
-    const int gr = (NG == 2 && (j >> 3)) ? 1 : 0;
-    float v0 = gr ? o[j][2] : o[j][0];
-    float v1 = gr ? o[j][3] : o[j][1];
-    v0 += __shfl_xor_sync(0xffffffffu, v0, 4 * G);
-    v1 += __shfl_xor_sync(0xffffffffu, v1, 4 * G);
-    if (g < G) {
-      const int dim = 16 * (j >> 1) + 4 * t + (j & 1);
-      ow[(warp * G + g) * D + dim] = fmaf(v0, inv_e, bacc[gr]);
-      ow[(warp * G + g) * D + dim + 2] = fmaf(v1, inv_e, bacc[gr]);
+    for (int gr = 0; gr < NG; ++gr) {
+      ba[0][gr] = __shfl_sync(0xffffffffu, bacc[gr], 4 * (h0 % G));
+      ba[1][gr] = __shfl_sync(0xffffffffu, bacc[gr], 4 * (h1 % G));
+    }
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      const int gr = (NG == 2 && j >= D / 32) ? 1 : 0;
+      float v[4] = {o[j][0], o[j][1], o[j][2], o[j][3]};
+      if constexpr (G == 1) {  // head-row 0 (hi) and 1 (lo) are this lane's two columns
+        v[0] += v[1];
+        v[2] += v[3];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], G / 2);
+      }
+      const int dim = 16 * j + 2 * g;
+      if (G == 1 ? t == 0 : h1 < G) {
+        ow[(warp * G + h0) * D + dim] = fmaf(v[0], inv_e, ba[0][gr]);
+        ow[(warp * G + h0) * D + dim + 1] = fmaf(v[2], inv_e, ba[0][gr]);
+        if (G > 1) {
+          ow[(warp * G + h1) * D + dim] = fmaf(v[1], inv_e, ba[1][gr]);
+          ow[(warp * G + h1) * D + dim + 1] = fmaf(v[3], inv_e, ba[1][gr]);
+        }
+      }
     }
   }
   if (g < G && t == 0) {
