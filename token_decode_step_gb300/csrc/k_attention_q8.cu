@@ -40,15 +40,20 @@ namespace {
 
 using attn::kLog2e;
 
-constexpr int kQ8Tile = 128;  // positions per stage: four warps of two 16-position chunks
-constexpr int kQ8Warp = 32;   // positions per warp and stage
-
+// Two shapes: deep (one CTA per SM: 128-position stages, each warp two independent
+// 16-position chunks per stage, a five-stage ring at head_dim 128) and shallow (three CTAs
+// per SM, 12 warps to hide the latency of each warp's dependent chains: 64-position stages,
+// one chunk per warp, a three-stage ring, at most 170 registers).
 template <int D, bool DEEP>
 struct Q8Cfg {
   static constexpr int NG = D / 64;                        // groups of 64 per row
-  static constexpr int kStages = DEEP ? (D == 128 ? 5 : 10) : (D == 128 ? 3 : 5);
-  static constexpr int kCodeTile = kQ8Tile * D;            // one plane's codes
-  static constexpr int kParTile = kQ8Tile * NG * 4;        // one plane's (scale, bias) pairs
+  static constexpr int CH = DEEP ? 2 : 1;                  // 16-position chunks per warp and stage
+  static constexpr int kWarpPos = 16 * CH;                 // positions per warp and stage
+  static constexpr int kTile = 4 * kWarpPos;               // positions per stage
+  static constexpr int kMinBlocks = DEEP ? 1 : 3;          // CTAs per SM the registers are sized for
+  static constexpr int kStages = DEEP ? (D == 128 ? 5 : 10) : (D == 128 ? 3 : 6);
+  static constexpr int kCodeTile = kTile * D;              // one plane's codes
+  static constexpr int kParTile = kTile * NG * 4;          // one plane's (scale, bias) pairs
   static constexpr int kStageBytes = 2 * kCodeTile + 2 * kParTile;  // K codes, V codes, K pairs, V pairs
   static constexpr int kOffQ = 0;                          // [16][D] f16 A operand
   static constexpr int kOffStages = 16 * D * 2;
@@ -56,7 +61,7 @@ struct Q8Cfg {
   static constexpr int kNewBytes = (2 * D + 2 * NG * 4 + 15) / 16 * 16;
   // per warp [32 positions][NG] float4, over the Q operand (in registers before the first stage)
   static constexpr int kOffWp = kOffQ;
-  static_assert(4 * kQ8Warp * NG * 16 <= kOffStages, "per-warp floats must fit the Q operand's space");
+  static_assert(4 * kWarpPos * NG * 16 <= kOffStages, "per-warp floats must fit the Q operand's space");
   static constexpr int kOffXchg = kOffNew + kNewBytes;
   static constexpr int kOffMisc = kOffXchg + attn::Xchg<D>::kFloats * 4;  // merge weights, query group sums
   static constexpr int kBytes = kOffMisc + 64 * 4;
@@ -130,16 +135,16 @@ __device__ __forceinline__ void store_row_q8(const float (&x)[D / 32], unsigned 
   }
 }
 
-// One stage: K and V codes of positions pos0..pos0+127 (zero past valid_end) into swizzled
+// One stage: K and V codes of positions pos0.. (kTile of them; zero past valid_end) into swizzled
 // tiles, then their (scale, bias) pairs (zero past valid_end, so masked positions stay finite).
-template <int D>
+template <int D, bool DEEP>
 __device__ __forceinline__ void load_tile_q8(uint32_t stage, const unsigned char* kc, const unsigned char* vc,
                                              const unsigned char* kp, const unsigned char* vp, int pos0,
                                              int valid_end) {
-  using CF = Q8Cfg<D, false>;
+  using CF = Q8Cfg<D, DEEP>;
   constexpr int NG = CF::NG;
   constexpr int kPieces = D / 16;
-  constexpr int kTotal = kQ8Tile * kPieces;
+  constexpr int kTotal = CF::kTile * kPieces;
 #pragma unroll
   for (int j = 0; j < kTotal / kAttnThreads; ++j) {
     const int idx = threadIdx.x + j * kAttnThreads;
@@ -166,10 +171,12 @@ __device__ __forceinline__ void load_tile_q8(uint32_t stage, const unsigned char
 }  // namespace
 
 template <int D, int G, int C, bool DEEP>
-__global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, Q8Cfg<D, DEEP>::kMinBlocks) k_attention_q8(AttnParams p) {
   using CF = Q8Cfg<D, DEEP>;
   constexpr int S = CF::kStages;
   constexpr int NG = CF::NG;
+  constexpr int CH = CF::CH;
+  constexpr int kTile = CF::kTile;
   extern __shared__ __align__(128) unsigned char smem[];
 
   tl_mark(p.tl, 0);
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
   const int T = P + 1;
   int pos_begin, pos_end;
   attn::attention_run(T, C, rank, &pos_begin, &pos_end);
-  const int ntiles = (pos_end - pos_begin + kQ8Tile - 1) / kQ8Tile;
+  const int ntiles = (pos_end - pos_begin + kTile - 1) / kTile;
   const bool has_new = tps == 1 && (P >= pos_begin && P < pos_end);
 
   // (layer, plane, sequence, head) rows of the codes and of the pairs
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
 #pragma unroll
     for (int s = 0; s < S - 1; ++s) {
       if (s < ntiles)
-        load_tile_q8<D>(sStages + s * CF::kStageBytes, kc, vc, kp, vp, pos_begin + s * kQ8Tile, pos_end);
+        load_tile_q8<D, DEEP>(sStages + s * CF::kStageBytes, kc, vc, kp, vp, pos_begin + s * kTile, pos_end);
       cp_async_commit();
     }
   };
@@ -354,16 +361,16 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
       {  // refill the stage consumed in the previous iteration
         const int nxt = it + S - 1;
         if (nxt < ntiles)
-          load_tile_q8<D>(sStages + (nxt % S) * CF::kStageBytes, kc, vc, kp, vp, pos_begin + nxt * kQ8Tile,
+          load_tile_q8<D, DEEP>(sStages + (nxt % S) * CF::kStageBytes, kc, vc, kp, vp, pos_begin + nxt * kTile,
                           pos_end);
         cp_async_commit();
       }
       cp_async_wait<S - 1>();  // stage `it` has landed
       __syncthreads();
       const int st = it % S;
-      const int tile_pos0 = pos_begin + it * kQ8Tile;
+      const int tile_pos0 = pos_begin + it * kTile;
       unsigned char* stg = smem + CF::kOffStages + st * CF::kStageBytes;
-      if (has_new && P >= tile_pos0 && P < tile_pos0 + kQ8Tile) {
+      if (has_new && P >= tile_pos0 && P < tile_pos0 + kTile) {
         // the cache row at P was read before this step's append: use the fresh values
         const int r = P - tile_pos0;
         if (tid < D / 16) {
@@ -377,21 +384,20 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         }
         __syncthreads();
       }
-      const int wrow = warp * kQ8Warp;  // this warp's 32 positions (two chunks of 16) within the stage
+      const int wrow = warp * CF::kWarpPos;  // this warp's CH chunks of 16 positions within the stage
       if (tile_pos0 + wrow < pos_end) {  // (warp-uniform: a stage's tail beyond the run is skipped)
         // ---- (scale, bias - 1024 scale) of K and V as floats for this warp's positions, and the prescale
-        float4* wp = reinterpret_cast<float4*>(smem + CF::kOffWp) + warp * kQ8Warp * NG;
+        float4* wp = reinterpret_cast<float4*>(smem + CF::kOffWp) + warp * CF::kWarpPos * NG;
         float sv_max = 0.f;
-        {
-          const uint32_t* pkk = reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile) + (wrow + lane) * NG;
-          const uint32_t* pvv =
-              reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile + CF::kParTile) + (wrow + lane) * NG;
+        {  // pair q = (position q / NG, group q % NG) of this warp's positions
+          const uint32_t* pkk = reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile) + wrow * NG;
+          const uint32_t* pvv = reinterpret_cast<const uint32_t*>(stg + 2 * CF::kCodeTile + CF::kParTile) + wrow * NG;
 #pragma unroll
-          for (int gr = 0; gr < NG; ++gr) {
-            const uint32_t pk = pkk[gr], pv = pvv[gr];
+          for (int q = lane; q < CF::kWarpPos * NG; q += 32) {
+            const uint32_t pk = pkk[q], pv = pvv[q];
             const float sk = __uint_as_float(pk << 16), bk = __uint_as_float(pk & 0xffff0000u);
             const float sv = __uint_as_float(pv << 16), bv = __uint_as_float(pv & 0xffff0000u);
-            wp[lane * NG + gr] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(-1024.f, sv, bv));
+            wp[q] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(-1024.f, sv, bv));
             sv_max = fmaxf(sv_max, fabsf(sv));
           }
         }
@@ -416,9 +422,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         const uint32_t tK = sStages + st * CF::kStageBytes, tV = tK + CF::kCodeTile;
 
         // ---- S = Q K^T for both chunks: rows g (group 0) / g + 8 (group 1) x 16 positions each
-        float sacc[2][2][4];
+        float sacc[CH][2][4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < CH; ++c)
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) sacc[c][blk][0] = sacc[c][blk][1] = sacc[c][blk][2] = sacc[c][blk][3] = 0.f;
         {
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; kk += 2) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < CH; ++c) {
               // matrices (block 0, piece), (0, piece + 1), (1, piece), (1, piece + 1) of chunk c
               const int row = wrow + 16 * c + (mi >> 1) * 8 + rr;
               uint32_t r4[4];
@@ -444,9 +450,9 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
           }
         }
         // scores of head (g % G) at positions wrow + 16 c + 8 blk + 2 t + i, with the V factors
-        float sv[8], vs[8][NG], vb[8][NG];
+        float sv[4 * CH], vs[4 * CH][NG], vb[4 * CH][NG];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < CH; ++c) {
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
 #pragma unroll
@@ -469,16 +475,18 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         }
         float mx = sv[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) mx = fmaxf(mx, sv[i]);
+        for (int i = 1; i < 4 * CH; ++i) mx = fmaxf(mx, sv[i]);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float m_new = fmaxf(m_run, mx);
         const float mref = (m_new == -INFINITY) ? 0.f : m_new;
         const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-        float pr[8];
+        float pr[4 * CH];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pr[i] = exp2f(sv[i] - mref);
-        l_run = l_run * corr + (((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7])));
+        for (int i = 0; i < 4 * CH; ++i) pr[i] = exp2f(sv[i] - mref);
+        float psum = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+        if constexpr (CH == 2) psum += (pr[4] + pr[5]) + (pr[6] + pr[7]);
+        l_run = l_run * corr + psum;
         m_run = m_new;
         if (!__all_sync(0xffffffffu, corr * f_de == 1.f)) {
           // this lane's accumulator columns are head-rows 2t and 2t + 1, whose factors the
@@ -497,14 +505,14 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         for (int gr = 0; gr < NG; ++gr) {
           bacc[gr] *= corr;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) bacc[gr] = fmaf(pr[i], vb[i][gr], bacc[gr]);
+          for (int i = 0; i < 4 * CH; ++i) bacc[gr] = fmaf(pr[i], vb[i][gr], bacc[gr]);
         }
         // B operands of P^T per chunk and group: (k, column g) = head-row g at positions 2t..
         // (pa[c][gr], block 0) and 2t + 8.. (pa[c][2 + gr], block 1); hi rows the f16 value of
         // p scale_V 2^e, lo rows its remainder
-        uint32_t pa[2][4];
+        uint32_t pa[CH][4];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < CH; ++c) {
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
 #pragma unroll
@@ -532,7 +540,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attention_q8(AttnParams p) {
         {
           const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < CH; ++c) {
             // matrices (pos 0-7, piece), (8-15, piece), (0-7, piece + 1), (8-15, piece + 1) of chunk c
             const int row = wrow + 16 * c + (mi & 1) * 8 + rr;
 #pragma unroll
