@@ -271,30 +271,39 @@ def run_ours(args, rank: int, world: int) -> dict | None:
                 "params": "temperature 0.8, top_k 50, top_p 0.9", "logit_bytes": B * V * 4,
                 "logit_gbs": round(B * V * 4 / (samp_us * 1e-6) / 1e9, 1)}
 
-    # optional: the multi-token verify step (tokens_per_seq T) on the same weights and
-    # cache, one graph replay per verify, same tokens and positions every time
+    # optional: a multi-token step (tokens_per_seq T: a verify step, or a prefill chunk
+    # of T prompt tokens per sequence) on the same weights and cache, one graph replay per
+    # step, same tokens and positions every time (the K/V slots are rewritten with the
+    # same values); its logits are not written (a prefill keeps only the cache)
+    def multi_token(T: int, n: int) -> float:
+        vdec = Decoder(wl, model, tokens_per_seq=T)
+        vt = torch.randint(0, V, (B * T,), dtype=torch.int32, device=dev)
+        va = torch.empty((B * T,), dtype=torch.int32, device=dev)
+        vpos = torch.zeros_like(positions) if T > 8 else positions.clone()
+        for _ in range(3):
+            vdec.step(vt, vpos, kv, None, va, stream)
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for _ in range(n):
+            vdec.step(vt, vpos, kv, None, va, stream)
+        v1.record(stream)
+        torch.cuda.synchronize(dev)
+        vdec.close()
+        return v0.elapsed_time(v1) / n
+
     verify = None
     if args.verify > 1:
         T = args.verify
-        vdec = Decoder(wl, model, tokens_per_seq=T)
-        vt = torch.randint(0, V, (B * T,), dtype=torch.int32, device=dev)
-        vl = torch.empty((B * T, V), dtype=torch.float32, device=dev)
-        va = torch.empty((B * T,), dtype=torch.int32, device=dev)
-        vpos = positions.clone()
-        for _ in range(3):
-            vdec.step(vt, vpos, kv, vl, va, stream)
-        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        nv = 20
-        v0.record(stream)
-        for _ in range(nv):
-            vdec.step(vt, vpos, kv, vl, va, stream)
-        v1.record(stream)
-        torch.cuda.synchronize(dev)
-        vms = v0.elapsed_time(v1) / nv
-        vdec.close()
+        vms = multi_token(T, 20)
         verify = {"tokens_per_seq": T, "rows": B * T, "ms_per_verify": round(vms, 4),
                   "one_token_ms": round(ms / args.steps, 4), "verify_over_one": round(vms / (ms / args.steps), 3),
                   "tokens_checked_per_s": round(B * T / (vms / 1e3), 1)}
+    prefill = None
+    if args.prefill > 1:
+        T = args.prefill
+        pms = multi_token(T, 5)
+        prefill = {"tokens_per_seq": T, "rows": B * T, "positions": "0 .. T-1 of every sequence",
+                   "ms_per_chunk": round(pms, 3), "prompt_tok_per_s": round(B * T / (pms / 1e3), 1)}
 
     per_step = [1, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, 1]  # launches per class
     bytes_step = sum(n * dec.kernel_bytes(c, mean_p) for c, n in enumerate(per_step))
@@ -303,7 +312,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     dec.close()
     return {"ms": ms, "mean_p": mean_p, "bytes_step": bytes_step, "cls_ms": cls_ms, "cls_n": cls_n,
             "cls_bytes": cls_bytes, "e2e_s": e2e_s, "launches": launches, "wl": wl0, "B": B,
-            "clocks": clk.summary(), "sampling": sampling, "verify": verify}
+            "clocks": clk.summary(), "sampling": sampling, "verify": verify, "prefill": prefill}
 
 
 def cpu_oracle_sample(config: str, warmup: int, steps: int, budget_s: float) -> dict:
@@ -386,6 +395,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--verify", type=int, default=0,
                     help="also time the multi-token verify step with this many tokens per sequence (2..8)")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="also time one prefill chunk of T prompt tokens per sequence (tokens_per_seq = T)")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="reference arm: stop the timed oracle steps after this many seconds")
     args = ap.parse_args()
@@ -467,6 +478,8 @@ def main():
     line["sampling"] = r["sampling"]
     if r["verify"]:
         line["verify"] = r["verify"]
+    if r["prefill"]:
+        line["prefill"] = r["prefill"]
     e2e_tok_s = B * args.e2e_steps / r["e2e_s"]
     line["e2e"] = {"value": round(e2e_tok_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 8 * B,
                    "d2h_bytes_per_step": 4 * B}

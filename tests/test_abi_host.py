@@ -89,9 +89,9 @@ def test_kv_quantize_rejects_bad_arguments(dec):
     (dict(rms_eps=0.0), 1, "rms_eps"),
     (dict(linear_fmt=7), 1, "linear_fmt"),
     (dict(vocab=0), 1, "positive"),
-    (dict(tokens_per_seq=9), 2, "tokens_per_seq"),
+    (dict(tokens_per_seq=4097), 2, "tokens_per_seq"),
     (dict(tokens_per_seq=-1), 1, "tokens_per_seq"),
-    (dict(batch=5, tokens_per_seq=4), 2, "rows"),
+    (dict(batch=20, tokens_per_seq=4096), 2, "rows"),
     (dict(kv_fmt=3), 1, "kv_fmt"),
     (dict(kv_fmt=1, max_ctx=150), 2, "multiple of 16"),
 ])

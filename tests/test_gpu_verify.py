@@ -109,8 +109,11 @@ def test_verify_rows_agree_with_one_token_steps(glue):
 
 def test_verify_rejects_too_many_rows(glue):
     from token_decode_step_gb300 import dec as D
-    wl = synthetic.custom(name="v_big", batch=3, steps=8)
-    model = synthetic.generate(wl, device="cuda")  # 3 x 8 = 24 bf16 rows > 16
+    wl = synthetic.custom(name="v_big", batch=17, steps=8)
+    model = synthetic.generate(wl, device="cuda", with_kv=False)  # 17 x 4000 rows > 65535
     with pytest.raises(D.DecError) as ei:
-        glue.Decoder(wl, model, tokens_per_seq=8)
+        glue.Decoder(wl, model, tokens_per_seq=4000)
     assert "rows" in str(ei.value)
+    with pytest.raises(D.DecError) as ei:
+        glue.Decoder(wl, model, tokens_per_seq=4097)
+    assert "tokens_per_seq" in str(ei.value)

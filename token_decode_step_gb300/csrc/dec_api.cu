@@ -89,6 +89,7 @@ struct dec_handle {
   int wfmt = 0;
   int tps = 1;   // tokens per sequence (1: decode; 2..8: verify)
   int rows = 1;  // batch * tps: rows of every projection
+  int tblocks = 1;  // batched path: token blocks per projection launch
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
@@ -201,10 +202,10 @@ dec_status validate(const dec_config* c) {
     set_err("tokens_per_seq must be 0..%d (got %d)", kMaxTokensPerSeq, c->tokens_per_seq);
     return c->tokens_per_seq < 0 ? DEC_ERR_INVALID_ARG : DEC_ERR_UNSUPPORTED;
   }
-  const int rows = c->batch * (c->tokens_per_seq > 1 ? c->tokens_per_seq : 1);
-  if (rows > 1 && gemm_tc_ny(c->linear_fmt == DEC_W_BF16 ? kWBf16 : kWQ4, rows) == 0) {
-    set_err("batch %d x tokens_per_seq: %d rows, the batched path takes at most %d for this weight format",
-            c->batch, rows, c->linear_fmt == DEC_W_BF16 ? 16 : 32);
+  const long long rows = static_cast<long long>(c->batch) * (c->tokens_per_seq > 1 ? c->tokens_per_seq : 1);
+  if (rows > kMaxRows) {
+    set_err("batch %d x tokens_per_seq %d = %lld rows, at most %d per step", c->batch, c->tokens_per_seq, rows,
+            kMaxRows);
     return DEC_ERR_UNSUPPORTED;
   }
   if (static_cast<long long>(c->max_ctx) * c->n_kv_heads * c->batch * c->head_dim > (1ll << 40)) {
@@ -247,14 +248,15 @@ int choose_splits(int N, int K, int fmt, int num_sms) {
 // covers the SMs once (bf16) or twice (4-bit, whose CTAs are issue-bound), keeping at
 // least 512 (bf16) or 1024 (4-bit) inputs per split: finer splits measured slower, the
 // partial-sum round trip (fence, ticket, reload) outweighing the extra CTAs.
-void choose_tc_splits(PackedLinear& L, int wfmt, int ny, int num_sms) {
+void choose_tc_splits(PackedLinear& L, int wfmt, int ny, int num_sms, int tblocks) {
   const int rpb = gemm_tc_rows_per_block(wfmt, ny);
   const int blocks = (L.Npad + rpb - 1) / rpb;
   const int kc_max = gemm_tc_chunk(ny);
   const long long cover = wfmt == kWQ4 ? 2ll * num_sms : num_sms;
   const int min_ks = wfmt == kWQ4 ? 1024 : 512;
   int S = 1;
-  while (static_cast<long long>(blocks) * S < cover) {
+  // several token blocks already multiply the CTAs (and share one split-K counter set): no split
+  while (tblocks == 1 && static_cast<long long>(blocks) * S < cover) {
     const int S2 = S * 2;
     if (L.K % S2 != 0 || (L.K / S2) % kGroup != 0 || L.K / S2 < min_ks) break;
     S = S2;
@@ -384,6 +386,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       tp.KS = L.K / L.S;
       tp.KC = L.KC;
       tp.B = h->rows;
+      tp.tblocks = h->tblocks;
       tp.xhl = xin;
       tp.xhl_out = xout;
       tp.next_norm_w = next_norm;
@@ -587,7 +590,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
   const bool tc = h->rows > 1;
-  const int ny = tc ? gemm_tc_ny(h->wfmt, h->rows) : 0;
+  // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
+  const int blk_tok = gemm_tc_block_tokens(h->wfmt);
+  h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
+  const int ny = tc ? gemm_tc_ny(h->wfmt, h->rows > blk_tok ? blk_tok : h->rows) : 0;
   auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
@@ -612,7 +618,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     L.K = K;
     if (tc) {
       L.Npad = (N + 15) / 16 * 16;
-      choose_tc_splits(L, h->wfmt, ny, h->num_sms);
+      choose_tc_splits(L, h->wfmt, ny, h->num_sms, h->tblocks);
       L.w_bytes = linear_bytes_tc(fmt, N, K);
       L.w = take(L.w_bytes);
       return L;
@@ -729,7 +735,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const size_t o_xo = plan(static_cast<size_t>(2) * B * nq * d * 2);
   const size_t o_xg = plan(static_cast<size_t>(2) * B * I * 2);
   const size_t o_gp = plan((max_partials ? max_partials : 1) * 4);
-  const size_t o_gc = plan(static_cast<size_t>(max_tiles + 1) * 4);
+  const size_t o_gc = plan((static_cast<size_t>(max_tiles) * h->tblocks + 1) * 4);
   const size_t o_rope = plan(static_cast<size_t>(B) * (d / 2) * 8);
   const size_t o_inv = plan(static_cast<size_t>(d / 2) * 8);
   const size_t o_key = plan(static_cast<size_t>(B) * 8);
@@ -764,6 +770,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if (tc) {
     GemmParams gp{};
     gp.B = h->rows;
+    gp.tblocks = h->tblocks;
     gp.KC = gemm_tc_chunk(ny);
     const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
     for (auto& cb : combos)

@@ -16,7 +16,8 @@ constexpr int kResGroup = 8;        // rows per partial sum-of-squares of the re
 constexpr int kGemvRows = 8;        // rows per CTA of the batch-1 GEMV
 constexpr int kAttnTile = 64;       // positions per attention smem tile
 constexpr int kAttnThreads = 128;   // 4 warps, 16 positions each per tile
-constexpr int kMaxTokensPerSeq = 8; // verify step: new tokens per sequence
+constexpr int kMaxTokensPerSeq = 4096;  // verify step / prefill chunk: new tokens per sequence
+constexpr int kMaxRows = 65535;         // tokens per step (batch x tokens per sequence): a grid dimension
 constexpr int kGroup = 64;          // affine 4-bit group size
 constexpr int kGemmPrefetch = 4;    // 64-input weight units in flight per lane (batched path)
 
@@ -68,6 +69,7 @@ struct GemmParams {
   const void* w;            // packed tiles (see k_gemm_tc.cu)
   int N, Npad, K, S, KS, KC, B;  // rows, rows padded to 16, inputs, K splits, inputs per split,
                                  // inputs staged at once (divides KS), tokens
+  int tblocks;              // token blocks of gemm_tc_block_tokens() tokens (1: all B tokens at once; > 1: S = 1)
   const __nv_bfloat16* xhl; // input as bf16 hi, lo planes [2][B][K] (norm inputs already times the norm weight)
   const float* sumsq_in;    // norm inputs: [B][n_sumsq_in] partial sums of squares of the residual
   int n_sumsq_in;
@@ -269,6 +271,7 @@ cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_d
 cudaError_t launch_kv_append(const LaunchCtx& c, const AttnParams& p, int head_dim);
 // batched tensor-core projection
 int gemm_tc_ny(int wfmt, int batch);            // 8-token n-tiles per hi/lo half, 0 if unsupported
+int gemm_tc_block_tokens(int wfmt);             // most tokens one CTA takes (more: token blocks)
 int gemm_tc_rows_per_block(int wfmt, int ny);   // weight rows one CTA covers
 size_t gemm_tc_smem_bytes(int wfmt, int ny, int kc);
 int gemm_tc_chunk(int ny);                      // inputs staged per chunk

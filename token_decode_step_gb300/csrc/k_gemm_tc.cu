@@ -66,7 +66,12 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
   uint16_t* xs0 = reinterpret_cast<uint16_t*>(smem);
   float* xsum0 = reinterpret_cast<float*>(smem + 2 * buf_elems * 2);  // two [KC/64][NY*8] buffers
 
-  const int rb = blockIdx.x, split = blockIdx.y;
+  // x = row block * tblocks + token block (token blocks vary fastest, so that the CTAs
+  // streaming one weight tile for the different token blocks run together and all but
+  // the first read it from L2); y = K split (a single split when tblocks > 1)
+  const int tb = blockIdx.x % p.tblocks, rb = blockIdx.x / p.tblocks, split = blockIdx.y;
+  const int tok0 = tb * NY * 8;                                  // this block's first token
+  const int nb = p.B - tok0 < NY * 8 ? p.B - tok0 : NY * 8;      // and its number of tokens
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
   const int kbeg0 = split * p.KS;
   const int n_rt = p.Npad / 16;
@@ -132,8 +137,9 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int row = 16 * (rt0 + i) + g + 8 * (e >> 1), tok = 8 * n + 2 * t + (e & 1);
-          h_pre[i][n][e] = (valid[i] && row < p.N && tok < p.B) ? __ldcg(p.out + static_cast<size_t>(tok) * p.N + row)
-                                                                   : 0.f;
+          h_pre[i][n][e] = (valid[i] && row < p.N && tok < nb)
+                               ? __ldcg(p.out + static_cast<size_t>(tok0 + tok) * p.N + row)
+                               : 0.f;
         }
     }
   }
@@ -142,9 +148,9 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
   tl_mark(p.tl, 1);
 
   if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (fused RMSNorm)
-    for (int b = warp; b < p.B; b += WARPS) {
+    for (int b = warp; b < nb; b += WARPS) {
       float s = 0.f;
-      for (int i = lane; i < p.n_sumsq_in; i += 32) s += p.sumsq_in[static_cast<size_t>(b) * p.n_sumsq_in + i];
+      for (int i = lane; i < p.n_sumsq_in; i += 32) s += p.sumsq_in[static_cast<size_t>(tok0 + b) * p.n_sumsq_in + i];
       s = warp_sum(s);
       if (lane == 0) s_inv[b] = rsqrtf(s / static_cast<float>(p.K) + p.eps);
     }
@@ -156,10 +162,10 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
     const uint32_t dst0 = smem_u32(xs0 + (c & 1) * buf_elems);
     const int per_row = KC / 8;  // 16-byte pieces
     const int kb = kbeg0 + c * KC;
-    for (int idx = tid; idx < 2 * p.B * per_row; idx += NTH) {
+    for (int idx = tid; idx < 2 * nb * per_row; idx += NTH) {
       const int r = idx / per_row, j = idx % per_row;
-      const int plane = r / p.B, b = r % p.B;
-      const __nv_bfloat16* src = p.xhl + (static_cast<size_t>(plane) * p.B + b) * p.K + kb + 8 * j;
+      const int plane = r / nb, b = r % nb;
+      const __nv_bfloat16* src = p.xhl + (static_cast<size_t>(plane) * p.B + tok0 + b) * p.K + kb + 8 * j;
       const int srow = plane * NY * 8 + b;
       cp_async16(dst0 + (srow * KSP + 8 * j) * 2, src, 16);
     }
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = 8 * n + 2 * t + (e & 1);
-        const float r = tok < p.B ? s_inv[tok] : 0.f;
+        const float r = tok < nb ? s_inv[tok] : 0.f;
 #pragma unroll
         for (int i = 0; i < TPW; ++i) y[i][n][e] *= r;
       }
@@ -367,18 +373,19 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int row = 16 * rt + g + 8 * (e >> 1);
-        const int tok = 8 * n + 2 * t + (e & 1);
+        const int tok = 8 * n + 2 * t + (e & 1);   // within the block
+        const size_t gtok = static_cast<size_t>(tok0 + tok);
         if constexpr (EPI == kEpiStore) {
-          if (row < p.N && tok < p.B) p.out[static_cast<size_t>(tok) * p.N + row] = y[i][n][e];
+          if (row < p.N && tok < nb) p.out[gtok * p.N + row] = y[i][n][e];
         } else if constexpr (EPI == kEpiResid) {
           float hn = 0.f;
-          if (tok < p.B) {
+          if (tok < nb) {
             hn = h_pre[i][n][e] + y[i][n][e];
-            p.out[static_cast<size_t>(tok) * p.N + row] = hn;
+            p.out[gtok * p.N + row] = hn;
             // the next consumer's input: h times its norm weight, as hi + lo planes
             __nv_bfloat16 hi, lo;
             split_hl(hn * nw_pre[i][e >> 1], hi, lo);
-            const size_t o = static_cast<size_t>(tok) * p.N + row;
+            const size_t o = gtok * p.N + row;
             p.xhl_out[o] = hi;
             p.xhl_out[plane_out + o] = lo;
           }
@@ -386,12 +393,12 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
           ss += __shfl_xor_sync(0xffffffffu, ss, 4);
           ss += __shfl_xor_sync(0xffffffffu, ss, 8);
           ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-          if (g == 0 && tok < p.B) p.sumsq_out[static_cast<size_t>(tok) * (p.N / kResGroup) + 2 * rt + (e >> 1)] = ss;
+          if (g == 0 && tok < nb) p.sumsq_out[gtok * (p.N / kResGroup) + 2 * rt + (e >> 1)] = ss;
         } else if constexpr (EPI == kEpiSwiglu) {
           // rows 0..7 of a tile are gate rows, rows 8..15 the matching up rows
-          if (e < 2 && tok < p.B) {
+          if (e < 2 && tok < nb) {
             const float gv = silu_f(y[i][n][e]) * y[i][n][e + 2];
-            const size_t o = static_cast<size_t>(tok) * (p.N / 2) + 8 * rt + g;
+            const size_t o = gtok * (p.N / 2) + 8 * rt + g;
             p.out[o] = gv;
             __nv_bfloat16 hi, lo;
             split_hl(gv, hi, lo);
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
             p.xhl_out[plane_out + o] = lo;
           }
         } else {  // lm_head
-          if (row < p.N && tok < p.B && p.out) p.out[static_cast<size_t>(tok) * p.N + row] = y[i][n][e];
+          if (row < p.N && tok < nb && p.out) p.out[gtok * p.N + row] = y[i][n][e];
         }
       }
       if constexpr (EPI == kEpiLmHead) {
@@ -415,7 +422,7 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
             k = other > k ? other : k;
           }
           const int tok = 8 * n + 2 * t + c;
-          if (g == 0 && tok < p.B) atomicMax(p.amax_key + tok, k);
+          if (g == 0 && tok < nb) atomicMax(p.amax_key + tok0 + tok, k);
         }
       }
     }
@@ -424,14 +431,13 @@ __global__ void __launch_bounds__(WARPS * 32, WARPS == 8 ? 2 : 1) k_gemm_tc(Gemm
   if constexpr (EPI == kEpiLmHead) {
     __threadfence();
     __syncthreads();
-    if (tid == 0) {
-      const unsigned nblk = gridDim.x;
-      const unsigned done = atomicAdd(&p.counters[nblk], 1u);
-      if (done == nblk - 1) {
-        __threadfence();
-        for (int b = 0; b < p.B; ++b) p.argmax_out[b] = argmax_key_index(atomicOr(p.amax_key + b, 0ull));
-        p.counters[nblk] = 0u;
-      }
+    const unsigned nblk = gridDim.x;
+    if (tid == 0) s_ticket = atomicAdd(&p.counters[nblk], 1u);
+    __syncthreads();
+    if (s_ticket == nblk - 1) {  // the last CTA publishes every token's argmax
+      __threadfence();
+      for (int b = tid; b < p.B; b += NTH) p.argmax_out[b] = argmax_key_index(atomicOr(p.amax_key + b, 0ull));
+      if (tid == 0) p.counters[nblk] = 0u;
     }
   }
 }
@@ -446,7 +452,7 @@ cudaError_t launch_t(const LaunchCtx& c, const GemmParams& p, bool prepare) {
   const int n_rt = p.Npad / 16;
   const int per_blk = WARPS * TPW;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((n_rt + per_blk - 1) / per_blk, p.S);
+  cfg.gridDim = dim3((n_rt + per_blk - 1) / per_blk * p.tblocks, p.S);
   cfg.blockDim = dim3(WARPS * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = c.stream;
@@ -471,7 +477,8 @@ cudaError_t dispatch_epi(const LaunchCtx& c, const GemmParams& p, int in_mode, i
 // of two tiles up to 16 tokens, 16 warps of one tile for 17..32 tokens (256 rows
 // share each staged chunk of activations).
 cudaError_t dispatch(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi, bool prepare) {
-  const int ny = gemm_tc_ny(wfmt, p.B);
+  if (p.tblocks < 1) return cudaErrorInvalidValue;
+  const int ny = gemm_tc_ny(wfmt, p.tblocks > 1 ? gemm_tc_block_tokens(wfmt) : p.B);
   if (wfmt == kWBf16) {
     if (ny == 1) return dispatch_epi<kWBf16, 1, 1, 8>(c, p, in_mode, epi, prepare);
     if (ny == 2) return dispatch_epi<kWBf16, 2, 1, 8>(c, p, in_mode, epi, prepare);
@@ -492,6 +499,8 @@ int gemm_tc_ny(int wfmt, int batch) {
 }
 
 int gemm_tc_rows_per_block(int wfmt, int) { return wfmt == kWQ4 ? 256 : 128; }
+
+int gemm_tc_block_tokens(int wfmt) { return wfmt == kWQ4 ? 32 : 16; }
 
 int gemm_tc_chunk(int ny) { return ny == 1 ? 1024 : 512; }
 
