@@ -19,7 +19,8 @@ import torch
 import oracle
 import synthetic
 from oracle import numerics
-from parity import ATTN_ATOL, ATTN_RTOL, check_logits, gpu_greedy, np_model, oracle_replay
+from parity import (ATTN_ATOL, ATTN_RTOL, check_logits, check_logits_conditioned, gpu_greedy, np_model,
+                    oracle_noise_spread, oracle_replay)
 
 pytestmark = pytest.mark.gpu
 
@@ -213,10 +214,12 @@ def _run_kv8(glue, wl, steps, check_steps=None, graph=True, cache_weights=True, 
     finally:
         dec.close()
     res, ref_cache = oracle_replay(wl, host, init, gpu_steps, check_steps, cache_weights=cache_weights)
-    worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0}
+    worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0, "ill_conditioned": 0}
     for s, lg, am in res:
-        w = check_logits(gpu_steps[s][2], lg, gpu_steps[s][3], am, f"{wl.name} step {s}")
-        worst = {k: max(worst[k], w[k]) if k != "exempt" else worst[k] + w[k] for k in worst}
+        w = check_logits_conditioned(gpu_steps[s][2], lg, gpu_steps[s][3], am, f"{wl.name} step {s}",
+                                     lambda b, s=s: oracle_noise_spread(wl, host, init, gpu_steps, s, b))
+        worst = {k: max(worst[k], w[k]) if k in ("max_abs", "rel_l2") else worst[k] + w[k] for k in worst}
+    assert worst["ill_conditioned"] <= max(1, wl.batch // 8), f"{worst['ill_conditioned']} ill-conditioned sequences"
     if check_steps is None:
         L, B, nkv, d = wl.n_layers, wl.batch, wl.n_kv_heads, wl.head_dim
         if full_kv_check:

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import synthetic
-from parity import check_logits, gpu_greedy, kv_appended_close, np_model, oracle_replay
+from parity import (check_logits, check_logits_conditioned, gpu_greedy, kv_appended_close, np_model,
+                    oracle_noise_spread, oracle_replay)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,10 +35,12 @@ def _run(glue, wl, steps, check_steps=None, graph=True, full_kv_check=True, cach
     finally:
         dec.close()
     res, kv_ref = oracle_replay(wl, host, kv_init, gpu_steps, check_steps, cache_weights=cache_weights)
-    worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0}
+    worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0, "ill_conditioned": 0}
     for s, lg, am in res:
-        w = check_logits(gpu_steps[s][2], lg, gpu_steps[s][3], am, f"{wl.name} step {s}")
-        worst = {k: max(worst[k], w[k]) if k != "exempt" else worst[k] + w[k] for k in worst}
+        w = check_logits_conditioned(gpu_steps[s][2], lg, gpu_steps[s][3], am, f"{wl.name} step {s}",
+                                     lambda b, s=s: oracle_noise_spread(wl, host, kv_init, gpu_steps, s, b))
+        worst = {k: max(worst[k], w[k]) if k in ("max_abs", "rel_l2") else worst[k] + w[k] for k in worst}
+    assert worst["ill_conditioned"] <= max(1, wl.batch // 8), f"{worst['ill_conditioned']} ill-conditioned sequences"
     if check_steps is None:
         if full_kv_check:
             kv_gpu = np_model({"kv": kv.cpu()})["kv"]

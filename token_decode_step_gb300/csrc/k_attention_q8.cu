@@ -13,8 +13,12 @@
 // distributed shared memory); what differs is how a stage becomes tensor-core operands:
 //  * Codes enter mma.sync m16n8k16 as the f16 values 1024 + c: one byte_perm writes two
 //    code bytes under the high byte 0x64 (an f16 of exponent 10, whose low mantissa bits
-//    count by one).  The offset folds into the bias: scale (1024 + c) + (bias - 1024 scale)
-//    = scale c + bias.
+//    count by one).  For K the offset folds into the bias: scale (1024 + c) + (bias - 1024
+//    scale) = scale c + bias (each product sums 64 dimensions and starts from zero every
+//    stage).  V's codes are centred first, c - 128 (one exact f16 subtraction for two), with
+//    bias + 128 scale: its products accumulate over every position of the run, and an
+//    accumulator carrying 1024 times the weights' sum lost precision in proportion to the
+//    run length (a systematic 1e-5 at 6000 positions before, measured).
 //  * K: ldmatrix over the position-major code rows (a 16-byte piece = 16 codes of one
 //    position); each thread receives four consecutive codes of a position, which become
 //    its two f16x2 B registers.  The query's dimensions are permuted within each 16 to
@@ -92,6 +96,13 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// two f16 1024 + c (from byte_perm) -> c - 128, exact: the V products accumulate centred codes, so
+// that the running sums stay near the signal instead of carrying 1024 times the weights' sum
+__device__ __forceinline__ uint32_t centre_codes(uint32_t x) {
+  __half2 v = *reinterpret_cast<__half2*>(&x);
+  return h2_bits(__hsub2(v, __float2half2_rn(1152.f)));
+}
 
 // 2^e for an integer e in [-126, 127], exact
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
@@ -397,7 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, Q8Cfg<D, DEEP>::kMinBlocks) k_at
             const uint32_t pk = pkk[q], pv = pvv[q];
             const float sk = __uint_as_float(pk << 16), bk = __uint_as_float(pk & 0xffff0000u);
             const float sv = __uint_as_float(pv << 16), bv = __uint_as_float(pv & 0xffff0000u);
-            wp[q] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(-1024.f, sv, bv));
+            wp[q] = make_float4(sk, fmaf(-1024.f, sk, bk), sv, fmaf(128.f, sv, bv));
             sv_max = fmaxf(sv_max, fabsf(sv));
           }
         }
@@ -551,9 +562,10 @@ __global__ void __launch_bounds__(kAttnThreads, Q8Cfg<D, DEEP>::kMinBlocks) k_at
               for (int u = 0; u < 2; ++u) {
                 const uint32_t lo8 = r4[2 * u], hi8 = r4[2 * u + 1];
                 const int sj = jj + u, gr = (NG == 2 && sj >= D / 32) ? 1 : 0;
-                mma_f16_16816(o[sj], __byte_perm(lo8, 0x64646464u, 0x4240), __byte_perm(lo8, 0x64646464u, 0x4341),
-                              __byte_perm(hi8, 0x64646464u, 0x4240), __byte_perm(hi8, 0x64646464u, 0x4341),
-                              pa[c][gr], pa[c][2 + gr]);
+                mma_f16_16816(o[sj], centre_codes(__byte_perm(lo8, 0x64646464u, 0x4240)),
+                              centre_codes(__byte_perm(lo8, 0x64646464u, 0x4341)),
+                              centre_codes(__byte_perm(hi8, 0x64646464u, 0x4240)),
+                              centre_codes(__byte_perm(hi8, 0x64646464u, 0x4341)), pa[c][gr], pa[c][2 + gr]);
               }
             }
           }
