@@ -9,7 +9,8 @@
  *     xn = RMSNorm(h) * in_norm                        (fused into the QKV GEMV)
  *     q, k, v = Wq xn, Wk xn, Wv xn                    (one fused GEMV)
  *     q, k = per-head RMSNorm (q_norm / k_norm), then rotate-half RoPE at P
- *     cache[P] = bf16(k), bf16(v); o = softmax(q K^T / sqrt(d)) V over 0..P
+ *     cache[P] = bf16(k), bf16(v) (or their affine 8-bit form);
+ *     o = softmax(q K^T / sqrt(d)) V over 0..P
  *                                                      (one fused attention kernel,
  *                                                       split over the positions,
  *                                                       log-sum-exp merge)
@@ -85,10 +86,10 @@ typedef enum {
 
 /* Model and run shape.  Supported (else DEC_ERR_UNSUPPORTED): head_dim in {64, 128};
    n_q_heads / n_kv_heads in {1, 2, 4}; hidden and intermediate multiples of 64;
-   vocab >= 1; rows = batch * tokens_per_seq at most 16 for bf16 weights and 32 for
-   affine 4-bit (one row runs CUDA-core GEMV kernels, more rows tensor-core kernels);
-   tokens_per_seq 0..8 (0 means 1); max_ctx >= 1, and a multiple of 16 for the affine
-   8-bit cache.  Required (else DEC_ERR_INVALID_ARG): every size positive, rms_eps > 0,
+   vocab >= 1; rows = batch * tokens_per_seq at most 65535 (one row runs CUDA-core GEMV
+   kernels, more rows tensor-core kernels, in blocks of 16 rows for bf16 weights and 32
+   for affine 4-bit); tokens_per_seq 0..4096 (0 means 1); max_ctx >= 1, and a multiple
+   of 16 for the affine 8-bit cache.  Required (else DEC_ERR_INVALID_ARG): every size positive, rms_eps > 0,
    rope_theta > 1, n_q_heads a multiple of n_kv_heads, kv_fmt a dec_kvfmt.
 
    tokens_per_seq T > 1 makes dec_step a multi-token verify step (speculative decoding's
@@ -97,13 +98,17 @@ typedef enum {
    positions[b] + t of sequence b, attends causally to that sequence's slots 0 ..
    positions[b] + t, and its K/V are written at that slot; logits_out and argmax_out
    hold one row per (b, t).  The result of row (b, t) is that of a one-token step of
-   sequence b at position positions[b] + t after the rows (b, 0..t-1). */
+   sequence b at position positions[b] + t after the rows (b, 0..t-1).  The same step with
+   T prompt tokens per sequence is a chunked prefill (the step before decode): it fills
+   slots positions[b] .. positions[b] + T - 1 with the prompt's K/V in one forward, and the
+   last row of each sequence gives the first generated token; logits_out may be NULL. */
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
     float rms_eps, rope_theta;
     int linear_fmt;            /* dec_wfmt, applies to every linear including lm_head */
     int batch, max_ctx;        /* sequences per step; cache slots per sequence */
-    int tokens_per_seq;        /* new tokens per sequence and step: 1 (decode) .. 8 (verify); 0 = 1 */
+    int tokens_per_seq;        /* new tokens per sequence and step: 1 (decode), 2..8 (verify), up to
+                                  4096 (a prefill chunk); 0 = 1 */
     int kv_fmt;                /* dec_kvfmt of the KV cache (0 = bf16) */
 } dec_config;
 
@@ -176,6 +181,16 @@ DEC_API void dec_destroy(dec_handle *h);
        [n_layers][2][batch][n_kv_heads][max_ctx][head_dim/64][2]: element i of a row reads
        scale[i/64] * code[i] + bias[i/64]. */
 DEC_API size_t dec_kv_cache_bytes(const dec_config *cfg);
+
+/* Test hook: the tensor-core projection kernel of long prefill chunks (tcgen05.mma with TMA
+   operands, the accumulator in tensor memory) on caller buffers, plain store epilogue:
+   out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) * w[n][k] in fp32.
+     x_hl  device bf16 [2][M][K] (plane 0 hi, plane 1 lo), 16-byte aligned
+     w     device bf16 [N][K] row-major, 16-byte aligned
+     out   device float [M][N]
+   K a positive multiple of 64, M and N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
+DEC_API dec_status dec_debug_gemm_tc5(const void *x_hl, int M, const void *w, int N, int K, float *out,
+                                      dec_stream_t stream);
 
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:

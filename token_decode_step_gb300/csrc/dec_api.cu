@@ -52,7 +52,8 @@ void set_last_error(const char* fmt, ...) {
 namespace {
 
 struct PackedLinear {
-  void* w = nullptr;       // batch 1: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
+  alignas(64) unsigned char tmap[128] = {};  // tcgen05 path: TMA tensor map of w (bf16 [N][K])
+  void* w = nullptr;       // batch 1 and tcgen05 path: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
   uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
   int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
@@ -90,6 +91,11 @@ struct dec_handle {
   int tps = 1;   // tokens per sequence (1: decode; 2..8: verify)
   int rows = 1;  // batch * tps: rows of every projection
   int tblocks = 1;  // batched path: token blocks per projection launch
+  // tcgen05 path (bf16 weights, at least a 128-token tile of rows): row-major weights and
+  // TMA tensor maps of the three activation hi/lo planes (inputs of QKV / gate_up / lm_head,
+  // of O, of down)
+  bool umma = false;
+  alignas(64) unsigned char map_u[128] = {}, map_o[128] = {}, map_g[128] = {};
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
@@ -374,7 +380,26 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     note(cls);
     ev_begin();
     dec_status s2;
-    if (h->rows == 1) {
+    if (h->umma) {
+      UmmaParams up{};
+      up.M = h->rows;
+      up.N = L.N;
+      up.K = L.K;
+      up.m_tiles = (h->rows + umma_tokens_per_tile() - 1) / umma_tokens_per_tile();
+      up.sumsq_in = h->sumsq;
+      up.n_sumsq_in = H / kResGroup;
+      up.eps = c.rms_eps;
+      up.out = out;
+      up.sumsq_out = h->sumsq;
+      up.xhl_out = xout;
+      up.next_norm_w = next_norm;
+      up.amax_key = h->amax_key;
+      up.argmax_out = sp.argmax;
+      up.counters = h->gemv_counters;
+      up.status = h->status;
+      const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
+      s2 = check(launch_gemm_umma(lc, mx, L.tmap, up, in_mode, epi), what);
+    } else if (h->rows == 1) {
       s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
       GemmParams tp{};
@@ -594,7 +619,9 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
   h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
   const int ny = tc ? gemm_tc_ny(h->wfmt, h->rows > blk_tok ? blk_tok : h->rows) : 0;
-  auto lbytes = [&](int N, int K) { return tc ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
+  h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16;
+  const bool frag = tc && !h->umma;  // fragment-packed weights for the mma.sync path
+  auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
   const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +
@@ -616,14 +643,14 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     PackedLinear L;
     L.N = N;
     L.K = K;
-    if (tc) {
+    if (frag) {
       L.Npad = (N + 15) / 16 * 16;
       choose_tc_splits(L, h->wfmt, ny, h->num_sms, h->tblocks);
       L.w_bytes = linear_bytes_tc(fmt, N, K);
       L.w = take(L.w_bytes);
       return L;
     }
-    L.S = choose_splits(N, K, fmt, h->num_sms);
+    L.S = h->umma ? 1 : choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
       L.w_bytes = static_cast<size_t>(N) * K * 2;
       L.w = take(L.w_bytes);
@@ -656,7 +683,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   auto cp = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto pack_lin = [&](const PackedLinear& P, size_t row_off, const dec_linear& a, const dec_linear* b, int rows,
                       int K, int ib) -> cudaError_t {
-    if (tc) {
+    if (frag) {
       const int npad = (rows + 15) / 16 * 16;
       if (fmt == DEC_W_BF16)
         return pack_frag_bf16(s, static_cast<uint32_t*>(P.w), static_cast<const __nv_bfloat16*>(a.w),
@@ -695,7 +722,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = pack_lin(L.qkv, static_cast<size_t>(nq + nkv) * d, lw.v, nullptr, nkv * d, H, 0)) != cudaSuccess)
       return fail("pack v", e);
     if ((e = pack_lin(L.o, 0, lw.o, nullptr, H, nq * d, 0)) != cudaSuccess) return fail("pack o", e);
-    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, tc ? 8 : kGemvRows / 2)) != cudaSuccess)
+    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, h->umma ? 16 : frag ? 8 : kGemvRows / 2)) !=
+        cudaSuccess)
       return fail("pack gate/up", e);
     if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
   }
@@ -709,7 +737,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     const int tiles = (L.N + kGemvRows - 1) / kGemvRows;  // >= row blocks of the batched path too
     max_tiles = tiles > max_tiles ? tiles : max_tiles;
     if (L.S > 1) {
-      const size_t pp = tc ? static_cast<size_t>(L.S) * (L.Npad / 16) * 32 * ny * 4 : static_cast<size_t>(L.S) * L.N * B;
+      const size_t pp = frag ? static_cast<size_t>(L.S) * (L.Npad / 16) * 32 * ny * 4 : static_cast<size_t>(L.S) * L.N * B;
       max_partials = pp > max_partials ? pp : max_partials;
     }
   };
@@ -767,7 +795,22 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail("upload inv_freq", e);
   if ((e = prepare_attention(d, G, c.kv_fmt)) != cudaSuccess) return fail("attention kernel attributes", e);
-  if (tc) {
+  if (h->umma) {  // tensor maps of every weight and of the activation planes, kernel attributes
+    auto lmap = [&](PackedLinear& L) { return umma_tensor_map(L.tmap, L.w, L.N, L.K); };
+    if ((e = lmap(h->lm_head)) != cudaSuccess) return fail("tensor map", e);
+    for (auto& L : h->layers)
+      if ((e = lmap(L.qkv)) != cudaSuccess || (e = lmap(L.o)) != cudaSuccess || (e = lmap(L.gateup)) != cudaSuccess ||
+          (e = lmap(L.down)) != cudaSuccess)
+        return fail("tensor map", e);
+    if ((e = umma_tensor_map(h->map_u, h->xh_u, 2 * h->rows, H)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_o, h->xh_o, 2 * h->rows, nq * d)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_g, h->xh_g, 2 * h->rows, I)) != cudaSuccess)
+      return fail("tensor map", e);
+    const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
+    for (auto& cb : combos)
+      if ((e = prepare_gemm_umma(cb[0], cb[1])) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
+  }
+  if (frag) {
     GemmParams gp{};
     gp.B = h->rows;
     gp.tblocks = h->tblocks;
@@ -839,6 +882,11 @@ extern "C" dec_status dec_get_device_status(dec_handle* h, int* out) {
   return DEC_OK;
 }
 
+namespace {
+// rows per gate (then up) block of the packed gate/up projection
+int gate_up_block(const dec_handle* h) { return h->umma ? 16 : h->rows > 1 ? 8 : kGemvRows / 2; }
+}  // namespace
+
 extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, float* out, dec_stream_t stream) {
   if (!h || !out || which < 0 || which > 7 || (which < 7 && (layer < 0 || layer >= h->cfg.n_layers))) {
     set_err("dec_debug_dequant: bad arguments");
@@ -860,12 +908,12 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       case 1: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = c.n_q_heads * d; break;
       case 2: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = (c.n_q_heads + c.n_kv_heads) * d; break;
       case 3: P = &L.o; rows = H; K = c.n_q_heads * d; break;
-      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = h->rows > 1 ? 8 : kGemvRows / 2; half = 0; break;
-      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = h->rows > 1 ? 8 : kGemvRows / 2; half = 1; break;
+      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h); half = 0; break;
+      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h); half = 1; break;
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  if (h->rows > 1) {
+  if (h->rows > 1 && !h->umma) {
     DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
   } else {
     DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
@@ -1030,6 +1078,27 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
   ap.out = out;
   ap.status = nullptr;
   DEC_CUDA(launch_attention(LaunchCtx{cs, false}, ap, cfg->head_dim));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_debug_gemm_tc5(const void* x_hl, int M, const void* w, int N, int K, float* out,
+                                         dec_stream_t stream) {
+  g_err[0] = 0;
+  if (!x_hl || !w || !out || M < 1 || N < 1 || K < 64 || K % 64 != 0 || !aligned16(x_hl) || !aligned16(w)) {
+    set_err("dec_debug_gemm_tc5: NULL or misaligned pointer, M or N < 1, or K not a positive multiple of 64");
+    return DEC_ERR_INVALID_ARG;
+  }
+  alignas(64) unsigned char mx[128], mw[128];
+  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K));
+  DEC_CUDA(umma_tensor_map(mw, w, N, K));
+  DEC_CUDA(prepare_gemm_umma(kInPlain, kEpiStore));
+  UmmaParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.m_tiles = (M + umma_tokens_per_tile() - 1) / umma_tokens_per_tile();
+  p.out = out;
+  DEC_CUDA(launch_gemm_umma(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mw, p, kInPlain, kEpiStore));
   return DEC_OK;
 }
 

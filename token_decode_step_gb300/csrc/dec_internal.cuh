@@ -84,6 +84,23 @@ struct GemmParams {
   int32_t* argmax_out;      // lmhead: [B]
 };
 
+// Prefill projections on tcgen05 (k_gemm_umma.cu): Y[M][N] = X[M][K] W[N][K]^T, X as bf16 hi, lo
+// planes [2][M][K] and W bf16 [N][K] row-major, both read through TMA tensor maps.
+struct UmmaParams {
+  int M, N, K, m_tiles;     // tokens, weight rows, inputs (multiple of 64), ceil(M / 128)
+  const float* sumsq_in;    // norm inputs: [M][n_sumsq_in] partial sums of squares of the residual
+  int n_sumsq_in;
+  float eps;
+  float* out;               // store / lmhead: [M][N] (lmhead: may be null); resid: h [M][N] (+=); swiglu: g [M][N/2]
+  float* sumsq_out;         // resid: [M][N / kResGroup]
+  __nv_bfloat16* xhl_out;   // resid: h * next_norm_w, swiglu: g, as hi, lo planes
+  const __nv_bfloat16* next_norm_w;  // resid: [N]
+  unsigned long long* amax_key;      // lmhead: [M]
+  int32_t* argmax_out;               // lmhead: [M]
+  unsigned* counters;                // lmhead: one counter, zero on entry, left zero
+  unsigned* status;                  // time-out flag (may be null)
+};
+
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
 struct AttnParams {
   Timeline tl;
@@ -277,6 +294,14 @@ size_t gemm_tc_smem_bytes(int wfmt, int ny, int kc);
 int gemm_tc_chunk(int ny);                      // inputs staged per chunk
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi);
 cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
+// tcgen05 projections of many tokens (k_gemm_umma.cu)
+int umma_rows_per_tile();
+int umma_tokens_per_tile();
+int umma_k_step();
+cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K);  // CUtensorMap (128 bytes)
+cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* map_w, const UmmaParams& p,
+                             int in_mode, int epi);
+cudaError_t prepare_gemm_umma(int in_mode, int epi);
 size_t attention_smem_bytes(int head_dim);
 // set the dynamic smem limits and record the shapes' occupancy (before capture)
 cudaError_t prepare_attention(int head_dim, int G, int kv_fmt);

@@ -1,0 +1,363 @@
+// Projections of many tokens at once (prefill chunks) on the fifth-generation tensor cores:
+// Y[t][n] = sum_k X[t][k] W[n][k] with tcgen05.mma, operands staged by the Tensor Memory
+// Accelerator, the accumulator in tensor memory.
+//
+// Sources: Butter architecture.md, "SINGLE-TOKEN DECODE" (the projection sequence, here run
+// over a chunk of prompt tokens); oxinfer crate page (prefill is compute-bound: a chunk of
+// tokens reads the weights once).
+//
+// Tile: 128 tokens (the accumulator's 128 lanes) x 128 weight rows (128 fp32 columns), 64
+// inputs per stage: one 128-byte row of bf16 per token and per weight row, so both operands
+// are K-major tiles in the 128-byte swizzle that the TMA writes and the MMA reads.  The
+// activations arrive as bf16 hi and lo planes (x = hi + lo, ~16 significant bits, the same
+// planes the decode path's batched kernels read); both halves are multiplied into the same
+// accumulator.  Four stages; one thread issues the TMA copies (full barriers complete on
+// their bytes), one thread issues the MMAs (each stage's commit frees it for the copies),
+// then all four warps read their 32 lanes of the accumulator for the epilogue.  Every wait
+// on a barrier is bounded: on time-out the kernel flags the status word and leaves.
+#include <cuda.h>
+
+#include "dec_internal.cuh"
+
+namespace dec {
+
+namespace {
+
+constexpr int kUM = 128;                     // tokens per tile
+constexpr int kUN = 128;                     // weight rows per tile
+constexpr int kUK = 64;                      // inputs per stage
+constexpr int kUStages = 4;
+constexpr int kUTile = 128 * kUK * 2;        // 16 KB: 128 rows of 128 bytes
+constexpr int kUStage = 3 * kUTile;          // x hi, x lo, w
+constexpr int kUSmem = 1024 + kUStages * kUStage + 256 + kUM * 4;
+constexpr uint32_t kUWaitPolls = 1u << 22;
+
+// instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 128 (N >> 3 at bit 17), M = 128 (M >> 4 at bit 24)
+constexpr uint32_t kUIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kUN >> 3) << 17) | ((kUM >> 4) << 24);
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kUWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// shared-memory descriptor of a K-major tile in the 128-byte swizzle: start address >> 4,
+// leading offset 16 B (unused for this layout), stride 1024 B between 8-row groups, the
+// descriptor version 1 at bit 46, swizzle mode 2 (128 B) at bit 61
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          tmem_d),
+      "l"(da), "l"(db), "r"(kUIdesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's accumulator lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float silu_u(float x) { return x / (1.0f + expf(-x)); }
+
+}  // namespace
+
+// grid: (token tiles x weight-row tiles), token tiles fastest (the CTAs of one weight tile
+// run together and share it through L2); 128 threads
+template <int IN, int EPI>
+__global__ void __launch_bounds__(128, 1)
+    k_gemm_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, UmmaParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t bar_full = base + kUStages * kUStage;
+  const uint32_t bar_empty = bar_full + 8 * kUStages;
+  const uint32_t bar_done = bar_empty + 8 * kUStages;
+  const uint32_t tmem_slot = bar_done + 8;
+  float* s_inv = reinterpret_cast<float*>(smem + kUStages * kUStage + 256);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = static_cast<int>(blockIdx.x) % p.m_tiles, nt = static_cast<int>(blockIdx.x) / p.m_tiles;
+
+  if (warp == 0) {  // 128 accumulator columns (one CTA per SM: never contended)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(kUN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tmem_slot - base));
+
+  griddep_wait();  // the activations are the previous kernel's output
+  if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
+    for (int j = 0; j < 32; ++j) {
+      const int tok = mt * kUM + warp * 32 + j;
+      float s = 0.f;
+      if (tok < p.M)
+        for (int i = lane; i < p.n_sumsq_in; i += 32) s += p.sumsq_in[static_cast<size_t>(tok) * p.n_sumsq_in + i];
+      s = warp_sum(s);
+      if (lane == 0) s_inv[warp * 32 + j] = rsqrtf(s / static_cast<float>(p.K) + p.eps);
+    }
+  }
+
+  const int nk = p.K / kUK;
+  bool ok = true;
+  if (tid == 0) {  // TMA producer
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kUStages;
+      if (kb >= kUStages && !mbar_wait(bar_empty + 8 * s, ((kb / kUStages) - 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = bar_full + 8 * s, st = base + s * kUStage;
+      mbar_expect_tx(full, kUStage);
+      tma_load_2d(st, &tm_x, kb * kUK, mt * kUM, full);
+      tma_load_2d(st + kUTile, &tm_x, kb * kUK, p.M + mt * kUM, full);
+      tma_load_2d(st + 2 * kUTile, &tm_w, kb * kUK, nt * kUN, full);
+    }
+  } else if (tid == 32) {  // MMA issuer
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kUStages;
+      if (!mbar_wait(bar_full + 8 * s, (kb / kUStages) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t st = base + s * kUStage;
+      const uint64_t dxh = sw128_desc(st), dxl = sw128_desc(st + kUTile), dw = sw128_desc(st + 2 * kUTile);
+#pragma unroll
+      for (int k = 0; k < kUK / 16; ++k) {  // 16 inputs = 32 bytes further along the swizzled row
+        umma_bf16(tmem, dxh + 2 * k, dw + 2 * k, (kb | k) != 0 ? 1u : 0u);
+        umma_bf16(tmem, dxl + 2 * k, dw + 2 * k, 1u);
+      }
+      umma_commit(bar_empty + 8 * s);  // the stage is free once these MMAs have read it
+    }
+    umma_commit(bar_done);
+  }
+  __syncwarp();
+  if (!mbar_wait(bar_done, 0)) ok = false;
+  tc_fence_after();
+  __syncthreads();
+
+  // ---- epilogue: this thread's token is lane 32 warp + lane of the tile
+  const int tok = mt * kUM + warp * 32 + lane;
+  const bool live = tok < p.M;
+  const float r = (IN == kInNorm) ? s_inv[warp * 32 + lane] : 1.f;
+  const uint32_t tlane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  unsigned long long best = 0ull;
+#pragma unroll 1
+  for (int c = 0; c < kUN / 32; ++c) {
+    float v[32];
+    tmem_ld32(tlane + 32 * c, v);  // (all lanes of the warp: the load is warp-collective)
+    const int n0 = nt * kUN + 32 * c;
+    // (N is a multiple of 32 for every epilogue but the lm_head's: a chunk is in or out)
+    if (!live || !ok || n0 >= p.N) continue;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= r;
+    if constexpr (EPI == kEpiStore || EPI == kEpiLmHead) {
+      if (p.out) {
+        float* dst = p.out + static_cast<size_t>(tok) * p.N + n0;
+        if (n0 + 32 <= p.N && (p.N & 3) == 0) {  // 16-byte aligned rows
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+          for (int i = 0; i < 32 && n0 + i < p.N; ++i) dst[i] = v[i];
+        }
+      }
+      if constexpr (EPI == kEpiLmHead) {
+        for (int i = 0; i < 32 && n0 + i < p.N; ++i) {
+          const unsigned long long key = argmax_key(v[i], n0 + i);
+          best = key > best ? key : best;
+        }
+      }
+    } else if constexpr (EPI == kEpiResid) {
+      // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per 8 rows
+      float* hrow = p.out + static_cast<size_t>(tok) * p.N + n0;
+      const size_t plane = static_cast<size_t>(p.M) * p.N;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // groups of 8 rows (N is a multiple of 64)
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 8 * q; i < 8 * q + 8; ++i) {
+          const float hn = hrow[i] + v[i];
+          hrow[i] = hn;
+          ss += hn * hn;
+          const float x = hn * bf16_to_f(p.next_norm_w[n0 + i]);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          const size_t o = static_cast<size_t>(tok) * p.N + n0 + i;
+          p.xhl_out[o] = hi;
+          p.xhl_out[plane + o] = __float2bfloat16_rn(x - __bfloat162float(hi));
+        }
+        p.sumsq_out[static_cast<size_t>(tok) * (p.N / kResGroup) + (n0 + 8 * q) / kResGroup] = ss;
+      }
+    } else {  // SwiGLU: columns 32 c .. 32 c + 15 are gate rows, the next 16 the matching up rows
+      const int g0 = nt * (kUN / 2) + 16 * c;  // output index of the first pair
+      const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float gv = silu_u(v[i]) * v[16 + i];
+        const size_t o = static_cast<size_t>(tok) * (p.N / 2) + g0 + i;
+        p.out[o] = gv;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(gv);
+        p.xhl_out[o] = hi;
+        p.xhl_out[plane + o] = __float2bfloat16_rn(gv - __bfloat162float(hi));
+      }
+    }
+  }
+  if constexpr (EPI == kEpiLmHead) {
+    if (live && ok) atomicMax(p.amax_key + tok, best);
+  }
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUN) : "memory");
+  if (!ok && tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+  if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
+    __shared__ unsigned s_last;
+    __threadfence();
+    if (tid == 0) s_last = atomicAdd(&p.counters[0], 1u);
+    __syncthreads();
+    if (s_last == gridDim.x - 1) {
+      __threadfence();
+      for (int b = tid; b < p.M; b += 128) p.argmax_out[b] = argmax_key_index(atomicOr(p.amax_key + b, 0ull));
+      if (tid == 0) p.counters[0] = 0u;
+    }
+  }
+}
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// bf16 [rows][K] row-major, boxes of 64 inputs x 128 rows in the 128-byte swizzle; rows
+// past the end read as zero
+cudaError_t make_map(CUtensorMap* map, const void* ptr, int rows, int K) {
+  EncodeTiled enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kUK), 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int IN, int EPI>
+cudaError_t launch_umma_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
+                          bool prepare) {
+  auto kern = k_gemm_umma<IN, EPI>;
+  if (prepare) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.m_tiles * ((p.N + kUN - 1) / kUN));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kUSmem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
+}
+
+cudaError_t dispatch_umma(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
+                          int in_mode, int epi, bool prepare) {
+  if (in_mode == kInNorm && epi == kEpiStore) return launch_umma_t<kInNorm, kEpiStore>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiStore) return launch_umma_t<kInPlain, kEpiStore>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiResid) return launch_umma_t<kInPlain, kEpiResid>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_umma_t<kInNorm, kEpiSwiglu>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_umma_t<kInNorm, kEpiLmHead>(c, mx, mw, p, prepare);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int umma_rows_per_tile() { return kUN; }
+int umma_tokens_per_tile() { return kUM; }
+int umma_k_step() { return kUK; }
+
+cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K) {
+  static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+  return make_map(static_cast<CUtensorMap*>(map128), ptr, rows, K);
+}
+
+cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* map_w, const UmmaParams& p,
+                             int in_mode, int epi) {
+  return dispatch_umma(c, *static_cast<const CUtensorMap*>(map_x), *static_cast<const CUtensorMap*>(map_w), p,
+                       in_mode, epi, false);
+}
+
+cudaError_t prepare_gemm_umma(int in_mode, int epi) {
+  CUtensorMap dummy{};
+  UmmaParams p{};
+  return dispatch_umma(LaunchCtx{nullptr, false}, dummy, dummy, p, in_mode, epi, true);
+}
+
+}  // namespace dec
