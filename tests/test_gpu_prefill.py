@@ -36,13 +36,16 @@ CASES = [
     ("pf_b1_t129_q4_kv8", 129, dict(batch=1, weight_format=synthetic.AFFINE4_G64, head_dim=64, n_q_heads=4,
                                     n_kv_heads=2, hidden=320, intermediate=640, prefill=3, n_layers=2, vocab=400,
                                     kv_format=synthetic.AFFINE8_G64)),
-    # 128 rows or more with bf16 weights: the tcgen05 projections (ragged token and weight tiles,
-    # a vocabulary that is not a multiple of 4)
-    ("pf_b1_t200_bf16_tc5", 200, dict(batch=1, head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=256,
-                                      intermediate=576, prefill=0, n_layers=2, vocab=777)),
-    ("pf_b2_t130_bf16_tc5_ragged", 130, dict(batch=2, head_dim=64, n_q_heads=8, n_kv_heads=2, hidden=192,
-                                             intermediate=384, prefill=(5, 90), n_layers=2, vocab=500)),
-    ("pf_b1_t160_bf16_tc5_kv8", 160, dict(batch=1, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=512,
+    # 128 rows or more with bf16 weights and hidden >= 2048: the tcgen05 projections (ragged token
+    # and weight tiles, a vocabulary that is not a multiple of 4)
+    ("pf_b1_t200_bf16_tc5", 200, dict(batch=1, head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=2048,
+                                      intermediate=2112, prefill=0, n_layers=2, vocab=777)),
+    ("pf_b2_t130_bf16_tc5_ragged", 130, dict(batch=2, head_dim=64, n_q_heads=8, n_kv_heads=2, hidden=2240,
+                                             intermediate=1024, prefill=(5, 90), n_layers=2, vocab=500)),
+    # gate/up (19456 rows) and lm_head (vocabulary 20000) fill the GPU with 256-row weight tiles
+    ("pf_b2_t128_bf16_tc5_wide", 128, dict(batch=2, head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=2048,
+                                           intermediate=9728, prefill=(0, 30), n_layers=1, vocab=20000)),
+    ("pf_b1_t160_bf16_tc5_kv8", 160, dict(batch=1, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=2048,
                                           intermediate=1024, prefill=40, n_layers=2, vocab=1000,
                                           kv_format=synthetic.AFFINE8_G64)),
 ]
@@ -130,7 +133,7 @@ def test_tc5_weights_dequant_bit_exact(glue):
     """The row-major packing of the tcgen05 path (gate/up interleaved in blocks of 16) through
     dec_debug_dequant: every linear equals its bf16 source exactly."""
     from oracle import numerics
-    wl = synthetic.custom(name="dq5", head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=192, intermediate=320,
+    wl = synthetic.custom(name="dq5", head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=2048, intermediate=320,
                           vocab=200, n_layers=2, batch=1, steps=130)
     model = synthetic.generate(wl, device="cuda", with_kv=False)
     host = np_model(synthetic.to_host(model))

@@ -19,7 +19,9 @@ def dec():
     return d
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 200, 320), (77, 384, 1024), (1000, 130, 256)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 200, 320), (77, 384, 1024), (1000, 130, 256),
+                                   # grids of one CTA per SM or more take 256-row weight tiles (ragged N here)
+                                   (2048, 2600, 192), (1100, 5000, 128)])
 def test_tc5_gemm_matches_fp64(dec, M, N, K):
     g = torch.Generator(device="cpu")
     g.manual_seed(M + N + K)

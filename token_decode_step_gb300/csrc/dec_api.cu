@@ -53,6 +53,7 @@ namespace {
 
 struct PackedLinear {
   alignas(64) unsigned char tmap[128] = {};  // tcgen05 path: TMA tensor map of w (bf16 [N][K])
+  int tile_n = 128;                            // tcgen05 path: weight rows per tile (the map's box)
   void* w = nullptr;       // batch 1 and tcgen05 path: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
   uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
@@ -386,6 +387,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       up.N = L.N;
       up.K = L.K;
       up.m_tiles = (h->rows + umma_tokens_per_tile() - 1) / umma_tokens_per_tile();
+      up.tile_n = L.tile_n;
       up.sumsq_in = h->sumsq;
       up.n_sumsq_in = H / kResGroup;
       up.eps = c.rms_eps;
@@ -619,7 +621,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
   h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
   const int ny = tc ? gemm_tc_ny(h->wfmt, h->rows > blk_tok ? blk_tok : h->rows) : 0;
-  h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16;
+  // tcgen05 projections for chunks of 128+ rows with bf16 weights on models of hidden >= 2048;
+  // below that (the 0.6B shapes) the token-blocked mma.sync kernel's many small CTAs fill the
+  // GPU better (512-token chunk: 14.2 ms against 16.2 ms, measured)
+  h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16 && H >= 2048;
   const bool frag = tc && !h->umma;  // fragment-packed weights for the mma.sync path
   auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
@@ -796,19 +801,24 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     return fail("upload inv_freq", e);
   if ((e = prepare_attention(d, G, c.kv_fmt)) != cudaSuccess) return fail("attention kernel attributes", e);
   if (h->umma) {  // tensor maps of every weight and of the activation planes, kernel attributes
-    auto lmap = [&](PackedLinear& L) { return umma_tensor_map(L.tmap, L.w, L.N, L.K); };
+    auto lmap = [&](PackedLinear& L) {
+      L.tile_n = umma_tile_n(h->rows, L.N, h->num_sms);
+      return umma_tensor_map(L.tmap, L.w, L.N, L.K, L.tile_n);
+    };
     if ((e = lmap(h->lm_head)) != cudaSuccess) return fail("tensor map", e);
     for (auto& L : h->layers)
       if ((e = lmap(L.qkv)) != cudaSuccess || (e = lmap(L.o)) != cudaSuccess || (e = lmap(L.gateup)) != cudaSuccess ||
           (e = lmap(L.down)) != cudaSuccess)
         return fail("tensor map", e);
-    if ((e = umma_tensor_map(h->map_u, h->xh_u, 2 * h->rows, H)) != cudaSuccess ||
-        (e = umma_tensor_map(h->map_o, h->xh_o, 2 * h->rows, nq * d)) != cudaSuccess ||
-        (e = umma_tensor_map(h->map_g, h->xh_g, 2 * h->rows, I)) != cudaSuccess)
+    const int tok = umma_tokens_per_tile();
+    if ((e = umma_tensor_map(h->map_u, h->xh_u, 2 * h->rows, H, tok)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_o, h->xh_o, 2 * h->rows, nq * d, tok)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_g, h->xh_g, 2 * h->rows, I, tok)) != cudaSuccess)
       return fail("tensor map", e);
     const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
     for (auto& cb : combos)
-      if ((e = prepare_gemm_umma(cb[0], cb[1])) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
+      for (int tn : {128, 256})
+        if ((e = prepare_gemm_umma(cb[0], cb[1], tn)) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
   }
   if (frag) {
     GemmParams gp{};
@@ -1089,10 +1099,15 @@ extern "C" dec_status dec_debug_gemm_tc5(const void* x_hl, int M, const void* w,
     return DEC_ERR_INVALID_ARG;
   }
   alignas(64) unsigned char mx[128], mw[128];
-  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K));
-  DEC_CUDA(umma_tensor_map(mw, w, N, K));
-  DEC_CUDA(prepare_gemm_umma(kInPlain, kEpiStore));
+  int dev = 0, sms = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int tn = umma_tile_n(M, N, sms);
+  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K, umma_tokens_per_tile()));
+  DEC_CUDA(umma_tensor_map(mw, w, N, K, tn));
+  DEC_CUDA(prepare_gemm_umma(kInPlain, kEpiStore, tn));
   UmmaParams p{};
+  p.tile_n = tn;
   p.M = M;
   p.N = N;
   p.K = K;

@@ -88,6 +88,7 @@ struct GemmParams {
 // planes [2][M][K] and W bf16 [N][K] row-major, both read through TMA tensor maps.
 struct UmmaParams {
   int M, N, K, m_tiles;     // tokens, weight rows, inputs (multiple of 64), ceil(M / 128)
+  int tile_n;               // weight rows per tile: 128 or 256 (the weight map's box rows)
   const float* sumsq_in;    // norm inputs: [M][n_sumsq_in] partial sums of squares of the residual
   int n_sumsq_in;
   float eps;
@@ -295,13 +296,13 @@ int gemm_tc_chunk(int ny);                      // inputs staged per chunk
 cudaError_t launch_gemm_tc(const LaunchCtx& c, const GemmParams& p, int wfmt, int in_mode, int epi);
 cudaError_t prepare_gemm_tc(const GemmParams& p, int wfmt, int in_mode, int epi);  // smem limit, before capture
 // tcgen05 projections of many tokens (k_gemm_umma.cu)
-int umma_rows_per_tile();
 int umma_tokens_per_tile();
 int umma_k_step();
-cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K);  // CUtensorMap (128 bytes)
+int umma_tile_n(int M, int N, int num_sms);  // weight rows per tile for an M x N projection
+cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K, int box_rows);  // CUtensorMap (128 B)
 cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* map_w, const UmmaParams& p,
                              int in_mode, int epi);
-cudaError_t prepare_gemm_umma(int in_mode, int epi);
+cudaError_t prepare_gemm_umma(int in_mode, int epi, int tile_n);
 size_t attention_smem_bytes(int head_dim);
 // set the dynamic smem limits and record the shapes' occupancy (before capture)
 cudaError_t prepare_attention(int head_dim, int G, int kv_fmt);

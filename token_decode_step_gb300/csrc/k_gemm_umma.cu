@@ -24,17 +24,21 @@ namespace dec {
 namespace {
 
 constexpr int kUM = 128;                     // tokens per tile
-constexpr int kUN = 128;                     // weight rows per tile
 constexpr int kUK = 64;                      // inputs per stage
-constexpr int kUStages = 4;
 constexpr int kUTile = 128 * kUK * 2;        // 16 KB: 128 rows of 128 bytes
-constexpr int kUStage = 3 * kUTile;          // x hi, x lo, w
-constexpr int kUSmem = 1024 + kUStages * kUStage + 256 + kUM * 4;
 constexpr uint32_t kUWaitPolls = 1u << 22;
 
-// instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 128 (N >> 3 at bit 17), M = 128 (M >> 4 at bit 24)
-constexpr uint32_t kUIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kUN >> 3) << 17) | ((kUM >> 4) << 24);
+// Per weight-tile width UN (128 or 256 rows = accumulator columns): the stage holds the x hi
+// and lo tiles and UN weight rows; four stages of 48 KB, or three of 64 KB.
+template <int UN>
+struct UCfg {
+  static constexpr int kStages = UN == 128 ? 4 : 3;
+  static constexpr int kStage = 2 * kUTile + UN * kUK * 2;
+  static constexpr int kSmem = 1024 + kStages * kStage + 256 + kUM * 4;
+  // instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both
+  // K-major, N = UN (N >> 3 at bit 17), M = 128 (M >> 4 at bit 24)
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((UN >> 3) << 17) | ((kUM >> 4) << 24);
+};
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -69,11 +73,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
 }
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t acc) {
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
           tmem_d),
-      "l"(da), "l"(db), "r"(kUIdesc), "r"(acc)
+      "l"(da), "l"(db), "r"(idesc), "r"(acc)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -104,9 +108,11 @@ __device__ __forceinline__ float silu_u(float x) { return x / (1.0f + expf(-x));
 
 // grid: (token tiles x weight-row tiles), token tiles fastest (the CTAs of one weight tile
 // run together and share it through L2); 128 threads
-template <int IN, int EPI>
+template <int IN, int EPI, int UN>
 __global__ void __launch_bounds__(128, 1)
     k_gemm_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, UmmaParams p) {
+  using CF = UCfg<UN>;
+  constexpr int kUStages = CF::kStages, kUStage = CF::kStage, kUN = UN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
@@ -178,8 +184,8 @@ __global__ void __launch_bounds__(128, 1)
       const uint64_t dxh = sw128_desc(st), dxl = sw128_desc(st + kUTile), dw = sw128_desc(st + 2 * kUTile);
 #pragma unroll
       for (int k = 0; k < kUK / 16; ++k) {  // 16 inputs = 32 bytes further along the swizzled row
-        umma_bf16(tmem, dxh + 2 * k, dw + 2 * k, (kb | k) != 0 ? 1u : 0u);
-        umma_bf16(tmem, dxl + 2 * k, dw + 2 * k, 1u);
+        umma_bf16(tmem, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
+        umma_bf16(tmem, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
       }
       umma_commit(bar_empty + 8 * s);  // the stage is free once these MMAs have read it
     }
@@ -294,14 +300,14 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// bf16 [rows][K] row-major, boxes of 64 inputs x 128 rows in the 128-byte swizzle; rows
-// past the end read as zero
-cudaError_t make_map(CUtensorMap* map, const void* ptr, int rows, int K) {
+// bf16 [rows][K] row-major, boxes of 64 inputs x box_rows rows in the 128-byte swizzle;
+// rows past the end read as zero
+cudaError_t make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) {
   EncodeTiled enc = encoder();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kUK), 128u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kUK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -309,15 +315,15 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, int rows, int K) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int IN, int EPI>
+template <int IN, int EPI, int UN>
 cudaError_t launch_umma_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
                           bool prepare) {
-  auto kern = k_gemm_umma<IN, EPI>;
-  if (prepare) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmem);
+  auto kern = k_gemm_umma<IN, EPI, UN>;
+  if (prepare) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, UCfg<UN>::kSmem);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.m_tiles * ((p.N + kUN - 1) / kUN));
+  cfg.gridDim = dim3(p.m_tiles * ((p.N + UN - 1) / UN));
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = kUSmem;
+  cfg.dynamicSmemBytes = UCfg<UN>::kSmem;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -327,25 +333,39 @@ cudaError_t launch_umma_t(const LaunchCtx& c, const CUtensorMap& mx, const CUten
   return cudaLaunchKernelEx(&cfg, kern, mx, mw, p);
 }
 
+template <int UN>
+cudaError_t dispatch_umma_n(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
+                            int in_mode, int epi, bool prepare) {
+  if (in_mode == kInNorm && epi == kEpiStore) return launch_umma_t<kInNorm, kEpiStore, UN>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiStore) return launch_umma_t<kInPlain, kEpiStore, UN>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiResid) return launch_umma_t<kInPlain, kEpiResid, UN>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_umma_t<kInNorm, kEpiSwiglu, UN>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_umma_t<kInNorm, kEpiLmHead, UN>(c, mx, mw, p, prepare);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t dispatch_umma(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
                           int in_mode, int epi, bool prepare) {
-  if (in_mode == kInNorm && epi == kEpiStore) return launch_umma_t<kInNorm, kEpiStore>(c, mx, mw, p, prepare);
-  if (in_mode == kInPlain && epi == kEpiStore) return launch_umma_t<kInPlain, kEpiStore>(c, mx, mw, p, prepare);
-  if (in_mode == kInPlain && epi == kEpiResid) return launch_umma_t<kInPlain, kEpiResid>(c, mx, mw, p, prepare);
-  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_umma_t<kInNorm, kEpiSwiglu>(c, mx, mw, p, prepare);
-  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_umma_t<kInNorm, kEpiLmHead>(c, mx, mw, p, prepare);
+  if (p.tile_n == 256) return dispatch_umma_n<256>(c, mx, mw, p, in_mode, epi, prepare);
+  if (p.tile_n == 128) return dispatch_umma_n<128>(c, mx, mw, p, in_mode, epi, prepare);
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int umma_rows_per_tile() { return kUN; }
 int umma_tokens_per_tile() { return kUM; }
 int umma_k_step() { return kUK; }
 
-cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K) {
+// 256-row weight tiles halve the activation re-reads per flop; 128-row tiles when 256 would
+// leave SMs idle (small projections)
+int umma_tile_n(int M, int N, int num_sms) {
+  const long long m_tiles = (M + kUM - 1) / kUM;
+  return m_tiles * ((N + 255) / 256) >= num_sms ? 256 : 128;
+}
+
+cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K, int box_rows) {
   static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
-  return make_map(static_cast<CUtensorMap*>(map128), ptr, rows, K);
+  return make_map(static_cast<CUtensorMap*>(map128), ptr, rows, K, box_rows);
 }
 
 cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* map_w, const UmmaParams& p,
@@ -354,9 +374,10 @@ cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* 
                        in_mode, epi, false);
 }
 
-cudaError_t prepare_gemm_umma(int in_mode, int epi) {
+cudaError_t prepare_gemm_umma(int in_mode, int epi, int tile_n) {
   CUtensorMap dummy{};
   UmmaParams p{};
+  p.tile_n = tile_n;
   return dispatch_umma(LaunchCtx{nullptr, false}, dummy, dummy, p, in_mode, epi, true);
 }
 
