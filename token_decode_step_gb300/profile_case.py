@@ -31,23 +31,30 @@ def main(argv=None) -> int:
     ap.add_argument("--vocab", type=int, default=0, help="0 keeps the workload's vocabulary")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--graph", action="store_true")
+    ap.add_argument("--tps", type=int, default=1,
+                    help="tokens per sequence and step (> 1: a verify step or a prefill chunk from position 0)")
     a = ap.parse_args(argv)
 
-    kw = {"n_layers": a.layers, "steps": a.steps}
+    kw = {"n_layers": a.layers, "steps": a.steps * a.tps}
     if a.vocab:
         kw["vocab"] = a.vocab
     wl = synthetic.WORKLOADS[a.config].replace(**kw)
     model = synthetic.generate(wl, device="cuda")
-    d = Decoder(wl, model)
+    d = Decoder(wl, model, tokens_per_seq=a.tps)
     d.set_graph_mode(a.graph)
     B = wl.batch
-    logits = torch.empty((B, wl.vocab), device="cuda")
-    amax = torch.empty((B,), dtype=torch.int32, device="cuda")
+    rows = B * a.tps
+    logits = torch.empty((rows, wl.vocab), device="cuda")
+    amax = torch.empty((rows,), dtype=torch.int32, device="cuda")
     tok, pos = model["tokens"].clone(), model["positions"].clone()
     kv = synthetic.kv_buffer(model["kv"])
+    if a.tps > 1:  # the same chunk of tokens from position 0 every step
+        tok = torch.randint(0, wl.vocab, (rows,), dtype=torch.int32, device="cuda")
+        pos = torch.zeros_like(pos)
     for _ in range(a.steps):
         d.step(tok, pos, kv, logits, amax)
-        d.advance(amax, tok, pos)
+        if a.tps == 1:
+            d.advance(amax, tok, pos)
     torch.cuda.synchronize()
     st = d.device_status()
     d.close()
