@@ -188,9 +188,12 @@ DEC_API size_t dec_kv_cache_bytes(const dec_config *cfg);
      x_hl  device bf16 [2][M][K] (plane 0 hi, plane 1 lo), 16-byte aligned
      w     device bf16 [N][K] row-major, 16-byte aligned
      out   device float [M][N]
+   persistent: 0 = one CTA per tile; 1 = the persistent form (one CTA per SM walking the tiles,
+   TMA / MMA / epilogue warps, two accumulators so that an epilogue overlaps the next tile's
+   MMAs), the one dec_step uses.
    K a positive multiple of 64, M and N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
 DEC_API dec_status dec_debug_gemm_tc5(const void *x_hl, int M, const void *w, int N, int K, float *out,
-                                      dec_stream_t stream);
+                                      int persistent, dec_stream_t stream);
 
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:

@@ -22,7 +22,8 @@ def dec():
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 200, 320), (77, 384, 1024), (1000, 130, 256),
                                    # grids of one CTA per SM or more take 256-row weight tiles (ragged N here)
                                    (2048, 2600, 192), (1100, 5000, 128)])
-def test_tc5_gemm_matches_fp64(dec, M, N, K):
+@pytest.mark.parametrize("persistent", [0, 1])
+def test_tc5_gemm_matches_fp64(dec, M, N, K, persistent):
     g = torch.Generator(device="cpu")
     g.manual_seed(M + N + K)
     x = torch.randn((M, K), generator=g, dtype=torch.float64)
@@ -32,7 +33,7 @@ def test_tc5_gemm_matches_fp64(dec, M, N, K):
     xhl = torch.stack([hi, lo]).contiguous().cuda()
     wd = w.contiguous().cuda()
     out = torch.full((M, N), float("nan"), device="cuda")
-    dec.dec_debug_gemm_tc5(xhl.data_ptr(), M, wd.data_ptr(), N, K, out.data_ptr(),
+    dec.dec_debug_gemm_tc5(xhl.data_ptr(), M, wd.data_ptr(), N, K, out.data_ptr(), persistent,
                            torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     ref = (hi.double() + lo.double()) @ w.double().T

@@ -388,6 +388,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       up.K = L.K;
       up.m_tiles = (h->rows + umma_tokens_per_tile() - 1) / umma_tokens_per_tile();
       up.tile_n = L.tile_n;
+      up.persistent = h->num_sms;
       up.sumsq_in = h->sumsq;
       up.n_sumsq_in = H / kResGroup;
       up.eps = c.rms_eps;
@@ -1092,7 +1093,7 @@ extern "C" dec_status dec_attention(const dec_config* cfg, int layer, const floa
 }
 
 extern "C" dec_status dec_debug_gemm_tc5(const void* x_hl, int M, const void* w, int N, int K, float* out,
-                                         dec_stream_t stream) {
+                                         int persistent, dec_stream_t stream) {
   g_err[0] = 0;
   if (!x_hl || !w || !out || M < 1 || N < 1 || K < 64 || K % 64 != 0 || !aligned16(x_hl) || !aligned16(w)) {
     set_err("dec_debug_gemm_tc5: NULL or misaligned pointer, M or N < 1, or K not a positive multiple of 64");
@@ -1108,6 +1109,7 @@ extern "C" dec_status dec_debug_gemm_tc5(const void* x_hl, int M, const void* w,
   DEC_CUDA(prepare_gemm_umma(kInPlain, kEpiStore, tn));
   UmmaParams p{};
   p.tile_n = tn;
+  p.persistent = persistent ? sms : 0;
   p.M = M;
   p.N = N;
   p.K = K;

@@ -89,6 +89,7 @@ struct GemmParams {
 struct UmmaParams {
   int M, N, K, m_tiles;     // tokens, weight rows, inputs (multiple of 64), ceil(M / 128)
   int tile_n;               // weight rows per tile: 128 or 256 (the weight map's box rows)
+  int persistent;           // > 0: the persistent warp-specialized kernel on this many CTAs (one per SM)
   const float* sumsq_in;    // norm inputs: [M][n_sumsq_in] partial sums of squares of the residual
   int n_sumsq_in;
   float eps;

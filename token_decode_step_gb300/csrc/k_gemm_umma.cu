@@ -106,6 +106,65 @@ __device__ __forceinline__ float silu_u(float x) { return x / (1.0f + expf(-x));
 
 }  // namespace
 
+// One 32-column chunk of a token's accumulator row (columns n0 .. n0 + 31, chunk c of weight
+// tile nt): scale by the token's 1/rms, then the fused epilogue.
+template <int IN, int EPI, int UN>
+__device__ __forceinline__ void epi_chunk(const UmmaParams& p, float (&v)[32], int tok, int n0, int nt, int c,
+                                          float r, unsigned long long& best) {
+  constexpr int kUN = UN;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] *= r;
+  if constexpr (EPI == kEpiStore || EPI == kEpiLmHead) {
+    if (p.out) {
+      float* dst = p.out + static_cast<size_t>(tok) * p.N + n0;
+      if (n0 + 32 <= p.N && (p.N & 3) == 0) {  // 16-byte aligned rows
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      } else {
+        for (int i = 0; i < 32 && n0 + i < p.N; ++i) dst[i] = v[i];
+      }
+    }
+    if constexpr (EPI == kEpiLmHead) {
+      for (int i = 0; i < 32 && n0 + i < p.N; ++i) {
+        const unsigned long long key = argmax_key(v[i], n0 + i);
+        best = key > best ? key : best;
+      }
+    }
+  } else if constexpr (EPI == kEpiResid) {
+    // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per 8 rows
+    float* hrow = p.out + static_cast<size_t>(tok) * p.N + n0;
+    const size_t plane = static_cast<size_t>(p.M) * p.N;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // groups of 8 rows (N is a multiple of 64)
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 8 * q; i < 8 * q + 8; ++i) {
+        const float hn = hrow[i] + v[i];
+        hrow[i] = hn;
+        ss += hn * hn;
+        const float x = hn * bf16_to_f(p.next_norm_w[n0 + i]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+        const size_t o = static_cast<size_t>(tok) * p.N + n0 + i;
+        p.xhl_out[o] = hi;
+        p.xhl_out[plane + o] = __float2bfloat16_rn(x - __bfloat162float(hi));
+      }
+      p.sumsq_out[static_cast<size_t>(tok) * (p.N / kResGroup) + (n0 + 8 * q) / kResGroup] = ss;
+    }
+  } else {  // SwiGLU: columns 32 c .. 32 c + 15 are gate rows, the next 16 the matching up rows
+    const int g0 = nt * (kUN / 2) + 16 * c;  // output index of the first pair
+    const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float gv = silu_u(v[i]) * v[16 + i];
+      const size_t o = static_cast<size_t>(tok) * (p.N / 2) + g0 + i;
+      p.out[o] = gv;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(gv);
+      p.xhl_out[o] = hi;
+      p.xhl_out[plane + o] = __float2bfloat16_rn(gv - __bfloat162float(hi));
+    }
+  }
+}
+
 // grid: (token tiles x weight-row tiles), token tiles fastest (the CTAs of one weight tile
 // run together and share it through L2); 128 threads
 template <int IN, int EPI, int UN>
@@ -209,57 +268,7 @@ __global__ void __launch_bounds__(128, 1)
     const int n0 = nt * kUN + 32 * c;
     // (N is a multiple of 32 for every epilogue but the lm_head's: a chunk is in or out)
     if (!live || !ok || n0 >= p.N) continue;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= r;
-    if constexpr (EPI == kEpiStore || EPI == kEpiLmHead) {
-      if (p.out) {
-        float* dst = p.out + static_cast<size_t>(tok) * p.N + n0;
-        if (n0 + 32 <= p.N && (p.N & 3) == 0) {  // 16-byte aligned rows
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else {
-          for (int i = 0; i < 32 && n0 + i < p.N; ++i) dst[i] = v[i];
-        }
-      }
-      if constexpr (EPI == kEpiLmHead) {
-        for (int i = 0; i < 32 && n0 + i < p.N; ++i) {
-          const unsigned long long key = argmax_key(v[i], n0 + i);
-          best = key > best ? key : best;
-        }
-      }
-    } else if constexpr (EPI == kEpiResid) {
-      // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per 8 rows
-      float* hrow = p.out + static_cast<size_t>(tok) * p.N + n0;
-      const size_t plane = static_cast<size_t>(p.M) * p.N;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // groups of 8 rows (N is a multiple of 64)
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 8 * q; i < 8 * q + 8; ++i) {
-          const float hn = hrow[i] + v[i];
-          hrow[i] = hn;
-          ss += hn * hn;
-          const float x = hn * bf16_to_f(p.next_norm_w[n0 + i]);
-          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-          const size_t o = static_cast<size_t>(tok) * p.N + n0 + i;
-          p.xhl_out[o] = hi;
-          p.xhl_out[plane + o] = __float2bfloat16_rn(x - __bfloat162float(hi));
-        }
-        p.sumsq_out[static_cast<size_t>(tok) * (p.N / kResGroup) + (n0 + 8 * q) / kResGroup] = ss;
-      }
-    } else {  // SwiGLU: columns 32 c .. 32 c + 15 are gate rows, the next 16 the matching up rows
-      const int g0 = nt * (kUN / 2) + 16 * c;  // output index of the first pair
-      const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float gv = silu_u(v[i]) * v[16 + i];
-        const size_t o = static_cast<size_t>(tok) * (p.N / 2) + g0 + i;
-        p.out[o] = gv;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(gv);
-        p.xhl_out[o] = hi;
-        p.xhl_out[plane + o] = __float2bfloat16_rn(gv - __bfloat162float(hi));
-      }
-    }
+    epi_chunk<IN, EPI, UN>(p, v, tok, n0, nt, c, r, best);
   }
   if constexpr (EPI == kEpiLmHead) {
     if (live && ok) atomicMax(p.amax_key + tok, best);
@@ -277,6 +286,158 @@ __global__ void __launch_bounds__(128, 1)
     if (s_last == gridDim.x - 1) {
       __threadfence();
       for (int b = tid; b < p.M; b += 128) p.argmax_out[b] = argmax_key_index(atomicOr(p.amax_key + b, 0ull));
+      if (tid == 0) p.counters[0] = 0u;
+    }
+  }
+}
+
+// Persistent form: one CTA per SM walks the tiles (token tiles fastest); warp 0 issues the
+// TMA copies, warp 1 the MMAs, warps 2..5 run the epilogue.  Two accumulators in tensor
+// memory: while the epilogue warps read tile i's, the MMAs of tile i + 1 fill the other
+// (tmem_full: the MMA warp's commit after a tile; tmem_empty: 128 epilogue arrivals).
+template <int IN, int EPI, int UN>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_umma_ps(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, UmmaParams p) {
+  using CF = UCfg<UN>;
+  constexpr int S = CF::kStages, kStage = CF::kStage;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t bar_full = base + S * kStage;
+  const uint32_t bar_empty = bar_full + 8 * S;
+  const uint32_t bar_tfull = bar_empty + 8 * S;   // [2]
+  const uint32_t bar_tempty = bar_tfull + 16;     // [2]
+  const uint32_t tmem_slot = bar_tempty + 16;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = p.m_tiles * ((p.N + UN - 1) / UN);
+  const int nk = p.K / kUK;
+
+  if (warp == 1) {  // two accumulators of UN columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(2 * UN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tmem_slot - base));
+  griddep_wait();
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: the stage ring runs on across tiles
+      int it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if (it >= S && !mbar_wait(bar_empty + 8 * s, ((it / S) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar_full + 8 * s, st = base + s * kStage;
+          mbar_expect_tx(full, kStage);
+          tma_load_2d(st, &tm_x, kb * kUK, mt * kUM, full);
+          tma_load_2d(st + kUTile, &tm_x, kb * kUK, p.M + mt * kUM, full);
+          tma_load_2d(st + 2 * kUTile, &tm_w, kb * kUK, nt * UN, full);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      int it = 0, local = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
+        const int b = local & 1;
+        if (local >= 2 && !mbar_wait(bar_tempty + 8 * b, ((local >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + b * UN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if (!mbar_wait(bar_full + 8 * s, (it / S) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = base + s * kStage;
+          const uint64_t dxh = sw128_desc(st), dxl = sw128_desc(st + kUTile), dw = sw128_desc(st + 2 * kUTile);
+#pragma unroll
+          for (int k = 0; k < kUK / 16; ++k) {
+            umma_bf16(acc, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(acc, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
+          }
+          umma_commit(bar_empty + 8 * s);
+        }
+        umma_commit(bar_tfull + 8 * b);
+      }
+    }
+  } else {  // epilogue warps 2..5: lanes 32 q .. 32 q + 31 of the accumulators, q = warp % 4
+    const int q = warp & 3;
+    const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
+    unsigned long long best = 0ull;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles, b = local & 1;
+      const int tok = mt * kUM + 32 * q + lane;
+      const bool live = tok < p.M;
+      float r = 1.f;
+      if constexpr (IN == kInNorm) {  // this warp's 32 tokens: lanes share each token's sum
+        for (int j = 0; j < 32; ++j) {
+          const int tj = mt * kUM + 32 * q + j;
+          float sj = 0.f;
+          if (tj < p.M)
+            for (int i = lane; i < p.n_sumsq_in; i += 32) sj += p.sumsq_in[static_cast<size_t>(tj) * p.n_sumsq_in + i];
+          sj = warp_sum(sj);
+          if (lane == j) r = rsqrtf(sj / static_cast<float>(p.K) + p.eps);
+        }
+      }
+      if (!mbar_wait(bar_tfull + 8 * b, (local >> 1) & 1)) ok = false;
+      tc_fence_after();
+      if constexpr (EPI == kEpiLmHead) best = 0ull;
+#pragma unroll 1
+      for (int c = 0; c < UN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + b * UN + tq + 32 * c, v);
+        const int n0 = nt * UN + 32 * c;
+        if (!live || !ok || n0 >= p.N) continue;
+        epi_chunk<IN, EPI, UN>(p, v, tok, n0, nt, c, r, best);
+      }
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_tempty + 8 * b) : "memory");
+      if constexpr (EPI == kEpiLmHead) {
+        if (live && ok) atomicMax(p.amax_key + tok, best);
+      }
+    }
+  }
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * UN) : "memory");
+  if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
+  if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
+    __shared__ unsigned s_last;
+    __threadfence();
+    if (tid == 0) s_last = atomicAdd(&p.counters[0], 1u);
+    __syncthreads();
+    if (s_last == gridDim.x - 1) {
+      __threadfence();
+      for (int bb = tid; bb < p.M; bb += 192) p.argmax_out[bb] = argmax_key_index(atomicOr(p.amax_key + bb, 0ull));
       if (tid == 0) p.counters[0] = 0u;
     }
   }
@@ -318,11 +479,18 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, int rows, int K, int box
 template <int IN, int EPI, int UN>
 cudaError_t launch_umma_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const UmmaParams& p,
                           bool prepare) {
-  auto kern = k_gemm_umma<IN, EPI, UN>;
-  if (prepare) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, UCfg<UN>::kSmem);
+  auto kern = p.persistent ? k_gemm_umma_ps<IN, EPI, UN> : k_gemm_umma<IN, EPI, UN>;
+  if (prepare) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_umma<IN, EPI, UN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         UCfg<UN>::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_gemm_umma_ps<IN, EPI, UN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                UCfg<UN>::kSmem);
+  }
+  const int tiles = p.m_tiles * ((p.N + UN - 1) / UN);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.m_tiles * ((p.N + UN - 1) / UN));
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(p.persistent ? (tiles < p.persistent ? tiles : p.persistent) : tiles);
+  cfg.blockDim = dim3(p.persistent ? 192 : 128);
   cfg.dynamicSmemBytes = UCfg<UN>::kSmem;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];

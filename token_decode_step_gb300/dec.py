@@ -98,7 +98,7 @@ def _load() -> ctypes.CDLL:
                                                  vp]),
         "dec_sample": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(SamplingParams), vp, vp]),
         "dec_kv_quantize": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp]),
-        "dec_debug_gemm_tc5": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, vp]),
+        "dec_debug_gemm_tc5": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -206,8 +206,9 @@ def dec_sample(logits: int, batch: int, vocab: int, params: SamplingParams, toke
     return _check(lib.dec_sample(logits, batch, vocab, ctypes.byref(params), tokens, stream), "dec_sample")
 
 
-def dec_debug_gemm_tc5(x_hl: int, M: int, w: int, N: int, K: int, out: int, stream: int = 0) -> int:
-    return _check(lib.dec_debug_gemm_tc5(x_hl, M, w, N, K, out, stream), "dec_debug_gemm_tc5")
+def dec_debug_gemm_tc5(x_hl: int, M: int, w: int, N: int, K: int, out: int, persistent: int = 1,
+                       stream: int = 0) -> int:
+    return _check(lib.dec_debug_gemm_tc5(x_hl, M, w, N, K, out, persistent, stream), "dec_debug_gemm_tc5")
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:

@@ -51,7 +51,10 @@ def main(argv=None) -> int:
     if a.tps > 1:  # the same chunk of tokens from position 0 every step
         tok = torch.randint(0, wl.vocab, (rows,), dtype=torch.int32, device="cuda")
         pos = torch.zeros_like(pos)
-    for _ in range(a.steps):
+    for i in range(a.steps):
+        # the algorithmic bytes of this step's attention launches (at its mean cached length)
+        mean_p = float(pos.float().mean())
+        print(f"step {i}: attention algorithmic bytes per launch {d.kernel_bytes(2, mean_p):.0f}", flush=True)
         d.step(tok, pos, kv, logits, amax)
         if a.tps == 1:
             d.advance(amax, tok, pos)
