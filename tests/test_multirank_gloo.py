@@ -36,7 +36,7 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_take_the_slowest_time():
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of a threaded process
     mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
     assert out[0][0] == out[1][0] == 30.0
     assert out[0][1] == pytest.approx(2 * 4 * 32 / 0.030)
