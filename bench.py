@@ -184,6 +184,7 @@ def job_tokens_per_s(world: int, batch: int, steps: int, ms_max: float) -> float
 
 
 def run_ours(args, rank: int, world: int) -> dict | None:
+    import numpy as np
     import torch
     import synthetic
     from token_decode_step_gb300 import build as build_mod
@@ -245,22 +246,13 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     torch.cuda.synchronize(dev)
     prof_mean_p = prof_p + (args.profile_steps - 1) / 2.0
 
-    # end to end through the C ABI with host buffers: H2D tokens+positions, step, D2H argmax
-    h_tok = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    h_pos = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    h_am = torch.empty((B,), dtype=torch.int32, pin_memory=True)
-    h_tok.copy_(tokens.cpu())
-    h_pos.copy_(positions.cpu())
-    d_tok = torch.empty_like(tokens)
-    d_pos = torch.empty_like(positions)
+    # end to end through the C ABI with host buffers (dec_step_host): the host greedy loop's
+    # call, H2D of tokens + positions, the step and D2H of the argmax inside it, every step
+    h_tok = tokens.cpu().numpy().astype(np.int32).copy()
+    h_pos = positions.cpu().numpy().astype(np.int32).copy()
     def e2e_step():
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        dec.step(d_tok, d_pos, kv, None, argmax, stream)
-        h_am.copy_(argmax, non_blocking=True)
-        stream.synchronize()
-        h_tok.copy_(h_am)
-        h_pos.add_(1)
+        dec.step_host(h_tok, h_pos, kv, None, h_tok, stream)  # the argmax overwrites the tokens
+        h_pos[...] += 1
 
     e2e_step()  # captures the graph for this pointer set (untimed)
     torch.cuda.synchronize(dev)

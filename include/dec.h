@@ -168,6 +168,23 @@ DEC_API dec_status dec_step(dec_handle *h, const int32_t *token_ids, const int32
                     void *kv_cache, float *logits_out, int32_t *argmax_out,
                     dec_stream_t stream);
 
+/* dec_step for a host-driven decode loop: the token ids, positions and greedy result live
+   in host memory (Butter architecture.md, "SINGLE-TOKEN DECODE": one submission per token,
+   a 4-byte result read back per sequence).
+     token_ids  host int32 [rows], positions host int32 [batch], argmax_out host int32 [rows]
+                (may alias token_ids); pageable or pinned.
+     kv_cache, logits_out  device, as in dec_step.
+   The inputs are copied into the handle's pinned staging buffer; then one CUDA graph on
+   `stream` copies them to the device, runs the step and copies the argmax back, and the
+   call returns after synchronising `stream` with argmax_out written.  The staging buffers
+   (pinned host and device, 4 (2 rows + batch) bytes each) are allocated by the first call
+   (DEC_ERR_OOM if that fails) and freed by dec_destroy.  Errors as dec_step; a CUDA fault of
+   the step surfaces here as DEC_ERR_CUDA.  The same graph rule as dec_step (re-captured when
+   kv_cache or logits_out changes); the two calls keep separate graphs. */
+DEC_API dec_status dec_step_host(dec_handle *h, const int32_t *token_ids, const int32_t *positions,
+                    void *kv_cache, float *logits_out, int32_t *argmax_out,
+                    dec_stream_t stream);
+
 /* Free every device resource of the handle (caller buffers are untouched).
    The caller must make sure no step of this handle is still running. */
 DEC_API void dec_destroy(dec_handle *h);

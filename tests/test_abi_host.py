@@ -125,6 +125,12 @@ def test_step_rejects_null_handle(dec):
     assert "handle" in dec.dec_last_error()
 
 
+def test_step_host_rejects_null_handle(dec):
+    st = dec.lib.dec_step_host(None, 16, 16, 16, None, 16, None)
+    assert st == dec.DEC_ERR_INVALID_ARG
+    assert "handle" in dec.dec_last_error()
+
+
 @pytest.mark.parametrize("kw,msg", [
     (dict(logits=None), "NULL"),
     (dict(tokens=None), "NULL"),

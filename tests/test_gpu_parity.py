@@ -131,6 +131,36 @@ def test_graph_equals_eager_bitwise(glue, batch):
         assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3])
 
 
+@pytest.mark.parametrize("batch,graph", [(1, True), (4, True), (4, False)])
+def test_host_step_equals_device_step_bitwise(glue, batch, graph):
+    """dec_step_host (host token ids, positions and argmax, copies inside the call) gives
+    the device-pointer step's logits, argmax and appended K/V bit for bit; its argmax
+    output aliases its token input, the host greedy loop's natural form."""
+    wl = synthetic.WORKLOADS["tiny"].replace(batch=batch)
+    model = synthetic.generate(wl, device="cuda")
+    dec = glue.Decoder(wl, model)
+    dec.set_graph_mode(graph)
+    kv0 = model["kv"].clone()
+    try:
+        ref, kv_ref = gpu_greedy(dec, model, 4)
+        kv_ref = kv_ref.clone()
+        model["kv"].copy_(kv0)
+        tok = model["tokens"].cpu().numpy().astype(np.int32).copy()
+        pos = model["positions"].cpu().numpy().astype(np.int32).copy()
+        logits = torch.empty((batch, wl.vocab), device="cuda")
+        for s, (tin, pin, lg, am) in enumerate(ref):
+            assert np.array_equal(tok, tin) and np.array_equal(pos, pin), f"step {s} inputs"
+            dec.step_host(tok, pos, model["kv"], logits, tok)
+            assert np.array_equal(tok, am), f"step {s} argmax"
+            assert np.array_equal(logits.cpu().numpy(), lg), f"step {s} logits"
+            pos += 1
+        torch.cuda.synchronize()
+        assert torch.equal(model["kv"], kv_ref)
+        assert dec.device_status()[1] == 0
+    finally:
+        dec.close()
+
+
 def test_repeated_step_is_deterministic(glue):
     wl = synthetic.custom(name="det", head_dim=128, n_q_heads=4, n_kv_heads=1, hidden=256, intermediate=512,
                           vocab=999, prefill=900, steps=1)

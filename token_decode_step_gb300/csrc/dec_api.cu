@@ -132,6 +132,15 @@ struct dec_handle {
   cudaGraphExec_t exec = nullptr;
   bool have_graph = false;
   StepPtrs captured{};
+  // dec_step_host: staging int32 [rows tokens | batch positions | rows argmax], pinned on
+  // the host and on the device (allocated by the first call), and the graph that copies
+  // in, runs the step and copies the argmax back
+  int32_t* io_host = nullptr;
+  int32_t* io_dev = nullptr;
+  cudaGraph_t hgraph = nullptr;
+  cudaGraphExec_t hexec = nullptr;
+  bool have_hgraph = false;
+  StepPtrs hcaptured{};
   // profiling: events around every launch; the stream is held (by a sleeping kernel
   // on hold_stream) until the host has enqueued the whole step
   std::vector<cudaEvent_t> events;
@@ -500,18 +509,41 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   return DEC_OK;
 }
 
-void drop_graph(dec_handle* h) {
-  if (h->exec) cudaGraphExecDestroy(h->exec);
-  if (h->graph) cudaGraphDestroy(h->graph);
-  h->exec = nullptr;
-  h->graph = nullptr;
-  h->have_graph = false;
+void drop_one_graph(cudaGraph_t& graph, cudaGraphExec_t& exec, bool& have) {
+  if (exec) cudaGraphExecDestroy(exec);
+  if (graph) cudaGraphDestroy(graph);
+  exec = nullptr;
+  graph = nullptr;
+  have = false;
 }
 
-dec_status capture_graph(dec_handle* h, const StepPtrs& sp) {
-  drop_graph(h);
+void drop_graph(dec_handle* h) {
+  drop_one_graph(h->graph, h->exec, h->have_graph);
+  drop_one_graph(h->hgraph, h->hexec, h->have_hgraph);
+}
+
+// The host-staged step's copies: inputs in (tokens and positions are adjacent), argmax out.
+dec_status enqueue_io_in(dec_handle* h, cudaStream_t s) {
+  DEC_CUDA(cudaMemcpyAsync(h->io_dev, h->io_host, static_cast<size_t>(h->rows + h->cfg.batch) * 4,
+                           cudaMemcpyHostToDevice, s));
+  return DEC_OK;
+}
+dec_status enqueue_io_out(dec_handle* h, cudaStream_t s) {
+  const size_t off = static_cast<size_t>(h->rows) + h->cfg.batch;
+  DEC_CUDA(cudaMemcpyAsync(h->io_host + off, h->io_dev + off, static_cast<size_t>(h->rows) * 4,
+                           cudaMemcpyDeviceToHost, s));
+  return DEC_OK;
+}
+
+// Capture the step for the pointer set sp (with the staging copies around it when `io`) into
+// graph / exec.
+dec_status capture_into(dec_handle* h, const StepPtrs& sp, bool io, cudaGraph_t& graph_out, cudaGraphExec_t& exec_out,
+                        bool& have) {
+  drop_one_graph(graph_out, exec_out, have);
   DEC_CUDA(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
-  dec_status st = enqueue_step(h, sp, h->cap_stream, true, nullptr);
+  dec_status st = io ? enqueue_io_in(h, h->cap_stream) : DEC_OK;
+  if (st == DEC_OK) st = enqueue_step(h, sp, h->cap_stream, true, nullptr);
+  if (st == DEC_OK && io) st = enqueue_io_out(h, h->cap_stream);
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
   if (st != DEC_OK) {
@@ -522,16 +554,21 @@ dec_status capture_graph(dec_handle* h, const StepPtrs& sp) {
     set_err("cudaStreamEndCapture failed: %s", cudaGetErrorString(e));
     return DEC_ERR_CUDA;
   }
-  h->graph = graph;
-  e = cudaGraphInstantiateWithFlags(&h->exec, graph, 0);
+  graph_out = graph;
+  e = cudaGraphInstantiateWithFlags(&exec_out, graph, 0);
   if (e != cudaSuccess) {
     set_err("cudaGraphInstantiate failed: %s", cudaGetErrorString(e));
-    drop_graph(h);
+    drop_one_graph(graph_out, exec_out, have);
     return DEC_ERR_CUDA;
   }
-  h->captured = sp;
-  h->have_graph = true;
+  have = true;
   return DEC_OK;
+}
+
+dec_status capture_graph(dec_handle* h, const StepPtrs& sp) {
+  const dec_status st = capture_into(h, sp, false, h->graph, h->exec, h->have_graph);
+  if (st == DEC_OK) h->captured = sp;
+  return st;
 }
 
 dec_status check_step_args(dec_handle* h, const StepPtrs& sp) {
@@ -841,6 +878,8 @@ extern "C" void dec_destroy(dec_handle* h) {
   if (h->hold_ev) cudaEventDestroy(h->hold_ev);
   if (h->hold_stream) cudaStreamDestroy(h->hold_stream);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->io_host) cudaFreeHost(h->io_host);
+  if (h->io_dev) cudaFree(h->io_dev);
   if (h->wmem) cudaFree(h->wmem);
   if (h->ws) cudaFree(h->ws);
   delete h;
@@ -860,6 +899,54 @@ extern "C" dec_status dec_step(dec_handle* h, const int32_t* token_ids, const in
     if ((st = capture_graph(h, sp)) != DEC_OK) return st;
   }
   DEC_CUDA(cudaGraphLaunch(h->exec, cs));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_step_host(dec_handle* h, const int32_t* token_ids, const int32_t* positions,
+                                    void* kv_cache, float* logits_out, int32_t* argmax_out, dec_stream_t stream) {
+  if (!h) {
+    set_err("handle is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (!token_ids || !positions || !argmax_out) {
+    set_err("token_ids, positions and argmax_out must be non-NULL host pointers");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const size_t rows = static_cast<size_t>(h->rows), B = static_cast<size_t>(h->cfg.batch);
+  const size_t n_io = 2 * rows + B;
+  if (!h->io_host) {
+    void* ph = nullptr;
+    void* pd = nullptr;
+    cudaError_t e = cudaHostAlloc(&ph, n_io * 4, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaMalloc(&pd, n_io * 4);
+    if (e != cudaSuccess) {
+      if (ph) cudaFreeHost(ph);
+      set_err("staging buffers for dec_step_host (%zu bytes): %s", n_io * 4, cudaGetErrorString(e));
+      return DEC_ERR_OOM;
+    }
+    h->io_host = static_cast<int32_t*>(ph);
+    h->io_dev = static_cast<int32_t*>(pd);
+  }
+  const StepPtrs sp{h->io_dev, h->io_dev + rows, kv_cache, logits_out, h->io_dev + rows + B};
+  dec_status st = check_step_args(h, sp);
+  if (st != DEC_OK) return st;
+  // inputs into the pinned staging first: argmax_out may alias token_ids
+  std::memcpy(h->io_host, token_ids, rows * 4);
+  std::memcpy(h->io_host + rows, positions, B * 4);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (!h->graph_mode) {
+    if ((st = enqueue_io_in(h, cs)) != DEC_OK) return st;
+    if ((st = enqueue_step(h, sp, cs, true, nullptr)) != DEC_OK) return st;
+    if ((st = enqueue_io_out(h, cs)) != DEC_OK) return st;
+  } else {
+    if (!h->have_hgraph || !(h->hcaptured == sp)) {
+      if ((st = capture_into(h, sp, true, h->hgraph, h->hexec, h->have_hgraph)) != DEC_OK) return st;
+      h->hcaptured = sp;
+    }
+    DEC_CUDA(cudaGraphLaunch(h->hexec, cs));
+  }
+  DEC_CUDA(cudaStreamSynchronize(cs));
+  std::memcpy(argmax_out, h->io_host + rows + B, rows * 4);
   return DEC_OK;
 }
 

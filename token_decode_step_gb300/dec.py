@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "dec_create": (vp, [ctypes.POINTER(DecConfig), ctypes.POINTER(DecWeights)]),
         "dec_step": (ctypes.c_int, [vp, i32p, i32p, vp, vp, i32p, vp]),
+        "dec_step_host": (ctypes.c_int, [vp, i32p, i32p, vp, vp, i32p, vp]),
         "dec_destroy": (None, [vp]),
         "dec_kv_cache_bytes": (ctypes.c_size_t, [ctypes.POINTER(DecConfig)]),
         "dec_last_error": (ctypes.c_char_p, []),
@@ -143,6 +144,13 @@ def dec_create(cfg: DecConfig, weights: DecWeights) -> int:
 def dec_step(h: int, token_ids: int, positions: int, kv_cache: int, logits_out: int | None, argmax_out: int,
              stream: int = 0) -> int:
     return _check(lib.dec_step(h, token_ids, positions, kv_cache, logits_out, argmax_out, stream), "dec_step")
+
+
+def dec_step_host(h: int, token_ids: int, positions: int, kv_cache: int, logits_out: int | None,
+                  argmax_out: int, stream: int = 0) -> int:
+    """token_ids, positions and argmax_out are HOST addresses; returns after the step."""
+    return _check(lib.dec_step_host(h, token_ids, positions, kv_cache, logits_out, argmax_out, stream),
+                  "dec_step_host")
 
 
 def dec_destroy(h: int) -> None:

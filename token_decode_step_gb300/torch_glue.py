@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import torch
 
 from . import dec
@@ -77,6 +78,19 @@ class Decoder:
              argmax: torch.Tensor, stream: torch.cuda.Stream | None = None) -> None:
         s = (stream or torch.cuda.current_stream()).cuda_stream
         dec.dec_step(self.handle, _ptr(tokens), _ptr(positions), _ptr(kv), _ptr(logits), _ptr(argmax), s)
+
+    def step_host(self, tokens: np.ndarray, positions: np.ndarray, kv: torch.Tensor, logits: torch.Tensor | None,
+                  argmax: np.ndarray, stream: torch.cuda.Stream | None = None) -> None:
+        """One step with host int32 arrays (C-contiguous numpy) for tokens, positions and the argmax."""
+        for a in (tokens, positions, argmax):
+            if a.dtype != np.int32 or not a.flags["C_CONTIGUOUS"]:
+                raise ValueError("tokens, positions and argmax must be C-contiguous int32 numpy arrays")
+        rows = self.cfg.batch * max(1, self.cfg.tokens_per_seq)
+        if tokens.size < rows or positions.size < self.cfg.batch or argmax.size < rows:
+            raise ValueError("host arrays are smaller than the step's rows / batch")
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        dec.dec_step_host(self.handle, tokens.ctypes.data, positions.ctypes.data, _ptr(kv), _ptr(logits),
+                          argmax.ctypes.data, s)
 
     def profile_step(self, tokens, positions, kv, logits, argmax, ms: list[float], launches: list[int],
                      stream: torch.cuda.Stream | None = None) -> None:
