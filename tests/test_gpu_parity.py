@@ -111,7 +111,7 @@ def test_custom_batched(glue, name, kw):
 
 @pytest.mark.parametrize("name,kw", CUSTOM, ids=[c[0] for c in CUSTOM])
 def test_custom_shapes(glue, name, kw):
-    wl = synthetic.custom(name=name, seed=hash(name) % 1000, **kw)
+    wl = synthetic.custom(name=name, seed=sum(map(ord, name)), **kw)  # stable across processes
     w = _run(glue, wl, wl.steps)
     print(name, w)
 
