@@ -30,7 +30,7 @@ Sources (page title and section):
     AffineQuantizedKVCache) for oracle/kvcache.py: the cache may hold affine 8-bit
     codes with a bf16 scale and bias per group of 64 instead of bf16 rows.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * RoPE pairs element i with element i + d/2 (rotate-half), angle
     pos * theta^(-2i/d), theta = 1e6.
   * RMSNorm multiplies by the stored weight w (not 1 + w), eps = 1e-6; the q/k

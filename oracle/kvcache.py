@@ -13,7 +13,7 @@ KVCache, AffineQuantizedKVCache) and its component list (Caches: KVCache,
 AffineQuantizedKVCache); oxinfer crate page, "MLX checkpoints" (the affine form
 w = scale * q + bias with one bf16 scale and bias per group of 64).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * 8-bit codes, groups of 64 consecutive elements of one row (one position of one
     head), bf16 scale and bias, like the affine weight format.
   * Min-max quantization, decided in float32: mn, mx = min, max of the group;

@@ -7,7 +7,7 @@ largest, mask the rest), top-p (cumulative softmax, threshold mask) and an
 inverse-CDF draw with an RNG state; greedy (temperature 0) is the argmax.  oxinfer's
 crate page lists the same knobs (--temp, --top-k, --top-p, --seed).
 
-Readings where the page is silent (each is listed in the design doc):
+Readings where the page is silent:
   * Candidates: the k largest logits under the total order (logit descending, index
     ascending), k = top_k for 1 <= top_k <= 1024, else 1024 (the page sorts "top k";
     a sort of the whole vocabulary has no counterpart).  k is at most the vocabulary.
