@@ -212,6 +212,14 @@ DEC_API size_t dec_kv_cache_bytes(const dec_config *cfg);
 DEC_API dec_status dec_debug_gemm_tc5(const void *x_hl, int M, const void *w, int N, int K, float *out,
                                       int persistent, dec_stream_t stream);
 
+/* Test hook for the time-out path: enqueues on `stream` one bounded wait that can only run out
+   (an mbarrier that nothing arrives on, polled `polls` times, 1..65536), which sets the
+   time-out bit of h's device status word exactly as a bounded wait of the tensor-memory kernels
+   does when a copy or an MMA never completes.  After a stream synchronisation,
+   dec_get_device_status returns DEC_ERR_TIMEOUT (and clears the word); the handle and the CUDA
+   context stay usable.  No GPU fault or trap is involved. */
+DEC_API dec_status dec_debug_force_timeout(dec_handle *h, int polls, dec_stream_t stream);
+
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:
    mn, mx = min, max; scale = bf16(fl(fl(mx - mn) / 255)); bias = bf16(mn) (round to

@@ -125,6 +125,11 @@ def test_step_rejects_null_handle(dec):
     assert "handle" in dec.dec_last_error()
 
 
+def test_force_timeout_rejects_bad_arguments(dec):
+    assert dec.lib.dec_debug_force_timeout(None, 16, None) == dec.DEC_ERR_INVALID_ARG
+    assert "polls" in dec.dec_last_error()
+
+
 def test_step_host_rejects_null_handle(dec):
     st = dec.lib.dec_step_host(None, 16, 16, 16, None, 16, None)
     assert st == dec.DEC_ERR_INVALID_ARG

@@ -207,6 +207,29 @@ def test_debug_dequant_bit_exact(glue, fmt, batch):
         dec.close()
 
 
+def test_forced_timeout_is_reported_and_the_handle_stays_usable(glue):
+    """A bounded device wait that can only run out (an mbarrier nothing arrives on) sets the
+    time-out bit; dec_get_device_status reports DEC_ERR_TIMEOUT once and clears it, and the next
+    step runs normally.  No fault or trap is involved."""
+    from token_decode_step_gb300 import dec as D
+    wl = synthetic.WORKLOADS["tiny"]
+    model = synthetic.generate(wl, device="cuda")
+    dec = glue.Decoder(wl, model)
+    logits = torch.empty((1, wl.vocab), device="cuda")
+    am = torch.empty((1,), dtype=torch.int32, device="cuda")
+    try:
+        D.dec_debug_force_timeout(dec.handle, 256, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        st, bits = dec.device_status()
+        assert st == D.DEC_ERR_TIMEOUT and bits & 4
+        assert dec.device_status() == (0, 0)
+        dec.step(model["tokens"], model["positions"], model["kv"], logits, am)
+        torch.cuda.synchronize()
+        assert dec.device_status() == (0, 0) and torch.isfinite(logits).all()
+    finally:
+        dec.close()
+
+
 def test_out_of_range_inputs_are_flagged(glue):
     wl = synthetic.custom(name="bad", vocab=300, prefill=10, steps=1)
     model = synthetic.generate(wl, device="cuda")

@@ -1019,6 +1019,15 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
   return DEC_OK;
 }
 
+extern "C" dec_status dec_debug_force_timeout(dec_handle* h, int polls, dec_stream_t stream) {
+  if (!h || polls < 1 || polls > 65536) {
+    set_err("dec_debug_force_timeout: handle is NULL or polls outside 1..65536");
+    return DEC_ERR_INVALID_ARG;
+  }
+  DEC_CUDA(launch_force_timeout(reinterpret_cast<cudaStream_t>(stream), h->status, polls));
+  return DEC_OK;
+}
+
 extern "C" dec_status dec_advance(const int32_t* argmax, int32_t* token_ids, int32_t* positions, int batch,
                                   dec_stream_t stream) {
   if (!argmax || !token_ids || !positions || batch < 1) {

@@ -358,6 +358,7 @@ cudaError_t debug_dequant_frag(cudaStream_t s, float* out, const void* w, int wf
                                int row_offset, int interleave_block, int which_half);
 cudaError_t launch_hold(cudaStream_t s, unsigned long long ns);
 cudaError_t launch_sample(cudaStream_t s, const SampleParams& p, int batch);
+cudaError_t launch_force_timeout(cudaStream_t s, unsigned* status, int polls);
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch);
 

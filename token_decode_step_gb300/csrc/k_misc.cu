@@ -361,6 +361,33 @@ cudaError_t launch_hold(cudaStream_t s, unsigned long long ns) {
   return cudaGetLastError();
 }
 
+// A bounded wait that can only run out: one thread initialises an mbarrier that nothing ever
+// arrives on and polls its first phase `polls` times, then sets the time-out bit of the status
+// word, as every bounded wait of the tensor-memory kernels does when a copy or an MMA never
+// completes.  The host reads it through dec_get_device_status (DEC_ERR_TIMEOUT); the context
+// stays usable.
+__global__ void k_force_timeout(unsigned* status, int polls) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(1) : "memory");
+  bool done = false;
+  for (int i = 0; i < polls && !done; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b), "r"(0u)
+        : "memory");
+    done = ok != 0;
+  }
+  if (!done) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_force_timeout(cudaStream_t s, unsigned* status, int polls) {
+  k_force_timeout<<<1, 1, 0, s>>>(status, polls);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* tokens, int32_t* positions,
                            int batch) {
   k_advance<<<(batch + 127) / 128, 128, 0, s>>>(argmax, tokens, positions, batch);

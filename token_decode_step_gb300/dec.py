@@ -100,6 +100,7 @@ def _load() -> ctypes.CDLL:
         "dec_sample": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(SamplingParams), vp, vp]),
         "dec_kv_quantize": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp]),
         "dec_debug_gemm_tc5": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp]),
+        "dec_debug_force_timeout": (ctypes.c_int, [vp, ctypes.c_int, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -217,6 +218,10 @@ def dec_sample(logits: int, batch: int, vocab: int, params: SamplingParams, toke
 def dec_debug_gemm_tc5(x_hl: int, M: int, w: int, N: int, K: int, out: int, persistent: int = 1,
                        stream: int = 0) -> int:
     return _check(lib.dec_debug_gemm_tc5(x_hl, M, w, N, K, out, persistent, stream), "dec_debug_gemm_tc5")
+
+
+def dec_debug_force_timeout(h: int, polls: int = 256, stream: int = 0) -> int:
+    return _check(lib.dec_debug_force_timeout(h, polls, stream), "dec_debug_force_timeout")
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
