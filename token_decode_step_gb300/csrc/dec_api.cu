@@ -14,6 +14,8 @@
 #include <cstring>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dec_internal.cuh"
 
 using namespace dec;
@@ -295,8 +297,14 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   const dec_config& c = h->cfg;
   const int d = c.head_dim, H = c.hidden;
   LaunchCtx lc{stream, false};
+  // every launch is an NVTX range named after its kernel class (host-side, around the launch
+  // call: a profiler attributes the kernels by range, e.g. ncu --nvtx --nvtx-include "gate_up/");
+  // a tool-less process pays a no-op call
+  static const char* const kClassNames[DEC_K_COUNT] = {"embed", "qkv", "attention", "o_proj",
+                                                       "gate_up", "down", "lm_head"};
   auto note = [&](int cls) {
     if (classes) classes->push_back(cls);
+    nvtxRangePushA(kClassNames[cls]);
   };
   auto check = [&](cudaError_t e, const char* what) -> dec_status {
     if (e != cudaSuccess) {
@@ -312,6 +320,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     return cudaEventRecord(h->events[2 * ev], stream);
   };
   auto ev_end = [&]() -> cudaError_t {
+    nvtxRangePop();
     if (!classes) return cudaSuccess;
     cudaError_t e = cudaEventRecord(h->events[2 * ev + 1], stream);
     ++ev;
