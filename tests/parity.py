@@ -55,64 +55,6 @@ def check_logits(gpu: np.ndarray, ref: np.ndarray, gpu_argmax, ref_argmax, where
     return worst
 
 
-def oracle_noise_spread(wl, model_host: dict, kv_init, gpu_steps, step: int, b: int, rel: float = 1e-5,
-                        cache_weights: bool = False) -> float:
-    """Conditioning check for one sequence: replays sequence b alone in the oracle up to
-    `step` twice, the second time with every attention output multiplied elementwise by
-    (1 + rel N(0, 1)) -- a perturbation below the attention kernel's own float32 error --
-    and returns max |logit difference| between the two at `step`.  A spread above the
-    logits tolerance means the oracle's answer is not determined to that tolerance at
-    float32 precision: several results are correct."""
-    import oracle.decoder as odec
-    if isinstance(kv_init, np.ndarray):
-        kv1 = kv_init[:, :, b:b + 1].copy()
-    else:
-        kv1 = oracle.Affine8Cache(kv_init.codes[:, :, b:b + 1].copy(), kv_init.params[:, :, b:b + 1].copy())
-    kv2 = kv1.copy()
-    m = oracle.OracleModel.from_synthetic(wl.replace(batch=1), model_host, cache_weights=cache_weights)
-    plain = odec.gqa_attention
-    rng = np.random.default_rng(b)
-
-    def noisy(q, K, V):
-        o = plain(q, K, V)
-        return o * (1.0 + rel * rng.standard_normal(o.shape))
-
-    out = []
-    for attn in (plain, noisy):
-        odec.gqa_attention = attn
-        kv = kv1 if attn is plain else kv2
-        try:
-            for s2 in range(step + 1):
-                tin, pin = gpu_steps[s2][0], gpu_steps[s2][1]
-                lg, _ = oracle.decode_step(m, kv, tin[b:b + 1], pin[b:b + 1])
-        finally:
-            odec.gqa_attention = plain
-        out.append(lg[0])
-    return float(np.max(np.abs(out[0] - out[1])))
-
-
-def check_logits_conditioned(gpu, ref, gpu_argmax, ref_argmax, where, spread_fn) -> dict:
-    """check_logits per sequence; a sequence outside the tolerance passes only when the
-    oracle's own spread under the conditioning check (spread_fn(b)) exceeds the tolerance."""
-    worst = {"max_abs": 0.0, "rel_l2": 0.0, "exempt": 0, "ill_conditioned": 0}
-    for b in range(ref.shape[0]):
-        try:
-            w = check_logits(gpu[b:b + 1], ref[b:b + 1], gpu_argmax[b:b + 1], ref_argmax[b:b + 1], f"{where} seq {b}")
-        except AssertionError as err:
-            spread = spread_fn(b)
-            if spread <= MAX_ABS:
-                raise AssertionError(f"{err} (the oracle's own spread under 1e-5 attention noise is only "
-                                     f"{spread:.3e})") from None
-            print(f"{where} seq {b}: outside the tolerance, ill-conditioned (oracle spread {spread:.3e} under "
-                  f"1e-5 attention noise)")
-            worst["ill_conditioned"] += 1
-            continue
-        worst["max_abs"] = max(worst["max_abs"], w["max_abs"])
-        worst["rel_l2"] = max(worst["rel_l2"], w["rel_l2"])
-        worst["exempt"] += w["exempt"]
-    return worst
-
-
 def gpu_greedy(dec_obj, model_dev: dict, steps: int, want_logits: bool = True):
     """Greedy loop on the device: tokens <- argmax, positions += 1 after every step.
     Returns per-step (input tokens, input positions, logits, argmax) on the host and
@@ -135,21 +77,50 @@ def gpu_greedy(dec_obj, model_dev: dict, steps: int, want_logits: bool = True):
     return out, kv
 
 
-def oracle_replay(wl, model_host: dict, kv_init_np: np.ndarray, gpu_steps, check_steps=None,
-                  cache_weights: bool = True):
+def select_seqs(kv, seqs):
+    """The oracle-side cache of the sequences `seqs` (a copy): bf16 bit patterns
+    [L][2][B][...] or an affine 8-bit cache, sliced along the batch axis."""
+    if seqs is None:
+        return kv.copy()
+    idx = np.asarray(seqs)
+    if isinstance(kv, np.ndarray):
+        return kv[:, :, idx].copy()
+    return oracle.Affine8Cache(kv.codes[:, :, idx].copy(), kv.params[:, :, idx].copy())
+
+
+def oracle_replay(wl, model_host: dict, kv_init, gpu_steps, check_steps=None, cache_weights: bool = True,
+                  seqs=None, model=None):
     """Replay the oracle on the GPU's token sequence (each side keeps its own KV).
-    Returns ([(step, oracle logits, oracle argmax)] for the checked steps, final
-    oracle KV); every step up to the last checked one is computed, since the KV
-    state depends on all of them."""
-    m = oracle.OracleModel.from_synthetic(wl, model_host, cache_weights=cache_weights)
-    kv = kv_init_np.copy()
+
+    seqs: the sequences to replay (None: the whole batch).  The sequences of a batch are
+    independent (own token, cache and position), so a subset replays exactly what the
+    batched step computed for them.  Returns ([(step, oracle logits [len(seqs)][V],
+    oracle argmax)] for the checked steps, final oracle KV of those sequences); every
+    step up to the last checked one is computed, since the KV state depends on all of
+    them.  `model`: an OracleModel to reuse (its float64 weights already converted)."""
+    m = model if model is not None else oracle.OracleModel.from_synthetic(wl, model_host,
+                                                                          cache_weights=cache_weights)
+    kv = select_seqs(kv_init, seqs)
+    sel = slice(None) if seqs is None else np.asarray(seqs)
     last = max(check_steps) if check_steps else len(gpu_steps) - 1
     res = []
     for s, (tin, pin, _, _) in enumerate(gpu_steps[: last + 1]):
-        logits, am = oracle.decode_step(m, kv, tin, pin)
+        logits, am = oracle.decode_step(m, kv, tin[sel], pin[sel])
         if check_steps is None or s in check_steps:
             res.append((s, logits, am))
     return res, kv
+
+
+def replay_plan(wl):
+    """Which (sequences, steps) the full-size step tests replay in the oracle.
+
+    Every config is replayed over ALL of its greedy steps.  Batches above 4 sequences are
+    replayed over all steps for 3 fixed sequences (the first, the middle one and the last)
+    and, for every sequence, over the first 2 steps.  Returns a list of (seqs or None, steps)."""
+    if wl.batch <= 4:
+        return [(None, wl.steps)]
+    fixed = sorted({0, wl.batch // 2, wl.batch - 1})
+    return [(fixed, wl.steps), (None, 2)]
 
 
 def kv_appended_close(gpu_kv: np.ndarray, ref_kv: np.ndarray, kv_init: np.ndarray) -> None:

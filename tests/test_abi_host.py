@@ -152,3 +152,24 @@ def test_sample_rejects_bad_arguments(dec, kw, msg):
     st = dec.lib.dec_sample(args["logits"], args["batch"], args["vocab"], prm, args["tokens"], None)
     assert st == dec.DEC_ERR_INVALID_ARG
     assert msg in dec.dec_last_error()
+
+
+@pytest.mark.parametrize("entry", ["dec_attention", "dec_attention_noalloc"])
+@pytest.mark.parametrize("kw,status,msg", [
+    (dict(tokens_per_seq=2), 2, "tokens_per_seq"),
+    (dict(kv_fmt=4), 1, "kv_fmt"),
+    (dict(kv_fmt=1, max_ctx=150), 2, "multiple of 16"),
+    (dict(head_dim=96), 2, "head_dim"),
+    (dict(n_q_heads=5, n_kv_heads=2), 1, "multiple"),
+])
+def test_attention_entry_points_reject_the_same_configs(dec, entry, kw, status, msg):
+    """dec_attention and dec_attention_noalloc share their config checks: a multi-token
+    config (whose rows the stand-alone kernels would read as separate sequences) and the
+    other unsupported shapes are refused by both, before any CUDA call."""
+    cfg = _cfg(dec, **kw)
+    if entry == "dec_attention":
+        st = dec.lib.dec_attention(ctypes.byref(cfg), 0, 16, 16, 16, 16, 16, 16, 256, 1 << 20, None)
+    else:
+        st = dec.lib.dec_attention_noalloc(ctypes.byref(cfg), 0, 16, 16, 16, 16, 16, 16, None)
+    assert st == status
+    assert msg in dec.dec_last_error()

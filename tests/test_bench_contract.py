@@ -36,3 +36,14 @@ def test_reference_arm_prints_one_contract_line():
 def test_warmup_is_at_least_three():
     d = _line("--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "1")
     assert d["warmup"] == 3
+
+
+def test_reference_arm_config_is_the_gpu_arms_config():
+    """Both arms print the same `config` object for a workload (the GPU arm builds it with
+    the same function and adds nothing to it), so the driver can pair the two lines."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+    import synthetic
+    d = _line("--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "3")
+    assert d["config"] == bench.workload_config(synthetic.WORKLOADS["tiny"], 1)
+    assert bench.DEFAULT_CONFIG == "qwen3-8b-b1"

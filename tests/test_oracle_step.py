@@ -15,9 +15,10 @@ def _bf(bits):
     return float(numerics.bf16_bits_to_f64(np.array([bits], dtype=np.uint16))[0])
 
 
-def _scalar_step(wl, model, kv, tokens, positions):
+def _scalar_step(wl, model, kv, tokens, positions, kv_out=None):
     """A second statement of the decode step with Python scalars and loops only
-    (no numpy linear algebra, no shared helper besides bf16 bit reading)."""
+    (no numpy linear algebra, no shared helper besides bf16 bit reading).  With kv_out,
+    the new token's bf16 K and V bits are also written at slot P of every layer there."""
     L, H, nq, nkv, d, I, V = (wl.n_layers, wl.hidden, wl.n_q_heads, wl.n_kv_heads, wl.head_dim,
                               wl.intermediate, wl.vocab)
     eps, theta = wl.rms_eps, wl.rope_theta
@@ -68,6 +69,9 @@ def _scalar_step(wl, model, kv, tokens, positions):
                 vals = [[_bf(x) for x in kv[l, 1, b, hk, t]] for t in range(P)]
                 keys.append([float(numerics.round_to_bf16(np.array(x))) for x in kh[hk]])
                 vals.append([float(numerics.round_to_bf16(np.array(x))) for x in vh[hk]])
+                if kv_out is not None and j % group == 0:
+                    kv_out[l, 0, b, hk, P] = numerics.f64_to_bf16_bits(np.array(kh[hk]))
+                    kv_out[l, 1, b, hk, P] = numerics.f64_to_bf16_bits(np.array(vh[hk]))
                 sc = [sum(qh[j][i] * key[i] for i in range(d)) / math.sqrt(d) for key in keys]
                 mx = max(sc)
                 ex = [math.exp(s - mx) for s in sc]
@@ -150,3 +154,58 @@ def test_step_sequences_are_independent():
         l1, a1 = oracle.decode_step(m1, kv1, npm["tokens"][b:b + 1], npm["positions"][b:b + 1])
         assert np.allclose(l1[0], logits[b], rtol=1e-13, atol=1e-13)
         assert np.array_equal(kv1[:, :, 0], kv[:, :, b])
+
+
+def _verify_case(fmt=synthetic.BF16):
+    wl = synthetic.custom(n_layers=2, hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, intermediate=128,
+                          vocab=40, weight_format=fmt, batch=2, prefill=5, steps=4, seed=21)
+    model = synthetic.generate(wl)
+    model["positions"][1] = 2  # ragged lengths
+    npm = _np_model(model)
+    rng = np.random.default_rng(5)
+    toks = rng.integers(0, wl.vocab, (2, 3)).astype(np.int32)
+    return wl, model, npm, toks
+
+
+@pytest.mark.parametrize("fmt", [synthetic.BF16, synthetic.AFFINE4_G64])
+def test_verify_step_matches_scalar_teacher_forcing(fmt):
+    """Row (b, t) of the verify step is the one-token step of sequence b at position P_b + t
+    after rows (b, 0..t-1) were appended: the scalar restatement, run row by row and
+    writing each row's K/V into its own cache copy, gives the same logits and cache."""
+    wl, model, npm, toks = _verify_case(fmt)
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    kv = npm["kv"].copy()
+    logits, am = oracle.verify_step(m, kv, toks, npm["positions"])
+    assert logits.shape == (2, 3, wl.vocab) and am.shape == (2, 3)
+    kv_s = npm["kv"].copy()
+    for t in range(3):
+        ref = _scalar_step(wl, npm, kv_s, toks[:, t], npm["positions"] + t, kv_out=kv_s)
+        assert np.allclose(logits[:, t], ref, rtol=1e-11, atol=1e-12), f"row {t}"
+        assert am[:, t].tolist() == [int(np.argmax(r)) for r in ref]
+    assert np.array_equal(kv, kv_s)
+    # slots P_b .. P_b + 2 written, nothing else
+    changed = np.argwhere(np.any(kv != npm["kv"], axis=-1))
+    for l, p, b, h, slot in changed:
+        assert npm["positions"][b] <= slot < npm["positions"][b] + 3
+
+
+def test_verify_step_rows_do_not_see_later_tokens():
+    """Causality inside the step: row t does not depend on the tokens of rows t+1 .. T-1."""
+    wl, model, npm, toks = _verify_case()
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    lg1, _ = oracle.verify_step(m, npm["kv"].copy(), toks, npm["positions"])
+    toks2 = toks.copy()
+    toks2[:, 2] = (toks2[:, 2] + 7) % wl.vocab
+    lg2, _ = oracle.verify_step(m, npm["kv"].copy(), toks2, npm["positions"])
+    assert np.array_equal(lg1[:, :2], lg2[:, :2])
+    assert not np.allclose(lg1[:, 2], lg2[:, 2])
+
+
+def test_verify_step_of_one_token_is_the_decode_step():
+    wl, model, npm, toks = _verify_case()
+    m = oracle.OracleModel.from_synthetic(wl, model)
+    kv1, kv2 = npm["kv"].copy(), npm["kv"].copy()
+    lg, am = oracle.verify_step(m, kv1, toks[:, :1], npm["positions"])
+    ref = _scalar_step(wl, npm, npm["kv"], toks[:, 0], npm["positions"], kv_out=kv2)
+    assert np.allclose(lg[:, 0], ref, rtol=1e-11, atol=1e-12)
+    assert np.array_equal(kv1, kv2)

@@ -9,11 +9,10 @@ stops at the first failure has already run every other test; it must also pass
 when run alone in a fresh process.
 """
 
-import numpy as np
 import pytest
 import torch
 
-from parity import ATTN_ATOL, ATTN_RTOL, attention_cfg, make_attention_case
+from parity import attention_cfg, make_attention_case
 
 pytestmark = pytest.mark.gpu
 
@@ -28,14 +27,32 @@ def dec():
     return d
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls(dec):
-    B, nq, nkv, d, max_ctx = 3, 16, 4, 128, 2100
+def _kv8_cache(seed, B, nkv, d, max_ctx, L=2):
+    """A flat affine 8-bit cache buffer (codes, then (scale, bias) pairs) with the synthetic
+    recipe's stored form."""
+    import synthetic
+    wl = synthetic.custom(name="noalloc", seed=seed, n_layers=L, n_kv_heads=nkv, n_q_heads=nkv, head_dim=d,
+                          batch=B, prefill=max_ctx - 1, steps=1, kv_format=synthetic.AFFINE8_G64)
+    assert wl.max_ctx == max_ctx
+    return synthetic.kv_buffer(synthetic.generate(wl, device="cuda")["kv"])
+
+
+@pytest.mark.parametrize("kv_fmt", [0, 1], ids=["bf16_cache", "affine8_cache"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(dec, kv_fmt):
+    """Both entry points run the same kernels on the same inputs: outputs and the appended
+    K/V must be identical bit for bit, on a first call and on a second call that appends the
+    next position (the fixed array then holds the first call's table)."""
+    B, nq, nkv, d, max_ctx = 3, 16, 4, 128, 2112
     positions = [1500, 37, 0]
     qkv, q_norm, k_norm, kv, pos = make_attention_case(77, B, nq, nkv, d, positions, max_ctx)
     cfg = attention_cfg(dec, B, nq, nkv, d, max_ctx)
+    cfg.kv_fmt = kv_fmt
+    if kv_fmt == 1:
+        kv = _kv8_cache(78, B, nkv, d, max_ctx)
+        assert kv.numel() == dec.dec_kv_cache_bytes(cfg)
     ws = torch.empty((dec.dec_attention_workspace_bytes(cfg),), dtype=torch.uint8, device="cuda")
     d_qkv, d_qn, d_kn, d_pos = (t.cuda() for t in (qkv, q_norm, k_norm, pos))
-    kv_a, kv_b = kv.cuda(), kv.cuda()
+    kv_a, kv_b = kv.cuda().clone(), kv.cuda().clone()
     s = torch.cuda.current_stream().cuda_stream
     for call in range(2):
         # the second call appends the next position of every sequence
@@ -47,9 +64,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dec):
         dec.dec_attention_noalloc(cfg, 1, d_qkv.data_ptr(), d_qn.data_ptr(), d_kn.data_ptr(), d_pos.data_ptr(),
                                   kv_b.data_ptr(), out_b.data_ptr(), s)
         torch.cuda.synchronize()
-        a, b = out_a.cpu().double().numpy(), out_b.cpu().double().numpy()
-        assert np.all(np.isfinite(b))
-        assert np.all(np.abs(a - b) <= ATTN_ATOL + ATTN_RTOL * np.abs(a)), f"call {call}"
+        assert torch.isfinite(out_b).all(), f"call {call}"
+        assert torch.equal(out_a, out_b), f"call {call}: outputs differ"
         assert torch.equal(kv_a, kv_b), f"call {call}: appended K/V differ"
 
 

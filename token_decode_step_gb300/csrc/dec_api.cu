@@ -38,6 +38,42 @@ void set_last_error(const char* fmt, ...) {
   vsnprintf(g_err, sizeof(g_err), fmt, ap);
   va_end(ap);
 }
+// Checks of a config for the stand-alone attention entry points (dec_attention and
+// dec_attention_noalloc share them, so that the two cannot drift apart).
+dec_status validate_attention_cfg(const dec_config* c, int layer) {
+  if (!c) {
+    set_last_error("config is NULL");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_layers < 1 || c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->max_ctx < 1 ||
+      layer < 0 || layer >= c->n_layers || !(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) {
+    set_last_error("attention: sizes must be positive, 0 <= layer < n_layers, rms_eps > 0, rope_theta > 1");
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->n_q_heads % c->n_kv_heads != 0) {
+    set_last_error("n_q_heads (%d) must be a multiple of n_kv_heads (%d)", c->n_q_heads, c->n_kv_heads);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->tokens_per_seq > 1) {
+    set_last_error("attention: the stand-alone entry points take tokens_per_seq 0 or 1");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  if (c->kv_fmt != DEC_KV_BF16 && c->kv_fmt != DEC_KV_AFFINE8_G64) {
+    set_last_error("attention: unknown kv_fmt %d", c->kv_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->kv_fmt == DEC_KV_AFFINE8_G64 && c->max_ctx % 16 != 0) {
+    set_last_error("attention: the affine 8-bit KV cache needs max_ctx to be a multiple of 16 (got %d)", c->max_ctx);
+    return DEC_ERR_UNSUPPORTED;
+  }
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if ((G != 1 && G != 2 && G != 4) || (c->head_dim != 64 && c->head_dim != 128)) {
+    set_last_error("attention: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
+    return DEC_ERR_UNSUPPORTED;
+  }
+  return DEC_OK;
+}
+
 }  // namespace dec
 
 #define DEC_CUDA(call)                                                                     \
@@ -302,9 +338,17 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   // a tool-less process pays a no-op call
   static const char* const kClassNames[DEC_K_COUNT] = {"embed", "qkv", "attention", "o_proj",
                                                        "gate_up", "down", "lm_head"};
+  // ranges still open when an error return leaves this function are popped by the guard
+  struct NvtxOpen {
+    int depth = 0;
+    ~NvtxOpen() {
+      for (; depth > 0; --depth) nvtxRangePop();
+    }
+  } nvtx_open;
   auto note = [&](int cls) {
     if (classes) classes->push_back(cls);
     nvtxRangePushA(kClassNames[cls]);
+    ++nvtx_open.depth;
   };
   auto check = [&](cudaError_t e, const char* what) -> dec_status {
     if (e != cudaSuccess) {
@@ -320,7 +364,10 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     return cudaEventRecord(h->events[2 * ev], stream);
   };
   auto ev_end = [&]() -> cudaError_t {
-    nvtxRangePop();
+    if (nvtx_open.depth > 0) {
+      nvtxRangePop();
+      --nvtx_open.depth;
+    }
     if (!classes) return cudaSuccess;
     cudaError_t e = cudaEventRecord(h->events[2 * ev + 1], stream);
     ++ev;
@@ -1113,39 +1160,6 @@ extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cac
 
 namespace {
 
-dec_status validate_attention_cfg(const dec_config* c, int layer) {
-  if (!c) {
-    set_err("config is NULL");
-    return DEC_ERR_INVALID_ARG;
-  }
-  if (c->n_layers < 1 || c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->max_ctx < 1 ||
-      layer < 0 || layer >= c->n_layers || !(c->rms_eps > 0.f) || !(c->rope_theta > 1.f)) {
-    set_err("attention: sizes must be positive, 0 <= layer < n_layers, rms_eps > 0, rope_theta > 1");
-    return DEC_ERR_INVALID_ARG;
-  }
-  if (c->n_q_heads % c->n_kv_heads != 0) {
-    set_err("n_q_heads (%d) must be a multiple of n_kv_heads (%d)", c->n_q_heads, c->n_kv_heads);
-    return DEC_ERR_INVALID_ARG;
-  }
-  if (c->tokens_per_seq > 1) {
-    set_err("attention: the stand-alone entry points take tokens_per_seq 0 or 1");
-    return DEC_ERR_UNSUPPORTED;
-  }
-  if (c->kv_fmt != DEC_KV_BF16 && c->kv_fmt != DEC_KV_AFFINE8_G64) {
-    set_err("attention: unknown kv_fmt %d", c->kv_fmt);
-    return DEC_ERR_INVALID_ARG;
-  }
-  if (c->kv_fmt == DEC_KV_AFFINE8_G64 && c->max_ctx % 16 != 0) {
-    set_err("attention: the affine 8-bit KV cache needs max_ctx to be a multiple of 16 (got %d)", c->max_ctx);
-    return DEC_ERR_UNSUPPORTED;
-  }
-  const int G = c->n_q_heads / c->n_kv_heads;
-  if ((G != 1 && G != 2 && G != 4) || (c->head_dim != 64 && c->head_dim != 128)) {
-    set_err("attention: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
-    return DEC_ERR_UNSUPPORTED;
-  }
-  return DEC_OK;
-}
 
 size_t attention_workspace_total(const dec_config* c) {
   return align_up(static_cast<size_t>(c->batch) * (c->head_dim / 2) * 8, 256);  // RoPE (cos, sin) table

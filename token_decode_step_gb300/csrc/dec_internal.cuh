@@ -223,8 +223,10 @@ __device__ __forceinline__ uint32_t float_order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
-  // larger value wins; among equal values the lower index wins (larger ~idx)
-  return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
+  // larger value wins; among equal values the lower index wins (larger ~idx).  -0 and +0
+  // compare equal as numbers, so -0 is keyed as +0 (adding +0 in round-to-nearest maps -0
+  // to +0 and leaves every other value, NaN included, as it is).
+  return (static_cast<unsigned long long>(float_order_key(__fadd_rn(v, 0.0f))) << 32) |
          static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(idx));
 }
 __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
@@ -364,5 +366,9 @@ cudaError_t launch_advance(cudaStream_t s, const int32_t* argmax, int32_t* token
 
 // Record the message returned by dec_last_error() on this thread.
 void set_last_error(const char* fmt, ...);
+
+// Argument checks of the stand-alone attention entry points (config limits, layer range,
+// tokens_per_seq 0 or 1, kv_fmt); sets the last error and returns its status.
+dec_status validate_attention_cfg(const dec_config* c, int layer);
 
 }  // namespace dec

@@ -54,30 +54,10 @@ dec_status setup_device(int dev, unsigned char** addr) {
 extern "C" dec_status dec_attention_noalloc(const dec_config* cfg, int layer, const float* qkv, const void* q_norm,
                                             const void* k_norm, const int32_t* positions, void* kv_cache, float* out,
                                             dec_stream_t stream) {
-  if (!cfg) {
-    set_last_error("dec_attention_noalloc: config is NULL");
-    return DEC_ERR_INVALID_ARG;
-  }
+  // the same config checks as dec_attention (tokens_per_seq > 1 included)
+  dec_status vst = validate_attention_cfg(cfg, layer);
+  if (vst != DEC_OK) return vst;
   const dec_config& c = *cfg;
-  if (c.n_layers < 1 || c.batch < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.max_ctx < 1 || layer < 0 ||
-      layer >= c.n_layers || !(c.rms_eps > 0.f) || !(c.rope_theta > 1.f) || c.n_q_heads % c.n_kv_heads != 0) {
-    set_last_error("dec_attention_noalloc: sizes must be positive, 0 <= layer < n_layers, rms_eps > 0, "
-                   "rope_theta > 1, n_q_heads a multiple of n_kv_heads");
-    return DEC_ERR_INVALID_ARG;
-  }
-  const int G = c.n_q_heads / c.n_kv_heads;
-  if ((G != 1 && G != 2 && G != 4) || (c.head_dim != 64 && c.head_dim != 128)) {
-    set_last_error("dec_attention_noalloc: head_dim must be 64 or 128 and n_q_heads/n_kv_heads 1, 2 or 4");
-    return DEC_ERR_UNSUPPORTED;
-  }
-  if (c.kv_fmt != DEC_KV_BF16 && c.kv_fmt != DEC_KV_AFFINE8_G64) {
-    set_last_error("dec_attention_noalloc: unknown kv_fmt %d", c.kv_fmt);
-    return DEC_ERR_INVALID_ARG;
-  }
-  if (c.kv_fmt == DEC_KV_AFFINE8_G64 && c.max_ctx % 16 != 0) {
-    set_last_error("dec_attention_noalloc: the affine 8-bit KV cache needs max_ctx to be a multiple of 16");
-    return DEC_ERR_UNSUPPORTED;
-  }
   if (!qkv || !q_norm || !k_norm || !positions || !kv_cache || !out ||
       (reinterpret_cast<uintptr_t>(kv_cache) & 15u)) {
     set_last_error("dec_attention_noalloc: NULL pointer or kv_cache not 16-byte aligned");
