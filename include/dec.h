@@ -220,6 +220,20 @@ DEC_API dec_status dec_debug_gemm_tc5(const void *x_hl, int M, const void *w, in
    context stay usable.  No GPU fault or trap is involved. */
 DEC_API dec_status dec_debug_force_timeout(dec_handle *h, int polls, dec_stream_t stream);
 
+/* Test hook: the tensor-core projection kernel of batched decode steps with affine 4-bit weights
+   (tcgen05.mma on dequantized weight tiles, TMA operands, the accumulator in tensor memory) on
+   caller buffers, plain store epilogue:
+     out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) * w[n][k],  w = fl(scale * q + bias) per group of 64.
+     x_hl      device bf16 [2][M][K] (plane 0 hi, plane 1 lo), 16-byte aligned, M in 1..32
+     codes     device uint32 [N][K/8] (element 8 j + k in bits 4k..4k+3 of word j), 16-byte aligned
+     sb        device uint32 [N][K/64]: bf16 scale bits | bf16 bias bits << 16, 16-byte aligned
+     out       device float [M][N]
+     S         K splits (dividing K / 64); S > 1 needs partials (device float [S][M][N]) and
+               counters (device uint32 [ceil(N / 128) + 1], zero, left zero)
+   K a positive multiple of 64, N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
+DEC_API dec_status dec_debug_gemm_q4tc(const void *x_hl, int M, const void *codes, const void *sb, int N, int K,
+                    int S, float *out, float *partials, unsigned *counters, dec_stream_t stream);
+
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:
    mn, mx = min, max; scale = bf16(fl(fl(mx - mn) / 255)); bias = bf16(mn) (round to

@@ -110,6 +110,11 @@ CUSTOM_BATCHED = [
                            n_layers=1)),
     ("b8_bf16_long_k", dict(batch=8, prefill=(50, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=4096,
                             intermediate=6144, vocab=700, steps=2, n_layers=1)),
+    # 4-bit, hidden >= 2048, at most 32 rows: the tcgen05 path over dequantized weight tiles
+    ("b3_q4_tc5", dict(batch=3, weight_format=synthetic.AFFINE4_G64, prefill=(0, 200), head_dim=128, n_q_heads=8,
+                       n_kv_heads=2, hidden=2048, intermediate=2880, vocab=1234, steps=2, n_layers=2)),
+    ("b20_q4_tc5", dict(batch=20, weight_format=synthetic.AFFINE4_G64, prefill=(5, 600), head_dim=64, n_q_heads=16,
+                        n_kv_heads=4, hidden=2048, intermediate=5632, vocab=3001, steps=2, n_layers=1)),
 ]
 
 
@@ -190,11 +195,13 @@ def test_repeated_step_is_deterministic(glue):
     assert torch.equal(res[0], res[1]) and torch.equal(res[0], res[2])
 
 
-@pytest.mark.parametrize("batch", [1, 6])
+@pytest.mark.parametrize("batch,hidden", [(1, 192), (6, 192), (4, 2048)])
 @pytest.mark.parametrize("fmt", [synthetic.BF16, synthetic.AFFINE4_G64])
-def test_debug_dequant_bit_exact(glue, fmt, batch):
+def test_debug_dequant_bit_exact(glue, fmt, batch, hidden):
+    """Every packing (batch 1; batched mma.sync fragments; at hidden 2048 the 4-bit batched
+    tcgen05 path's row-major packing) reads back the caller's weights bit for bit."""
     from oracle import affine4, numerics
-    wl = synthetic.custom(name="dq", weight_format=fmt, head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=192,
+    wl = synthetic.custom(name="dq", weight_format=fmt, head_dim=64, n_q_heads=4, n_kv_heads=2, hidden=hidden,
                           intermediate=320, vocab=200, n_layers=2, batch=batch)
     model = synthetic.generate(wl, device="cuda", with_kv=False)
     host = np_model(synthetic.to_host(model))

@@ -1,0 +1,61 @@
+"""The batched-decode projection kernel for affine 4-bit weights on tcgen05
+(dec_debug_gemm_q4tc, plain store epilogue) against an fp64 product of the same inputs, the
+weights dequantized by the oracle (fl(scale * q + bias), float32): ragged token counts and
+weight-row tiles, K splits, more groups than the stage rings hold."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dec():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from token_decode_step_gb300 import build
+    build.build()
+    from token_decode_step_gb300 import dec as d
+    return d
+
+
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("M,N,K,S", [(32, 128, 64, 1), (32, 256, 1024, 2), (8, 200, 512, 1), (17, 1000, 2560, 5),
+                                     (1, 130, 384, 3), (32, 6144, 4096, 8), (32, 4096, 12288, 4)])
+def test_q4tc_gemm_matches_fp64(dec, M, N, K, S):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(M * 7 + N + K + S)
+    x = torch.randn((M, K), generator=g, dtype=torch.float64)
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.double()).to(torch.bfloat16)
+    words = torch.randint(-(2 ** 31), 2 ** 31, (N, K // 8), generator=g, dtype=torch.int64).to(torch.int32)
+    scales = _bf16_bits(torch.rand((N, K // 64), generator=g) * 0.009 + 0.001)
+    biases = _bf16_bits(torch.randn((N, K // 64), generator=g) * 0.02)
+    w = oracle.dequant_affine4_g64_f32(words.numpy().view(np.uint32), scales, biases).astype(np.float64)
+    sb = scales.astype(np.uint32) | (biases.astype(np.uint32) << 16)
+
+    xhl = torch.stack([hi, lo]).contiguous().cuda()
+    wd = words.contiguous().cuda()
+    sbd = torch.from_numpy(sb.view(np.int32)).contiguous().cuda()
+    out = torch.full((M, N), float("nan"), device="cuda")
+    partials = torch.empty((S, M, N), device="cuda") if S > 1 else None
+    counters = torch.zeros(((N + 127) // 128 + 1,), dtype=torch.int32, device="cuda") if S > 1 else None
+    dec.dec_debug_gemm_q4tc(xhl.data_ptr(), M, wd.data_ptr(), sbd.data_ptr(), N, K, S, out.data_ptr(),
+                            partials.data_ptr() if S > 1 else None, counters.data_ptr() if S > 1 else None,
+                            torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    xs = (hi.double() + lo.double()).numpy()
+    ref = xs @ w.T
+    bound = np.abs(xs) @ np.abs(w).T  # the products' magnitudes: the weights' hi/lo split is ~2^-16 relative
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all(), "unwritten outputs"
+    err = np.abs(got - ref)
+    assert np.all(err <= 4e-5 * bound + 1e-6), f"max err {float(err.max()):.3e} (rel {float((err / bound).max()):.3e})"
+    if S > 1:
+        assert int(counters.abs().sum()) == 0, "split counters not left zero"

@@ -134,6 +134,11 @@ struct dec_handle {
   // TMA tensor maps of the three activation hi/lo planes (inputs of QKV / gate_up / lm_head,
   // of O, of down)
   bool umma = false;
+  // batched decode (2..32 rows) with 4-bit weights on models of hidden >= 2048: tcgen05 over
+  // dequantized weight tiles; the weights stay in the batch-1 row-major packing, read by TMA
+  // (the codes) and plain loads (scale and bias); the activation maps (map_u, map_o, map_g)
+  // have 32-row boxes
+  bool q4tc = false;
   alignas(64) unsigned char map_u[128] = {}, map_o[128] = {}, map_g[128] = {};
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
@@ -467,6 +472,28 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       up.status = h->status;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
       s2 = check(launch_gemm_umma(lc, mx, L.tmap, up, in_mode, epi), what);
+    } else if (h->q4tc) {
+      Q4tcParams qp{};
+      qp.M = h->rows;
+      qp.N = L.N;
+      qp.K = L.K;
+      qp.S = L.S;
+      qp.ctas = h->num_sms;
+      qp.sb = L.sb;
+      qp.sumsq_in = h->sumsq;
+      qp.n_sumsq_in = H / kResGroup;
+      qp.eps = c.rms_eps;
+      qp.out = out;
+      qp.sumsq_out = h->sumsq;
+      qp.xhl_out = xout;
+      qp.next_norm_w = next_norm;
+      qp.partials = h->gemv_partials;
+      qp.counters = h->gemv_counters;
+      qp.amax_key = h->amax_key;
+      qp.argmax_out = sp.argmax;
+      qp.status = h->status;
+      const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
+      s2 = check(launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi), what);
     } else if (h->rows == 1) {
       s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
@@ -719,7 +746,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // below that (the 0.6B shapes) the token-blocked mma.sync kernel's many small CTAs fill the
   // GPU better (512-token chunk: 14.2 ms against 16.2 ms, measured)
   h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16 && H >= 2048;
-  const bool frag = tc && !h->umma;  // fragment-packed weights for the mma.sync path
+  h->q4tc = tc && h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
+  const bool frag = tc && !h->umma && !h->q4tc;  // fragment-packed weights for the mma.sync path
   auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
@@ -749,7 +777,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       L.w = take(L.w_bytes);
       return L;
     }
-    L.S = h->umma ? 1 : choose_splits(N, K, fmt, h->num_sms);
+    L.S = h->umma ? 1 : h->q4tc ? q4tc_splits(N, K, h->num_sms) : choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
       L.w_bytes = static_cast<size_t>(N) * K * 2;
       L.w = take(L.w_bytes);
@@ -914,6 +942,22 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       for (int tn : {128, 256})
         if ((e = prepare_gemm_umma(cb[0], cb[1], tn)) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
   }
+  if (h->q4tc) {  // TMA maps of every weight's codes and of the activation planes, kernel attributes
+    auto cmap = [&](PackedLinear& L) { return q4tc_code_map(L.tmap, L.w, L.N, L.K); };
+    if ((e = cmap(h->lm_head)) != cudaSuccess) return fail("tensor map", e);
+    for (auto& L : h->layers)
+      if ((e = cmap(L.qkv)) != cudaSuccess || (e = cmap(L.o)) != cudaSuccess || (e = cmap(L.gateup)) != cudaSuccess ||
+          (e = cmap(L.down)) != cudaSuccess)
+        return fail("tensor map", e);
+    const int tok = q4tc_max_tokens();
+    if ((e = umma_tensor_map(h->map_u, h->xh_u, 2 * h->rows, H, tok)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_o, h->xh_o, 2 * h->rows, nq * d, tok)) != cudaSuccess ||
+        (e = umma_tensor_map(h->map_g, h->xh_g, 2 * h->rows, I, tok)) != cudaSuccess)
+      return fail("tensor map", e);
+    const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
+    for (auto& cb : combos)
+      if ((e = prepare_gemm_q4tc(cb[0], cb[1])) != cudaSuccess) return fail("tcgen05 4-bit kernel attributes", e);
+  }
   if (frag) {
     GemmParams gp{};
     gp.B = h->rows;
@@ -1038,7 +1082,7 @@ extern "C" dec_status dec_get_device_status(dec_handle* h, int* out) {
 
 namespace {
 // rows per gate (then up) block of the packed gate/up projection
-int gate_up_block(const dec_handle* h) { return h->umma ? 16 : h->rows > 1 ? 8 : kGemvRows / 2; }
+int gate_up_block(const dec_handle* h) { return h->umma ? 16 : h->rows > 1 && !h->q4tc ? 8 : kGemvRows / 2; }
 }  // namespace
 
 extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, float* out, dec_stream_t stream) {
@@ -1067,7 +1111,7 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  if (h->rows > 1 && !h->umma) {
+  if (h->rows > 1 && !h->umma && !h->q4tc) {
     DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
   } else {
     DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
@@ -1235,6 +1279,39 @@ extern "C" dec_status dec_debug_gemm_tc5(const void* x_hl, int M, const void* w,
   p.m_tiles = (M + umma_tokens_per_tile() - 1) / umma_tokens_per_tile();
   p.out = out;
   DEC_CUDA(launch_gemm_umma(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mw, p, kInPlain, kEpiStore));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_debug_gemm_q4tc(const void* x_hl, int M, const void* codes, const void* sb, int N, int K,
+                                          int S, float* out, float* partials, unsigned* counters,
+                                          dec_stream_t stream) {
+  g_err[0] = 0;
+  if (!x_hl || !codes || !sb || !out || M < 1 || M > q4tc_max_tokens() || N < 1 || K < 64 || K % 64 != 0 || S < 1 ||
+      (K / 64) % S != 0 || (S > 1 && (!partials || !counters)) || !aligned16(x_hl) || !aligned16(codes) ||
+      !aligned16(sb)) {
+    set_err("dec_debug_gemm_q4tc: NULL or misaligned pointer, M outside 1..%d, N < 1, K not a positive multiple of "
+            "64, or S not dividing K / 64 (S > 1 needs partials and counters)",
+            q4tc_max_tokens());
+    return DEC_ERR_INVALID_ARG;
+  }
+  alignas(64) unsigned char mx[128], mc[128];
+  int dev = 0, sms = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K, q4tc_max_tokens()));
+  DEC_CUDA(q4tc_code_map(mc, codes, N, K));
+  DEC_CUDA(prepare_gemm_q4tc(kInPlain, kEpiStore));
+  Q4tcParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.S = S;
+  p.ctas = sms;
+  p.sb = static_cast<const uint32_t*>(sb);
+  p.out = out;
+  p.partials = partials;
+  p.counters = counters;
+  DEC_CUDA(launch_gemm_q4tc(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mc, p, kInPlain, kEpiStore));
   return DEC_OK;
 }
 

@@ -103,6 +103,27 @@ struct UmmaParams {
   unsigned* status;                  // time-out flag (may be null)
 };
 
+// Batched decode projections of 4-bit weights on tcgen05 (k_gemm_q4tc.cu): Y[M][N] = X W^T for
+// M <= 32 token rows; X as bf16 hi, lo planes [2][M][K] read through a TMA tensor map (boxes of
+// 32 rows), W as row-major codes [N][K/2] bytes (a TMA tensor map) and sb words [N][K/64].
+struct Q4tcParams {
+  int M, N, K, S;           // tokens (<= 32), weight rows, inputs (multiple of 64), K splits (dividing K / 64)
+  int ctas;                 // persistent CTAs (one per SM)
+  const uint32_t* sb;       // (scale | bias << 16) [N][K/64]
+  const float* sumsq_in;    // norm inputs: [M][n_sumsq_in] partial sums of squares of the residual
+  int n_sumsq_in;
+  float eps;
+  float* out;               // store / lmhead: [M][N] (lmhead: may be null); resid: h [M][N] (+=); swiglu: g [M][N/2]
+  float* sumsq_out;         // resid: [M][N / kResGroup]
+  __nv_bfloat16* xhl_out;   // resid: h * next_norm_w, swiglu: g, as hi, lo planes
+  const __nv_bfloat16* next_norm_w;  // resid: [N]
+  float* partials;          // [S][M][N] when S > 1
+  unsigned* counters;       // [ceil(N / 128) + 1], zero on entry, left zero
+  unsigned long long* amax_key;      // lmhead: [M]
+  int32_t* argmax_out;               // lmhead: [M]
+  unsigned* status;                  // time-out flag (may be null)
+};
+
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
 struct AttnParams {
   Timeline tl;
@@ -306,6 +327,12 @@ cudaError_t umma_tensor_map(void* map128, const void* ptr, int rows, int K, int 
 cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* map_w, const UmmaParams& p,
                              int in_mode, int epi);
 cudaError_t prepare_gemm_umma(int in_mode, int epi, int tile_n);
+int q4tc_max_tokens();
+int q4tc_splits(int N, int K, int num_sms);
+cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K);  // CUtensorMap (128 B)
+cudaError_t launch_gemm_q4tc(const LaunchCtx& c, const void* map_x, const void* map_codes, const Q4tcParams& p,
+                             int in_mode, int epi);
+cudaError_t prepare_gemm_q4tc(int in_mode, int epi);
 size_t attention_smem_bytes(int head_dim);
 // set the dynamic smem limits and record the shapes' occupancy (before capture)
 cudaError_t prepare_attention(int head_dim, int G, int kv_fmt);

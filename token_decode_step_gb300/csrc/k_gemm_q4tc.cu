@@ -1,0 +1,488 @@
+// Batched decode projections with affine 4-bit weights on the fifth-generation tensor cores:
+// Y[t][n] = sum_k X[t][k] W[n][k] for up to 32 token rows, W = scale * q + bias per group of
+// 64 inputs (q in 0..15, eight per uint32, one bf16 scale and bias per group).
+//
+// Sources: oxinfer crate page, "MLX checkpoints" (the affine 4-bit format); Butter
+// architecture.md, "SINGLE-TOKEN DECODE" (the projection sequence, here over a batch of
+// independent sequences).
+//
+// The 128 weight rows of a tile are the accumulator's lanes (the MMA's M) and the 32 tokens'
+// bf16 hi and lo activation rows its 64 columns (N): the MMAs of a group of 64 inputs take the
+// weight tile as A and the activation tile as B, both K-major in the 128-byte swizzle.
+// Dequantizer warps turn each group's codes into the float32 weights fl(scale * q + bias) (the
+// format's exact values) and store them as bf16 hi and lo planes (w = hi + lo to ~16
+// significant bits), so a group takes two MMAs per 16 inputs (hi plane, lo plane) into one
+// accumulator; a token's result is the sum of its hi and lo columns.
+//
+// Warp roles (one persistent CTA per SM, 448 threads): warp 0 issues the TMA copies of the
+// codes (128 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
+// warp 1 allocates two 64-column accumulators and issues the MMAs; warps 2..9 dequantize (two
+// threads per weight row, 32 inputs each); warps 10..13 read the accumulator and run the
+// fused epilogue, so the epilogue of one unit overlaps the MMAs of the next.  A unit is a
+// (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile adds the S
+// partial results in split order (deterministic).  Every wait on a barrier is bounded: on
+// time-out the kernel flags the status word and stops.
+#include "q4.cuh"
+#include "umma_common.cuh"
+
+namespace dec {
+
+namespace {
+
+using namespace umma;
+
+constexpr int kQM = 128;                   // weight rows per tile
+constexpr int kQT = 32;                    // token rows (accumulator columns 0..31 hi, 32..63 lo)
+constexpr int kQK = 64;                    // inputs per stage: one group of the format
+constexpr int kQStages = 6;                // TMA ring: codes + activations
+constexpr int kQAStages = 3;               // dequantized weight ring
+constexpr int kQCode = kQM * kQK / 2;      // 4 KB: 128 rows x 32 bytes of codes
+constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
+constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
+constexpr int kQPlane = kQM * kQK * 2;     // 16 KB: one bf16 plane of the weight tile
+constexpr int kQA = 2 * kQPlane;           // hi plane, lo plane
+constexpr int kQDeq = 256;                 // dequantizer threads
+constexpr int kQThreads = 448;
+constexpr int kQOffS = kQAStages * kQA;
+constexpr int kQOffBar = kQOffS + kQStages * kQStage;
+constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 4;
+constexpr int kQOffTmem = kQOffBar + 8 * kQBars;
+constexpr int kQOffInv = kQOffTmem + 16;
+constexpr int kQOffBest = kQOffInv + 4 * kQT;
+constexpr int kQOffTicket = kQOffBest + 8 * kQT;
+constexpr int kQSmem = 1024 + kQOffTicket + 16;
+// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
+constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0, "smem layout");
+
+__device__ __forceinline__ float silu_q(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void split_hl_q(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// Codes of one word (element 8 j + k in bits 4k..4k+3) -> 8 weights w = fl(s q + b) as bf16
+// hi and lo pairs (element 2i in the low half of pair i).  The byte permute puts a code into
+// bits 16..19 of 128.0f (giving 128 + q exactly); q = (128 + q) - 128 is exact.
+__device__ __forceinline__ void dequant_word(uint32_t w, float s, float b, uint4& hi, uint4& lo) {
+  const uint32_t ev = w & 0x0f0f0f0fu, od = (w >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
+  constexpr uint32_t kMagic = 0x43000000u;
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t sel = 0x7044u | (static_cast<uint32_t>(i) << 8);
+    const float q0 = __uint_as_float(__byte_perm(ev, kMagic, sel)) - 128.0f;
+    const float q1 = __uint_as_float(__byte_perm(od, kMagic, sel)) - 128.0f;
+    const float w0 = fmaf(s, q0, b), w1 = fmaf(s, q1, b);
+    const __nv_bfloat162 hp = __floats2bfloat162_rn(w0, w1);  // .x = w0 (low half)
+    const float2 hf = __bfloat1622float2(hp);
+    const __nv_bfloat162 lp = __floats2bfloat162_rn(w0 - hf.x, w1 - hf.y);
+    h[i] = *reinterpret_cast<const uint32_t*>(&hp);
+    l[i] = *reinterpret_cast<const uint32_t*>(&lp);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+}  // namespace
+
+template <int IN, int EPI>
+__global__ void __launch_bounds__(kQThreads, 1)
+    k_gemm_q4tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c, Q4tcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t sA = base, sS = base + kQOffS;
+  const uint32_t st_full = base + kQOffBar, st_empty = st_full + 8 * kQStages;
+  const uint32_t a_full = st_empty + 8 * kQStages, a_empty = a_full + 8 * kQAStages;
+  const uint32_t t_full = a_empty + 8 * kQAStages, t_empty = t_full + 16;
+  const uint32_t tmem_slot = base + kQOffTmem;
+  float* s_inv = reinterpret_cast<float*>(smem + kQOffInv);
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + kQOffBest);
+  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + kQOffTicket);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = (p.N + kQM - 1) / kQM;
+  const int units = n_tiles * p.S;
+  const int gps = p.K / kQK / p.S;  // groups per split
+
+  if (warp == 1) {  // two accumulators of 64 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(128)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(st_full + 8 * s, 1);
+      mbar_init(st_empty + 8 * s, kQDeq + 1);  // the dequantizers' reads, then the MMAs' commit
+    }
+    for (int s = 0; s < kQAStages; ++s) {
+      mbar_init(a_full + 8 * s, kQDeq);
+      mbar_init(a_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(t_full + 8 * b, 1);
+      mbar_init(t_empty + 8 * b, 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (tid < kQT) s_best[tid] = 0ull;
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kQOffTmem);
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer; stage i of this CTA is group i % gps of its unit i / gps
+      const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      const int total = my_units * gps;
+      auto group_of = [&](int i, int& tile, int& g) {
+        const int u = blockIdx.x + (i / gps) * gridDim.x;
+        tile = u % n_tiles;
+        g = (u / n_tiles) * gps + i % gps;
+      };
+      // the codes do not depend on upstream kernels: the first stages' are requested before
+      // the grid-dependency wait, their activations after it
+      const int pre = total < kQStages ? total : kQStages;
+      for (int i = 0; i < pre; ++i) {
+        int tile, g;
+        group_of(i, tile, g);
+        const uint32_t full = st_full + 8 * i, st = sS + i * kQStage;
+        mbar_expect_tx(full, kQStage);
+        tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
+      }
+      griddep_wait();
+      for (int i = 0; i < total; ++i) {
+        int tile, g;
+        group_of(i, tile, g);
+        const int s = i % kQStages;
+        const uint32_t full = st_full + 8 * s, st = sS + s * kQStage;
+        if (i >= pre) {
+          if (!mbar_wait(st_empty + 8 * s, ((i / kQStages) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full, kQStage);
+          tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
+        }
+        tma_load_2d(st, &tm_x, g * kQK, 0, full);                // hi plane: tokens 0..31
+        tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);    // lo plane
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      int it = 0, local = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+        const int b = local & 1;
+        if (local >= 2 && !mbar_wait(t_empty + 8 * b, ((local >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t acc = tmem + 64 * b;
+        for (int j = 0; j < gps; ++j, ++it) {
+          const int s = it % kQStages, a = it % kQAStages;
+          if (!mbar_wait(a_full + 8 * a, (it / kQAStages) & 1) || !mbar_wait(st_full + 8 * s, (it / kQStages) & 1)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint64_t dx = sw128_desc(sS + s * kQStage);
+          const uint64_t dh = sw128_desc(sA + a * kQA), dl = sw128_desc(sA + a * kQA + kQPlane);
+#pragma unroll
+          for (int k = 0; k < kQK / 16; ++k) {  // 16 inputs = 32 bytes further along the swizzled rows
+            mma_bf16(acc, dh + 2 * k, dx + 2 * k, kQIdesc, (j | k) != 0 ? 1u : 0u);
+            mma_bf16(acc, dl + 2 * k, dx + 2 * k, kQIdesc, 1u);
+          }
+          commit(a_empty + 8 * a);
+          commit(st_empty + 8 * s);
+        }
+        if (!ok) break;
+        commit(t_full + 8 * b);
+      }
+    }
+  } else if (warp < 10) {  // dequantizers: weight row r of the tile, inputs 32 h .. 32 h + 31 of a group
+    const int dt = tid - 64, r = dt & (kQM - 1), h = dt >> 7;
+    int it = 0;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int tile = u % n_tiles, split = u / n_tiles;
+      const int row = tile * kQM + r;
+      const uint32_t* sbrow = p.sb + static_cast<size_t>(row < p.N ? row : 0) * (p.K / kGroup);
+      for (int j = 0; j < gps; ++j, ++it) {
+        const int s = it % kQStages, a = it % kQAStages;
+        const uint32_t sbw = __ldg(sbrow + split * gps + j);  // eight groups share a 32-byte sector
+        if (!mbar_wait(st_full + 8 * s, (it / kQStages) & 1)) {
+          ok = false;
+          break;
+        }
+        uint4 cw;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                     : "r"(sS + s * kQStage + kQX + r * 32 + h * 16));
+        mbar_arrive(st_empty + 8 * s);
+        if (it >= kQAStages && !mbar_wait(a_empty + 8 * a, ((it / kQAStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const float sc = sb_scale(sbw), bi = sb_bias(sbw);
+        const uint32_t arow = sA + a * kQA + r * 128;
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // word i = 16-byte chunk 4 h + i of the row
+          uint4 hv, lv;
+          dequant_word(words[i], sc, bi, hv, lv);
+          const uint32_t off = static_cast<uint32_t>(((4 * h + i) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + off), "r"(hv.x), "r"(hv.y), "r"(hv.z),
+                       "r"(hv.w)
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + kQPlane + off), "r"(lv.x), "r"(lv.y),
+                       "r"(lv.z), "r"(lv.w)
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
+        mbar_arrive(a_full + 8 * a);
+      }
+    }
+  } else {  // epilogue warps 10..13: accumulator lanes 32 q .. 32 q + 31, q = warp % 4
+    const int et = tid - 320, q = warp & 3, r = 32 * q + lane;
+    const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
+    griddep_wait();  // the residual and the sums of squares are upstream outputs
+    if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
+      for (int i = 0; i < kQT / 4; ++i) {
+        const int t = (warp - 10) * (kQT / 4) + i;
+        float sacc = 0.f;
+        if (t < p.M)
+          for (int k = lane; k < p.n_sumsq_in; k += 32) sacc += p.sumsq_in[static_cast<size_t>(t) * p.n_sumsq_in + k];
+        sacc = warp_sum(sacc);
+        if (lane == 0) s_inv[t] = t < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
+      }
+    }
+    epi_sync();
+    int local = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+      const int tile = u % n_tiles, split = u / n_tiles, b = local & 1;
+      if (ok && !mbar_wait(t_full + 8 * b, (local >> 1) & 1)) ok = false;
+      fence_after();
+      float y[kQT], yl[kQT];
+      tmem_ld32(tmem + 64 * b + tq, y);        // hi columns: tokens 0..31
+      tmem_ld32(tmem + 64 * b + 32 + tq, yl);  // lo columns
+      fence_before();
+      mbar_arrive(t_empty + 8 * b);
+#pragma unroll
+      for (int t = 0; t < kQT; ++t) y[t] += yl[t];
+      const int n = tile * kQM + r;
+      const bool live = ok && n < p.N;
+      if (p.S > 1) {  // partial results; the last CTA of the tile adds them in split order
+        if (live) {
+#pragma unroll
+          for (int t = 0; t < kQT; ++t)
+            if (t < p.M) p.partials[(static_cast<size_t>(split) * p.M + t) * p.N + n] = y[t];
+        }
+        __threadfence();
+        epi_sync();
+        if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
+        epi_sync();
+        if (*s_ticket != static_cast<unsigned>(p.S - 1)) continue;
+        __threadfence();
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) y[t] = 0.f;
+        if (live)
+          for (int s = 0; s < p.S; ++s)
+#pragma unroll
+            for (int t = 0; t < kQT; ++t)
+              if (t < p.M) y[t] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t) * p.N + n);
+        if (et == 0) p.counters[tile] = 0u;
+      }
+      if constexpr (IN == kInNorm) {
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) y[t] *= s_inv[t];
+      }
+      if constexpr (EPI == kEpiStore) {
+        if (live) {
+#pragma unroll
+          for (int t = 0; t < kQT; ++t)
+            if (t < p.M) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
+        }
+      } else if constexpr (EPI == kEpiResid) {
+        // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per
+        // 8 rows (lanes 8 j .. 8 j + 7; N is a multiple of 8, so all of them are live or none)
+        const float nw = live ? bf16_to_f(p.next_norm_w[n]) : 0.f;
+        const size_t plane = static_cast<size_t>(p.M) * p.N;
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) {
+          float hn = 0.f;
+          const bool on = live && t < p.M;
+          if (on) {
+            const size_t o = static_cast<size_t>(t) * p.N + n;
+            hn = p.out[o] + y[t];
+            p.out[o] = hn;
+            __nv_bfloat16 hi, lo;
+            split_hl_q(hn * nw, hi, lo);
+            p.xhl_out[o] = hi;
+            p.xhl_out[plane + o] = lo;
+          }
+          float ss = hn * hn;
+          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+          ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+          ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+          if (on && (lane & 7) == 0) p.sumsq_out[static_cast<size_t>(t) * (p.N / kResGroup) + n / kResGroup] = ss;
+        }
+      } else if constexpr (EPI == kEpiSwiglu) {
+        // packed rows in blocks of 4: rows 8 j .. 8 j + 3 gate outputs 4 j .. 4 j + 3, the
+        // next 4 rows the matching up outputs (lane ^ 4)
+        const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
+        const int o = (n >> 3) * 4 + (n & 3);
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) {
+          const float up = __shfl_xor_sync(0xffffffffu, y[t], 4);
+          if (live && (n & 4) == 0 && t < p.M) {
+            const float gv = silu_q(y[t]) * up;
+            const size_t oo = static_cast<size_t>(t) * (p.N / 2) + o;
+            p.out[oo] = gv;
+            __nv_bfloat16 hi, lo;
+            split_hl_q(gv, hi, lo);
+            p.xhl_out[oo] = hi;
+            p.xhl_out[plane + oo] = lo;
+          }
+        }
+      } else {  // lm_head: logits, and every token's best (value, index) key over the warp's rows
+#pragma unroll
+        for (int t = 0; t < kQT; ++t) {
+          const bool on = live && t < p.M;
+          if (on && p.out) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
+          unsigned long long k = on ? argmax_key(y[t], n) : 0ull;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+            k = other > k ? other : k;
+          }
+          if (lane == 0 && k != 0ull) atomicMax(s_best + t, k);
+        }
+      }
+    }
+    if constexpr (EPI == kEpiLmHead) {
+      epi_sync();
+      if (et < p.M && s_best[et] != 0ull) atomicMax(p.amax_key + et, s_best[et]);
+    }
+  }
+  griddep_launch_dependents();
+  fence_before();
+  __syncthreads();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
+  if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
+  if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
+    __threadfence();
+    if (tid == 0) *s_ticket = atomicAdd(&p.counters[n_tiles], 1u);
+    __syncthreads();
+    if (*s_ticket == gridDim.x - 1) {
+      __threadfence();
+      for (int b = tid; b < p.M; b += kQThreads) p.argmax_out[b] = argmax_key_index(atomicOr(p.amax_key + b, 0ull));
+      if (tid == 0) p.counters[n_tiles] = 0u;
+    }
+  }
+}
+
+namespace {
+
+using EncodeTiledQ = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledQ encoder_q() {
+  static EncodeTiledQ fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledQ>(ptr);
+  }
+  return fn;
+}
+
+template <int IN, int EPI>
+cudaError_t launch_q4tc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mc, const Q4tcParams& p,
+                          bool prepare) {
+  if (prepare)
+    return cudaFuncSetAttribute(k_gemm_q4tc<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  const int units = ((p.N + kQM - 1) / kQM) * p.S;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units < p.ctas ? units : p.ctas));
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = kQSmem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm_q4tc<IN, EPI>, mx, mc, p);
+}
+
+cudaError_t dispatch_q4tc(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mc, const Q4tcParams& p,
+                          int in_mode, int epi, bool prepare) {
+  if (in_mode == kInNorm && epi == kEpiStore) return launch_q4tc_t<kInNorm, kEpiStore>(c, mx, mc, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiStore) return launch_q4tc_t<kInPlain, kEpiStore>(c, mx, mc, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiResid) return launch_q4tc_t<kInPlain, kEpiResid>(c, mx, mc, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_q4tc_t<kInNorm, kEpiSwiglu>(c, mx, mc, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_q4tc_t<kInNorm, kEpiLmHead>(c, mx, mc, p, prepare);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int q4tc_max_tokens() { return kQT; }
+
+// K splits of an N x K projection: a divisor of the K / 64 groups (at most 16) that brings the
+// units of the one-CTA-per-SM grid closest to whole waves; a larger split count only when it
+// gains 5% of the waves' occupancy (each split adds a partial round trip)
+int q4tc_splits(int N, int K, int num_sms) {
+  const int tiles = (N + kQM - 1) / kQM, groups = K / kQK;
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 16 && s <= groups; ++s) {
+    if (groups % s) continue;
+    const long long units = static_cast<long long>(tiles) * s;
+    const long long waves = (units + num_sms - 1) / num_sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
+    if (eff > best_eff + 0.05) {
+      best = s;
+      best_eff = eff;
+    }
+  }
+  return best;
+}
+
+// 4-bit codes [N][K/2] bytes, boxes of 32 bytes x 128 rows (one group of a tile), no swizzle;
+// rows past the end read as zero
+cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K) {
+  EncodeTiledQ enc = encoder_q();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQK / 2), static_cast<cuuint32_t>(kQM)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_q4tc(const LaunchCtx& c, const void* map_x, const void* map_codes, const Q4tcParams& p,
+                             int in_mode, int epi) {
+  return dispatch_q4tc(c, *static_cast<const CUtensorMap*>(map_x), *static_cast<const CUtensorMap*>(map_codes), p,
+                       in_mode, epi, false);
+}
+
+cudaError_t prepare_gemm_q4tc(int in_mode, int epi) {
+  CUtensorMap dummy{};
+  Q4tcParams p{};
+  return dispatch_q4tc(LaunchCtx{nullptr, false}, dummy, dummy, p, in_mode, epi, true);
+}
+
+}  // namespace dec

@@ -17,7 +17,7 @@
 // on a barrier is bounded: on time-out the kernel flags the status word and leaves.
 #include <cuda.h>
 
-#include "dec_internal.cuh"
+#include "umma_common.cuh"
 
 namespace dec {
 
@@ -26,7 +26,6 @@ namespace {
 constexpr int kUM = 128;                     // tokens per tile
 constexpr int kUK = 64;                      // inputs per stage
 constexpr int kUTile = 128 * kUK * 2;        // 16 KB: 128 rows of 128 bytes
-constexpr uint32_t kUWaitPolls = 1u << 22;
 
 // Per weight-tile width UN (128 or 256 rows = accumulator columns): the stage holds the x hi
 // and lo tiles and UN weight rows; four stages of 48 KB, or three of 64 KB.
@@ -40,67 +39,7 @@ struct UCfg {
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((UN >> 3) << 17) | ((kUM >> 4) << 24);
 };
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kUWaitPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-// shared-memory descriptor of a K-major tile in the 128-byte swizzle: start address >> 4,
-// leading offset 16 B (unused for this layout), stride 1024 B between 8-row groups, the
-// descriptor version 1 at bit 46, swizzle mode 2 (128 B) at bit 61
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
-}
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this thread's accumulator lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+using namespace umma;
 
 __device__ __forceinline__ float silu_u(float x) { return x / (1.0f + expf(-x)); }
 
@@ -199,9 +138,9 @@ __global__ void __launch_bounds__(128, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tmem_slot - base));
 
   griddep_wait();  // the activations are the previous kernel's output
@@ -238,21 +177,21 @@ __global__ void __launch_bounds__(128, 1)
         ok = false;
         break;
       }
-      tc_fence_after();
+      fence_after();
       const uint32_t st = base + s * kUStage;
       const uint64_t dxh = sw128_desc(st), dxl = sw128_desc(st + kUTile), dw = sw128_desc(st + 2 * kUTile);
 #pragma unroll
       for (int k = 0; k < kUK / 16; ++k) {  // 16 inputs = 32 bytes further along the swizzled row
-        umma_bf16(tmem, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
-        umma_bf16(tmem, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
+        mma_bf16(tmem, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
+        mma_bf16(tmem, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
       }
-      umma_commit(bar_empty + 8 * s);  // the stage is free once these MMAs have read it
+      commit(bar_empty + 8 * s);  // the stage is free once these MMAs have read it
     }
-    umma_commit(bar_done);
+    commit(bar_done);
   }
   __syncwarp();
   if (!mbar_wait(bar_done, 0)) ok = false;
-  tc_fence_after();
+  fence_after();
   __syncthreads();
 
   // ---- epilogue: this thread's token is lane 32 warp + lane of the tile
@@ -274,7 +213,7 @@ __global__ void __launch_bounds__(128, 1)
     if (live && ok) atomicMax(p.amax_key + tok, best);
   }
   griddep_launch_dependents();
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kUN) : "memory");
   if (!ok && tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
@@ -331,9 +270,9 @@ __global__ void __launch_bounds__(192, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + (tmem_slot - base));
   griddep_wait();
 
@@ -366,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        tc_fence_after();
+        fence_after();
         const uint32_t acc = tmem + b * UN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
@@ -374,17 +313,17 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
+          fence_after();
           const uint32_t st = base + s * kStage;
           const uint64_t dxh = sw128_desc(st), dxl = sw128_desc(st + kUTile), dw = sw128_desc(st + 2 * kUTile);
 #pragma unroll
           for (int k = 0; k < kUK / 16; ++k) {
-            umma_bf16(acc, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
-            umma_bf16(acc, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
+            mma_bf16(acc, dxh + 2 * k, dw + 2 * k, CF::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16(acc, dxl + 2 * k, dw + 2 * k, CF::kIdesc, 1u);
           }
-          umma_commit(bar_empty + 8 * s);
+          commit(bar_empty + 8 * s);
         }
-        umma_commit(bar_tfull + 8 * b);
+        commit(bar_tfull + 8 * b);
       }
     }
   } else {  // epilogue warps 2..5: lanes 32 q .. 32 q + 31 of the accumulators, q = warp % 4
@@ -408,7 +347,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (!mbar_wait(bar_tfull + 8 * b, (local >> 1) & 1)) ok = false;
-      tc_fence_after();
+      fence_after();
       if constexpr (EPI == kEpiLmHead) best = 0ull;
 #pragma unroll 1
       for (int c = 0; c < UN / 32; ++c) {
@@ -418,7 +357,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!live || !ok || n0 >= p.N) continue;
         epi_chunk<IN, EPI, UN>(p, v, tok, n0, nt, c, r, best);
       }
-      tc_fence_before();
+      fence_before();
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_tempty + 8 * b) : "memory");
       if constexpr (EPI == kEpiLmHead) {
         if (live && ok) atomicMax(p.amax_key + tok, best);
@@ -426,7 +365,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   griddep_launch_dependents();
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * UN) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);

@@ -101,6 +101,8 @@ def _load() -> ctypes.CDLL:
         "dec_kv_quantize": (ctypes.c_int, [vp, ctypes.c_int, ctypes.c_int, vp, vp, vp]),
         "dec_debug_gemm_tc5": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int, vp]),
         "dec_debug_force_timeout": (ctypes.c_int, [vp, ctypes.c_int, vp]),
+        "dec_debug_gemm_q4tc": (ctypes.c_int, [vp, ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
+                                               vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -222,6 +224,10 @@ def dec_debug_gemm_tc5(x_hl: int, M: int, w: int, N: int, K: int, out: int, pers
 
 def dec_debug_force_timeout(h: int, polls: int = 256, stream: int = 0) -> int:
     return _check(lib.dec_debug_force_timeout(h, polls, stream), "dec_debug_force_timeout")
+def dec_debug_gemm_q4tc(x_hl: int, M: int, codes: int, sb: int, N: int, K: int, S: int, out: int,
+                        partials: int | None = None, counters: int | None = None, stream: int = 0) -> int:
+    return _check(lib.dec_debug_gemm_q4tc(x_hl, M, codes, sb, N, K, S, out, partials, counters, stream),
+                  "dec_debug_gemm_q4tc")
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
