@@ -2,26 +2,26 @@
 // Y[t][n] = sum_k X[t][k] W[n][k] for up to 32 token rows, W = scale * q + bias per group of
 // 64 inputs (q in 0..15, eight per uint32, one bf16 scale and bias per group).
 //
-// Sources: oxinfer crate page, "MLX checkpoints" (the affine 4-bit format); Butter
-// architecture.md, "SINGLE-TOKEN DECODE" (the projection sequence, here over a batch of
-// independent sequences).
+// Sources: oxinfer crate page, "MLX checkpoints" (the affine 4-bit format and its per-group
+// sum: sum_k (s q_k + b) x_k = s sum_k q_k x_k + b sum_k x_k); Butter architecture.md,
+// "SINGLE-TOKEN DECODE" (the projection sequence, here over a batch of independent sequences).
 //
-// The 128 weight rows of a tile are the accumulator's lanes (the MMA's M) and the 32 tokens'
-// bf16 hi and lo activation rows its 64 columns (N): the MMAs of a group of 64 inputs take the
-// weight tile as A and the activation tile as B, both K-major in the 128-byte swizzle.
-// Dequantizer warps turn each group's codes into the float32 weights fl(scale * q + bias) (the
-// format's exact values) and store them as bf16 hi and lo planes (w = hi + lo to ~16
-// significant bits), so a group takes two MMAs per 16 inputs (hi plane, lo plane) into one
-// accumulator; a token's result is the sum of its hi and lo columns.
+// Per group of 64 inputs the tensor cores compute D[n][t] = sum_k (q[n][k] - 8) x[t][k] with
+// the codes as exact bf16 integers: the 128 weight rows of a tile are the MMA's M (the
+// accumulator's lanes), the 32 tokens' bf16 hi and lo activation rows its N = 64 columns,
+// both operands K-major in the 128-byte swizzle.  The epilogue warps read every group's
+// accumulator from a ring of four in tensor memory and add s D + (b + 8 s) sum_k x[t][k] in
+// float32, in group order, so the scale and bias cost one multiply-add each per (row, token,
+// group) instead of a dequantization per weight.
 //
 // Warp roles (one persistent CTA per SM, 448 threads): warp 0 issues the TMA copies of the
 // codes (128 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
-// warp 1 allocates two 64-column accumulators and issues the MMAs; warps 2..9 dequantize (two
-// threads per weight row, 32 inputs each); warps 10..13 read the accumulator and run the
-// fused epilogue, so the epilogue of one unit overlaps the MMAs of the next.  A unit is a
-// (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile adds the S
-// partial results in split order (deterministic).  Every wait on a barrier is bounded: on
-// time-out the kernel flags the status word and stops.
+// warp 1 allocates the accumulator ring and issues the MMAs; warps 2..9 expand the codes into
+// bf16 (a byte permute builds 128 + q for two codes, an exact subtraction centres them) and sum
+// each token's inputs of the group; warps 10..13 scale, accumulate and run the fused epilogue.
+// A unit is a (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
+// adds the S partial results in split order (deterministic).  Every wait on a barrier is
+// bounded: on time-out the kernel flags the status word and stops.
 #include "q4.cuh"
 #include "umma_common.cuh"
 
@@ -35,25 +35,26 @@ constexpr int kQM = 128;                   // weight rows per tile
 constexpr int kQT = 32;                    // token rows (accumulator columns 0..31 hi, 32..63 lo)
 constexpr int kQK = 64;                    // inputs per stage: one group of the format
 constexpr int kQStages = 6;                // TMA ring: codes + activations
-constexpr int kQAStages = 3;               // dequantized weight ring
+constexpr int kQAStages = 4;               // expanded-code ring
+constexpr int kQG = 4;                     // accumulator ring (64 columns each) and sum-of-x ring
 constexpr int kQCode = kQM * kQK / 2;      // 4 KB: 128 rows x 32 bytes of codes
 constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
 constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
-constexpr int kQPlane = kQM * kQK * 2;     // 16 KB: one bf16 plane of the weight tile
-constexpr int kQA = 2 * kQPlane;           // hi plane, lo plane
-constexpr int kQDeq = 256;                 // dequantizer threads
+constexpr int kQA = kQM * kQK * 2;         // 16 KB: the expanded codes of a tile, bf16
+constexpr int kQDeq = 256;                 // expansion threads
 constexpr int kQThreads = 448;
 constexpr int kQOffS = kQAStages * kQA;
 constexpr int kQOffBar = kQOffS + kQStages * kQStage;
-constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 4;
+constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 4 * kQG;
 constexpr int kQOffTmem = kQOffBar + 8 * kQBars;
-constexpr int kQOffInv = kQOffTmem + 16;
+constexpr int kQOffSx = kQOffTmem + 16;                  // float [kQG][kQT]
+constexpr int kQOffInv = kQOffSx + 4 * kQG * kQT;
 constexpr int kQOffBest = kQOffInv + 4 * kQT;
 constexpr int kQOffTicket = kQOffBest + 8 * kQT;
 constexpr int kQSmem = 1024 + kQOffTicket + 16;
 // tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
 constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
-static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0, "smem layout");
+static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && kQOffBest % 8 == 0, "smem layout");
 
 __device__ __forceinline__ float silu_q(float x) { return x / (1.0f + expf(-x)); }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -62,27 +63,22 @@ __device__ __forceinline__ void split_hl_q(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-// Codes of one word (element 8 j + k in bits 4k..4k+3) -> 8 weights w = fl(s q + b) as bf16
-// hi and lo pairs (element 2i in the low half of pair i).  The byte permute puts a code into
-// bits 16..19 of 128.0f (giving 128 + q exactly); q = (128 + q) - 128 is exact.
-__device__ __forceinline__ void dequant_word(uint32_t w, float s, float b, uint4& hi, uint4& lo) {
+// Codes of one word (element 8 j + k in bits 4k..4k+3) -> the 16 bytes of bf16 (q - 8) for
+// elements 8 j .. 8 j + 7 in order.  The permutes interleave even and odd codes and set 0x43
+// as each high byte, giving bf16 128 + q exactly; subtracting 136 is exact (|q - 8| <= 8).
+__device__ __forceinline__ uint4 expand_word(uint32_t w) {
   const uint32_t ev = w & 0x0f0f0f0fu, od = (w >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
-  constexpr uint32_t kMagic = 0x43000000u;
-  uint32_t h[4], l[4];
+  const uint32_t t0 = __byte_perm(ev, od, 0x5140), t1 = __byte_perm(ev, od, 0x7362);  // c0..c3 / c4..c7
+  constexpr uint32_t k43 = 0x43434343u, k136 = 0x43084308u;  // bf16 136 in both halves
+  uint32_t r[4] = {__byte_perm(t0, k43, 0x4140), __byte_perm(t0, k43, 0x4342), __byte_perm(t1, k43, 0x4140),
+                   __byte_perm(t1, k43, 0x4342)};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t sel = 0x7044u | (static_cast<uint32_t>(i) << 8);
-    const float q0 = __uint_as_float(__byte_perm(ev, kMagic, sel)) - 128.0f;
-    const float q1 = __uint_as_float(__byte_perm(od, kMagic, sel)) - 128.0f;
-    const float w0 = fmaf(s, q0, b), w1 = fmaf(s, q1, b);
-    const __nv_bfloat162 hp = __floats2bfloat162_rn(w0, w1);  // .x = w0 (low half)
-    const float2 hf = __bfloat1622float2(hp);
-    const __nv_bfloat162 lp = __floats2bfloat162_rn(w0 - hf.x, w1 - hf.y);
-    h[i] = *reinterpret_cast<const uint32_t*>(&hp);
-    l[i] = *reinterpret_cast<const uint32_t*>(&lp);
+    const __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&r[i]),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&k136));
+    r[i] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
+  return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 }  // namespace
@@ -97,8 +93,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t sA = base, sS = base + kQOffS;
   const uint32_t st_full = base + kQOffBar, st_empty = st_full + 8 * kQStages;
   const uint32_t a_full = st_empty + 8 * kQStages, a_empty = a_full + 8 * kQAStages;
-  const uint32_t t_full = a_empty + 8 * kQAStages, t_empty = t_full + 16;
+  const uint32_t g_full = a_empty + 8 * kQAStages, g_empty = g_full + 8 * kQG;
+  const uint32_t x_full = g_empty + 8 * kQG, x_empty = x_full + 8 * kQG;
   const uint32_t tmem_slot = base + kQOffTmem;
+  float* s_x = reinterpret_cast<float*>(smem + kQOffSx);
   float* s_inv = reinterpret_cast<float*>(smem + kQOffInv);
   unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + kQOffBest);
   unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + kQOffTicket);
@@ -108,23 +106,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int units = n_tiles * p.S;
   const int gps = p.K / kQK / p.S;  // groups per split
 
-  if (warp == 1) {  // two accumulators of 64 columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(128)
+  if (warp == 1) {  // the accumulator ring: kQG x 64 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(64 * kQG)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(st_full + 8 * s, 1);
-      mbar_init(st_empty + 8 * s, kQDeq + 1);  // the dequantizers' reads, then the MMAs' commit
+      mbar_init(st_empty + 8 * s, kQDeq + 1);  // the expanders' reads, then the MMAs' commit
     }
     for (int s = 0; s < kQAStages; ++s) {
       mbar_init(a_full + 8 * s, kQDeq);
       mbar_init(a_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(t_full + 8 * b, 1);
-      mbar_init(t_empty + 8 * b, 128);
+    for (int b = 0; b < kQG; ++b) {
+      mbar_init(g_full + 8 * b, 1);     // the MMAs' commit
+      mbar_init(g_empty + 8 * b, 128);  // the epilogue's accumulator reads
+      mbar_init(x_full + 8 * b, kQDeq); // the expanders' sums of x
+      mbar_init(x_empty + 8 * b, 128);  // the epilogue's reads of them
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {  // TMA producer; stage i of this CTA is group i % gps of its unit i / gps
-      const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      const int my_units = static_cast<int>(blockIdx.x) < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
       const int total = my_units * gps;
       auto group_of = [&](int i, int& tile, int& g) {
         const int u = blockIdx.x + (i / gps) * gridDim.x;
@@ -169,78 +169,83 @@ __global__ void __launch_bounds__(kQThreads, 1)
           mbar_expect_tx(full, kQStage);
           tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
         }
-        tma_load_2d(st, &tm_x, g * kQK, 0, full);                // hi plane: tokens 0..31
-        tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);    // lo plane
+        tma_load_2d(st, &tm_x, g * kQK, 0, full);              // hi plane: tokens 0..31
+        tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);  // lo plane
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
-      int it = 0, local = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
-        const int b = local & 1;
-        if (local >= 2 && !mbar_wait(t_empty + 8 * b, ((local >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        fence_after();
-        const uint32_t acc = tmem + 64 * b;
+    if (lane == 0) {  // MMA issuer: one accumulator of the ring per group
+      int it = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         for (int j = 0; j < gps; ++j, ++it) {
-          const int s = it % kQStages, a = it % kQAStages;
-          if (!mbar_wait(a_full + 8 * a, (it / kQAStages) & 1) || !mbar_wait(st_full + 8 * s, (it / kQStages) & 1)) {
+          const int s = it % kQStages, a = it % kQAStages, gb = it % kQG;
+          if (!mbar_wait(a_full + 8 * a, (it / kQAStages) & 1) || !mbar_wait(st_full + 8 * s, (it / kQStages) & 1) ||
+              (it >= kQG && !mbar_wait(g_empty + 8 * gb, ((it / kQG) - 1) & 1))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint64_t dx = sw128_desc(sS + s * kQStage);
-          const uint64_t dh = sw128_desc(sA + a * kQA), dl = sw128_desc(sA + a * kQA + kQPlane);
+          const uint64_t dx = sw128_desc(sS + s * kQStage), da = sw128_desc(sA + a * kQA);
 #pragma unroll
-          for (int k = 0; k < kQK / 16; ++k) {  // 16 inputs = 32 bytes further along the swizzled rows
-            mma_bf16(acc, dh + 2 * k, dx + 2 * k, kQIdesc, (j | k) != 0 ? 1u : 0u);
-            mma_bf16(acc, dl + 2 * k, dx + 2 * k, kQIdesc, 1u);
-          }
+          for (int k = 0; k < kQK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
+            mma_bf16(tmem + 64 * gb, da + 2 * k, dx + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
           commit(a_empty + 8 * a);
           commit(st_empty + 8 * s);
+          commit(g_full + 8 * gb);
         }
-        if (!ok) break;
-        commit(t_full + 8 * b);
       }
     }
-  } else if (warp < 10) {  // dequantizers: weight row r of the tile, inputs 32 h .. 32 h + 31 of a group
+  } else if (warp < 10) {
+    // expanders: the codes of weight row r, inputs 32 h .. 32 h + 31 of a group; and the sum of
+    // x over the group for token t (lanes 8 t' .. 8 t' + 7: hi row quarters, then lo row quarters)
     const int dt = tid - 64, r = dt & (kQM - 1), h = dt >> 7;
+    const int xt = dt >> 3, xp = dt & 7, xrow = (xp < 4 ? 0 : kQT) + xt, xq = xp & 3;
     int it = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const int tile = u % n_tiles, split = u / n_tiles;
-      const int row = tile * kQM + r;
-      const uint32_t* sbrow = p.sb + static_cast<size_t>(row < p.N ? row : 0) * (p.K / kGroup);
       for (int j = 0; j < gps; ++j, ++it) {
-        const int s = it % kQStages, a = it % kQAStages;
-        const uint32_t sbw = __ldg(sbrow + split * gps + j);  // eight groups share a 32-byte sector
+        const int s = it % kQStages, a = it % kQAStages, gb = it % kQG;
         if (!mbar_wait(st_full + 8 * s, (it / kQStages) & 1)) {
           ok = false;
           break;
         }
-        uint4 cw;
+        const uint32_t st = sS + s * kQStage;
+        uint4 cw, x0, x1;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                     : "r"(sS + s * kQStage + kQX + r * 32 + h * 16));
+                     : "r"(st + kQX + r * 32 + h * 16));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x0.x), "=r"(x0.y), "=r"(x0.z), "=r"(x0.w)
+                     : "r"(st + xrow * 128 + (((2 * xq) ^ (xrow & 7)) << 4)));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x1.x), "=r"(x1.y), "=r"(x1.z), "=r"(x1.w)
+                     : "r"(st + xrow * 128 + (((2 * xq + 1) ^ (xrow & 7)) << 4)));
         mbar_arrive(st_empty + 8 * s);
+        // this thread's 16 inputs, then the 8 lanes of the token (fixed order)
+        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float sx = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sx += bf16_lo(xs[i]) + bf16_hi(xs[i]);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+        sx += __shfl_xor_sync(0xffffffffu, sx, 4);
+        if (it >= kQG && !mbar_wait(x_empty + 8 * gb, ((it / kQG) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (xp == 0) s_x[gb * kQT + xt] = sx;
+        mbar_arrive(x_full + 8 * gb);
         if (it >= kQAStages && !mbar_wait(a_empty + 8 * a, ((it / kQAStages) - 1) & 1)) {
           ok = false;
           break;
         }
-        const float sc = sb_scale(sbw), bi = sb_bias(sbw);
         const uint32_t arow = sA + a * kQA + r * 128;
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // word i = 16-byte chunk 4 h + i of the row
-          uint4 hv, lv;
-          dequant_word(words[i], sc, bi, hv, lv);
+          const uint4 v = expand_word(words[i]);
           const uint32_t off = static_cast<uint32_t>(((4 * h + i) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + off), "r"(hv.x), "r"(hv.y), "r"(hv.z),
-                       "r"(hv.w)
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + kQPlane + off), "r"(lv.x), "r"(lv.y),
-                       "r"(lv.z), "r"(lv.w)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + off), "r"(v.x), "r"(v.y), "r"(v.z),
+                       "r"(v.w)
                        : "memory");
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
@@ -262,20 +267,45 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
     }
     epi_sync();
-    int local = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
-      const int tile = u % n_tiles, split = u / n_tiles, b = local & 1;
-      if (ok && !mbar_wait(t_full + 8 * b, (local >> 1) & 1)) ok = false;
-      fence_after();
-      float y[kQT], yl[kQT];
-      tmem_ld32(tmem + 64 * b + tq, y);        // hi columns: tokens 0..31
-      tmem_ld32(tmem + 64 * b + 32 + tq, yl);  // lo columns
-      fence_before();
-      mbar_arrive(t_empty + 8 * b);
-#pragma unroll
-      for (int t = 0; t < kQT; ++t) y[t] += yl[t];
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int tile = u % n_tiles, split = u / n_tiles;
       const int n = tile * kQM + r;
-      const bool live = ok && n < p.N;
+      const bool row_ok = n < p.N;
+      const uint32_t* sbrow = p.sb + static_cast<size_t>(row_ok ? n : 0) * (p.K / kGroup) + split * gps;
+      float y[kQT];
+#pragma unroll
+      for (int t = 0; t < kQT; ++t) y[t] = 0.f;
+      uint32_t sbw = __ldg(sbrow);
+      for (int j = 0; j < gps; ++j, ++it) {
+        const int gb = it % kQG;
+        const uint32_t sbn = j + 1 < gps ? __ldg(sbrow + j + 1) : 0u;  // next group's, in flight
+        if (ok && (!mbar_wait(g_full + 8 * gb, (it / kQG) & 1) || !mbar_wait(x_full + 8 * gb, (it / kQG) & 1)))
+          ok = false;
+        fence_after();
+        float dh[kQT], dl[kQT];
+        tmem_ld32(tmem + 64 * gb + tq, dh);       // hi columns: tokens 0..31
+        tmem_ld32(tmem + 64 * gb + 32 + tq, dl);  // lo columns
+        fence_before();
+        mbar_arrive(g_empty + 8 * gb);
+        // w = s q + b = s (q - 8) + (b + 8 s): y += s D + (b + 8 s) sum x
+        const float sc = sb_scale(sbw), bc = fmaf(8.0f, sc, sb_bias(sbw));
+        const float4* sxv = reinterpret_cast<const float4*>(s_x + gb * kQT);
+#pragma unroll
+        for (int t4 = 0; t4 < kQT / 4; ++t4) {
+          const float4 xv = sxv[t4];
+          const float xs4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int t = 4 * t4 + e;
+            y[t] = fmaf(sc, dh[t] + dl[t], y[t]);
+            y[t] = fmaf(bc, xs4[e], y[t]);
+          }
+        }
+        mbar_arrive(x_empty + 8 * gb);
+        sbw = sbn;
+      }
+      const bool live = ok && row_ok;
       if (p.S > 1) {  // partial results; the last CTA of the tile adds them in split order
         if (live) {
 #pragma unroll
@@ -372,7 +402,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   griddep_launch_dependents();
   fence_before();
   __syncthreads();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64 * kQG) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
   if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
     __threadfence();
@@ -438,19 +469,20 @@ cudaError_t dispatch_q4tc(const LaunchCtx& c, const CUtensorMap& mx, const CUten
 
 int q4tc_max_tokens() { return kQT; }
 
-// K splits of an N x K projection: a divisor of the K / 64 groups (at most 16) that brings the
+// K splits of an N x K projection: a divisor of the K / 64 groups (at most 8) that brings the
 // units of the one-CTA-per-SM grid closest to whole waves; a larger split count only when it
-// gains 5% of the waves' occupancy (each split adds a partial round trip)
+// gains 10% of the waves' occupancy (each split adds a partial round trip, and short units
+// pay their epilogue more often: 8 splits of the 8B gate/up were the slowest measured)
 int q4tc_splits(int N, int K, int num_sms) {
   const int tiles = (N + kQM - 1) / kQM, groups = K / kQK;
   int best = 1;
   double best_eff = 0.0;
-  for (int s = 1; s <= 16 && s <= groups; ++s) {
+  for (int s = 1; s <= 8 && s <= groups; ++s) {
     if (groups % s) continue;
     const long long units = static_cast<long long>(tiles) * s;
     const long long waves = (units + num_sms - 1) / num_sms;
     const double eff = static_cast<double>(units) / static_cast<double>(waves * num_sms);
-    if (eff > best_eff + 0.05) {
+    if (eff > best_eff + 0.10) {
       best = s;
       best_eff = eff;
     }
