@@ -391,7 +391,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.amax_key = h->amax_key;
   ep.status = h->status;
   ep.norm_w0 = h->layers[0].in_norm;
-  ep.xhl_out = h->rows > 1 ? h->xh_u : nullptr;
+  ep.xhl_out = h->rows > 1 || h->q4tc ? h->xh_u : nullptr;
   ep.T = h->tps;
   ep.tl = Timeline{h->timeline, 0};
   ep.V = c.vocab;
@@ -555,7 +555,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.eps = c.rms_eps;
     ap.out = h->attn_o;
     ap.status = h->status;
-    ap.out_hl = h->rows > 1 ? h->xh_o : nullptr;
+    ap.out_hl = h->rows > 1 || h->q4tc ? h->xh_o : nullptr;
     if (h->tps > 1) {
       // verify step: every row's K/V go into the cache before any row attends, so
       // that row (b, t) sees the rows (b, 0..t-1) of this step
@@ -737,7 +737,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  const bool tc = h->rows > 1;
+  // 4-bit weights, at most 32 rows (batch 1 included), hidden >= 2048: tcgen05 over the codes
+  // expanded in shared memory, on the batched path's hi/lo activation planes
+  h->q4tc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
+  const bool tc = h->rows > 1 || h->q4tc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
   h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
@@ -746,7 +749,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // below that (the 0.6B shapes) the token-blocked mma.sync kernel's many small CTAs fill the
   // GPU better (512-token chunk: 14.2 ms against 16.2 ms, measured)
   h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16 && H >= 2048;
-  h->q4tc = tc && h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
   const bool frag = tc && !h->umma && !h->q4tc;  // fragment-packed weights for the mma.sync path
   auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
