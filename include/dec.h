@@ -234,6 +234,15 @@ DEC_API dec_status dec_debug_force_timeout(dec_handle *h, int polls, dec_stream_
 DEC_API dec_status dec_debug_gemm_q4tc(const void *x_hl, int M, const void *codes, const void *sb, int N, int K,
                     int S, float *out, float *partials, unsigned *counters, dec_stream_t stream);
 
+/* Test hook: the bf16 form of the batched-decode tensor-core projection (weights streamed by TMA
+   into the MMA) on caller buffers, plain store: out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) w[n][k].
+     x_hl  device bf16 [2][M][K], 16-byte aligned, M in 1..32
+     w     device bf16 [N][K] row-major, 16-byte aligned
+     out, S, partials, counters  as in dec_debug_gemm_q4tc.
+   K a positive multiple of 64, N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
+DEC_API dec_status dec_debug_gemm_btc(const void *x_hl, int M, const void *w, int N, int K, int S, float *out,
+                    float *partials, unsigned *counters, dec_stream_t stream);
+
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:
    mn, mx = min, max; scale = bf16(fl(fl(mx - mn) / 255)); bias = bf16(mn) (round to

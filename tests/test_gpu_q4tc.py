@@ -1,7 +1,7 @@
 """The batched-decode projection kernel for affine 4-bit weights on tcgen05
 (dec_debug_gemm_q4tc, plain store epilogue) against an fp64 product of the same inputs, the
 weights dequantized by the oracle (fl(scale * q + bias), float32): ragged token counts and
-weight-row tiles, K splits, more groups than the stage rings hold."""
+weight-row tiles, K splits, more groups than the stage rings hold; and the bf16 form."""
 
 import numpy as np
 import pytest
@@ -52,10 +52,41 @@ def test_q4tc_gemm_matches_fp64(dec, M, N, K, S):
     torch.cuda.synchronize()
     xs = (hi.double() + lo.double()).numpy()
     ref = xs @ w.T
-    bound = np.abs(xs) @ np.abs(w).T  # the products' magnitudes: the weights' hi/lo split is ~2^-16 relative
+    bound = np.abs(xs) @ np.abs(w).T  # the products' magnitudes (x's hi/lo split keeps ~16 bits)
     got = out.cpu().double().numpy()
     assert np.isfinite(got).all(), "unwritten outputs"
     err = np.abs(got - ref)
     assert np.all(err <= 4e-5 * bound + 1e-6), f"max err {float(err.max()):.3e} (rel {float((err / bound).max()):.3e})"
+    if S > 1:
+        assert int(counters.abs().sum()) == 0, "split counters not left zero"
+
+
+@pytest.mark.parametrize("M,N,K,S", [(8, 128, 64, 1), (8, 24576, 4096, 2), (16, 200, 512, 1), (32, 1000, 2560, 5),
+                                     (3, 130, 384, 3), (8, 4096, 12288, 4)])
+def test_btc_gemm_matches_fp64(dec, M, N, K, S):
+    """The bf16 form (dec_debug_gemm_btc): weights streamed by TMA into the MMA."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(M * 11 + N + K + S)
+    x = torch.randn((M, K), generator=g, dtype=torch.float64)
+    hi = x.to(torch.bfloat16)
+    lo = (x - hi.double()).to(torch.bfloat16)
+    w = (torch.randn((N, K), generator=g) * 0.05).to(torch.bfloat16)
+    xhl = torch.stack([hi, lo]).contiguous().cuda()
+    wd = w.contiguous().cuda()
+    out = torch.full((M, N), float("nan"), device="cuda")
+    partials = torch.empty((S, M, N), device="cuda") if S > 1 else None
+    counters = torch.zeros(((N + 127) // 128 + 1,), dtype=torch.int32, device="cuda") if S > 1 else None
+    dec.dec_debug_gemm_btc(xhl.data_ptr(), M, wd.data_ptr(), N, K, S, out.data_ptr(),
+                           partials.data_ptr() if S > 1 else None, counters.data_ptr() if S > 1 else None,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    xs = (hi.double() + lo.double()).numpy()
+    wf = w.double().numpy()
+    ref = xs @ wf.T
+    bound = np.abs(xs) @ np.abs(wf).T
+    got = out.cpu().double().numpy()
+    assert np.isfinite(got).all(), "unwritten outputs"
+    err = np.abs(got - ref)
+    assert np.all(err <= 1e-5 * bound + 1e-6), f"max err {float(err.max()):.3e}"
     if S > 1:
         assert int(counters.abs().sum()) == 0, "split counters not left zero"

@@ -139,6 +139,8 @@ struct dec_handle {
   // (the codes) and plain loads (scale and bias); the activation maps (map_u, map_o, map_g)
   // have 32-row boxes
   bool q4tc = false;
+  // the same for bf16 weights at 2..32 rows (k_gemm_btc): row-major weights read by TMA
+  bool btc = false;
   alignas(64) unsigned char map_u[128] = {}, map_o[128] = {}, map_g[128] = {};
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
@@ -472,7 +474,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       up.status = h->status;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
       s2 = check(launch_gemm_umma(lc, mx, L.tmap, up, in_mode, epi), what);
-    } else if (h->q4tc) {
+    } else if (h->q4tc || h->btc) {
       Q4tcParams qp{};
       qp.M = h->rows;
       qp.N = L.N;
@@ -493,7 +495,9 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       qp.argmax_out = sp.argmax;
       qp.status = h->status;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
-      s2 = check(launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi), what);
+      s2 = check(h->q4tc ? launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi)
+                         : launch_gemm_btc(lc, mx, L.tmap, qp, in_mode, epi),
+                 what);
     } else if (h->rows == 1) {
       s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
@@ -741,6 +745,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // expanded in shared memory, on the batched path's hi/lo activation planes
   h->q4tc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
   const bool tc = h->rows > 1 || h->q4tc;
+  h->btc = h->rows > 1 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
   h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
@@ -749,7 +754,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // below that (the 0.6B shapes) the token-blocked mma.sync kernel's many small CTAs fill the
   // GPU better (512-token chunk: 14.2 ms against 16.2 ms, measured)
   h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16 && H >= 2048;
-  const bool frag = tc && !h->umma && !h->q4tc;  // fragment-packed weights for the mma.sync path
+  const bool frag = tc && !h->umma && !h->q4tc && !h->btc;  // fragment-packed weights for the mma.sync path
   auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
                  lbytes(V, H);
@@ -779,7 +784,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       L.w = take(L.w_bytes);
       return L;
     }
-    L.S = h->umma ? 1 : h->q4tc ? q4tc_splits(N, K, h->num_sms) : choose_splits(N, K, fmt, h->num_sms);
+    L.S = h->umma ? 1 : h->q4tc || h->btc ? q4tc_splits(N, K, h->num_sms) : choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
       L.w_bytes = static_cast<size_t>(N) * K * 2;
       L.w = take(L.w_bytes);
@@ -944,8 +949,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       for (int tn : {128, 256})
         if ((e = prepare_gemm_umma(cb[0], cb[1], tn)) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
   }
-  if (h->q4tc) {  // TMA maps of every weight's codes and of the activation planes, kernel attributes
-    auto cmap = [&](PackedLinear& L) { return q4tc_code_map(L.tmap, L.w, L.N, L.K); };
+  if (h->q4tc || h->btc) {  // TMA maps of every weight and of the activation planes, kernel attributes
+    auto cmap = [&](PackedLinear& L) {
+      return h->q4tc ? q4tc_code_map(L.tmap, L.w, L.N, L.K) : umma_tensor_map(L.tmap, L.w, L.N, L.K, 128);
+    };
     if ((e = cmap(h->lm_head)) != cudaSuccess) return fail("tensor map", e);
     for (auto& L : h->layers)
       if ((e = cmap(L.qkv)) != cudaSuccess || (e = cmap(L.o)) != cudaSuccess || (e = cmap(L.gateup)) != cudaSuccess ||
@@ -958,7 +965,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       return fail("tensor map", e);
     const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
     for (auto& cb : combos)
-      if ((e = prepare_gemm_q4tc(cb[0], cb[1])) != cudaSuccess) return fail("tcgen05 4-bit kernel attributes", e);
+      if ((e = h->q4tc ? prepare_gemm_q4tc(cb[0], cb[1]) : prepare_gemm_btc(cb[0], cb[1])) != cudaSuccess)
+        return fail("tcgen05 decode kernel attributes", e);
   }
   if (frag) {
     GemmParams gp{};
@@ -1084,7 +1092,9 @@ extern "C" dec_status dec_get_device_status(dec_handle* h, int* out) {
 
 namespace {
 // rows per gate (then up) block of the packed gate/up projection
-int gate_up_block(const dec_handle* h) { return h->umma ? 16 : h->rows > 1 && !h->q4tc ? 8 : kGemvRows / 2; }
+int gate_up_block(const dec_handle* h) {
+  return h->umma ? 16 : h->rows > 1 && !h->q4tc && !h->btc ? 8 : kGemvRows / 2;
+}
 }  // namespace
 
 extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, float* out, dec_stream_t stream) {
@@ -1113,7 +1123,7 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  if (h->rows > 1 && !h->umma && !h->q4tc) {
+  if (h->rows > 1 && !h->umma && !h->q4tc && !h->btc) {
     DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
   } else {
     DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));
@@ -1314,6 +1324,36 @@ extern "C" dec_status dec_debug_gemm_q4tc(const void* x_hl, int M, const void* c
   p.partials = partials;
   p.counters = counters;
   DEC_CUDA(launch_gemm_q4tc(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mc, p, kInPlain, kEpiStore));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w, int N, int K, int S, float* out,
+                                         float* partials, unsigned* counters, dec_stream_t stream) {
+  g_err[0] = 0;
+  if (!x_hl || !w || !out || M < 1 || M > q4tc_max_tokens() || N < 1 || K < 64 || K % 64 != 0 || S < 1 ||
+      (K / 64) % S != 0 || (S > 1 && (!partials || !counters)) || !aligned16(x_hl) || !aligned16(w)) {
+    set_err("dec_debug_gemm_btc: NULL or misaligned pointer, M outside 1..%d, N < 1, K not a positive multiple of "
+            "64, or S not dividing K / 64 (S > 1 needs partials and counters)",
+            q4tc_max_tokens());
+    return DEC_ERR_INVALID_ARG;
+  }
+  alignas(64) unsigned char mx[128], mw[128];
+  int dev = 0, sms = 0;
+  DEC_CUDA(cudaGetDevice(&dev));
+  DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K, q4tc_max_tokens()));
+  DEC_CUDA(umma_tensor_map(mw, w, N, K, 128));
+  DEC_CUDA(prepare_gemm_btc(kInPlain, kEpiStore));
+  Q4tcParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.S = S;
+  p.ctas = sms;
+  p.out = out;
+  p.partials = partials;
+  p.counters = counters;
+  DEC_CUDA(launch_gemm_btc(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mw, p, kInPlain, kEpiStore));
   return DEC_OK;
 }
 

@@ -333,6 +333,11 @@ cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K);  // CU
 cudaError_t launch_gemm_q4tc(const LaunchCtx& c, const void* map_x, const void* map_codes, const Q4tcParams& p,
                              int in_mode, int epi);
 cudaError_t prepare_gemm_q4tc(int in_mode, int epi);
+// the bf16 form (k_gemm_btc.cu): the same parameters (sb unused), W bf16 [N][K] through a TMA
+// map with 128-row boxes (umma_tensor_map)
+cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* map_w, const Q4tcParams& p, int in_mode,
+                            int epi);
+cudaError_t prepare_gemm_btc(int in_mode, int epi);
 size_t attention_smem_bytes(int head_dim);
 // set the dynamic smem limits and record the shapes' occupancy (before capture)
 cudaError_t prepare_attention(int head_dim, int G, int kv_fmt);

@@ -1,0 +1,254 @@
+// Batched decode projections with bf16 weights on the fifth-generation tensor cores:
+// Y[t][n] = sum_k X[t][k] W[n][k] for up to 32 token rows (a batch of sequences, or the rows of
+// a verify step).
+//
+// Sources: Butter architecture.md, "SINGLE-TOKEN DECODE" (the projection sequence, here over a
+// batch of independent sequences).
+//
+// The 128 weight rows of a tile are the MMA's M (the accumulator's lanes) and the 32 tokens'
+// bf16 hi and lo activation rows its N = 64 columns; both operands arrive by TMA as K-major
+// tiles in the 128-byte swizzle, so the weights stream from HBM straight into the MMA's A
+// operand.  The step is bound by that stream: one persistent CTA per SM keeps a 7-stage ring of
+// weight tiles in flight, and two accumulators in tensor memory let the epilogue of one unit
+// overlap the MMAs of the next.  Warp roles (192 threads): warp 0 issues the TMA copies, warp 1
+// allocates the accumulators and issues the MMAs, warps 2..5 run the epilogue.  A unit is a
+// (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile adds the S
+// partial results in split order (deterministic).  Every wait on a barrier is bounded: on
+// time-out the kernel flags the status word and stops.
+#include "tc_decode_epi.cuh"
+#include "umma_common.cuh"
+
+namespace dec {
+
+namespace {
+
+using namespace umma;
+
+constexpr int kBM = 128;                  // weight rows per tile
+constexpr int kBT = tcdec::kT;            // token rows (accumulator columns 0..31 hi, 32..63 lo)
+constexpr int kBK = 64;                   // inputs per stage (one 128-byte row)
+constexpr int kBStages = 7;
+constexpr int kBX = 2 * kBT * kBK * 2;    // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
+constexpr int kBW = kBM * kBK * 2;        // 16 KB: 128 weight rows of 128 bytes
+constexpr int kBStage = kBX + kBW;
+constexpr int kBThreads = 192;
+constexpr int kBOffBar = kBStages * kBStage;
+constexpr int kBBars = 2 * kBStages + 4;
+constexpr int kBOffTmem = kBOffBar + 8 * kBBars;
+constexpr int kBOffInv = kBOffTmem + 16;
+constexpr int kBOffBest = kBOffInv + 4 * kBT;
+constexpr int kBOffTicket = kBOffBest + 8 * kBT;
+constexpr int kBSmem = 1024 + kBOffTicket + 16;
+// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
+constexpr uint32_t kBIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+static_assert(kBStage % 1024 == 0 && kBX % 1024 == 0 && kBOffBar % 8 == 0 && kBOffBest % 8 == 0, "smem layout");
+
+}  // namespace
+
+template <int IN, int EPI>
+__global__ void __launch_bounds__(kBThreads, 1)
+    k_gemm_btc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, Q4tcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t st_full = base + kBOffBar, st_empty = st_full + 8 * kBStages;
+  const uint32_t t_full = st_empty + 8 * kBStages, t_empty = t_full + 16;
+  const uint32_t tmem_slot = base + kBOffTmem;
+  float* s_inv = reinterpret_cast<float*>(smem + kBOffInv);
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + kBOffBest);
+  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + kBOffTicket);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = (p.N + kBM - 1) / kBM;
+  const int units = n_tiles * p.S;
+  const int gps = p.K / kBK / p.S;  // stages per unit
+
+  if (warp == 1) {  // two accumulators of 64 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(128)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(st_full + 8 * s, 1);
+      mbar_init(st_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(t_full + 8 * b, 1);
+      mbar_init(t_empty + 8 * b, 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (tid < kBT) s_best[tid] = 0ull;
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kBOffTmem);
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer; stage i of this CTA is stage i % gps of its unit i / gps
+      const int my_units = static_cast<int>(blockIdx.x) < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+      const int total = my_units * gps;
+      auto stage_of = [&](int i, int& tile, int& kb) {
+        const int u = blockIdx.x + (i / gps) * gridDim.x;
+        tile = u % n_tiles;
+        kb = (u / n_tiles) * gps + i % gps;
+      };
+      // the weights do not depend on upstream kernels: the first stages' are requested before
+      // the grid-dependency wait, their activations after it
+      const int pre = total < kBStages ? total : kBStages;
+      for (int i = 0; i < pre; ++i) {
+        int tile, kb;
+        stage_of(i, tile, kb);
+        const uint32_t full = st_full + 8 * i, st = base + i * kBStage;
+        mbar_expect_tx(full, kBStage);
+        tma_load_2d(st + kBX, &tm_w, kb * kBK, tile * kBM, full);
+      }
+      griddep_wait();
+      for (int i = 0; i < total; ++i) {
+        int tile, kb;
+        stage_of(i, tile, kb);
+        const int s = i % kBStages;
+        const uint32_t full = st_full + 8 * s, st = base + s * kBStage;
+        if (i >= pre) {
+          if (!mbar_wait(st_empty + 8 * s, ((i / kBStages) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full, kBStage);
+          tma_load_2d(st + kBX, &tm_w, kb * kBK, tile * kBM, full);
+        }
+        tma_load_2d(st, &tm_x, kb * kBK, 0, full);              // hi plane: tokens 0..31
+        tma_load_2d(st + kBX / 2, &tm_x, kb * kBK, p.M, full);  // lo plane
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      int it = 0, local = 0;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+        const int b = local & 1;
+        if (local >= 2 && !mbar_wait(t_empty + 8 * b, ((local >> 1) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t acc = tmem + 64 * b;
+        for (int j = 0; j < gps; ++j, ++it) {
+          const int s = it % kBStages;
+          if (!mbar_wait(st_full + 8 * s, (it / kBStages) & 1)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t st = base + s * kBStage;
+          const uint64_t dx = sw128_desc(st), dw = sw128_desc(st + kBX);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
+            mma_bf16(acc, dw + 2 * k, dx + 2 * k, kBIdesc, (j | k) != 0 ? 1u : 0u);
+          commit(st_empty + 8 * s);
+        }
+        if (!ok) break;
+        commit(t_full + 8 * b);
+      }
+    }
+  } else {  // epilogue warps 2..5: accumulator lanes 32 q .. 32 q + 31, q = warp % 4
+    const int et = tid - 64, q = warp & 3, r = 32 * q + lane;
+    const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
+    griddep_wait();  // the residual and the sums of squares are upstream outputs
+    if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
+      for (int i = 0; i < kBT / 4; ++i) {
+        const int t = (warp - 2) * (kBT / 4) + i;
+        float sacc = 0.f;
+        if (t < p.M)
+          for (int k = lane; k < p.n_sumsq_in; k += 32) sacc += p.sumsq_in[static_cast<size_t>(t) * p.n_sumsq_in + k];
+        sacc = warp_sum(sacc);
+        if (lane == 0) s_inv[t] = t < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
+      }
+    }
+    tcdec::epi_sync();
+    int local = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+      const int tile = u % n_tiles, split = u / n_tiles, b = local & 1;
+      if (ok && !mbar_wait(t_full + 8 * b, (local >> 1) & 1)) ok = false;
+      fence_after();
+      float y[kBT], yl[kBT];
+      tmem_ld32(tmem + 64 * b + tq, y);        // hi columns: tokens 0..31
+      tmem_ld32(tmem + 64 * b + 32 + tq, yl);  // lo columns
+      fence_before();
+      mbar_arrive(t_empty + 8 * b);
+#pragma unroll
+      for (int t = 0; t < kBT; ++t) y[t] += yl[t];
+      const int n = tile * kBM + r;
+      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, ok && n < p.N, et, lane, s_inv, s_best, s_ticket);
+    }
+    if constexpr (EPI == kEpiLmHead) {
+      tcdec::epi_sync();
+      if (et < p.M && s_best[et] != 0ull) atomicMax(p.amax_key + et, s_best[et]);
+    }
+  }
+  griddep_launch_dependents();
+  fence_before();
+  __syncthreads();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
+  if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
+  if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
+    __threadfence();
+    if (tid == 0) *s_ticket = atomicAdd(&p.counters[n_tiles], 1u);
+    __syncthreads();
+    if (*s_ticket == gridDim.x - 1) {
+      __threadfence();
+      for (int bb = tid; bb < p.M; bb += kBThreads)
+        p.argmax_out[bb] = argmax_key_index(atomicOr(p.amax_key + bb, 0ull));
+      if (tid == 0) p.counters[n_tiles] = 0u;
+    }
+  }
+}
+
+namespace {
+
+template <int IN, int EPI>
+cudaError_t launch_btc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
+                         bool prepare) {
+  if (prepare) return cudaFuncSetAttribute(k_gemm_btc<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmem);
+  const int units = ((p.N + kBM - 1) / kBM) * p.S;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units < p.ctas ? units : p.ctas));
+  cfg.blockDim = dim3(kBThreads);
+  cfg.dynamicSmemBytes = kBSmem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm_btc<IN, EPI>, mx, mw, p);
+}
+
+cudaError_t dispatch_btc(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
+                         int in_mode, int epi, bool prepare) {
+  if (in_mode == kInNorm && epi == kEpiStore) return launch_btc_t<kInNorm, kEpiStore>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiStore) return launch_btc_t<kInPlain, kEpiStore>(c, mx, mw, p, prepare);
+  if (in_mode == kInPlain && epi == kEpiResid) return launch_btc_t<kInPlain, kEpiResid>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiSwiglu) return launch_btc_t<kInNorm, kEpiSwiglu>(c, mx, mw, p, prepare);
+  if (in_mode == kInNorm && epi == kEpiLmHead) return launch_btc_t<kInNorm, kEpiLmHead>(c, mx, mw, p, prepare);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* map_w, const Q4tcParams& p, int in_mode,
+                            int epi) {
+  return dispatch_btc(c, *static_cast<const CUtensorMap*>(map_x), *static_cast<const CUtensorMap*>(map_w), p, in_mode,
+                      epi, false);
+}
+
+cudaError_t prepare_gemm_btc(int in_mode, int epi) {
+  CUtensorMap dummy{};
+  Q4tcParams p{};
+  return dispatch_btc(LaunchCtx{nullptr, false}, dummy, dummy, p, in_mode, epi, true);
+}
+
+}  // namespace dec

@@ -23,6 +23,7 @@
 // adds the S partial results in split order (deterministic).  Every wait on a barrier is
 // bounded: on time-out the kernel flags the status word and stops.
 #include "q4.cuh"
+#include "tc_decode_epi.cuh"
 #include "umma_common.cuh"
 
 namespace dec {
@@ -56,12 +57,7 @@ constexpr int kQSmem = 1024 + kQOffTicket + 16;
 constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && kQOffBest % 8 == 0, "smem layout");
 
-__device__ __forceinline__ float silu_q(float x) { return x / (1.0f + expf(-x)); }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void split_hl_q(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(v);
-  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-}
+using tcdec::epi_sync;
 
 // Codes of one word (element 8 j + k in bits 4k..4k+3) -> the 16 bytes of bf16 (q - 8) for
 // elements 8 j .. 8 j + 7 in order.  The permutes interleave even and odd codes and set 0x43
@@ -306,93 +302,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         sbw = sbn;
       }
       const bool live = ok && row_ok;
-      if (p.S > 1) {  // partial results; the last CTA of the tile adds them in split order
-        if (live) {
-#pragma unroll
-          for (int t = 0; t < kQT; ++t)
-            if (t < p.M) p.partials[(static_cast<size_t>(split) * p.M + t) * p.N + n] = y[t];
-        }
-        __threadfence();
-        epi_sync();
-        if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
-        epi_sync();
-        if (*s_ticket != static_cast<unsigned>(p.S - 1)) continue;
-        __threadfence();
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) y[t] = 0.f;
-        if (live)
-          for (int s = 0; s < p.S; ++s)
-#pragma unroll
-            for (int t = 0; t < kQT; ++t)
-              if (t < p.M) y[t] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t) * p.N + n);
-        if (et == 0) p.counters[tile] = 0u;
-      }
-      if constexpr (IN == kInNorm) {
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) y[t] *= s_inv[t];
-      }
-      if constexpr (EPI == kEpiStore) {
-        if (live) {
-#pragma unroll
-          for (int t = 0; t < kQT; ++t)
-            if (t < p.M) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
-        }
-      } else if constexpr (EPI == kEpiResid) {
-        // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per
-        // 8 rows (lanes 8 j .. 8 j + 7; N is a multiple of 8, so all of them are live or none)
-        const float nw = live ? bf16_to_f(p.next_norm_w[n]) : 0.f;
-        const size_t plane = static_cast<size_t>(p.M) * p.N;
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) {
-          float hn = 0.f;
-          const bool on = live && t < p.M;
-          if (on) {
-            const size_t o = static_cast<size_t>(t) * p.N + n;
-            hn = p.out[o] + y[t];
-            p.out[o] = hn;
-            __nv_bfloat16 hi, lo;
-            split_hl_q(hn * nw, hi, lo);
-            p.xhl_out[o] = hi;
-            p.xhl_out[plane + o] = lo;
-          }
-          float ss = hn * hn;
-          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-          ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-          ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-          if (on && (lane & 7) == 0) p.sumsq_out[static_cast<size_t>(t) * (p.N / kResGroup) + n / kResGroup] = ss;
-        }
-      } else if constexpr (EPI == kEpiSwiglu) {
-        // packed rows in blocks of 4: rows 8 j .. 8 j + 3 gate outputs 4 j .. 4 j + 3, the
-        // next 4 rows the matching up outputs (lane ^ 4)
-        const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
-        const int o = (n >> 3) * 4 + (n & 3);
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) {
-          const float up = __shfl_xor_sync(0xffffffffu, y[t], 4);
-          if (live && (n & 4) == 0 && t < p.M) {
-            const float gv = silu_q(y[t]) * up;
-            const size_t oo = static_cast<size_t>(t) * (p.N / 2) + o;
-            p.out[oo] = gv;
-            __nv_bfloat16 hi, lo;
-            split_hl_q(gv, hi, lo);
-            p.xhl_out[oo] = hi;
-            p.xhl_out[plane + oo] = lo;
-          }
-        }
-      } else {  // lm_head: logits, and every token's best (value, index) key over the warp's rows
-#pragma unroll
-        for (int t = 0; t < kQT; ++t) {
-          const bool on = live && t < p.M;
-          if (on && p.out) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
-          unsigned long long k = on ? argmax_key(y[t], n) : 0ull;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
-            k = other > k ? other : k;
-          }
-          if (lane == 0 && k != 0ull) atomicMax(s_best + t, k);
-        }
-      }
+      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, live, et, lane, s_inv, s_best, s_ticket);
     }
     if constexpr (EPI == kEpiLmHead) {
       epi_sync();

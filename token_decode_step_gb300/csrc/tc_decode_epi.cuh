@@ -1,0 +1,118 @@
+// The unit epilogue of the batched tcgen05 decode projections (k_gemm_q4tc.cu, k_gemm_btc.cu):
+// the thread holds weight row n of a 128-row tile and y[t], its results for the 32 token
+// columns.  With S > 1 K splits the partial results go to p.partials and the last CTA to finish
+// the tile adds them in split order; then the input RMSNorm's per-token 1/rms and the fused
+// epilogue (store / residual + next-norm hi/lo planes + sums of squares / SwiGLU / lm_head keys).
+// Called by the kernel's 128 epilogue threads together (named barrier 1).
+#pragma once
+
+#include "dec_internal.cuh"
+
+namespace dec {
+namespace tcdec {
+
+constexpr int kT = 32;  // token columns
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+template <int IN, int EPI>
+__device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT], int n, int tile, int split,
+                                              bool live, int et, int lane, const float* s_inv,
+                                              unsigned long long* s_best, unsigned* s_ticket) {
+  constexpr int kQT = kT;
+  if (p.S > 1) {  // partial results; the last CTA of the tile adds them in split order
+    if (live) {
+#pragma unroll
+      for (int t = 0; t < kQT; ++t)
+        if (t < p.M) p.partials[(static_cast<size_t>(split) * p.M + t) * p.N + n] = y[t];
+    }
+    __threadfence();
+    epi_sync();
+    if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
+    epi_sync();
+    if (*s_ticket != static_cast<unsigned>(p.S - 1)) return;
+    __threadfence();
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) y[t] = 0.f;
+    if (live)
+      for (int s = 0; s < p.S; ++s)
+#pragma unroll
+        for (int t = 0; t < kQT; ++t)
+          if (t < p.M) y[t] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t) * p.N + n);
+    if (et == 0) p.counters[tile] = 0u;
+  }
+  if constexpr (IN == kInNorm) {
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) y[t] *= s_inv[t];
+  }
+  if constexpr (EPI == kEpiStore) {
+    if (live) {
+#pragma unroll
+      for (int t = 0; t < kQT; ++t)
+        if (t < p.M) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
+    }
+  } else if constexpr (EPI == kEpiResid) {
+    // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per
+    // 8 rows (lanes 8 j .. 8 j + 7; N is a multiple of 8, so all of them are live or none)
+    const float nw = live ? bf16_to_f(p.next_norm_w[n]) : 0.f;
+    const size_t plane = static_cast<size_t>(p.M) * p.N;
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) {
+      float hn = 0.f;
+      const bool on = live && t < p.M;
+      if (on) {
+        const size_t o = static_cast<size_t>(t) * p.N + n;
+        hn = p.out[o] + y[t];
+        p.out[o] = hn;
+        __nv_bfloat16 hi, lo;
+        split_hl(hn * nw, hi, lo);
+        p.xhl_out[o] = hi;
+        p.xhl_out[plane + o] = lo;
+      }
+      float ss = hn * hn;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      if (on && (lane & 7) == 0) p.sumsq_out[static_cast<size_t>(t) * (p.N / kResGroup) + n / kResGroup] = ss;
+    }
+  } else if constexpr (EPI == kEpiSwiglu) {
+    // packed rows in blocks of 4: rows 8 j .. 8 j + 3 gate outputs 4 j .. 4 j + 3, the
+    // next 4 rows the matching up outputs (lane ^ 4)
+    const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
+    const int o = (n >> 3) * 4 + (n & 3);
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) {
+      const float up = __shfl_xor_sync(0xffffffffu, y[t], 4);
+      if (live && (n & 4) == 0 && t < p.M) {
+        const float gv = silu(y[t]) * up;
+        const size_t oo = static_cast<size_t>(t) * (p.N / 2) + o;
+        p.out[oo] = gv;
+        __nv_bfloat16 hi, lo;
+        split_hl(gv, hi, lo);
+        p.xhl_out[oo] = hi;
+        p.xhl_out[plane + oo] = lo;
+      }
+    }
+  } else {  // lm_head: logits, and every token's best (value, index) key over the warp's rows
+#pragma unroll
+    for (int t = 0; t < kQT; ++t) {
+      const bool on = live && t < p.M;
+      if (on && p.out) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
+      unsigned long long k = on ? argmax_key(y[t], n) : 0ull;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
+        k = other > k ? other : k;
+      }
+      if (lane == 0 && k != 0ull) atomicMax(s_best + t, k);
+    }
+  }
+}
+
+}  // namespace tcdec
+}  // namespace dec

@@ -103,6 +103,8 @@ def _load() -> ctypes.CDLL:
         "dec_debug_force_timeout": (ctypes.c_int, [vp, ctypes.c_int, vp]),
         "dec_debug_gemm_q4tc": (ctypes.c_int, [vp, ctypes.c_int, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
                                                vp, vp, vp]),
+        "dec_debug_gemm_btc": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
+                                              vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -228,6 +230,11 @@ def dec_debug_gemm_q4tc(x_hl: int, M: int, codes: int, sb: int, N: int, K: int, 
                         partials: int | None = None, counters: int | None = None, stream: int = 0) -> int:
     return _check(lib.dec_debug_gemm_q4tc(x_hl, M, codes, sb, N, K, S, out, partials, counters, stream),
                   "dec_debug_gemm_q4tc")
+
+
+def dec_debug_gemm_btc(x_hl: int, M: int, w: int, N: int, K: int, S: int, out: int, partials: int | None = None,
+                       counters: int | None = None, stream: int = 0) -> int:
+    return _check(lib.dec_debug_gemm_btc(x_hl, M, w, N, K, S, out, partials, counters, stream), "dec_debug_gemm_btc")
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
