@@ -139,7 +139,7 @@ struct dec_handle {
   // (the codes) and plain loads (scale and bias); the activation maps (map_u, map_o, map_g)
   // have 32-row boxes
   bool q4tc = false;
-  // the same for bf16 weights at 2..32 rows (k_gemm_btc): row-major weights read by TMA
+  // the same for bf16 weights at 1..32 rows (k_gemm_btc): row-major weights read by TMA
   bool btc = false;
   alignas(64) unsigned char map_u[128] = {}, map_o[128] = {}, map_g[128] = {};
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
@@ -393,7 +393,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
   ep.amax_key = h->amax_key;
   ep.status = h->status;
   ep.norm_w0 = h->layers[0].in_norm;
-  ep.xhl_out = h->rows > 1 || h->q4tc ? h->xh_u : nullptr;
+  ep.xhl_out = h->rows > 1 || h->q4tc || h->btc ? h->xh_u : nullptr;
   ep.T = h->tps;
   ep.tl = Timeline{h->timeline, 0};
   ep.V = c.vocab;
@@ -559,7 +559,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.eps = c.rms_eps;
     ap.out = h->attn_o;
     ap.status = h->status;
-    ap.out_hl = h->rows > 1 || h->q4tc ? h->xh_o : nullptr;
+    ap.out_hl = h->rows > 1 || h->q4tc || h->btc ? h->xh_o : nullptr;
     if (h->tps > 1) {
       // verify step: every row's K/V go into the cache before any row attends, so
       // that row (b, t) sees the rows (b, 0..t-1) of this step
@@ -744,8 +744,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // 4-bit weights, at most 32 rows (batch 1 included), hidden >= 2048: tcgen05 over the codes
   // expanded in shared memory, on the batched path's hi/lo activation planes
   h->q4tc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
-  const bool tc = h->rows > 1 || h->q4tc;
-  h->btc = h->rows > 1 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
+  h->btc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
+  const bool tc = h->rows > 1 || h->q4tc || h->btc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
   h->tblocks = h->rows > blk_tok ? (h->rows + blk_tok - 1) / blk_tok : 1;
