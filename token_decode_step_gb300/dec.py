@@ -226,6 +226,8 @@ def dec_debug_gemm_tc5(x_hl: int, M: int, w: int, N: int, K: int, out: int, pers
 
 def dec_debug_force_timeout(h: int, polls: int = 256, stream: int = 0) -> int:
     return _check(lib.dec_debug_force_timeout(h, polls, stream), "dec_debug_force_timeout")
+
+
 def dec_debug_gemm_q4tc(x_hl: int, M: int, codes: int, sb: int, N: int, K: int, S: int, out: int,
                         partials: int | None = None, counters: int | None = None, stream: int = 0) -> int:
     return _check(lib.dec_debug_gemm_q4tc(x_hl, M, codes, sb, N, K, S, out, partials, counters, stream),
