@@ -494,6 +494,14 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       qp.amax_key = h->amax_key;
       qp.argmax_out = sp.argmax;
       qp.status = h->status;
+      qp.pf_kv = gp.pf_kv;  // batch 1: the QKV launch prefetches the attention's K/V (as the GEMV does)
+      qp.pf_positions = gp.pf_positions;
+      qp.pf_plane_bytes = gp.pf_plane_bytes;
+      qp.pf_head_bytes = gp.pf_head_bytes;
+      qp.pf_B = gp.pf_B;
+      qp.pf_nkv = gp.pf_nkv;
+      qp.pf_row_bytes = gp.pf_row_bytes;
+      qp.pf_max_ctx = gp.pf_max_ctx;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
       s2 = check(h->q4tc ? launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi)
                          : launch_gemm_btc(lc, mx, L.tmap, qp, in_mode, epi),

@@ -122,6 +122,11 @@ struct Q4tcParams {
   unsigned long long* amax_key;      // lmhead: [M]
   int32_t* argmax_out;               // lmhead: [M]
   unsigned* status;                  // time-out flag (may be null)
+  // optional L2 prefetch of the next attention's cached K/V rows (as GemvParams); null: off
+  const unsigned char* pf_kv;
+  const int32_t* pf_positions;
+  unsigned long long pf_plane_bytes, pf_head_bytes;
+  int pf_B, pf_nkv, pf_row_bytes, pf_max_ctx;
 };
 
 // Fused q/k RMSNorm + RoPE + KV append + split-KV attention + LSE merge.
@@ -203,6 +208,35 @@ __device__ __forceinline__ void tl_mark(const Timeline& tl, int slot) {
 // Bulk prefetch of [src, src + bytes) into L2 (src and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// One CTA's share of the cached K/V rows (positions 0..P_b - 1 of every sequence b) that the
+// next attention reads, prefetched into L2 by `nlanes` lanes: the 2 B nkv runs (plane,
+// sequence, head) are dealt to the ncta CTAs round-robin, the CTAs of a run split it into equal
+// 16-byte-aligned byte ranges, issued in pieces of at most 32 KB.
+__device__ __forceinline__ void prefetch_kv_rows(const unsigned char* kv, const int32_t* positions,
+                                                 unsigned long long plane_bytes, unsigned long long head_bytes,
+                                                 int B, int nkv, int row_bytes, int max_ctx, int cta, int ncta,
+                                                 int lane, int nlanes) {
+  const int nruns = 2 * B * nkv;
+  const int run = cta % nruns, slice = cta / nruns;
+  const int nslices = (ncta - run + nruns - 1) / nruns;
+  const int plane = run / (B * nkv), bh = run % (B * nkv), b = bh / nkv;
+  int P = positions[b];
+  P = P < 0 ? 0 : (P >= max_ctx ? max_ctx - 1 : P);
+  const unsigned long long bytes = static_cast<unsigned long long>(P) * row_bytes;
+  const unsigned long long per = ((bytes + nslices - 1) / nslices + 15) / 16 * 16;
+  const unsigned long long off = per * slice;
+  if (off >= bytes) return;
+  const unsigned long long n = bytes - off < per ? bytes - off : per;
+  const unsigned char* src = kv + plane * plane_bytes + bh * head_bytes + off;
+  constexpr unsigned long long kPiece = 32768;
+  const unsigned long long npieces = (n + kPiece - 1) / kPiece;
+  for (unsigned long long i = lane; i < npieces; i += nlanes) {
+    const unsigned long long o = i * kPiece;
+    const unsigned long long m = n - o < kPiece ? n - o : kPiece;
+    prefetch_l2_bulk(src + o, static_cast<uint32_t>(m));
+  }
 }
 
 __device__ __forceinline__ void griddep_launch_dependents() {

@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tma_load_2d(st, &tm_x, g * kQK, 0, full);              // hi plane: tokens 0..31
         tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);  // lo plane
       }
+    } else if (p.pf_kv) {  // the producer warp's other lanes: the next attention's K/V into L2
+      prefetch_kv_rows(p.pf_kv, p.pf_positions, p.pf_plane_bytes, p.pf_head_bytes, p.pf_B, p.pf_nkv, p.pf_row_bytes,
+                       p.pf_max_ctx, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), lane - 1, 31);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer: one accumulator of the ring per group
