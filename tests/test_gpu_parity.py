@@ -93,8 +93,8 @@ CUSTOM = [
                        intermediate=1024, vocab=2049, prefill=63, steps=3, n_layers=2)),
     ("bf16_tile_edge", dict(head_dim=128, n_q_heads=2, n_kv_heads=1, hidden=128, intermediate=192, vocab=64,
                             prefill=127, steps=3)),
-    # 4-bit at batch 1, hidden >= 2048: the tcgen05 path on the batched hi/lo activation planes
-    ("q4_b1_tc5", dict(weight_format=synthetic.AFFINE4_G64, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=2048,
+    # 4-bit at batch 1, hidden 2048 (the tcgen05 paths start at 2 rows)
+    ("q4_b1_h2048", dict(weight_format=synthetic.AFFINE4_G64, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=2048,
                        intermediate=2880, vocab=1500, prefill=300, steps=3, n_layers=2)),
 ]
 

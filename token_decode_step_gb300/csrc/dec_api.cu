@@ -749,10 +749,11 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  // 4-bit weights, at most 32 rows (batch 1 included), hidden >= 2048: tcgen05 over the codes
-  // expanded in shared memory, on the batched path's hi/lo activation planes
-  h->q4tc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
-  h->btc = h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
+  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048: tcgen05
+  // on the batched path's hi/lo activation planes, 4-bit codes expanded in shared memory or
+  // bf16 weights streamed by TMA; one row stays on the batch-1 GEMV
+  h->q4tc = h->rows >= 2 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
+  h->btc = h->rows >= 2 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
   const bool tc = h->rows > 1 || h->q4tc || h->btc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
