@@ -5,7 +5,7 @@ and must agree with its own logits output (argmax = first index of the row's max
 
 Ties are built, not hoped for: (1) an all-zero lm_head makes every logit +0, so the whole
 vocabulary ties and the answer is index 0; (2) the lm_head row that won a first step is
-copied to rows 256, 512, ... above it (the same position inside every tile of 8, 16, 128
+copied to rows 256, 512, ... above and below it (the same position inside every tile of 8, 16, 128
 or 256 rows, so the copies take the same arithmetic and their logits are bit-identical,
 which the test checks) and the step is run again on the same inputs.
 Sources: Butter architecture.md, GPU sampling section (greedy = argmax over the vocab);
@@ -95,8 +95,9 @@ def test_copied_winner_row_ties_across_tiles(glue, name, fmt, batch, tps, hidden
     _consistent(logits, am, f"{name} first run")
     r0 = wl.batch * tps - 1  # the last row: for a prefill chunk, the row that yields the next token
     a = int(am[r0])
-    copies = [a + 256 * j for j in range(1, 8) if a + 256 * j < wl.vocab]
+    copies = [a + 256 * j for j in range(-7, 8) if j != 0 and 0 <= a + 256 * j < wl.vocab]
     assert len(copies) >= 3
+    want = min(copies + [a])  # the lowest index among the tied rows
     lm = model["lm_head"]
     for c in copies:
         if fmt == synthetic.BF16:
@@ -110,5 +111,5 @@ def test_copied_winner_row_ties_across_tiles(glue, name, fmt, batch, tps, hidden
         assert logits2[r0, c] == logits2[r0, a], f"{name}: copy {c} gives {logits2[r0, c]!r}, row {a} " \
                                                  f"{logits2[r0, a]!r}"
     assert logits2[r0, a] == logits[r0, a]
-    assert int(am2[r0]) == a, f"{name}: argmax {int(am2[r0])} among tied rows {[a] + copies}"
+    assert int(am2[r0]) == want, f"{name}: argmax {int(am2[r0])} among tied rows {sorted([a] + copies)}"
     _consistent(logits2, am2, f"{name} with copies")
