@@ -142,7 +142,10 @@ typedef struct dec_handle dec_handle;
 
 /* Validate cfg, allocate the handle's device memory, repack every weight into
    the handle's own layout (device-to-device, on an internal stream that is
-   synchronised before returning), and upload the RoPE frequency table.  The
+   synchronised before returning), and upload the RoPE frequency table.
+   (Butter architecture.md, dispatch-mode section: weight buffers are immutable after
+   load and bound once, the per-token state stays small; oxinfer crate page, "MLX
+   checkpoints": the affine 4-bit layout the packing reads.)  The
    caller may free its weight buffers once this returns.  Returns NULL on
    failure (see dec_last_error()).  Uses the current CUDA device. */
 DEC_API dec_handle *dec_create(const dec_config *cfg, const dec_weights *weights);
@@ -186,12 +189,16 @@ DEC_API dec_status dec_step_host(dec_handle *h, const int32_t *token_ids, const 
                     dec_stream_t stream);
 
 /* Free every device resource of the handle (caller buffers are untouched).
-   The caller must make sure no step of this handle is still running. */
+   The caller must make sure no step of this handle is still running.  (The end of
+   the load-time binding of Butter architecture.md, dispatch-mode section: what
+   dec_create bound once is released once.) */
 DEC_API void dec_destroy(dec_handle *h);
 
-/* Bytes of the KV cache for cfg (0 if cfg is NULL or invalid).  Plane 0 holds the keys
-   (after the per-head norm and RoPE), plane 1 the values; slot s of a sequence holds its
-   position s.
+/* Bytes of the KV cache for cfg (0 if cfg is NULL or invalid): the caller preallocates the
+   whole cache once and each step appends at offset = cache length (Butter architecture.md,
+   figure "SINGLE-TOKEN DECODE", cache.append; ANEForge "LLMs on the ANE", "Prefill and
+   decode": a resident KV cache).  Plane 0 holds the keys (after the per-head norm and
+   RoPE), plane 1 the values; slot s of a sequence holds its position s.
      DEC_KV_BF16: bf16 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim].
      DEC_KV_AFFINE8_G64: the codes, uint8 [n_layers][2][batch][n_kv_heads][max_ctx][head_dim],
        then, from the first multiple of 256 bytes after them, the (scale, bias) pairs, bf16
@@ -260,17 +267,23 @@ DEC_API dec_status dec_debug_gemm_btc(const void *x_hl, int M, const void *w, in
 DEC_API dec_status dec_kv_quantize(const float *src, int rows, int head_dim, uint8_t *codes, void *params,
                                    dec_stream_t stream);
 
-/* Message of the last failing call on this thread ("" if none). */
+/* Message of the last failing call on this thread ("" if none).  (The error side of a C
+   API over the engine, as the oxinfer crate page lists one, capi feature and
+   include/oxinfer.h; the page gives no error convention, so this one is a plain
+   status code plus a thread-local message.) */
 DEC_API const char *dec_last_error(void);
 
 /* Read and clear the device status word (call after synchronising the stream of
-   the steps in question).  *out receives the raw bits (1: token id out of range,
+   the steps in question).  The step never reads the token ids or positions back to the
+   host (Butter architecture.md, GPU sampling section: the greedy token stays on the
+   device, a 4-byte result), so range errors the kernels detect are recorded here.  *out receives the raw bits (1: token id out of range,
    2: position out of range, 4: bounded wait timed out).  Returns DEC_OK when the
    word was 0, DEC_ERR_DEVICE_INPUT / DEC_ERR_TIMEOUT otherwise. */
 DEC_API dec_status dec_get_device_status(dec_handle *h, int *out);
 
-/* Test hook: write the dequantised weights of one linear as float32 [out][in]
-   (row-major, canonical row order) to device memory `out`, computed from the
+/* Test hook (oxinfer crate page, "MLX checkpoints": w = scale * q + bias per group of
+   64, eight codes per uint32): write the dequantised weights of one linear as float32
+   [out][in] (row-major, canonical row order) to device memory `out`, computed from the
    handle's packed copy with the same nibble unpacking the GEMV kernels use and a
    single rounding (fmaf(scale, q, bias)); for bf16 the exact value.
    which: 0 q, 1 k, 2 v, 3 o, 4 gate, 5 up, 6 down, 7 lm_head (layer ignored). */
