@@ -46,8 +46,9 @@ NCU_TRAFFIC: dict = {
     "qwen3-0.6b": {"attention": {"bytes": 4263680, "alg": 4203008, "src": "attention", "csrc": "7606bcbf82634d56"}},
     "qwen3-8b-b1": {"gate_up": {"bytes": 201390080 + 2952192, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
     "qwen3-8b-b1-kv8": {"gate_up": {"bytes": 201390080 + 2952192, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
-    "qwen3-4b-q4": {"gate_up": {"bytes": 28075008, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
-    "qwen3-8b-b8": {"gate_up": {"bytes": 201520128 + 2948096, "src": "gemm_tc", "csrc": "560790667e6b9504"}},
+    "qwen3-4b-q4": {"gate_up": {"bytes": 28075008, "src": "gemv_q4r", "csrc": "26eb0a8e1ec81d9a"}},
+    "qwen3-8b-b8": {"gate_up": {"bytes": 201520128 + 2948096, "src": "gemm_tc", "csrc": "560790667e6b9504",
+                                "proj": [0, 1]}},
     "qwen3-8b-q4-b32": {"attention": {"bytes": 607751680 + 4087552, "alg": 606966272, "src": "attention",
                                       "csrc": "7606bcbf82634d56"}},
     "qwen3-8b-q4-b32-kv8": {"attention": {"bytes": 299072512 + 3900672, "alg": 298216720, "src": "attention",
@@ -59,7 +60,8 @@ NCU_TRAFFIC: dict = {
 # are unchanged)
 KERNEL_SOURCES = {
     "attention": ["k_attention.cu", "k_attention_q8.cu", "attn_common.cuh"],
-    "gemv": ["k_gemv1.cu", "q4.cuh"],
+    "gemv": ["k_gemv1.cu", "gemv_common.cuh", "q4.cuh"],
+    "gemv_q4r": ["k_gemv_q4r.cu", "gemv_common.cuh", "q4.cuh"],
     "gemm_tc": ["k_gemm_tc.cu", "q4.cuh"],
 }
 
@@ -204,7 +206,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     total = args.warmup + args.steps + args.profile_steps + args.e2e_steps + 2  # the repeats rewind
     wl = wl0.replace(steps=total)  # cache capacity for every step this run takes
     model = synthetic.generate(wl, device=dev)
-    dec = Decoder(wl, model)
+    dec = Decoder(wl, model, proj_kernels=args.proj)
     B, V = wl.batch, wl.vocab
     tokens = model["tokens"].clone()
     positions = model["positions"].clone()
@@ -296,8 +298,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     # of T prompt tokens per sequence) on the same weights and cache, one graph replay per
     # step, same tokens and positions every time (the K/V slots are rewritten with the
     # same values); its logits are not written (a prefill keeps only the cache)
-    def multi_token(T: int, n: int) -> float:
-        vdec = Decoder(wl, model, tokens_per_seq=T)
+    def multi_token(T: int, n: int) -> tuple[float, dict]:
+        vdec = Decoder(wl, model, tokens_per_seq=T, proj_kernels=args.proj)
         vt = torch.randint(0, V, (B * T,), dtype=torch.int32, device=dev)
         va = torch.empty((B * T,), dtype=torch.int32, device=dev)
         vpos = torch.zeros_like(positions) if T > 8 else positions.clone()
@@ -309,21 +311,29 @@ def run_ours(args, rank: int, world: int) -> dict | None:
             vdec.step(vt, vpos, kv, None, va, stream)
         v1.record(stream)
         torch.cuda.synchronize(dev)
+        # the same step with per-launch events: milliseconds per kernel class (attention
+        # includes the K/V append pass)
+        pm, pn = [0.0] * D.DEC_K_COUNT, [0] * D.DEC_K_COUNT
+        vdec.profile_step(vt, vpos, kv, None, va, pm, pn, stream)
+        torch.cuda.synchronize(dev)
         vdec.close()
-        return v0.elapsed_time(v1) / n
+        tot = sum(pm)
+        by_class = {name: {"ms": round(pm[c], 4), "share": round(pm[c] / tot, 4) if tot > 0 else None}
+                    for c, name in enumerate(D.KERNEL_CLASS_NAMES)}
+        return v0.elapsed_time(v1) / n, by_class
 
     verify = None
     if args.verify > 1:
         T = args.verify
-        vms = multi_token(T, 20)
-        verify = {"tokens_per_seq": T, "rows": B * T, "ms_per_verify": round(vms, 4),
+        vms, vcls = multi_token(T, 20)
+        verify = {"kernel_classes": vcls, "tokens_per_seq": T, "rows": B * T, "ms_per_verify": round(vms, 4),
                   "one_token_ms": round(ms / args.steps, 4), "verify_over_one": round(vms / (ms / args.steps), 3),
                   "tokens_checked_per_s": round(B * T / (vms / 1e3), 1)}
     prefill = None
     if args.prefill > 1:
         T = args.prefill
-        pms = multi_token(T, 5)
-        prefill = {"tokens_per_seq": T, "rows": B * T, "positions": "0 .. T-1 of every sequence",
+        pms, pcls = multi_token(T, 5)
+        prefill = {"kernel_classes": pcls, "tokens_per_seq": T, "rows": B * T, "positions": "0 .. T-1 of every sequence",
                    "ms_per_chunk": round(pms, 3), "prompt_tok_per_s": round(B * T / (pms / 1e3), 1)}
 
     per_step = [1, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, wl.n_layers, 1]  # launches per class
@@ -413,6 +423,8 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--proj", type=int, default=0, choices=[0, 1, 2],
+                    help="dec_config.proj_kernels of the 2..32-row projections: 0 auto, 1 mma.sync, 2 tcgen05")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--verify", type=int, default=0,
                     help="also time the multi-token verify step with this many tokens per sequence (2..8)")
@@ -500,6 +512,7 @@ def main():
         "kernel_share": {D.KERNEL_CLASS_NAMES[c]: round(cls_ms[c] / max(1e-12, sum(cls_ms)), 4)
                          for c in range(D.DEC_K_COUNT)},
     }
+    line["proj_kernels"] = {0: "auto", 1: "mma.sync", 2: "tcgen05"}[args.proj]
     line["sampling"] = r["sampling"]
     if r["verify"]:
         line["verify"] = r["verify"]
@@ -516,7 +529,8 @@ def main():
         line["roofline"].update({"achieved": round(ach, 1), "frac": round(ach / hbm_peak, 4),
                                  "bytes_per_launch": int(db), "avg_launch_ms": round(dom_avg_ms, 5)})
         tr = NCU_TRAFFIC.get(args.config, {}).get(dom_name)
-        if tr and tr.get("src") in KERNEL_SOURCES and tr.get("csrc") == csrc_digest(KERNEL_SOURCES[tr["src"]]):
+        if (tr and tr.get("src") in KERNEL_SOURCES and tr.get("csrc") == csrc_digest(KERNEL_SOURCES[tr["src"]])
+                and args.proj in tr.get("proj", [0, 1, 2])):
             if tr.get("alg"):  # captured at other cached lengths: scaled to this launch's algorithmic bytes
                 line["roofline"]["traffic"] = int(round(tr["bytes"] * db / tr["alg"]))
                 line["roofline"]["traffic_note"] = (f"ncu capture of {tr['bytes']} bytes for {tr['alg']} algorithmic "

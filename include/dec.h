@@ -102,6 +102,18 @@ typedef enum {
    T prompt tokens per sequence is a chunked prefill (the step before decode): it fills
    slots positions[b] .. positions[b] + T - 1 with the prompt's K/V in one forward, and the
    last row of each sequence gives the first generated token; logits_out may be NULL. */
+/* Kernel family of the projections of steps with 2..32 rows on models of hidden >= 2048 (a
+   batch of sequences, or the rows of a verify step).  Both compute the same products; AUTO
+   takes the one measured faster on this part, currently the mma.sync kernels over
+   fragment-packed weight tiles.  TCGEN05 selects the tensor-memory kernels (bf16 weights
+   streamed by TMA into tcgen05.mma; 4-bit codes expanded in shared memory with a per-group
+   accumulator readout). */
+typedef enum {
+    DEC_PROJ_AUTO = 0,
+    DEC_PROJ_MMA_SYNC = 1,
+    DEC_PROJ_TCGEN05 = 2
+} dec_projk;
+
 typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
     float rms_eps, rope_theta;
@@ -110,6 +122,7 @@ typedef struct {
     int tokens_per_seq;        /* new tokens per sequence and step: 1 (decode), 2..8 (verify), up to
                                   4096 (a prefill chunk); 0 = 1 */
     int kv_fmt;                /* dec_kvfmt of the KV cache (0 = bf16) */
+    int proj_kernels;          /* dec_projk (0 = AUTO); DEC_ERR_INVALID_ARG outside 0..2 */
 } dec_config;
 
 /* One linear layer, row-major [out][in] in device memory.  bf16: w only (scales,

@@ -94,6 +94,8 @@ def test_kv_quantize_rejects_bad_arguments(dec):
     (dict(batch=20, tokens_per_seq=4096), 2, "rows"),
     (dict(kv_fmt=3), 1, "kv_fmt"),
     (dict(kv_fmt=1, max_ctx=150), 2, "multiple of 16"),
+    (dict(proj_kernels=3), 1, "proj_kernels"),
+    (dict(proj_kernels=-1), 1, "proj_kernels"),
 ])
 def test_create_rejects_bad_config(dec, kw, status, msg):
     with pytest.raises(dec.DecError) as ei:

@@ -1,7 +1,8 @@
 """Exact argmax ties on the GPU: every lm_head epilogue (the batch-1 GEMV, the batched
-projections, the tensor-memory prefill projections) must return the lowest index among
-equal maxima, also when the equal logits sit in different vocab tiles and different CTAs,
-and must agree with its own logits output (argmax = first index of the row's maximum).
+projections on mma.sync and on tcgen05, the tensor-memory prefill projections) must return
+the lowest index among equal maxima, also when the equal logits sit in different vocab tiles
+and different CTAs, and must agree with its own logits output (argmax = first index of the
+row's maximum).
 
 Ties are built, not hoped for: (1) an all-zero lm_head makes every logit +0, so the whole
 vocabulary ties and the answer is index 0; (2) the lm_head row that won a first step is
@@ -20,7 +21,8 @@ import synthetic
 
 pytestmark = pytest.mark.gpu
 
-# name, weight format, batch, tokens per sequence, hidden: which lm_head epilogue runs
+# name, weight format, batch, tokens per sequence, hidden: which lm_head epilogue runs (the
+# tc_decode cases select the tcgen05 decode projections, dec_config.proj_kernels = 2)
 CASES = [
     ("gemv_bf16", synthetic.BF16, 1, 1, 256),
     ("gemv_q4", synthetic.AFFINE4_G64, 1, 1, 256),
@@ -28,6 +30,10 @@ CASES = [
     ("batched_q4_b12", synthetic.AFFINE4_G64, 12, 1, 256),
     ("batched_q4_b32", synthetic.AFFINE4_G64, 32, 1, 512),
     ("prefill_tc_bf16_t128", synthetic.BF16, 1, 128, 2048),
+    # hidden >= 2048 at 2..32 rows: the tcgen05 decode projections (bf16 weights by TMA, 4-bit
+    # codes expanded in shared memory)
+    ("tc_decode_bf16_b4", synthetic.BF16, 4, 1, 2048),
+    ("tc_decode_q4_b32", synthetic.AFFINE4_G64, 32, 1, 2048),
 ]
 
 
@@ -56,7 +62,8 @@ def _step(glue, wl, model, tps, kv):
     toks = torch.randint(0, wl.vocab, (rows,), generator=g, dtype=torch.int32).cuda()
     if tps == 1:
         toks = model["tokens"]
-    dec = glue.Decoder(wl, model, tokens_per_seq=tps)
+    proj = 2 if wl.name.startswith("tc_decode") else 0
+    dec = glue.Decoder(wl, model, tokens_per_seq=tps, proj_kernels=proj)
     try:
         logits = torch.empty((rows, wl.vocab), dtype=torch.float32, device="cuda")
         am = torch.empty((rows,), dtype=torch.int32, device="cuda")

@@ -22,7 +22,7 @@ def glue():
     return torch_glue
 
 
-def _run(glue, wl, steps, graph=True, full_kv_check=True, cache_weights=True, plan=None):
+def _run(glue, wl, steps, graph=True, full_kv_check=True, cache_weights=True, plan=None, proj=0):
     """Greedy loop of `steps` steps on the GPU, then the oracle replays the GPU's tokens.
 
     plan: [(sequences or None for all, number of leading steps)] to replay (default: every
@@ -31,7 +31,7 @@ def _run(glue, wl, steps, graph=True, full_kv_check=True, cache_weights=True, pl
     model = synthetic.generate(wl, device="cuda")
     host = synthetic.to_host(model)
     kv_init = np_model({"kv": host["kv"]})["kv"]
-    dec = glue.Decoder(wl, model)
+    dec = glue.Decoder(wl, model, proj_kernels=proj)
     dec.set_graph_mode(graph)
     try:
         gpu_steps, kv = gpu_greedy(dec, model, steps)
@@ -113,18 +113,26 @@ CUSTOM_BATCHED = [
                            n_layers=1)),
     ("b8_bf16_long_k", dict(batch=8, prefill=(50, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=4096,
                             intermediate=6144, vocab=700, steps=2, n_layers=1)),
-    # 4-bit, hidden >= 2048, at most 32 rows: the tcgen05 path over dequantized weight tiles
-    ("b3_q4_tc5", dict(batch=3, weight_format=synthetic.AFFINE4_G64, prefill=(0, 200), head_dim=128, n_q_heads=8,
+    # hidden >= 2048, at most 32 rows, the tcgen05 decode projections selected (proj 2): 4-bit
+    # codes expanded in shared memory, bf16 weights streamed by TMA
+    ("b3_q4_tc5", dict(proj=2, batch=3, weight_format=synthetic.AFFINE4_G64, prefill=(0, 200), head_dim=128, n_q_heads=8,
                        n_kv_heads=2, hidden=2048, intermediate=2880, vocab=1234, steps=2, n_layers=2)),
-    ("b20_q4_tc5", dict(batch=20, weight_format=synthetic.AFFINE4_G64, prefill=(5, 600), head_dim=64, n_q_heads=16,
+    ("b20_q4_tc5", dict(proj=2, batch=20, weight_format=synthetic.AFFINE4_G64, prefill=(5, 600), head_dim=64, n_q_heads=16,
                         n_kv_heads=4, hidden=2048, intermediate=5632, vocab=3001, steps=2, n_layers=1)),
+    ("b8_bf16_tc5", dict(proj=2, batch=8, prefill=(50, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=2048,
+                         intermediate=3072, vocab=1100, steps=2, n_layers=2)),
+    ("b32_q4_tc5_long_k", dict(proj=2, batch=32, weight_format=synthetic.AFFINE4_G64, prefill=(100, 400),
+                               head_dim=128, n_q_heads=4, n_kv_heads=1, hidden=2560, intermediate=4096, vocab=333,
+                               steps=2, n_layers=1)),
 ]
 
 
 @pytest.mark.parametrize("name,kw", CUSTOM_BATCHED, ids=[c[0] for c in CUSTOM_BATCHED])
 def test_custom_batched(glue, name, kw):
+    kw = dict(kw)
+    proj = kw.pop("proj", 0)
     wl = synthetic.custom(name=name, seed=sum(map(ord, name)), **kw)
-    w = _run(glue, wl, wl.steps)
+    w = _run(glue, wl, wl.steps, proj=proj)
     print(name, w)
 
 

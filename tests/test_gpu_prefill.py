@@ -36,6 +36,15 @@ CASES = [
     ("pf_b1_t129_q4_kv8", 129, dict(batch=1, weight_format=synthetic.AFFINE4_G64, head_dim=64, n_q_heads=4,
                                     n_kv_heads=2, hidden=320, intermediate=640, prefill=3, n_layers=2, vocab=400,
                                     kv_format=synthetic.AFFINE8_G64)),
+    # the causal prefill attention (16+ tokens, bf16 cache): one query head per KV head with a
+    # ragged last query tile; a chunk after a long cached prompt (many unmasked K/V tiles); the
+    # smallest chunk that takes it
+    ("pf_b2_t50_g1_bf16", 50, dict(batch=2, head_dim=64, n_q_heads=2, n_kv_heads=2, hidden=128, intermediate=256,
+                                   prefill=(60, 130), n_layers=1, vocab=300)),
+    ("pf_b1_t64_long_ctx", 64, dict(batch=1, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=256,
+                                    intermediate=512, prefill=3000, n_layers=1, vocab=300)),
+    ("pf_b3_t16_g4", 16, dict(batch=3, head_dim=128, n_q_heads=8, n_kv_heads=2, hidden=256, intermediate=512,
+                              prefill=(0, 70), n_layers=1, vocab=300)),
     # 128 rows or more with bf16 weights and hidden >= 2048: the tcgen05 projections (ragged token
     # and weight tiles, a vocabulary that is not a multiple of 4)
     ("pf_b1_t200_bf16_tc5", 200, dict(batch=1, head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=2048,

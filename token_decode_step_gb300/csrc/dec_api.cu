@@ -95,6 +95,7 @@ struct PackedLinear {
   void* w = nullptr;       // batch 1 and tcgen05 path: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
   uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
+  bool staged = false;     // batch-1 4-bit: the shared-memory staged GEMV (k_gemv_q4r)
   int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
   size_t w_bytes = 0, sb_bytes = 0;  // sizes of the two regions (sb_bytes 0 when sb is null)
 };
@@ -145,6 +146,10 @@ struct dec_handle {
   // batch 1: the QKV GEMV prefetches the attention's cached K/V rows into L2 (when a
   // layer's K/V at max_ctx takes at most a quarter of L2)
   bool kv_prefetch = false;
+  // prefill chunks (16+ tokens per sequence, bf16 cache): the causal attention that stages
+  // each K/V tile once for 64 query rows (k_attn_prefill) instead of one decode attention
+  // per row
+  bool attn_prefill = false;
 
   // packed weights (one allocation)
   unsigned char* wmem = nullptr;
@@ -232,6 +237,10 @@ dec_status validate(const dec_config* c) {
   }
   if (c->linear_fmt != DEC_W_BF16 && c->linear_fmt != DEC_W_AFFINE4_G64) {
     set_err("unknown linear_fmt %d", c->linear_fmt);
+    return DEC_ERR_INVALID_ARG;
+  }
+  if (c->proj_kernels < DEC_PROJ_AUTO || c->proj_kernels > DEC_PROJ_TCGEN05) {
+    set_err("unknown proj_kernels %d", c->proj_kernels);
     return DEC_ERR_INVALID_ARG;
   }
   if (c->n_q_heads % c->n_kv_heads != 0) {
@@ -439,6 +448,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     gp.counters = h->gemv_counters;
     gp.amax_key = h->amax_key;
     gp.argmax_out = sp.argmax;
+    gp.status = h->status;
     gp.tl = Timeline{h->timeline, launched - 1};
     if (kv_pf.kv) {
       gp.pf_kv = kv_pf.kv;
@@ -507,7 +517,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
                          : launch_gemm_btc(lc, mx, L.tmap, qp, in_mode, epi),
                  what);
     } else if (h->rows == 1) {
-      s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
+      s2 = check(L.staged ? launch_gemv_q4r(lc, gp, in_mode, epi) : launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
       GemmParams tp{};
       tp.w = L.w;
@@ -584,7 +594,9 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     ap.tl = Timeline{h->timeline, launched - 1};
     note(DEC_K_ATTN);
     ev_begin();
-    if ((st = check(launch_attention(lc, ap, d), "attention")) != DEC_OK) return st;
+    if ((st = check(h->attn_prefill ? launch_attn_prefill(lc, ap, d) : launch_attention(lc, ap, d), "attention")) !=
+        DEC_OK)
+      return st;
     ev_end();
 
     const __nv_bfloat16* after = (l + 1 < c.n_layers) ? h->layers[l + 1].in_norm : h->final_norm;
@@ -749,11 +761,13 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048: tcgen05
-  // on the batched path's hi/lo activation planes, 4-bit codes expanded in shared memory or
-  // bf16 weights streamed by TMA; one row stays on the batch-1 GEMV
-  h->q4tc = h->rows >= 2 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_AFFINE4_G64 && H >= 2048;
-  h->btc = h->rows >= 2 && h->rows <= q4tc_max_tokens() && fmt == DEC_W_BF16 && H >= 2048;
+  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048, when
+  // selected: tcgen05 on the batched path's hi/lo activation planes, 4-bit codes expanded in
+  // shared memory or bf16 weights streamed by TMA (DEC_PROJ_AUTO keeps the mma.sync kernels,
+  // measured faster at these row counts); one row stays on the batch-1 GEMV
+  const bool tc_rows = h->rows >= 2 && h->rows <= q4tc_max_tokens() && H >= 2048 && c.proj_kernels == DEC_PROJ_TCGEN05;
+  h->q4tc = tc_rows && fmt == DEC_W_AFFINE4_G64;
+  h->btc = tc_rows && fmt == DEC_W_BF16;
   const bool tc = h->rows > 1 || h->q4tc || h->btc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
@@ -794,6 +808,13 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       return L;
     }
     L.S = h->umma ? 1 : h->q4tc || h->btc ? q4tc_splits(N, K, h->num_sms) : choose_splits(N, K, fmt, h->num_sms);
+    if (h->rows == 1 && fmt == DEC_W_AFFINE4_G64 && !h->q4tc) {
+      const int S = gemv_q4r_splits(N, K, h->num_sms);
+      if (S > 0) {
+        L.S = S;
+        L.staged = true;
+      }
+    }
     if (fmt == DEC_W_BF16) {
       L.w_bytes = static_cast<size_t>(N) * K * 2;
       L.w = take(L.w_bytes);
@@ -938,6 +959,14 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail("upload inv_freq", e);
   if ((e = prepare_attention(d, G, c.kv_fmt)) != cudaSuccess) return fail("attention kernel attributes", e);
+  if (h->rows == 1 && fmt == DEC_W_AFFINE4_G64) {
+    const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
+    for (auto& cb : combos)
+      if ((e = prepare_gemv_q4r(cb[0], cb[1])) != cudaSuccess) return fail("staged GEMV kernel attributes", e);
+  }
+  h->attn_prefill = h->tps >= attn_prefill_min_tokens() && c.kv_fmt == DEC_KV_BF16;
+  if (h->attn_prefill && (e = prepare_attn_prefill(d, G)) != cudaSuccess)
+    return fail("prefill attention kernel attributes", e);
   if (h->umma) {  // tensor maps of every weight and of the activation planes, kernel attributes
     auto lmap = [&](PackedLinear& L) {
       L.tile_n = umma_tile_n(h->rows, L.N, h->num_sms);
@@ -1208,9 +1237,11 @@ extern "C" double dec_kernel_bytes(const dec_handle* h, int cls, double mean_cac
     case DEC_K_EMBED: return B * H * 2.0;
     case DEC_K_QKV: return (nq + 2 * nkv) * d * H * wb + H * 2.0;
     // every row reads its sequence's slots 0 .. P + t (t < T: its place among the step's rows);
-    // a slot is a bf16 row, or a row of codes and a (scale, bias) pair per 64
+    // a slot is a bf16 row, or a row of codes and a (scale, bias) pair per 64.  The prefill
+    // attention reads each sequence's slots 0 .. P + T - 1 once for all of its rows.
     case DEC_K_ATTN: {
       const double row = c.kv_fmt == DEC_KV_AFFINE8_G64 ? d + 4.0 * (d / 64.0) : 2.0 * d;
+      if (h->attn_prefill) return (B / T) * nkv * 2.0 * row * (mean_cached_len + T);
       return B * nkv * 2.0 * row * (mean_cached_len + 1.0 + (T - 1.0) / 2.0) + 2.0 * row;
     }
     case DEC_K_OPROJ: return H * nq * d * wb;

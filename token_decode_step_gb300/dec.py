@@ -27,6 +27,10 @@ DEC_W_AFFINE4_G64 = 1
 DEC_KV_BF16 = 0
 DEC_KV_AFFINE8_G64 = 1
 
+DEC_PROJ_AUTO = 0
+DEC_PROJ_MMA_SYNC = 1
+DEC_PROJ_TCGEN05 = 2
+
 DEC_K_EMBED, DEC_K_QKV, DEC_K_ATTN, DEC_K_OPROJ, DEC_K_GATEUP, DEC_K_DOWN, DEC_K_LMHEAD, DEC_K_COUNT = range(8)
 KERNEL_CLASS_NAMES = ["embed", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head"]
 
@@ -45,7 +49,7 @@ class DecConfig(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("intermediate", ctypes.c_int),
         ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
         ("linear_fmt", ctypes.c_int), ("batch", ctypes.c_int), ("max_ctx", ctypes.c_int),
-        ("tokens_per_seq", ctypes.c_int), ("kv_fmt", ctypes.c_int),
+        ("tokens_per_seq", ctypes.c_int), ("kv_fmt", ctypes.c_int), ("proj_kernels", ctypes.c_int),
     ]
 
 

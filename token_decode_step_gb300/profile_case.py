@@ -31,6 +31,8 @@ def main(argv=None) -> int:
     ap.add_argument("--vocab", type=int, default=0, help="0 keeps the workload's vocabulary")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--graph", action="store_true")
+    ap.add_argument("--proj", type=int, default=0, choices=[0, 1, 2],
+                    help="dec_config.proj_kernels: 0 auto, 1 mma.sync, 2 tcgen05 (2..32-row projections)")
     ap.add_argument("--tps", type=int, default=1,
                     help="tokens per sequence and step (> 1: a verify step or a prefill chunk from position 0)")
     a = ap.parse_args(argv)
@@ -40,7 +42,7 @@ def main(argv=None) -> int:
         kw["vocab"] = a.vocab
     wl = synthetic.WORKLOADS[a.config].replace(**kw)
     model = synthetic.generate(wl, device="cuda")
-    d = Decoder(wl, model, tokens_per_seq=a.tps)
+    d = Decoder(wl, model, tokens_per_seq=a.tps, proj_kernels=a.proj)
     d.set_graph_mode(a.graph)
     B = wl.batch
     rows = B * a.tps

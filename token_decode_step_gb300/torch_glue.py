@@ -22,12 +22,13 @@ def _ptr(t: torch.Tensor | None) -> int | None:
 
 
 def make_config(shape, batch: int | None = None, max_ctx: int | None = None,
-                tokens_per_seq: int = 1) -> dec.DecConfig:
+                tokens_per_seq: int = 1, proj_kernels: int = dec.DEC_PROJ_AUTO) -> dec.DecConfig:
     """dec_config from any object with the model-shape attributes (n_layers, hidden, ...,
     and optionally kv_format "bf16" / "affine8_g64")."""
     fmt = dec.DEC_W_BF16 if shape.weight_format == "bf16" else dec.DEC_W_AFFINE4_G64
     kv_fmt = dec.DEC_KV_AFFINE8_G64 if getattr(shape, "kv_format", "bf16") == "affine8_g64" else dec.DEC_KV_BF16
-    return dec.DecConfig(kv_fmt=kv_fmt, **_shape_fields(shape, fmt, batch, max_ctx, tokens_per_seq))
+    return dec.DecConfig(kv_fmt=kv_fmt, proj_kernels=proj_kernels,
+                         **_shape_fields(shape, fmt, batch, max_ctx, tokens_per_seq))
 
 
 def _shape_fields(shape, fmt, batch, max_ctx, tokens_per_seq) -> dict:
@@ -57,8 +58,8 @@ class Decoder:
     k_norm, q, k, v, o, gate, up, down])."""
 
     def __init__(self, shape, weights: dict, batch: int | None = None, max_ctx: int | None = None,
-                 tokens_per_seq: int = 1):
-        self.cfg = make_config(shape, batch, max_ctx, tokens_per_seq)
+                 tokens_per_seq: int = 1, proj_kernels: int = dec.DEC_PROJ_AUTO):
+        self.cfg = make_config(shape, batch, max_ctx, tokens_per_seq, proj_kernels)
         L = self.cfg.n_layers
         layers = (dec.DecLayerWeights * L)()
         for i, lw in enumerate(weights["layers"][:L]):
