@@ -258,13 +258,23 @@ DEC_API dec_status dec_debug_gemm_q4tc(const void *x_hl, int M, const void *code
                     int S, float *out, float *partials, unsigned *counters, dec_stream_t stream);
 
 /* Test hook: the bf16 form of the batched-decode tensor-core projection (weights streamed by TMA
-   into the MMA) on caller buffers, plain store: out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) w[n][k].
-     x_hl  device bf16 [2][M][K], 16-byte aligned, M in 1..32
-     w     device bf16 [N][K] row-major, 16-byte aligned
-     out, S, partials, counters  as in dec_debug_gemm_q4tc.
+   into the MMA, stream-K schedule) on caller buffers, plain store:
+   out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) w[n][k].
+     x_hl      device bf16 [2][M][K], 16-byte aligned, M in 1..32
+     w         device bf16 [N][K] row-major, 16-byte aligned
+     out       device float [M][N]
+     ctas      CTAs of the schedule (<= 0: one per SM); the tiles' 64-input stages are dealt to
+               them in contiguous ranges
+     partials  device float [K/64][M][N] (slots for the segments of a tile shared by CTAs)
+     counters  device uint32 [ceil(N / 128) + 1], zero, left zero
    K a positive multiple of 64, N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
-DEC_API dec_status dec_debug_gemm_btc(const void *x_hl, int M, const void *w, int N, int K, int S, float *out,
+DEC_API dec_status dec_debug_gemm_btc(const void *x_hl, int M, const void *w, int N, int K, int ctas, float *out,
                     float *partials, unsigned *counters, dec_stream_t stream);
+
+/* Test hook (host only, no CUDA call): the partial-result slots that the stream-K schedule of
+   dec_debug_gemm_btc needs for an N x K projection on `ctas` CTAs, i.e. the most CTAs that
+   share one 128-row tile; 0 for a non-positive argument. */
+DEC_API int dec_debug_btc_max_segments(int N, int K, int ctas);
 
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:

@@ -175,3 +175,18 @@ def test_attention_entry_points_reject_the_same_configs(dec, entry, kw, status, 
         st = dec.lib.dec_attention_noalloc(ctypes.byref(cfg), 0, 16, 16, 16, 16, 16, 16, None)
     assert st == status
     assert msg in dec.dec_last_error()
+
+
+def test_btc_schedule_segments(dec):
+    """Host side of the stream-K deal: the partial slots it asks for cover every tile's
+    segments (checked against a direct count of the CTA ranges)."""
+    for N, K, ctas in [(24576, 4096, 152), (4096, 12288, 152), (6144, 4096, 152), (128, 64, 152), (1000, 2560, 5)]:
+        tiles, kst = (N + 127) // 128, K // 64
+        total = tiles * kst
+        grid = min(total, ctas)
+        begin = [c * total // grid for c in range(grid + 1)]
+        most = 1
+        for t in range(tiles):
+            owners = {c for c in range(grid) if begin[c] < (t + 1) * kst and begin[c + 1] > t * kst}
+            most = max(most, len(owners))
+        assert dec.lib.dec_debug_btc_max_segments(N, K, ctas) == most

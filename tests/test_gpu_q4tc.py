@@ -61,12 +61,14 @@ def test_q4tc_gemm_matches_fp64(dec, M, N, K, S):
         assert int(counters.abs().sum()) == 0, "split counters not left zero"
 
 
-@pytest.mark.parametrize("M,N,K,S", [(8, 128, 64, 1), (8, 24576, 4096, 2), (16, 200, 512, 1), (32, 1000, 2560, 5),
-                                     (3, 130, 384, 3), (8, 4096, 12288, 4)])
-def test_btc_gemm_matches_fp64(dec, M, N, K, S):
-    """The bf16 form (dec_debug_gemm_btc): weights streamed by TMA into the MMA."""
+@pytest.mark.parametrize("M,N,K,ctas", [(8, 128, 64, 0), (8, 24576, 4096, 0), (16, 200, 512, 0), (32, 1000, 2560, 5),
+                                        (3, 130, 384, 3), (8, 4096, 12288, 0), (8, 6144, 4096, 7), (17, 300, 1024, 1)])
+def test_btc_gemm_matches_fp64(dec, M, N, K, ctas):
+    """The bf16 form (dec_debug_gemm_btc): weights streamed by TMA into the MMA, the tiles' stages
+    dealt stream-K to `ctas` CTAs (0: one per SM), so tiles split over several CTAs and their
+    segments added through the partial slots."""
     g = torch.Generator(device="cpu")
-    g.manual_seed(M * 11 + N + K + S)
+    g.manual_seed(M * 11 + N + K + ctas)
     x = torch.randn((M, K), generator=g, dtype=torch.float64)
     hi = x.to(torch.bfloat16)
     lo = (x - hi.double()).to(torch.bfloat16)
@@ -74,11 +76,10 @@ def test_btc_gemm_matches_fp64(dec, M, N, K, S):
     xhl = torch.stack([hi, lo]).contiguous().cuda()
     wd = w.contiguous().cuda()
     out = torch.full((M, N), float("nan"), device="cuda")
-    partials = torch.empty((S, M, N), device="cuda") if S > 1 else None
-    counters = torch.zeros(((N + 127) // 128 + 1,), dtype=torch.int32, device="cuda") if S > 1 else None
-    dec.dec_debug_gemm_btc(xhl.data_ptr(), M, wd.data_ptr(), N, K, S, out.data_ptr(),
-                           partials.data_ptr() if S > 1 else None, counters.data_ptr() if S > 1 else None,
-                           torch.cuda.current_stream().cuda_stream)
+    partials = torch.empty((K // 64, M, N), device="cuda")
+    counters = torch.zeros(((N + 127) // 128 + 1,), dtype=torch.int32, device="cuda")
+    dec.dec_debug_gemm_btc(xhl.data_ptr(), M, wd.data_ptr(), N, K, ctas, out.data_ptr(), partials.data_ptr(),
+                           counters.data_ptr(), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     xs = (hi.double() + lo.double()).numpy()
     wf = w.double().numpy()
@@ -88,5 +89,5 @@ def test_btc_gemm_matches_fp64(dec, M, N, K, S):
     assert np.isfinite(got).all(), "unwritten outputs"
     err = np.abs(got - ref)
     assert np.all(err <= 1e-5 * bound + 1e-6), f"max err {float(err.max()):.3e}"
-    if S > 1:
-        assert int(counters.abs().sum()) == 0, "split counters not left zero"
+    assert int(counters.abs().sum()) == 0, "tile counters not left zero"
+

@@ -807,7 +807,11 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       L.w = take(L.w_bytes);
       return L;
     }
-    L.S = h->umma ? 1 : h->q4tc || h->btc ? q4tc_splits(N, K, h->num_sms) : choose_splits(N, K, fmt, h->num_sms);
+    // (the stream-K bf16 kernel: S = the partial slots its schedule needs)
+    L.S = h->umma ? 1
+          : h->q4tc ? q4tc_splits(N, K, h->num_sms)
+          : h->btc ? btc_max_segments(N, K, h->num_sms)
+                   : choose_splits(N, K, fmt, h->num_sms);
     if (h->rows == 1 && fmt == DEC_W_AFFINE4_G64 && !h->q4tc) {
       const int S = gemv_q4r_splits(N, K, h->num_sms);
       if (S > 0) {
@@ -1367,13 +1371,13 @@ extern "C" dec_status dec_debug_gemm_q4tc(const void* x_hl, int M, const void* c
   return DEC_OK;
 }
 
-extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w, int N, int K, int S, float* out,
+extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w, int N, int K, int ctas, float* out,
                                          float* partials, unsigned* counters, dec_stream_t stream) {
   g_err[0] = 0;
-  if (!x_hl || !w || !out || M < 1 || M > q4tc_max_tokens() || N < 1 || K < 64 || K % 64 != 0 || S < 1 ||
-      (K / 64) % S != 0 || (S > 1 && (!partials || !counters)) || !aligned16(x_hl) || !aligned16(w)) {
-    set_err("dec_debug_gemm_btc: NULL or misaligned pointer, M outside 1..%d, N < 1, K not a positive multiple of "
-            "64, or S not dividing K / 64 (S > 1 needs partials and counters)",
+  if (!x_hl || !w || !out || !partials || !counters || M < 1 || M > q4tc_max_tokens() || N < 1 || K < 64 ||
+      K % 64 != 0 || !aligned16(x_hl) || !aligned16(w)) {
+    set_err("dec_debug_gemm_btc: NULL or misaligned pointer, M outside 1..%d, N < 1, or K not a positive multiple "
+            "of 64",
             q4tc_max_tokens());
     return DEC_ERR_INVALID_ARG;
   }
@@ -1388,13 +1392,18 @@ extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w,
   p.M = M;
   p.N = N;
   p.K = K;
-  p.S = S;
-  p.ctas = sms;
+  p.S = 1;
+  p.ctas = ctas > 0 ? ctas : sms;
   p.out = out;
   p.partials = partials;
   p.counters = counters;
   DEC_CUDA(launch_gemm_btc(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mw, p, kInPlain, kEpiStore));
   return DEC_OK;
+}
+
+extern "C" int dec_debug_btc_max_segments(int N, int K, int ctas) {
+  if (N < 1 || K < 64 || ctas < 1) return 0;
+  return btc_max_segments(N, K, ctas);
 }
 
 extern "C" dec_status dec_kv_quantize(const float* src, int rows, int head_dim, uint8_t* codes, void* params,

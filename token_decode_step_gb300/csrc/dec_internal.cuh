@@ -378,6 +378,7 @@ cudaError_t prepare_gemm_q4tc(int in_mode, int epi);
 cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* map_w, const Q4tcParams& p, int in_mode,
                             int epi);
 cudaError_t prepare_gemm_btc(int in_mode, int epi);
+int btc_max_segments(int N, int K, int ctas);  // partial-result slots of its stream-K schedule
 // causal attention of prefill chunks (k_attn_prefill.cu): bf16 cache, head_dim 64 or 128,
 // 1, 2 or 4 query heads per KV head; used from attn_prefill_min_tokens() tokens per sequence
 int attn_prefill_min_tokens();

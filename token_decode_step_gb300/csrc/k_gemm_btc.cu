@@ -9,12 +9,17 @@
 // bf16 hi and lo activation rows its N = 64 columns; both operands arrive by TMA as K-major
 // tiles in the 128-byte swizzle, so the weights stream from HBM straight into the MMA's A
 // operand.  The step is bound by that stream: one persistent CTA per SM keeps a 7-stage ring of
-// weight tiles in flight, and two accumulators in tensor memory let the epilogue of one unit
+// weight tiles in flight, and two accumulators in tensor memory let the epilogue of one segment
 // overlap the MMAs of the next.  Warp roles (192 threads): warp 0 issues the TMA copies, warp 1
-// allocates the accumulators and issues the MMAs, warps 2..5 run the epilogue.  A unit is a
-// (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile adds the S
-// partial results in split order (deterministic).  Every wait on a barrier is bounded: on
-// time-out the kernel flags the status word and stops.
+// allocates the accumulators and issues the MMAs, warps 2..5 run the epilogue.
+//
+// Work is dealt stream-K: the tiles' 64-input stages, tile-major, are split into one contiguous
+// range per CTA, so every SM streams the same number of weight bytes whatever the tile count
+// (a whole-tile or K-split deal leaves the last wave part-empty: 384 units of the 8B gate/up on
+// 152 SMs measured 49 us, 2.5 units a CTA).  A tile whose stages span several CTAs is computed
+// in segments; each segment's partial result goes to a slot of the partial buffer and the last
+// CTA to finish the tile adds the slots in K order (deterministic).  Every wait on a barrier is
+// bounded: on time-out the kernel flags the status word and stops.
 #include "tc_decode_epi.cuh"
 #include "umma_common.cuh"
 
@@ -61,8 +66,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kBM - 1) / kBM;
-  const int units = n_tiles * p.S;
-  const int gps = p.K / kBK / p.S;  // stages per unit
+  const int kst = p.K / kBK;  // stages per tile
+  const long long total = static_cast<long long>(n_tiles) * kst, grid = gridDim.x;
+  const long long g_begin = tcdec::sk_begin(blockIdx.x, total, grid), g_end = tcdec::sk_begin(blockIdx.x + 1, total, grid);
 
   if (warp == 1) {  // two accumulators of 64 columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(128)
@@ -89,28 +95,21 @@ __global__ void __launch_bounds__(kBThreads, 1)
 
   bool ok = true;
   if (warp == 0) {
-    if (lane == 0) {  // TMA producer; stage i of this CTA is stage i % gps of its unit i / gps
-      const int my_units = static_cast<int>(blockIdx.x) < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-      const int total = my_units * gps;
-      auto stage_of = [&](int i, int& tile, int& kb) {
-        const int u = blockIdx.x + (i / gps) * gridDim.x;
-        tile = u % n_tiles;
-        kb = (u / n_tiles) * gps + i % gps;
-      };
+    if (lane == 0) {  // TMA producer: stage i of this CTA is global stage g_begin + i
+      const int nst = static_cast<int>(g_end - g_begin);
       // the weights do not depend on upstream kernels: the first stages' are requested before
       // the grid-dependency wait, their activations after it
-      const int pre = total < kBStages ? total : kBStages;
+      const int pre = nst < kBStages ? nst : kBStages;
       for (int i = 0; i < pre; ++i) {
-        int tile, kb;
-        stage_of(i, tile, kb);
+        const long long g = g_begin + i;
         const uint32_t full = st_full + 8 * i, st = base + i * kBStage;
         mbar_expect_tx(full, kBStage);
-        tma_load_2d(st + kBX, &tm_w, kb * kBK, tile * kBM, full);
+        tma_load_2d(st + kBX, &tm_w, static_cast<int>(g % kst) * kBK, static_cast<int>(g / kst) * kBM, full);
       }
       griddep_wait();
-      for (int i = 0; i < total; ++i) {
-        int tile, kb;
-        stage_of(i, tile, kb);
+      for (int i = 0; i < nst; ++i) {
+        const long long g = g_begin + i;
+        const int kb = static_cast<int>(g % kst), tile = static_cast<int>(g / kst);
         const int s = i % kBStages;
         const uint32_t full = st_full + 8 * s, st = base + s * kBStage;
         if (i >= pre) {
@@ -129,9 +128,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
                        p.pf_max_ctx, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), lane - 1, 31);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer
+    if (lane == 0) {  // MMA issuer: one accumulator per segment (a run of one tile's stages)
       int it = 0, local = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+      for (long long g = g_begin; g < g_end && ok; ++local) {
+        const long long tile_end = (g / kst + 1) * kst, seg_end = tile_end < g_end ? tile_end : g_end;
         const int b = local & 1;
         if (local >= 2 && !mbar_wait(t_empty + 8 * b, ((local >> 1) - 1) & 1)) {
           ok = false;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         }
         fence_after();
         const uint32_t acc = tmem + 64 * b;
-        for (int j = 0; j < gps; ++j, ++it) {
+        for (bool first = true; g < seg_end; ++g, ++it, first = false) {
           const int s = it % kBStages;
           if (!mbar_wait(st_full + 8 * s, (it / kBStages) & 1)) {
             ok = false;
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           const uint64_t dx = sw128_desc(st), dw = sw128_desc(st + kBX);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
-            mma_bf16(acc, dw + 2 * k, dx + 2 * k, kBIdesc, (j | k) != 0 ? 1u : 0u);
+            mma_bf16(acc, dw + 2 * k, dx + 2 * k, kBIdesc, (!first || k != 0) ? 1u : 0u);
           commit(st_empty + 8 * s);
         }
         if (!ok) break;
@@ -173,8 +173,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
     }
     tcdec::epi_sync();
     int local = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
-      const int tile = u % n_tiles, split = u / n_tiles, b = local & 1;
+    for (long long g = g_begin; g < g_end; ++local) {
+      const int tile = static_cast<int>(g / kst), b = local & 1;
+      const long long tile_end = static_cast<long long>(tile + 1) * kst;
+      // the tile's segments: CTAs c_first .. c_last hold its stages, in K order
+      const int c_first = tcdec::sk_cta_of(static_cast<long long>(tile) * kst, total, grid);
+      const int c_last = tcdec::sk_cta_of(tile_end - 1, total, grid);
+      g = tile_end < g_end ? tile_end : g_end;
       if (ok && !mbar_wait(t_full + 8 * b, (local >> 1) & 1)) ok = false;
       fence_after();
       float y[kBT], yl[kBT];
@@ -185,7 +190,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll
       for (int t = 0; t < kBT; ++t) y[t] += yl[t];
       const int n = tile * kBM + r;
-      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, ok && n < p.N, et, lane, s_inv, s_best, s_ticket);
+      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, static_cast<int>(blockIdx.x) - c_first, c_last - c_first + 1,
+                                    ok && n < p.N, et, lane, s_inv, s_best, s_ticket);
     }
     if constexpr (EPI == kEpiLmHead) {
       tcdec::epi_sync();
@@ -216,9 +222,9 @@ template <int IN, int EPI>
 cudaError_t launch_btc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
                          bool prepare) {
   if (prepare) return cudaFuncSetAttribute(k_gemm_btc<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmem);
-  const int units = ((p.N + kBM - 1) / kBM) * p.S;
+  const long long stages = static_cast<long long>((p.N + kBM - 1) / kBM) * (p.K / kBK);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units < p.ctas ? units : p.ctas));
+  cfg.gridDim = dim3(static_cast<unsigned>(stages < p.ctas ? stages : p.ctas));
   cfg.blockDim = dim3(kBThreads);
   cfg.dynamicSmemBytes = kBSmem;
   cfg.stream = c.stream;
@@ -246,6 +252,19 @@ cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* m
                             int epi) {
   return dispatch_btc(c, *static_cast<const CUtensorMap*>(map_x), *static_cast<const CUtensorMap*>(map_w), p, in_mode,
                       epi, false);
+}
+
+// Partial-result slots the stream-K schedule needs for an N x K projection on `ctas` CTAs: the
+// most CTAs that share one tile (1: no tile is split)
+int btc_max_segments(int N, int K, int ctas) {
+  const long long n_tiles = (N + kBM - 1) / kBM, kst = K / kBK, total = n_tiles * kst;
+  const long long grid = total < ctas ? total : ctas;
+  int most = 1;
+  for (long long t = 0; t < n_tiles; ++t) {
+    const int segs = tcdec::sk_cta_of((t + 1) * kst - 1, total, grid) - tcdec::sk_cta_of(t * kst, total, grid) + 1;
+    most = segs > most ? segs : most;
+  }
+  return most;
 }
 
 cudaError_t prepare_gemm_btc(int in_mode, int epi) {

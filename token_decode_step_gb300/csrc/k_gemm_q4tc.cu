@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         sbw = sbn;
       }
       const bool live = ok && row_ok;
-      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, live, et, lane, s_inv, s_best, s_ticket);
+      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, p.S, live, et, lane, s_inv, s_best, s_ticket);
     }
     if constexpr (EPI == kEpiLmHead) {
       epi_sync();

@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(kRMaxConsumers + 32) k_gemv_q4r(GemvParams p) 
       prefetch_kv_rows(p.pf_kv, p.pf_positions, p.pf_plane_bytes, p.pf_head_bytes, p.pf_B, p.pf_nkv, p.pf_row_bytes,
                        p.pf_max_ctx, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), lane - 1, 31);
     }
-    griddep_launch_dependents();
+    // No griddepcontrol.launch_dependents here: the first thread of a CTA to execute it
+    // releases the dependent grid for that CTA, and a dependent reads data of the kernel
+    // before this one (the residual) before its own wait, relying on this kernel having
+    // passed its wait first.  The consumers release it after their wait.
   } else {
     // ---- consumers
     int u = blockIdx.x;

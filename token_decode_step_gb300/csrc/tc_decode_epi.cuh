@@ -1,15 +1,26 @@
 // The unit epilogue of the batched tcgen05 decode projections (k_gemm_q4tc.cu, k_gemm_btc.cu):
 // the thread holds weight row n of a 128-row tile and y[t], its results for the 32 token
-// columns.  With S > 1 K splits the partial results go to p.partials and the last CTA to finish
-// the tile adds them in split order; then the input RMSNorm's per-token 1/rms and the fused
-// epilogue (store / residual + next-norm hi/lo planes + sums of squares / SwiGLU / lm_head keys).
-// Called by the kernel's 128 epilogue threads together (named barrier 1).
+// columns.  When S > 1 pieces of the tile's K range were computed apart (K splits, or the
+// segments of a stream-K schedule), the partial results go to p.partials slot `split` and the
+// last CTA to finish the tile adds them in slot order; then the input RMSNorm's per-token
+// 1/rms and the fused epilogue (store / residual + next-norm hi/lo planes + sums of squares /
+// SwiGLU / lm_head keys).  Called by the kernel's 128 epilogue threads together (named barrier 1).
 #pragma once
 
 #include "dec_internal.cuh"
 
 namespace dec {
 namespace tcdec {
+
+// Stream-K schedule of the bf16 kernel: the n_tiles x (K / 64) stages, tile-major, are dealt
+// to `grid` CTAs in contiguous ranges [sk_begin(c), sk_begin(c + 1)); sk_cta_of(s) is the CTA
+// whose range holds stage s.  A tile's stages then fall to consecutive CTAs, one segment each.
+__host__ __device__ inline long long sk_begin(long long c, long long total, long long grid) {
+  return c * total / grid;
+}
+__host__ __device__ inline int sk_cta_of(long long s, long long total, long long grid) {
+  return static_cast<int>(((s + 1) * grid + total - 1) / total) - 1;
+}
 
 constexpr int kT = 32;  // token columns
 
@@ -22,10 +33,10 @@ __device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat
 
 template <int IN, int EPI>
 __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT], int n, int tile, int split,
-                                              bool live, int et, int lane, const float* s_inv,
+                                              int S, bool live, int et, int lane, const float* s_inv,
                                               unsigned long long* s_best, unsigned* s_ticket) {
   constexpr int kQT = kT;
-  if (p.S > 1) {  // partial results; the last CTA of the tile adds them in split order
+  if (S > 1) {  // partial results; the last CTA of the tile adds them in slot order
     if (live) {
 #pragma unroll
       for (int t = 0; t < kQT; ++t)
@@ -35,12 +46,12 @@ __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT
     epi_sync();
     if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
     epi_sync();
-    if (*s_ticket != static_cast<unsigned>(p.S - 1)) return;
+    if (*s_ticket != static_cast<unsigned>(S - 1)) return;
     __threadfence();
 #pragma unroll
     for (int t = 0; t < kQT; ++t) y[t] = 0.f;
     if (live)
-      for (int s = 0; s < p.S; ++s)
+      for (int s = 0; s < S; ++s)
 #pragma unroll
         for (int t = 0; t < kQT; ++t)
           if (t < p.M) y[t] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t) * p.N + n);

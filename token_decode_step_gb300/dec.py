@@ -109,6 +109,7 @@ def _load() -> ctypes.CDLL:
                                                vp, vp, vp]),
         "dec_debug_gemm_btc": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
                                               vp, vp]),
+        "dec_debug_btc_max_segments": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -238,9 +239,10 @@ def dec_debug_gemm_q4tc(x_hl: int, M: int, codes: int, sb: int, N: int, K: int, 
                   "dec_debug_gemm_q4tc")
 
 
-def dec_debug_gemm_btc(x_hl: int, M: int, w: int, N: int, K: int, S: int, out: int, partials: int | None = None,
-                       counters: int | None = None, stream: int = 0) -> int:
-    return _check(lib.dec_debug_gemm_btc(x_hl, M, w, N, K, S, out, partials, counters, stream), "dec_debug_gemm_btc")
+def dec_debug_gemm_btc(x_hl: int, M: int, w: int, N: int, K: int, ctas: int, out: int, partials: int,
+                       counters: int, stream: int = 0) -> int:
+    return _check(lib.dec_debug_gemm_btc(x_hl, M, w, N, K, ctas, out, partials, counters, stream),
+                  "dec_debug_gemm_btc")
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
