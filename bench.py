@@ -46,7 +46,7 @@ NCU_TRAFFIC: dict = {
     "qwen3-0.6b": {"attention": {"bytes": 4263680, "alg": 4203008, "src": "attention", "csrc": "7606bcbf82634d56"}},
     "qwen3-8b-b1": {"gate_up": {"bytes": 201390080 + 2952192, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
     "qwen3-8b-b1-kv8": {"gate_up": {"bytes": 201390080 + 2952192, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
-    "qwen3-4b-q4": {"gate_up": {"bytes": 28075008, "src": "gemv_q4r", "csrc": "26eb0a8e1ec81d9a"}},
+    "qwen3-4b-q4": {"gate_up": {"bytes": 28075008, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
     "qwen3-8b-b8": {"gate_up": {"bytes": 201520128 + 2948096, "src": "gemm_tc", "csrc": "560790667e6b9504",
                                 "proj": [0, 1]}},
     "qwen3-8b-q4-b32": {"attention": {"bytes": 607751680 + 4087552, "alg": 606966272, "src": "attention",
@@ -61,7 +61,6 @@ NCU_TRAFFIC: dict = {
 KERNEL_SOURCES = {
     "attention": ["k_attention.cu", "k_attention_q8.cu", "attn_common.cuh"],
     "gemv": ["k_gemv1.cu", "gemv_common.cuh", "q4.cuh"],
-    "gemv_q4r": ["k_gemv_q4r.cu", "gemv_common.cuh", "q4.cuh"],
     "gemm_tc": ["k_gemm_tc.cu", "q4.cuh"],
 }
 

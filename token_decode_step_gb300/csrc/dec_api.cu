@@ -95,7 +95,6 @@ struct PackedLinear {
   void* w = nullptr;       // batch 1 and tcgen05 path: bf16 [N][K] or uint32 [N][K/8]; batched: fragment tiles
   uint32_t* sb = nullptr;  // batch-1 q4 only: [N][K/64]
   int N = 0, K = 0, S = 1;
-  bool staged = false;     // batch-1 4-bit: the shared-memory staged GEMV (k_gemv_q4r)
   int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
   size_t w_bytes = 0, sb_bytes = 0;  // sizes of the two regions (sb_bytes 0 when sb is null)
 };
@@ -448,7 +447,6 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
     gp.counters = h->gemv_counters;
     gp.amax_key = h->amax_key;
     gp.argmax_out = sp.argmax;
-    gp.status = h->status;
     gp.tl = Timeline{h->timeline, launched - 1};
     if (kv_pf.kv) {
       gp.pf_kv = kv_pf.kv;
@@ -517,7 +515,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
                          : launch_gemm_btc(lc, mx, L.tmap, qp, in_mode, epi),
                  what);
     } else if (h->rows == 1) {
-      s2 = check(L.staged ? launch_gemv_q4r(lc, gp, in_mode, epi) : launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
+      s2 = check(launch_gemv1(lc, gp, h->wfmt, in_mode, epi), what);
     } else {
       GemmParams tp{};
       tp.w = L.w;
@@ -812,13 +810,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
           : h->q4tc ? q4tc_splits(N, K, h->num_sms)
           : h->btc ? btc_max_segments(N, K, h->num_sms)
                    : choose_splits(N, K, fmt, h->num_sms);
-    if (h->rows == 1 && fmt == DEC_W_AFFINE4_G64 && !h->q4tc) {
-      const int S = gemv_q4r_splits(N, K, h->num_sms);
-      if (S > 0) {
-        L.S = S;
-        L.staged = true;
-      }
-    }
     if (fmt == DEC_W_BF16) {
       L.w_bytes = static_cast<size_t>(N) * K * 2;
       L.w = take(L.w_bytes);
@@ -963,11 +954,6 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   if ((e = cudaMemcpyAsync(h->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return fail("upload inv_freq", e);
   if ((e = prepare_attention(d, G, c.kv_fmt)) != cudaSuccess) return fail("attention kernel attributes", e);
-  if (h->rows == 1 && fmt == DEC_W_AFFINE4_G64) {
-    const int combos[4][2] = {{kInNorm, kEpiStore}, {kInPlain, kEpiResid}, {kInNorm, kEpiSwiglu}, {kInNorm, kEpiLmHead}};
-    for (auto& cb : combos)
-      if ((e = prepare_gemv_q4r(cb[0], cb[1])) != cudaSuccess) return fail("staged GEMV kernel attributes", e);
-  }
   h->attn_prefill = h->tps >= attn_prefill_min_tokens() && c.kv_fmt == DEC_KV_BF16;
   if (h->attn_prefill && (e = prepare_attn_prefill(d, G)) != cudaSuccess)
     return fail("prefill attention kernel attributes", e);

@@ -61,7 +61,6 @@ struct GemvParams {
   const int32_t* pf_positions;    // [pf_B] cached positions P per sequence
   unsigned long long pf_plane_bytes, pf_head_bytes;  // one plane of a layer; one (sequence, head) run
   int pf_B, pf_nkv, pf_row_bytes, pf_max_ctx;
-  unsigned* status;               // the staged 4-bit kernel's time-out bit
 };
 
 // Batched (B >= 2) projection on tensor cores over fragment-packed weight tiles.
@@ -344,11 +343,6 @@ struct LaunchCtx {
 
 cudaError_t launch_embed(const LaunchCtx& c, const EmbedParams& p, int B);
 cudaError_t launch_gemv1(const LaunchCtx& c, const GemvParams& p, int wfmt, int in_mode, int epi);
-// batch-1 affine 4-bit GEMV with the weights staged in shared memory (k_gemv_q4r.cu):
-// K splits for an N x K projection, 0 if the shape does not suit the kernel
-int gemv_q4r_splits(int N, int K, int num_sms);
-cudaError_t launch_gemv_q4r(const LaunchCtx& c, const GemvParams& p, int in_mode, int epi);
-cudaError_t prepare_gemv_q4r(int in_mode, int epi);  // smem limit, before capture
 cudaError_t launch_attention(const LaunchCtx& c, const AttnParams& p, int head_dim);
 cudaError_t launch_kv_append(const LaunchCtx& c, const AttnParams& p, int head_dim);
 // batched tensor-core projection

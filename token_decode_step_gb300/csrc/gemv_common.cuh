@@ -1,4 +1,4 @@
-// Helpers of the batch-1 GEMV kernels (k_gemv1.cu, k_gemv_q4r.cu): the input chunk with the
+// Helpers of the batch-1 GEMV kernel (k_gemv1.cu): the input chunk with the
 // folded norm weight, the bf16 and affine 4-bit dot products of one chunk, SiLU, and the
 // warp sum of eight row sums at once.
 #pragma once

@@ -33,6 +33,9 @@ def main(argv=None) -> int:
     ap.add_argument("--graph", action="store_true")
     ap.add_argument("--proj", type=int, default=0, choices=[0, 1, 2],
                     help="dec_config.proj_kernels: 0 auto, 1 mma.sync, 2 tcgen05 (2..32-row projections)")
+    ap.add_argument("--sample", type=int, default=0,
+                    help="after the steps, this many dec_sample calls on the last step's logits "
+                         "(temperature 0.8, top_k 50, top_p 0.9)")
     ap.add_argument("--tps", type=int, default=1,
                     help="tokens per sequence and step (> 1: a verify step or a prefill chunk from position 0)")
     a = ap.parse_args(argv)
@@ -60,6 +63,14 @@ def main(argv=None) -> int:
         d.step(tok, pos, kv, logits, amax)
         if a.tps == 1:
             d.advance(amax, tok, pos)
+    if a.sample:
+        from token_decode_step_gb300 import dec as D
+        prm = D.SamplingParams(temperature=0.8, top_k=50, top_p=0.9, seed=1, offset=0, offset_device=None)
+        stok = torch.empty((rows,), dtype=torch.int32, device="cuda")
+        for i in range(a.sample):
+            prm.offset = i
+            D.dec_sample(logits.data_ptr(), rows, wl.vocab, prm, stok.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     st = d.device_status()
     d.close()
