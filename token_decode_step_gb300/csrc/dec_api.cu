@@ -986,7 +986,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       if ((e = cmap(L.qkv)) != cudaSuccess || (e = cmap(L.o)) != cudaSuccess || (e = cmap(L.gateup)) != cudaSuccess ||
           (e = cmap(L.down)) != cudaSuccess)
         return fail("tensor map", e);
-    const int tok = q4tc_max_tokens();
+    const int tok = h->q4tc ? q4tc_max_tokens() : btc_box_rows(h->rows);
     if ((e = umma_tensor_map(h->map_u, h->xh_u, 2 * h->rows, H, tok)) != cudaSuccess ||
         (e = umma_tensor_map(h->map_o, h->xh_o, 2 * h->rows, nq * d, tok)) != cudaSuccess ||
         (e = umma_tensor_map(h->map_g, h->xh_g, 2 * h->rows, I, tok)) != cudaSuccess)
@@ -1371,7 +1371,7 @@ extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w,
   int dev = 0, sms = 0;
   DEC_CUDA(cudaGetDevice(&dev));
   DEC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K, q4tc_max_tokens()));
+  DEC_CUDA(umma_tensor_map(mx, x_hl, 2 * M, K, btc_box_rows(M)));
   DEC_CUDA(umma_tensor_map(mw, w, N, K, 128));
   DEC_CUDA(prepare_gemm_btc(kInPlain, kEpiStore));
   Q4tcParams p{};

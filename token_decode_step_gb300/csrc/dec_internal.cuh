@@ -373,6 +373,7 @@ cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* m
                             int epi);
 cudaError_t prepare_gemm_btc(int in_mode, int epi);
 int btc_max_segments(int N, int K, int ctas);  // partial-result slots of its stream-K schedule
+int btc_box_rows(int M);                       // rows of its activation map's box for M tokens
 // causal attention of prefill chunks (k_attn_prefill.cu): bf16 cache, head_dim 64 or 128,
 // 1, 2 or 4 query heads per KV head; used from attn_prefill_min_tokens() tokens per sequence
 int attn_prefill_min_tokens();

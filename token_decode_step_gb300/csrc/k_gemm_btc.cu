@@ -5,12 +5,12 @@
 // Sources: Butter architecture.md, "SINGLE-TOKEN DECODE" (the projection sequence, here over a
 // batch of independent sequences).
 //
-// The 128 weight rows of a tile are the MMA's M (the accumulator's lanes) and the 32 tokens'
-// bf16 hi and lo activation rows its N = 64 columns; both operands arrive by TMA as K-major
-// tiles in the 128-byte swizzle, so the weights stream from HBM straight into the MMA's A
-// operand.  The step is bound by that stream: one persistent CTA per SM keeps a 7-stage ring of
-// weight tiles in flight, and two accumulators in tensor memory let the epilogue of one segment
-// overlap the MMAs of the next.  Warp roles (192 threads): warp 0 issues the TMA copies, warp 1
+// The 128 weight rows of a tile are the MMA's M (the accumulator's lanes) and the tokens' bf16
+// hi and lo activation rows its N columns (16 + 16 rows up to 16 tokens, 32 + 32 beyond); both
+// operands arrive by TMA as K-major tiles in the 128-byte swizzle, so the weights stream from
+// HBM straight into the MMA's A operand.  The step is bound by that stream: one persistent CTA
+// per SM keeps a ring of 8 or 10 weight tiles in flight, and two accumulators in tensor memory
+// let the epilogue of one segment overlap the MMAs of the next.  Warp roles (192 threads): warp 0 issues the TMA copies, warp 1
 // allocates the accumulators and issues the MMAs, warps 2..5 run the epilogue.
 //
 // Work is dealt stream-K: the tiles' 64-input stages, tile-major, are split into one contiguous
@@ -30,39 +30,50 @@ namespace {
 using namespace umma;
 
 constexpr int kBM = 128;                  // weight rows per tile
-constexpr int kBT = tcdec::kT;            // token rows (accumulator columns 0..31 hi, 32..63 lo)
+constexpr int kBT = tcdec::kT;            // most token rows
 constexpr int kBK = 64;                   // inputs per stage (one 128-byte row)
-constexpr int kBStages = 7;
-constexpr int kBX = 2 * kBT * kBK * 2;    // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
 constexpr int kBW = kBM * kBK * 2;        // 16 KB: 128 weight rows of 128 bytes
-constexpr int kBStage = kBX + kBW;
 constexpr int kBThreads = 192;
-constexpr int kBOffBar = kBStages * kBStage;
-constexpr int kBBars = 2 * kBStages + 4;
-constexpr int kBOffTmem = kBOffBar + 8 * kBBars;
-constexpr int kBOffInv = kBOffTmem + 16;
-constexpr int kBOffBest = kBOffInv + 4 * kBT;
-constexpr int kBOffTicket = kBOffBest + 8 * kBT;
-constexpr int kBSmem = 1024 + kBOffTicket + 16;
-// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
-constexpr uint32_t kBIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
-static_assert(kBStage % 1024 == 0 && kBX % 1024 == 0 && kBOffBar % 8 == 0 && kBOffBest % 8 == 0, "smem layout");
+constexpr int kBSmemBudget = 200 * 1024;  // stage ring
+
+// Activation tiles of MR rows (MR = 16 for up to 16 tokens, else 32): the hi rows, then the lo
+// rows, are the MMA's N = 2 MR columns; the stage ring takes what the budget holds (10 stages
+// at MR 16, 8 at MR 32), so fewer tokens keep more weight bytes in flight.
+template <int MR>
+struct BtcCfg {
+  static constexpr int kX = 2 * MR * kBK * 2;
+  static constexpr int kStage = kX + kBW;
+  static constexpr int kStages = kBSmemBudget / kStage;
+  static constexpr int kOffBar = kStages * kStage;
+  static constexpr int kBars = 2 * kStages + 4;
+  static constexpr int kOffTmem = kOffBar + 8 * kBars;
+  static constexpr int kOffInv = kOffTmem + 16;
+  static constexpr int kOffBest = kOffInv + 4 * kBT;
+  static constexpr int kOffTicket = kOffBest + 8 * kBT;
+  static constexpr int kSmem = 1024 + kOffTicket + 16;
+  // tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 2 MR, M = 128
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(2 * MR) >> 3) << 17) | ((128u >> 4) << 24);
+  static_assert(kStage % 1024 == 0 && kX % 1024 == 0 && kOffBar % 8 == 0 && kOffBest % 8 == 0, "smem layout");
+};
 
 }  // namespace
 
-template <int IN, int EPI>
+template <int IN, int EPI, int MR>
 __global__ void __launch_bounds__(kBThreads, 1)
     k_gemm_btc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, Q4tcParams p) {
+  using CF = BtcCfg<MR>;
+  constexpr int kBStages = CF::kStages, kBStage = CF::kStage, kBX = CF::kX;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
   unsigned char* smem = smem_raw + (base - raw);
-  const uint32_t st_full = base + kBOffBar, st_empty = st_full + 8 * kBStages;
+  const uint32_t st_full = base + CF::kOffBar, st_empty = st_full + 8 * kBStages;
   const uint32_t t_full = st_empty + 8 * kBStages, t_empty = t_full + 16;
-  const uint32_t tmem_slot = base + kBOffTmem;
-  float* s_inv = reinterpret_cast<float*>(smem + kBOffInv);
-  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + kBOffBest);
-  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + kBOffTicket);
+  const uint32_t tmem_slot = base + CF::kOffTmem;
+  float* s_inv = reinterpret_cast<float*>(smem + CF::kOffInv);
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + CF::kOffBest);
+  unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + CF::kOffTicket);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kBM - 1) / kBM;
@@ -91,7 +102,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   fence_before();
   __syncthreads();
   fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kBOffTmem);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + CF::kOffTmem);
 
   bool ok = true;
   if (warp == 0) {
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           mbar_expect_tx(full, kBStage);
           tma_load_2d(st + kBX, &tm_w, kb * kBK, tile * kBM, full);
         }
-        tma_load_2d(st, &tm_x, kb * kBK, 0, full);              // hi plane: tokens 0..31
+        tma_load_2d(st, &tm_x, kb * kBK, 0, full);              // hi plane: tokens 0..MR-1
         tma_load_2d(st + kBX / 2, &tm_x, kb * kBK, p.M, full);  // lo plane
       }
     } else if (p.pf_kv) {  // the producer warp's other lanes: the next attention's K/V into L2
@@ -150,7 +161,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
           const uint64_t dx = sw128_desc(st), dw = sw128_desc(st + kBX);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
-            mma_bf16(acc, dw + 2 * k, dx + 2 * k, kBIdesc, (!first || k != 0) ? 1u : 0u);
+            mma_bf16(acc, dw + 2 * k, dx + 2 * k, CF::kIdesc, (!first || k != 0) ? 1u : 0u);
           commit(st_empty + 8 * s);
         }
         if (!ok) break;
@@ -183,12 +194,19 @@ __global__ void __launch_bounds__(kBThreads, 1)
       if (ok && !mbar_wait(t_full + 8 * b, (local >> 1) & 1)) ok = false;
       fence_after();
       float y[kBT], yl[kBT];
-      tmem_ld32(tmem + 64 * b + tq, y);        // hi columns: tokens 0..31
-      tmem_ld32(tmem + 64 * b + 32 + tq, yl);  // lo columns
+      tmem_ld32(tmem + 64 * b + tq, y);  // hi columns 0..MR-1, then lo columns
+      if constexpr (MR == 32) tmem_ld32(tmem + 64 * b + 32 + tq, yl);
       fence_before();
       mbar_arrive(t_empty + 8 * b);
+      if constexpr (MR == 32) {
 #pragma unroll
-      for (int t = 0; t < kBT; ++t) y[t] += yl[t];
+        for (int t = 0; t < kBT; ++t) y[t] += yl[t];
+      } else {
+#pragma unroll
+        for (int t = 0; t < MR; ++t) y[t] += y[MR + t];
+#pragma unroll
+        for (int t = MR; t < kBT; ++t) y[t] = 0.f;
+      }
       const int n = tile * kBM + r;
       tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, static_cast<int>(blockIdx.x) - c_first, c_last - c_first + 1,
                                     ok && n < p.N, et, lane, s_inv, s_best, s_ticket);
@@ -218,22 +236,33 @@ __global__ void __launch_bounds__(kBThreads, 1)
 
 namespace {
 
-template <int IN, int EPI>
-cudaError_t launch_btc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
-                         bool prepare) {
-  if (prepare) return cudaFuncSetAttribute(k_gemm_btc<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBSmem);
+template <int IN, int EPI, int MR>
+cudaError_t launch_btc_mr(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
+                          bool prepare) {
+  constexpr int kSmem = BtcCfg<MR>::kSmem;
+  if (prepare) return cudaFuncSetAttribute(k_gemm_btc<IN, EPI, MR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   const long long stages = static_cast<long long>((p.N + kBM - 1) / kBM) * (p.K / kBK);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(stages < p.ctas ? stages : p.ctas));
   cfg.blockDim = dim3(kBThreads);
-  cfg.dynamicSmemBytes = kBSmem;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm_btc<IN, EPI>, mx, mw, p);
+  return cudaLaunchKernelEx(&cfg, k_gemm_btc<IN, EPI, MR>, mx, mw, p);
+}
+
+template <int IN, int EPI>
+cudaError_t launch_btc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
+                         bool prepare) {
+  if (prepare) {
+    const cudaError_t e = launch_btc_mr<IN, EPI, 16>(c, mx, mw, p, true);
+    return e != cudaSuccess ? e : launch_btc_mr<IN, EPI, 32>(c, mx, mw, p, true);
+  }
+  return p.M <= 16 ? launch_btc_mr<IN, EPI, 16>(c, mx, mw, p, false) : launch_btc_mr<IN, EPI, 32>(c, mx, mw, p, false);
 }
 
 cudaError_t dispatch_btc(const LaunchCtx& c, const CUtensorMap& mx, const CUtensorMap& mw, const Q4tcParams& p,
@@ -253,6 +282,9 @@ cudaError_t launch_gemm_btc(const LaunchCtx& c, const void* map_x, const void* m
   return dispatch_btc(c, *static_cast<const CUtensorMap*>(map_x), *static_cast<const CUtensorMap*>(map_w), p, in_mode,
                       epi, false);
 }
+
+// Rows of the activation map's box (hi rows, then lo rows of a stage) for M tokens
+int btc_box_rows(int M) { return M <= 16 ? 16 : 32; }
 
 // Partial-result slots the stream-K schedule needs for an N x K projection on `ctas` CTAs: the
 // most CTAs that share one tile (1: no tile is split)

@@ -82,37 +82,6 @@ __device__ __noinline__ void prefetch_kv_share(const GemvParams& p, int lane) {
   }
 }
 
-// [src, src + bytes) widened to 16-byte boundaries and prefetched into L2 (the packed weight
-// regions start on 256-byte boundaries and are padded to 256 bytes, so the widened range stays
-// inside them).
-__device__ __forceinline__ void prefetch_l2_range(const void* src, size_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(src) & ~static_cast<uintptr_t>(15);
-  const uintptr_t e = (reinterpret_cast<uintptr_t>(src) + bytes + 15) & ~static_cast<uintptr_t>(15);
-  prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(e - a));
-}
-
-// The weights (and 4-bit scale/bias words) of unit u into L2: one range when the unit is whole
-// rows (no K split), else one per row.
-template <int WF>
-__device__ __forceinline__ void prefetch_unit(const GemvParams& p, int u, int ntiles) {
-  const int tile = u % ntiles, split = u / ntiles;
-  const int row0 = tile * kGemvRows, nrows = min(kGemvRows, p.N - row0);
-  const size_t row_bytes = WF == kWBf16 ? static_cast<size_t>(p.K) * 2 : static_cast<size_t>(p.K) / 2;
-  const size_t split_bytes = WF == kWBf16 ? static_cast<size_t>(p.KS) * 2 : static_cast<size_t>(p.KS) / 2;
-  const unsigned char* w = static_cast<const unsigned char*>(p.w);
-  const unsigned char* sb = reinterpret_cast<const unsigned char*>(p.sb);
-  if (p.S == 1) {
-    prefetch_l2_range(w + row0 * row_bytes, nrows * row_bytes);
-    if constexpr (WF == kWQ4) prefetch_l2_range(sb + row0 * (p.K / 16), nrows * (p.K / 16));
-  } else {
-    for (int r = 0; r < nrows; ++r) {
-      prefetch_l2_range(w + (row0 + r) * row_bytes + split * split_bytes, split_bytes);
-      if constexpr (WF == kWQ4)
-        prefetch_l2_range(sb + (row0 + r) * (p.K / 16) + split * (p.KS / 16), p.KS / 16);
-    }
-  }
-}
-
 }  // namespace
 
 // Four CTAs of 256 threads per SM for bf16 (64 registers), three for the 4-bit decode.
@@ -183,10 +152,6 @@ __global__ void __launch_bounds__(256, (WF == kWBf16 ? 4 : 3)) k_gemv1(GemvParam
   if (tid == 0) s_best = 0ull;          // written and read by thread 0 only
 
   for (bool first = true; u < nunits; u += gridDim.x, first = false) {
-    // the unit after the next one into L2: its register loads, issued while this unit is
-    // reduced, then wait for L2 instead of DRAM
-    if (tid == nt - 1 && u + 2 * static_cast<int>(gridDim.x) < nunits)
-      prefetch_unit<WF>(p, u + 2 * static_cast<int>(gridDim.x), ntiles);
     const int tile = u % ntiles, split = u / ntiles;
     const int row0 = tile * R;
     const int nrows = min(R, p.N - row0);
