@@ -46,7 +46,7 @@ NCU_TRAFFIC: dict = {
     "qwen3-0.6b": {"attention": {"bytes": 4263680, "alg": 4203008, "src": "attention", "csrc": "7606bcbf82634d56"}},
     "qwen3-8b-b1": {"gate_up": {"bytes": 201391360 + 3057152, "src": "gemv", "csrc": "9b1e690fbc265ef7"}},
     "qwen3-8b-b1-kv8": {"gate_up": {"bytes": 201391360 + 3057152, "src": "gemv", "csrc": "9b1e690fbc265ef7"}},
-    "qwen3-4b-q4": {"gate_up": {"bytes": 28075008, "src": "gemv", "csrc": "26eb0a8e1ec81d9a"}},
+    "qwen3-4b-q4": {"gate_up": {"bytes": 28072448, "src": "gemv", "csrc": "9b1e690fbc265ef7"}},
     "qwen3-8b-b8": {"gate_up": {"bytes": 201520128 + 2948096, "src": "gemm_tc", "csrc": "560790667e6b9504",
                                 "proj": [0, 1]}},
     "qwen3-8b-q4-b32": {"attention": {"bytes": 607751680 + 4087552, "alg": 606966272, "src": "attention",

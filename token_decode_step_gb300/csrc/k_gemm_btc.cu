@@ -208,8 +208,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
         for (int t = MR; t < kBT; ++t) y[t] = 0.f;
       }
       const int n = tile * kBM + r;
-      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, static_cast<int>(blockIdx.x) - c_first, c_last - c_first + 1,
-                                    ok && n < p.N, et, lane, s_inv, s_best, s_ticket);
+      tcdec::unit_epilogue<IN, EPI, kBT, 128>(p, y, 0, n, tile, static_cast<int>(blockIdx.x) - c_first,
+                                              c_last - c_first + 1, ok && n < p.N, et, lane, s_inv, s_best,
+                                              s_ticket);
     }
     if constexpr (EPI == kEpiLmHead) {
       tcdec::epi_sync();

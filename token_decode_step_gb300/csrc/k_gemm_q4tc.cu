@@ -8,17 +8,19 @@
 //
 // Per group of 64 inputs the tensor cores compute D[n][t] = sum_k (q[n][k] - 8) x[t][k] with
 // the codes as exact bf16 integers: the 128 weight rows of a tile are the MMA's M (the
-// accumulator's lanes), the 32 tokens' bf16 hi and lo activation rows its N = 64 columns,
-// both operands K-major in the 128-byte swizzle.  The epilogue warps read every group's
-// accumulator from a ring of four in tensor memory and add s D + (b + 8 s) sum_k x[t][k] in
+// accumulator's lanes), the 32 tokens its N = 32 columns, both operands K-major in the 128-byte
+// swizzle; the activations' bf16 hi and lo halves are two further K steps against the same code
+// tile, so the accumulator holds the sum of both.  The epilogue warps read every group's
+// accumulator from a ring of eight in tensor memory and add s D + (b + 8 s) sum_k x[t][k] in
 // float32, in group order, so the scale and bias cost one multiply-add each per (row, token,
 // group) instead of a dequantization per weight.
 //
-// Warp roles (one persistent CTA per SM, 448 threads): warp 0 issues the TMA copies of the
+// Warp roles (one persistent CTA per SM, 576 threads): warp 0 issues the TMA copies of the
 // codes (128 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
 // warp 1 allocates the accumulator ring and issues the MMAs; warps 2..9 expand the codes into
 // bf16 (a byte permute builds 128 + q for two codes, an exact subtraction centres them) and sum
-// each token's inputs of the group; warps 10..13 scale, accumulate and run the fused epilogue.
+// each token's inputs of the group; warps 10..17 scale, accumulate and run the fused epilogue,
+// two warps per 32-lane quarter of the accumulator, 16 token columns each.
 // A unit is a (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
 // adds the S partial results in split order (deterministic).  Every wait on a barrier is
 // bounded: on time-out the kernel flags the status word and stops.
@@ -33,17 +35,18 @@ namespace {
 using namespace umma;
 
 constexpr int kQM = 128;                   // weight rows per tile
-constexpr int kQT = 32;                    // token rows (accumulator columns 0..31 hi, 32..63 lo)
+constexpr int kQT = 32;                    // token rows (accumulator columns)
 constexpr int kQK = 64;                    // inputs per stage: one group of the format
 constexpr int kQStages = 6;                // TMA ring: codes + activations
 constexpr int kQAStages = 4;               // expanded-code ring
-constexpr int kQG = 4;                     // accumulator ring (64 columns each) and sum-of-x ring
+constexpr int kQG = 8;                     // accumulator ring (32 columns each) and sum-of-x ring
 constexpr int kQCode = kQM * kQK / 2;      // 4 KB: 128 rows x 32 bytes of codes
 constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
 constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
 constexpr int kQA = kQM * kQK * 2;         // 16 KB: the expanded codes of a tile, bf16
 constexpr int kQDeq = 256;                 // expansion threads
-constexpr int kQThreads = 448;
+constexpr int kQEpi = 256;                 // epilogue threads
+constexpr int kQThreads = 64 + kQDeq + kQEpi;
 constexpr int kQOffS = kQAStages * kQA;
 constexpr int kQOffBar = kQOffS + kQStages * kQStage;
 constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 4 * kQG;
@@ -53,8 +56,8 @@ constexpr int kQOffInv = kQOffSx + 4 * kQG * kQT;
 constexpr int kQOffBest = kQOffInv + 4 * kQT;
 constexpr int kQOffTicket = kQOffBest + 8 * kQT;
 constexpr int kQSmem = 1024 + kQOffTicket + 16;
-// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
-constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 32, M = 128
+constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
 static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && kQOffBest % 8 == 0, "smem layout");
 
 using tcdec::epi_sync;
@@ -102,8 +105,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int units = n_tiles * p.S;
   const int gps = p.K / kQK / p.S;  // groups per split
 
-  if (warp == 1) {  // the accumulator ring: kQG x 64 columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(64 * kQG)
+  if (warp == 1) {  // the accumulator ring: kQG x 32 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(32 * kQG)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -118,9 +121,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     for (int b = 0; b < kQG; ++b) {
       mbar_init(g_full + 8 * b, 1);     // the MMAs' commit
-      mbar_init(g_empty + 8 * b, 128);  // the epilogue's accumulator reads
-      mbar_init(x_full + 8 * b, kQDeq); // the expanders' sums of x
-      mbar_init(x_empty + 8 * b, 128);  // the epilogue's reads of them
+      mbar_init(g_empty + 8 * b, kQEpi);  // the epilogue's accumulator reads
+      mbar_init(x_full + 8 * b, kQDeq);   // the expanders' sums of x
+      mbar_init(x_empty + 8 * b, kQEpi);  // the epilogue's reads of them
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -184,10 +187,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
           }
           fence_after();
-          const uint64_t dx = sw128_desc(sS + s * kQStage), da = sw128_desc(sA + a * kQA);
+          // the hi rows, then the lo rows, against the same code tile: D = sum (q - 8)(x_hi + x_lo)
+          const uint64_t dxh = sw128_desc(sS + s * kQStage), dxl = sw128_desc(sS + s * kQStage + kQX / 2);
+          const uint64_t da = sw128_desc(sA + a * kQA);
 #pragma unroll
           for (int k = 0; k < kQK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
-            mma_bf16(tmem + 64 * gb, da + 2 * k, dx + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
+            mma_bf16(tmem + 32 * gb, da + 2 * k, dxh + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < kQK / 16; ++k) mma_bf16(tmem + 32 * gb, da + 2 * k, dxl + 2 * k, kQIdesc, 1u);
           commit(a_empty + 8 * a);
           commit(st_empty + 8 * s);
           commit(g_full + 8 * gb);
@@ -195,9 +202,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
     }
   } else if (warp < 10) {
-    // expanders: the codes of weight row r, inputs 32 h .. 32 h + 31 of a group; and the sum of
+    // expanders: the codes of weight row r, inputs 32 h .. 32 h + 31 of a group (neighbouring
+    // lanes read neighbouring 16-byte chunks of the code tile: no bank conflicts); and the sum of
     // x over the group for token t (lanes 8 t' .. 8 t' + 7: hi row quarters, then lo row quarters)
-    const int dt = tid - 64, r = dt & (kQM - 1), h = dt >> 7;
+    const int dt = tid - 64, r = dt >> 1, h = dt & 1;
     const int xt = dt >> 3, xp = dt & 7, xrow = (xp < 4 ? 0 : kQT) + xt, xq = xp & 3;
     int it = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -251,13 +259,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         mbar_arrive(a_full + 8 * a);
       }
     }
-  } else {  // epilogue warps 10..13: accumulator lanes 32 q .. 32 q + 31, q = warp % 4
-    const int et = tid - 320, q = warp & 3, r = 32 * q + lane;
+  } else {  // epilogue warps 10..17: accumulator lanes 32 q .. 32 q + 31 (q = warp % 4), columns 16 c .. 16 c + 15
+    const int et = tid - 64 - kQDeq, q = warp & 3, c = (warp - 10) >> 2, r = 32 * q + lane;
     const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
+    constexpr int kTPT = kQT / 2;  // token columns per thread
     griddep_wait();  // the residual and the sums of squares are upstream outputs
     if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
-      for (int i = 0; i < kQT / 4; ++i) {
-        const int t = (warp - 10) * (kQT / 4) + i;
+      for (int i = 0; i < kQT / 8; ++i) {
+        const int t = (warp - 10) * (kQT / 8) + i;
         float sacc = 0.f;
         if (t < p.M)
           for (int k = lane; k < p.n_sumsq_in; k += 32) sacc += p.sumsq_in[static_cast<size_t>(t) * p.n_sumsq_in + k];
@@ -265,16 +274,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (lane == 0) s_inv[t] = t < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
       }
     }
-    epi_sync();
+    epi_sync<kQEpi>();
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int tile = u % n_tiles, split = u / n_tiles;
       const int n = tile * kQM + r;
       const bool row_ok = n < p.N;
       const uint32_t* sbrow = p.sb + static_cast<size_t>(row_ok ? n : 0) * (p.K / kGroup) + split * gps;
-      float y[kQT];
+      float y[kTPT];
 #pragma unroll
-      for (int t = 0; t < kQT; ++t) y[t] = 0.f;
+      for (int t = 0; t < kTPT; ++t) y[t] = 0.f;
       uint32_t sbw = __ldg(sbrow);
       for (int j = 0; j < gps; ++j, ++it) {
         const int gb = it % kQG;
@@ -282,22 +291,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (ok && (!mbar_wait(g_full + 8 * gb, (it / kQG) & 1) || !mbar_wait(x_full + 8 * gb, (it / kQG) & 1)))
           ok = false;
         fence_after();
-        float dh[kQT], dl[kQT];
-        tmem_ld32(tmem + 64 * gb + tq, dh);       // hi columns: tokens 0..31
-        tmem_ld32(tmem + 64 * gb + 32 + tq, dl);  // lo columns
+        float d[kTPT];
+        tmem_ld16(tmem + 32 * gb + kTPT * c + tq, d);  // tokens 16 c .. 16 c + 15
         fence_before();
         mbar_arrive(g_empty + 8 * gb);
         // w = s q + b = s (q - 8) + (b + 8 s): y += s D + (b + 8 s) sum x
         const float sc = sb_scale(sbw), bc = fmaf(8.0f, sc, sb_bias(sbw));
-        const float4* sxv = reinterpret_cast<const float4*>(s_x + gb * kQT);
+        const float4* sxv = reinterpret_cast<const float4*>(s_x + gb * kQT + kTPT * c);
 #pragma unroll
-        for (int t4 = 0; t4 < kQT / 4; ++t4) {
+        for (int t4 = 0; t4 < kTPT / 4; ++t4) {
           const float4 xv = sxv[t4];
           const float xs4[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int t = 4 * t4 + e;
-            y[t] = fmaf(sc, dh[t] + dl[t], y[t]);
+            y[t] = fmaf(sc, d[t], y[t]);
             y[t] = fmaf(bc, xs4[e], y[t]);
           }
         }
@@ -305,10 +313,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
         sbw = sbn;
       }
       const bool live = ok && row_ok;
-      tcdec::unit_epilogue<IN, EPI>(p, y, n, tile, split, p.S, live, et, lane, s_inv, s_best, s_ticket);
+      tcdec::unit_epilogue<IN, EPI, kTPT, kQEpi>(p, y, kTPT * c, n, tile, split, p.S, live, et, lane, s_inv, s_best,
+                                                 s_ticket);
     }
     if constexpr (EPI == kEpiLmHead) {
-      epi_sync();
+      epi_sync<kQEpi>();
       if (et < p.M && s_best[et] != 0ull) atomicMax(p.amax_key + et, s_best[et]);
     }
   }
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   fence_before();
   __syncthreads();
   if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(64 * kQG) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(32 * kQG) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
   if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
     __threadfence();

@@ -1,5 +1,5 @@
 // The unit epilogue of the batched tcgen05 decode projections (k_gemm_q4tc.cu, k_gemm_btc.cu):
-// the thread holds weight row n of a 128-row tile and y[t], its results for the 32 token
+// the thread holds weight row n of a 128-row tile and its results for TPT of the token
 // columns.  When S > 1 pieces of the tile's K range were computed apart (K splits, or the
 // segments of a stream-K schedule), the partial results go to p.partials slot `split` and the
 // last CTA to finish the tile adds them in slot order; then the input RMSNorm's per-token
@@ -25,47 +25,51 @@ __host__ __device__ inline int sk_cta_of(long long s, long long total, long long
 constexpr int kT = 32;  // token columns
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NTH = 128>
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NTH) : "memory");
+}
 __device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(v);
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-template <int IN, int EPI>
-__device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT], int n, int tile, int split,
-                                              int S, bool live, int et, int lane, const float* s_inv,
+// TPT tokens per thread, starting at token t0 (the thread's accumulator columns); NTH epilogue
+// threads take part in the named barrier.
+template <int IN, int EPI, int TPT, int NTH>
+__device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[TPT], int t0, int n, int tile,
+                                              int split, int S, bool live, int et, int lane, const float* s_inv,
                                               unsigned long long* s_best, unsigned* s_ticket) {
-  constexpr int kQT = kT;
   if (S > 1) {  // partial results; the last CTA of the tile adds them in slot order
     if (live) {
 #pragma unroll
-      for (int t = 0; t < kQT; ++t)
-        if (t < p.M) p.partials[(static_cast<size_t>(split) * p.M + t) * p.N + n] = y[t];
+      for (int i = 0; i < TPT; ++i)
+        if (t0 + i < p.M) p.partials[(static_cast<size_t>(split) * p.M + t0 + i) * p.N + n] = y[i];
     }
     __threadfence();
-    epi_sync();
+    epi_sync<NTH>();
     if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
-    epi_sync();
+    epi_sync<NTH>();
     if (*s_ticket != static_cast<unsigned>(S - 1)) return;
     __threadfence();
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) y[t] = 0.f;
+    for (int i = 0; i < TPT; ++i) y[i] = 0.f;
     if (live)
       for (int s = 0; s < S; ++s)
 #pragma unroll
-        for (int t = 0; t < kQT; ++t)
-          if (t < p.M) y[t] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t) * p.N + n);
+        for (int i = 0; i < TPT; ++i)
+          if (t0 + i < p.M) y[i] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t0 + i) * p.N + n);
     if (et == 0) p.counters[tile] = 0u;
   }
   if constexpr (IN == kInNorm) {
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) y[t] *= s_inv[t];
+    for (int i = 0; i < TPT; ++i) y[i] *= s_inv[t0 + i];
   }
   if constexpr (EPI == kEpiStore) {
     if (live) {
 #pragma unroll
-      for (int t = 0; t < kQT; ++t)
-        if (t < p.M) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
+      for (int i = 0; i < TPT; ++i)
+        if (t0 + i < p.M) p.out[static_cast<size_t>(t0 + i) * p.N + n] = y[i];
     }
   } else if constexpr (EPI == kEpiResid) {
     // h += y; the next consumer's input h * next_norm as hi, lo planes; sums of squares per
@@ -73,12 +77,13 @@ __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT
     const float nw = live ? bf16_to_f(p.next_norm_w[n]) : 0.f;
     const size_t plane = static_cast<size_t>(p.M) * p.N;
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) {
+    for (int i = 0; i < TPT; ++i) {
+      const int t = t0 + i;
       float hn = 0.f;
       const bool on = live && t < p.M;
       if (on) {
         const size_t o = static_cast<size_t>(t) * p.N + n;
-        hn = p.out[o] + y[t];
+        hn = p.out[o] + y[i];
         p.out[o] = hn;
         __nv_bfloat16 hi, lo;
         split_hl(hn * nw, hi, lo);
@@ -97,10 +102,11 @@ __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT
     const size_t plane = static_cast<size_t>(p.M) * (p.N / 2);
     const int o = (n >> 3) * 4 + (n & 3);
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) {
-      const float up = __shfl_xor_sync(0xffffffffu, y[t], 4);
+    for (int i = 0; i < TPT; ++i) {
+      const int t = t0 + i;
+      const float up = __shfl_xor_sync(0xffffffffu, y[i], 4);
       if (live && (n & 4) == 0 && t < p.M) {
-        const float gv = silu(y[t]) * up;
+        const float gv = silu(y[i]) * up;
         const size_t oo = static_cast<size_t>(t) * (p.N / 2) + o;
         p.out[oo] = gv;
         __nv_bfloat16 hi, lo;
@@ -111,10 +117,11 @@ __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[kT
     }
   } else {  // lm_head: logits, and every token's best (value, index) key over the warp's rows
 #pragma unroll
-    for (int t = 0; t < kQT; ++t) {
+    for (int i = 0; i < TPT; ++i) {
+      const int t = t0 + i;
       const bool on = live && t < p.M;
-      if (on && p.out) p.out[static_cast<size_t>(t) * p.N + n] = y[t];
-      unsigned long long k = on ? argmax_key(y[t], n) : 0ull;
+      if (on && p.out) p.out[static_cast<size_t>(t) * p.N + n] = y[i];
+      unsigned long long k = on ? argmax_key(y[i], n) : 0ull;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const unsigned long long other = __shfl_xor_sync(0xffffffffu, k, o);
