@@ -10,7 +10,11 @@
 namespace dec {
 namespace umma {
 
-constexpr uint32_t kWaitPolls = 1u << 22;  // bounded waits: the caller flags a time-out
+// Bounded waits: a waiting thread is suspended in each poll until the phase completes or about
+// kWaitHintNs pass (so waiting warps do not take issue slots from working ones); after
+// kWaitPolls polls (a few seconds) the caller flags a time-out.
+constexpr uint32_t kWaitPolls = 1u << 20;
+constexpr uint32_t kWaitHintNs = 4000;
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -24,9 +28,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kWaitHintNs)
       : "memory");
   return ok != 0;
 }
