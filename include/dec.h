@@ -103,11 +103,11 @@ typedef enum {
    slots positions[b] .. positions[b] + T - 1 with the prompt's K/V in one forward, and the
    last row of each sequence gives the first generated token; logits_out may be NULL. */
 /* Kernel family of the projections of steps with 2..32 rows on models of hidden >= 2048 (a
-   batch of sequences, or the rows of a verify step).  Both compute the same products; AUTO
-   takes the one measured faster on this part, currently the mma.sync kernels over
-   fragment-packed weight tiles.  TCGEN05 selects the tensor-memory kernels (bf16 weights
-   streamed by TMA into tcgen05.mma; 4-bit codes expanded in shared memory with a per-group
-   accumulator readout). */
+   batch of sequences, or the rows of a verify step).  Both compute the same products.
+   TCGEN05 selects the tensor-memory kernels (bf16 weights streamed by TMA into tcgen05.mma;
+   4-bit codes expanded in shared memory with a per-group accumulator readout), MMA_SYNC the
+   mma.sync kernels over fragment-packed weight tiles.  AUTO takes what measured faster on
+   this part, currently mma.sync. */
 typedef enum {
     DEC_PROJ_AUTO = 0,
     DEC_PROJ_MMA_SYNC = 1,

@@ -108,7 +108,8 @@ CUSTOM_BATCHED = [
                    n_kv_heads=2, hidden=256, intermediate=640, vocab=999, steps=3, n_layers=2)),
     ("b20_q4", dict(batch=20, weight_format=synthetic.AFFINE4_G64, prefill=(0, 1500), head_dim=64, n_q_heads=4,
                     n_kv_heads=1, hidden=320, intermediate=768, vocab=2000, steps=2, n_layers=2)),
-    ("b32_q4_long_k", dict(batch=32, weight_format=synthetic.AFFINE4_G64, prefill=(100, 400), head_dim=128,
+    # 32 rows of 4-bit weights at hidden >= 2048, mma.sync selected explicitly (proj 1)
+    ("b32_q4_long_k", dict(proj=1, batch=32, weight_format=synthetic.AFFINE4_G64, prefill=(100, 400), head_dim=128,
                            n_q_heads=4, n_kv_heads=1, hidden=2560, intermediate=4096, vocab=333, steps=2,
                            n_layers=1)),
     ("b8_bf16_long_k", dict(batch=8, prefill=(50, 300), head_dim=128, n_q_heads=4, n_kv_heads=2, hidden=4096,
