@@ -502,6 +502,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       qp.amax_key = h->amax_key;
       qp.argmax_out = sp.argmax;
       qp.status = h->status;
+      qp.tl = gp.tl;
       qp.pf_kv = gp.pf_kv;  // batch 1: the QKV launch prefetches the attention's K/V (as the GEMV does)
       qp.pf_positions = gp.pf_positions;
       qp.pf_plane_bytes = gp.pf_plane_bytes;

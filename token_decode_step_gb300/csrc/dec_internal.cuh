@@ -107,6 +107,7 @@ struct UmmaParams {
 // M <= 32 token rows; X as bf16 hi, lo planes [2][M][K] read through a TMA tensor map (boxes of
 // 32 rows), W as row-major codes [N][K/2] bytes (a TMA tensor map) and sb words [N][K/64].
 struct Q4tcParams {
+  Timeline tl;
   int M, N, K, S;           // tokens (<= 32), weight rows, inputs (multiple of 64), K splits (dividing K / 64)
   int ctas;                 // persistent CTAs (one per SM)
   const uint32_t* sb;       // (scale | bias << 16) [N][K/64]

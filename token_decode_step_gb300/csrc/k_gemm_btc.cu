@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + CF::kOffBest);
   unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + CF::kOffTicket);
 
+  tl_mark(p.tl, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kBM - 1) / kBM;
   const int kst = p.K / kBK;  // stages per tile
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
         tma_load_2d(st + kBX, &tm_w, static_cast<int>(g % kst) * kBK, static_cast<int>(g / kst) * kBM, full);
       }
       griddep_wait();
+      tl_mark(p.tl, 1);
       for (int i = 0; i < nst; ++i) {
         const long long g = g_begin + i;
         const int kb = static_cast<int>(g % kst), tile = static_cast<int>(g / kst);
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
   griddep_launch_dependents();
   fence_before();
   __syncthreads();
+  tl_mark(p.tl, 2);
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(128) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
   if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   unsigned long long* s_best = reinterpret_cast<unsigned long long*>(smem + kQOffBest);
   unsigned* s_ticket = reinterpret_cast<unsigned*>(smem + kQOffTicket);
 
+  tl_mark(p.tl, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.N + kQM - 1) / kQM;
   const int units = n_tiles * p.S;
@@ -155,6 +156,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
       }
       griddep_wait();
+      tl_mark(p.tl, 1);
       for (int i = 0; i < total; ++i) {
         int tile, g;
         group_of(i, tile, g);
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   griddep_launch_dependents();
   fence_before();
   __syncthreads();
+  tl_mark(p.tl, 2);
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(32 * kQG) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
