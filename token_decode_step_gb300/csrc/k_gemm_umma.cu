@@ -330,21 +330,23 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;
     const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
     unsigned long long best = 0ull;
-    int local = 0;
+    int local = 0, r_mt = -1;
+    float r = 1.f;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles, b = local & 1;
       const int tok = mt * kUM + 32 * q + lane;
       const bool live = tok < p.M;
-      float r = 1.f;
-      if constexpr (IN == kInNorm) {  // this warp's 32 tokens: lanes share each token's sum
-        for (int j = 0; j < 32; ++j) {
-          const int tj = mt * kUM + 32 * q + j;
-          float sj = 0.f;
-          if (tj < p.M)
-            for (int i = lane; i < p.n_sumsq_in; i += 32) sj += p.sumsq_in[static_cast<size_t>(tj) * p.n_sumsq_in + i];
-          sj = warp_sum(sj);
-          if (lane == j) r = rsqrtf(sj / static_cast<float>(p.K) + p.eps);
+      if (IN == kInNorm && mt != r_mt) {  // the lane's token's 1/rms, once per token tile
+        float sj = 0.f;
+        if (live) {  // its row of partial sums (n_sumsq_in a multiple of 8), independent loads
+          const float4* row = reinterpret_cast<const float4*>(p.sumsq_in + static_cast<size_t>(tok) * p.n_sumsq_in);
+          for (int i = 0; i < p.n_sumsq_in / 4; ++i) {
+            const float4 v = __ldg(row + i);
+            sj += (v.x + v.y) + (v.z + v.w);
+          }
         }
+        r = rsqrtf(sj / static_cast<float>(p.K) + p.eps);
+        r_mt = mt;
       }
       if (!mbar_wait(bar_tfull + 8 * b, (local >> 1) & 1)) ok = false;
       fence_after();
