@@ -175,13 +175,16 @@ __global__ void __launch_bounds__(kBThreads, 1)
     const uint32_t tq = static_cast<uint32_t>(32 * q) << 16;
     griddep_wait();  // the residual and the sums of squares are upstream outputs
     if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
-      for (int i = 0; i < kBT / 4; ++i) {
-        const int t = (warp - 2) * (kBT / 4) + i;
+      if (warp == 2) {  // lane t sums token t's row of partial sums (a multiple of 8), independent loads
         float sacc = 0.f;
-        if (t < p.M)
-          for (int k = lane; k < p.n_sumsq_in; k += 32) sacc += p.sumsq_in[static_cast<size_t>(t) * p.n_sumsq_in + k];
-        sacc = warp_sum(sacc);
-        if (lane == 0) s_inv[t] = t < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
+        if (lane < p.M) {
+          const float4* row = reinterpret_cast<const float4*>(p.sumsq_in + static_cast<size_t>(lane) * p.n_sumsq_in);
+          for (int k = 0; k < p.n_sumsq_in / 4; ++k) {
+            const float4 v = __ldg(row + k);
+            sacc += (v.x + v.y) + (v.z + v.w);
+          }
+        }
+        s_inv[lane] = lane < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
       }
     }
     tcdec::epi_sync();

@@ -267,13 +267,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
     constexpr int kTPT = kQT / 2;  // token columns per thread
     griddep_wait();  // the residual and the sums of squares are upstream outputs
     if constexpr (IN == kInNorm) {  // per-token 1/rms of the residual (the fused RMSNorm)
-      for (int i = 0; i < kQT / 8; ++i) {
-        const int t = (warp - 10) * (kQT / 8) + i;
+      if (warp == 10) {  // lane t sums token t's row of partial sums (a multiple of 8), independent loads
         float sacc = 0.f;
-        if (t < p.M)
-          for (int k = lane; k < p.n_sumsq_in; k += 32) sacc += p.sumsq_in[static_cast<size_t>(t) * p.n_sumsq_in + k];
-        sacc = warp_sum(sacc);
-        if (lane == 0) s_inv[t] = t < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
+        if (lane < p.M) {
+          const float4* row = reinterpret_cast<const float4*>(p.sumsq_in + static_cast<size_t>(lane) * p.n_sumsq_in);
+          for (int k = 0; k < p.n_sumsq_in / 4; ++k) {
+            const float4 v = __ldg(row + k);
+            sacc += (v.x + v.y) + (v.z + v.w);
+          }
+        }
+        s_inv[lane] = lane < p.M ? rsqrtf(sacc / static_cast<float>(p.K) + p.eps) : 0.f;
       }
     }
     epi_sync<kQEpi>();
