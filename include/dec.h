@@ -243,16 +243,16 @@ DEC_API dec_status dec_debug_force_timeout(dec_handle *h, int polls, dec_stream_
 /* Test hook: the tensor-core projection kernel of batched decode steps with affine 4-bit weights
    (oxinfer crate page, "MLX checkpoints": w = scale * q + bias per group of 64, so that
    sum_k w_k x_k = scale * sum_k (q_k - 8) x_k + (bias + 8 scale) * sum_k x_k): the codes are
-   expanded exactly to bf16 (q - 8) in shared memory, tcgen05.mma forms each group's sum into
-   tensor memory, and the scale and bias are applied per group in float32; on caller buffers,
-   plain store epilogue:
+   expanded exactly to bf16 (q - 8) into tensor memory, tcgen05.mma forms each group's sum (and,
+   through rows of ones, the sum of x) into tensor memory, and the scale and bias are applied per
+   group in float32; on caller buffers, plain store epilogue:
      out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) * w[n][k],  w = fl(scale * q + bias) per group of 64.
      x_hl      device bf16 [2][M][K] (plane 0 hi, plane 1 lo), 16-byte aligned, M in 1..32
      codes     device uint32 [N][K/8] (element 8 j + k in bits 4k..4k+3 of word j), 16-byte aligned
      sb        device uint32 [N][K/64]: bf16 scale bits | bf16 bias bits << 16, 16-byte aligned
      out       device float [M][N]
      S         K splits (dividing K / 64); S > 1 needs partials (device float [S][M][N]) and
-               counters (device uint32 [ceil(N / 128) + 1], zero, left zero)
+               counters (device uint32 [ceil(N / 120) + 1]: one per 120-row tile, zero, left zero)
    K a positive multiple of 64, N >= 1 (else DEC_ERR_INVALID_ARG).  One launch on `stream`. */
 DEC_API dec_status dec_debug_gemm_q4tc(const void *x_hl, int M, const void *codes, const void *sb, int N, int K,
                     int S, float *out, float *partials, unsigned *counters, dec_stream_t stream);

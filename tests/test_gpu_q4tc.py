@@ -45,7 +45,7 @@ def test_q4tc_gemm_matches_fp64(dec, M, N, K, S):
     sbd = torch.from_numpy(sb.view(np.int32)).contiguous().cuda()
     out = torch.full((M, N), float("nan"), device="cuda")
     partials = torch.empty((S, M, N), device="cuda") if S > 1 else None
-    counters = torch.zeros(((N + 127) // 128 + 1,), dtype=torch.int32, device="cuda") if S > 1 else None
+    counters = torch.zeros(((N + 119) // 120 + 1,), dtype=torch.int32, device="cuda") if S > 1 else None
     dec.dec_debug_gemm_q4tc(xhl.data_ptr(), M, wd.data_ptr(), sbd.data_ptr(), N, K, S, out.data_ptr(),
                             partials.data_ptr() if S > 1 else None, counters.data_ptr() if S > 1 else None,
                             torch.cuda.current_stream().cuda_stream)

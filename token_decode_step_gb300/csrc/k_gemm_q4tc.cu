@@ -7,21 +7,23 @@
 // "SINGLE-TOKEN DECODE" (the projection sequence, here over a batch of independent sequences).
 //
 // Per group of 64 inputs the tensor cores compute D[n][t] = sum_k (q[n][k] - 8) x[t][k] with
-// the codes as exact bf16 integers: the 128 weight rows of a tile are the MMA's M (the
-// accumulator's lanes), the 32 tokens its N = 32 columns, both operands K-major in the 128-byte
-// swizzle; the activations' bf16 hi and lo halves are two further K steps against the same code
-// tile, so the accumulator holds the sum of both.  The epilogue warps read every group's
-// accumulator from a ring of eight in tensor memory and add s D + (b + 8 s) sum_k x[t][k] in
-// float32, in group order, so the scale and bias cost one multiply-add each per (row, token,
-// group) instead of a dequantization per weight.
+// the codes as exact bf16 integers: a tile's 120 weight rows and 8 rows of ones are the MMA's
+// M = 128 (the accumulator's lanes) and its A operand, which the expanding threads write straight
+// into tensor memory (row n in lane n, two codes per 32-bit column); the activations' 32 bf16 hi
+// rows and 32 lo rows are its N = 64 columns (B, K-major in the 128-byte swizzle, read from
+// shared memory).  The rows of ones give each token's sum of the group's inputs in the same
+// instruction.  The epilogue warps read every group's accumulator from a ring in tensor memory,
+// add the hi and lo columns and then s D + (b + 8 s) sum_k x[t][k] in float32, in group order, so
+// the scale and bias cost one multiply-add each per (row, token, group) instead of a
+// dequantization per weight.
 //
 // Warp roles (one persistent CTA per SM, 576 threads): warp 0 issues the TMA copies of the
-// codes (128 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
-// warp 1 allocates the accumulator ring and issues the MMAs; warps 2..9 expand the codes into
-// bf16 (a byte permute builds 128 + q for two codes, an exact subtraction centres them) and sum
-// each token's inputs of the group; warps 10..17 scale, accumulate and run the fused epilogue,
-// two warps per 32-lane quarter of the accumulator, 16 token columns each.
-// A unit is a (128-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
+// codes (120 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
+// warp 1 allocates tensor memory and issues the MMAs; warps 2..9 expand the codes into bf16 (a
+// byte permute builds 128 + q for two codes, an exact subtraction centres them) and store them
+// to the A ring in tensor memory; warps 10..17 scale, accumulate and run the fused epilogue, two
+// warps per 32-lane quarter of the accumulator, 16 tokens each.
+// A unit is a (120-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
 // adds the S partial results in split order (deterministic).  Every wait on a barrier is
 // bounded: on time-out the kernel flags the status word and stops.
 #include "q4.cuh"
@@ -34,30 +36,37 @@ namespace {
 
 using namespace umma;
 
-constexpr int kQM = 128;                   // weight rows per tile
+constexpr int kQM = 128;                   // MMA rows: accumulator lanes
+constexpr int kQRows = 120;                // weight rows per tile; lanes 120..127 are rows of ones
 constexpr int kQT = 32;                    // token rows (accumulator columns)
 constexpr int kQK = 64;                    // inputs per stage: one group of the format
+constexpr int kQN = 2 * kQT;               // MMA N: the hi rows, then the lo rows, of the tokens
 constexpr int kQStages = 6;                // TMA ring: codes + activations
-constexpr int kQAStages = 4;               // expanded-code ring
-constexpr int kQG = 8;                     // accumulator ring (32 columns each) and sum-of-x ring
-constexpr int kQCode = kQM * kQK / 2;      // 4 KB: 128 rows x 32 bytes of codes
+constexpr int kQAStages = 4;               // expanded-code ring in tensor memory
+constexpr int kQG = 6;                     // accumulator ring (64 columns each)
+constexpr int kQACols = kQK / 2;           // 32 columns: a group of 64 bf16 codes per lane
+constexpr int kQAOff = kQN * kQG;          // first column of the code ring
+constexpr int kQTmemCols = 512;            // kQAOff + kQAStages * kQACols, as a power of two
+constexpr int kQCode = kQM * kQK / 2;      // 4 KB slot: kQRows rows x 32 bytes of codes
 constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
 constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
-constexpr int kQA = kQM * kQK * 2;         // 16 KB: the expanded codes of a tile, bf16
+constexpr int kQStageTx = kQX + kQRows * kQK / 2;  // bytes the copies of a stage deliver
 constexpr int kQDeq = 256;                 // expansion threads
 constexpr int kQEpi = 256;                 // epilogue threads
 constexpr int kQThreads = 64 + kQDeq + kQEpi;
-constexpr int kQOffS = kQAStages * kQA;
+constexpr int kQOffS = 0;
 constexpr int kQOffBar = kQOffS + kQStages * kQStage;
-constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 4 * kQG;
+constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 2 * kQG;
 constexpr int kQOffTmem = kQOffBar + 8 * kQBars;
-constexpr int kQOffSx = kQOffTmem + 16;                  // float [kQG][kQT]
-constexpr int kQOffInv = kQOffSx + 4 * kQG * kQT;
+constexpr int kQOffSx = kQOffTmem + 16;                  // float [2][kQT]: sums of x, by group parity
+constexpr int kQOffInv = kQOffSx + 4 * 2 * kQT;
 constexpr int kQOffBest = kQOffInv + 4 * kQT;
 constexpr int kQOffTicket = kQOffBest + 8 * kQT;
 constexpr int kQSmem = 1024 + kQOffTicket + 16;
-// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 32, M = 128
-constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+// tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
+constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(kQN) >> 3) << 17) |
+                             ((128u >> 4) << 24);
+static_assert(kQAOff + kQAStages * kQACols <= kQTmemCols, "tensor memory layout");
 static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && kQOffBest % 8 == 0, "smem layout");
 
 using tcdec::epi_sync;
@@ -89,11 +98,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms are 1024-byte aligned
   unsigned char* smem = smem_raw + (base - raw);
-  const uint32_t sA = base, sS = base + kQOffS;
+  const uint32_t sS = base + kQOffS;
   const uint32_t st_full = base + kQOffBar, st_empty = st_full + 8 * kQStages;
   const uint32_t a_full = st_empty + 8 * kQStages, a_empty = a_full + 8 * kQAStages;
   const uint32_t g_full = a_empty + 8 * kQAStages, g_empty = g_full + 8 * kQG;
-  const uint32_t x_full = g_empty + 8 * kQG, x_empty = x_full + 8 * kQG;
   const uint32_t tmem_slot = base + kQOffTmem;
   float* s_x = reinterpret_cast<float*>(smem + kQOffSx);
   float* s_inv = reinterpret_cast<float*>(smem + kQOffInv);
@@ -102,12 +110,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   tl_mark(p.tl, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles = (p.N + kQM - 1) / kQM;
+  const int n_tiles = (p.N + kQRows - 1) / kQRows;
   const int units = n_tiles * p.S;
   const int gps = p.K / kQK / p.S;  // groups per split
 
-  if (warp == 1) {  // the accumulator ring: kQG x 32 columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(32 * kQG)
+  if (warp == 1) {  // the accumulator ring (kQG x 64 columns), then the code ring (kQAStages x 32)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(kQTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -123,8 +131,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int b = 0; b < kQG; ++b) {
       mbar_init(g_full + 8 * b, 1);     // the MMAs' commit
       mbar_init(g_empty + 8 * b, kQEpi);  // the epilogue's accumulator reads
-      mbar_init(x_full + 8 * b, kQDeq);   // the expanders' sums of x
-      mbar_init(x_empty + 8 * b, kQEpi);  // the epilogue's reads of them
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -152,8 +158,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
         int tile, g;
         group_of(i, tile, g);
         const uint32_t full = st_full + 8 * i, st = sS + i * kQStage;
-        mbar_expect_tx(full, kQStage);
-        tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
+        mbar_expect_tx(full, kQStageTx);
+        tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQRows, full);
       }
       griddep_wait();
       tl_mark(p.tl, 1);
@@ -167,8 +173,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(full, kQStage);
-          tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQM, full);
+          mbar_expect_tx(full, kQStageTx);
+          tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQRows, full);
         }
         tma_load_2d(st, &tm_x, g * kQK, 0, full);              // hi plane: tokens 0..31
         tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);  // lo plane
@@ -189,14 +195,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
           }
           fence_after();
-          // the hi rows, then the lo rows, against the same code tile: D = sum (q - 8)(x_hi + x_lo)
-          const uint64_t dxh = sw128_desc(sS + s * kQStage), dxl = sw128_desc(sS + s * kQStage + kQX / 2);
-          const uint64_t da = sw128_desc(sA + a * kQA);
+          // D[n][0..31] = sum (q - 8) x_hi, D[n][32..63] = sum (q - 8) x_lo; A from tensor memory
+          const uint64_t dx = sw128_desc(sS + s * kQStage);
+          const uint32_t ta = tmem + kQAOff + kQACols * a;
 #pragma unroll
-          for (int k = 0; k < kQK / 16; ++k)  // 16 inputs = 32 bytes further along the swizzled rows
-            mma_bf16(tmem + 32 * gb, da + 2 * k, dxh + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < kQK / 16; ++k) mma_bf16(tmem + 32 * gb, da + 2 * k, dxl + 2 * k, kQIdesc, 1u);
+          for (int k = 0; k < kQK / 16; ++k)  // 16 inputs: 8 columns of A, 32 bytes along the swizzled B rows
+            mma_bf16_ta(tmem + kQN * gb, ta + 8 * k, dx + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
           commit(a_empty + 8 * a);
           commit(st_empty + 8 * s);
           commit(g_full + 8 * gb);
@@ -204,60 +208,48 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
     }
   } else if (warp < 10) {
-    // expanders: the codes of weight row r, inputs 32 h .. 32 h + 31 of a group (neighbouring
-    // lanes read neighbouring 16-byte chunks of the code tile: no bank conflicts); and the sum of
-    // x over the group for token t (lanes 8 t' .. 8 t' + 7: hi row quarters, then lo row quarters)
-    const int dt = tid - 64, r = dt >> 1, h = dt & 1;
-    const int xt = dt >> 3, xp = dt & 7, xrow = (xp < 4 ? 0 : kQT) + xt, xq = xp & 3;
+    // expanders: weight row r = 32 (warp % 4) + lane of the tile (the tensor-memory lanes this
+    // warp may write), inputs 32 h .. 32 h + 31 of a group.  Lanes 120..127 store ones instead:
+    // the accumulator's lanes there then hold each token's sum of the group's inputs.
+    const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
+    const bool ones = r >= kQRows;
+    const uint32_t ta_row = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kQAOff + 16 * h;
     int it = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       for (int j = 0; j < gps; ++j, ++it) {
-        const int s = it % kQStages, a = it % kQAStages, gb = it % kQG;
-        if (!mbar_wait(st_full + 8 * s, (it / kQStages) & 1)) {
+        const int s = it % kQStages, a = it % kQAStages;
+        // waits are made warp-uniform: the tensor-memory store below is a whole-warp instruction
+        if (!__all_sync(0xffffffffu, mbar_wait(st_full + 8 * s, (it / kQStages) & 1))) {
           ok = false;
           break;
         }
-        const uint32_t st = sS + s * kQStage;
-        uint4 cw, x0, x1;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                     : "r"(st + kQX + r * 32 + h * 16));
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(x0.x), "=r"(x0.y), "=r"(x0.z), "=r"(x0.w)
-                     : "r"(st + xrow * 128 + (((2 * xq) ^ (xrow & 7)) << 4)));
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(x1.x), "=r"(x1.y), "=r"(x1.z), "=r"(x1.w)
-                     : "r"(st + xrow * 128 + (((2 * xq + 1) ^ (xrow & 7)) << 4)));
+        uint4 cw = make_uint4(0u, 0u, 0u, 0u);
+        if (!ones)
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                       : "r"(sS + s * kQStage + kQX + r * 32 + h * 16));
         mbar_arrive(st_empty + 8 * s);
-        // this thread's 16 inputs, then the 8 lanes of the token (fixed order)
-        const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        float sx = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sx += bf16_lo(xs[i]) + bf16_hi(xs[i]);
-        sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-        sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-        sx += __shfl_xor_sync(0xffffffffu, sx, 4);
-        if (it >= kQG && !mbar_wait(x_empty + 8 * gb, ((it / kQG) - 1) & 1)) {
+        if (it >= kQAStages && !__all_sync(0xffffffffu, mbar_wait(a_empty + 8 * a, ((it / kQAStages) - 1) & 1))) {
           ok = false;
           break;
         }
-        if (xp == 0) s_x[gb * kQT + xt] = sx;
-        mbar_arrive(x_full + 8 * gb);
-        if (it >= kQAStages && !mbar_wait(a_empty + 8 * a, ((it / kQAStages) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        const uint32_t arow = sA + a * kQA + r * 128;
+        fence_after();
+        uint32_t v[16];  // inputs 32 h + 2 j, 32 h + 2 j + 1 in column j (low half first)
         const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // word i = 16-byte chunk 4 h + i of the row
-          const uint4 v = expand_word(words[i]);
-          const uint32_t off = static_cast<uint32_t>(((4 * h + i) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(arow + off), "r"(v.x), "r"(v.y), "r"(v.z),
-                       "r"(v.w)
-                       : "memory");
+        for (int i = 0; i < 4; ++i) {
+          const uint4 e = expand_word(words[i]);
+          v[4 * i] = e.x;
+          v[4 * i + 1] = e.y;
+          v[4 * i + 2] = e.z;
+          v[4 * i + 3] = e.w;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
+        if (ones) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0x3F803F80u;  // bf16 1.0 in both halves
+        }
+        tmem_st16(ta_row + kQACols * a, v);
+        fence_before();
         mbar_arrive(a_full + 8 * a);
       }
     }
@@ -283,8 +275,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int tile = u % n_tiles, split = u / n_tiles;
-      const int n = tile * kQM + r;
-      const bool row_ok = n < p.N;
+      const int n = tile * kQRows + r;
+      const bool row_ok = r < kQRows && n < p.N;
       const uint32_t* sbrow = p.sb + static_cast<size_t>(row_ok ? n : 0) * (p.K / kGroup) + split * gps;
       float y[kTPT];
 #pragma unroll
@@ -293,16 +285,28 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int j = 0; j < gps; ++j, ++it) {
         const int gb = it % kQG;
         const uint32_t sbn = j + 1 < gps ? __ldg(sbrow + j + 1) : 0u;  // next group's, in flight
-        if (ok && (!mbar_wait(g_full + 8 * gb, (it / kQG) & 1) || !mbar_wait(x_full + 8 * gb, (it / kQG) & 1)))
-          ok = false;
+        if (ok && !mbar_wait(g_full + 8 * gb, (it / kQG) & 1)) ok = false;
         fence_after();
-        float d[kTPT];
-        tmem_ld16(tmem + 32 * gb + kTPT * c + tq, d);  // tokens 16 c .. 16 c + 15
+        float d[kTPT], dl[kTPT];
+        tmem_ld16(tmem + kQN * gb + kTPT * c + tq, d);         // hi columns of tokens 16 c .. 16 c + 15
+        tmem_ld16(tmem + kQN * gb + kQT + kTPT * c + tq, dl);  // their lo columns
         fence_before();
         mbar_arrive(g_empty + 8 * gb);
+#pragma unroll
+        for (int t = 0; t < kTPT; ++t) d[t] += dl[t];
+        // the first ones lane holds the group's sums of x: published for the other lanes (two
+        // buffers by group parity; the barrier of group it - 1 orders this write after every
+        // read of group it - 2)
+        float* sx = s_x + (it & 1) * kQT + kTPT * c;
+        if (r == kQRows) {
+#pragma unroll
+          for (int t4 = 0; t4 < kTPT / 4; ++t4)
+            reinterpret_cast<float4*>(sx)[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+        }
+        epi_sync<kQEpi>();
         // w = s q + b = s (q - 8) + (b + 8 s): y += s D + (b + 8 s) sum x
         const float sc = sb_scale(sbw), bc = fmaf(8.0f, sc, sb_bias(sbw));
-        const float4* sxv = reinterpret_cast<const float4*>(s_x + gb * kQT + kTPT * c);
+        const float4* sxv = reinterpret_cast<const float4*>(sx);
 #pragma unroll
         for (int t4 = 0; t4 < kTPT / 4; ++t4) {
           const float4 xv = sxv[t4];
@@ -314,7 +318,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
             y[t] = fmaf(bc, xs4[e], y[t]);
           }
         }
-        mbar_arrive(x_empty + 8 * gb);
         sbw = sbn;
       }
       const bool live = ok && row_ok;
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   __syncthreads();
   tl_mark(p.tl, 2);
   if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(32 * kQG) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kQTmemCols) : "memory");
   if (!ok && p.status) atomicOr(p.status, kStatusTimeout);
   if constexpr (EPI == kEpiLmHead) {  // the last CTA publishes every token's argmax
     __threadfence();
@@ -369,7 +372,7 @@ cudaError_t launch_q4tc_t(const LaunchCtx& c, const CUtensorMap& mx, const CUten
                           bool prepare) {
   if (prepare)
     return cudaFuncSetAttribute(k_gemm_q4tc<IN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
-  const int units = ((p.N + kQM - 1) / kQM) * p.S;
+  const int units = ((p.N + kQRows - 1) / kQRows) * p.S;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(units < p.ctas ? units : p.ctas));
   cfg.blockDim = dim3(kQThreads);
@@ -397,12 +400,14 @@ cudaError_t dispatch_q4tc(const LaunchCtx& c, const CUtensorMap& mx, const CUten
 
 int q4tc_max_tokens() { return kQT; }
 
+int q4tc_tile_rows() { return kQRows; }
+
 // K splits of an N x K projection: a divisor of the K / 64 groups (at most 8) that brings the
 // units of the one-CTA-per-SM grid closest to whole waves; a larger split count only when it
 // gains 10% of the waves' occupancy (each split adds a partial round trip, and short units
 // pay their epilogue more often: 8 splits of the 8B gate/up were the slowest measured)
 int q4tc_splits(int N, int K, int num_sms) {
-  const int tiles = (N + kQM - 1) / kQM, groups = K / kQK;
+  const int tiles = (N + kQRows - 1) / kQRows, groups = K / kQK;
   int best = 1;
   double best_eff = 0.0;
   for (int s = 1; s <= 8 && s <= groups; ++s) {
@@ -418,14 +423,14 @@ int q4tc_splits(int N, int K, int num_sms) {
   return best;
 }
 
-// 4-bit codes [N][K/2] bytes, boxes of 32 bytes x 128 rows (one group of a tile), no swizzle;
+// 4-bit codes [N][K/2] bytes, boxes of 32 bytes x 120 rows (one group of a tile), no swizzle;
 // rows past the end read as zero
 cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K) {
   EncodeTiledQ enc = encoder_q();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQK / 2), static_cast<cuuint32_t>(kQM)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQK / 2), static_cast<cuuint32_t>(kQRows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
