@@ -104,10 +104,12 @@ typedef enum {
    last row of each sequence gives the first generated token; logits_out may be NULL. */
 /* Kernel family of the projections of steps with 2..32 rows on models of hidden >= 2048 (a
    batch of sequences, or the rows of a verify step).  Both compute the same products.
-   TCGEN05 selects the tensor-memory kernels (bf16 weights streamed by TMA into tcgen05.mma;
-   4-bit codes expanded in shared memory with a per-group accumulator readout), MMA_SYNC the
-   mma.sync kernels over fragment-packed weight tiles.  AUTO takes what measured faster on
-   this part, currently mma.sync. */
+   TCGEN05 selects the tensor-memory kernels for every projection (bf16 weights streamed by TMA
+   into tcgen05.mma; 4-bit codes expanded into tensor memory with a per-group accumulator
+   readout), MMA_SYNC the mma.sync kernels over fragment-packed weight tiles.  AUTO takes, per
+   projection, what measured faster on this part: with 4-bit weights and 16 or more rows the
+   gate/up and lm_head projections on tcgen05 and the others on mma.sync; with bf16 weights
+   mma.sync. */
 typedef enum {
     DEC_PROJ_AUTO = 0,
     DEC_PROJ_MMA_SYNC = 1,
@@ -242,8 +244,8 @@ DEC_API dec_status dec_debug_force_timeout(dec_handle *h, int polls, dec_stream_
 
 /* Test hook: the tensor-core projection kernel of batched decode steps with affine 4-bit weights
    (oxinfer crate page, "MLX checkpoints": w = scale * q + bias per group of 64, so that
-   sum_k w_k x_k = scale * sum_k (q_k - 8) x_k + (bias + 8 scale) * sum_k x_k): the codes are
-   expanded exactly to bf16 (q - 8) into tensor memory, tcgen05.mma forms each group's sum (and,
+   sum_k w_k x_k = scale * sum_k (128 + q_k) x_k + (bias - 128 scale) * sum_k x_k): the codes are
+   expanded exactly to bf16 (128 + q) into tensor memory, tcgen05.mma forms each group's sum (and,
    through rows of ones, the sum of x) into tensor memory, and the scale and bias are applied per
    group in float32; on caller buffers, plain store epilogue:
      out[m][n] = sum_k (x_hi[m][k] + x_lo[m][k]) * w[n][k],  w = fl(scale * q + bias) per group of 64.

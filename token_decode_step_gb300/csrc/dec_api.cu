@@ -97,6 +97,8 @@ struct PackedLinear {
   int N = 0, K = 0, S = 1;
   int Npad = 0, KC = 0;    // batched path: rows padded to 16, inputs staged per chunk
   size_t w_bytes = 0, sb_bytes = 0;  // sizes of the two regions (sb_bytes 0 when sb is null)
+  bool frag = false;       // fragment tiles of the mma.sync batched kernel (else row-major)
+  bool q4tc = false;       // launched on the tcgen05 4-bit kernel (k_gemm_q4tc)
 };
 
 struct PackedLayer {
@@ -134,10 +136,10 @@ struct dec_handle {
   // TMA tensor maps of the three activation hi/lo planes (inputs of QKV / gate_up / lm_head,
   // of O, of down)
   bool umma = false;
-  // batched decode (2..32 rows) with 4-bit weights on models of hidden >= 2048: tcgen05 over
-  // dequantized weight tiles; the weights stay in the batch-1 row-major packing, read by TMA
-  // (the codes) and plain loads (scale and bias); the activation maps (map_u, map_o, map_g)
-  // have 32-row boxes
+  // batched decode (2..32 rows) with 4-bit weights on models of hidden >= 2048: some or all
+  // projections on tcgen05 over expanded code tiles (PackedLinear::q4tc); their weights stay in
+  // the batch-1 row-major packing, read by TMA (the codes) and plain loads (scale and bias); the
+  // activation maps (map_u, map_o, map_g) have 32-row boxes
   bool q4tc = false;
   // the same for bf16 weights at 1..32 rows (k_gemm_btc): row-major weights read by TMA
   bool btc = false;
@@ -482,7 +484,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       up.status = h->status;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
       s2 = check(launch_gemm_umma(lc, mx, L.tmap, up, in_mode, epi), what);
-    } else if (h->q4tc || h->btc) {
+    } else if (L.q4tc || h->btc) {
       Q4tcParams qp{};
       qp.M = h->rows;
       qp.N = L.N;
@@ -512,7 +514,7 @@ dec_status enqueue_step(dec_handle* h, const StepPtrs& sp, cudaStream_t stream, 
       qp.pf_row_bytes = gp.pf_row_bytes;
       qp.pf_max_ctx = gp.pf_max_ctx;
       const void* mx = xin == h->xh_u ? h->map_u : xin == h->xh_o ? h->map_o : h->map_g;
-      s2 = check(h->q4tc ? launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi)
+      s2 = check(L.q4tc ? launch_gemm_q4tc(lc, mx, L.tmap, qp, in_mode, epi)
                          : launch_gemm_btc(lc, mx, L.tmap, qp, in_mode, epi),
                  what);
     } else if (h->rows == 1) {
@@ -760,14 +762,20 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048, when
-  // selected: tcgen05 on the batched path's hi/lo activation planes, 4-bit codes expanded in
-  // shared memory or bf16 weights streamed by TMA (DEC_PROJ_AUTO keeps the mma.sync kernels:
-  // side by side on one GPU the 8B steps took 9.70 against 10.15 ms at 32 rows of 4-bit
-  // weights and 3.79 against 5.20 ms at 8 rows of bf16); one row stays on the batch-1 GEMV
-  const bool tc_rows = h->rows >= 2 && h->rows <= q4tc_max_tokens() && H >= 2048 && c.proj_kernels == DEC_PROJ_TCGEN05;
-  h->q4tc = tc_rows && fmt == DEC_W_AFFINE4_G64;
-  h->btc = tc_rows && fmt == DEC_W_BF16;
+  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048:
+  // tcgen05 on the batched path's hi/lo activation planes, 4-bit codes expanded into tensor
+  // memory or bf16 weights streamed by TMA.  DEC_PROJ_TCGEN05 puts every projection there.
+  // DEC_PROJ_AUTO takes what measured faster side by side on one GPU: with 4-bit weights from 16
+  // rows on, the gate/up and lm_head projections on tcgen05 and the others on mma.sync (8B, 32
+  // rows: gate/up 76 against 84 us, lm_head 0.32 against 0.40 ms; q/k/v, o and down 39-54
+  // against 35-50 us), with bf16 weights every projection on mma.sync (8 rows: 3.79 against
+  // 5.20 ms a step).  One row stays on the batch-1 GEMV.
+  const bool tc_rows = h->rows >= 2 && h->rows <= q4tc_max_tokens() && H >= 2048;
+  const bool q4 = fmt == DEC_W_AFFINE4_G64;
+  const bool q4tc_all = tc_rows && q4 && c.proj_kernels == DEC_PROJ_TCGEN05;
+  const bool q4tc_gu = q4tc_all || (tc_rows && q4 && c.proj_kernels == DEC_PROJ_AUTO && h->rows >= 16);
+  h->q4tc = q4tc_gu;  // some projection runs on k_gemm_q4tc
+  h->btc = tc_rows && fmt == DEC_W_BF16 && c.proj_kernels == DEC_PROJ_TCGEN05;
   const bool tc = h->rows > 1 || h->q4tc || h->btc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
@@ -777,12 +785,17 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // below that (the 0.6B shapes) the token-blocked mma.sync kernel's many small CTAs fill the
   // GPU better (512-token chunk: 14.2 ms against 16.2 ms, measured)
   h->umma = h->rows >= umma_tokens_per_tile() && fmt == DEC_W_BF16 && H >= 2048;
-  const bool frag = tc && !h->umma && !h->q4tc && !h->btc;  // fragment-packed weights for the mma.sync path
-  auto lbytes = [&](int N, int K) { return frag ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K); };
+  // fragment-packed weights for the mma.sync path, per projection
+  auto is_frag = [&](bool on_q4tc) { return tc && !h->umma && !on_q4tc && !h->btc; };
+  bool any_frag = false;
+  auto lbytes = [&](int N, int K, bool on_q4tc) {
+    return is_frag(on_q4tc) ? linear_bytes_tc(fmt, N, K) : linear_bytes(fmt, N, K);
+  };
   size_t total = align_up(static_cast<size_t>(V) * H * 2, 256) + align_up(static_cast<size_t>(H) * 2, 256) +
-                 lbytes(V, H);
+                 lbytes(V, H, q4tc_gu);
   const size_t per_layer = 2 * align_up(static_cast<size_t>(H) * 2, 256) + 2 * align_up(static_cast<size_t>(d) * 2, 256) +
-                           lbytes(nqkv, H) + lbytes(H, nq * d) + lbytes(2 * I, H) + lbytes(H, I);
+                           lbytes(nqkv, H, q4tc_all) + lbytes(H, nq * d, q4tc_all) + lbytes(2 * I, H, q4tc_gu) +
+                           lbytes(H, I, q4tc_all);
   total += per_layer * c.n_layers;
   if ((e = cudaMalloc(&h->wmem, total)) != cudaSuccess) {
     set_err("cudaMalloc of %zu bytes of packed weights failed: %s", total, cudaGetErrorString(e));
@@ -796,11 +809,14 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     cur += align_up(bytes, 256);
     return p;
   };
-  auto take_linear = [&](int N, int K) {
+  auto take_linear = [&](int N, int K, bool on_q4tc) {
     PackedLinear L;
     L.N = N;
     L.K = K;
-    if (frag) {
+    L.q4tc = on_q4tc;
+    L.frag = is_frag(on_q4tc);
+    any_frag = any_frag || L.frag;
+    if (L.frag) {
       L.Npad = (N + 15) / 16 * 16;
       choose_tc_splits(L, h->wfmt, ny, h->num_sms, h->tblocks);
       L.w_bytes = linear_bytes_tc(fmt, N, K);
@@ -809,7 +825,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     }
     // (the stream-K bf16 kernel: S = the partial slots its schedule needs)
     L.S = h->umma ? 1
-          : h->q4tc ? q4tc_splits(N, K, h->num_sms)
+          : L.q4tc ? q4tc_splits(N, K, h->num_sms)
           : h->btc ? btc_max_segments(N, K, h->num_sms)
                    : choose_splits(N, K, fmt, h->num_sms);
     if (fmt == DEC_W_BF16) {
@@ -825,7 +841,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   };
   h->embed = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(V) * H * 2));
   h->final_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(H) * 2));
-  h->lm_head = take_linear(V, H);
+  h->lm_head = take_linear(V, H, q4tc_gu);
   h->layers.resize(c.n_layers);
   for (int l = 0; l < c.n_layers; ++l) {
     PackedLayer& L = h->layers[l];
@@ -833,10 +849,10 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     L.post_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(H) * 2));
     L.q_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(d) * 2));
     L.k_norm = reinterpret_cast<__nv_bfloat16*>(take(static_cast<size_t>(d) * 2));
-    L.qkv = take_linear(nqkv, H);
-    L.o = take_linear(H, nq * d);
-    L.gateup = take_linear(2 * I, H);
-    L.down = take_linear(H, I);
+    L.qkv = take_linear(nqkv, H, q4tc_all);
+    L.o = take_linear(H, nq * d, q4tc_all);
+    L.gateup = take_linear(2 * I, H, q4tc_gu);
+    L.down = take_linear(H, I, q4tc_all);
   }
 
   // ---- pack (device to device on the internal stream)
@@ -844,7 +860,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   auto cp = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto pack_lin = [&](const PackedLinear& P, size_t row_off, const dec_linear& a, const dec_linear* b, int rows,
                       int K, int ib) -> cudaError_t {
-    if (frag) {
+    if (P.frag) {
       const int npad = (rows + 15) / 16 * 16;
       if (fmt == DEC_W_BF16)
         return pack_frag_bf16(s, static_cast<uint32_t*>(P.w), static_cast<const __nv_bfloat16*>(a.w),
@@ -883,7 +899,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     if ((e = pack_lin(L.qkv, static_cast<size_t>(nq + nkv) * d, lw.v, nullptr, nkv * d, H, 0)) != cudaSuccess)
       return fail("pack v", e);
     if ((e = pack_lin(L.o, 0, lw.o, nullptr, H, nq * d, 0)) != cudaSuccess) return fail("pack o", e);
-    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, h->umma ? 16 : frag ? 8 : kGemvRows / 2)) !=
+    if ((e = pack_lin(L.gateup, 0, lw.gate, &lw.up, 2 * I, H, h->umma ? 16 : L.gateup.frag ? 8 : kGemvRows / 2)) !=
         cudaSuccess)
       return fail("pack gate/up", e);
     if ((e = pack_lin(L.down, 0, lw.down, nullptr, H, I, 0)) != cudaSuccess) return fail("pack down", e);
@@ -898,7 +914,8 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
     const int tiles = (L.N + kGemvRows - 1) / kGemvRows;  // >= row blocks of the batched path too
     max_tiles = tiles > max_tiles ? tiles : max_tiles;
     if (L.S > 1) {
-      const size_t pp = frag ? static_cast<size_t>(L.S) * (L.Npad / 16) * 32 * ny * 4 : static_cast<size_t>(L.S) * L.N * B;
+      const size_t pp =
+          L.frag ? static_cast<size_t>(L.S) * (L.Npad / 16) * 32 * ny * 4 : static_cast<size_t>(L.S) * L.N * B;
       max_partials = pp > max_partials ? pp : max_partials;
     }
   };
@@ -979,9 +996,11 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       for (int tn : {128, 256})
         if ((e = prepare_gemm_umma(cb[0], cb[1], tn)) != cudaSuccess) return fail("tcgen05 kernel attributes", e);
   }
-  if (h->q4tc || h->btc) {  // TMA maps of every weight and of the activation planes, kernel attributes
+  if (h->q4tc || h->btc) {  // TMA maps of their weights and of the activation planes, kernel attributes
     auto cmap = [&](PackedLinear& L) {
-      return h->q4tc ? q4tc_code_map(L.tmap, L.w, L.N, L.K) : umma_tensor_map(L.tmap, L.w, L.N, L.K, 128);
+      return L.q4tc ? q4tc_code_map(L.tmap, L.w, L.N, L.K)
+             : h->btc ? umma_tensor_map(L.tmap, L.w, L.N, L.K, 128)
+                      : cudaSuccess;
     };
     if ((e = cmap(h->lm_head)) != cudaSuccess) return fail("tensor map", e);
     for (auto& L : h->layers)
@@ -998,7 +1017,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
       if ((e = h->q4tc ? prepare_gemm_q4tc(cb[0], cb[1]) : prepare_gemm_btc(cb[0], cb[1])) != cudaSuccess)
         return fail("tcgen05 decode kernel attributes", e);
   }
-  if (frag) {
+  if (any_frag) {
     GemmParams gp{};
     gp.B = h->rows;
     gp.tblocks = h->tblocks;
@@ -1122,8 +1141,8 @@ extern "C" dec_status dec_get_device_status(dec_handle* h, int* out) {
 
 namespace {
 // rows per gate (then up) block of the packed gate/up projection
-int gate_up_block(const dec_handle* h) {
-  return h->umma ? 16 : h->rows > 1 && !h->q4tc && !h->btc ? 8 : kGemvRows / 2;
+int gate_up_block(const dec_handle* h, const PackedLinear& L) {
+  return h->umma ? 16 : L.frag ? 8 : kGemvRows / 2;
 }
 }  // namespace
 
@@ -1148,12 +1167,12 @@ extern "C" dec_status dec_debug_dequant(dec_handle* h, int layer, int which, flo
       case 1: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = c.n_q_heads * d; break;
       case 2: P = &L.qkv; rows = c.n_kv_heads * d; K = H; off = (c.n_q_heads + c.n_kv_heads) * d; break;
       case 3: P = &L.o; rows = H; K = c.n_q_heads * d; break;
-      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h); half = 0; break;
-      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h); half = 1; break;
+      case 4: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h, L.gateup); half = 0; break;
+      case 5: P = &L.gateup; rows = c.intermediate; K = H; ib = gate_up_block(h, L.gateup); half = 1; break;
       default: P = &L.down; rows = H; K = c.intermediate; break;
     }
   }
-  if (h->rows > 1 && !h->umma && !h->q4tc && !h->btc) {
+  if (P->frag) {
     DEC_CUDA(debug_dequant_frag(cs, out, P->w, h->wfmt, rows, K, off, ib, half));
   } else {
     DEC_CUDA(debug_dequant(cs, out, P->w, P->sb, h->wfmt, rows, K, off, ib, half));

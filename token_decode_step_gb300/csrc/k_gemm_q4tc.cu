@@ -6,22 +6,21 @@
 // sum: sum_k (s q_k + b) x_k = s sum_k q_k x_k + b sum_k x_k); Butter architecture.md,
 // "SINGLE-TOKEN DECODE" (the projection sequence, here over a batch of independent sequences).
 //
-// Per group of 64 inputs the tensor cores compute D[n][t] = sum_k (q[n][k] - 8) x[t][k] with
+// Per group of 64 inputs the tensor cores compute D[n][t] = sum_k (128 + q[n][k]) x[t][k] with
 // the codes as exact bf16 integers: a tile's 120 weight rows and 8 rows of ones are the MMA's
 // M = 128 (the accumulator's lanes) and its A operand, which the expanding threads write straight
 // into tensor memory (row n in lane n, two codes per 32-bit column); the activations' 32 bf16 hi
 // rows and 32 lo rows are its N = 64 columns (B, K-major in the 128-byte swizzle, read from
 // shared memory).  The rows of ones give each token's sum of the group's inputs in the same
 // instruction.  The epilogue warps read every group's accumulator from a ring in tensor memory,
-// add the hi and lo columns and then s D + (b + 8 s) sum_k x[t][k] in float32, in group order, so
+// add s D + (b - 128 s) sum_k x[t][k] (hi and lo columns) in float32, in group order, so
 // the scale and bias cost one multiply-add each per (row, token, group) instead of a
 // dequantization per weight.
 //
 // Warp roles (one persistent CTA per SM, 576 threads): warp 0 issues the TMA copies of the
 // codes (120 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
 // warp 1 allocates tensor memory and issues the MMAs; warps 2..9 expand the codes into bf16 (a
-// byte permute builds 128 + q for two codes, an exact subtraction centres them) and store them
-// to the A ring in tensor memory; warps 10..17 scale, accumulate and run the fused epilogue, two
+// byte permute builds 128 + q for two codes) and store them to the A ring in tensor memory; warps 10..17 scale, accumulate and run the fused epilogue, two
 // warps per 32-lane quarter of the accumulator, 16 tokens each.
 // A unit is a (120-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
 // adds the S partial results in split order (deterministic).  Every wait on a barrier is
@@ -41,7 +40,7 @@ constexpr int kQRows = 120;                // weight rows per tile; lanes 120..1
 constexpr int kQT = 32;                    // token rows (accumulator columns)
 constexpr int kQK = 64;                    // inputs per stage: one group of the format
 constexpr int kQN = 2 * kQT;               // MMA N: the hi rows, then the lo rows, of the tokens
-constexpr int kQStages = 6;                // TMA ring: codes + activations
+constexpr int kQStages = 8;                // TMA ring: codes + activations
 constexpr int kQAStages = 4;               // expanded-code ring in tensor memory
 constexpr int kQG = 6;                     // accumulator ring (64 columns each)
 constexpr int kQACols = kQK / 2;           // 32 columns: a group of 64 bf16 codes per lane
@@ -71,22 +70,28 @@ static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && 
 
 using tcdec::epi_sync;
 
-// Codes of one word (element 8 j + k in bits 4k..4k+3) -> the 16 bytes of bf16 (q - 8) for
+// Codes of one word (element 8 j + k in bits 4k..4k+3) -> the 16 bytes of bf16 (128 + q) for
 // elements 8 j .. 8 j + 7 in order.  The permutes interleave even and odd codes and set 0x43
-// as each high byte, giving bf16 128 + q exactly; subtracting 136 is exact (|q - 8| <= 8).
+// as each high byte: bf16 0x43qq is 128 + q exactly.  (The products then accumulate in float32
+// at about 17 times the magnitude of centred codes: rounding stays near 1e-7 of the bound.)
 __device__ __forceinline__ uint4 expand_word(uint32_t w) {
   const uint32_t ev = w & 0x0f0f0f0fu, od = (w >> 4) & 0x0f0f0f0fu;  // codes 0,2,4,6 / 1,3,5,7
   const uint32_t t0 = __byte_perm(ev, od, 0x5140), t1 = __byte_perm(ev, od, 0x7362);  // c0..c3 / c4..c7
-  constexpr uint32_t k43 = 0x43434343u, k136 = 0x43084308u;  // bf16 136 in both halves
-  uint32_t r[4] = {__byte_perm(t0, k43, 0x4140), __byte_perm(t0, k43, 0x4342), __byte_perm(t1, k43, 0x4140),
-                   __byte_perm(t1, k43, 0x4342)};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 v = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&r[i]),
-                                     *reinterpret_cast<const __nv_bfloat162*>(&k136));
-    r[i] = *reinterpret_cast<const uint32_t*>(&v);
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
+  constexpr uint32_t k43 = 0x43434343u;
+  return make_uint4(__byte_perm(t0, k43, 0x4140), __byte_perm(t0, k43, 0x4342), __byte_perm(t1, k43, 0x4140),
+                    __byte_perm(t1, k43, 0x4342));
+}
+
+// (y0, y1) += (a0, a1) * (b0, b1), one packed float32 FMA
+__device__ __forceinline__ void fma2(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, y;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 y, {%0, %1};\n\t"
+      "fma.rn.f32x2 y, a, b, y;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "+f"(y0), "+f"(y1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 }  // namespace
@@ -195,7 +200,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             break;
           }
           fence_after();
-          // D[n][0..31] = sum (q - 8) x_hi, D[n][32..63] = sum (q - 8) x_lo; A from tensor memory
+          // D[n][0..31] = sum (128 + q) x_hi, D[n][32..63] = sum (128 + q) x_lo; A from tensor memory
           const uint64_t dx = sw128_desc(sS + s * kQStage);
           const uint32_t ta = tmem + kQAOff + kQACols * a;
 #pragma unroll
@@ -292,8 +297,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
         tmem_ld16(tmem + kQN * gb + kQT + kTPT * c + tq, dl);  // their lo columns
         fence_before();
         mbar_arrive(g_empty + 8 * gb);
-#pragma unroll
-        for (int t = 0; t < kTPT; ++t) d[t] += dl[t];
         // the first ones lane holds the group's sums of x: published for the other lanes (two
         // buffers by group parity; the barrier of group it - 1 orders this write after every
         // read of group it - 2)
@@ -301,22 +304,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (r == kQRows) {
 #pragma unroll
           for (int t4 = 0; t4 < kTPT / 4; ++t4)
-            reinterpret_cast<float4*>(sx)[t4] = make_float4(d[4 * t4], d[4 * t4 + 1], d[4 * t4 + 2], d[4 * t4 + 3]);
+            reinterpret_cast<float4*>(sx)[t4] = make_float4(d[4 * t4] + dl[4 * t4], d[4 * t4 + 1] + dl[4 * t4 + 1],
+                                                            d[4 * t4 + 2] + dl[4 * t4 + 2], d[4 * t4 + 3] + dl[4 * t4 + 3]);
         }
         epi_sync<kQEpi>();
-        // w = s q + b = s (q - 8) + (b + 8 s): y += s D + (b + 8 s) sum x
-        const float sc = sb_scale(sbw), bc = fmaf(8.0f, sc, sb_bias(sbw));
+        // w = s q + b = s (128 + q) + (b - 128 s): y += s D_hi + s D_lo + (b - 128 s) sum x
+        const float sc = sb_scale(sbw), bc = fmaf(-128.0f, sc, sb_bias(sbw));
         const float4* sxv = reinterpret_cast<const float4*>(sx);
 #pragma unroll
         for (int t4 = 0; t4 < kTPT / 4; ++t4) {
           const float4 xv = sxv[t4];
-          const float xs4[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int t = 4 * t4 + e;
-            y[t] = fmaf(sc, d[t], y[t]);
-            y[t] = fmaf(bc, xs4[e], y[t]);
-          }
+          const int t = 4 * t4;
+          fma2(y[t], y[t + 1], sc, sc, d[t], d[t + 1]);
+          fma2(y[t + 2], y[t + 3], sc, sc, d[t + 2], d[t + 3]);
+          fma2(y[t], y[t + 1], sc, sc, dl[t], dl[t + 1]);
+          fma2(y[t + 2], y[t + 3], sc, sc, dl[t + 2], dl[t + 3]);
+          fma2(y[t], y[t + 1], bc, bc, xv.x, xv.y);
+          fma2(y[t + 2], y[t + 3], bc, bc, xv.z, xv.w);
         }
         sbw = sbn;
       }
