@@ -50,6 +50,7 @@ constexpr int kQCode = kQM * kQK / 2;      // 4 KB slot: kQRows rows x 32 bytes 
 constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
 constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
 constexpr int kQStageTx = kQX + kQRows * kQK / 2;  // bytes the copies of a stage deliver
+constexpr int kQDefer = 2;                 // group of the next unit after which a split exchange runs
 constexpr int kQDeq = 256;                 // expansion threads
 constexpr int kQEpi = 256;                 // epilogue threads
 constexpr int kQThreads = 64 + kQDeq + kQEpi;
@@ -277,6 +278,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
     }
     epi_sync<kQEpi>();
+    // With K splits a unit's partial results are written at its end and the exchange (fence,
+    // ticket, and in the tile's last CTA the sum of the slots and the fused epilogue) waits
+    // until the next unit's first groups are under way: done at once, its round trips stalled
+    // the epilogue while the rings filled and the MMAs and expansion stopped behind it.
+    int pend_tile = -1, pend_n = 0;
+    bool pend_live = false;
+    auto finish_pending = [&]() {
+      float yp[kTPT];
+      if (tcdec::split_finish<kTPT, kQEpi>(p, yp, kTPT * c, pend_n, pend_tile, p.S, pend_live, et, s_ticket))
+        tcdec::fused_epilogue<IN, EPI, kTPT>(p, yp, kTPT * c, pend_n, pend_live, lane, s_inv, s_best);
+      pend_tile = -1;
+    };
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       const int tile = u % n_tiles, split = u / n_tiles;
@@ -323,11 +336,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
           fma2(y[t + 2], y[t + 3], bc, bc, xv.z, xv.w);
         }
         sbw = sbn;
+        if (pend_tile >= 0 && (j == kQDefer || j == gps - 1)) finish_pending();
       }
       const bool live = ok && row_ok;
-      tcdec::unit_epilogue<IN, EPI, kTPT, kQEpi>(p, y, kTPT * c, n, tile, split, p.S, live, et, lane, s_inv, s_best,
-                                                 s_ticket);
+      if (p.S > 1) {
+        tcdec::split_write<kTPT>(p, y, kTPT * c, n, split, live);
+        pend_tile = tile;
+        pend_n = n;
+        pend_live = live;
+      } else {
+        tcdec::fused_epilogue<IN, EPI, kTPT>(p, y, kTPT * c, n, live, lane, s_inv, s_best);
+      }
     }
+    if (pend_tile >= 0) finish_pending();
     if constexpr (EPI == kEpiLmHead) {
       epi_sync<kQEpi>();
       if (et < p.M && s_best[et] != 0ull) atomicMax(p.amax_key + et, s_best[et]);

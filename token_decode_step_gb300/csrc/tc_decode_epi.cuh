@@ -34,33 +34,43 @@ __device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-// TPT tokens per thread, starting at token t0 (the thread's accumulator columns); NTH epilogue
-// threads take part in the named barrier.
-template <int IN, int EPI, int TPT, int NTH>
-__device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[TPT], int t0, int n, int tile,
-                                              int split, int S, bool live, int et, int lane, const float* s_inv,
-                                              unsigned long long* s_best, unsigned* s_ticket) {
-  if (S > 1) {  // partial results; the last CTA of the tile adds them in slot order
-    if (live) {
+// The split exchange in two halves, for a kernel that defers the second past the start of its
+// next unit: split_write stores this unit's partial results (slot `split`); split_finish, later,
+// takes the tile's ticket and, in the last CTA to arrive, leaves the slots' sum (in slot order)
+// in y and returns true.  Called by the NTH epilogue threads together.
+template <int TPT>
+__device__ __forceinline__ void split_write(const Q4tcParams& p, const float (&y)[TPT], int t0, int n, int split,
+                                            bool live) {
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+      if (t0 + i < p.M) p.partials[(static_cast<size_t>(split) * p.M + t0 + i) * p.N + n] = y[i];
+  }
+}
+template <int TPT, int NTH>
+__device__ __forceinline__ bool split_finish(const Q4tcParams& p, float (&y)[TPT], int t0, int n, int tile, int S,
+                                             bool live, int et, unsigned* s_ticket) {
+  __threadfence();
+  epi_sync<NTH>();
+  if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
+  epi_sync<NTH>();
+  if (*s_ticket != static_cast<unsigned>(S - 1)) return false;
+  __threadfence();
+#pragma unroll
+  for (int i = 0; i < TPT; ++i) y[i] = 0.f;
+  if (live)
+    for (int s = 0; s < S; ++s)
 #pragma unroll
       for (int i = 0; i < TPT; ++i)
-        if (t0 + i < p.M) p.partials[(static_cast<size_t>(split) * p.M + t0 + i) * p.N + n] = y[i];
-    }
-    __threadfence();
-    epi_sync<NTH>();
-    if (et == 0) *s_ticket = atomicAdd(&p.counters[tile], 1u);
-    epi_sync<NTH>();
-    if (*s_ticket != static_cast<unsigned>(S - 1)) return;
-    __threadfence();
-#pragma unroll
-    for (int i = 0; i < TPT; ++i) y[i] = 0.f;
-    if (live)
-      for (int s = 0; s < S; ++s)
-#pragma unroll
-        for (int i = 0; i < TPT; ++i)
-          if (t0 + i < p.M) y[i] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t0 + i) * p.N + n);
-    if (et == 0) p.counters[tile] = 0u;
-  }
+        if (t0 + i < p.M) y[i] += __ldcg(p.partials + (static_cast<size_t>(s) * p.M + t0 + i) * p.N + n);
+  if (et == 0) p.counters[tile] = 0u;
+  return true;
+}
+
+// The fused epilogue of a tile's complete results y (TPT tokens per thread from token t0).
+template <int IN, int EPI, int TPT>
+__device__ __forceinline__ void fused_epilogue(const Q4tcParams& p, float (&y)[TPT], int t0, int n, bool live,
+                                               int lane, const float* s_inv, unsigned long long* s_best) {
   if constexpr (IN == kInNorm) {
 #pragma unroll
     for (int i = 0; i < TPT; ++i) y[i] *= s_inv[t0 + i];
@@ -130,6 +140,19 @@ __device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[TP
       if (lane == 0 && k != 0ull) atomicMax(s_best + t, k);
     }
   }
+}
+
+// Both: TPT tokens per thread, starting at token t0 (the thread's accumulator columns); NTH
+// epilogue threads take part in the named barrier.
+template <int IN, int EPI, int TPT, int NTH>
+__device__ __forceinline__ void unit_epilogue(const Q4tcParams& p, float (&y)[TPT], int t0, int n, int tile,
+                                              int split, int S, bool live, int et, int lane, const float* s_inv,
+                                              unsigned long long* s_best, unsigned* s_ticket) {
+  if (S > 1) {  // partial results; the last CTA of the tile adds them in slot order
+    split_write<TPT>(p, y, t0, n, split, live);
+    if (!split_finish<TPT, NTH>(p, y, t0, n, tile, S, live, et, s_ticket)) return;
+  }
+  fused_epilogue<IN, EPI, TPT>(p, y, t0, n, live, lane, s_inv, s_best);
 }
 
 }  // namespace tcdec
