@@ -107,9 +107,9 @@ typedef enum {
    TCGEN05 selects the tensor-memory kernels for every projection (bf16 weights streamed by TMA
    into tcgen05.mma; 4-bit codes expanded into tensor memory with a per-group accumulator
    readout), MMA_SYNC the mma.sync kernels over fragment-packed weight tiles.  AUTO takes, per
-   projection, what measured faster on this part: with 4-bit weights and 16 or more rows the
-   gate/up and lm_head projections on tcgen05 and the others on mma.sync; with bf16 weights
-   mma.sync. */
+   projection, what measured faster on this part (8B shapes at 32 rows of 4-bit weights and 8
+   rows of bf16): with 4-bit weights and 16 or more rows the gate/up and lm_head projections on
+   tcgen05 and the others on mma.sync; with bf16 weights, or fewer rows, mma.sync. */
 typedef enum {
     DEC_PROJ_AUTO = 0,
     DEC_PROJ_MMA_SYNC = 1,

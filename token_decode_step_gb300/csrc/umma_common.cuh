@@ -1,6 +1,7 @@
 // tcgen05 / TMA / mbarrier building blocks shared by the tensor-memory GEMM kernels:
 // bounded mbarrier waits, 2-D tensor copies, shared-memory descriptors of K-major tiles in
-// the 128-byte swizzle, the bf16 MMA with its commit, and accumulator loads.
+// the 128-byte swizzle, the bf16 MMA (A from shared or from tensor memory) with its commit,
+// and tensor-memory loads and stores.
 #pragma once
 
 #include <cuda.h>
