@@ -27,7 +27,9 @@ def _bf16_bits(x: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("M,N,K,S", [(32, 128, 64, 1), (32, 256, 1024, 2), (8, 200, 512, 1), (17, 1000, 2560, 5),
-                                     (1, 130, 384, 3), (32, 6144, 4096, 8), (32, 4096, 12288, 4)])
+                                     (1, 130, 384, 3), (32, 6144, 4096, 8), (32, 4096, 12288, 4),
+                                     # odd groups per split: the last two-group stage of each unit holds one
+                                     (32, 250, 320, 1), (8, 300, 2560, 8), (5, 977, 1344, 3)])
 def test_q4tc_gemm_matches_fp64(dec, M, N, K, S):
     g = torch.Generator(device="cpu")
     g.manual_seed(M * 7 + N + K + S)

@@ -12,16 +12,18 @@
 // into tensor memory (row n in lane n, two codes per 32-bit column); the activations' 32 bf16 hi
 // rows and 32 lo rows are its N = 64 columns (B, K-major in the 128-byte swizzle, read from
 // shared memory).  The rows of ones give each token's sum of the group's inputs in the same
-// instruction.  The epilogue warps read every group's accumulator from a ring in tensor memory,
-// add s D + (b - 128 s) sum_k x[t][k] (hi and lo columns) in float32, in group order, so
-// the scale and bias cost one multiply-add each per (row, token, group) instead of a
-// dequantization per weight.
+// instruction.  The epilogue warps read every group's accumulator from a ring in tensor memory
+// and add s D (hi and lo columns) and (b - 128 s) sum_k x[t][k] in float32, in a fixed order (per
+// stage the s D terms of its groups, then their sum-of-x terms), so the scale and bias cost one
+// multiply-add each per (row, token, group) instead of a dequantization per weight.
 //
-// Warp roles (one persistent CTA per SM, 576 threads): warp 0 issues the TMA copies of the
-// codes (120 rows x 32 bytes per group) and of the activation tile (32 hi rows, 32 lo rows);
+// Warp roles (one persistent CTA per SM, 576 threads), handing over stages of two groups
+// (halving the barrier round trips per byte): warp 0 issues the TMA copies of the codes (120
+// rows x 64 bytes a stage) and of the activation tiles (32 hi rows, 32 lo rows per group);
 // warp 1 allocates tensor memory and issues the MMAs; warps 2..9 expand the codes into bf16 (a
-// byte permute builds 128 + q for two codes) and store them to the A ring in tensor memory; warps 10..17 scale, accumulate and run the fused epilogue, two
-// warps per 32-lane quarter of the accumulator, 16 tokens each.
+// byte permute builds 128 + q for two codes) and store them to the A ring in tensor memory;
+// warps 10..17 scale, accumulate and run the fused epilogue, two warps per 32-lane quarter of
+// the accumulator, 16 tokens each.
 // A unit is a (120-row tile, K split) pair; with S > 1 splits the last CTA to finish a tile
 // adds the S partial results in split order (deterministic).  Every wait on a barrier is
 // bounded: on time-out the kernel flags the status word and stops.
@@ -38,19 +40,22 @@ using namespace umma;
 constexpr int kQM = 128;                   // MMA rows: accumulator lanes
 constexpr int kQRows = 120;                // weight rows per tile; lanes 120..127 are rows of ones
 constexpr int kQT = 32;                    // token rows (accumulator columns)
-constexpr int kQK = 64;                    // inputs per stage: one group of the format
+constexpr int kQK = 64;                    // inputs per group of the format
+constexpr int kQSG = 2;                    // groups per stage: every hand-off covers two groups
 constexpr int kQN = 2 * kQT;               // MMA N: the hi rows, then the lo rows, of the tokens
-constexpr int kQStages = 8;                // TMA ring: codes + activations
-constexpr int kQAStages = 4;               // expanded-code ring in tensor memory
-constexpr int kQG = 6;                     // accumulator ring (64 columns each)
+constexpr int kQStages = 6;                // TMA ring: codes + activations, of kQSG groups each
+constexpr int kQAStages = 2;               // expanded-code ring in tensor memory (stages)
+constexpr int kQG = 3;                     // accumulator ring (stages of kQSG x 64 columns)
 constexpr int kQACols = kQK / 2;           // 32 columns: a group of 64 bf16 codes per lane
-constexpr int kQAOff = kQN * kQG;          // first column of the code ring
-constexpr int kQTmemCols = 512;            // kQAOff + kQAStages * kQACols, as a power of two
-constexpr int kQCode = kQM * kQK / 2;      // 4 KB slot: kQRows rows x 32 bytes of codes
-constexpr int kQX = 2 * kQT * kQK * 2;     // 8 KB: 32 hi rows, then 32 lo rows, of 128 bytes
+constexpr int kQAOff = kQN * kQSG * kQG;   // first column of the code ring
+constexpr int kQTmemCols = 512;            // kQAOff + kQAStages * kQSG * kQACols
+constexpr int kQCodeRow = kQSG * kQK / 2;  // 64 bytes of codes per row and stage
+constexpr int kQCode = kQM * kQCodeRow;    // 8 KB slot: kQRows rows x 64 bytes of codes
+constexpr int kQXg = 2 * kQT * kQK * 2;    // 8 KB per group: 32 hi rows, then 32 lo rows, of 128 bytes
+constexpr int kQX = kQSG * kQXg;
 constexpr int kQStage = kQX + kQCode;      // activations first (1024-byte aligned atoms)
-constexpr int kQStageTx = kQX + kQRows * kQK / 2;  // bytes the copies of a stage deliver
-constexpr int kQDefer = 2;                 // group of the next unit after which a split exchange runs
+constexpr int kQCodeTx = kQRows * kQCodeRow;  // bytes of a stage's code box
+constexpr int kQDefer = 1;                 // stage of the next unit after which a split exchange runs
 constexpr int kQDeq = 256;                 // expansion threads
 constexpr int kQEpi = 256;                 // epilogue threads
 constexpr int kQThreads = 64 + kQDeq + kQEpi;
@@ -58,15 +63,15 @@ constexpr int kQOffS = 0;
 constexpr int kQOffBar = kQOffS + kQStages * kQStage;
 constexpr int kQBars = 2 * kQStages + 2 * kQAStages + 2 * kQG;
 constexpr int kQOffTmem = kQOffBar + 8 * kQBars;
-constexpr int kQOffSx = kQOffTmem + 16;                  // float [2][kQT]: sums of x, by group parity
-constexpr int kQOffInv = kQOffSx + 4 * 2 * kQT;
+constexpr int kQOffSx = kQOffTmem + 16;  // float [2][kQSG][kQT]: sums of x, by stage parity
+constexpr int kQOffInv = kQOffSx + 4 * 2 * kQSG * kQT;
 constexpr int kQOffBest = kQOffInv + 4 * kQT;
 constexpr int kQOffTicket = kQOffBest + 8 * kQT;
 constexpr int kQSmem = 1024 + kQOffTicket + 16;
 // tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B, both K-major, N = 64, M = 128
 constexpr uint32_t kQIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((static_cast<uint32_t>(kQN) >> 3) << 17) |
                              ((128u >> 4) << 24);
-static_assert(kQAOff + kQAStages * kQACols <= kQTmemCols, "tensor memory layout");
+static_assert(kQAOff + kQAStages * kQSG * kQACols <= kQTmemCols, "tensor memory layout");
 static_assert(kQOffS % 1024 == 0 && kQStage % 1024 == 0 && kQOffBar % 8 == 0 && kQOffBest % 8 == 0, "smem layout");
 
 using tcdec::epi_sync;
@@ -119,8 +124,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int n_tiles = (p.N + kQRows - 1) / kQRows;
   const int units = n_tiles * p.S;
   const int gps = p.K / kQK / p.S;  // groups per split
+  const int spu = (gps + kQSG - 1) / kQSG;  // stages per unit; with gps odd the last holds one group
 
-  if (warp == 1) {  // the accumulator ring (kQG x 64 columns), then the code ring (kQAStages x 32)
+  if (warp == 1) {  // the accumulator ring (kQG x kQSG x 64 columns), then the code ring
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(kQTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -149,29 +155,31 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   bool ok = true;
   if (warp == 0) {
-    if (lane == 0) {  // TMA producer; stage i of this CTA is group i % gps of its unit i / gps
+    if (lane == 0) {  // TMA producer; stage i of this CTA holds groups 2 (i % spu) .. of its unit i / spu
       const int my_units = static_cast<int>(blockIdx.x) < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-      const int total = my_units * gps;
-      auto group_of = [&](int i, int& tile, int& g) {
-        const int u = blockIdx.x + (i / gps) * gridDim.x;
+      const int total = my_units * spu;
+      auto stage_of = [&](int i, int& tile, int& g0, int& ng) {
+        const int u = blockIdx.x + (i / spu) * gridDim.x, js = i % spu;
         tile = u % n_tiles;
-        g = (u / n_tiles) * gps + i % gps;
+        g0 = (u / n_tiles) * gps + kQSG * js;
+        ng = gps - kQSG * js < kQSG ? gps - kQSG * js : kQSG;
       };
       // the codes do not depend on upstream kernels: the first stages' are requested before
-      // the grid-dependency wait, their activations after it
+      // the grid-dependency wait, their activations after it (a code box always spans kQSG
+      // groups; past the end of a split it reads codes that are not used, past K zeros)
       const int pre = total < kQStages ? total : kQStages;
       for (int i = 0; i < pre; ++i) {
-        int tile, g;
-        group_of(i, tile, g);
+        int tile, g0, ng;
+        stage_of(i, tile, g0, ng);
         const uint32_t full = st_full + 8 * i, st = sS + i * kQStage;
-        mbar_expect_tx(full, kQStageTx);
-        tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQRows, full);
+        mbar_expect_tx(full, kQCodeTx + ng * kQXg);
+        tma_load_2d(st + kQX, &tm_c, g0 * (kQK / 2), tile * kQRows, full);
       }
       griddep_wait();
       tl_mark(p.tl, 1);
       for (int i = 0; i < total; ++i) {
-        int tile, g;
-        group_of(i, tile, g);
+        int tile, g0, ng;
+        stage_of(i, tile, g0, ng);
         const int s = i % kQStages;
         const uint32_t full = st_full + 8 * s, st = sS + s * kQStage;
         if (i >= pre) {
@@ -179,22 +187,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(full, kQStageTx);
-          tma_load_2d(st + kQX, &tm_c, g * (kQK / 2), tile * kQRows, full);
+          mbar_expect_tx(full, kQCodeTx + ng * kQXg);
+          tma_load_2d(st + kQX, &tm_c, g0 * (kQK / 2), tile * kQRows, full);
         }
-        tma_load_2d(st, &tm_x, g * kQK, 0, full);              // hi plane: tokens 0..31
-        tma_load_2d(st + kQX / 2, &tm_x, g * kQK, p.M, full);  // lo plane
+        for (int gg = 0; gg < ng; ++gg) {
+          tma_load_2d(st + gg * kQXg, &tm_x, (g0 + gg) * kQK, 0, full);                // hi plane: tokens 0..31
+          tma_load_2d(st + gg * kQXg + kQXg / 2, &tm_x, (g0 + gg) * kQK, p.M, full);  // lo plane
+        }
       }
     } else if (p.pf_kv) {  // the producer warp's other lanes: the next attention's K/V into L2
       prefetch_kv_rows(p.pf_kv, p.pf_positions, p.pf_plane_bytes, p.pf_head_bytes, p.pf_B, p.pf_nkv, p.pf_row_bytes,
                        p.pf_max_ctx, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), lane - 1, 31);
     }
   } else if (warp == 1) {
-    if (lane == 0) {  // MMA issuer: one accumulator of the ring per group
+    if (lane == 0) {  // MMA issuer: one accumulator per group, kQSG of them per stage
       int it = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        for (int j = 0; j < gps; ++j, ++it) {
+        for (int js = 0; js < spu; ++js, ++it) {
           const int s = it % kQStages, a = it % kQAStages, gb = it % kQG;
+          const int ng = gps - kQSG * js < kQSG ? gps - kQSG * js : kQSG;
           if (!mbar_wait(a_full + 8 * a, (it / kQAStages) & 1) || !mbar_wait(st_full + 8 * s, (it / kQStages) & 1) ||
               (it >= kQG && !mbar_wait(g_empty + 8 * gb, ((it / kQG) - 1) & 1))) {
             ok = false;
@@ -202,11 +213,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
           fence_after();
           // D[n][0..31] = sum (128 + q) x_hi, D[n][32..63] = sum (128 + q) x_lo; A from tensor memory
-          const uint64_t dx = sw128_desc(sS + s * kQStage);
-          const uint32_t ta = tmem + kQAOff + kQACols * a;
+          for (int gg = 0; gg < ng; ++gg) {
+            const uint64_t dx = sw128_desc(sS + s * kQStage + gg * kQXg);
+            const uint32_t ta = tmem + kQAOff + kQACols * (kQSG * a + gg);
+            const uint32_t td = tmem + kQN * (kQSG * gb + gg);
 #pragma unroll
-          for (int k = 0; k < kQK / 16; ++k)  // 16 inputs: 8 columns of A, 32 bytes along the swizzled B rows
-            mma_bf16_ta(tmem + kQN * gb, ta + 8 * k, dx + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
+            for (int k = 0; k < kQK / 16; ++k)  // 16 inputs: 8 columns of A, 32 bytes along the swizzled B rows
+              mma_bf16_ta(td, ta + 8 * k, dx + 2 * k, kQIdesc, k != 0 ? 1u : 0u);
+          }
           commit(a_empty + 8 * a);
           commit(st_empty + 8 * s);
           commit(g_full + 8 * gb);
@@ -215,46 +229,55 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
   } else if (warp < 10) {
     // expanders: weight row r = 32 (warp % 4) + lane of the tile (the tensor-memory lanes this
-    // warp may write), inputs 32 h .. 32 h + 31 of a group.  Lanes 120..127 store ones instead:
+    // warp may write), inputs 32 h .. 32 h + 31 of each group.  Lanes 120..127 store ones instead:
     // the accumulator's lanes there then hold each token's sum of the group's inputs.
     const int r = 32 * (warp & 3) + lane, h = (warp - 2) >> 2;
     const bool ones = r >= kQRows;
     const uint32_t ta_row = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kQAOff + 16 * h;
     int it = 0;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      for (int j = 0; j < gps; ++j, ++it) {
+      for (int js = 0; js < spu; ++js, ++it) {
         const int s = it % kQStages, a = it % kQAStages;
-        // waits are made warp-uniform: the tensor-memory store below is a whole-warp instruction
+        const int ng = gps - kQSG * js < kQSG ? gps - kQSG * js : kQSG;
+        // waits are made warp-uniform: the tensor-memory stores below are whole-warp instructions
         if (!__all_sync(0xffffffffu, mbar_wait(st_full + 8 * s, (it / kQStages) & 1))) {
           ok = false;
           break;
         }
-        uint4 cw = make_uint4(0u, 0u, 0u, 0u);
-        if (!ones)
-          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                       : "r"(sS + s * kQStage + kQX + r * 32 + h * 16));
+        uint4 cw[kQSG];
+#pragma unroll
+        for (int gg = 0; gg < kQSG; ++gg) {
+          cw[gg] = make_uint4(0u, 0u, 0u, 0u);
+          if (!ones && gg < ng)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(cw[gg].x), "=r"(cw[gg].y), "=r"(cw[gg].z), "=r"(cw[gg].w)
+                         : "r"(sS + s * kQStage + kQX + r * kQCodeRow + gg * (kQK / 2) + h * 16));
+        }
         mbar_arrive(st_empty + 8 * s);
         if (it >= kQAStages && !__all_sync(0xffffffffu, mbar_wait(a_empty + 8 * a, ((it / kQAStages) - 1) & 1))) {
           ok = false;
           break;
         }
         fence_after();
-        uint32_t v[16];  // inputs 32 h + 2 j, 32 h + 2 j + 1 in column j (low half first)
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 e = expand_word(words[i]);
-          v[4 * i] = e.x;
-          v[4 * i + 1] = e.y;
-          v[4 * i + 2] = e.z;
-          v[4 * i + 3] = e.w;
-        }
-        if (ones) {
+        for (int gg = 0; gg < kQSG; ++gg) {
+          if (gg >= ng) break;  // ng is the same for the whole warp
+          uint32_t v[16];  // inputs 32 h + 2 j, 32 h + 2 j + 1 in column j (low half first)
+          const uint32_t words[4] = {cw[gg].x, cw[gg].y, cw[gg].z, cw[gg].w};
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0x3F803F80u;  // bf16 1.0 in both halves
+          for (int i = 0; i < 4; ++i) {
+            const uint4 e = expand_word(words[i]);
+            v[4 * i] = e.x;
+            v[4 * i + 1] = e.y;
+            v[4 * i + 2] = e.z;
+            v[4 * i + 3] = e.w;
+          }
+          if (ones) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0x3F803F80u;  // bf16 1.0 in both halves
+          }
+          tmem_st16(ta_row + kQACols * (kQSG * a + gg), v);
         }
-        tmem_st16(ta_row + kQACols * a, v);
         fence_before();
         mbar_arrive(a_full + 8 * a);
       }
@@ -299,44 +322,61 @@ __global__ void __launch_bounds__(kQThreads, 1)
       float y[kTPT];
 #pragma unroll
       for (int t = 0; t < kTPT; ++t) y[t] = 0.f;
-      uint32_t sbw = __ldg(sbrow);
-      for (int j = 0; j < gps; ++j, ++it) {
-        const int gb = it % kQG;
-        const uint32_t sbn = j + 1 < gps ? __ldg(sbrow + j + 1) : 0u;  // next group's, in flight
+      uint32_t sbw[kQSG], sbn[kQSG];  // this stage's scale/bias words; the next stage's, in flight
+#pragma unroll
+      for (int gg = 0; gg < kQSG; ++gg) sbw[gg] = gg < gps ? __ldg(sbrow + gg) : 0u;
+      for (int js = 0; js < spu; ++js, ++it) {
+        const int gb = it % kQG, j0 = kQSG * js;
+        const int ng = gps - j0 < kQSG ? gps - j0 : kQSG;
+#pragma unroll
+        for (int gg = 0; gg < kQSG; ++gg) sbn[gg] = j0 + kQSG + gg < gps ? __ldg(sbrow + j0 + kQSG + gg) : 0u;
         if (ok && !mbar_wait(g_full + 8 * gb, (it / kQG) & 1)) ok = false;
         fence_after();
-        float d[kTPT], dl[kTPT];
-        tmem_ld16(tmem + kQN * gb + kTPT * c + tq, d);         // hi columns of tokens 16 c .. 16 c + 15
-        tmem_ld16(tmem + kQN * gb + kQT + kTPT * c + tq, dl);  // their lo columns
+        // w = s q + b = s (128 + q) + (b - 128 s): y += s D_hi + s D_lo, per group, now; the
+        // (b - 128 s) sum x terms after the barrier that publishes the sums.  The first ones
+        // lane holds each group's sums of x and publishes them for the other lanes (two buffers
+        // by stage parity; the barrier of stage it - 1 orders these writes after every read of
+        // stage it - 2).
+        float* sx = s_x + (it & 1) * (kQSG * kQT) + kTPT * c;
+#pragma unroll
+        for (int gg = 0; gg < kQSG; ++gg) {
+          if (gg >= ng) break;  // ng is the same for every epilogue thread
+          float d[kTPT], dl[kTPT];
+          const uint32_t td = tmem + kQN * (kQSG * gb + gg) + kTPT * c + tq;
+          tmem_ld16(td, d);         // hi columns of tokens 16 c .. 16 c + 15
+          tmem_ld16(td + kQT, dl);  // their lo columns
+          if (r == kQRows) {
+#pragma unroll
+            for (int t4 = 0; t4 < kTPT / 4; ++t4)
+              reinterpret_cast<float4*>(sx + gg * kQT)[t4] =
+                  make_float4(d[4 * t4] + dl[4 * t4], d[4 * t4 + 1] + dl[4 * t4 + 1], d[4 * t4 + 2] + dl[4 * t4 + 2],
+                              d[4 * t4 + 3] + dl[4 * t4 + 3]);
+          }
+          const float sc = sb_scale(sbw[gg]);
+#pragma unroll
+          for (int t = 0; t < kTPT; t += 2) {
+            fma2(y[t], y[t + 1], sc, sc, d[t], d[t + 1]);
+            fma2(y[t], y[t + 1], sc, sc, dl[t], dl[t + 1]);
+          }
+        }
         fence_before();
         mbar_arrive(g_empty + 8 * gb);
-        // the first ones lane holds the group's sums of x: published for the other lanes (two
-        // buffers by group parity; the barrier of group it - 1 orders this write after every
-        // read of group it - 2)
-        float* sx = s_x + (it & 1) * kQT + kTPT * c;
-        if (r == kQRows) {
-#pragma unroll
-          for (int t4 = 0; t4 < kTPT / 4; ++t4)
-            reinterpret_cast<float4*>(sx)[t4] = make_float4(d[4 * t4] + dl[4 * t4], d[4 * t4 + 1] + dl[4 * t4 + 1],
-                                                            d[4 * t4 + 2] + dl[4 * t4 + 2], d[4 * t4 + 3] + dl[4 * t4 + 3]);
-        }
         epi_sync<kQEpi>();
-        // w = s q + b = s (128 + q) + (b - 128 s): y += s D_hi + s D_lo + (b - 128 s) sum x
-        const float sc = sb_scale(sbw), bc = fmaf(-128.0f, sc, sb_bias(sbw));
-        const float4* sxv = reinterpret_cast<const float4*>(sx);
 #pragma unroll
-        for (int t4 = 0; t4 < kTPT / 4; ++t4) {
-          const float4 xv = sxv[t4];
-          const int t = 4 * t4;
-          fma2(y[t], y[t + 1], sc, sc, d[t], d[t + 1]);
-          fma2(y[t + 2], y[t + 3], sc, sc, d[t + 2], d[t + 3]);
-          fma2(y[t], y[t + 1], sc, sc, dl[t], dl[t + 1]);
-          fma2(y[t + 2], y[t + 3], sc, sc, dl[t + 2], dl[t + 3]);
-          fma2(y[t], y[t + 1], bc, bc, xv.x, xv.y);
-          fma2(y[t + 2], y[t + 3], bc, bc, xv.z, xv.w);
+        for (int gg = 0; gg < kQSG; ++gg) {
+          if (gg >= ng) break;
+          const float bc = fmaf(-128.0f, sb_scale(sbw[gg]), sb_bias(sbw[gg]));
+          const float4* sxv = reinterpret_cast<const float4*>(sx + gg * kQT);
+#pragma unroll
+          for (int t4 = 0; t4 < kTPT / 4; ++t4) {
+            const float4 xv = sxv[t4];
+            fma2(y[4 * t4], y[4 * t4 + 1], bc, bc, xv.x, xv.y);
+            fma2(y[4 * t4 + 2], y[4 * t4 + 3], bc, bc, xv.z, xv.w);
+          }
         }
-        sbw = sbn;
-        if (pend_tile >= 0 && (j == kQDefer || j == gps - 1)) finish_pending();
+#pragma unroll
+        for (int gg = 0; gg < kQSG; ++gg) sbw[gg] = sbn[gg];
+        if (pend_tile >= 0 && (js == kQDefer || js == spu - 1)) finish_pending();
       }
       const bool live = ok && row_ok;
       if (p.S > 1) {
@@ -448,14 +488,14 @@ int q4tc_splits(int N, int K, int num_sms) {
   return best;
 }
 
-// 4-bit codes [N][K/2] bytes, boxes of 32 bytes x 120 rows (one group of a tile), no swizzle;
+// 4-bit codes [N][K/2] bytes, boxes of 64 bytes x 120 rows (two groups of a tile), no swizzle;
 // rows past the end read as zero
 cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K) {
   EncodeTiledQ enc = encoder_q();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQK / 2), static_cast<cuuint32_t>(kQRows)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kQCodeRow), static_cast<cuuint32_t>(kQRows)};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes),
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
