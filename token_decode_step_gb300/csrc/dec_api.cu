@@ -767,7 +767,7 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
   // memory or bf16 weights streamed by TMA.  DEC_PROJ_TCGEN05 puts every projection there.
   // DEC_PROJ_AUTO takes what measured faster side by side on one GPU: with 4-bit weights from 16
   // rows on (measured at 32), the gate/up and lm_head projections on tcgen05 and the others on
-  // mma.sync (8B, 32 rows: gate/up 74 against 84 us, lm_head 0.32 against 0.40 ms; q/k/v, o and down 37-53
+  // mma.sync (8B, 32 rows: gate/up 69 against 84 us, lm_head 0.30 against 0.40 ms; q/k/v, o and down 37-53
   // against 35-49 us), with bf16 weights every projection on mma.sync (8 rows: 3.79 against
   // 5.20 ms a step).  One row stays on the batch-1 GEMV.
   const bool tc_rows = h->rows >= 2 && h->rows <= q4tc_max_tokens() && H >= 2048;
