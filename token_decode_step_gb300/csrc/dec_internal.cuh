@@ -363,7 +363,6 @@ cudaError_t launch_gemm_umma(const LaunchCtx& c, const void* map_x, const void* 
                              int in_mode, int epi);
 cudaError_t prepare_gemm_umma(int in_mode, int epi, int tile_n);
 int q4tc_max_tokens();
-int q4tc_tile_rows();  // weight rows per tile (and per tile counter)
 int q4tc_splits(int N, int K, int num_sms);
 cudaError_t q4tc_code_map(void* map128, const void* codes, int N, int K);  // CUtensorMap (128 B)
 cudaError_t launch_gemm_q4tc(const LaunchCtx& c, const void* map_x, const void* map_codes, const Q4tcParams& p,

@@ -465,8 +465,6 @@ cudaError_t dispatch_q4tc(const LaunchCtx& c, const CUtensorMap& mx, const CUten
 
 int q4tc_max_tokens() { return kQT; }
 
-int q4tc_tile_rows() { return kQRows; }
-
 // K splits of an N x K projection: a divisor of the K / 64 groups (at most 8) that brings the
 // units of the one-CTA-per-SM grid closest to whole waves; a larger split count only when it
 // gains 10% of the waves' occupancy (each split adds a partial round trip, and short units

@@ -1,10 +1,11 @@
 // The unit epilogue of the batched tcgen05 decode projections (k_gemm_q4tc.cu, k_gemm_btc.cu):
-// the thread holds weight row n of a 128-row tile and its results for TPT of the token
-// columns.  When S > 1 pieces of the tile's K range were computed apart (K splits, or the
-// segments of a stream-K schedule), the partial results go to p.partials slot `split` and the
-// last CTA to finish the tile adds them in slot order; then the input RMSNorm's per-token
-// 1/rms and the fused epilogue (store / residual + next-norm hi/lo planes + sums of squares /
-// SwiGLU / lm_head keys).  Called by the kernel's 128 epilogue threads together (named barrier 1).
+// the thread holds weight row n of a tile (128 rows, or 120 in the 4-bit kernel) and its results
+// for TPT of the token columns.  When S > 1 pieces of the tile's K range were computed apart (K
+// splits, or the segments of a stream-K schedule), the partial results go to p.partials slot
+// `split` and the last CTA to finish the tile adds them in slot order; then the input RMSNorm's
+// per-token 1/rms and the fused epilogue (store / residual + next-norm hi/lo planes + sums of
+// squares / SwiGLU / lm_head keys).  Called by the kernel's NTH epilogue threads together (named
+// barrier 1).
 #pragma once
 
 #include "dec_internal.cuh"
