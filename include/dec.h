@@ -278,6 +278,16 @@ DEC_API dec_status dec_debug_gemm_btc(const void *x_hl, int M, const void *w, in
    share one 128-row tile; 0 for a non-positive argument. */
 DEC_API int dec_debug_btc_max_segments(int N, int K, int ctas);
 
+/* Test hook (host only, no CUDA call): the kernel family that each projection of a handle
+   created from *cfg runs on, as dec_config.proj_kernels selects it (the projection kernel
+   family, above).  Bit i of *tcgen05_mask is set when projection i (0 q/k/v, 1 o, 2 gate/up,
+   3 down, 4 lm_head) runs on a tcgen05 decode kernel (k_gemm_q4tc for 4-bit weights,
+   k_gemm_btc for bf16) rather than the mma.sync kernel, the batch-1 GEMV or the prefill GEMM.
+     cfg           host pointer; the config dec_create would check (same checks, same status)
+     tcgen05_mask  host int, written on success
+   DEC_ERR_INVALID_ARG for a NULL argument; a config that dec_create refuses gets its status. */
+DEC_API dec_status dec_debug_proj_plan(const dec_config *cfg, int *tcgen05_mask);
+
 /* The affine 8-bit quantizer of the KV cache (the one dec_step applies to new rows), on
    caller buffers.  For each group of 64 consecutive values x of a row, in float32:
    mn, mx = min, max; scale = bf16(fl(fl(mx - mn) / 255)); bias = bf16(mn) (round to

@@ -190,3 +190,38 @@ def test_btc_schedule_segments(dec):
             owners = {c for c in range(grid) if begin[c] < (t + 1) * kst and begin[c + 1] > t * kst}
             most = max(most, len(owners))
         assert dec.lib.dec_debug_btc_max_segments(N, K, ctas) == most
+
+
+def test_projection_plan(dec):
+    """Host side of dec_config.proj_kernels: which projections run on the tcgen05 decode kernels
+    (bit i: 0 q/k/v, 1 o, 2 gate/up, 3 down, 4 lm_head).  AUTO puts the gate/up and lm_head
+    projections of 4-bit steps with 16..32 rows at hidden >= 2048 there; TCGEN05 every projection
+    of 2..32-row steps at hidden >= 2048; batch-1, bf16-under-AUTO, small-hidden and 33+-row steps
+    none."""
+    big = dict(n_layers=1, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, intermediate=12288,
+               vocab=151936, max_ctx=64)
+    GU_LM, ALL = 4 | 16, 31
+    cases = [
+        (dict(linear_fmt=1, batch=32, proj_kernels=0), GU_LM),
+        (dict(linear_fmt=1, batch=32, proj_kernels=1), 0),
+        (dict(linear_fmt=1, batch=32, proj_kernels=2), ALL),
+        (dict(linear_fmt=1, batch=16, proj_kernels=0), GU_LM),
+        (dict(linear_fmt=1, batch=15, proj_kernels=0), 0),
+        (dict(linear_fmt=1, batch=8, proj_kernels=2), ALL),
+        (dict(linear_fmt=1, batch=2, tokens_per_seq=8, proj_kernels=0), GU_LM),  # a 16-row verify step
+        (dict(linear_fmt=1, batch=33, proj_kernels=2), 0),
+        (dict(linear_fmt=1, batch=1, proj_kernels=2), 0),
+        (dict(linear_fmt=0, batch=8, proj_kernels=0), 0),
+        (dict(linear_fmt=0, batch=8, proj_kernels=2), ALL),
+        (dict(linear_fmt=0, batch=1, tokens_per_seq=512, proj_kernels=2), 0),  # a prefill chunk
+        (dict(linear_fmt=1, batch=32, proj_kernels=2, hidden=1024, n_q_heads=16, intermediate=3072), 0),
+    ]
+    for kw, want in cases:
+        cfg = _cfg(dec, **{**big, **kw})
+        assert dec.dec_debug_proj_plan(cfg) == want, kw
+    mask = ctypes.c_int(-1)
+    assert dec.lib.dec_debug_proj_plan(None, ctypes.byref(mask)) == dec.DEC_ERR_INVALID_ARG
+    bad = _cfg(dec, **{**big, "proj_kernels": 3})
+    assert dec.lib.dec_debug_proj_plan(ctypes.byref(bad), ctypes.byref(mask)) == dec.DEC_ERR_INVALID_ARG
+    assert mask.value == -1
+

@@ -301,6 +301,30 @@ dec_status check_linear(const dec_linear& l, int fmt, const char* name, int laye
 // K splits of a batch-1 GEMV: split only while the CTAs would cover fewer than half the
 // SMs.  Every split costs a round trip through the partial sums (fence, ticket, reload:
 // about 2 us measured on the 1024-row projections, more than the idle SMs give back).
+// Which projections of a step with `rows` rows run on the tcgen05 decode kernels.  2..32 rows (a
+// batch of sequences, or the rows of a verify step) at hidden >= 2048: tcgen05 on the batched
+// path's hi/lo activation planes, 4-bit codes expanded into tensor memory (k_gemm_q4tc) or bf16
+// weights streamed by TMA (k_gemm_btc).  DEC_PROJ_TCGEN05 puts every projection there.
+// DEC_PROJ_AUTO takes what measured faster side by side on one GPU: with 4-bit weights from 16
+// rows on (measured at 32), the gate/up and lm_head projections on tcgen05 and the others on
+// mma.sync (8B, 32 rows: gate/up 69 against 84 us, lm_head 0.30 against 0.40 ms; q/k/v, o and
+// down 37-53 against 35-49 us), with bf16 weights every projection on mma.sync (8 rows: 3.79
+// against 5.20 ms a step).  One row stays on the batch-1 GEMV.
+struct ProjPlan {
+  bool q4tc_all = false;  // every projection on k_gemm_q4tc
+  bool q4tc_gu = false;   // the gate/up and lm_head projections on k_gemm_q4tc
+  bool btc = false;       // every projection on k_gemm_btc
+};
+ProjPlan plan_projections(const dec_config& c, int rows) {
+  ProjPlan pl;
+  const bool tc_rows = rows >= 2 && rows <= q4tc_max_tokens() && c.hidden >= 2048;
+  const bool q4 = c.linear_fmt == DEC_W_AFFINE4_G64;
+  pl.q4tc_all = tc_rows && q4 && c.proj_kernels == DEC_PROJ_TCGEN05;
+  pl.q4tc_gu = pl.q4tc_all || (tc_rows && q4 && c.proj_kernels == DEC_PROJ_AUTO && rows >= 16);
+  pl.btc = tc_rows && c.linear_fmt == DEC_W_BF16 && c.proj_kernels == DEC_PROJ_TCGEN05;
+  return pl;
+}
+
 int choose_splits(int N, int K, int fmt, int num_sms) {
   const int cols = fmt == DEC_W_BF16 ? 8 : 16;  // inputs per thread chunk (k_gemv1.cu)
   const int tiles = (N + kGemvRows - 1) / kGemvRows;
@@ -762,20 +786,11 @@ extern "C" dec_handle* dec_create(const dec_config* cfg, const dec_weights* wts)
 
   // ---- packed weight memory
   const int nqkv = (nq + 2 * nkv) * d;
-  // 2..32 rows (a batch of sequences, or the rows of a verify step) at hidden >= 2048:
-  // tcgen05 on the batched path's hi/lo activation planes, 4-bit codes expanded into tensor
-  // memory or bf16 weights streamed by TMA.  DEC_PROJ_TCGEN05 puts every projection there.
-  // DEC_PROJ_AUTO takes what measured faster side by side on one GPU: with 4-bit weights from 16
-  // rows on (measured at 32), the gate/up and lm_head projections on tcgen05 and the others on
-  // mma.sync (8B, 32 rows: gate/up 69 against 84 us, lm_head 0.30 against 0.40 ms; q/k/v, o and down 37-53
-  // against 35-49 us), with bf16 weights every projection on mma.sync (8 rows: 3.79 against
-  // 5.20 ms a step).  One row stays on the batch-1 GEMV.
-  const bool tc_rows = h->rows >= 2 && h->rows <= q4tc_max_tokens() && H >= 2048;
-  const bool q4 = fmt == DEC_W_AFFINE4_G64;
-  const bool q4tc_all = tc_rows && q4 && c.proj_kernels == DEC_PROJ_TCGEN05;
-  const bool q4tc_gu = q4tc_all || (tc_rows && q4 && c.proj_kernels == DEC_PROJ_AUTO && h->rows >= 16);
+  // the projections' kernel families (plan_projections)
+  const ProjPlan pplan = plan_projections(c, h->rows);
+  const bool q4tc_all = pplan.q4tc_all, q4tc_gu = pplan.q4tc_gu;
   h->q4tc = q4tc_gu;  // some projection runs on k_gemm_q4tc
-  h->btc = tc_rows && fmt == DEC_W_BF16 && c.proj_kernels == DEC_PROJ_TCGEN05;
+  h->btc = pplan.btc;
   const bool tc = h->rows > 1 || h->q4tc || h->btc;
   // more rows than one CTA takes: token blocks of gemm_tc_block_tokens() rows each
   const int blk_tok = gemm_tc_block_tokens(h->wfmt);
@@ -1405,6 +1420,21 @@ extern "C" dec_status dec_debug_gemm_btc(const void* x_hl, int M, const void* w,
   p.partials = partials;
   p.counters = counters;
   DEC_CUDA(launch_gemm_btc(LaunchCtx{reinterpret_cast<cudaStream_t>(stream), false}, mx, mw, p, kInPlain, kEpiStore));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_debug_proj_plan(const dec_config* cfg, int* tcgen05_mask) {
+  g_err[0] = 0;
+  if (!cfg || !tcgen05_mask) {
+    set_err("dec_debug_proj_plan: NULL argument");
+    return DEC_ERR_INVALID_ARG;
+  }
+  const dec_status st = validate(cfg);
+  if (st != DEC_OK) return st;
+  const int tps = cfg->tokens_per_seq > 1 ? cfg->tokens_per_seq : 1;
+  const ProjPlan pl = plan_projections(*cfg, cfg->batch * tps);
+  const bool rest = pl.q4tc_all || pl.btc, gu = pl.q4tc_gu || pl.btc;
+  *tcgen05_mask = (rest ? 1 | 2 | 8 : 0) | (gu ? 4 | 16 : 0);
   return DEC_OK;
 }
 

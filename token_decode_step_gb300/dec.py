@@ -110,6 +110,7 @@ def _load() -> ctypes.CDLL:
         "dec_debug_gemm_btc": (ctypes.c_int, [vp, ctypes.c_int, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp,
                                               vp, vp]),
         "dec_debug_btc_max_segments": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+        "dec_debug_proj_plan": (ctypes.c_int, [ctypes.POINTER(DecConfig), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -243,6 +244,13 @@ def dec_debug_gemm_btc(x_hl: int, M: int, w: int, N: int, K: int, ctas: int, out
                        counters: int, stream: int = 0) -> int:
     return _check(lib.dec_debug_gemm_btc(x_hl, M, w, N, K, ctas, out, partials, counters, stream),
                   "dec_debug_gemm_btc")
+
+
+def dec_debug_proj_plan(cfg: DecConfig) -> int:
+    """Bit mask of the projections (0 q/k/v, 1 o, 2 gate/up, 3 down, 4 lm_head) on tcgen05 kernels."""
+    mask = ctypes.c_int(-1)
+    _check(lib.dec_debug_proj_plan(ctypes.byref(cfg), ctypes.byref(mask)), "dec_debug_proj_plan")
+    return mask.value
 
 
 def dec_kv_quantize(src: int, rows: int, head_dim: int, codes: int, params: int, stream: int = 0) -> int:
